@@ -1,0 +1,176 @@
+"""CPU oracle for paged decode attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's
+``cpu_baseline`` / ``--impl reference`` leg may import this package.  The CUDA
+library never links, loads or calls it, and it imports nothing from the CUDA
+package.  ``pkv_oracle.c`` holds the arithmetic (fp64 over the exact bf16
+input values); this module compiles it with gcc and marshals numpy arrays.
+
+Functions (each follows the passage cited in ``pkv_oracle.c``):
+
+* :func:`paged_attn`   -- softmax(q K^T * scale + causal_mask) V per query row,
+  K/V gathered through the block table, GQA group map h -> h // (n_q/n_kv).
+* :func:`attn_partial` -- (o, m, l) of one key range: the online-softmax state.
+* :func:`lse_merge`    -- exact combination of partials.
+* :func:`kv_append`    -- bit copy of new K/V rows into their slots.
+* :func:`kv_bytes`     -- M_kv = 2 L n_kv d_h (s b) p.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "pkv_oracle.c")
+BUILD_DIR = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(BUILD_DIR, "libpkv_oracle.so")
+
+_lock = threading.Lock()
+_default = None
+
+
+def compile_oracle(src: str = SOURCE, out: str = LIB_PATH, openmp: bool = True) -> str:
+    """Compile the C oracle into a shared library with gcc (IEEE fp64, no fast-math)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-o", out, src, "-lm"]
+    if openmp:
+        try:
+            subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                           capture_output=True, text=True)
+            return out
+        except subprocess.CalledProcessError:
+            pass  # no OpenMP runtime on this host: build the serial oracle
+    subprocess.run(base, check=True, capture_output=True, text=True)
+    return out
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, lib_path: str):
+        self.lib_path = lib_path
+        lib = ctypes.CDLL(lib_path)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        c_int = ctypes.c_int
+        lib.oracle_paged_attn.argtypes = [u16p, u16p, u16p, i32p, i32p] + [c_int] * 8 + \
+            [ctypes.c_double, f64p]
+        lib.oracle_paged_attn.restype = c_int
+        lib.oracle_attn_partial.argtypes = [u16p, u16p, u16p, i32p, i32p] + [c_int] * 8 + \
+            [ctypes.c_double, c_int, c_int, f64p, f64p, f64p]
+        lib.oracle_attn_partial.restype = c_int
+        lib.oracle_lse_merge.argtypes = [c_int, ctypes.c_long, c_int, f64p, f64p, f64p, f64p]
+        lib.oracle_lse_merge.restype = None
+        lib.oracle_kv_append.argtypes = [u16p, u16p, i32p] + [c_int] * 5 + [u16p, u16p]
+        lib.oracle_kv_append.restype = c_int
+        lib.oracle_kv_bytes.argtypes = [c_int, c_int, c_int, c_int, ctypes.c_int64]
+        lib.oracle_kv_bytes.restype = ctypes.c_int64
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = c_int
+        self._lib = lib
+
+    # -- attention ---------------------------------------------------------
+    def paged_attn(self, q, k_cache, v_cache, block_tables, context_lens, *, n_q, n_kv,
+                   head_dim, block_size, scale, num_blocks=None, q_len=None):
+        """fp64 output [num_seqs, q_len, n_q, head_dim]; raises on invalid tables."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        k_cache = np.ascontiguousarray(k_cache, dtype=np.uint16)
+        v_cache = np.ascontiguousarray(v_cache, dtype=np.uint16)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        num_seqs = cl.shape[0]
+        if q_len is None:
+            q_len = q.shape[1]
+        if num_blocks is None:
+            num_blocks = k_cache.shape[0]
+        max_blocks = bt.shape[1] if bt.ndim == 2 else 0
+        out = np.zeros((num_seqs, q_len, n_q, head_dim), dtype=np.float64)
+        st = self._lib.oracle_paged_attn(
+            _ptr(q, ctypes.c_uint16), _ptr(k_cache, ctypes.c_uint16),
+            _ptr(v_cache, ctypes.c_uint16), _ptr(bt, ctypes.c_int32), _ptr(cl, ctypes.c_int32),
+            num_seqs, q_len, n_q, n_kv, head_dim, block_size, max_blocks, num_blocks,
+            float(scale), _ptr(out, ctypes.c_double))
+        if st != 0:
+            raise ValueError(f"oracle_paged_attn rejected its inputs (status {st})")
+        return out
+
+    def attn_partial(self, q, k_cache, v_cache, block_tables, context_lens, *, n_q, n_kv,
+                     head_dim, block_size, scale, t_begin, t_end, num_blocks=None):
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        k_cache = np.ascontiguousarray(k_cache, dtype=np.uint16)
+        v_cache = np.ascontiguousarray(v_cache, dtype=np.uint16)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        num_seqs, q_len = cl.shape[0], q.shape[1]
+        if num_blocks is None:
+            num_blocks = k_cache.shape[0]
+        o = np.zeros((num_seqs, q_len, n_q, head_dim), dtype=np.float64)
+        m = np.zeros((num_seqs, q_len, n_q), dtype=np.float64)
+        l = np.zeros((num_seqs, q_len, n_q), dtype=np.float64)
+        st = self._lib.oracle_attn_partial(
+            _ptr(q, ctypes.c_uint16), _ptr(k_cache, ctypes.c_uint16),
+            _ptr(v_cache, ctypes.c_uint16), _ptr(bt, ctypes.c_int32), _ptr(cl, ctypes.c_int32),
+            num_seqs, q_len, n_q, n_kv, head_dim, block_size, bt.shape[1], num_blocks,
+            float(scale), int(t_begin), int(t_end), _ptr(o, ctypes.c_double),
+            _ptr(m, ctypes.c_double), _ptr(l, ctypes.c_double))
+        if st != 0:
+            raise ValueError(f"oracle_attn_partial rejected its inputs (status {st})")
+        return o, m, l
+
+    def lse_merge(self, o, m, l):
+        """o [nsplit, rows..., d], m/l [nsplit, rows...] -> out [rows..., d]."""
+        o = np.ascontiguousarray(o, dtype=np.float64)
+        m = np.ascontiguousarray(m, dtype=np.float64)
+        l = np.ascontiguousarray(l, dtype=np.float64)
+        nsplit, d = o.shape[0], o.shape[-1]
+        rows = int(np.prod(o.shape[1:-1]))
+        out = np.zeros(o.shape[1:], dtype=np.float64)
+        self._lib.oracle_lse_merge(nsplit, rows, d, _ptr(o, ctypes.c_double),
+                                   _ptr(m, ctypes.c_double), _ptr(l, ctypes.c_double),
+                                   _ptr(out, ctypes.c_double))
+        return out
+
+    # -- cache write ------------------------------------------------------
+    def kv_append(self, k_new, v_new, slot_mapping, k_cache, v_cache, *, block_size):
+        """In-place scatter into k_cache / v_cache (numpy uint16 arrays)."""
+        k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+        v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int32)
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        assert k_cache.dtype == np.uint16 and v_cache.dtype == np.uint16
+        num_blocks, n_kv, bs, d = k_cache.shape
+        assert bs == block_size
+        st = self._lib.oracle_kv_append(
+            _ptr(k_new, ctypes.c_uint16), _ptr(v_new, ctypes.c_uint16), _ptr(sm, ctypes.c_int32),
+            sm.shape[0], n_kv, d, block_size, num_blocks,
+            _ptr(k_cache, ctypes.c_uint16), _ptr(v_cache, ctypes.c_uint16))
+        if st != 0:
+            raise ValueError(f"oracle_kv_append rejected its inputs (status {st})")
+
+    # -- sizes --------------------------------------------------------------
+    def kv_bytes(self, layers, n_kv, head_dim, elem_bytes, tokens):
+        return int(self._lib.oracle_kv_bytes(layers, n_kv, head_dim, elem_bytes, tokens))
+
+    def num_threads(self):
+        return int(self._lib.oracle_num_threads())
+
+
+def get() -> Oracle:
+    """The oracle built from this directory's source (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            if (not os.path.exists(LIB_PATH)
+                    or os.path.getmtime(LIB_PATH) < os.path.getmtime(SOURCE)):
+                compile_oracle()
+            _default = Oracle(LIB_PATH)
+        return _default

@@ -1,0 +1,324 @@
+/*
+ * pkv_oracle.c -- CPU oracle for paged decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the paged decode-attention path computes.  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg may load it.  It
+ * shares no code, header, table or constant with the CUDA library and the
+ * product path never calls it.
+ *
+ * Arithmetic is IEEE fp64 over the exact values of the bf16 inputs.  Nothing
+ * is blocked, fused or reordered beyond the definition:
+ *
+ *   Attention(Q, K, V) = softmax((Q K^T / sqrt(d_k)) + causal_mask) V
+ *     -- "Transformer inference mechanics", What Q, K, and V do in causal
+ *        attention (per-head decoder attention and the causal mask);
+ *        "Transformer and attention intuition", Q, K, V -- and why they force
+ *        a cache.
+ *
+ * The KV cache holds K[1..t], V[1..t] per layer and gains the new token's K/V
+ * each step ("Transformer inference mechanics", What the KV cache stores per
+ * layer).  It is stored in fixed-size blocks reached through a per-request
+ * block table that maps logical positions to physical blocks ("Inference
+ * Engines", The Breakthrough, PagedAttention paragraph; CS336 lecture-10
+ * notes, PagedAttention (vLLM)).  Query heads share K/V heads in contiguous
+ * groups (GQA; MQA is one group, MHA one head per group) ("Transformer
+ * inference mechanics", MHA versus MQA versus GQA).
+ *
+ * Readings where the pages leave a detail open (each is also listed with the
+ * design notes):
+ *   - cache layout [num_blocks][n_kv][block_size][head_dim];
+ *   - query head h reads KV head h / (n_q / n_kv);
+ *   - context_lens[b] counts every resident token including the q_len new
+ *     ones, and new token i sits at position ctx - q_len + i, seeing keys at
+ *     positions <= its own (the causal mask);
+ *   - a row that sees no key (ctx == 0, or ctx < q_len) outputs zeros;
+ *   - the softmax is evaluated as max, then sum of exp(s - max): subtracting
+ *     the row maximum leaves softmax unchanged and keeps exp finite.
+ *
+ * Parallelism: one OpenMP loop over independent (sequence, KV head) units.
+ * Each unit is computed by one thread, start to finish, in sequential order,
+ * so the result does not depend on the thread count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Exact widening: a bf16 is the top 16 bits of an fp32. */
+static double bf16_value(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Copy sequence b's logical keys and values for KV head g into dense
+ * K[ctx][d], V[ctx][d] by walking its block table: logical token t lives in
+ * physical block block_tables[b][t / block_size] at offset t % block_size.
+ * Returns 0, or -1 if a block index the walk needs is outside [0, num_blocks).
+ */
+static int gather_sequence(const uint16_t *k_cache, const uint16_t *v_cache,
+                           const int32_t *table_row, int ctx, int g, int n_kv,
+                           int head_dim, int block_size, int num_blocks,
+                           double *K, double *V)
+{
+    for (int t = 0; t < ctx; ++t) {
+        int blk = table_row[t / block_size];
+        int off = t % block_size;
+        if (blk < 0 || blk >= num_blocks)
+            return -1;
+        size_t base = (((size_t)blk * n_kv + g) * block_size + off) * head_dim;
+        for (int e = 0; e < head_dim; ++e) {
+            K[(size_t)t * head_dim + e] = bf16_value(k_cache[base + e]);
+            V[(size_t)t * head_dim + e] = bf16_value(v_cache[base + e]);
+        }
+    }
+    return 0;
+}
+
+/*
+ * out[b][i][h][:] for all b, query tokens i, query heads h (fp64).
+ * q: [num_seqs][q_len][n_q][head_dim] bf16 bits.  Returns 0 on success,
+ * 1 on bad shape arguments, 2 if a block table or context length is invalid.
+ */
+int oracle_paged_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens,
+                      int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
+                      int block_size, int max_blocks_per_seq, int num_blocks,
+                      double scale, double *out)
+{
+    if (num_seqs < 0 || q_len < 1 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 ||
+        head_dim < 1 || block_size < 1 || max_blocks_per_seq < 0 || num_blocks < 0)
+        return 1;
+    const int G = n_q / n_kv;
+    int status = 0;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long unit = 0; unit < (long)num_seqs * n_kv; ++unit) {
+        const int b = (int)(unit / n_kv);
+        const int g = (int)(unit % n_kv);
+        const int ctx = context_lens[b];
+        if (ctx < 0 || (long)ctx > (long)max_blocks_per_seq * block_size) {
+#pragma omp atomic write
+            status = 2;
+            continue;
+        }
+        double *K = (double *)malloc(sizeof(double) * ((size_t)ctx * head_dim + 1));
+        double *V = (double *)malloc(sizeof(double) * ((size_t)ctx * head_dim + 1));
+        double *s = (double *)malloc(sizeof(double) * ((size_t)ctx + 1));
+        double *acc = (double *)malloc(sizeof(double) * (size_t)head_dim);
+        if (gather_sequence(k_cache, v_cache, block_tables + (size_t)b * max_blocks_per_seq,
+                            ctx, g, n_kv, head_dim, block_size, num_blocks, K, V) != 0) {
+#pragma omp atomic write
+            status = 2;
+        } else {
+            for (int i = 0; i < q_len; ++i) {
+                /* New token i sits at position ctx - q_len + i and sees keys 0..pos. */
+                const long pos = (long)ctx - q_len + i;
+                const int nvis = pos < 0 ? 0 : (int)(pos + 1 < ctx ? pos + 1 : ctx);
+                for (int h = g * G; h < (g + 1) * G; ++h) {
+                    const uint16_t *qrow = q + (((size_t)b * q_len + i) * n_q + h) * head_dim;
+                    double *orow = out + (((size_t)b * q_len + i) * n_q + h) * head_dim;
+                    for (int e = 0; e < head_dim; ++e)
+                        acc[e] = 0.0;
+                    if (nvis == 0) {
+                        for (int e = 0; e < head_dim; ++e)
+                            orow[e] = 0.0;
+                        continue;
+                    }
+                    /* scores s_t = scale * q . K_t */
+                    double mx = -INFINITY;
+                    for (int t = 0; t < nvis; ++t) {
+                        double dot = 0.0;
+                        for (int e = 0; e < head_dim; ++e)
+                            dot += bf16_value(qrow[e]) * K[(size_t)t * head_dim + e];
+                        s[t] = scale * dot;
+                        if (s[t] > mx)
+                            mx = s[t];
+                    }
+                    /* softmax weights and the weighted sum of values */
+                    double denom = 0.0;
+                    for (int t = 0; t < nvis; ++t) {
+                        double w = exp(s[t] - mx);
+                        denom += w;
+                        for (int e = 0; e < head_dim; ++e)
+                            acc[e] += w * V[(size_t)t * head_dim + e];
+                    }
+                    for (int e = 0; e < head_dim; ++e)
+                        orow[e] = acc[e] / denom;
+                }
+            }
+        }
+        free(K);
+        free(V);
+        free(s);
+        free(acc);
+    }
+    return status;
+}
+
+/*
+ * Attention of one query row restricted to the logical key range
+ * [t_begin, t_end) (further cut by the causal limit), returned as the three
+ * quantities that FlashAttention's online softmax keeps per row: the running
+ * maximum m, the running sum l = sum_t exp(s_t - m) and the unnormalised
+ * output o = sum_t exp(s_t - m) V_t.  An empty range gives m = -inf, l = 0,
+ * o = 0.  ("Efficient inference", FlashAttention: exact attention without
+ * the matrix -- partial results from different key blocks are rescaled and
+ * combined exactly; CS336 lecture-10 notes, PagedAttention (vLLM), where
+ * FlashDecoding splits the context.)
+ * Output rows are laid out like the full output: [num_seqs][q_len][n_q].
+ */
+int oracle_attn_partial(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *block_tables, const int32_t *context_lens,
+                        int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
+                        int block_size, int max_blocks_per_seq, int num_blocks,
+                        double scale, int t_begin, int t_end,
+                        double *o, double *m, double *l)
+{
+    if (num_seqs < 0 || q_len < 1 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 ||
+        head_dim < 1 || block_size < 1 || t_begin < 0 || t_end < t_begin)
+        return 1;
+    const int G = n_q / n_kv;
+    for (int b = 0; b < num_seqs; ++b) {
+        const int ctx = context_lens[b];
+        if (ctx < 0 || (long)ctx > (long)max_blocks_per_seq * block_size)
+            return 2;
+        for (int i = 0; i < q_len; ++i) {
+            const long pos = (long)ctx - q_len + i;
+            long hi = pos + 1 < ctx ? pos + 1 : ctx;
+            if (hi > t_end)
+                hi = t_end;
+            for (int h = 0; h < n_q; ++h) {
+                const int g = h / G;
+                const size_t row = ((size_t)b * q_len + i) * n_q + h;
+                const uint16_t *qrow = q + row * head_dim;
+                double *orow = o + row * head_dim;
+                for (int e = 0; e < head_dim; ++e)
+                    orow[e] = 0.0;
+                double mx = -INFINITY;
+                for (long t = t_begin; t < hi; ++t) {
+                    int blk = block_tables[(size_t)b * max_blocks_per_seq + t / block_size];
+                    if (blk < 0 || blk >= num_blocks)
+                        return 2;
+                    size_t base = (((size_t)blk * n_kv + g) * block_size + t % block_size) * head_dim;
+                    double dot = 0.0;
+                    for (int e = 0; e < head_dim; ++e)
+                        dot += bf16_value(qrow[e]) * bf16_value(k_cache[base + e]);
+                    if (scale * dot > mx)
+                        mx = scale * dot;
+                }
+                double sum = 0.0;
+                for (long t = t_begin; t < hi; ++t) {
+                    int blk = block_tables[(size_t)b * max_blocks_per_seq + t / block_size];
+                    size_t base = (((size_t)blk * n_kv + g) * block_size + t % block_size) * head_dim;
+                    double dot = 0.0;
+                    for (int e = 0; e < head_dim; ++e)
+                        dot += bf16_value(qrow[e]) * bf16_value(k_cache[base + e]);
+                    double w = exp(scale * dot - mx);
+                    sum += w;
+                    for (int e = 0; e < head_dim; ++e)
+                        orow[e] += w * bf16_value(v_cache[base + e]);
+                }
+                m[row] = mx;
+                l[row] = sum;
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Combine nsplit partial results of the same rows into the final output:
+ * M = max_s m_s, w_s = exp(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s.
+ * A partial with l_s == 0 (empty range, m_s = -inf) gets weight 0; a row whose
+ * partials are all empty outputs zeros.  Layouts: o [nsplit][rows][head_dim],
+ * m and l [nsplit][rows], out [rows][head_dim].
+ * ("Efficient inference", FlashAttention: running maximum and running sum,
+ * partial results rescaled and combined exactly.)
+ */
+void oracle_lse_merge(int nsplit, long rows, int head_dim, const double *o,
+                      const double *m, const double *l, double *out)
+{
+    for (long r = 0; r < rows; ++r) {
+        double M = -INFINITY;
+        for (int s = 0; s < nsplit; ++s)
+            if (l[(size_t)s * rows + r] > 0.0 && m[(size_t)s * rows + r] > M)
+                M = m[(size_t)s * rows + r];
+        double denom = 0.0;
+        for (int e = 0; e < head_dim; ++e)
+            out[(size_t)r * head_dim + e] = 0.0;
+        if (M == -INFINITY)
+            continue;
+        for (int s = 0; s < nsplit; ++s) {
+            double ls = l[(size_t)s * rows + r];
+            if (ls <= 0.0)
+                continue;
+            double w = exp(m[(size_t)s * rows + r] - M);
+            denom += w * ls;
+            for (int e = 0; e < head_dim; ++e)
+                out[(size_t)r * head_dim + e] += w * o[((size_t)s * rows + r) * head_dim + e];
+        }
+        for (int e = 0; e < head_dim; ++e)
+            out[(size_t)r * head_dim + e] /= denom;
+    }
+}
+
+/*
+ * Write each new token's K and V rows into its cache slot: slot s names
+ * physical block s / block_size, offset s % block_size.  Slots < 0 and slots
+ * >= num_blocks * block_size are skipped; every other cache byte is left as
+ * it was.  The copy is of the bf16 bits.  ("Transformer inference
+ * mechanics", What the KV cache stores per layer: "+ new K/V for t+1";
+ * "Transformer and attention intuition": the cache is appended to on every
+ * decode step.)
+ * k_new, v_new: [num_tokens][n_kv][head_dim]; caches: [num_blocks][n_kv][block_size][head_dim].
+ */
+int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, const int32_t *slot_mapping,
+                     int num_tokens, int n_kv, int head_dim, int block_size, int num_blocks,
+                     uint16_t *k_cache, uint16_t *v_cache)
+{
+    if (num_tokens < 0 || n_kv < 1 || head_dim < 1 || block_size < 1 || num_blocks < 0)
+        return 1;
+    for (int i = 0; i < num_tokens; ++i) {
+        long slot = slot_mapping[i];
+        if (slot < 0 || slot >= (long)num_blocks * block_size)
+            continue;
+        long blk = slot / block_size;
+        long off = slot % block_size;
+        for (int g = 0; g < n_kv; ++g) {
+            size_t dst = (((size_t)blk * n_kv + g) * block_size + off) * head_dim;
+            size_t src = ((size_t)i * n_kv + g) * head_dim;
+            memcpy(k_cache + dst, k_new + src, sizeof(uint16_t) * head_dim);
+            memcpy(v_cache + dst, v_new + src, sizeof(uint16_t) * head_dim);
+        }
+    }
+    return 0;
+}
+
+/*
+ * KV-cache bytes M_kv = 2 * L * n_kv * d_h * (s * b) * p, with s * b given as
+ * the number of resident tokens ("Inference Engines", The Mathematics;
+ * "Efficient inference", Key ideas).  Returns -1 on a negative argument.
+ */
+int64_t oracle_kv_bytes(int layers, int n_kv, int head_dim, int elem_bytes, int64_t tokens)
+{
+    if (layers < 0 || n_kv < 0 || head_dim < 0 || elem_bytes < 0 || tokens < 0)
+        return -1;
+    return (int64_t)2 * layers * n_kv * head_dim * elem_bytes * tokens;
+}

@@ -1,0 +1,363 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each ``pin_*`` function takes an oracle handle (``oracle.Oracle``) and raises
+``AssertionError`` when the oracle disagrees with what the pages or the
+mathematics fix.  ``test_oracle_pins.py`` runs them against the real oracle;
+``test_oracle_mutants.py`` runs them against copies of the oracle with one
+planted mistake each and requires every mutant to fail at least one pin.
+
+What pins what:
+
+* ``pin_library_sdpa``      -- torch's own scaled-dot-product attention (fp64,
+  CPU) on the logical, contiguous K/V the paged cache was built from: the
+  textbook definition softmax(QK^T/sqrt(d) + causal_mask)V ("Transformer
+  inference mechanics", What Q, K, and V do in causal attention), with GQA
+  expressed by the library's own head repeat.
+* ``pin_equal_scores_mean`` -- q = 0 makes all scores equal, so the output is
+  the plain mean of the visible V rows.
+* ``pin_single_token``      -- one resident token: the output is that token's V.
+* ``pin_hardmax``           -- a huge scale turns softmax into argmax: the output
+  is V at the largest score.
+* ``pin_block_permutation`` -- paging changes only where K/V live ("Transformer
+  inference mechanics", FlashAttention versus PagedAttention): any relabelling
+  of physical blocks gives the identical output.
+* ``pin_gqa_equals_repeated_mha`` -- GQA over n_kv heads equals MHA over
+  K/V heads repeated group-wise ("Transformer inference mechanics", MHA versus
+  MQA versus GQA).
+* ``pin_causal_rows``       -- draft token i of gamma equals a one-token query
+  over the prefix ending at its own position.
+* ``pin_merge_exact``       -- partials of any split of the key range merge to
+  the unsplit result ("Efficient inference", FlashAttention: partial results
+  are rescaled and combined exactly).
+* ``pin_kv_append``         -- slots written, everything else byte-identical.
+* ``pin_kv_bytes_golden`` / ``pin_gqa_ratio`` -- the sizes printed on the pages.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+from paged_kv_cache_256_gb300.workloads import (
+    BF16_POISON, bf16_bits_to_f32, f32_to_bf16_bits, make_custom)
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "kv_bytes.txt")
+
+
+# ---------------------------------------------------------------------------
+# helpers (test-side only)
+# ---------------------------------------------------------------------------
+def _rand_bf16(rng, shape, scale=1.0):
+    return f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * np.float32(scale))
+
+
+def _paged_from_logical(rng, K, V, block_size, extra_blocks=3):
+    """Scatter logical K/V [num_seqs][n_kv][ctx_b][d] (lists) into a shuffled paged cache.
+
+    Built by the test itself, independently of the oracle's gather.
+    Returns (k_cache, v_cache, block_tables) with poison in every unused slot.
+    """
+    num_seqs = len(K)
+    n_kv, d = K[0].shape[0], K[0].shape[2]
+    nblk = [max(0, math.ceil(k.shape[1] / block_size)) for k in K]
+    used = sum(nblk)
+    pool = used + extra_blocks
+    perm = rng.permutation(pool)
+    max_blocks = max(1, max(nblk))
+    bt = np.full((num_seqs, max_blocks), perm[-1], dtype=np.int32)
+    kc = np.full((pool, n_kv, block_size, d), BF16_POISON, dtype=np.uint16)
+    vc = np.full_like(kc, BF16_POISON)
+    o = 0
+    for b in range(num_seqs):
+        for j in range(nblk[b]):
+            phys = perm[o]
+            o += 1
+            bt[b, j] = phys
+            lo, hi = j * block_size, min((j + 1) * block_size, K[b].shape[1])
+            kc[phys, :, : hi - lo, :] = K[b][:, lo:hi, :]
+            vc[phys, :, : hi - lo, :] = V[b][:, lo:hi, :]
+    return kc, vc, bt
+
+
+def _case(rng, ctxs, n_q, n_kv, d, bs, q_len, kscale=1.0):
+    K = [_rand_bf16(rng, (n_kv, c, d), kscale) for c in ctxs]
+    V = [_rand_bf16(rng, (n_kv, c, d)) for c in ctxs]
+    kc, vc, bt = _paged_from_logical(rng, K, V, bs)
+    q = _rand_bf16(rng, (len(ctxs), q_len, n_q, d))
+    return dict(q=q, K=K, V=V, k_cache=kc, v_cache=vc, block_tables=bt,
+                context_lens=np.asarray(ctxs, dtype=np.int32), n_q=n_q, n_kv=n_kv,
+                head_dim=d, block_size=bs, q_len=q_len)
+
+
+def _run(orc, c, scale, **over):
+    args = dict(c)
+    args.update(over)
+    return orc.paged_attn(args["q"], args["k_cache"], args["v_cache"], args["block_tables"],
+                          args["context_lens"], n_q=args["n_q"], n_kv=args["n_kv"],
+                          head_dim=args["head_dim"], block_size=args["block_size"],
+                          scale=scale)
+
+
+SHAPES = [
+    # ctxs, n_q, n_kv, d, bs, q_len
+    ([5, 17, 33], 4, 4, 16, 4, 1),       # MHA, ragged, partial last blocks
+    ([1, 9, 40], 8, 2, 8, 4, 1),         # GQA G=4
+    ([7, 23], 6, 1, 16, 8, 1),           # MQA
+    ([6, 19, 12], 4, 2, 8, 4, 3),        # GQA + causal draft tokens
+    ([4, 30], 8, 1, 16, 16, 4),          # MQA verify, gamma = 4
+]
+
+
+# ---------------------------------------------------------------------------
+# pins
+# ---------------------------------------------------------------------------
+def pin_library_sdpa(orc):
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(11)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        scale = float(np.float32(1.0 / math.sqrt(d)))
+        got = _run(orc, c, scale)
+        G = n_q // n_kv
+        for b, ctx in enumerate(ctxs):
+            q = torch.from_numpy(bf16_bits_to_f32(c["q"][b]).astype(np.float64))  # [q_len, n_q, d]
+            k = torch.from_numpy(bf16_bits_to_f32(c["K"][b]).astype(np.float64))  # [n_kv, ctx, d]
+            v = torch.from_numpy(bf16_bits_to_f32(c["V"][b]).astype(np.float64))
+            k = k.repeat_interleave(G, dim=0)
+            v = v.repeat_interleave(G, dim=0)
+            qh = q.permute(1, 0, 2)  # [n_q, q_len, d]
+            pos = ctx - q_len + torch.arange(q_len)
+            mask = torch.arange(ctx)[None, :] <= pos[:, None]
+            ref = F.scaled_dot_product_attention(qh[None], k[None], v[None],
+                                                 attn_mask=mask[None, None], scale=scale)[0]
+            ref = ref.permute(1, 0, 2).numpy()
+            np.testing.assert_allclose(got[b], ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_numpy_dense(orc):
+    """Dense matrix form: S = Q K^T * scale with -inf above the causal diagonal."""
+    rng = np.random.default_rng(12)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        scale = 0.37
+        got = _run(orc, c, scale)
+        G = n_q // n_kv
+        for b, ctx in enumerate(ctxs):
+            for h in range(n_q):
+                Q = bf16_bits_to_f32(c["q"][b, :, h, :]).astype(np.float64)
+                K = bf16_bits_to_f32(c["K"][b][h // G]).astype(np.float64)
+                V = bf16_bits_to_f32(c["V"][b][h // G]).astype(np.float64)
+                S = Q @ K.T * scale
+                rows = (ctx - q_len + np.arange(q_len))[:, None]
+                S = np.where(np.arange(ctx)[None, :] <= rows, S, -np.inf)
+                P = np.exp(S - S.max(axis=1, keepdims=True))
+                ref = (P / P.sum(axis=1, keepdims=True)) @ V
+                np.testing.assert_allclose(got[b, :, h, :], ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_equal_scores_mean(orc):
+    rng = np.random.default_rng(13)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        c["q"] = np.zeros_like(c["q"])
+        got = _run(orc, c, 0.125)
+        G = n_q // n_kv
+        for b, ctx in enumerate(ctxs):
+            for i in range(q_len):
+                nvis = ctx - q_len + i + 1
+                for h in range(n_q):
+                    V = bf16_bits_to_f32(c["V"][b][h // G][:nvis]).astype(np.float64)
+                    np.testing.assert_allclose(got[b, i, h], V.mean(axis=0), rtol=1e-13,
+                                               atol=1e-15)
+
+
+def pin_single_token(orc):
+    rng = np.random.default_rng(14)
+    c = _case(rng, [1, 1, 1], 6, 3, 16, 4, 1)
+    got = _run(orc, c, 0.25)
+    for b in range(3):
+        for h in range(6):
+            ref = bf16_bits_to_f32(c["V"][b][h // 2][0]).astype(np.float64)
+            assert np.array_equal(got[b, 0, h], ref), (b, h)
+
+
+def pin_hardmax(orc):
+    rng = np.random.default_rng(15)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        got = _run(orc, c, 1.0e6)
+        G = n_q // n_kv
+        for b, ctx in enumerate(ctxs):
+            for i in range(q_len):
+                nvis = ctx - q_len + i + 1
+                for h in range(n_q):
+                    q = bf16_bits_to_f32(c["q"][b, i, h]).astype(np.float64)
+                    K = bf16_bits_to_f32(c["K"][b][h // G][:nvis]).astype(np.float64)
+                    V = bf16_bits_to_f32(c["V"][b][h // G][:nvis]).astype(np.float64)
+                    s = K @ q
+                    top = np.sort(s)[::-1]
+                    if len(top) > 1 and (top[0] - top[1]) * 1.0e6 < 800:
+                        continue  # a near tie: not a clean argmax case
+                    assert np.array_equal(got[b, i, h], V[int(np.argmax(s))]), (b, i, h)
+
+
+def pin_block_permutation(orc):
+    rng = np.random.default_rng(16)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        base = _run(orc, c, 0.3)
+        pool = c["k_cache"].shape[0]
+        relabel = rng.permutation(pool)  # old physical index -> new physical index
+        kc = np.empty_like(c["k_cache"])
+        vc = np.empty_like(c["v_cache"])
+        kc[relabel] = c["k_cache"]
+        vc[relabel] = c["v_cache"]
+        bt = relabel[c["block_tables"]].astype(np.int32)
+        got = _run(orc, c, 0.3, k_cache=kc, v_cache=vc, block_tables=bt)
+        assert np.array_equal(base, got)
+
+
+def pin_gqa_equals_repeated_mha(orc):
+    rng = np.random.default_rng(17)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        if n_q == n_kv:
+            continue
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        G = n_q // n_kv
+        gqa = _run(orc, c, 0.2)
+        kc = np.repeat(c["k_cache"], G, axis=1)  # KV head g -> query heads g*G .. g*G+G-1
+        vc = np.repeat(c["v_cache"], G, axis=1)
+        mha = _run(orc, c, 0.2, k_cache=kc, v_cache=vc, n_kv=n_q)
+        assert np.array_equal(gqa, mha)
+
+
+def pin_causal_rows(orc):
+    rng = np.random.default_rng(18)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        if q_len == 1:
+            continue
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        full = _run(orc, c, 0.25)
+        for i in range(q_len):
+            ctx_i = np.asarray(ctxs, dtype=np.int32) - q_len + i + 1
+            one = _run(orc, c, 0.25, q=np.ascontiguousarray(c["q"][:, i:i + 1]),
+                       context_lens=ctx_i, q_len=1)
+            assert np.array_equal(full[:, i:i + 1], one), i
+
+
+def pin_empty_context(orc):
+    rng = np.random.default_rng(19)
+    c = _case(rng, [0, 5, 0], 4, 2, 8, 4, 1)
+    got = _run(orc, c, 0.5)
+    assert np.all(got[0] == 0.0) and np.all(got[2] == 0.0)
+    assert np.all(np.isfinite(got[1])) and np.any(got[1] != 0.0)
+
+
+def pin_merge_exact(orc):
+    rng = np.random.default_rng(20)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len, kscale=3.0)
+        full = _run(orc, c, 0.4)
+        hi = max(ctxs)
+        for nsplit in (1, 2, 3, 5):
+            cuts = np.sort(rng.integers(0, hi + 1, size=nsplit - 1))
+            edges = [0] + [int(x) for x in cuts] + [hi]
+            parts = [orc.attn_partial(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                      c["context_lens"], n_q=n_q, n_kv=n_kv, head_dim=d,
+                                      block_size=bs, scale=0.4, t_begin=a, t_end=b)
+                     for a, b in zip(edges[:-1], edges[1:])]
+            o = np.stack([p[0] for p in parts])
+            m = np.stack([p[1] for p in parts])
+            l = np.stack([p[2] for p in parts])
+            merged = orc.lse_merge(o, m, l)
+            np.testing.assert_allclose(merged, full, rtol=1e-12, atol=1e-13)
+        # the whole range as one part: o / l is the output, m the largest score
+        o, m, l = orc.attn_partial(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                   c["context_lens"], n_q=n_q, n_kv=n_kv, head_dim=d,
+                                   block_size=bs, scale=0.4, t_begin=0, t_end=hi)
+        np.testing.assert_allclose(o / l[..., None], full, rtol=1e-12, atol=1e-13)
+        G = n_q // n_kv
+        for b, ctx in enumerate(ctxs):
+            for i in range(q_len):
+                nvis = ctx - q_len + i + 1
+                for h in range(n_q):
+                    q = bf16_bits_to_f32(c["q"][b, i, h]).astype(np.float64)
+                    K = bf16_bits_to_f32(c["K"][b][h // G][:nvis]).astype(np.float64)
+                    assert math.isclose(m[b, i, h], 0.4 * float((K @ q).max()),
+                                        rel_tol=1e-12, abs_tol=1e-12)
+
+
+def pin_kv_append(orc):
+    rng = np.random.default_rng(21)
+    for n_kv, d, bs, pool in [(2, 8, 4, 6), (1, 16, 16, 3), (4, 64, 16, 5)]:
+        kc = rng.integers(0, 1 << 16, size=(pool, n_kv, bs, d), dtype=np.uint16)
+        vc = rng.integers(0, 1 << 16, size=(pool, n_kv, bs, d), dtype=np.uint16)
+        nslots = pool * bs
+        slots = rng.permutation(nslots)[:7].astype(np.int32)
+        slots = np.concatenate([slots, np.asarray([-1, nslots, nslots + 5, -100], np.int32)])
+        rng.shuffle(slots)
+        T = slots.shape[0]
+        kn = rng.integers(0, 1 << 16, size=(T, n_kv, d), dtype=np.uint16)
+        vn = rng.integers(0, 1 << 16, size=(T, n_kv, d), dtype=np.uint16)
+        k_ref, v_ref = kc.copy(), vc.copy()
+        for i, s in enumerate(slots):
+            if 0 <= s < nslots:
+                k_ref[s // bs, :, s % bs, :] = kn[i]
+                v_ref[s // bs, :, s % bs, :] = vn[i]
+        k_got, v_got = kc.copy(), vc.copy()
+        orc.kv_append(kn, vn, slots, k_got, v_got, block_size=bs)
+        assert np.array_equal(k_got, k_ref) and np.array_equal(v_got, v_ref)
+
+
+def pin_append_then_attend(orc):
+    """The tiny workload: attend at ctx - 1, append one token, attend at ctx."""
+    wl = make_custom(num_seqs=2, q_len=1, n_q=4, n_kv=2, head_dim=64, block_size=16,
+                     context_lens=[18, 41], seed=99)
+    kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+    kw = dict(n_q=4, n_kv=2, head_dim=64, block_size=16, scale=wl.scale)
+    before = orc.paged_attn(wl.q, kc, vc, wl.block_tables, wl.context_lens - 1, **kw)
+    assert np.all(np.isfinite(before))  # the not-yet-written slot is never read
+    orc.kv_append(wl.k_new, wl.v_new, wl.slot_mapping, kc, vc, block_size=16)
+    after = orc.paged_attn(wl.q, kc, vc, wl.block_tables, wl.context_lens, **kw)
+    assert np.all(np.isfinite(after))
+    # With a huge scale the appended token wins whenever its score is the top one.
+    for b in range(2):
+        pos = int(wl.context_lens[b]) - 1
+        blk = wl.block_tables[b, pos // 16]
+        assert np.array_equal(kc[blk, :, pos % 16], wl.k_new[b])
+
+
+def _golden_rows():
+    rows = []
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            p = line.split()
+            rows.append((p[0], *[int(x) for x in p[1:7]]))
+    return rows
+
+
+def pin_kv_bytes_golden(orc):
+    rows = _golden_rows()
+    assert len(rows) >= 6
+    for name, L, n_kv, d, p, tokens, expected in rows:
+        assert orc.kv_bytes(L, n_kv, d, p, tokens) == expected, name
+
+
+def pin_gqa_ratio(orc):
+    # ("Inference Engines", The Mathematics: M_MHA / M_GQA = n_h / n_kv; MQA is n_kv = 1)
+    for n_h, n_kv in [(32, 8), (64, 8), (32, 1), (40, 8)]:
+        mha = orc.kv_bytes(32, n_h, 128, 2, 4096)
+        gqa = orc.kv_bytes(32, n_kv, 128, 2, 4096)
+        assert mha * n_kv == gqa * n_h
+
+
+ALL_PINS = [
+    pin_library_sdpa, pin_numpy_dense, pin_equal_scores_mean, pin_single_token, pin_hardmax,
+    pin_block_permutation, pin_gqa_equals_repeated_mha, pin_causal_rows, pin_empty_context,
+    pin_merge_exact, pin_kv_append, pin_append_then_attend, pin_kv_bytes_golden, pin_gqa_ratio,
+]

@@ -1,0 +1,70 @@
+"""Plant one plausible mistake at a time in a copy of the oracle; some pin must catch it.
+
+The mistakes are made on the CPU, in a temporary copy of the C source; the
+committed oracle is never touched.  Each mutant must fail at least one pin,
+which shows the pins are strong enough to notice a dropped term, a wrong sign,
+a wrong index or a swapped operand.
+"""
+import os
+import shutil
+import tempfile
+
+import pytest
+
+import oracle as oracle_pkg
+from tests import oracle_pins
+
+MUTANTS = {
+    "offset_uses_division": ("int off = t % block_size;", "int off = t / block_size;"),
+    "cache_layout_transposed": (
+        "size_t base = (((size_t)blk * n_kv + g) * block_size + off) * head_dim;",
+        "size_t base = (((size_t)blk * block_size + off) * n_kv + g) * head_dim;"),
+    "no_causal_limit": ("const long pos = (long)ctx - q_len + i;\n                const int nvis",
+                        "const long pos = (long)ctx - 1;\n                const int nvis"),
+    "scale_dropped": ("s[t] = scale * dot;", "s[t] = dot;"),
+    "exp_sign_flipped": ("double w = exp(s[t] - mx);", "double w = exp(mx - s[t]);"),
+    "not_normalised": ("orow[e] = acc[e] / denom;", "orow[e] = acc[e];"),
+    "strided_group_map": ("for (int h = g * G; h < (g + 1) * G; ++h) {",
+                          "for (int h = g; h < n_q; h += n_kv) {"),
+    "scores_use_V": ("dot += bf16_value(qrow[e]) * K[(size_t)t * head_dim + e];",
+                     "dot += bf16_value(qrow[e]) * V[(size_t)t * head_dim + e];"),
+    "values_use_K": ("acc[e] += w * V[(size_t)t * head_dim + e];",
+                     "acc[e] += w * K[(size_t)t * head_dim + e];"),
+    "bf16_widening_wrong": ("uint32_t u = ((uint32_t)bits) << 16;",
+                            "uint32_t u = ((uint32_t)bits) << 15;"),
+    "own_token_excluded": ("(int)(pos + 1 < ctx ? pos + 1 : ctx);", "(int)(pos < ctx ? pos : ctx);"),
+    "append_skips_slot0": ("if (slot < 0 || slot >= (long)num_blocks * block_size)",
+                           "if (slot <= 0 || slot >= (long)num_blocks * block_size)"),
+    "append_k_into_v": ("memcpy(v_cache + dst, v_new + src", "memcpy(v_cache + dst, k_new + src"),
+    "kv_bytes_no_factor2": ("return (int64_t)2 * layers", "return (int64_t)1 * layers"),
+    "merge_no_rescale": ("double w = exp(m[(size_t)s * rows + r] - M);", "double w = 1.0;"),
+    "merge_denominator_unweighted": ("denom += w * ls;", "denom += ls;"),
+    "partial_max_not_reported": ("m[row] = mx;", "m[row] = 0.0;"),
+}
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    d = tempfile.mkdtemp(prefix="pkv_mutants_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(workdir, name):
+    old, new = MUTANTS[name]
+    src = open(oracle_pkg.SOURCE).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new, 1)
+    path = os.path.join(workdir, f"{name}.c")
+    with open(path, "w") as f:
+        f.write(mutated)
+    lib = oracle_pkg.compile_oracle(path, os.path.join(workdir, f"lib_{name}.so"), openmp=False)
+    orc = oracle_pkg.Oracle(lib)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the planted mistake {name}"
