@@ -1,0 +1,170 @@
+/*
+ * pkv.h -- C ABI of the paged decode-attention library (libpkv.so, GB300 / sm_103a).
+ *
+ * The library computes one decode step of attention over a KV cache that is
+ * stored in fixed-size blocks and reached through per-sequence block tables
+ * (PagedAttention: "Inference Engines", The Breakthrough, PagedAttention
+ * paragraph; CS336 lecture-10 notes, PagedAttention (vLLM)), and writes each
+ * step's new keys and values into that cache.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named *_cache, q, out, k_new, v_new, block_tables,
+ *     context_lens, slot_mapping and workspace are DEVICE pointers owned by
+ *     the caller.  The library allocates no device memory and keeps no
+ *     per-call state; it only caches per-device attributes and driver entry
+ *     points.
+ *   - bf16 tensors are passed as raw 16-bit patterns (`const void *`).
+ *   - `stream` is a cudaStream_t passed as `void *` (NULL = legacy default
+ *     stream) and must belong to the current CUDA device.  Calls are
+ *     asynchronous on that stream: a PKV_OK return means "validated and
+ *     launched"; faults inside a kernel surface at the next synchronisation.
+ *   - Argument checks run on the host before anything is launched; a failed
+ *     check returns a status and launches nothing.
+ *   - Device pointers to bf16 / fp32 tensors must be 16-byte aligned, int32
+ *     arrays 4-byte aligned.
+ *   - Every index is int32; products that address memory are computed in 64 bits.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,     /* null pointer, negative size, n_q % n_kv != 0, misalignment */
+    PKV_ERR_UNSUPPORTED = 2,     /* valid but outside the built kernels (head_dim, block_size, rows) */
+    PKV_ERR_WORKSPACE = 3,       /* workspace missing or smaller than the size query asked for */
+    PKV_ERR_CUDA = 4,            /* a CUDA runtime / driver call or a launch failed */
+    PKV_ERR_BAD_BLOCK_TABLE = 5, /* CHECKED mode found a block index or context length out of range */
+    PKV_ERR_TIMEOUT = 6          /* a bounded in-kernel wait gave up (the kernel returned early) */
+} pkv_status;
+
+/* out_dtype values. */
+#define PKV_OUT_BF16 0 /* round-to-nearest-even bf16 */
+#define PKV_OUT_F32 1  /* fp32 (debug / tight-parity path; probabilities kept to ~16 bits) */
+
+/* flags bits. */
+#define PKV_FLAG_CHECKED 0x1u /* bounds-check block indices and context lengths on the device */
+/* Bits 16..31 force the number of attention CTAs (0 = one per SM).  Tests
+ * use it to move where long contexts are split; results stay within the
+ * stated tolerance for every value. */
+#define PKV_FLAG_GRID_SHIFT 16
+#define PKV_FLAG_GRID(n) (((unsigned)(n) & 0xFFFFu) << PKV_FLAG_GRID_SHIFT)
+
+/*
+ * pkv_paged_decode_attn -- one decode step of paged attention.
+ *
+ * Computes, for every sequence b, new query token i < q_len and query head h,
+ *     out[b][i][h] = softmax_t( scale * q[b][i][h] . K_b[t] ) . V_b[t],
+ *     over logical positions t <= context_lens[b] - q_len + i,
+ * the causal decoder attention of "Transformer inference mechanics", What Q,
+ * K, and V do in causal attention, with K_b, V_b read through the block
+ * table.  Query head h reads KV head h / (n_q / n_kv): MHA when n_kv == n_q,
+ * GQA for groups, MQA when n_kv == 1 ("Transformer inference mechanics", MHA
+ * versus MQA versus GQA).  Each KV block is read once for all query heads of
+ * its group and all q_len tokens.  Long contexts are split across CTAs and
+ * combined with a log-sum-exp merge (FlashDecoding, named in CS336 lecture-10
+ * notes, PagedAttention (vLLM); exact combination of partial softmax
+ * results, "Efficient inference", FlashAttention section).
+ *
+ * Layouts (all row-major, contiguous):
+ *   q            [num_seqs][q_len][n_q][head_dim]           bf16
+ *   k_cache      [num_blocks][n_kv][block_size][head_dim]    bf16 (v_cache alike)
+ *   block_tables [num_seqs][max_blocks_per_seq]              int32 physical block ids
+ *   context_lens [num_seqs]                                  int32 resident tokens,
+ *                including the q_len new ones (their K/V must already be appended)
+ *   out          [num_seqs][q_len][n_q][head_dim]            bf16 or fp32 (out_dtype)
+ *   Token t of sequence b lives in block block_tables[b][t / block_size] at
+ *   offset t % block_size.  Only entries t / block_size < ceil(ctx/block_size)
+ *   are read; slots past the context in the last block are never used, and
+ *   may hold any bits (NaN included).
+ *
+ * Supported: head_dim in {64, 128}; block_size in {16, 32};
+ *   rows = (n_q / n_kv) * q_len <= 128; num_blocks * n_kv * block_size < 2^31.
+ * Rows that see no key (context_lens[b] == 0, or < q_len) are written as zeros.
+ *
+ * workspace: device memory of at least pkv_paged_decode_attn_workspace_size(...)
+ *   bytes, zero-filled once before its first use; the library leaves it
+ *   reusable (its error word is cleared by pkv_check_error).  One workspace
+ *   must not be shared by calls that may run concurrently.
+ * flags: PKV_FLAG_CHECKED makes the kernel validate every block index it
+ *   reads (0 <= id < num_blocks) and every context length
+ *   (0 <= ctx <= max_blocks_per_seq * block_size, ctx == 0 or ctx >= q_len);
+ *   violations are clamped, recorded in the workspace and reported by
+ *   pkv_check_error as PKV_ERR_BAD_BLOCK_TABLE.  Without it, context lengths
+ *   are still clamped to the table width and an out-of-range block id reads
+ *   zeros (the tensor-memory-access unit fills out-of-bounds tiles), so no
+ *   call reads outside the caches.
+ * Returns PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE
+ *   or PKV_ERR_CUDA.  num_seqs == 0 returns PKV_OK and launches nothing.
+ */
+int pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens,
+                          int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
+                          int block_size, int max_blocks_per_seq, int num_blocks,
+                          float scale, void *out, int out_dtype,
+                          void *workspace, size_t workspace_bytes, unsigned flags,
+                          void *stream);
+
+/*
+ * Bytes of workspace pkv_paged_decode_attn needs for these sizes on the
+ * current device (the split-K partials of at most two pieces per CTA plus
+ * an error word).  max_context_len is accepted for interface stability and
+ * does not change the result.  Returns 0 for arguments the call would reject.
+ */
+size_t pkv_paged_decode_attn_workspace_size(int num_seqs, int q_len, int n_q, int n_kv,
+                                            int head_dim, int block_size,
+                                            int max_context_len, unsigned flags);
+
+/*
+ * pkv_kv_append -- write this step's new keys and values into the paged cache.
+ *
+ * For every token i < num_tokens with 0 <= slot_mapping[i] < num_blocks * block_size:
+ *   k_cache[slot / block_size][g][slot % block_size][:] = k_new[i][g][:]   for all g < n_kv
+ *   (v_cache likewise).  The copy is bit-exact; every other cache byte is unchanged.
+ * Slots outside that range (e.g. -1 for padding tokens) are skipped.
+ * ("Transformer inference mechanics", What the KV cache stores per layer:
+ * the cache gains the new token's K/V each step.)
+ * Layouts: k_new, v_new [num_tokens][n_kv][head_dim] bf16; slot_mapping
+ *   [num_tokens] int32; caches as for pkv_paged_decode_attn.  head_dim must be
+ *   a multiple of 8.  Two tokens naming the same slot leave either one's row.
+ * flags: reserved, pass 0.
+ * Returns PKV_OK, PKV_ERR_INVALID_ARG or PKV_ERR_CUDA; num_tokens == 0 launches nothing.
+ */
+int pkv_kv_append(const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                  int num_tokens, int n_kv, int head_dim, int block_size, int num_blocks,
+                  void *k_cache, void *v_cache, unsigned flags, void *stream);
+
+/*
+ * Synchronise `stream`, read and clear the error word of `workspace`.
+ * Returns PKV_OK, PKV_ERR_BAD_BLOCK_TABLE (CHECKED mode saw a bad block id or
+ * context length), PKV_ERR_TIMEOUT (a bounded wait inside the kernel expired;
+ * that call's output is not valid), PKV_ERR_INVALID_ARG (null workspace) or
+ * PKV_ERR_CUDA.  Not usable inside CUDA-graph capture (it synchronises).
+ */
+int pkv_check_error(const void *workspace, void *stream);
+
+/*
+ * KV-cache bytes M_kv = 2 * layers * n_kv * head_dim * tokens * elem_bytes
+ * ("Inference Engines", The Mathematics; "Efficient inference", Key ideas),
+ * where tokens = sequence length x batch.  Returns -1 for a negative argument.
+ */
+int64_t pkv_kv_bytes(int layers, int n_kv, int head_dim, int elem_bytes, int64_t tokens);
+
+/* Static, human-readable name of a pkv_status value. */
+const char *pkv_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

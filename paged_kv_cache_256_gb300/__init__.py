@@ -1,0 +1,21 @@
+"""Paged decode attention for one GB300 GPU (sm_103a).
+
+The product is ``libpkv.so``, a C-ABI library of hand-written CUDA kernels
+(declared in ``include/pkv.h``):
+
+* ``pkv_kv_append``          -- write each step's new K/V into the paged cache;
+* ``pkv_paged_decode_attn``  -- one decode step of attention over the paged
+  cache, GQA/MQA groups sharing each KV tile, ragged contexts, long contexts
+  split across CTAs and combined by a log-sum-exp merge.
+
+This package holds the CUDA sources (``csrc/``), the in-tree build
+(``build.py``), the ctypes binding under the C names (``_lib.py``) and the
+seeded synthetic inputs (``workloads.py``).  PyTorch is used only for device
+memory and streams.
+"""
+from ._lib import (  # noqa: F401
+    PKV_ERR_BAD_BLOCK_TABLE, PKV_ERR_CUDA, PKV_ERR_INVALID_ARG, PKV_ERR_TIMEOUT,
+    PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_FLAG_CHECKED, PKV_FLAG_GRID, PKV_OK, PKV_OUT_BF16,
+    PKV_OUT_F32, PkvError, alloc_workspace, load_library, pkv_check_error, pkv_kv_append,
+    pkv_kv_bytes, pkv_paged_decode_attn, pkv_paged_decode_attn_workspace_size,
+    pkv_status_string, pkv_version)

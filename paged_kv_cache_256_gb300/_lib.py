@@ -1,0 +1,192 @@
+"""ctypes binding of libpkv.so: the C ABI of include/pkv.h, under the same names.
+
+Argument marshalling only: every function checks tensor dtypes, shapes and
+devices, passes raw pointers and sizes to the C entry point, and raises
+:class:`PkvError` for a non-zero status.  No computation happens here and
+there is no CPU fallback: if the shared library cannot be built or loaded,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import build as _build
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = 1
+PKV_ERR_UNSUPPORTED = 2
+PKV_ERR_WORKSPACE = 3
+PKV_ERR_CUDA = 4
+PKV_ERR_BAD_BLOCK_TABLE = 5
+PKV_ERR_TIMEOUT = 6
+
+PKV_OUT_BF16 = 0
+PKV_OUT_F32 = 1
+PKV_FLAG_CHECKED = 0x1
+PKV_FLAG_GRID_SHIFT = 16
+
+
+def PKV_FLAG_GRID(n: int) -> int:
+    return (int(n) & 0xFFFF) << PKV_FLAG_GRID_SHIFT
+
+
+# Every symbol include/pkv.h declares, with its ctypes signature.
+_c_int, _c_float, _c_size = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_vp, _i32p = ctypes.c_void_p, ctypes.c_void_p
+SIGNATURES = {
+    "pkv_paged_decode_attn": ([_vp, _vp, _vp, _i32p, _i32p] + [_c_int] * 8 +
+                              [_c_float, _vp, _c_int, _vp, _c_size, ctypes.c_uint, _vp], _c_int),
+    "pkv_paged_decode_attn_workspace_size": ([_c_int] * 7 + [ctypes.c_uint], _c_size),
+    "pkv_kv_append": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp, _vp, ctypes.c_uint, _vp], _c_int),
+    "pkv_check_error": ([_vp, _vp], _c_int),
+    "pkv_kv_bytes": ([_c_int] * 4 + [ctypes.c_int64], ctypes.c_int64),
+    "pkv_status_string": ([_c_int], ctypes.c_char_p),
+    "pkv_version": ([], _c_int),
+}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {status_name(status)} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load (building first if needed) the CUDA library; raises if that fails."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            lib_path = path or _build.build()
+            lib = ctypes.CDLL(lib_path)
+            for name, (argtypes, restype) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = argtypes
+                fn.restype = restype
+            if path is not None:
+                return lib
+            _lib = lib
+        return _lib
+
+
+def status_name(status: int) -> str:
+    return load_library().pkv_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != PKV_OK:
+        raise PkvError(status, where)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _bf16_like(t, name):
+    import torch
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must hold bf16 (torch.bfloat16 or a 16-bit view), got {t.dtype}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def _i32(t, name):
+    import torch
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+
+
+# ---------------------------------------------------------------------------
+def pkv_kv_bytes(layers: int, n_kv: int, head_dim: int, elem_bytes: int, tokens: int) -> int:
+    return int(load_library().pkv_kv_bytes(layers, n_kv, head_dim, elem_bytes, tokens))
+
+
+def pkv_status_string(status: int) -> str:
+    return status_name(status)
+
+
+def pkv_version() -> int:
+    return int(load_library().pkv_version())
+
+
+def pkv_paged_decode_attn_workspace_size(num_seqs, q_len, n_q, n_kv, head_dim, block_size,
+                                         max_context_len=0, flags=0) -> int:
+    return int(load_library().pkv_paged_decode_attn_workspace_size(
+        num_seqs, q_len, n_q, n_kv, head_dim, block_size, max_context_len, flags))
+
+
+def alloc_workspace(num_seqs, q_len, n_q, n_kv, head_dim, block_size, flags=0, device=None):
+    """A zero-filled uint8 CUDA tensor of the size the library asks for."""
+    import torch
+    n = pkv_paged_decode_attn_workspace_size(num_seqs, q_len, n_q, n_kv, head_dim, block_size,
+                                             0, flags)
+    if n == 0:
+        raise PkvError(PKV_ERR_INVALID_ARG, "pkv_paged_decode_attn_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                          flags=0, stream=None):
+    """out <- paged decode attention (see include/pkv.h for the full contract).
+
+    q [num_seqs, q_len, n_q, d] bf16; k_cache/v_cache [num_blocks, n_kv, bs, d]
+    bf16; block_tables [num_seqs, max_blocks] int32; context_lens [num_seqs]
+    int32; out like q, bf16 or float32; workspace a uint8 CUDA tensor.
+    """
+    import torch
+    _bf16_like(q, "q")
+    _bf16_like(k_cache, "k_cache")
+    _bf16_like(v_cache, "v_cache")
+    _i32(block_tables, "block_tables")
+    _i32(context_lens, "context_lens")
+    if q.dim() != 4 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("q must be 4-D and k_cache / v_cache 4-D of equal shape")
+    num_seqs, q_len, n_q, d = q.shape
+    num_blocks, n_kv, bs, d2 = k_cache.shape
+    if d2 != d or block_tables.dim() != 2 or block_tables.shape[0] != num_seqs or \
+            context_lens.shape != (num_seqs,) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("inconsistent shapes")
+    if out.dtype == torch.float32:
+        out_dtype = PKV_OUT_F32
+    elif out.dtype in (torch.bfloat16, torch.int16, torch.uint16):
+        out_dtype = PKV_OUT_BF16
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    if not out.is_cuda or not out.is_contiguous() or not workspace.is_cuda:
+        raise ValueError("out and workspace must be contiguous CUDA tensors")
+    st = load_library().pkv_paged_decode_attn(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), num_seqs, q_len, n_q, n_kv, d, bs, block_tables.shape[1],
+        num_blocks, float(scale), out.data_ptr(), out_dtype, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), int(flags), _stream_ptr(stream))
+    _check(st, "pkv_paged_decode_attn")
+
+
+def pkv_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, flags=0, stream=None):
+    """Scatter k_new/v_new [T, n_kv, d] into their cache slots (bit copy)."""
+    _bf16_like(k_new, "k_new")
+    _bf16_like(v_new, "v_new")
+    _bf16_like(k_cache, "k_cache")
+    _bf16_like(v_cache, "v_cache")
+    _i32(slot_mapping, "slot_mapping")
+    T, n_kv, d = k_new.shape
+    num_blocks, n_kv2, bs, d2 = k_cache.shape
+    if v_new.shape != k_new.shape or n_kv2 != n_kv or d2 != d or slot_mapping.shape != (T,) \
+            or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent shapes")
+    st = load_library().pkv_kv_append(
+        k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), T, n_kv, d, bs, num_blocks,
+        k_cache.data_ptr(), v_cache.data_ptr(), int(flags), _stream_ptr(stream))
+    _check(st, "pkv_kv_append")
+
+
+def pkv_check_error(workspace, stream=None) -> int:
+    """Synchronise and return (and clear) the workspace's device status as a pkv_status."""
+    return int(load_library().pkv_check_error(workspace.data_ptr(), _stream_ptr(stream)))

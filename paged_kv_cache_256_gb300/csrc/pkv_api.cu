@@ -1,0 +1,246 @@
+// pkv_api.cu -- the C ABI declared in include/pkv.h.
+//
+// Host side only: argument checks (no launch on failure), the tensor maps
+// that let the TMA unit fetch (block, KV head) tiles of the caches, the
+// workspace layout, and the launches.  The kernels live in decode_attn.cu,
+// lse_merge.cu and kv_append.cu.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/pkv.h"
+#include "pkv_internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int sm_count(int dev) {
+    static int cache[kMaxDevices] = {0};
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D view of a cache: rows = num_blocks * n_kv * block_size, columns = head_dim
+// bf16; one box = 64 columns x block_size rows with the 128-byte swizzle.
+bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, long long rows,
+                    int block_size) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)block_size};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int warp_rows_for(int rows) {
+    const int tiles = (rows + 15) / 16;
+    return tiles <= 1 ? 1 : tiles <= 2 ? 2 : tiles <= 4 ? 4 : 8;
+}
+
+// Number of attention CTAs: forced by the flags, else one per SM.
+int attn_grid(unsigned flags, int dev) {
+    const int forced = (int)((flags >> PKV_FLAG_GRID_SHIFT) & 0xFFFFu);
+    if (forced > 0) return forced;
+    return sm_count(dev);
+}
+
+int check_shape(int num_seqs, int q_len, int n_q, int n_kv, int head_dim, int block_size) {
+    if (num_seqs < 0 || q_len < 1 || n_q < 1 || n_kv < 1 || head_dim < 1 || block_size < 1)
+        return PKV_ERR_INVALID_ARG;
+    if (n_q % n_kv != 0) return PKV_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if ((long long)(n_q / n_kv) * q_len > 128) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+}  // namespace
+
+WorkspaceLayout workspace_layout(int grid, int rows, int head_dim) {
+    WorkspaceLayout L;
+    L.err_off = 0;
+    L.info_off = 256;
+    L.ml_off = round_up(L.info_off + (size_t)grid * 2 * sizeof(int4), 256);
+    L.o_off = round_up(L.ml_off + (size_t)grid * 2 * rows * 2 * sizeof(float), 256);
+    L.total = round_up(L.o_off + (size_t)grid * 2 * rows * head_dim * sizeof(float), 256);
+    return L;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_version(void) { return 10000; }
+
+const char* pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        case PKV_ERR_BAD_BLOCK_TABLE: return "PKV_ERR_BAD_BLOCK_TABLE";
+        case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
+        default: return "PKV_ERR_UNKNOWN";
+    }
+}
+
+int64_t pkv_kv_bytes(int layers, int n_kv, int head_dim, int elem_bytes, int64_t tokens) {
+    if (layers < 0 || n_kv < 0 || head_dim < 0 || elem_bytes < 0 || tokens < 0) return -1;
+    return (int64_t)2 * layers * n_kv * head_dim * elem_bytes * tokens;
+}
+
+size_t pkv_paged_decode_attn_workspace_size(int num_seqs, int q_len, int n_q, int n_kv,
+                                            int head_dim, int block_size, int max_context_len,
+                                            unsigned flags) {
+    (void)max_context_len;
+    if (check_shape(num_seqs, q_len, n_q, n_kv, head_dim, block_size) != PKV_OK) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int grid = attn_grid(flags, dev);
+    if (grid <= 0) return 0;
+    return workspace_layout(grid, (n_q / n_kv) * q_len, head_dim).total;
+}
+
+int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens,
+                          int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
+                          int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                          void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                          unsigned flags, void* stream) {
+    int st = check_shape(num_seqs, q_len, n_q, n_kv, head_dim, block_size);
+    if (st != PKV_OK) return st;
+    if (out_dtype != PKV_OUT_BF16 && out_dtype != PKV_OUT_F32) return PKV_ERR_INVALID_ARG;
+    if (max_blocks_per_seq < 1 || num_blocks < 1) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+    const long long rows_total = (long long)num_blocks * n_kv * block_size;
+    if (rows_total >= (1LL << 31) - 64) return PKV_ERR_UNSUPPORTED;
+    if ((long long)max_blocks_per_seq * block_size >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const int grid = attn_grid(flags, dev);
+    if (grid <= 0) return PKV_ERR_CUDA;
+    const int rows = (n_q / n_kv) * q_len;
+    const WorkspaceLayout L = workspace_layout(grid, rows, head_dim);
+    if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
+        return PKV_ERR_WORKSPACE;
+
+    CUtensorMap tk, tv;
+    if (!make_cache_map(&tk, k_cache, head_dim, rows_total, block_size) ||
+        !make_cache_map(&tv, v_cache, head_dim, rows_total, block_size))
+        return PKV_ERR_CUDA;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    AttnArgs a;
+    a.q = static_cast<const uint16_t*>(q);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.out = out;
+    a.err = reinterpret_cast<unsigned*>(ws + L.err_off);
+    a.rec_info = reinterpret_cast<int4*>(ws + L.info_off);
+    a.rec_ml = reinterpret_cast<float*>(ws + L.ml_off);
+    a.rec_o = reinterpret_cast<float*>(ws + L.o_off);
+    a.num_seqs = num_seqs;
+    a.q_len = q_len;
+    a.n_q = n_q;
+    a.n_kv = n_kv;
+    a.group = n_q / n_kv;
+    a.rows = rows;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.tile_rows_total = (int)rows_total;
+    a.warp_rows = warp_rows_for(rows);
+    a.checked = (flags & PKV_FLAG_CHECKED) ? 1 : 0;
+    a.scale_log2 = scale * 1.4426950408889634f;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool f32 = out_dtype == PKV_OUT_F32;
+    if (launch_decode_attn(a, tk, tv, head_dim, block_size, f32, grid, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (grid > 1 && launch_lse_merge(a, head_dim, f32, grid, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+int pkv_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                  int num_tokens, int n_kv, int head_dim, int block_size, int num_blocks,
+                  void* k_cache, void* v_cache, unsigned flags, void* stream) {
+    (void)flags;
+    if (num_tokens < 0 || n_kv < 1 || head_dim < 8 || head_dim % 8 != 0 || block_size < 1 ||
+        num_blocks < 1)
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 4))
+        return PKV_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return PKV_ERR_CUDA;
+    if (launch_kv_append(k_new, v_new, slot_mapping, num_tokens, n_kv, head_dim, block_size,
+                         num_blocks, k_cache, v_cache, sms,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+int pkv_check_error(const void* workspace, void* stream) {
+    if (!workspace) return PKV_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (word == 0) return PKV_OK;
+    if (cudaMemset(const_cast<void*>(workspace), 0, sizeof word) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (word & kErrTimeout) return PKV_ERR_TIMEOUT;
+    if (word & (kErrBadBlock | kErrBadContext)) return PKV_ERR_BAD_BLOCK_TABLE;
+    return PKV_ERR_CUDA;
+}
+
+}  // extern "C"

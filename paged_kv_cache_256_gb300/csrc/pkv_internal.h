@@ -1,0 +1,63 @@
+// pkv_internal.h -- declarations shared by the C-ABI front end and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+// Record flags of a split piece (see decode_attn.cu).
+constexpr int kRecValid = 1;  // the slot holds a piece of a split unit
+constexpr int kRecFirst = 2;  // the piece starts at the unit's first block
+constexpr int kRecLast = 4;   // the piece ends at the unit's last block
+constexpr int kRecEmpty = 8;  // the CTA owned no blocks at all
+
+constexpr unsigned kErrInternal = 8u;  // inconsistent split records (after a timeout)
+
+struct AttnArgs {
+    const uint16_t* q;            // [num_seqs][q_len][n_q][head_dim] bf16
+    const int32_t* block_tables;  // [num_seqs][max_blocks_per_seq]
+    const int32_t* context_lens;  // [num_seqs]
+    void* out;                    // [num_seqs][q_len][n_q][head_dim] bf16 or f32
+    unsigned* err;                // workspace error word
+    int4* rec_info;               // [grid][2] {seq, kv head, flags, 0}
+    float* rec_ml;                // [grid][2][rows][2] {m (log2 domain), l}
+    float* rec_o;                 // [grid][2][rows][head_dim] unnormalised output
+    int num_seqs;
+    int q_len;
+    int n_q;
+    int n_kv;
+    int group;  // n_q / n_kv
+    int rows;   // group * q_len: query rows sharing one KV head
+    int max_blocks_per_seq;
+    int num_blocks;
+    int tile_rows_total;  // num_blocks * n_kv * block_size (rows of the 2-D cache view)
+    int warp_rows;        // 16-row tiles per KV unit (1, 2, 4 or 8)
+    int checked;
+    float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
+};
+
+struct WorkspaceLayout {
+    size_t err_off, info_off, ml_off, o_off, total;
+};
+
+WorkspaceLayout workspace_layout(int grid, int rows, int head_dim);
+
+// Dynamic shared memory the attention kernel needs for (head_dim, block_size).
+int decode_attn_smem_bytes(int head_dim, int block_size);
+
+cudaError_t launch_decode_attn(const AttnArgs& a, const CUtensorMap& tmap_k,
+                               const CUtensorMap& tmap_v, int head_dim, int block_size,
+                               bool out_f32, int grid, cudaStream_t stream);
+
+cudaError_t launch_lse_merge(const AttnArgs& a, int head_dim, bool out_f32, int grid,
+                             cudaStream_t stream);
+
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                             int num_tokens, int n_kv, int head_dim, int block_size,
+                             int num_blocks, void* k_cache, void* v_cache, int num_sms,
+                             cudaStream_t stream);
+
+}  // namespace pkv
