@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--workload", default="llama3_8b_gqa")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-soak", action="store_true",
+                    help="skip the 1 s untimed load before the timed steps (profiling runs)")
     return ap.parse_args()
 
 
@@ -281,7 +283,7 @@ def run_ours(args):
     clocks.start()
     # Let the sampler see the GPU under load before and through the timed steps.
     t_soak = time.perf_counter()
-    while time.perf_counter() - t_soak < 1.0:
+    while not args.no_soak and time.perf_counter() - t_soak < 1.0:
         for _ in range(50):
             step()
         torch.cuda.synchronize(device)
