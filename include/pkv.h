@@ -123,6 +123,40 @@ size_t pkv_paged_decode_attn_workspace_size(int num_seqs, int q_len, int n_q, in
                                             int max_context_len, unsigned flags);
 
 /*
+ * pkv_paged_decode_attn_noalloc -- pkv_paged_decode_attn without a caller workspace.
+ *
+ * The pages have no counterpart to this entry point.  It is for callers that
+ * cannot allocate device memory at all: a plugin inside another inference
+ * engine whose per-step hook must not allocate, a process whose device memory
+ * is reserved up front by some other pool, or a latency-critical loop that
+ * must never reach cudaMalloc / cudaFree (which can synchronise the device).
+ *
+ * Arguments and results are those of pkv_paged_decode_attn minus the
+ * workspace: the split-K records live in a scratch array of 24 MiB that the
+ * library holds in the device memory of every GPU that loads it, until the
+ * process exits.  The call allocates nothing.
+ *   - Sizes whose workspace would exceed 24 MiB return PKV_ERR_WORKSPACE
+ *     (every supported shape fits at up to 180 SMs; a forced CTA count in
+ *     `flags` can exceed it).
+ *   - PKV_FLAG_CHECKED returns PKV_ERR_UNSUPPORTED: the device-side report
+ *     would land in the scratch array, which the caller cannot read.  For the
+ *     same reason an expired in-kernel wait is not reported by this call.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture on the device.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls that may overlap
+ *     on the GPU -- different streams, or different host threads -- race on
+ *     it: issue them on one stream.
+ */
+int pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, const int32_t *context_lens,
+                                  int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
+                                  int block_size, int max_blocks_per_seq, int num_blocks,
+                                  float scale, void *out, int out_dtype, unsigned flags,
+                                  void *stream);
+
+/*
  * pkv_kv_append -- write this step's new keys and values into the paged cache.
  *
  * For every token i < num_tokens with 0 <= slot_mapping[i] < num_blocks * block_size:

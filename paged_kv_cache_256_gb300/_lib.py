@@ -38,6 +38,8 @@ SIGNATURES = {
     "pkv_paged_decode_attn": ([_vp, _vp, _vp, _i32p, _i32p] + [_c_int] * 8 +
                               [_c_float, _vp, _c_int, _vp, _c_size, ctypes.c_uint, _vp], _c_int),
     "pkv_paged_decode_attn_workspace_size": ([_c_int] * 7 + [ctypes.c_uint], _c_size),
+    "pkv_paged_decode_attn_noalloc": ([_vp, _vp, _vp, _i32p, _i32p] + [_c_int] * 8 +
+                                      [_c_float, _vp, _c_int, ctypes.c_uint, _vp], _c_int),
     "pkv_kv_append": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp, _vp, ctypes.c_uint, _vp], _c_int),
     "pkv_check_error": ([_vp, _vp], _c_int),
     "pkv_kv_bytes": ([_c_int] * 4 + [ctypes.c_int64], ctypes.c_int64),
@@ -167,6 +169,31 @@ def pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale
         num_blocks, float(scale), out.data_ptr(), out_dtype, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), int(flags), _stream_ptr(stream))
     _check(st, "pkv_paged_decode_attn")
+
+
+def pkv_paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                                  flags=0, stream=None):
+    """pkv_paged_decode_attn using the library's own fixed scratch (no workspace argument).
+
+    For callers that cannot allocate device memory; see include/pkv.h for the
+    24 MiB limit, the shared-scratch caveats and the first-call set-up.
+    """
+    import torch
+    _bf16_like(q, "q")
+    _bf16_like(k_cache, "k_cache")
+    _bf16_like(v_cache, "v_cache")
+    _i32(block_tables, "block_tables")
+    _i32(context_lens, "context_lens")
+    num_seqs, q_len, n_q, d = q.shape
+    num_blocks, n_kv, bs, d2 = k_cache.shape
+    if d2 != d or tuple(out.shape) != tuple(q.shape) or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent shapes")
+    out_dtype = PKV_OUT_F32 if out.dtype == torch.float32 else PKV_OUT_BF16
+    st = load_library().pkv_paged_decode_attn_noalloc(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), num_seqs, q_len, n_q, n_kv, d, bs, block_tables.shape[1],
+        num_blocks, float(scale), out.data_ptr(), out_dtype, int(flags), _stream_ptr(stream))
+    _check(st, "pkv_paged_decode_attn_noalloc")
 
 
 def pkv_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, flags=0, stream=None):
