@@ -47,13 +47,20 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kMergeSlots = 4;                   // (WN / 2) * WM is at most 4
+constexpr int kIssueLanes = 4;                   // producer lanes issuing loads side by side
 
 template <int D, int BS>
 struct AttnCfg {
     static constexpr int kTileBytes = BS * D * 2;  // one K (or V) tile of one (block, head)
     static constexpr int kStageBytes = 2 * kTileBytes;
+    // The ring depth is a multiple of the consumer-warp count: block g and
+    // block g - kStages then belong to the same warp, so when a warp waits for
+    // round r of a stage it has itself already seen round r - 1 complete.
+    // (mbarrier parity waits cannot tell round r from round r - 2; with
+    // another warp owning round r - 1 a still-in-flight load would read as
+    // complete.)
     static constexpr int kStagesRaw = (160 * 1024) / kStageBytes;
-    static constexpr int kStages = kStagesRaw > 32 ? 32 : kStagesRaw;
+    static constexpr int kStages = kStagesRaw > 32 ? 32 : (kStagesRaw / 8) * 8;
     static constexpr int kBoxBytes = BS * 128;  // one 64-column swizzled box
     static constexpr int kLaneFloats = D / 2 + 4;  // o (D/8 n-tiles x 4) + m[2] + l[2]
     static constexpr int kScratchBytes = kMergeSlots * 32 * kLaneFloats * 4;
@@ -62,6 +69,7 @@ struct AttnCfg {
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BS == 16 || BS == 32, "block_size");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+    static_assert(kStages % 8 == 0 && kStages >= 8, "ring depth must be a multiple of 8 warps");
 };
 
 // Byte offset of the 16-byte chunk holding (row, col..col+7) inside a tile
@@ -223,44 +231,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j1 = (long long)w.nb < (long long)w.j + w.left ? w.nb
                                                                      : static_cast<int>(w.j + w.left);
             const int32_t* bt = a.block_tables + (size_t)w.s * a.max_blocks_per_seq;
+            int my = w.j + lane < j1 ? __ldg(bt + w.j + lane) : 0;
             for (int jb = w.j; jb < j1 && ok; jb += 32) {
                 const int n = min(32, j1 - jb);
-                int my = lane < n ? __ldg(bt + jb + lane) : 0;
+                // The next 32 block ids load while this batch is issued.
+                const int nxt = jb + 32 + lane < j1 ? __ldg(bt + jb + 32 + lane) : 0;
                 if (lane < n && (my < 0 || my >= a.num_blocks)) {
                     if (a.checked) atomicOr(a.err, kErrBadBlock);
                     my = -1;  // read as an out-of-bounds (zero-filled) tile
                 }
-                for (int k = 0; k < n; ++k) {
-                    const int blk = __shfl_sync(0xffffffffu, my, k);
-                    if (lane == 0 && ok) {
-                        const uint32_t stage = gidx % kStages;
-                        const uint32_t par = ((gidx / kStages) & 1u) ^ 1u;
-                        if (!mbar_wait_bounded(&empty_bar[stage], par) ||
-                            *((volatile int*)&s_abort)) {
-                            ok = false;
-                            atomicOr(a.err, kErrTimeout);
-                            *((volatile int*)&s_abort) = 1;
-                        } else {
-                            mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kTileBytes);
-                            const long long y64 = ((long long)blk * a.n_kv + w.h) * BS;
-                            const int y = (blk < 0 || y64 >= a.tile_rows_total)
-                                              ? a.tile_rows_total
-                                              : static_cast<int>(y64);
-                            uint8_t* kdst = stages + stage * C::kStageBytes;
-                            uint8_t* vdst = kdst + C::kTileBytes;
+                if (*((volatile int*)&s_abort)) ok = false;  // a consumer gave up
+                // Lanes 0..kIssueLanes-1 issue the next blocks side by side:
+                // one serial wait/issue chain per block would cap the stream.
+                for (int k0 = 0; k0 < n && ok; k0 += kIssueLanes) {
+                    const int kk = k0 + lane;
+                    const int blk = __shfl_sync(0xffffffffu, my, kk & 31);
+                    const bool act = lane < kIssueLanes && kk < n;
+                    const uint32_t gl = gidx + lane;
+                    const uint32_t stage = gl % kStages;
+                    bool good = true;
+                    if (act) good = mbar_wait_bounded(&empty_bar[stage], ((gl / kStages) & 1u) ^ 1u);
+                    const unsigned act_mask = __ballot_sync(0xffffffffu, act);
+                    const unsigned good_mask = __ballot_sync(0xffffffffu, act && good);
+                    const unsigned fail = act_mask & ~good_mask;
+                    // Only the lanes below the first failed wait issue, so the
+                    // issued fills stay a prefix of the block sequence.
+                    const unsigned issue_mask =
+                        fail ? (good_mask & ((1u << (__ffs(fail) - 1)) - 1u)) : good_mask;
+                    if ((issue_mask >> lane) & 1u) {
+                        mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kTileBytes);
+                        const long long y64 = ((long long)blk * a.n_kv + w.h) * BS;
+                        const int y = (blk < 0 || y64 >= a.tile_rows_total)
+                                          ? a.tile_rows_total
+                                          : static_cast<int>(y64);
+                        uint8_t* kdst = stages + stage * C::kStageBytes;
+                        uint8_t* vdst = kdst + C::kTileBytes;
 #pragma unroll
-                            for (int half = 0; half < D / 64; ++half) {
-                                tma_load_2d(kdst + half * C::kBoxBytes, &tmap_k, half * 64, y,
-                                            &full_bar[stage], policy);
-                                tma_load_2d(vdst + half * C::kBoxBytes, &tmap_v, half * 64, y,
-                                            &full_bar[stage], policy);
-                            }
-                            issued = gidx + 1;
+                        for (int half = 0; half < D / 64; ++half) {
+                            tma_load_2d(kdst + half * C::kBoxBytes, &tmap_k, half * 64, y,
+                                        &full_bar[stage], policy);
+                            tma_load_2d(vdst + half * C::kBoxBytes, &tmap_v, half * 64, y,
+                                        &full_bar[stage], policy);
                         }
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    ++gidx;
+                    issued = gidx + __popc(issue_mask);
+                    if (fail) {
+                        ok = false;
+                        if (lane == 0) {
+                            atomicOr(a.err, kErrTimeout);
+                            *((volatile int*)&s_abort) = 1;
+                        }
+                    }
+                    gidx += min(kIssueLanes, n - k0);
                 }
+                my = nxt;
             }
             w.left -= j1 - w.j;
             if (w.left > 0) walk_next_unit<BS>(a, w);
