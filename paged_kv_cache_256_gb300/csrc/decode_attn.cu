@@ -18,18 +18,22 @@
 //     ragged the context lengths are.  A unit cut by a slice boundary is a
 //     split (flash-decoding); its pieces leave (O, m, l) partials that the
 //     LSE merge kernel combines.
-//   * Warp 8 is the producer: it reads block ids, and one lane issues 2-D TMA
-//     tile loads (128-byte swizzle) of the K and V tiles of each
-//     (block, KV head) into a ring of shared-memory stages, each guarded by a
-//     full/empty mbarrier pair.  Its walk never stops at unit boundaries, so
-//     HBM stays busy while consumers finish a unit.
-//   * Warps 0..7 consume.  Warp w owns 16-row tile (w % WM) of the unit and
-//     every WN-th block (WN = 8 / WM).  Scores S = Q K^T and the update
-//     O += P V run on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
-//     accumulate); the online softmax (running max m and sum l, fp32, base 2)
-//     is the FlashAttention recurrence ("Efficient inference", FlashAttention:
-//     exact attention without the matrix).  At the end of a unit the WN
-//     column partials are combined in shared memory by the same exact rule.
+//   * Warp 8 is the producer: it reads block ids and four of its lanes issue,
+//     side by side, 2-D TMA tile loads (128-byte swizzle) of the K and V
+//     tiles of each (block, KV head) into a ring of shared-memory stages, each
+//     guarded by a full/empty mbarrier pair.  Its walk never stops at unit
+//     boundaries, so HBM stays busy while consumers finish a unit.
+//   * Warps 0..7 consume, each taking every 8th block (and, for more than 8
+//     rows, one 16-row slice of them).  Products run on the tensor cores
+//     (mma.sync m16n8k16, bf16 in, fp32 accumulate); the online softmax
+//     (running max m and sum l, fp32, base 2) is the FlashAttention recurrence
+//     ("Efficient inference", FlashAttention: exact attention without the
+//     matrix).  At the end of a unit the warps' partials are combined in
+//     shared memory by the same exact rule.
+//       - narrow (rows <= 8): tokens on the MMA's M side, S^T = K Q^T and
+//         O^T += V^T P^T, rows padded only to 8;
+//       - wide (rows > 8): rows on the M side in 16-row slices, S = Q K^T and
+//         O += P V.
 //   * fp32 output keeps each probability as a bf16 pair (hi + lo) so the PV
 //     product keeps ~16 bits of it; bf16 output uses one bf16.
 //
@@ -46,30 +50,38 @@ namespace pkv {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kMergeSlots = 4;                   // (WN / 2) * WM is at most 4
+constexpr int kMergeSlots = 4;                   // warps that park a partial per merge round
 constexpr int kIssueLanes = 4;                   // producer lanes issuing loads side by side
+constexpr int kNarrowRows = 8;                   // rows up to which the narrow consumer is used
 
-template <int D, int BS>
+template <int D, int BS, bool NARROW>
 struct AttnCfg {
     static constexpr int kTileBytes = BS * D * 2;  // one K (or V) tile of one (block, head)
     static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kBoxBytes = BS * 128;  // one 64-column swizzled box
+    // Per-lane floats a warp parks for a merge round: its accumulator, m[2], l[2].
+    static constexpr int kLaneFloats = (NARROW ? D / 4 : D / 2) + 4;
+    static constexpr int kMergeBytes = kMergeSlots * 32 * kLaneFloats * 4;
+    // Narrow emit: rows x head_dim fp32 tile (+4 floats of row padding) and (m, l) per row.
+    static constexpr int kTileStride = D + 4;
+    static constexpr int kEmitBytes = NARROW ? (kNarrowRows * kTileStride + 2 * kNarrowRows) * 4 : 0;
+    static constexpr int kScratchBytes = kMergeBytes + kEmitBytes;
+    static constexpr int kBarrierBytes = 2 * 32 * 8;
+    static constexpr int kBudget = 227 * 1024 - 1024 - kScratchBytes - kBarrierBytes - 1024;
     // The ring depth is a multiple of the consumer-warp count: block g and
     // block g - kStages then belong to the same warp, so when a warp waits for
     // round r of a stage it has itself already seen round r - 1 complete.
     // (mbarrier parity waits cannot tell round r from round r - 2; with
     // another warp owning round r - 1 a still-in-flight load would read as
     // complete.)
-    static constexpr int kStagesRaw = (160 * 1024) / kStageBytes;
-    static constexpr int kStages = kStagesRaw > 32 ? 32 : (kStagesRaw / 8) * 8;
-    static constexpr int kBoxBytes = BS * 128;  // one 64-column swizzled box
-    static constexpr int kLaneFloats = D / 2 + 4;  // o (D/8 n-tiles x 4) + m[2] + l[2]
-    static constexpr int kScratchBytes = kMergeSlots * 32 * kLaneFloats * 4;
-    static constexpr int kBarrierBytes = 2 * kStages * 8;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kScratchBytes + kBarrierBytes;
+    static constexpr int kStagesRaw = kBudget / kStageBytes;
+    static constexpr int kStages = kStagesRaw >= 32 ? 32 : (kStagesRaw / 8) * 8;
+    static constexpr int kSmemBytes =
+        1024 + kStages * kStageBytes + kScratchBytes + 2 * kStages * 8;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BS == 16 || BS == 32, "block_size");
+    static_assert(kStages % kConsumerWarps == 0 && kStages >= kConsumerWarps, "ring depth");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-    static_assert(kStages % 8 == 0 && kStages >= 8, "ring depth must be a multiple of 8 warps");
 };
 
 // Byte offset of the 16-byte chunk holding (row, col..col+7) inside a tile
@@ -81,17 +93,14 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
                                  ((((col & 63) >> 3) ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ int unit_blocks(const AttnArgs& a, int s, int bs) {
-    int ctx = __ldg(a.context_lens + s);
-    const int cap = a.max_blocks_per_seq * bs;
-    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-    return (ctx + bs - 1) / bs;
-}
-
 __device__ __forceinline__ int unit_ctx(const AttnArgs& a, int s, int bs) {
     int ctx = __ldg(a.context_lens + s);
     const int cap = a.max_blocks_per_seq * bs;
     return ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+}
+
+__device__ __forceinline__ int unit_blocks(const AttnArgs& a, int s, int bs) {
+    return (unit_ctx(a, s, bs) + bs - 1) / bs;
 }
 
 // Position in the flat work list: sequence s, KV head h, block j of that unit,
@@ -112,6 +121,10 @@ __device__ __forceinline__ void walk_next_unit(const AttnArgs& a, Walk& w) {
         } while (w.nb == 0);
         w.ctx = unit_ctx(a, w.s, BS);
     }
+}
+
+__device__ __forceinline__ int piece_end(const Walk& w) {
+    return (long long)w.nb < (long long)w.j + w.left ? w.nb : static_cast<int>(w.j + w.left);
 }
 
 // Block-wide inclusive scan of one 64-bit value per thread (all kThreads).
@@ -137,59 +150,19 @@ __device__ __forceinline__ long long block_inclusive_scan(long long v, long long
     return v + before;
 }
 
-template <int D, int BS, bool OUT_F32>
-__global__ void __launch_bounds__(kThreads, 1)
-    paged_decode_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                             const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
-    using C = AttnCfg<D, BS>;
-    constexpr int kStages = C::kStages;
-    constexpr int NT = D / 8;    // 8-wide output column tiles
-    constexpr int KT = D / 16;   // 16-deep k steps over head_dim
-    constexpr int ST = BS / 8;   // 8-token score tiles per block
-    constexpr int PT = BS / 16;  // 16-token k steps of the PV product
-
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_addr(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    uint8_t* stages = smem;
-    float* scratch = reinterpret_cast<float*>(smem + kStages * C::kStageBytes);
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes +
-                                                     C::kScratchBytes);
-    uint64_t* empty_bar = full_bar + kStages;
-
-    __shared__ long long s_red[kThreads / 32];
-    __shared__ long long s_start[2];
-    __shared__ int s_abort;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int WM = a.warp_rows;
-    const int WN = kConsumerWarps / WM;
-    const int cta = blockIdx.x, grid = gridDim.x;
-
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], WM);
-        }
-        fence_barrier_init();
-        s_abort = 0;
-        s_start[0] = -1;
-        s_start[1] = 0;
-    }
-    if (warp == kConsumerWarps && lane == 0) {
-        prefetch_tensormap(&tmap_k);
-        prefetch_tensormap(&tmap_v);
-    }
-
-    // ---- this CTA's slice of the flat (unit, block) work list --------------
+// All threads: this CTA's slice [start, end) of the flat (unit, block) list,
+// as the walk position of its first item.
+template <int BS>
+__device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
+                                           long long* s_start) {
+    const int tid = threadIdx.x, cta = blockIdx.x, grid = gridDim.x;
     long long mine = 0;
     for (int s = tid; s < a.num_seqs; s += kThreads) mine += unit_blocks(a, s, BS);
     long long total_blocks;
-    (void)block_inclusive_scan(mine, s_red, total_blocks);  // also publishes barrier init
+    (void)block_inclusive_scan(mine, s_red, total_blocks);
     const long long W = total_blocks * a.n_kv;
     const long long start = (W * cta) / grid;
     const long long end = (W * (cta + 1)) / grid;
-
     if (start < end) {
         long long base = 0;
         for (int s0 = 0; s0 < a.num_seqs; s0 += kThreads) {
@@ -208,134 +181,439 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-
-    Walk w0;
-    w0.left = end - start;
-    if (w0.left > 0) {
-        w0.s = static_cast<int>(s_start[0]);
-        w0.nb = unit_blocks(a, w0.s, BS);
-        w0.ctx = unit_ctx(a, w0.s, BS);
-        w0.h = static_cast<int>(s_start[1] / w0.nb);
-        w0.j = static_cast<int>(s_start[1] % w0.nb);
+    Walk w;
+    w.left = end - start;
+    if (w.left > 0) {
+        w.s = static_cast<int>(s_start[0]);
+        w.nb = unit_blocks(a, w.s, BS);
+        w.ctx = unit_ctx(a, w.s, BS);
+        w.h = static_cast<int>(s_start[1] / w.nb);
+        w.j = static_cast<int>(s_start[1] % w.nb);
     } else {
-        w0.s = w0.h = w0.j = w0.nb = w0.ctx = 0;
+        w.s = w.h = w.j = w.nb = w.ctx = 0;
     }
+    return w;
+}
 
-    if (warp == kConsumerWarps) {
-        // ===================== producer warp =====================
-        const uint64_t policy = l2_policy_evict_first();
-        uint32_t gidx = 0, issued = 0;  // issued: fills actually started (a prefix of gidx)
-        bool ok = true;
-        Walk w = w0;
-        while (w.left > 0 && ok) {
-            const int j1 = (long long)w.nb < (long long)w.j + w.left ? w.nb
-                                                                     : static_cast<int>(w.j + w.left);
-            const int32_t* bt = a.block_tables + (size_t)w.s * a.max_blocks_per_seq;
-            int my = w.j + lane < j1 ? __ldg(bt + w.j + lane) : 0;
-            for (int jb = w.j; jb < j1 && ok; jb += 32) {
-                const int n = min(32, j1 - jb);
-                // The next 32 block ids load while this batch is issued.
-                const int nxt = jb + 32 + lane < j1 ? __ldg(bt + jb + 32 + lane) : 0;
-                if (lane < n && (my < 0 || my >= a.num_blocks)) {
-                    if (a.checked) atomicOr(a.err, kErrBadBlock);
-                    my = -1;  // read as an out-of-bounds (zero-filled) tile
-                }
-                if (*((volatile int*)&s_abort)) ok = false;  // a consumer gave up
-                // Lanes 0..kIssueLanes-1 issue the next blocks side by side:
-                // one serial wait/issue chain per block would cap the stream.
-                for (int k0 = 0; k0 < n && ok; k0 += kIssueLanes) {
-                    const int kk = k0 + lane;
-                    const int blk = __shfl_sync(0xffffffffu, my, kk & 31);
-                    const bool act = lane < kIssueLanes && kk < n;
-                    const uint32_t gl = gidx + lane;
-                    const uint32_t stage = gl % kStages;
-                    bool good = true;
-                    if (act) good = mbar_wait_bounded(&empty_bar[stage], ((gl / kStages) & 1u) ^ 1u);
-                    const unsigned act_mask = __ballot_sync(0xffffffffu, act);
-                    const unsigned good_mask = __ballot_sync(0xffffffffu, act && good);
-                    const unsigned fail = act_mask & ~good_mask;
-                    // Only the lanes below the first failed wait issue, so the
-                    // issued fills stay a prefix of the block sequence.
-                    const unsigned issue_mask =
-                        fail ? (good_mask & ((1u << (__ffs(fail) - 1)) - 1u)) : good_mask;
-                    if ((issue_mask >> lane) & 1u) {
-                        mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kTileBytes);
-                        const long long y64 = ((long long)blk * a.n_kv + w.h) * BS;
-                        const int y = (blk < 0 || y64 >= a.tile_rows_total)
-                                          ? a.tile_rows_total
-                                          : static_cast<int>(y64);
-                        uint8_t* kdst = stages + stage * C::kStageBytes;
-                        uint8_t* vdst = kdst + C::kTileBytes;
+// ===================== producer warp =====================
+template <int D, int BS, int kStages, int kStageBytes, int kTileBytes, int kBoxBytes>
+__device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tmap_k,
+                                        const CUtensorMap* tmap_v, Walk w, uint8_t* stages,
+                                        uint64_t* full_bar, uint64_t* empty_bar,
+                                        volatile int* s_abort) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t policy = l2_policy_evict_first();
+    uint32_t gidx = 0, issued = 0;  // issued: fills actually started (a prefix of gidx)
+    bool ok = true;
+    while (w.left > 0 && ok) {
+        const int j1 = piece_end(w);
+        const int32_t* bt = a.block_tables + (size_t)w.s * a.max_blocks_per_seq;
+        int my = w.j + lane < j1 ? __ldg(bt + w.j + lane) : 0;
+        for (int jb = w.j; jb < j1 && ok; jb += 32) {
+            const int n = min(32, j1 - jb);
+            // The next 32 block ids load while this batch is issued.
+            const int nxt = jb + 32 + lane < j1 ? __ldg(bt + jb + 32 + lane) : 0;
+            if (lane < n && (my < 0 || my >= a.num_blocks)) {
+                if (a.checked) atomicOr(a.err, kErrBadBlock);
+                my = -1;  // read as an out-of-bounds (zero-filled) tile
+            }
+            if (*s_abort) ok = false;  // a consumer gave up
+            // Lanes 0..kIssueLanes-1 issue the next blocks side by side: one
+            // serial wait/issue chain per block would cap the stream.
+            for (int k0 = 0; k0 < n && ok; k0 += kIssueLanes) {
+                const int kk = k0 + lane;
+                const int blk = __shfl_sync(0xffffffffu, my, kk & 31);
+                const bool act = lane < kIssueLanes && kk < n;
+                const uint32_t gl = gidx + lane;
+                const uint32_t stage = gl % kStages;
+                bool good = true;
+                if (act) good = mbar_wait_bounded(&empty_bar[stage], ((gl / kStages) & 1u) ^ 1u);
+                const unsigned act_mask = __ballot_sync(0xffffffffu, act);
+                const unsigned good_mask = __ballot_sync(0xffffffffu, act && good);
+                const unsigned fail = act_mask & ~good_mask;
+                // Only the lanes below the first failed wait issue, so the
+                // issued fills stay a prefix of the block sequence.
+                const unsigned issue_mask =
+                    fail ? (good_mask & ((1u << (__ffs(fail) - 1)) - 1u)) : good_mask;
+                if ((issue_mask >> lane) & 1u) {
+                    mbar_arrive_expect_tx(&full_bar[stage], 2 * kTileBytes);
+                    const long long y64 = ((long long)blk * a.n_kv + w.h) * BS;
+                    const int y = (blk < 0 || y64 >= a.tile_rows_total)
+                                      ? a.tile_rows_total
+                                      : static_cast<int>(y64);
+                    uint8_t* kdst = stages + stage * kStageBytes;
+                    uint8_t* vdst = kdst + kTileBytes;
 #pragma unroll
-                        for (int half = 0; half < D / 64; ++half) {
-                            tma_load_2d(kdst + half * C::kBoxBytes, &tmap_k, half * 64, y,
-                                        &full_bar[stage], policy);
-                            tma_load_2d(vdst + half * C::kBoxBytes, &tmap_v, half * 64, y,
-                                        &full_bar[stage], policy);
-                        }
+                    for (int half = 0; half < D / 64; ++half) {
+                        tma_load_2d(kdst + half * kBoxBytes, tmap_k, half * 64, y,
+                                    &full_bar[stage], policy);
+                        tma_load_2d(vdst + half * kBoxBytes, tmap_v, half * 64, y,
+                                    &full_bar[stage], policy);
                     }
-                    issued = gidx + __popc(issue_mask);
-                    if (fail) {
-                        ok = false;
-                        if (lane == 0) {
-                            atomicOr(a.err, kErrTimeout);
-                            *((volatile int*)&s_abort) = 1;
-                        }
-                    }
-                    gidx += min(kIssueLanes, n - k0);
                 }
-                my = nxt;
+                issued = gidx + __popc(issue_mask);
+                if (fail) {
+                    ok = false;
+                    if (lane == 0) {
+                        atomicOr(a.err, kErrTimeout);
+                        *s_abort = 1;
+                    }
+                }
+                gidx += min(kIssueLanes, n - k0);
             }
-            w.left -= j1 - w.j;
-            if (w.left > 0) walk_next_unit<BS>(a, w);
+            my = nxt;
         }
-        // Do not leave the CTA while copies into its shared memory are in flight.
-        if (lane == 0) {
-            const uint32_t first = issued > (uint32_t)kStages ? issued - kStages : 0u;
-            for (uint32_t qi = first; qi < issued; ++qi)
-                if (!mbar_wait_bounded(&full_bar[qi % kStages], (qi / kStages) & 1u)) break;
-        }
-        return;
+        w.left -= j1 - w.j;
+        if (w.left > 0) walk_next_unit<BS>(a, w);
     }
-
-    // ===================== consumer warps =====================
-    // Sequences with nothing resident produce zero rows (and are checked).
-    for (int s = cta; s < a.num_seqs; s += grid) {
-        const int raw = __ldg(a.context_lens + s);
-        if (a.checked && tid == 0 &&
-            (raw < 0 || raw > a.max_blocks_per_seq * BS || (raw > 0 && raw < a.q_len)))
-            atomicOr(a.err, kErrBadContext);
-        if (unit_blocks(a, s, BS) == 0) {
-            const size_t n = (size_t)a.q_len * a.n_q * D;
-            const size_t o0 = (size_t)s * n;
-            for (size_t e = tid; e < n; e += kConsumerThreads) {
-                if (OUT_F32)
-                    static_cast<float*>(a.out)[o0 + e] = 0.f;
-                else
-                    static_cast<uint16_t*>(a.out)[o0 + e] = 0;
-            }
-        }
+    // Do not leave the CTA while copies into its shared memory are in flight.
+    if (lane == 0) {
+        const uint32_t first = issued > (uint32_t)kStages ? issued - kStages : 0u;
+        for (uint32_t qi = first; qi < issued; ++qi)
+            if (!mbar_wait_bounded(&full_bar[qi % kStages], (qi / kStages) & 1u)) break;
     }
+}
 
-    const int mt = warp % WM;  // which 16-row tile of the unit's rows
-    const int col = warp / WM; // which residue class of blocks
-    const int g = lane >> 2, t = lane & 3;
-    const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix index, row within matrix
-    const int G = a.group;
+// Wait for a stage as a consumer (all 32 lanes).  The verdict is a warp vote,
+// so the warp-collective work that follows runs on all lanes or on none; once
+// anything failed the warp stops waiting and the CTA is told.
+__device__ __forceinline__ bool consumer_wait(const AttnArgs& a, uint64_t* bar, uint32_t parity,
+                                              bool ok, volatile int* s_abort) {
+    bool good = ok && !*s_abort;
+    if (good && !mbar_wait_bounded(bar, parity)) {
+        good = false;
+        atomicOr(a.err, kErrTimeout);
+        *s_abort = 1;
+    }
+    return __all_sync(0xffffffffu, good);
+}
 
-    int4 info0 = make_int4(0, 0, 0, 0), info1 = make_int4(0, 0, 0, 0);
-    if (w0.left <= 0) info0.z = info1.z = kRecEmpty;
+// Combine two online-softmax states of one row: weights a1, a2 for the two
+// accumulators, and the combined (m, l).
+__device__ __forceinline__ void merge_weights(float& m, float& l, float m2, float l2, float& a1,
+                                              float& a2) {
+    const float mn = fmaxf(m, m2);
+    const float mb = mn == -INFINITY ? 0.f : mn;
+    a1 = fast_exp2(m - mb);
+    a2 = fast_exp2(m2 - mb);
+    l = a1 * l + a2 * l2;
+    m = mn;
+}
 
-    uint32_t gidx = 0;
+// ===================== narrow consumer (rows <= 8) =====================
+// Warp w takes blocks g == w (mod 8).  Per 16-token tile of a block:
+//   S^T[tok][row] = K[tok][:] . Q^T[:][row]       (A = K tile via ldmatrix, B = Q^T)
+//   P^T B-fragment = movmatrix.trans of bf16(S^T) (rows move from the column
+//                    index of the accumulator to the lane index of the operand)
+//   O^T[d][row]  += V^T[d][tok] . P^T[tok][row]    (A = V tile via ldmatrix.trans)
+// Lane (g, t) holds rows 2t, 2t+1 of the softmax state; a row's max and sum
+// reduce over the 8 lanes sharing t.
+template <int D, int BS, bool OUT_F32>
+__device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_t* stages,
+                                               float* scratch, uint64_t* full_bar,
+                                               uint64_t* empty_bar, volatile int* s_abort,
+                                               int4& info0, int4& info1) {
+    using C = AttnCfg<D, BS, true>;
+    constexpr int kStages = C::kStages;
+    constexpr int MT = D / 16;   // 16-wide head_dim tiles (M of the PV product)
+    constexpr int KT = D / 16;   // 16-deep k steps of the score product
+    constexpr int PT = BS / 16;  // 16-token tiles per block
+    constexpr int WN = kConsumerWarps;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3, mi = lane >> 3, rr = lane & 7;
+    const int G = a.group, R = a.rows, cta = blockIdx.x;
+    float* emit_tile = scratch + C::kMergeBytes / 4;
+    float* emit_ml = emit_tile + kNarrowRows * C::kTileStride;
+
+    uint32_t gbase = 0;  // sequence number (in this CTA) of the piece's first block
     bool ok = true;
     int piece = 0;
-    Walk w = w0;
     while (w.left > 0) {
-        const int j0 = w.j;
-        const int j1 = (long long)w.nb < (long long)w.j + w.left ? w.nb
-                                                                 : static_cast<int>(w.j + w.left);
-        const int ctx = w.ctx;
-        const int s = w.s, h = w.h;
+        const int j0 = w.j, j1 = piece_end(w);
+        const int ctx = w.ctx, s = w.s, h = w.h;
+
+        // Q^T as B fragments: (k = head_dim 2t.., n = row g); rows >= R are zero.
+        uint32_t qb[KT][2];
+        {
+            const bool valid = g < R;
+            const int i = valid ? g / G : 0;
+            const int hq = h * G + (valid ? g % G : 0);
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                a.q + (((size_t)s * a.q_len + i) * a.n_q + hq) * D);
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                qb[kk][0] = valid ? __ldg(qrow + kk * 8 + t) : 0u;
+                qb[kk][1] = valid ? __ldg(qrow + kk * 8 + 4 + t) : 0u;
+            }
+        }
+        int lim[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 2 * t + e;
+            lim[e] = r < R ? ctx - a.q_len + r / G : -1;
+        }
+        const int lim_min = ctx - a.q_len;
+
+        float o[MT][4];
+#pragma unroll
+        for (int n = 0; n < MT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+
+        const int first = static_cast<int>((uint32_t)(warp + WN - (int)(gbase % WN)) % WN);
+        for (int jj = first; jj < j1 - j0; jj += WN) {
+            const int j = j0 + jj;
+            const uint32_t gidx = gbase + jj;
+            const uint32_t stage = gidx % kStages;
+            ok = consumer_wait(a, &full_bar[stage], (gidx / kStages) & 1u, ok, s_abort);
+            if (ok) {
+                const uint32_t kb = smem_addr(stages + stage * C::kStageBytes);
+                const uint32_t vb = kb + C::kTileBytes;
+
+                // ---- S^T = K Q^T, two interleaved accumulators per 16-token tile
+                float st[PT][4], st2[PT][4];
+#pragma unroll
+                for (int p = 0; p < PT; ++p)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) st[p][e] = st2[p][e] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < KT; ++kk) {
+#pragma unroll
+                    for (int tp = 0; tp < PT; ++tp) {
+                        uint32_t ka[4];
+                        ldmatrix_x4(ka, kb + swz<BS>(tp * 16 + (mi & 1) * 8 + rr,
+                                                      kk * 16 + (mi >> 1) * 8));
+                        if (kk & 1)
+                            mma_bf16_16816(st2[tp], ka, qb[kk][0], qb[kk][1]);
+                        else
+                            mma_bf16_16816(st[tp], ka, qb[kk][0], qb[kk][1]);
+                    }
+                }
+
+                // ---- scale, causal / tail mask, online softmax (base 2)
+                const int tok0 = j * BS;
+                const bool need_mask = tok0 + BS - 1 > lim_min;
+                float mloc[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int tp = 0; tp < PT; ++tp) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float x = (st[tp][e] + st2[tp][e]) * a.scale_log2;
+                        if (need_mask && tok0 + tp * 16 + g + (e >> 1) * 8 > lim[e & 1])
+                            x = -INFINITY;
+                        st[tp][e] = x;
+                        mloc[e & 1] = fmaxf(mloc[e & 1], x);
+                    }
+                }
+                float alpha[2], mbase[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    mloc[e] = fmaxf(mloc[e], __shfl_xor_sync(0xffffffffu, mloc[e], 4));
+                    mloc[e] = fmaxf(mloc[e], __shfl_xor_sync(0xffffffffu, mloc[e], 8));
+                    mloc[e] = fmaxf(mloc[e], __shfl_xor_sync(0xffffffffu, mloc[e], 16));
+                    const float mnew = fmaxf(m[e], mloc[e]);
+                    mbase[e] = mnew == -INFINITY ? 0.f : mnew;
+                    alpha[e] = fast_exp2(m[e] - mbase[e]);
+                    m[e] = mnew;
+                }
+                float rsum[2] = {0.f, 0.f};
+#pragma unroll
+                for (int tp = 0; tp < PT; ++tp) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float p = fast_exp2(st[tp][e] - mbase[e & 1]);
+                        st[tp][e] = p;
+                        rsum[e & 1] += p;
+                    }
+                }
+                l[0] = l[0] * alpha[0] + rsum[0];
+                l[1] = l[1] * alpha[1] + rsum[1];
+                if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
+#pragma unroll
+                    for (int n = 0; n < MT; ++n) {
+                        o[n][0] *= alpha[0];
+                        o[n][1] *= alpha[1];
+                        o[n][2] *= alpha[0];
+                        o[n][3] *= alpha[1];
+                    }
+                }
+
+                // ---- P^T as B fragments: pack (tok g, rows 2t..) then transpose
+                uint32_t pb[PT][2], pl[PT][2];
+#pragma unroll
+                for (int tp = 0; tp < PT; ++tp) {
+                    const uint32_t h0 = pack_bf16x2(st[tp][0], st[tp][1]);
+                    const uint32_t h1 = pack_bf16x2(st[tp][2], st[tp][3]);
+                    pb[tp][0] = movmatrix_trans(h0);
+                    pb[tp][1] = movmatrix_trans(h1);
+                    if (OUT_F32) {
+                        pl[tp][0] = movmatrix_trans(pack_bf16x2(st[tp][0] - bf16_lo_to_f32(h0),
+                                                                st[tp][1] - bf16_hi_to_f32(h0)));
+                        pl[tp][1] = movmatrix_trans(pack_bf16x2(st[tp][2] - bf16_lo_to_f32(h1),
+                                                                st[tp][3] - bf16_hi_to_f32(h1)));
+                    }
+                }
+
+                // ---- O^T += V^T P^T (V rows past the context are zeroed: they may hold NaN)
+                const bool need_vmask = tok0 + BS > ctx;
+#pragma unroll
+                for (int tp = 0; tp < PT; ++tp) {
+                    uint32_t vm0 = 0xFFFFFFFFu, vm8 = 0xFFFFFFFFu;
+                    if (need_vmask) {
+                        const int ta = tok0 + tp * 16 + 2 * t;
+                        vm0 = (ta < ctx ? 0x0000FFFFu : 0u) | (ta + 1 < ctx ? 0xFFFF0000u : 0u);
+                        vm8 = (ta + 8 < ctx ? 0x0000FFFFu : 0u) | (ta + 9 < ctx ? 0xFFFF0000u : 0u);
+                    }
+#pragma unroll
+                    for (int dm = 0; dm < MT; ++dm) {
+                        uint32_t va[4];
+                        ldmatrix_x4_trans(va, vb + swz<BS>(tp * 16 + (mi >> 1) * 8 + rr,
+                                                            dm * 16 + (mi & 1) * 8));
+                        va[0] &= vm0;
+                        va[1] &= vm0;
+                        va[2] &= vm8;
+                        va[3] &= vm8;
+                        mma_bf16_16816(o[dm], va, pb[tp][0], pb[tp][1]);
+                        if (OUT_F32) mma_bf16_16816(o[dm], va, pl[tp][0], pl[tp][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        }
+        gbase += j1 - j0;
+
+        // ---- row sums across the 8 lanes of a row, then combine the warps' partials
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            l[e] += __shfl_xor_sync(0xffffffffu, l[e], 4);
+            l[e] += __shfl_xor_sync(0xffffffffu, l[e], 8);
+            l[e] += __shfl_xor_sync(0xffffffffu, l[e], 16);
+        }
+        for (int step = WN >> 1; step >= 1; step >>= 1) {
+            if (warp >= step && warp < 2 * step) {
+                float* sl = scratch + (size_t)(warp - step) * 32 * C::kLaneFloats;
+#pragma unroll
+                for (int n = 0; n < MT; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sl[(n * 4 + e) * 32 + lane] = o[n][e];
+                sl[(MT * 4 + 0) * 32 + lane] = m[0];
+                sl[(MT * 4 + 1) * 32 + lane] = m[1];
+                sl[(MT * 4 + 2) * 32 + lane] = l[0];
+                sl[(MT * 4 + 3) * 32 + lane] = l[1];
+            }
+            named_barrier_sync(1, kConsumerThreads);
+            if (warp < step) {
+                const float* sl = scratch + (size_t)warp * 32 * C::kLaneFloats;
+                float a1[2], a2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    merge_weights(m[e], l[e], sl[(MT * 4 + e) * 32 + lane],
+                                  sl[(MT * 4 + 2 + e) * 32 + lane], a1[e], a2[e]);
+#pragma unroll
+                for (int n = 0; n < MT; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        o[n][e] = a1[e & 1] * o[n][e] + a2[e & 1] * sl[(n * 4 + e) * 32 + lane];
+            }
+            named_barrier_sync(1, kConsumerThreads);
+        }
+
+        // ---- emit (warp 0): through a row-major tile, then 16-byte stores
+        const bool first_piece = j0 == 0, last_piece = j1 == w.nb;
+        const bool whole = first_piece && last_piece;
+        if (warp == 0) {
+            float scl[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) scl[e] = whole ? (l[e] > 0.f ? 1.f / l[e] : 0.f) : 1.f;
+#pragma unroll
+            for (int n = 0; n < MT; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    emit_tile[(2 * t + (e & 1)) * C::kTileStride + n * 16 + g + (e >> 1) * 8] =
+                        o[n][e] * scl[e & 1];
+            if (g == 0) {
+                emit_ml[(2 * t) * 2 + 0] = m[0];
+                emit_ml[(2 * t) * 2 + 1] = l[0];
+                emit_ml[(2 * t + 1) * 2 + 0] = m[1];
+                emit_ml[(2 * t + 1) * 2 + 1] = l[1];
+            }
+            __syncwarp();
+            if (whole) {
+                constexpr int V = OUT_F32 ? 4 : 8;  // elements per 16-byte store
+                for (int idx = lane; idx < R * (D / V); idx += 32) {
+                    const int r = idx / (D / V), c = (idx % (D / V)) * V;
+                    const int i = r / G, hq = h * G + r % G;
+                    const size_t ob = (((size_t)s * a.q_len + i) * a.n_q + hq) * D + c;
+                    const float* src = emit_tile + r * C::kTileStride + c;
+                    if (OUT_F32) {
+                        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + ob) =
+                            make_float4(src[0], src[1], src[2], src[3]);
+                    } else {
+                        uint4 v;
+                        v.x = pack_bf16x2(src[0], src[1]);
+                        v.y = pack_bf16x2(src[2], src[3]);
+                        v.z = pack_bf16x2(src[4], src[5]);
+                        v.w = pack_bf16x2(src[6], src[7]);
+                        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ob) = v;
+                    }
+                }
+            } else {
+                const int slot = piece == 0 ? 0 : 1;
+                const size_t rec = (size_t)cta * 2 + slot;
+                for (int idx = lane; idx < R * (D / 4); idx += 32) {
+                    const int r = idx / (D / 4), c = (idx % (D / 4)) * 4;
+                    const float* src = emit_tile + r * C::kTileStride + c;
+                    *reinterpret_cast<float4*>(a.rec_o + (rec * R + r) * D + c) =
+                        make_float4(src[0], src[1], src[2], src[3]);
+                }
+                if (lane < R)
+                    *reinterpret_cast<float2*>(a.rec_ml + (rec * R + lane) * 2) =
+                        make_float2(emit_ml[lane * 2], emit_ml[lane * 2 + 1]);
+                const int4 rinfo = make_int4(
+                    s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0), 0);
+                if (slot == 0)
+                    info0 = rinfo;
+                else
+                    info1 = rinfo;
+            }
+            __syncwarp();
+        }
+        ++piece;
+        w.left -= j1 - w.j;
+        if (w.left > 0) walk_next_unit<BS>(a, w);
+    }
+}
+
+// ===================== wide consumer (rows > 8) =====================
+// Warp w owns 16-row slice (w % WM) of the unit's rows and blocks g == w / WM
+// (mod WN), WM * WN = 8.  S = Q K^T (A = Q rows, B = K via ldmatrix), P stays
+// in registers as the A operand of O += P V (B = V via ldmatrix.trans).
+template <int D, int BS, bool OUT_F32>
+__device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t* stages,
+                                             float* scratch, uint64_t* full_bar,
+                                             uint64_t* empty_bar, volatile int* s_abort,
+                                             int4& info0, int4& info1) {
+    using C = AttnCfg<D, BS, false>;
+    constexpr int kStages = C::kStages;
+    constexpr int NT = D / 8;    // 8-wide output column tiles
+    constexpr int KT = D / 16;   // 16-deep k steps over head_dim
+    constexpr int ST = BS / 8;   // 8-token score tiles per block
+    constexpr int PT = BS / 16;  // 16-token k steps of the PV product
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int WM = a.warp_rows;
+    const int WN = kConsumerWarps / WM;
+    const int mt = warp % WM;   // which 16-row slice of the unit's rows
+    const int col = warp / WM;  // which residue class of blocks
+    const int g = lane >> 2, t = lane & 3;
+    const int mi = lane >> 3, rr = lane & 7;
+    const int G = a.group, cta = blockIdx.x;
+
+    uint32_t gbase = 0;
+    bool ok = true;
+    int piece = 0;
+    while (w.left > 0) {
+        const int j0 = w.j, j1 = piece_end(w);
+        const int ctx = w.ctx, s = w.s, h = w.h;
 
         // Query fragments of this unit's two rows per thread (rows >= a.rows are zero).
         uint32_t qf[KT][4];
@@ -362,15 +640,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
 
-        for (int j = j0; j < j1; ++j, ++gidx) {
-            if ((int)(gidx % (uint32_t)WN) != col) continue;
+        const int first = static_cast<int>((uint32_t)(col + WN - (int)(gbase % WN)) % WN);
+        for (int jj = first; jj < j1 - j0; jj += WN) {
+            const int j = j0 + jj;
+            const uint32_t gidx = gbase + jj;
             const uint32_t stage = gidx % kStages;
-            if (ok && *((volatile int*)&s_abort)) ok = false;  // another warp gave up
-            if (ok && !mbar_wait_bounded(&full_bar[stage], (gidx / kStages) & 1u)) {
-                ok = false;
-                atomicOr(a.err, kErrTimeout);
-                *((volatile int*)&s_abort) = 1;
-            }
+            ok = consumer_wait(a, &full_bar[stage], (gidx / kStages) & 1u, ok, s_abort);
             if (ok) {
                 const uint32_t kbase = smem_addr(stages + stage * C::kStageBytes);
                 const uint32_t vbase = kbase + C::kTileBytes;
@@ -384,9 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int tp = 0; tp < PT; ++tp) {
                         uint32_t b[4];
-                        const int tok = tp * 16 + (mi >> 1) * 8 + rr;
-                        const int dc = kk * 16 + (mi & 1) * 8;
-                        ldmatrix_x4(b, kbase + swz<BS>(tok, dc));
+                        ldmatrix_x4(b, kbase + swz<BS>(tp * 16 + (mi >> 1) * 8 + rr,
+                                                        kk * 16 + (mi & 1) * 8));
                         mma_bf16_16816(sc[2 * tp], qf[kk], b[0], b[1]);
                         mma_bf16_16816(sc[2 * tp + 1], qf[kk], b[2], b[3]);
                     }
@@ -401,10 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float x = sc[n][e] * a.scale_log2;
-                        if (need_mask) {
-                            const int tk = tok0 + n * 8 + 2 * t + (e & 1);
-                            if (tk > lim[e >> 1]) x = -INFINITY;
-                        }
+                        if (need_mask && tok0 + n * 8 + 2 * t + (e & 1) > lim[e >> 1])
+                            x = -INFINITY;
                         sc[n][e] = x;
                         mloc[e >> 1] = fmaxf(mloc[e >> 1], x);
                     }
@@ -431,12 +703,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) l[hh] = l[hh] * alpha[hh] + rsum[hh];
+                if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    o[n][0] *= alpha[0];
-                    o[n][1] *= alpha[0];
-                    o[n][2] *= alpha[1];
-                    o[n][3] *= alpha[1];
+                    for (int n = 0; n < NT; ++n) {
+                        o[n][0] *= alpha[0];
+                        o[n][1] *= alpha[0];
+                        o[n][2] *= alpha[1];
+                        o[n][3] *= alpha[1];
+                    }
                 }
 
                 // ---- P as bf16 A fragments (fp32 output: hi + lo pair)
@@ -469,9 +743,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int dp = 0; dp < D / 16; ++dp) {
                         uint32_t b[4];
-                        const int tok = tp * 16 + (mi & 1) * 8 + rr;
-                        const int dc = dp * 16 + (mi >> 1) * 8;
-                        ldmatrix_x4_trans(b, vbase + swz<BS>(tok, dc));
+                        ldmatrix_x4_trans(b, vbase + swz<BS>(tp * 16 + (mi & 1) * 8 + rr,
+                                                              dp * 16 + (mi >> 1) * 8));
                         b[0] &= vm0;
                         b[1] &= vm8;
                         b[2] &= vm0;
@@ -488,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
         }
+        gbase += j1 - j0;
 
         // ---- row sums across the quad, then combine the WN column partials
 #pragma unroll
@@ -512,16 +786,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float* sl = scratch + (size_t)(col * WM + mt) * 32 * C::kLaneFloats;
                 float a1[2], a2[2];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const float m2 = sl[(NT * 4 + hh) * 32 + lane];
-                    const float l2 = sl[(NT * 4 + 2 + hh) * 32 + lane];
-                    const float mn = fmaxf(m[hh], m2);
-                    const float mb = mn == -INFINITY ? 0.f : mn;
-                    a1[hh] = fast_exp2(m[hh] - mb);
-                    a2[hh] = fast_exp2(m2 - mb);
-                    l[hh] = a1[hh] * l[hh] + a2[hh] * l2;
-                    m[hh] = mn;
-                }
+                for (int hh = 0; hh < 2; ++hh)
+                    merge_weights(m[hh], l[hh], sl[(NT * 4 + hh) * 32 + lane],
+                                  sl[(NT * 4 + 2 + hh) * 32 + lane], a1[hh], a2[hh]);
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -532,9 +799,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---- emit: a whole unit goes straight to `out`; a piece becomes a record
-        const bool first = j0 == 0, last = j1 == w.nb;
+        const bool first_piece = j0 == 0, last_piece = j1 == w.nb;
         if (col == 0) {
-            if (first && last) {
+            if (first_piece && last_piece) {
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int r = mt * 16 + g + hh * 8;
@@ -569,8 +836,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<float2*>(a.rec_ml + (rec * a.rows + r) * 2) =
                             make_float2(m[hh], l[hh]);
                 }
-                const int4 rinfo = make_int4(s, h, kRecValid | (first ? kRecFirst : 0) |
-                                                       (last ? kRecLast : 0), 0);
+                const int4 rinfo = make_int4(
+                    s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0), 0);
                 if (slot == 0)
                     info0 = rinfo;
                 else
@@ -581,44 +848,119 @@ __global__ void __launch_bounds__(kThreads, 1)
         w.left -= j1 - w.j;
         if (w.left > 0) walk_next_unit<BS>(a, w);
     }
+}
+
+// ===================== kernel =====================
+template <int D, int BS, bool OUT_F32, bool NARROW>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_decode_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                             const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
+    using C = AttnCfg<D, BS, NARROW>;
+    constexpr int kStages = C::kStages;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t* stages = smem;
+    float* scratch = reinterpret_cast<float*>(smem + kStages * C::kStageBytes);
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes +
+                                                     C::kScratchBytes);
+    uint64_t* empty_bar = full_bar + kStages;
+
+    __shared__ long long s_red[kThreads / 32];
+    __shared__ long long s_start[2];
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int WM = NARROW ? 1 : a.warp_rows;
     if (tid == 0) {
-        a.rec_info[(size_t)cta * 2 + 0] = info0;
-        a.rec_info[(size_t)cta * 2 + 1] = info1;
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], WM);
+        }
+        fence_barrier_init();
+        s_abort = 0;
+        s_start[0] = -1;
+        s_start[1] = 0;
+    }
+    if (warp == kConsumerWarps && lane == 0) {
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
+    const Walk w0 = find_slice<BS>(a, s_red, s_start);  // also publishes the barrier init
+
+    if (warp == kConsumerWarps) {
+        produce<D, BS, kStages, C::kStageBytes, C::kTileBytes, C::kBoxBytes>(
+            a, &tmap_k, &tmap_v, w0, stages, full_bar, empty_bar, &s_abort);
+        return;
+    }
+
+    // Sequences with nothing resident produce zero rows (and are checked).
+    for (int s = blockIdx.x; s < a.num_seqs; s += gridDim.x) {
+        const int raw = __ldg(a.context_lens + s);
+        if (a.checked && tid == 0 &&
+            (raw < 0 || raw > a.max_blocks_per_seq * BS || (raw > 0 && raw < a.q_len)))
+            atomicOr(a.err, kErrBadContext);
+        if (unit_blocks(a, s, BS) == 0) {
+            const size_t n = (size_t)a.q_len * a.n_q * D;
+            const size_t o0 = (size_t)s * n;
+            for (size_t e = tid; e < n; e += kConsumerThreads) {
+                if (OUT_F32)
+                    static_cast<float*>(a.out)[o0 + e] = 0.f;
+                else
+                    static_cast<uint16_t*>(a.out)[o0 + e] = 0;
+            }
+        }
+    }
+
+    int4 info0 = make_int4(0, 0, 0, 0), info1 = make_int4(0, 0, 0, 0);
+    if (w0.left <= 0) info0.z = info1.z = kRecEmpty;
+    if (NARROW)
+        consume_narrow<D, BS, OUT_F32>(a, w0, stages, scratch, full_bar, empty_bar, &s_abort,
+                                       info0, info1);
+    else
+        consume_wide<D, BS, OUT_F32>(a, w0, stages, scratch, full_bar, empty_bar, &s_abort,
+                                     info0, info1);
+    if (tid == 0) {
+        a.rec_info[(size_t)blockIdx.x * 2 + 0] = info0;
+        a.rec_info[(size_t)blockIdx.x * 2 + 1] = info1;
     }
 }
 
 // ---------------------------------------------------------------------------
-int decode_attn_smem_bytes(int head_dim, int block_size) {
-    if (head_dim == 128 && block_size == 16) return AttnCfg<128, 16>::kSmemBytes;
-    if (head_dim == 128 && block_size == 32) return AttnCfg<128, 32>::kSmemBytes;
-    if (head_dim == 64 && block_size == 16) return AttnCfg<64, 16>::kSmemBytes;
-    if (head_dim == 64 && block_size == 32) return AttnCfg<64, 32>::kSmemBytes;
-    return -1;
-}
-
-template <int D, int BS, bool F32>
+template <int D, int BS, bool F32, bool NARROW>
 static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                               int grid, cudaStream_t stream) {
-    auto kern = paged_decode_attn_kernel<D, BS, F32>;
-    const int smem = AttnCfg<D, BS>::kSmemBytes;
+    auto kern = paged_decode_attn_kernel<D, BS, F32, NARROW>;
+    const int smem = AttnCfg<D, BS, NARROW>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, stream>>>(tk, tv, a);
     return cudaGetLastError();
 }
 
+template <int D, int BS>
+static cudaError_t launch_shape(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                bool out_f32, int grid, cudaStream_t stream) {
+    const bool narrow = a.rows <= kNarrowRows;
+    if (narrow)
+        return out_f32 ? launch_one<D, BS, true, true>(a, tk, tv, grid, stream)
+                       : launch_one<D, BS, false, true>(a, tk, tv, grid, stream);
+    return out_f32 ? launch_one<D, BS, true, false>(a, tk, tv, grid, stream)
+                   : launch_one<D, BS, false, false>(a, tk, tv, grid, stream);
+}
+
 cudaError_t launch_decode_attn(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                int head_dim, int block_size, bool out_f32, int grid,
                                cudaStream_t stream) {
-#define PKV_DISPATCH(D_, BS_)                                                         \
-    if (head_dim == D_ && block_size == BS_)                                          \
-        return out_f32 ? launch_one<D_, BS_, true>(a, tk, tv, grid, stream)           \
-                       : launch_one<D_, BS_, false>(a, tk, tv, grid, stream);
-    PKV_DISPATCH(128, 16)
-    PKV_DISPATCH(128, 32)
-    PKV_DISPATCH(64, 16)
-    PKV_DISPATCH(64, 32)
-#undef PKV_DISPATCH
+    if (head_dim == 128 && block_size == 16)
+        return launch_shape<128, 16>(a, tk, tv, out_f32, grid, stream);
+    if (head_dim == 128 && block_size == 32)
+        return launch_shape<128, 32>(a, tk, tv, out_f32, grid, stream);
+    if (head_dim == 64 && block_size == 16)
+        return launch_shape<64, 16>(a, tk, tv, out_f32, grid, stream);
+    if (head_dim == 64 && block_size == 32)
+        return launch_shape<64, 32>(a, tk, tv, out_f32, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -45,8 +45,6 @@ struct WorkspaceLayout {
 
 WorkspaceLayout workspace_layout(int grid, int rows, int head_dim);
 
-// Dynamic shared memory the attention kernel needs for (head_dim, block_size).
-int decode_attn_smem_bytes(int head_dim, int block_size);
 
 cudaError_t launch_decode_attn(const AttnArgs& a, const CUtensorMap& tmap_k,
                                const CUtensorMap& tmap_v, int head_dim, int block_size,

@@ -118,6 +118,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Transpose an 8x8 b16 matrix held one row-pair per lane (lane i: row i/4,
+// columns 2(i%4), 2(i%4)+1) into the same layout of its transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // ---------------------------------------------------------------- math
 // 2^x via the MUFU ex2 instruction (2^-inf = +0).
 __device__ __forceinline__ float fast_exp2(float x) {
