@@ -888,6 +888,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmap_v);
     }
     const Walk w0 = find_slice<BS>(a, s_red, s_start);  // also publishes the barrier init
+    // Let the merge kernel (launched as a programmatic dependent) be scheduled
+    // early; it waits for this whole grid before reading anything.
+    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == kConsumerWarps) {
         produce<D, BS, kStages, C::kStageBytes, C::kTileBytes, C::kBoxBytes>(

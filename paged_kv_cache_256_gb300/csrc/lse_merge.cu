@@ -9,24 +9,35 @@
 // in CS336 lecture-10 notes, PagedAttention (vLLM)).  Pieces with l == 0 (no
 // visible key) weigh nothing, and a row whose pieces are all empty is zero.
 //
-// Merge CTA c looks at the records of attention CTA c: if one of them starts
-// a split unit (the unit's first block, not its last), it walks forward over
-// CTAs c+1, c+2, ... whose first record continues that unit until the piece
-// holding the unit's last block, and writes the merged rows.  Every split
-// unit has exactly one starting piece, so each unit is merged exactly once.
+// Grid (attention CTAs) x (row groups of 8); one warp per output row.  Block
+// (c, y) looks at the records of attention CTA c: if one of them starts a
+// split unit (the unit's first block, not its last), its warps find the
+// CTAs c+1, c+2, ... holding the unit's other pieces with a lane-parallel
+// ballot over their records and combine rows 8y..8y+7.  Every split unit has
+// exactly one starting piece, so each unit is merged exactly once.  All loads
+// of one row are independent of each other, so a row costs a few memory
+// latencies whatever the number of pieces.
+//
+// The kernel is launched as a programmatic dependent of the attention kernel:
+// it may start while the attention grid drains and waits (griddepcontrol)
+// for the attention grid to finish before reading any record.
 #include "pkv_internal.h"
 #include "ptx.cuh"
 
 namespace pkv {
 
-constexpr int kMergeThreads = 128;
+constexpr int kMergeRowsPerBlock = 8;
+constexpr int kMergeThreads = kMergeRowsPerBlock * 32;
 
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(kMergeThreads)
     lse_merge_kernel(const AttnArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int V = D / 32;  // consecutive columns per lane
     const int c = blockIdx.x, grid = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.y * kMergeRowsPerBlock + warp;
+    if (r >= a.rows) return;
 
     const int4 i1 = a.rec_info[(size_t)c * 2 + 1];
     const int4 i0 = a.rec_info[(size_t)c * 2 + 0];
@@ -43,82 +54,134 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
     const int s = head.x, h = head.y;
 
-    // Find the CTA holding the unit's last piece.
-    int c_end = c;
-    bool closed = false;
-    for (int c2 = c + 1; c2 < grid; ++c2) {
-        const int4 in = a.rec_info[(size_t)c2 * 2];
-        if (in.z & kRecEmpty) continue;
-        if (!(in.z & kRecValid) || in.x != s || in.y != h) break;
-        c_end = c2;
-        if (in.z & kRecLast) {
-            closed = true;
-            break;
+    // Pieces: first_rec, then the first record of every non-empty CTA in
+    // (c, c_end].  Find c_end 32 CTAs at a time.
+    int c_end = -1;
+    for (int base = c + 1; base < grid && c_end < 0; base += 32) {
+        const int c2 = base + lane;
+        int4 in = make_int4(0, 0, 0, 0);
+        if (c2 < grid) in = a.rec_info[(size_t)c2 * 2];
+        const bool same = c2 < grid && (in.z & kRecValid) && in.x == s && in.y == h;
+        const bool cont = same || (c2 < grid && (in.z & kRecEmpty));
+        const unsigned ends = __ballot_sync(0xffffffffu, (same && (in.z & kRecLast)) || !cont);
+        if (ends) {
+            const int k = __ffs(ends) - 1;
+            const bool closed = __shfl_sync(0xffffffffu, same && (in.z & kRecLast), k);
+            if (!closed) {
+                if (lane == 0) atomicOr(a.err, kErrInternal);
+                return;
+            }
+            c_end = base + k;
         }
     }
-    if (!closed) {
-        if (threadIdx.x == 0) atomicOr(a.err, kErrInternal);
+    if (c_end < 0) {
+        if (lane == 0) atomicOr(a.err, kErrInternal);
         return;
     }
 
-    const int G = a.group;
-    for (int r = warp; r < a.rows; r += kMergeThreads / 32) {
-        // pass 1: the largest running max among non-empty pieces
-        float M = -INFINITY;
-        for (int c2 = c; c2 <= c_end; ++c2) {
-            const int rec = c2 == c ? first_rec : c2 * 2;
-            if (c2 != c && (a.rec_info[(size_t)c2 * 2].z & kRecEmpty)) continue;
-            const float2 ml = *reinterpret_cast<const float2*>(a.rec_ml + ((size_t)rec * a.rows + r) * 2);
-            if (ml.y > 0.f) M = fmaxf(M, ml.x);
-        }
-        const float mb = M == -INFINITY ? 0.f : M;
-        // pass 2: weighted sums
-        float acc[V];
-#pragma unroll
-        for (int v = 0; v < V; ++v) acc[v] = 0.f;
-        float den = 0.f;
-        for (int c2 = c; c2 <= c_end; ++c2) {
-            const int rec = c2 == c ? first_rec : c2 * 2;
-            if (c2 != c && (a.rec_info[(size_t)c2 * 2].z & kRecEmpty)) continue;
-            const float2 ml = *reinterpret_cast<const float2*>(a.rec_ml + ((size_t)rec * a.rows + r) * 2);
-            if (!(ml.y > 0.f)) continue;
-            const float wgt = fast_exp2(ml.x - mb);
-            den += wgt * ml.y;
-            const float* ro = a.rec_o + ((size_t)rec * a.rows + r) * D + lane * V;
-#pragma unroll
-            for (int v = 0; v < V; ++v) acc[v] += wgt * ro[v];
-        }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        const int i = r / G, hq = h * G + r % G;
-        const size_t ob = (((size_t)s * a.q_len + i) * a.n_q + hq) * D + lane * V;
-        if (OUT_F32) {
-            float* op = static_cast<float*>(a.out) + ob;
-#pragma unroll
-            for (int v = 0; v < V; ++v) op[v] = acc[v] * inv;
-        } else {
-            uint32_t* op = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + ob);
-#pragma unroll
-            for (int v = 0; v < V; v += 2) op[v / 2] = pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
+    // Pass 1 (lane k <-> piece k of each group of 32): largest running max and
+    // the weighted denominator.
+    const int npieces = c_end - c + 1;  // candidate slots; empty CTAs weigh 0
+    float M = -INFINITY;
+    for (int k0 = 0; k0 < npieces; k0 += 32) {
+        const int k = k0 + lane;
+        if (k < npieces) {
+            const int rec = k == 0 ? first_rec : (c + k) * 2;
+            const bool live = k == 0 || !(a.rec_info[(size_t)(c + k) * 2].z & kRecEmpty);
+            if (live) {
+                const float2 ml = *reinterpret_cast<const float2*>(a.rec_ml + ((size_t)rec * a.rows + r) * 2);
+                if (ml.y > 0.f) M = fmaxf(M, ml.x);
+            }
         }
     }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float mb = M == -INFINITY ? 0.f : M;
+
+    float acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    float den = 0.f;
+    for (int k0 = 0; k0 < npieces; k0 += 32) {
+        const int k = k0 + lane;
+        float wk = 0.f, lk = 0.f;
+        if (k < npieces) {
+            const int rec = k == 0 ? first_rec : (c + k) * 2;
+            const bool live = k == 0 || !(a.rec_info[(size_t)(c + k) * 2].z & kRecEmpty);
+            if (live) {
+                const float2 ml = *reinterpret_cast<const float2*>(a.rec_ml + ((size_t)rec * a.rows + r) * 2);
+                if (ml.y > 0.f) {
+                    wk = fast_exp2(ml.x - mb);
+                    lk = ml.y;
+                }
+            }
+        }
+        float dpart = wk * lk;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) dpart += __shfl_xor_sync(0xffffffffu, dpart, off);
+        den += dpart;
+        // Pass 2: every lane accumulates its V columns over the group's pieces.
+        const int cnt = min(32, npieces - k0);
+        for (int q = 0; q < cnt; ++q) {
+            const float wq = __shfl_sync(0xffffffffu, wk, q);
+            if (wq == 0.f) continue;  // uniform across the warp
+            const int kq = k0 + q;
+            const int rec = kq == 0 ? first_rec : (c + kq) * 2;
+            const float* ro = a.rec_o + ((size_t)rec * a.rows + r) * D + lane * V;
+            if (V == 4) {
+                const float4 x = *reinterpret_cast<const float4*>(ro);
+                acc[0] += wq * x.x;
+                acc[1] += wq * x.y;
+                acc[2] += wq * x.z;
+                acc[3] += wq * x.w;
+            } else {
+#pragma unroll
+                for (int v = 0; v < V; ++v) acc[v] += wq * ro[v];
+            }
+        }
+    }
+
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const int G = a.group;
+    const int i = r / G, hq = h * G + r % G;
+    const size_t ob = (((size_t)s * a.q_len + i) * a.n_q + hq) * D + lane * V;
+    if (OUT_F32) {
+        float* op = static_cast<float*>(a.out) + ob;
+#pragma unroll
+        for (int v = 0; v < V; ++v) op[v] = acc[v] * inv;
+    } else {
+        uint32_t* op = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + ob);
+#pragma unroll
+        for (int v = 0; v < V; v += 2) op[v / 2] = pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
+    }
+}
+
+template <int D, bool F32>
+static cudaError_t launch_merge_one(const AttnArgs& a, int grid, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, (a.rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock, 1);
+    cfg.blockDim = dim3(kMergeThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, lse_merge_kernel<D, F32>, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_lse_merge(const AttnArgs& a, int head_dim, bool out_f32, int grid,
                              cudaStream_t stream) {
-    if (head_dim == 128) {
-        if (out_f32)
-            lse_merge_kernel<128, true><<<grid, kMergeThreads, 0, stream>>>(a);
-        else
-            lse_merge_kernel<128, false><<<grid, kMergeThreads, 0, stream>>>(a);
-    } else if (head_dim == 64) {
-        if (out_f32)
-            lse_merge_kernel<64, true><<<grid, kMergeThreads, 0, stream>>>(a);
-        else
-            lse_merge_kernel<64, false><<<grid, kMergeThreads, 0, stream>>>(a);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    if (head_dim == 128)
+        return out_f32 ? launch_merge_one<128, true>(a, grid, stream)
+                       : launch_merge_one<128, false>(a, grid, stream);
+    if (head_dim == 64)
+        return out_f32 ? launch_merge_one<64, true>(a, grid, stream)
+                       : launch_merge_one<64, false>(a, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv
