@@ -597,8 +597,7 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
     constexpr int kStages = C::kStages;
     constexpr int NT = D / 8;    // 8-wide output column tiles
     constexpr int KT = D / 16;   // 16-deep k steps over head_dim
-    constexpr int ST = BS / 8;   // 8-token score tiles per block
-    constexpr int PT = BS / 16;  // 16-token k steps of the PV product
+    constexpr int PT = BS / 16;  // 16-token chunks per block
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int WM = a.warp_rows;
     const int WN = kConsumerWarps / WM;
@@ -650,93 +649,87 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                 const uint32_t kbase = smem_addr(stages + stage * C::kStageBytes);
                 const uint32_t vbase = kbase + C::kTileBytes;
 
-                // ---- S = Q K^T over this block's BS tokens
-                float sc[ST][4];
+                // The block is taken 16 tokens at a time (one online-softmax
+                // update per chunk), which keeps the live registers low.
+#pragma unroll 1
+                for (int tp = 0; tp < PT; ++tp) {
+                    // ---- S = Q K^T over 16 tokens
+                    float sc[2][4];
 #pragma unroll
-                for (int n = 0; n < ST; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+                    for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
-                for (int kk = 0; kk < KT; ++kk) {
-#pragma unroll
-                    for (int tp = 0; tp < PT; ++tp) {
+                    for (int kk = 0; kk < KT; ++kk) {
                         uint32_t b[4];
                         ldmatrix_x4(b, kbase + swz<BS>(tp * 16 + (mi >> 1) * 8 + rr,
                                                         kk * 16 + (mi & 1) * 8));
-                        mma_bf16_16816(sc[2 * tp], qf[kk], b[0], b[1]);
-                        mma_bf16_16816(sc[2 * tp + 1], qf[kk], b[2], b[3]);
+                        mma_bf16_16816(sc[0], qf[kk], b[0], b[1]);
+                        mma_bf16_16816(sc[1], qf[kk], b[2], b[3]);
                     }
-                }
 
-                // ---- scale, causal / tail mask, online softmax (base 2)
-                const int tok0 = j * BS;
-                const bool need_mask = tok0 + BS - 1 > lim_min;
-                float mloc[2] = {-INFINITY, -INFINITY};
+                    // ---- scale, causal / tail mask, online softmax (base 2)
+                    const int tok0 = j * BS + tp * 16;
+                    const bool need_mask = tok0 + 15 > lim_min;
+                    float mloc[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                for (int n = 0; n < ST; ++n) {
+                    for (int n = 0; n < 2; ++n) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float x = sc[n][e] * a.scale_log2;
-                        if (need_mask && tok0 + n * 8 + 2 * t + (e & 1) > lim[e >> 1])
-                            x = -INFINITY;
-                        sc[n][e] = x;
-                        mloc[e >> 1] = fmaxf(mloc[e >> 1], x);
+                        for (int e = 0; e < 4; ++e) {
+                            float x = sc[n][e] * a.scale_log2;
+                            if (need_mask && tok0 + n * 8 + 2 * t + (e & 1) > lim[e >> 1])
+                                x = -INFINITY;
+                            sc[n][e] = x;
+                            mloc[e >> 1] = fmaxf(mloc[e >> 1], x);
+                        }
                     }
-                }
-                float alpha[2], mbase[2];
+                    float alpha[2], mbase[2];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    mloc[hh] = fmaxf(mloc[hh], __shfl_xor_sync(0xffffffffu, mloc[hh], 1));
-                    mloc[hh] = fmaxf(mloc[hh], __shfl_xor_sync(0xffffffffu, mloc[hh], 2));
-                    const float mnew = fmaxf(m[hh], mloc[hh]);
-                    mbase[hh] = mnew == -INFINITY ? 0.f : mnew;
-                    alpha[hh] = fast_exp2(m[hh] - mbase[hh]);
-                    m[hh] = mnew;
-                }
-                float rsum[2] = {0.f, 0.f};
-#pragma unroll
-                for (int n = 0; n < ST; ++n) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p = fast_exp2(sc[n][e] - mbase[e >> 1]);
-                        sc[n][e] = p;
-                        rsum[e >> 1] += p;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        mloc[hh] = fmaxf(mloc[hh], __shfl_xor_sync(0xffffffffu, mloc[hh], 1));
+                        mloc[hh] = fmaxf(mloc[hh], __shfl_xor_sync(0xffffffffu, mloc[hh], 2));
+                        const float mnew = fmaxf(m[hh], mloc[hh]);
+                        mbase[hh] = mnew == -INFINITY ? 0.f : mnew;
+                        alpha[hh] = fast_exp2(m[hh] - mbase[hh]);
+                        m[hh] = mnew;
                     }
-                }
+                    float rsum[2] = {0.f, 0.f};
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) l[hh] = l[hh] * alpha[hh] + rsum[hh];
-                if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
+                    for (int n = 0; n < 2; ++n) {
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        o[n][0] *= alpha[0];
-                        o[n][1] *= alpha[0];
-                        o[n][2] *= alpha[1];
-                        o[n][3] *= alpha[1];
+                        for (int e = 0; e < 4; ++e) {
+                            const float p = fast_exp2(sc[n][e] - mbase[e >> 1]);
+                            sc[n][e] = p;
+                            rsum[e >> 1] += p;
+                        }
                     }
-                }
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) l[hh] = l[hh] * alpha[hh] + rsum[hh];
+                    if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
+#pragma unroll
+                        for (int n = 0; n < NT; ++n) {
+                            o[n][0] *= alpha[0];
+                            o[n][1] *= alpha[0];
+                            o[n][2] *= alpha[1];
+                            o[n][3] *= alpha[1];
+                        }
+                    }
 
-                // ---- P as bf16 A fragments (fp32 output: hi + lo pair)
-                uint32_t pa[PT][4];
-                uint32_t pl[PT][4];
-#pragma unroll
-                for (int tp = 0; tp < PT; ++tp) {
+                    // ---- P as bf16 A fragments (fp32 output: hi + lo pair)
+                    uint32_t pa[4], pl[4];
 #pragma unroll
                     for (int q2 = 0; q2 < 4; ++q2) {
-                        const int n = 2 * tp + (q2 >> 1);
+                        const int n = q2 >> 1;
                         const int e = (q2 & 1) * 2;
                         const float p0 = sc[n][e], p1 = sc[n][e + 1];
-                        pa[tp][q2] = pack_bf16x2(p0, p1);
+                        pa[q2] = pack_bf16x2(p0, p1);
                         if (OUT_F32)
-                            pl[tp][q2] = pack_bf16x2(p0 - bf16_lo_to_f32(pa[tp][q2]),
-                                                     p1 - bf16_hi_to_f32(pa[tp][q2]));
+                            pl[q2] = pack_bf16x2(p0 - bf16_lo_to_f32(pa[q2]),
+                                                 p1 - bf16_hi_to_f32(pa[q2]));
                     }
-                }
 
-                // ---- O += P V (V rows past the context are zeroed: they may hold NaN)
-                const bool need_vmask = tok0 + BS > ctx;
-#pragma unroll
-                for (int tp = 0; tp < PT; ++tp) {
+                    // ---- O += P V (V rows past the context are zeroed: they may hold NaN)
                     uint32_t vm0 = 0xFFFFFFFFu, vm8 = 0xFFFFFFFFu;
-                    if (need_vmask) {
-                        const int ta = tok0 + tp * 16 + 2 * t;
+                    if (tok0 + 16 > ctx) {
+                        const int ta = tok0 + 2 * t;
                         vm0 = (ta < ctx ? 0x0000FFFFu : 0u) | (ta + 1 < ctx ? 0xFFFF0000u : 0u);
                         vm8 = (ta + 8 < ctx ? 0x0000FFFFu : 0u) | (ta + 9 < ctx ? 0xFFFF0000u : 0u);
                     }
@@ -749,11 +742,11 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                         b[1] &= vm8;
                         b[2] &= vm0;
                         b[3] &= vm8;
-                        mma_bf16_16816(o[2 * dp], pa[tp], b[0], b[1]);
-                        mma_bf16_16816(o[2 * dp + 1], pa[tp], b[2], b[3]);
+                        mma_bf16_16816(o[2 * dp], pa, b[0], b[1]);
+                        mma_bf16_16816(o[2 * dp + 1], pa, b[2], b[3]);
                         if (OUT_F32) {
-                            mma_bf16_16816(o[2 * dp], pl[tp], b[0], b[1]);
-                            mma_bf16_16816(o[2 * dp + 1], pl[tp], b[2], b[3]);
+                            mma_bf16_16816(o[2 * dp], pl, b[0], b[1]);
+                            mma_bf16_16816(o[2 * dp + 1], pl, b[2], b[3]);
                         }
                     }
                 }
