@@ -44,6 +44,7 @@
 
 #include "pkv_internal.h"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
@@ -53,34 +54,46 @@ constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kMergeSlots = 4;                   // warps that park a partial per merge round
 constexpr int kIssueLanes = 4;                   // producer lanes issuing loads side by side
 constexpr int kNarrowRows = 8;                   // rows up to which the narrow consumer is used
+constexpr int kTmemMinRows = 64;                 // rows above which the TMEM consumer is used
 
-template <int D, int BS, bool NARROW>
+// Consumer modes, chosen by the number of query rows sharing a KV head.
+constexpr int kModeWide = 0;    // 8 < rows <= 64: mma.sync, rows on the M side
+constexpr int kModeNarrow = 1;  // rows <= 8: mma.sync, tokens on the M side
+constexpr int kModeTmem = 2;    // rows > 64: tcgen05, 128-row tiles, accumulators in TMEM
+
+template <int D, int BS, int MODE>
 struct AttnCfg {
     static constexpr int kTileBytes = BS * D * 2;  // one K (or V) tile of one (block, head)
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kBoxBytes = BS * 128;  // one 64-column swizzled box
     // Per-lane floats a warp parks for a merge round: its accumulator, m[2], l[2].
-    static constexpr int kLaneFloats = (NARROW ? D / 4 : D / 2) + 4;
-    static constexpr int kMergeBytes = kMergeSlots * 32 * kLaneFloats * 4;
+    static constexpr int kLaneFloats = (MODE == kModeNarrow ? D / 4 : D / 2) + 4;
+    static constexpr int kMergeBytes = MODE == kModeTmem ? 0 : kMergeSlots * 32 * kLaneFloats * 4;
     // Narrow emit: rows x head_dim fp32 tile (+4 floats of row padding) and (m, l) per row.
     static constexpr int kTileStride = D + 4;
-    static constexpr int kEmitBytes = NARROW ? (kNarrowRows * kTileStride + 2 * kNarrowRows) * 4 : 0;
-    static constexpr int kScratchBytes = kMergeBytes + kEmitBytes;
+    static constexpr int kEmitBytes =
+        MODE == kModeNarrow ? (kNarrowRows * kTileStride + 2 * kNarrowRows) * 4 : 0;
+    // TMEM mode: the unit's 128 query rows as a swizzled K-major tile.
+    static constexpr int kQTileBytes = MODE == kModeTmem ? 128 * D * 2 : 0;
+    static constexpr int kScratchBytes = kMergeBytes + kEmitBytes + kQTileBytes;
     static constexpr int kBarrierBytes = 2 * 32 * 8;
     static constexpr int kBudget = 227 * 1024 - 1024 - kScratchBytes - kBarrierBytes - 1024;
-    // The ring depth is a multiple of the consumer-warp count: block g and
-    // block g - kStages then belong to the same warp, so when a warp waits for
-    // round r of a stage it has itself already seen round r - 1 complete.
-    // (mbarrier parity waits cannot tell round r from round r - 2; with
-    // another warp owning round r - 1 a still-in-flight load would read as
-    // complete.)
+    // In the mma.sync modes the ring depth is a multiple of the consumer-warp
+    // count: block g and block g - kStages then belong to the same warp, so
+    // when a warp waits for round r of a stage it has itself already seen
+    // round r - 1 complete.  (mbarrier parity waits cannot tell round r from
+    // round r - 2; with another warp owning round r - 1 a still-in-flight load
+    // would read as complete.)  The TMEM mode has a single consumer thread.
     static constexpr int kStagesRaw = kBudget / kStageBytes;
-    static constexpr int kStages = kStagesRaw >= 32 ? 32 : (kStagesRaw / 8) * 8;
+    static constexpr int kStages =
+        kStagesRaw >= 32 ? 32 : (MODE == kModeTmem ? kStagesRaw : (kStagesRaw / 8) * 8);
     static constexpr int kSmemBytes =
         1024 + kStages * kStageBytes + kScratchBytes + 2 * kStages * 8;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BS == 16 || BS == 32, "block_size");
-    static_assert(kStages % kConsumerWarps == 0 && kStages >= kConsumerWarps, "ring depth");
+    static_assert(MODE == kModeTmem ? kStages >= 2
+                                    : (kStages % kConsumerWarps == 0 && kStages >= kConsumerWarps),
+                  "ring depth");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -313,7 +326,7 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                                                float* scratch, uint64_t* full_bar,
                                                uint64_t* empty_bar, volatile int* s_abort,
                                                int4& info0, int4& info1) {
-    using C = AttnCfg<D, BS, true>;
+    using C = AttnCfg<D, BS, kModeNarrow>;
     constexpr int kStages = C::kStages;
     constexpr int MT = D / 16;   // 16-wide head_dim tiles (M of the PV product)
     constexpr int KT = D / 16;   // 16-deep k steps of the score product
@@ -593,7 +606,7 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                                              float* scratch, uint64_t* full_bar,
                                              uint64_t* empty_bar, volatile int* s_abort,
                                              int4& info0, int4& info1) {
-    using C = AttnCfg<D, BS, false>;
+    using C = AttnCfg<D, BS, kModeWide>;
     constexpr int kStages = C::kStages;
     constexpr int NT = D / 8;    // 8-wide output column tiles
     constexpr int KT = D / 16;   // 16-deep k steps over head_dim
@@ -843,12 +856,299 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
     }
 }
 
+// ===================== TMEM consumer (rows > 64) =====================
+// One 128-row tile per unit (rows >= R are zero).  Warp 4 lane 0 issues the
+// tensor-core work; warps 0..3 run the softmax, one thread per row (TMEM lane
+// = row, so a row's max and sum never leave the thread).  Per block g:
+//   issuer : S[g&1] = Q K_g^T      (tcgen05.mma, A = Q tile, B = K stage, K-major)
+//   softmax: P[g&1] = 2^(S*scale - m) as bf16 in TMEM, running sum l; O is
+//            rescaled in TMEM only when a row's max grew by more than 2^8 (the
+//            stale max is used consistently in P and l, so the result is exact)
+//   issuer : O += P[g&1] V_g        (A from TMEM, B = V stage, MN-major)
+// The issuer runs one block ahead (QK of g+1 before PV of g), so scores of the
+// next block are computed while the softmax works on this one.
+template <int D, int BS, bool OUT_F32>
+__device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t* stages,
+                                             uint8_t* qtile, uint64_t* full_bar,
+                                             uint64_t* empty_bar, uint64_t* tcb,
+                                             uint32_t* s_tmem, volatile int* s_abort,
+                                             int4& info0, int4& info1) {
+    using C = AttnCfg<D, BS, kModeTmem>;
+    constexpr int kStages = C::kStages;
+    constexpr uint32_t kTmemCols = 256;
+    constexpr uint32_t kColO = 0, kColS = 128, kColP = 192, kColPL = 224;
+    constexpr int KT = D / 16;   // k steps of S = Q K^T
+    constexpr int PK = BS / 16;  // k steps of O += P V
+    constexpr int kQHalf = 128 * 128;  // bytes of one 64-column half of the Q tile
+    // tcb: [0..1] S ready, [2..3] P ready, [4] PV done, [5] teardown
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp > 4) return;  // warps 5..7 have no part in this mode
+    const bool softmax = warp < 4;
+    const int row = threadIdx.x;  // softmax threads: row = TMEM lane
+    const int R = a.rows, G = a.group, cta = blockIdx.x;
+
+    if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
+    tc_fence_before();
+    named_barrier_sync(2, 160);
+    tc_fence_after();
+    const uint32_t tbase = *s_tmem;
+    const uint32_t tlane = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t idesc_qk = umma_idesc_bf16(128, BS, false);
+    const uint32_t idesc_pv = umma_idesc_bf16(128, D, true);
+    const uint32_t q_saddr = smem_addr(qtile);
+
+    uint32_t gbase = 0;
+    bool ok = true;
+    int piece = 0;
+    while (w.left > 0) {
+        const int j0 = w.j, j1 = piece_end(w), n = j1 - j0;
+        const int ctx = w.ctx, s = w.s, h = w.h;
+        int lim = -1, i_row = 0, hq_row = 0;
+        if (softmax) {
+            // This unit's query rows into the swizzled Q tile (the previous
+            // unit's MMAs finished: every S of it was waited for).
+            const bool valid = row < R;
+            i_row = valid ? row / G : 0;
+            hq_row = h * G + (valid ? row % G : 0);
+            lim = valid ? ctx - a.q_len + i_row : -1;
+            const uint4* qrow = reinterpret_cast<const uint4*>(
+                a.q + (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + row * 128 +
+                                          (((c & 7) ^ (row & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        named_barrier_sync(2, 160);  // Q tile ready; the previous unit's O has been read
+        tc_fence_after();
+
+        if (warp == 4) {
+            // ===================== issuer =====================
+            if (lane == 0 && ok) {
+                for (int b = 0; b <= n; ++b) {
+                    if (b < n) {
+                        const uint32_t g = gbase + b, st = g % kStages;
+                        if (*s_abort || !mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u)) {
+                            ok = false;
+                            atomicOr(a.err, kErrTimeout);
+                            *s_abort = 1;
+                            break;
+                        }
+                        const uint32_t kb = smem_addr(stages + st * C::kStageBytes);
+                        const uint32_t scol = tbase + kColS + (g & 1u) * BS;
+#pragma unroll
+                        for (int kk = 0; kk < KT; ++kk) {
+                            const uint64_t ad =
+                                umma_smem_desc(q_saddr + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd = umma_smem_desc(
+                                kb + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
+                            umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&tcb[g & 1u]);
+                    }
+                    if (b > 0) {
+                        const uint32_t g = gbase + b - 1, st = g % kStages;
+                        if (*s_abort || !mbar_wait_bounded(&tcb[2 + (g & 1u)], (g >> 1) & 1u)) {
+                            ok = false;
+                            atomicOr(a.err, kErrTimeout);
+                            *s_abort = 1;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t vb = smem_addr(stages + st * C::kStageBytes) + C::kTileBytes;
+                        const uint32_t pcol = tbase + kColP + (g & 1u) * (BS / 2);
+#pragma unroll
+                        for (int kk = 0; kk < PK; ++kk) {
+                            const uint64_t bd = umma_smem_desc(vb + kk * 16 * 128, C::kBoxBytes, 1024);
+                            umma_ts(tbase + kColO, pcol + kk * 8, bd, idesc_pv,
+                                    (b > 1 || kk > 0) ? 1u : 0u);
+                            if (OUT_F32)
+                                umma_ts(tbase + kColO, tbase + kColPL + (g & 1u) * (BS / 2) + kk * 8,
+                                        bd, idesc_pv, 1u);
+                        }
+                        umma_commit(&empty_bar[st]);  // K and V of this stage are consumed
+                        umma_commit(&tcb[4]);         // PV of block g done
+                    }
+                }
+            }
+            __syncwarp();
+        } else {
+            // ===================== softmax (thread = row) =====================
+            float m_used = -INFINITY, l = 0.f;
+            const int lim_min = ctx - a.q_len;
+            for (int b = 0; b < n; ++b) {
+                const uint32_t g = gbase + b;
+                ok = consumer_wait(a, &tcb[g & 1u], (g >> 1) & 1u, ok, s_abort);
+                if (!ok) continue;
+                tc_fence_after();
+                float x[BS];
+                {
+                    uint32_t sr[BS];
+                    if constexpr (BS == 32)
+                        tmem_ld32(tlane + kColS + (g & 1u) * BS, sr);
+                    else
+                        tmem_ld16(tlane + kColS + (g & 1u) * BS, sr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < BS; ++c) x[c] = __uint_as_float(sr[c]) * a.scale_log2;
+                }
+                const int tok0 = (j0 + b) * BS;
+                float mloc = -INFINITY;
+                if (tok0 + BS - 1 > lim_min) {
+#pragma unroll
+                    for (int c = 0; c < BS; ++c)
+                        if (tok0 + c > lim) x[c] = -INFINITY;
+                }
+#pragma unroll
+                for (int c = 0; c < BS; ++c) mloc = fmaxf(mloc, x[c]);
+                // PV of the previous block must be done before O is rescaled
+                // or its P buffer (read by PV two blocks back) is rewritten.
+                if (b > 0) {
+                    ok = consumer_wait(a, &tcb[4], (g - 1) & 1u, ok, s_abort);
+                    if (!ok) continue;
+                    tc_fence_after();
+                }
+                const bool grow = mloc > m_used + 8.f;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float m_new = grow ? mloc : m_used;
+                    const float alpha = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
+                    l *= alpha;
+                    if (b > 0) {
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t ov[32];
+                            tmem_ld32(tlane + kColO + c0, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 32; ++c)
+                                ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+                            tmem_st32(tlane + kColO + c0, ov);
+                        }
+                        tmem_wait_st();
+                    }
+                    m_used = m_new;
+                }
+                uint32_t ph[BS / 2], pl[BS / 2];
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < BS; c += 2) {
+                    const float p0 = m_used == -INFINITY ? 0.f : fast_exp2(x[c] - m_used);
+                    const float p1 = m_used == -INFINITY ? 0.f : fast_exp2(x[c + 1] - m_used);
+                    rs += p0 + p1;
+                    ph[c / 2] = pack_bf16x2(p0, p1);
+                    if (OUT_F32)
+                        pl[c / 2] = pack_bf16x2(p0 - bf16_lo_to_f32(ph[c / 2]),
+                                                p1 - bf16_hi_to_f32(ph[c / 2]));
+                }
+                l += rs;
+                if constexpr (BS == 32) {
+                    tmem_st16(tlane + kColP + (g & 1u) * (BS / 2), ph);
+                    if (OUT_F32) tmem_st16(tlane + kColPL + (g & 1u) * (BS / 2), pl);
+                } else {
+                    tmem_st8(tlane + kColP + (g & 1u) * (BS / 2), ph);
+                    if (OUT_F32) tmem_st8(tlane + kColPL + (g & 1u) * (BS / 2), pl);
+                }
+                tmem_wait_st();
+                // V rows past the context may hold NaN; 0 * NaN would poison O.
+                if (tok0 + BS > ctx) {
+                    uint8_t* vt = stages + (g % kStages) * C::kStageBytes + C::kTileBytes;
+                    const int valid = ctx - tok0;  // >= 1: the block holds a resident token
+                    const int chunks = (BS - valid) * 8;  // 16-byte chunks per 64-column half
+                    for (int q = row; q < chunks * (D / 64); q += 128) {
+                        const int half = q / chunks, rq = q % chunks;
+                        *reinterpret_cast<uint4*>(vt + half * C::kBoxBytes + valid * 128 + rq * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                mbar_arrive(&tcb[2 + (g & 1u)]);
+            }
+
+            // ---- epilogue: the last PV, then O out of TMEM row by row
+            if (n > 0) ok = consumer_wait(a, &tcb[4], (gbase + n - 1) & 1u, ok, s_abort);
+            tc_fence_after();
+            const bool first_piece = j0 == 0, last_piece = j1 == w.nb;
+            const bool whole = first_piece && last_piece;
+            if (ok) {
+                const float scl = whole ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
+                const size_t rec = (size_t)cta * 2 + (piece == 0 ? 0 : 1);
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(tlane + kColO + c0, ov);
+                    tmem_wait_ld();
+                    if (row < R) {
+                        if (whole) {
+                            const size_t ob =
+                                (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D + c0;
+                            if (OUT_F32) {
+                                float4* op = reinterpret_cast<float4*>(static_cast<float*>(a.out) + ob);
+#pragma unroll
+                                for (int c = 0; c < 32; c += 4)
+                                    op[c / 4] = make_float4(__uint_as_float(ov[c]) * scl,
+                                                            __uint_as_float(ov[c + 1]) * scl,
+                                                            __uint_as_float(ov[c + 2]) * scl,
+                                                            __uint_as_float(ov[c + 3]) * scl);
+                            } else {
+                                uint4* op = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ob);
+#pragma unroll
+                                for (int c = 0; c < 32; c += 8)
+                                    op[c / 8] = make_uint4(
+                                        pack_bf16x2(__uint_as_float(ov[c]) * scl, __uint_as_float(ov[c + 1]) * scl),
+                                        pack_bf16x2(__uint_as_float(ov[c + 2]) * scl, __uint_as_float(ov[c + 3]) * scl),
+                                        pack_bf16x2(__uint_as_float(ov[c + 4]) * scl, __uint_as_float(ov[c + 5]) * scl),
+                                        pack_bf16x2(__uint_as_float(ov[c + 6]) * scl, __uint_as_float(ov[c + 7]) * scl));
+                            }
+                        } else {
+                            float4* op = reinterpret_cast<float4*>(a.rec_o + (rec * R + row) * D + c0);
+#pragma unroll
+                            for (int c = 0; c < 32; c += 4)
+                                op[c / 4] = make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]),
+                                                        __uint_as_float(ov[c + 2]), __uint_as_float(ov[c + 3]));
+                        }
+                    }
+                }
+                if (!whole) {
+                    if (row < R)
+                        *reinterpret_cast<float2*>(a.rec_ml + (rec * R + row) * 2) = make_float2(m_used, l);
+                    if (row == 0) {
+                        const int4 rinfo = make_int4(
+                            s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0), 0);
+                        if (piece == 0)
+                            info0 = rinfo;
+                        else
+                            info1 = rinfo;
+                    }
+                }
+            }
+            tc_fence_before();
+        }
+        gbase += n;
+        ++piece;
+        w.left -= j1 - w.j;
+        if (w.left > 0) walk_next_unit<BS>(a, w);
+    }
+    // Teardown: no tensor-core operation may still be running when TMEM is freed.
+    if (warp == 4 && lane == 0) {
+        umma_commit(&tcb[5]);
+        (void)mbar_wait_bounded(&tcb[5], 0u);
+    }
+    tc_fence_before();
+    named_barrier_sync(2, 160);
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+}
+
 // ===================== kernel =====================
-template <int D, int BS, bool OUT_F32, bool NARROW>
+template <int D, int BS, bool OUT_F32, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_decode_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
-    using C = AttnCfg<D, BS, NARROW>;
+    using C = AttnCfg<D, BS, MODE>;
     constexpr int kStages = C::kStages;
 
     extern __shared__ uint8_t smem_raw[];
@@ -863,13 +1163,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ long long s_red[kThreads / 32];
     __shared__ long long s_start[2];
     __shared__ int s_abort;
+    __shared__ uint64_t s_tcb[6];  // TMEM mode: S ready x2, P ready x2, PV done, teardown
+    __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int WM = NARROW ? 1 : a.warp_rows;
+    // Arrivals that release a stage: one per 16-row slice (wide), one warp
+    // (narrow), one tensor-core commit (TMEM mode).
+    const int releases = MODE == kModeWide ? a.warp_rows : 1;
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], WM);
+            mbar_init(&empty_bar[i], releases);
+        }
+        if (MODE == kModeTmem) {
+            mbar_init(&s_tcb[0], 1);
+            mbar_init(&s_tcb[1], 1);
+            mbar_init(&s_tcb[2], 128);
+            mbar_init(&s_tcb[3], 128);
+            mbar_init(&s_tcb[4], 1);
+            mbar_init(&s_tcb[5], 1);
         }
         fence_barrier_init();
         s_abort = 0;
@@ -911,12 +1223,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int4 info0 = make_int4(0, 0, 0, 0), info1 = make_int4(0, 0, 0, 0);
     if (w0.left <= 0) info0.z = info1.z = kRecEmpty;
-    if (NARROW)
+    if (MODE == kModeNarrow)
         consume_narrow<D, BS, OUT_F32>(a, w0, stages, scratch, full_bar, empty_bar, &s_abort,
                                        info0, info1);
-    else
+    else if (MODE == kModeWide)
         consume_wide<D, BS, OUT_F32>(a, w0, stages, scratch, full_bar, empty_bar, &s_abort,
                                      info0, info1);
+    else
+        consume_tmem<D, BS, OUT_F32>(a, w0, stages, reinterpret_cast<uint8_t*>(scratch), full_bar,
+                                     empty_bar, s_tcb, &s_tmem, &s_abort, info0, info1);
     if (tid == 0) {
         a.rec_info[(size_t)blockIdx.x * 2 + 0] = info0;
         a.rec_info[(size_t)blockIdx.x * 2 + 1] = info1;
@@ -924,11 +1239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int D, int BS, bool F32, bool NARROW>
+template <int D, int BS, bool F32, int MODE>
 static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                               int grid, cudaStream_t stream) {
-    auto kern = paged_decode_attn_kernel<D, BS, F32, NARROW>;
-    const int smem = AttnCfg<D, BS, NARROW>::kSmemBytes;
+    auto kern = paged_decode_attn_kernel<D, BS, F32, MODE>;
+    const int smem = AttnCfg<D, BS, MODE>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, stream>>>(tk, tv, a);
@@ -938,12 +1253,14 @@ static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CU
 template <int D, int BS>
 static cudaError_t launch_shape(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                 bool out_f32, int grid, cudaStream_t stream) {
-    const bool narrow = a.rows <= kNarrowRows;
-    if (narrow)
-        return out_f32 ? launch_one<D, BS, true, true>(a, tk, tv, grid, stream)
-                       : launch_one<D, BS, false, true>(a, tk, tv, grid, stream);
-    return out_f32 ? launch_one<D, BS, true, false>(a, tk, tv, grid, stream)
-                   : launch_one<D, BS, false, false>(a, tk, tv, grid, stream);
+    if (a.rows <= kNarrowRows)
+        return out_f32 ? launch_one<D, BS, true, kModeNarrow>(a, tk, tv, grid, stream)
+                       : launch_one<D, BS, false, kModeNarrow>(a, tk, tv, grid, stream);
+    if (a.rows > kTmemMinRows)
+        return out_f32 ? launch_one<D, BS, true, kModeTmem>(a, tk, tv, grid, stream)
+                       : launch_one<D, BS, false, kModeTmem>(a, tk, tv, grid, stream);
+    return out_f32 ? launch_one<D, BS, true, kModeWide>(a, tk, tv, grid, stream)
+                   : launch_one<D, BS, false, kModeWide>(a, tk, tv, grid, stream);
 }
 
 cudaError_t launch_decode_attn(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
