@@ -857,16 +857,19 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 }
 
 // ===================== TMEM consumer (rows > 64) =====================
-// One 128-row tile per unit (rows >= R are zero).  Warp 4 lane 0 issues the
-// tensor-core work; warps 0..3 run the softmax, one thread per row (TMEM lane
-// = row, so a row's max and sum never leave the thread).  Per block g:
-//   issuer : S[g&1] = Q K_g^T      (tcgen05.mma, A = Q tile, B = K stage, K-major)
-//   softmax: P[g&1] = 2^(S*scale - m) as bf16 in TMEM, running sum l; O is
-//            rescaled in TMEM only when a row's max grew by more than 2^8 (the
-//            stale max is used consistently in P and l, so the result is exact)
-//   issuer : O += P[g&1] V_g        (A from TMEM, B = V stage, MN-major)
-// The issuer runs one block ahead (QK of g+1 before PV of g), so scores of the
-// next block are computed while the softmax works on this one.
+// One 128-row tile per unit (rows >= R are zero), accumulators in TMEM.
+//   warp 4, lane 0 -- QK issuer: S[g&1] = Q K_g^T (tcgen05.mma; A = Q tile,
+//                     B = K stage, both K-major), as soon as the stage has
+//                     landed and the softmax has loaded S[g&1] of block g-2;
+//   warps 0..3     -- softmax, one thread per row (TMEM lane = row, so a row's
+//                     max and sum never leave the thread): P[g&1] = bf16 of
+//                     2^(S*scale - m) into TMEM, running sum l; O is rescaled
+//                     in TMEM only when a row's max grew by more than 2^8 (the
+//                     stale max is used consistently in P and l: exact);
+//   warp 5, lane 0 -- PV issuer: O += P[g&1] V_g (A from TMEM, B = V stage,
+//                     MN-major), then releases the stage.
+// Scores therefore run up to two blocks ahead of the softmax, and the PV
+// update of a block overlaps the softmax of the next.
 template <int D, int BS, bool OUT_F32>
 __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t* stages,
                                              uint8_t* qtile, uint64_t* full_bar,
@@ -880,22 +883,34 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     constexpr int KT = D / 16;   // k steps of S = Q K^T
     constexpr int PK = BS / 16;  // k steps of O += P V
     constexpr int kQHalf = 128 * 128;  // bytes of one 64-column half of the Q tile
-    // tcb: [0..1] S ready, [2..3] P ready, [4] PV done, [5] teardown
+    constexpr int kParty = 192;        // warps 0..5 take part in this mode
+    // tcb: [0..1] S ready, [2..3] S read, [4..5] P ready, [6..7] PV done, [8] QK teardown,
+    //      [9] PV teardown
+    uint64_t* s_full = tcb;
+    uint64_t* s_free = tcb + 2;
+    uint64_t* p_full = tcb + 4;
+    uint64_t* pv_done = tcb + 6;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp > 4) return;  // warps 5..7 have no part in this mode
+    if (warp > 5) return;  // warps 6, 7 have no part in this mode
     const bool softmax = warp < 4;
     const int row = threadIdx.x;  // softmax threads: row = TMEM lane
     const int R = a.rows, G = a.group, cta = blockIdx.x;
 
     if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
     tc_fence_before();
-    named_barrier_sync(2, 160);
+    named_barrier_sync(2, kParty);
     tc_fence_after();
     const uint32_t tbase = *s_tmem;
     const uint32_t tlane = tbase + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t idesc_qk = umma_idesc_bf16(128, BS, false);
     const uint32_t idesc_pv = umma_idesc_bf16(128, D, true);
     const uint32_t q_saddr = smem_addr(qtile);
+
+    auto issuer_fail = [&](bool& ok) {
+        ok = false;
+        atomicOr(a.err, kErrTimeout);
+        *s_abort = 1;
+    };
 
     uint32_t gbase = 0;
     bool ok = true;
@@ -906,72 +921,79 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         int lim = -1, i_row = 0, hq_row = 0;
         if (softmax) {
             // This unit's query rows into the swizzled Q tile (the previous
-            // unit's MMAs finished: every S of it was waited for).
+            // unit's score products finished: each of them was waited for).
             const bool valid = row < R;
             i_row = valid ? row / G : 0;
             hq_row = h * G + (valid ? row % G : 0);
             lim = valid ? ctx - a.q_len + i_row : -1;
             const uint4* qrow = reinterpret_cast<const uint4*>(
                 a.q + (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D);
+            uint4 qv[D / 8];
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < D / 8; ++c) qv[c] = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c)
                 *reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + row * 128 +
-                                          (((c & 7) ^ (row & 7)) << 4)) = v;
-            }
+                                          (((c & 7) ^ (row & 7)) << 4)) = qv[c];
             fence_proxy_async_smem();
         }
         tc_fence_before();
-        named_barrier_sync(2, 160);  // Q tile ready; the previous unit's O has been read
+        named_barrier_sync(2, kParty);  // Q tile ready; the previous unit's O has been read
         tc_fence_after();
 
         if (warp == 4) {
-            // ===================== issuer =====================
+            // ===================== QK issuer =====================
             if (lane == 0 && ok) {
-                for (int b = 0; b <= n; ++b) {
-                    if (b < n) {
-                        const uint32_t g = gbase + b, st = g % kStages;
-                        if (*s_abort || !mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u)) {
-                            ok = false;
-                            atomicOr(a.err, kErrTimeout);
-                            *s_abort = 1;
-                            break;
-                        }
-                        const uint32_t kb = smem_addr(stages + st * C::kStageBytes);
-                        const uint32_t scol = tbase + kColS + (g & 1u) * BS;
-#pragma unroll
-                        for (int kk = 0; kk < KT; ++kk) {
-                            const uint64_t ad =
-                                umma_smem_desc(q_saddr + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bd = umma_smem_desc(
-                                kb + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
-                            umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-                        }
-                        umma_commit(&tcb[g & 1u]);
+                for (int b = 0; b < n; ++b) {
+                    const uint32_t g = gbase + b, st = g % kStages;
+                    if (*s_abort || !mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u)) {
+                        issuer_fail(ok);
+                        break;
                     }
-                    if (b > 0) {
-                        const uint32_t g = gbase + b - 1, st = g % kStages;
-                        if (*s_abort || !mbar_wait_bounded(&tcb[2 + (g & 1u)], (g >> 1) & 1u)) {
-                            ok = false;
-                            atomicOr(a.err, kErrTimeout);
-                            *s_abort = 1;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t vb = smem_addr(stages + st * C::kStageBytes) + C::kTileBytes;
-                        const uint32_t pcol = tbase + kColP + (g & 1u) * (BS / 2);
-#pragma unroll
-                        for (int kk = 0; kk < PK; ++kk) {
-                            const uint64_t bd = umma_smem_desc(vb + kk * 16 * 128, C::kBoxBytes, 1024);
-                            umma_ts(tbase + kColO, pcol + kk * 8, bd, idesc_pv,
-                                    (b > 1 || kk > 0) ? 1u : 0u);
-                            if (OUT_F32)
-                                umma_ts(tbase + kColO, tbase + kColPL + (g & 1u) * (BS / 2) + kk * 8,
-                                        bd, idesc_pv, 1u);
-                        }
-                        umma_commit(&empty_bar[st]);  // K and V of this stage are consumed
-                        umma_commit(&tcb[4]);         // PV of block g done
+                    if (g >= 2 && !mbar_wait_bounded(&s_free[g & 1u], ((g - 2) >> 1) & 1u)) {
+                        issuer_fail(ok);
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t kb = smem_addr(stages + st * C::kStageBytes);
+                    const uint32_t scol = tbase + kColS + (g & 1u) * BS;
+#pragma unroll
+                    for (int kk = 0; kk < KT; ++kk) {
+                        const uint64_t ad =
+                            umma_smem_desc(q_saddr + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd =
+                            umma_smem_desc(kb + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
+                        umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&s_full[g & 1u]);
+                }
+            }
+            __syncwarp();
+        } else if (warp == 5) {
+            // ===================== PV issuer =====================
+            if (lane == 0 && ok) {
+                for (int b = 0; b < n; ++b) {
+                    const uint32_t g = gbase + b, st = g % kStages;
+                    if (*s_abort || !mbar_wait_bounded(&p_full[g & 1u], (g >> 1) & 1u)) {
+                        issuer_fail(ok);
+                        break;
+                    }
+                    tc_fence_after();
+                    // The softmax saw S of this block, so its score product
+                    // (the only other reader of the stage) has completed.
+                    const uint32_t vb = smem_addr(stages + st * C::kStageBytes) + C::kTileBytes;
+                    const uint32_t pcol = tbase + kColP + (g & 1u) * (BS / 2);
+#pragma unroll
+                    for (int kk = 0; kk < PK; ++kk) {
+                        const uint64_t bd = umma_smem_desc(vb + kk * 16 * 128, C::kBoxBytes, 1024);
+                        umma_ts(tbase + kColO, pcol + kk * 8, bd, idesc_pv,
+                                (b > 0 || kk > 0) ? 1u : 0u);
+                        if (OUT_F32)
+                            umma_ts(tbase + kColO, tbase + kColPL + (g & 1u) * (BS / 2) + kk * 8, bd,
+                                    idesc_pv, 1u);
+                    }
+                    umma_commit(&empty_bar[st]);    // K and V of this stage are consumed
+                    umma_commit(&pv_done[g & 1u]);  // its P buffer is free; O is current
                 }
             }
             __syncwarp();
@@ -981,7 +1003,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             const int lim_min = ctx - a.q_len;
             for (int b = 0; b < n; ++b) {
                 const uint32_t g = gbase + b;
-                ok = consumer_wait(a, &tcb[g & 1u], (g >> 1) & 1u, ok, s_abort);
+                ok = consumer_wait(a, &s_full[g & 1u], (g >> 1) & 1u, ok, s_abort);
                 if (!ok) continue;
                 tc_fence_after();
                 float x[BS];
@@ -992,6 +1014,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     else
                         tmem_ld16(tlane + kColS + (g & 1u) * BS, sr);
                     tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&s_free[g & 1u]);  // S buffer may take the block after next
 #pragma unroll
                     for (int c = 0; c < BS; ++c) x[c] = __uint_as_float(sr[c]) * a.scale_log2;
                 }
@@ -1004,15 +1028,21 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 }
 #pragma unroll
                 for (int c = 0; c < BS; ++c) mloc = fmaxf(mloc, x[c]);
-                // PV of the previous block must be done before O is rescaled
-                // or its P buffer (read by PV two blocks back) is rewritten.
-                if (b > 0) {
-                    ok = consumer_wait(a, &tcb[4], (g - 1) & 1u, ok, s_abort);
+                // This block's P buffer was last read by PV two blocks back.
+                if (b > 1) {
+                    ok = consumer_wait(a, &pv_done[g & 1u], ((g - 2) >> 1) & 1u, ok, s_abort);
                     if (!ok) continue;
                     tc_fence_after();
                 }
                 const bool grow = mloc > m_used + 8.f;
                 if (__any_sync(0xffffffffu, grow)) {
+                    // O may only be rescaled once the previous block's PV is done.
+                    if (b > 0) {
+                        ok = consumer_wait(a, &pv_done[(g - 1) & 1u], ((g - 1) >> 1) & 1u, ok,
+                                           s_abort);
+                        if (!ok) continue;
+                        tc_fence_after();
+                    }
                     const float m_new = grow ? mloc : m_used;
                     const float alpha = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
                     l *= alpha;
@@ -1065,11 +1095,14 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     fence_proxy_async_smem();
                 }
                 tc_fence_before();
-                mbar_arrive(&tcb[2 + (g & 1u)]);
+                mbar_arrive(&p_full[g & 1u]);
             }
 
             // ---- epilogue: the last PV, then O out of TMEM row by row
-            if (n > 0) ok = consumer_wait(a, &tcb[4], (gbase + n - 1) & 1u, ok, s_abort);
+            if (n > 0) {
+                const uint32_t gl = gbase + n - 1;
+                ok = consumer_wait(a, &pv_done[gl & 1u], (gl >> 1) & 1u, ok, s_abort);
+            }
             tc_fence_after();
             const bool first_piece = j0 == 0, last_piece = j1 == w.nb;
             const bool whole = first_piece && last_piece;
@@ -1133,12 +1166,13 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         if (w.left > 0) walk_next_unit<BS>(a, w);
     }
     // Teardown: no tensor-core operation may still be running when TMEM is freed.
-    if (warp == 4 && lane == 0) {
-        umma_commit(&tcb[5]);
-        (void)mbar_wait_bounded(&tcb[5], 0u);
+    if ((warp == 4 || warp == 5) && lane == 0) {
+        uint64_t* bar = &tcb[warp == 4 ? 8 : 9];
+        umma_commit(bar);
+        (void)mbar_wait_bounded(bar, 0u);
     }
     tc_fence_before();
-    named_barrier_sync(2, 160);
+    named_barrier_sync(2, kParty);
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
@@ -1163,7 +1197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ long long s_red[kThreads / 32];
     __shared__ long long s_start[2];
     __shared__ int s_abort;
-    __shared__ uint64_t s_tcb[6];  // TMEM mode: S ready x2, P ready x2, PV done, teardown
+    __shared__ uint64_t s_tcb[10];  // TMEM mode: S ready/read, P ready, PV done (x2 each), 2 teardowns
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1176,12 +1210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty_bar[i], releases);
         }
         if (MODE == kModeTmem) {
-            mbar_init(&s_tcb[0], 1);
-            mbar_init(&s_tcb[1], 1);
-            mbar_init(&s_tcb[2], 128);
-            mbar_init(&s_tcb[3], 128);
-            mbar_init(&s_tcb[4], 1);
-            mbar_init(&s_tcb[5], 1);
+            // S ready (a commit), S read (128 rows), P ready (128 rows),
+            // PV done (a commit), two issuer teardowns (a commit each)
+            const uint32_t counts[10] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1};
+            for (int i = 0; i < 10; ++i) mbar_init(&s_tcb[i], counts[i]);
         }
         fence_barrier_init();
         s_abort = 0;
