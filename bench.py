@@ -77,7 +77,7 @@ def hbm_peak():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("decode_attn.cu", "ptx.cuh", "pkv_internal.h"):
+    for name in ("decode_attn.cu", "ptx.cuh", "tcgen05.cuh", "pkv_internal.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_256_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -151,6 +151,27 @@ class ClockSampler:
                 "sm_max_mhz": max(r["smax"] for r in rows),
                 "power_w_max": max(r["power"] for r in rows),
                 "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of a list of floats over all ranks (identity at N = 1).
+
+    Uses the process group's own backend: NCCL on GPU tensors for the bench,
+    gloo on CPU tensors in the multi-process CPU tests.
+    """
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_gbps(bytes_per_rank, ms_per_step, world):
+    """Whole-job throughput of N independent replicas timed by the slowest rank."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -309,12 +330,7 @@ def run_ours(args):
     total_ms = ev_step[0].elapsed_time(ev_step[K])
     attn_ms = [ev_attn[k].elapsed_time(ev_step[k + 1]) for k in range(K)]
     step_ms = [ev_step[k].elapsed_time(ev_step[k + 1]) for k in range(K)]
-    ms_per_step = total_ms / K
-    attn_mean = sum(attn_ms) / K
-    if world > 1:
-        t = torch.tensor([ms_per_step, attn_mean], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step, attn_mean = float(t[0]), float(t[1])
+    ms_per_step, attn_mean = max_over_ranks([total_ms / K, sum(attn_ms) / K], device)
 
     # ---- end to end through the public API, host buffers, copies inside the timed region
     e2e = None
@@ -353,17 +369,13 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(device)
-        e2e_ms = e0.elapsed_time(e1) / K
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t[0])
-        e2e = {"value": round(world * total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+        e2e_ms = max_over_ranks([e0.elapsed_time(e1) / K], device)[0]
+        e2e = {"value": round(whole_job_gbps(total_bytes, e2e_ms, world), 2), "unit": UNIT,
                "us_per_step": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
     peak, peak_src = hbm_peak()
-    value = world * total_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbps(total_bytes, ms_per_step, world)
     achieved = total_bytes / (attn_mean * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,

@@ -51,6 +51,11 @@ typedef enum pkv_status {
 
 /* flags bits. */
 #define PKV_FLAG_CHECKED 0x1u /* bounds-check block indices and context lengths on the device */
+/* For tests of the failure path only: the attention kernel issues no loads,
+ * so every bounded in-kernel wait expires (after about a second), the kernel
+ * winds down and pkv_check_error reports PKV_ERR_TIMEOUT.  The output of
+ * such a call is not valid; the context stays usable. */
+#define PKV_FLAG_TEST_STALL 0x2u
 /* Bits 16..31 force the number of attention CTAs (0 = one per SM).  Tests
  * use it to move where long contexts are split; results stay within the
  * stated tolerance for every value. */

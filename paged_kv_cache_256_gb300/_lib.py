@@ -24,6 +24,7 @@ PKV_ERR_TIMEOUT = 6
 PKV_OUT_BF16 = 0
 PKV_OUT_F32 = 1
 PKV_FLAG_CHECKED = 0x1
+PKV_FLAG_TEST_STALL = 0x2
 PKV_FLAG_GRID_SHIFT = 16
 
 

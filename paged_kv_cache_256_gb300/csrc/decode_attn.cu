@@ -215,6 +215,7 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                                         uint64_t* full_bar, uint64_t* empty_bar,
                                         volatile int* s_abort) {
     const int lane = threadIdx.x & 31;
+    if (a.test_stall) return;  // failure-path tests: nothing is loaded, every wait expires
     const uint64_t policy = l2_policy_evict_first();
     uint32_t gidx = 0, issued = 0;  // issued: fills actually started (a prefix of gidx)
     bool ok = true;

@@ -194,6 +194,7 @@ int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cach
     a.tile_rows_total = (int)rows_total;
     a.warp_rows = warp_rows_for(rows);
     a.checked = (flags & PKV_FLAG_CHECKED) ? 1 : 0;
+    a.test_stall = (flags & PKV_FLAG_TEST_STALL) ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
