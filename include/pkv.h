@@ -42,7 +42,8 @@ typedef enum pkv_status {
     PKV_ERR_WORKSPACE = 3,       /* workspace missing or smaller than the size query asked for */
     PKV_ERR_CUDA = 4,            /* a CUDA runtime / driver call or a launch failed */
     PKV_ERR_BAD_BLOCK_TABLE = 5, /* CHECKED mode found a block index or context length out of range */
-    PKV_ERR_TIMEOUT = 6          /* a bounded in-kernel wait gave up (the kernel returned early) */
+    PKV_ERR_TIMEOUT = 6,         /* a bounded in-kernel wait gave up (the kernel returned early) */
+    PKV_ERR_OUT_OF_BLOCKS = 7    /* the block pool has too few free blocks (nothing was changed) */
 } pkv_status;
 
 /* out_dtype values. */
@@ -179,6 +180,68 @@ int pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache, const void
 int pkv_kv_append(const void *k_new, const void *v_new, const int32_t *slot_mapping,
                   int num_tokens, int n_kv, int head_dim, int block_size, int num_blocks,
                   void *k_cache, void *v_cache, unsigned flags, void *stream);
+
+/*
+ * pkv_copy_blocks -- copy whole physical blocks (every KV head, K and V).
+ *
+ * For each pair p < num_pairs: block pairs[2p+1] of k_cache and of v_cache
+ * becomes a bit copy of block pairs[2p].  This is the copy half of
+ * copy-on-write: a block shared by several sequences (a common prefix) is
+ * duplicated before one of them writes into it ("Inference Engines", The
+ * Breakthrough, PagedAttention paragraph; CS336 lecture-10 notes,
+ * PagedAttention (vLLM): copy-on-write at the block level).
+ * pairs: device int32 [num_pairs][2]; pairs with an id outside
+ *   [0, num_blocks) or with src == dst are skipped.  A destination must not
+ *   also be a source in the same call.
+ * Caches as for pkv_paged_decode_attn (head_dim a multiple of 8).
+ * Returns PKV_OK, PKV_ERR_INVALID_ARG or PKV_ERR_CUDA; num_pairs == 0 launches nothing.
+ */
+int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,
+                    int num_blocks, int n_kv, int head_dim, int block_size, unsigned flags,
+                    void *stream);
+
+/*
+ * Block pool -- host-side allocator of physical blocks with reference counts
+ * (on-demand allocation, prefix sharing, copy-on-write: "Transformer inference
+ * mechanics", FlashAttention versus PagedAttention; "Inference Engines", The
+ * Breakthrough).  Pure host bookkeeping: it never touches device memory.
+ * Every call either succeeds completely or changes nothing.  A pool is not
+ * thread-safe: callers serialise access.
+ */
+typedef struct pkv_block_pool pkv_block_pool;
+
+/* All num_blocks blocks free (reference count 0).  NULL on bad sizes or no memory. */
+pkv_block_pool *pkv_pool_create(int num_blocks, int block_size);
+void pkv_pool_destroy(pkv_block_pool *pool);
+/* Free blocks, or -1 for a NULL pool. */
+int pkv_pool_num_free(const pkv_block_pool *pool);
+/* Reference count of a block (0 = free), or -1 for a bad pool or id. */
+int pkv_pool_refcount(const pkv_block_pool *pool, int block);
+/* Take n free blocks (reference count 1 each) into out_blocks[0..n).
+ * PKV_ERR_OUT_OF_BLOCKS if fewer than n are free. */
+int pkv_pool_alloc(pkv_block_pool *pool, int n, int32_t *out_blocks);
+/* One more owner for each listed block (a forked sequence or a shared prefix);
+ * every block must be in use. */
+int pkv_pool_share(pkv_block_pool *pool, const int32_t *blocks, int n);
+/* One owner fewer for each listed block; a block whose count reaches 0 is free
+ * again.  Fails (changing nothing) if a count would go below 0. */
+int pkv_pool_release(pkv_block_pool *pool, const int32_t *blocks, int n);
+/*
+ * Make room for n_new tokens at the end of one sequence.
+ * table[0..*nblocks) is the sequence's block-table row (host memory, room for
+ * max_blocks entries) and ctx its resident token count.  Every block that
+ * will receive a new token is made exclusively owned: if it is shared, a
+ * fresh block takes its place in the table, the pair (old, new) is appended
+ * to copy_pairs (room for 2 * ceil(n_new / block_size + 1) ints) and the old
+ * block loses this owner; blocks are appended to the table as needed and
+ * *nblocks is updated.  slot_out[i] is the cache slot of new token i
+ * (block * block_size + offset), ready for pkv_kv_append; *num_pairs is the
+ * number of copies to make with pkv_copy_blocks before appending.
+ * Returns PKV_OK, PKV_ERR_INVALID_ARG or PKV_ERR_OUT_OF_BLOCKS.
+ */
+int pkv_pool_append_slots(pkv_block_pool *pool, int32_t *table, int *nblocks, int max_blocks,
+                          int ctx, int n_new, int32_t *slot_out, int32_t *copy_pairs,
+                          int *num_pairs);
 
 /*
  * Synchronise `stream`, read and clear the error word of `workspace`.

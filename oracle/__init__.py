@@ -13,6 +13,7 @@ Functions (each follows the passage cited in ``pkv_oracle.c``):
 * :func:`attn_partial` -- (o, m, l) of one key range: the online-softmax state.
 * :func:`lse_merge`    -- exact combination of partials.
 * :func:`kv_append`    -- bit copy of new K/V rows into their slots.
+* :func:`copy_blocks`  -- whole-block copies (copy-on-write).
 * :func:`kv_bytes`     -- M_kv = 2 L n_kv d_h (s b) p.
 """
 from __future__ import annotations
@@ -74,6 +75,8 @@ class Oracle:
         lib.oracle_kv_append.restype = c_int
         lib.oracle_kv_bytes.argtypes = [c_int, c_int, c_int, c_int, ctypes.c_int64]
         lib.oracle_kv_bytes.restype = ctypes.c_int64
+        lib.oracle_copy_blocks.argtypes = [i32p, c_int, c_int, c_int, c_int, c_int, u16p, u16p]
+        lib.oracle_copy_blocks.restype = c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = c_int
         self._lib = lib
@@ -155,6 +158,17 @@ class Oracle:
             _ptr(k_cache, ctypes.c_uint16), _ptr(v_cache, ctypes.c_uint16))
         if st != 0:
             raise ValueError(f"oracle_kv_append rejected its inputs (status {st})")
+
+    def copy_blocks(self, pairs, k_cache, v_cache):
+        """In-place whole-block copies: block pairs[p, 1] <- block pairs[p, 0]."""
+        pairs = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+        num_blocks, n_kv, bs, d = k_cache.shape
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        st = self._lib.oracle_copy_blocks(_ptr(pairs, ctypes.c_int32), pairs.shape[0], num_blocks,
+                                          n_kv, d, bs, _ptr(k_cache, ctypes.c_uint16),
+                                          _ptr(v_cache, ctypes.c_uint16))
+        if st != 0:
+            raise ValueError(f"oracle_copy_blocks rejected its inputs (status {st})")
 
     # -- sizes --------------------------------------------------------------
     def kv_bytes(self, layers, n_kv, head_dim, elem_bytes, tokens):

@@ -312,6 +312,31 @@ int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, const int32_t
 }
 
 /*
+ * Copy whole physical blocks: for each pair, block dst of both caches becomes
+ * a bit copy of block src (all KV heads).  Pairs with an id outside
+ * [0, num_blocks) or src == dst are skipped.  This is the copy of
+ * copy-on-write block sharing (CS336 lecture-10 notes, PagedAttention (vLLM):
+ * a shared block is split only when generations diverge).
+ */
+int oracle_copy_blocks(const int32_t *pairs, int num_pairs, int num_blocks, int n_kv,
+                       int head_dim, int block_size, uint16_t *k_cache, uint16_t *v_cache)
+{
+    if (num_pairs < 0 || num_blocks < 0 || n_kv < 1 || head_dim < 1 || block_size < 1)
+        return 1;
+    const size_t per_block = (size_t)n_kv * block_size * head_dim;
+    for (int p = 0; p < num_pairs; ++p) {
+        const int src = pairs[2 * p], dst = pairs[2 * p + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks || src == dst)
+            continue;
+        memcpy(k_cache + (size_t)dst * per_block, k_cache + (size_t)src * per_block,
+               sizeof(uint16_t) * per_block);
+        memcpy(v_cache + (size_t)dst * per_block, v_cache + (size_t)src * per_block,
+               sizeof(uint16_t) * per_block);
+    }
+    return 0;
+}
+
+/*
  * KV-cache bytes M_kv = 2 * L * n_kv * d_h * (s * b) * p, with s * b given as
  * the number of resident tokens ("Inference Engines", The Mathematics;
  * "Efficient inference", Key ideas).  Returns -1 on a negative argument.

@@ -16,7 +16,10 @@ memory and streams.
 from ._lib import (  # noqa: F401
     PKV_ERR_BAD_BLOCK_TABLE, PKV_ERR_CUDA, PKV_ERR_INVALID_ARG, PKV_ERR_TIMEOUT,
     PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_FLAG_CHECKED, PKV_FLAG_GRID, PKV_FLAG_TEST_STALL, PKV_OK, PKV_OUT_BF16,
-    PKV_OUT_F32, PkvError, alloc_workspace, load_library, pkv_check_error, pkv_kv_append,
+    PKV_ERR_OUT_OF_BLOCKS, PKV_OUT_F32, BlockPool, PkvError, alloc_workspace, load_library,
+    pkv_check_error, pkv_copy_blocks, pkv_kv_append, pkv_pool_alloc, pkv_pool_append_slots,
+    pkv_pool_create, pkv_pool_destroy, pkv_pool_num_free, pkv_pool_refcount, pkv_pool_release,
+    pkv_pool_share,
     pkv_kv_bytes, pkv_paged_decode_attn, pkv_paged_decode_attn_noalloc,
     pkv_paged_decode_attn_workspace_size,
     pkv_status_string, pkv_version)

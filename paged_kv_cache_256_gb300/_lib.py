@@ -20,6 +20,7 @@ PKV_ERR_WORKSPACE = 3
 PKV_ERR_CUDA = 4
 PKV_ERR_BAD_BLOCK_TABLE = 5
 PKV_ERR_TIMEOUT = 6
+PKV_ERR_OUT_OF_BLOCKS = 7
 
 PKV_OUT_BF16 = 0
 PKV_OUT_F32 = 1
@@ -43,6 +44,16 @@ SIGNATURES = {
                                       [_c_float, _vp, _c_int, ctypes.c_uint, _vp], _c_int),
     "pkv_kv_append": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp, _vp, ctypes.c_uint, _vp], _c_int),
     "pkv_check_error": ([_vp, _vp], _c_int),
+    "pkv_copy_blocks": ([_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.c_uint,
+                         _vp], _c_int),
+    "pkv_pool_create": ([_c_int, _c_int], _vp),
+    "pkv_pool_destroy": ([_vp], None),
+    "pkv_pool_num_free": ([_vp], _c_int),
+    "pkv_pool_refcount": ([_vp, _c_int], _c_int),
+    "pkv_pool_alloc": ([_vp, _c_int, _vp], _c_int),
+    "pkv_pool_share": ([_vp, _vp, _c_int], _c_int),
+    "pkv_pool_release": ([_vp, _vp, _c_int], _c_int),
+    "pkv_pool_append_slots": ([_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp], _c_int),
     "pkv_kv_bytes": ([_c_int] * 4 + [ctypes.c_int64], ctypes.c_int64),
     "pkv_status_string": ([_c_int], ctypes.c_char_p),
     "pkv_version": ([], _c_int),
@@ -213,6 +224,116 @@ def pkv_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, flags=0, stream=
         k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), T, n_kv, d, bs, num_blocks,
         k_cache.data_ptr(), v_cache.data_ptr(), int(flags), _stream_ptr(stream))
     _check(st, "pkv_kv_append")
+
+
+def pkv_copy_blocks(k_cache, v_cache, pairs, flags=0, stream=None):
+    """Copy whole blocks (all KV heads, K and V): block pairs[p,1] <- block pairs[p,0]."""
+    import torch
+    _bf16_like(k_cache, "k_cache")
+    _bf16_like(v_cache, "v_cache")
+    if pairs.dtype != torch.int32 or not pairs.is_cuda or not pairs.is_contiguous() or \
+            pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be a contiguous int32 CUDA tensor of shape [n, 2]")
+    num_blocks, n_kv, bs, d = k_cache.shape
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent shapes")
+    st = load_library().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(),
+                                        pairs.shape[0], num_blocks, n_kv, d, bs, int(flags),
+                                        _stream_ptr(stream))
+    _check(st, "pkv_copy_blocks")
+
+
+# ---- block pool (host memory only; numpy int32 arrays are passed by pointer)
+def _i32_host(a):
+    import numpy as np
+    if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous):
+        raise TypeError("expected a contiguous numpy int32 array")
+    return a.ctypes.data
+
+
+def pkv_pool_create(num_blocks: int, block_size: int):
+    h = load_library().pkv_pool_create(num_blocks, block_size)
+    if not h:
+        raise PkvError(PKV_ERR_INVALID_ARG, "pkv_pool_create")
+    return h
+
+
+def pkv_pool_destroy(pool) -> None:
+    load_library().pkv_pool_destroy(pool)
+
+
+def pkv_pool_num_free(pool) -> int:
+    return int(load_library().pkv_pool_num_free(pool))
+
+
+def pkv_pool_refcount(pool, block: int) -> int:
+    return int(load_library().pkv_pool_refcount(pool, block))
+
+
+def pkv_pool_alloc(pool, n: int):
+    import numpy as np
+    out = np.zeros(max(n, 0), dtype=np.int32)
+    _check(load_library().pkv_pool_alloc(pool, n, _i32_host(out)), "pkv_pool_alloc")
+    return out
+
+
+def pkv_pool_share(pool, blocks) -> None:
+    _check(load_library().pkv_pool_share(pool, _i32_host(blocks), blocks.shape[0]),
+           "pkv_pool_share")
+
+
+def pkv_pool_release(pool, blocks) -> None:
+    _check(load_library().pkv_pool_release(pool, _i32_host(blocks), blocks.shape[0]),
+           "pkv_pool_release")
+
+
+def pkv_pool_append_slots(pool, table, nblocks: int, ctx: int, n_new: int, block_size: int):
+    """Reserve slots for n_new tokens (copy-on-write); returns (nblocks, slots, copy_pairs).
+
+    table: numpy int32 row of max_blocks entries, updated in place.
+    copy_pairs: numpy int32 [k, 2] of (shared source, fresh destination) blocks.
+    """
+    import numpy as np
+    nb = ctypes.c_int(nblocks)
+    npairs = ctypes.c_int(0)
+    slots = np.zeros(max(n_new, 1), dtype=np.int32)
+    pairs = np.zeros((n_new // block_size + 2) * 2, dtype=np.int32)
+    st = load_library().pkv_pool_append_slots(
+        pool, _i32_host(table), ctypes.addressof(nb), table.shape[0], ctx, n_new,
+        _i32_host(slots), _i32_host(pairs), ctypes.addressof(npairs))
+    _check(st, "pkv_pool_append_slots")
+    return nb.value, slots[:n_new], pairs[: 2 * npairs.value].reshape(-1, 2)
+
+
+class BlockPool:
+    """Owning wrapper of a pkv_block_pool handle."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self.block_size = block_size
+        self.handle = pkv_pool_create(num_blocks, block_size)
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h:
+            pkv_pool_destroy(h)
+
+    def num_free(self):
+        return pkv_pool_num_free(self.handle)
+
+    def refcount(self, b):
+        return pkv_pool_refcount(self.handle, b)
+
+    def alloc(self, n):
+        return pkv_pool_alloc(self.handle, n)
+
+    def share(self, blocks):
+        pkv_pool_share(self.handle, blocks)
+
+    def release(self, blocks):
+        pkv_pool_release(self.handle, blocks)
+
+    def append_slots(self, table, nblocks, ctx, n_new):
+        return pkv_pool_append_slots(self.handle, table, nblocks, ctx, n_new, self.block_size)
 
 
 def pkv_check_error(workspace, stream=None) -> int:

@@ -1,4 +1,5 @@
-// kv_append.cu -- write each step's new K/V rows into their paged-cache slots.
+// kv_append.cu -- writes into the paged cache: each step's new K/V rows, and
+// whole-block copies for copy-on-write.
 //
 // For token i with slot s = slot_mapping[i] in [0, num_blocks * block_size):
 //   cache[s / block_size][g][s % block_size][:] = new[i][g][:]  for every KV head g,
@@ -54,6 +55,42 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
         num_tokens, n_kv, chunks, block_size, (long long)num_blocks * block_size,
         static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache));
+    return cudaGetLastError();
+}
+
+// One thread moves one 16-byte chunk of a (K or V) block; consecutive threads
+// cover consecutive chunks of the same block, so reads and writes are full
+// 16-byte vector accesses over whole contiguous blocks.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                       const int32_t* __restrict__ pairs, int num_pairs, int num_blocks,
+                       long long chunks_per_block) {
+    const long long total = (long long)num_pairs * 2 * chunks_per_block;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long chunk = idx % chunks_per_block;
+        const long long rest = idx / chunks_per_block;
+        const int which = static_cast<int>(rest & 1);  // 0: K, 1: V
+        const int p = static_cast<int>(rest >> 1);
+        const int src = __ldg(pairs + 2 * p), dst = __ldg(pairs + 2 * p + 1);
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks || src == dst) continue;
+        uint4* cache = which == 0 ? k_cache : v_cache;
+        cache[(size_t)dst * chunks_per_block + chunk] = cache[(size_t)src * chunks_per_block + chunk];
+    }
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                               int num_blocks, int n_kv, int head_dim, int block_size,
+                               int num_sms, cudaStream_t stream) {
+    const long long chunks = (long long)n_kv * block_size * head_dim / 8;
+    const long long total = (long long)num_pairs * 2 * chunks;
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    copy_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), pairs, num_pairs, num_blocks,
+        chunks);
     return cudaGetLastError();
 }
 

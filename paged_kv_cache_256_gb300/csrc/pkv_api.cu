@@ -117,6 +117,7 @@ const char* pkv_status_string(int status) {
         case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
         case PKV_ERR_BAD_BLOCK_TABLE: return "PKV_ERR_BAD_BLOCK_TABLE";
         case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
+        case PKV_ERR_OUT_OF_BLOCKS: return "PKV_ERR_OUT_OF_BLOCKS";
         default: return "PKV_ERR_UNKNOWN";
     }
 }
@@ -225,6 +226,27 @@ int pkv_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapp
     if (launch_kv_append(k_new, v_new, slot_mapping, num_tokens, n_kv, head_dim, block_size,
                          num_blocks, k_cache, v_cache, sms,
                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                    int num_blocks, int n_kv, int head_dim, int block_size, unsigned flags,
+                    void* stream) {
+    (void)flags;
+    if (num_pairs < 0 || num_blocks < 1 || n_kv < 1 || head_dim < 8 || head_dim % 8 != 0 ||
+        block_size < 1)
+        return PKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !pairs) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(pairs, 4))
+        return PKV_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return PKV_ERR_CUDA;
+    if (launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_blocks, n_kv, head_dim,
+                           block_size, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
 }

@@ -59,4 +59,8 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
                              int num_blocks, void* k_cache, void* v_cache, int num_sms,
                              cudaStream_t stream);
 
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                               int num_blocks, int n_kv, int head_dim, int block_size,
+                               int num_sms, cudaStream_t stream);
+
 }  // namespace pkv

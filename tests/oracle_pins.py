@@ -311,6 +311,22 @@ def pin_kv_append(orc):
         assert np.array_equal(k_got, k_ref) and np.array_equal(v_got, v_ref)
 
 
+def pin_copy_blocks(orc):
+    rng = np.random.default_rng(22)
+    pool, n_kv, bs, d = 9, 3, 4, 8
+    kc = rng.integers(0, 1 << 16, size=(pool, n_kv, bs, d), dtype=np.uint16)
+    vc = rng.integers(0, 1 << 16, size=(pool, n_kv, bs, d), dtype=np.uint16)
+    pairs = np.asarray([[1, 5], [2, 2], [0, 7], [3, 9], [-1, 4], [8, 6]], dtype=np.int32)
+    k_ref, v_ref = kc.copy(), vc.copy()
+    for src, dst in pairs:
+        if 0 <= src < pool and 0 <= dst < pool and src != dst:
+            k_ref[dst] = kc[src]
+            v_ref[dst] = vc[src]
+    k_got, v_got = kc.copy(), vc.copy()
+    orc.copy_blocks(pairs, k_got, v_got)
+    assert np.array_equal(k_got, k_ref) and np.array_equal(v_got, v_ref)
+
+
 def pin_append_then_attend(orc):
     """The tiny workload: attend at ctx - 1, append one token, attend at ctx."""
     wl = make_custom(num_seqs=2, q_len=1, n_q=4, n_kv=2, head_dim=64, block_size=16,
@@ -359,5 +375,6 @@ def pin_gqa_ratio(orc):
 ALL_PINS = [
     pin_library_sdpa, pin_numpy_dense, pin_equal_scores_mean, pin_single_token, pin_hardmax,
     pin_block_permutation, pin_gqa_equals_repeated_mha, pin_causal_rows, pin_empty_context,
-    pin_merge_exact, pin_kv_append, pin_append_then_attend, pin_kv_bytes_golden, pin_gqa_ratio,
+    pin_merge_exact, pin_kv_append, pin_copy_blocks, pin_append_then_attend, pin_kv_bytes_golden,
+    pin_gqa_ratio,
 ]

@@ -46,7 +46,7 @@ def test_binding_exposes_same_names():
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         assert _lib.status_name(code).startswith("PKV_")
     assert _lib.status_name(_lib.PKV_ERR_TIMEOUT) == "PKV_ERR_TIMEOUT"
     assert _lib.status_name(99) == "PKV_ERR_UNKNOWN"
