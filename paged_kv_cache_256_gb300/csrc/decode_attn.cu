@@ -39,6 +39,7 @@
 //
 // Bounded waits: every mbarrier wait gives up after a second, records
 // kErrTimeout in the workspace and the kernel winds down without hanging.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 
@@ -1277,8 +1278,17 @@ static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CU
                               int grid, cudaStream_t stream) {
     auto kern = paged_decode_attn_kernel<D, BS, F32, MODE>;
     const int smem = AttnCfg<D, BS, MODE>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // The shared-memory opt-in is set once per device for each instantiation.
+    static std::atomic<unsigned long long> opted_in{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(opted_in.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        opted_in.fetch_or(bit, std::memory_order_release);
+    }
     kern<<<grid, kThreads, smem, stream>>>(tk, tv, a);
     return cudaGetLastError();
 }

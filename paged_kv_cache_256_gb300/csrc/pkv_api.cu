@@ -62,6 +62,42 @@ bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, long long 
     return r == CUDA_SUCCESS;
 }
 
+// Encoding a tensor map is a driver call; decode loops pass the same caches
+// every step, so the last few encodings are kept (keyed by everything that
+// goes into them).
+struct MapKey {
+    const void* base;
+    long long rows;
+    int head_dim, block_size;
+};
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool used;
+};
+constexpr int kMapCache = 8;
+std::mutex g_map_mutex;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+bool cached_cache_map(CUtensorMap* map, const void* base, int head_dim, long long rows,
+                      int block_size) {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (const MapEntry& e : g_maps)
+        if (e.used && e.key.base == base && e.key.rows == rows && e.key.head_dim == head_dim &&
+            e.key.block_size == block_size) {
+            *map = e.map;
+            return true;
+        }
+    if (!make_cache_map(map, base, head_dim, rows, block_size)) return false;
+    MapEntry& e = g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCache;
+    e.key = MapKey{base, rows, head_dim, block_size};
+    e.map = *map;
+    e.used = true;
+    return true;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -162,16 +198,21 @@ int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cach
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-    const int grid = attn_grid(flags, dev);
+    int grid = attn_grid(flags, dev);
     if (grid <= 0) return PKV_ERR_CUDA;
+    // No more CTAs than (unit, block) items the call can have.
+    if (((flags >> PKV_FLAG_GRID_SHIFT) & 0xFFFFu) == 0) {
+        const long long items = (long long)num_seqs * n_kv * max_blocks_per_seq;
+        if (items < grid) grid = (int)items;
+    }
     const int rows = (n_q / n_kv) * q_len;
     const WorkspaceLayout L = workspace_layout(grid, rows, head_dim);
     if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
 
     CUtensorMap tk, tv;
-    if (!make_cache_map(&tk, k_cache, head_dim, rows_total, block_size) ||
-        !make_cache_map(&tv, v_cache, head_dim, rows_total, block_size))
+    if (!cached_cache_map(&tk, k_cache, head_dim, rows_total, block_size) ||
+        !cached_cache_map(&tv, v_cache, head_dim, rows_total, block_size))
         return PKV_ERR_CUDA;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
