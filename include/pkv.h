@@ -119,6 +119,47 @@ int pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cach
                           void *stream);
 
 /*
+ * pkv_paged_decode_attn_ex -- pkv_paged_decode_attn with every argument in
+ * one struct, plus the options the positional form does not have.
+ *
+ * window: 0 = full causal attention (exactly pkv_paged_decode_attn).  W > 0
+ *   is sliding-window (local) attention: query token i, at position
+ *   pos = context_lens[b] - q_len + i, sees only positions pos - W + 1 .. pos,
+ *   its own and the W - 1 before it (CS336 lecture-10 notes, Local attention &
+ *   sparse variants).  KV blocks that no row of a sequence can see are not
+ *   read, so a step costs about min(ctx, W + q_len) tokens per sequence.  The
+ *   cache itself is unchanged: the caller may keep or release blocks that
+ *   have left every window.  W >= max_blocks_per_seq * block_size is the same
+ *   as 0.  W < 0 returns PKV_ERR_INVALID_ARG.
+ * Every other field, the layouts and the return codes are those of
+ * pkv_paged_decode_attn.  `p` is read during the call only.
+ */
+typedef struct pkv_attn_params {
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    int num_seqs;
+    int q_len;
+    int n_q;
+    int n_kv;
+    int head_dim;
+    int block_size;
+    int max_blocks_per_seq;
+    int num_blocks;
+    float scale;
+    void *out;
+    int out_dtype;
+    void *workspace;
+    size_t workspace_bytes;
+    unsigned flags;
+    int window;
+} pkv_attn_params;
+
+int pkv_paged_decode_attn_ex(const pkv_attn_params *p, void *stream);
+
+/*
  * Bytes of workspace pkv_paged_decode_attn needs for these sizes on the
  * current device (the split-K partials of at most two pieces per CTA plus
  * an error word).  max_context_len is accepted for interface stability and

@@ -64,7 +64,7 @@ class Oracle:
         f64p = ctypes.POINTER(ctypes.c_double)
         c_int = ctypes.c_int
         lib.oracle_paged_attn.argtypes = [u16p, u16p, u16p, i32p, i32p] + [c_int] * 8 + \
-            [ctypes.c_double, f64p]
+            [ctypes.c_double, c_int, f64p]
         lib.oracle_paged_attn.restype = c_int
         lib.oracle_attn_partial.argtypes = [u16p, u16p, u16p, i32p, i32p] + [c_int] * 8 + \
             [ctypes.c_double, c_int, c_int, f64p, f64p, f64p]
@@ -83,8 +83,11 @@ class Oracle:
 
     # -- attention ---------------------------------------------------------
     def paged_attn(self, q, k_cache, v_cache, block_tables, context_lens, *, n_q, n_kv,
-                   head_dim, block_size, scale, num_blocks=None, q_len=None):
-        """fp64 output [num_seqs, q_len, n_q, head_dim]; raises on invalid tables."""
+                   head_dim, block_size, scale, num_blocks=None, q_len=None, window=0):
+        """fp64 output [num_seqs, q_len, n_q, head_dim]; raises on invalid tables.
+
+        window: 0 for full causal attention, W > 0 to see only the last W positions.
+        """
         q = np.ascontiguousarray(q, dtype=np.uint16)
         k_cache = np.ascontiguousarray(k_cache, dtype=np.uint16)
         v_cache = np.ascontiguousarray(v_cache, dtype=np.uint16)
@@ -101,7 +104,7 @@ class Oracle:
             _ptr(q, ctypes.c_uint16), _ptr(k_cache, ctypes.c_uint16),
             _ptr(v_cache, ctypes.c_uint16), _ptr(bt, ctypes.c_int32), _ptr(cl, ctypes.c_int32),
             num_seqs, q_len, n_q, n_kv, head_dim, block_size, max_blocks, num_blocks,
-            float(scale), _ptr(out, ctypes.c_double))
+            float(scale), int(window), _ptr(out, ctypes.c_double))
         if st != 0:
             raise ValueError(f"oracle_paged_attn rejected its inputs (status {st})")
         return out

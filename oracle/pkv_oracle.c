@@ -33,6 +33,9 @@
  *     ones, and new token i sits at position ctx - q_len + i, seeing keys at
  *     positions <= its own (the causal mask);
  *   - a row that sees no key (ctx == 0, or ctx < q_len) outputs zeros;
+ *   - sliding window W > 0: the query at position pos sees only positions
+ *     pos - W + 1 .. pos (its own and the W - 1 before it; CS336 lecture-10
+ *     notes, Local attention & sparse variants); W = 0 means no window;
  *   - the softmax is evaluated as max, then sum of exp(s - max): subtracting
  *     the row maximum leaves softmax unchanged and keeps exp finite.
  *
@@ -93,17 +96,20 @@ static int gather_sequence(const uint16_t *k_cache, const uint16_t *v_cache,
 
 /*
  * out[b][i][h][:] for all b, query tokens i, query heads h (fp64).
- * q: [num_seqs][q_len][n_q][head_dim] bf16 bits.  Returns 0 on success,
- * 1 on bad shape arguments, 2 if a block table or context length is invalid.
+ * q: [num_seqs][q_len][n_q][head_dim] bf16 bits.  window: 0 for full causal
+ * attention, W > 0 for a sliding window of W positions.  Returns 0 on
+ * success, 1 on bad shape arguments, 2 if a block table or context length is
+ * invalid.
  */
 int oracle_paged_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                       const int32_t *block_tables, const int32_t *context_lens,
                       int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
                       int block_size, int max_blocks_per_seq, int num_blocks,
-                      double scale, double *out)
+                      double scale, int window, double *out)
 {
     if (num_seqs < 0 || q_len < 1 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 ||
-        head_dim < 1 || block_size < 1 || max_blocks_per_seq < 0 || num_blocks < 0)
+        head_dim < 1 || block_size < 1 || max_blocks_per_seq < 0 || num_blocks < 0 ||
+        window < 0)
         return 1;
     const int G = n_q / n_kv;
     int status = 0;
@@ -128,22 +134,25 @@ int oracle_paged_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t
             status = 2;
         } else {
             for (int i = 0; i < q_len; ++i) {
-                /* New token i sits at position ctx - q_len + i and sees keys 0..pos. */
+                /* New token i sits at position ctx - q_len + i and sees keys
+                 * first..pos (first = 0, or pos - window + 1 with a window). */
                 const long pos = (long)ctx - q_len + i;
                 const int nvis = pos < 0 ? 0 : (int)(pos + 1 < ctx ? pos + 1 : ctx);
+                const long first_l = window > 0 ? pos - window + 1 : 0;
+                const int first = first_l < 0 ? 0 : (int)first_l;
                 for (int h = g * G; h < (g + 1) * G; ++h) {
                     const uint16_t *qrow = q + (((size_t)b * q_len + i) * n_q + h) * head_dim;
                     double *orow = out + (((size_t)b * q_len + i) * n_q + h) * head_dim;
                     for (int e = 0; e < head_dim; ++e)
                         acc[e] = 0.0;
-                    if (nvis == 0) {
+                    if (nvis <= first) {
                         for (int e = 0; e < head_dim; ++e)
                             orow[e] = 0.0;
                         continue;
                     }
                     /* scores s_t = scale * q . K_t */
                     double mx = -INFINITY;
-                    for (int t = 0; t < nvis; ++t) {
+                    for (int t = first; t < nvis; ++t) {
                         double dot = 0.0;
                         for (int e = 0; e < head_dim; ++e)
                             dot += bf16_value(qrow[e]) * K[(size_t)t * head_dim + e];
@@ -153,7 +162,7 @@ int oracle_paged_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t
                     }
                     /* softmax weights and the weighted sum of values */
                     double denom = 0.0;
-                    for (int t = 0; t < nvis; ++t) {
+                    for (int t = first; t < nvis; ++t) {
                         double w = exp(s[t] - mx);
                         denom += w;
                         for (int e = 0; e < head_dim; ++e)

@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     pkv_check_error, pkv_copy_blocks, pkv_kv_append, pkv_pool_alloc, pkv_pool_append_slots,
     pkv_pool_create, pkv_pool_destroy, pkv_pool_num_free, pkv_pool_refcount, pkv_pool_release,
     pkv_pool_share,
-    pkv_kv_bytes, pkv_paged_decode_attn, pkv_paged_decode_attn_noalloc,
+    pkv_kv_bytes, pkv_paged_decode_attn, pkv_paged_decode_attn_ex, pkv_paged_decode_attn_noalloc,
+    pkv_attn_params,
     pkv_paged_decode_attn_workspace_size,
     pkv_status_string, pkv_version)

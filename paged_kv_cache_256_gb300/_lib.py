@@ -33,12 +33,27 @@ def PKV_FLAG_GRID(n: int) -> int:
     return (int(n) & 0xFFFF) << PKV_FLAG_GRID_SHIFT
 
 
+class pkv_attn_params(ctypes.Structure):
+    """The struct of include/pkv.h, field for field."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("block_tables", ctypes.c_void_p), ("context_lens", ctypes.c_void_p),
+        ("num_seqs", ctypes.c_int), ("q_len", ctypes.c_int), ("n_q", ctypes.c_int),
+        ("n_kv", ctypes.c_int), ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
+        ("max_blocks_per_seq", ctypes.c_int), ("num_blocks", ctypes.c_int),
+        ("scale", ctypes.c_float), ("out", ctypes.c_void_p), ("out_dtype", ctypes.c_int),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("flags", ctypes.c_uint), ("window", ctypes.c_int),
+    ]
+
+
 # Every symbol include/pkv.h declares, with its ctypes signature.
 _c_int, _c_float, _c_size = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _vp, _i32p = ctypes.c_void_p, ctypes.c_void_p
 SIGNATURES = {
     "pkv_paged_decode_attn": ([_vp, _vp, _vp, _i32p, _i32p] + [_c_int] * 8 +
                               [_c_float, _vp, _c_int, _vp, _c_size, ctypes.c_uint, _vp], _c_int),
+    "pkv_paged_decode_attn_ex": ([ctypes.POINTER(pkv_attn_params), _vp], _c_int),
     "pkv_paged_decode_attn_workspace_size": ([_c_int] * 7 + [ctypes.c_uint], _c_size),
     "pkv_paged_decode_attn_noalloc": ([_vp, _vp, _vp, _i32p, _i32p] + [_c_int] * 8 +
                                       [_c_float, _vp, _c_int, ctypes.c_uint, _vp], _c_int),
@@ -146,14 +161,8 @@ def alloc_workspace(num_seqs, q_len, n_q, n_kv, head_dim, block_size, flags=0, d
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
-                          flags=0, stream=None):
-    """out <- paged decode attention (see include/pkv.h for the full contract).
-
-    q [num_seqs, q_len, n_q, d] bf16; k_cache/v_cache [num_blocks, n_kv, bs, d]
-    bf16; block_tables [num_seqs, max_blocks] int32; context_lens [num_seqs]
-    int32; out like q, bf16 or float32; workspace a uint8 CUDA tensor.
-    """
+def _attn_shapes(q, k_cache, v_cache, block_tables, context_lens, out, workspace):
+    """Checks shared by the attention entry points; returns (dims, out_dtype)."""
     import torch
     _bf16_like(q, "q")
     _bf16_like(k_cache, "k_cache")
@@ -175,12 +184,42 @@ def pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale
         raise TypeError("out must be bfloat16 or float32")
     if not out.is_cuda or not out.is_contiguous() or not workspace.is_cuda:
         raise ValueError("out and workspace must be contiguous CUDA tensors")
+    return (num_seqs, q_len, n_q, n_kv, d, bs, block_tables.shape[1], num_blocks), out_dtype
+
+
+def pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                          flags=0, stream=None):
+    """out <- paged decode attention (see include/pkv.h for the full contract).
+
+    q [num_seqs, q_len, n_q, d] bf16; k_cache/v_cache [num_blocks, n_kv, bs, d]
+    bf16; block_tables [num_seqs, max_blocks] int32; context_lens [num_seqs]
+    int32; out like q, bf16 or float32; workspace a uint8 CUDA tensor.
+    """
+    (num_seqs, q_len, n_q, n_kv, d, bs, max_blocks, num_blocks), out_dtype = _attn_shapes(
+        q, k_cache, v_cache, block_tables, context_lens, out, workspace)
     st = load_library().pkv_paged_decode_attn(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
-        context_lens.data_ptr(), num_seqs, q_len, n_q, n_kv, d, bs, block_tables.shape[1],
+        context_lens.data_ptr(), num_seqs, q_len, n_q, n_kv, d, bs, max_blocks,
         num_blocks, float(scale), out.data_ptr(), out_dtype, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), int(flags), _stream_ptr(stream))
     _check(st, "pkv_paged_decode_attn")
+
+
+def pkv_paged_decode_attn_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                             workspace, flags=0, stream=None, window=0):
+    """pkv_paged_decode_attn through the parameter struct; window > 0 = sliding window."""
+    (num_seqs, q_len, n_q, n_kv, d, bs, max_blocks, num_blocks), out_dtype = _attn_shapes(
+        q, k_cache, v_cache, block_tables, context_lens, out, workspace)
+    p = pkv_attn_params(
+        q=q.data_ptr(), k_cache=k_cache.data_ptr(), v_cache=v_cache.data_ptr(),
+        block_tables=block_tables.data_ptr(), context_lens=context_lens.data_ptr(),
+        num_seqs=num_seqs, q_len=q_len, n_q=n_q, n_kv=n_kv, head_dim=d, block_size=bs,
+        max_blocks_per_seq=max_blocks, num_blocks=num_blocks, scale=float(scale),
+        out=out.data_ptr(), out_dtype=out_dtype, workspace=workspace.data_ptr(),
+        workspace_bytes=workspace.numel() * workspace.element_size(), flags=int(flags),
+        window=int(window))
+    st = load_library().pkv_paged_decode_attn_ex(ctypes.byref(p), _stream_ptr(stream))
+    _check(st, "pkv_paged_decode_attn_ex")
 
 
 def pkv_paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, out,

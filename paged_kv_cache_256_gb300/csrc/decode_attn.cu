@@ -2,7 +2,9 @@
 //
 // What it computes: for every sequence b, new query token i and query head h,
 //   out = softmax_t(scale * q . K_t) V_t over the logical positions t the
-//   causal mask allows (t <= ctx - q_len + i), with K_t, V_t found through
+//   causal mask allows (t <= pos = ctx - q_len + i; with a sliding window of
+//   W positions also t > pos - W: CS336 lecture-10 notes, Local attention &
+//   sparse variants), with K_t, V_t found through
 //   the block table (PagedAttention: "Inference Engines", The Breakthrough;
 //   CS336 lecture-10 notes, PagedAttention (vLLM)), and query head h reading
 //   KV head h / (n_q / n_kv) ("Transformer inference mechanics", MHA versus
@@ -117,24 +119,41 @@ __device__ __forceinline__ int unit_blocks(const AttnArgs& a, int s, int bs) {
     return (unit_ctx(a, s, bs) + bs - 1) / bs;
 }
 
-// Position in the flat work list: sequence s, KV head h, block j of that unit,
-// `left` items still to process in this CTA's slice.
+// First block any row of a unit can see: with a sliding window, the earliest
+// row (position ctx - q_len) sees nothing before ctx - q_len - W + 1, so the
+// blocks before that one are never read.  Always < the unit's block count.
+__device__ __forceinline__ int unit_first_block(const AttnArgs& a, int ctx, int bs) {
+    if (a.window <= 0) return 0;
+    const long long lo = (long long)ctx - a.q_len - a.window + 1;
+    return lo > 0 ? static_cast<int>(lo / bs) : 0;
+}
+
+// Work items (blocks to read) of the units of sequence s: one per KV head each.
+__device__ __forceinline__ int unit_items(const AttnArgs& a, int s, int bs) {
+    const int ctx = unit_ctx(a, s, bs);
+    return (ctx + bs - 1) / bs - unit_first_block(a, ctx, bs);
+}
+
+// Position in the flat work list: sequence s, KV head h, block j of that unit
+// (the unit reads blocks jlo .. nb-1), `left` items still to process in this
+// CTA's slice.
 struct Walk {
-    int s, h, j, nb, ctx;
+    int s, h, j, jlo, nb, ctx;
     long long left;
 };
 
 template <int BS>
 __device__ __forceinline__ void walk_next_unit(const AttnArgs& a, Walk& w) {
-    w.j = 0;
     if (++w.h == a.n_kv) {
         w.h = 0;
         do {
             ++w.s;
             w.nb = w.s < a.num_seqs ? unit_blocks(a, w.s, BS) : 1;
         } while (w.nb == 0);
-        w.ctx = unit_ctx(a, w.s, BS);
+        w.ctx = w.s < a.num_seqs ? unit_ctx(a, w.s, BS) : 0;
+        w.jlo = unit_first_block(a, w.ctx, BS);
     }
+    w.j = w.jlo;
 }
 
 __device__ __forceinline__ int piece_end(const Walk& w) {
@@ -171,7 +190,7 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
                                            long long* s_start) {
     const int tid = threadIdx.x, cta = blockIdx.x, grid = gridDim.x;
     long long mine = 0;
-    for (int s = tid; s < a.num_seqs; s += kThreads) mine += unit_blocks(a, s, BS);
+    for (int s = tid; s < a.num_seqs; s += kThreads) mine += unit_items(a, s, BS);
     long long total_blocks;
     (void)block_inclusive_scan(mine, s_red, total_blocks);
     const long long W = total_blocks * a.n_kv;
@@ -181,7 +200,7 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
         long long base = 0;
         for (int s0 = 0; s0 < a.num_seqs; s0 += kThreads) {
             const int s = s0 + tid;
-            const long long v = s < a.num_seqs ? (long long)unit_blocks(a, s, BS) * a.n_kv : 0;
+            const long long v = s < a.num_seqs ? (long long)unit_items(a, s, BS) * a.n_kv : 0;
             long long chunk;
             const long long incl = block_inclusive_scan(v, s_red, chunk);
             const long long excl = incl - v;
@@ -201,10 +220,12 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
         w.s = static_cast<int>(s_start[0]);
         w.nb = unit_blocks(a, w.s, BS);
         w.ctx = unit_ctx(a, w.s, BS);
-        w.h = static_cast<int>(s_start[1] / w.nb);
-        w.j = static_cast<int>(s_start[1] % w.nb);
+        w.jlo = unit_first_block(a, w.ctx, BS);
+        const int items = w.nb - w.jlo;
+        w.h = static_cast<int>(s_start[1] / items);
+        w.j = w.jlo + static_cast<int>(s_start[1] % items);
     } else {
-        w.s = w.h = w.j = w.nb = w.ctx = 0;
+        w.s = w.h = w.j = w.jlo = w.nb = w.ctx = 0;
     }
     return w;
 }
@@ -361,13 +382,17 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                 qb[kk][1] = valid ? __ldg(qrow + kk * 8 + 4 + t) : 0u;
             }
         }
-        int lim[2];
+        // Row r sees tokens lo..lim: lim = its position, lo = lim - W + 1
+        // with a window (INT_MIN without); padding rows see nothing.
+        int lim[2], lo[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int r = 2 * t + e;
             lim[e] = r < R ? ctx - a.q_len + r / G : -1;
+            lo[e] = a.window > 0 ? lim[e] - a.window + 1 : INT_MIN;
         }
         const int lim_min = ctx - a.q_len;
+        const int lo_max = a.window > 0 ? ctx - a.window : INT_MIN;  // largest lo of a real row
 
         float o[MT][4];
 #pragma unroll
@@ -404,17 +429,17 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                     }
                 }
 
-                // ---- scale, causal / tail mask, online softmax (base 2)
+                // ---- scale, causal / window / tail mask, online softmax (base 2)
                 const int tok0 = j * BS;
-                const bool need_mask = tok0 + BS - 1 > lim_min;
+                const bool need_mask = tok0 + BS - 1 > lim_min || tok0 < lo_max;
                 float mloc[2] = {-INFINITY, -INFINITY};
 #pragma unroll
                 for (int tp = 0; tp < PT; ++tp) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float x = (st[tp][e] + st2[tp][e]) * a.scale_log2;
-                        if (need_mask && tok0 + tp * 16 + g + (e >> 1) * 8 > lim[e & 1])
-                            x = -INFINITY;
+                        const int tk = tok0 + tp * 16 + g + (e >> 1) * 8;
+                        if (need_mask && (tk > lim[e & 1] || tk < lo[e & 1])) x = -INFINITY;
                         st[tp][e] = x;
                         mloc[e & 1] = fmaxf(mloc[e & 1], x);
                     }
@@ -534,7 +559,7 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
         }
 
         // ---- emit (warp 0): through a row-major tile, then 16-byte stores
-        const bool first_piece = j0 == 0, last_piece = j1 == w.nb;
+        const bool first_piece = j0 == w.jlo, last_piece = j1 == w.nb;
         const bool whole = first_piece && last_piece;
         if (warp == 0) {
             float scl[2];
@@ -631,7 +656,7 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 
         // Query fragments of this unit's two rows per thread (rows >= a.rows are zero).
         uint32_t qf[KT][4];
-        int lim[2];
+        int lim[2], lo[2];  // row sees tokens lo..lim (lo = INT_MIN without a window)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int r = mt * 16 + g + hh * 8;
@@ -639,6 +664,7 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
             const int i = valid ? r / G : 0;
             const int hq = h * G + (valid ? r % G : 0);
             lim[hh] = valid ? ctx - a.q_len + i : -1;
+            lo[hh] = a.window > 0 ? lim[hh] - a.window + 1 : INT_MIN;
             const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
                 a.q + (((size_t)s * a.q_len + i) * a.n_q + hq) * D);
 #pragma unroll
@@ -648,6 +674,7 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
             }
         }
         const int lim_min = ctx - a.q_len;  // smallest causal limit of a real row
+        const int lo_max = a.window > 0 ? ctx - a.window : INT_MIN;  // largest lower limit
 
         float o[NT][4];
 #pragma unroll
@@ -681,17 +708,17 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                         mma_bf16_16816(sc[1], qf[kk], b[2], b[3]);
                     }
 
-                    // ---- scale, causal / tail mask, online softmax (base 2)
+                    // ---- scale, causal / window / tail mask, online softmax (base 2)
                     const int tok0 = j * BS + tp * 16;
-                    const bool need_mask = tok0 + 15 > lim_min;
+                    const bool need_mask = tok0 + 15 > lim_min || tok0 < lo_max;
                     float mloc[2] = {-INFINITY, -INFINITY};
 #pragma unroll
                     for (int n = 0; n < 2; ++n) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             float x = sc[n][e] * a.scale_log2;
-                            if (need_mask && tok0 + n * 8 + 2 * t + (e & 1) > lim[e >> 1])
-                                x = -INFINITY;
+                            const int tk = tok0 + n * 8 + 2 * t + (e & 1);
+                            if (need_mask && (tk > lim[e >> 1] || tk < lo[e >> 1])) x = -INFINITY;
                             sc[n][e] = x;
                             mloc[e >> 1] = fmaxf(mloc[e >> 1], x);
                         }
@@ -807,7 +834,7 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
         }
 
         // ---- emit: a whole unit goes straight to `out`; a piece becomes a record
-        const bool first_piece = j0 == 0, last_piece = j1 == w.nb;
+        const bool first_piece = j0 == w.jlo, last_piece = j1 == w.nb;
         if (col == 0) {
             if (first_piece && last_piece) {
 #pragma unroll
@@ -920,7 +947,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     while (w.left > 0) {
         const int j0 = w.j, j1 = piece_end(w), n = j1 - j0;
         const int ctx = w.ctx, s = w.s, h = w.h;
-        int lim = -1, i_row = 0, hq_row = 0;
+        int lim = -1, lo = INT_MIN, i_row = 0, hq_row = 0;
         if (softmax) {
             // This unit's query rows into the swizzled Q tile (the previous
             // unit's score products finished: each of them was waited for).
@@ -928,6 +955,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             i_row = valid ? row / G : 0;
             hq_row = h * G + (valid ? row % G : 0);
             lim = valid ? ctx - a.q_len + i_row : -1;
+            if (a.window > 0) lo = lim - a.window + 1;
             const uint4* qrow = reinterpret_cast<const uint4*>(
                 a.q + (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D);
             uint4 qv[D / 8];
@@ -1003,6 +1031,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             // ===================== softmax (thread = row) =====================
             float m_used = -INFINITY, l = 0.f;
             const int lim_min = ctx - a.q_len;
+            const int lo_max = a.window > 0 ? ctx - a.window : INT_MIN;
             for (int b = 0; b < n; ++b) {
                 const uint32_t g = gbase + b;
                 ok = consumer_wait(a, &s_full[g & 1u], (g >> 1) & 1u, ok, s_abort);
@@ -1023,10 +1052,10 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 }
                 const int tok0 = (j0 + b) * BS;
                 float mloc = -INFINITY;
-                if (tok0 + BS - 1 > lim_min) {
+                if (tok0 + BS - 1 > lim_min || tok0 < lo_max) {
 #pragma unroll
                     for (int c = 0; c < BS; ++c)
-                        if (tok0 + c > lim) x[c] = -INFINITY;
+                        if (tok0 + c > lim || tok0 + c < lo) x[c] = -INFINITY;
                 }
 #pragma unroll
                 for (int c = 0; c < BS; ++c) mloc = fmaxf(mloc, x[c]);
@@ -1106,7 +1135,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 ok = consumer_wait(a, &pv_done[gl & 1u], (gl >> 1) & 1u, ok, s_abort);
             }
             tc_fence_after();
-            const bool first_piece = j0 == 0, last_piece = j1 == w.nb;
+            const bool first_piece = j0 == w.jlo, last_piece = j1 == w.nb;
             const bool whole = first_piece && last_piece;
             if (ok) {
                 const float scl = whole ? (l > 0.f ? 1.f / l : 0.f) : 1.f;

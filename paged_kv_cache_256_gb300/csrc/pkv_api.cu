@@ -181,11 +181,50 @@ int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cach
                           int block_size, int max_blocks_per_seq, int num_blocks, float scale,
                           void* out, int out_dtype, void* workspace, size_t workspace_bytes,
                           unsigned flags, void* stream) {
+    pkv_attn_params p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.num_seqs = num_seqs;
+    p.q_len = q_len;
+    p.n_q = n_q;
+    p.n_kv = n_kv;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.scale = scale;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.workspace = workspace;
+    p.workspace_bytes = workspace_bytes;
+    p.flags = flags;
+    p.window = 0;
+    return pkv_paged_decode_attn_ex(&p, stream);
+}
+
+int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
+    if (!p) return PKV_ERR_INVALID_ARG;
+    const void *q = p->q, *k_cache = p->k_cache, *v_cache = p->v_cache;
+    const int32_t *block_tables = p->block_tables, *context_lens = p->context_lens;
+    const int num_seqs = p->num_seqs, q_len = p->q_len, n_q = p->n_q, n_kv = p->n_kv;
+    const int head_dim = p->head_dim, block_size = p->block_size;
+    const int max_blocks_per_seq = p->max_blocks_per_seq, num_blocks = p->num_blocks;
+    const float scale = p->scale;
+    void* out = p->out;
+    const int out_dtype = p->out_dtype;
+    void* workspace = p->workspace;
+    const size_t workspace_bytes = p->workspace_bytes;
+    const unsigned flags = p->flags;
     int st = check_shape(num_seqs, q_len, n_q, n_kv, head_dim, block_size);
     if (st != PKV_OK) return st;
     if (out_dtype != PKV_OUT_BF16 && out_dtype != PKV_OUT_F32) return PKV_ERR_INVALID_ARG;
     if (max_blocks_per_seq < 1 || num_blocks < 1) return PKV_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (p->window < 0) return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
         return PKV_ERR_INVALID_ARG;
@@ -235,6 +274,8 @@ int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cach
     a.num_blocks = num_blocks;
     a.tile_rows_total = (int)rows_total;
     a.warp_rows = warp_rows_for(rows);
+    // A window at least as wide as any context is no window.
+    a.window = (long long)p->window >= (long long)max_blocks_per_seq * block_size ? 0 : p->window;
     a.checked = (flags & PKV_FLAG_CHECKED) ? 1 : 0;
     a.test_stall = (flags & PKV_FLAG_TEST_STALL) ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;

@@ -35,6 +35,7 @@ struct AttnArgs {
     int num_blocks;
     int tile_rows_total;  // num_blocks * n_kv * block_size (rows of the 2-D cache view)
     int warp_rows;        // 16-row tiles per KV unit (1, 2, 4 or 8)
+    int window;        // 0: full causal attention; W > 0: a row sees its last W positions
     int checked;
     int test_stall;    // failure-path tests: the producer issues nothing
     float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain

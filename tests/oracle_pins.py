@@ -90,13 +90,13 @@ def _case(rng, ctxs, n_q, n_kv, d, bs, q_len, kscale=1.0):
                 head_dim=d, block_size=bs, q_len=q_len)
 
 
-def _run(orc, c, scale, **over):
+def _run(orc, c, scale, window=0, **over):
     args = dict(c)
     args.update(over)
     return orc.paged_attn(args["q"], args["k_cache"], args["v_cache"], args["block_tables"],
                           args["context_lens"], n_q=args["n_q"], n_kv=args["n_kv"],
                           head_dim=args["head_dim"], block_size=args["block_size"],
-                          scale=scale)
+                          scale=scale, window=window)
 
 
 SHAPES = [
@@ -247,6 +247,49 @@ def pin_causal_rows(orc):
             assert np.array_equal(full[:, i:i + 1], one), i
 
 
+WINDOWS = [1, 3, 4, 5, 17]
+
+
+def pin_window_sdpa(orc):
+    """Sliding window: torch SDPA with a banded causal mask (CS336 notes, Local attention)."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(23)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        G = n_q // n_kv
+        for W in WINDOWS:
+            got = _run(orc, c, 0.3, window=W)
+            for b, ctx in enumerate(ctxs):
+                q = torch.from_numpy(bf16_bits_to_f32(c["q"][b]).astype(np.float64))
+                k = torch.from_numpy(bf16_bits_to_f32(c["K"][b]).astype(np.float64))
+                v = torch.from_numpy(bf16_bits_to_f32(c["V"][b]).astype(np.float64))
+                k, v = k.repeat_interleave(G, dim=0), v.repeat_interleave(G, dim=0)
+                pos = ctx - q_len + torch.arange(q_len)
+                t = torch.arange(ctx)[None, :]
+                mask = (t <= pos[:, None]) & (t > pos[:, None] - W)
+                ref = F.scaled_dot_product_attention(q.permute(1, 0, 2)[None], k[None], v[None],
+                                                     attn_mask=mask[None, None], scale=0.3)[0]
+                np.testing.assert_allclose(got[b], ref.permute(1, 0, 2).numpy(), rtol=1e-12,
+                                           atol=1e-12)
+
+
+def pin_window_extremes(orc):
+    """A window at least as long as the context is no window; a window of 1 is the own V."""
+    rng = np.random.default_rng(24)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        assert np.array_equal(_run(orc, c, 0.3), _run(orc, c, 0.3, window=max(ctxs) + 5))
+        one = _run(orc, c, 0.3, window=1)
+        G = n_q // n_kv
+        for b, ctx in enumerate(ctxs):
+            for i in range(q_len):
+                pos = ctx - q_len + i
+                for h in range(n_q):
+                    want = bf16_bits_to_f32(c["V"][b][h // G][pos]).astype(np.float64)
+                    assert np.array_equal(one[b, i, h], want), (b, i, h)
+
+
 def pin_empty_context(orc):
     rng = np.random.default_rng(19)
     c = _case(rng, [0, 5, 0], 4, 2, 8, 4, 1)
@@ -374,7 +417,8 @@ def pin_gqa_ratio(orc):
 
 ALL_PINS = [
     pin_library_sdpa, pin_numpy_dense, pin_equal_scores_mean, pin_single_token, pin_hardmax,
-    pin_block_permutation, pin_gqa_equals_repeated_mha, pin_causal_rows, pin_empty_context,
+    pin_block_permutation, pin_gqa_equals_repeated_mha, pin_causal_rows, pin_window_sdpa,
+    pin_window_extremes, pin_empty_context,
     pin_merge_exact, pin_kv_append, pin_copy_blocks, pin_append_then_attend, pin_kv_bytes_golden,
     pin_gqa_ratio,
 ]

@@ -150,3 +150,48 @@ def test_product_sources_do_not_reach_the_oracle():
         text = open(f).read()
         for pat in (r"^\s*(from|import)\s+oracle\b", r"\boracle_\w+\s*\(", r"pkv_oracle"):
             assert not re.search(pat, text, flags=re.M), (f, pat)
+
+
+def test_params_struct_layout_matches_header(tmp_path):
+    """The ctypes mirror of pkv_attn_params has the C compiler's size and offsets."""
+    fields = [f for f, _ in _lib.pkv_attn_params._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "pkv.h"\nint main(void) {\n'
+        '  printf("%zu\\n", sizeof(pkv_attn_params));\n' +
+        "".join(f'  printf("%zu\\n", offsetof(pkv_attn_params, {f}));\n' for f in fields) +
+        "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(_lib.pkv_attn_params)
+    for f, off in zip(fields, got[1:]):
+        assert getattr(_lib.pkv_attn_params, f).offset == off, f
+
+
+def _params(**over):
+    p = _lib.pkv_attn_params(q=FAKE, k_cache=FAKE, v_cache=FAKE, block_tables=FAKE,
+                             context_lens=FAKE, num_seqs=0, q_len=1, n_q=4, n_kv=2, head_dim=64,
+                             block_size=16, max_blocks_per_seq=3, num_blocks=8, scale=0.125,
+                             out=FAKE, out_dtype=0, workspace=FAKE, workspace_bytes=1 << 20,
+                             flags=0, window=0)
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_params_entry_host_checks(lib):
+    assert lib.pkv_paged_decode_attn_ex(None, None) == _lib.PKV_ERR_INVALID_ARG
+    # num_seqs == 0 is accepted without touching a device ...
+    assert lib.pkv_paged_decode_attn_ex(ctypes.byref(_params()), None) == _lib.PKV_OK
+    assert lib.pkv_paged_decode_attn_ex(ctypes.byref(_params(window=5)), None) == _lib.PKV_OK
+    # ... after every argument check, so a bad window or shape is still refused.
+    assert lib.pkv_paged_decode_attn_ex(ctypes.byref(_params(window=-1)),
+                                        None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_paged_decode_attn_ex(ctypes.byref(_params(n_q=3)),
+                                        None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_paged_decode_attn_ex(ctypes.byref(_params(head_dim=96)),
+                                        None) == _lib.PKV_ERR_UNSUPPORTED

@@ -40,6 +40,8 @@ MUTANTS = {
     "merge_no_rescale": ("double w = exp(m[(size_t)s * rows + r] - M);", "double w = 1.0;"),
     "merge_denominator_unweighted": ("denom += w * ls;", "denom += ls;"),
     "partial_max_not_reported": ("m[row] = mx;", "m[row] = 0.0;"),
+    "window_one_too_wide": ("const long first_l = window > 0 ? pos - window + 1 : 0;",
+                            "const long first_l = window > 0 ? pos - window : 0;"),
     "copy_direction_swapped": ("memcpy(k_cache + (size_t)dst * per_block, k_cache + (size_t)src * per_block,",
                                "memcpy(k_cache + (size_t)src * per_block, k_cache + (size_t)dst * per_block,"),
 }
