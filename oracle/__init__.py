@@ -12,7 +12,10 @@ Functions (each follows the passage cited in ``pkv_oracle.c``):
   K/V gathered through the block table, GQA group map h -> h // (n_q/n_kv).
 * :func:`attn_partial` -- (o, m, l) of one key range: the online-softmax state.
 * :func:`lse_merge`    -- exact combination of partials.
+* :func:`paged_attn_fp8` -- the same attention over an e4m3 cache with per-KV-head scales.
 * :func:`kv_append`    -- bit copy of new K/V rows into their slots.
+* :func:`kv_append_fp8` -- quantising append into an e4m3 cache.
+* :func:`e4m3_encode`, :func:`e4m3_decode` -- the 8-bit float codec.
 * :func:`copy_blocks`  -- whole-block copies (copy-on-write).
 * :func:`kv_bytes`     -- M_kv = 2 L n_kv d_h (s b) p.
 """
@@ -66,6 +69,18 @@ class Oracle:
         lib.oracle_paged_attn.argtypes = [u16p, u16p, u16p, i32p, i32p] + [c_int] * 8 + \
             [ctypes.c_double, c_int, f64p]
         lib.oracle_paged_attn.restype = c_int
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_paged_attn_fp8.argtypes = [u16p, u8p, u8p, f32p, f32p, i32p, i32p] + \
+            [c_int] * 8 + [ctypes.c_double, c_int, f64p]
+        lib.oracle_paged_attn_fp8.restype = c_int
+        lib.oracle_kv_append_fp8.argtypes = [u16p, u16p, i32p] + [c_int] * 5 + \
+            [f32p, f32p, u8p, u8p]
+        lib.oracle_kv_append_fp8.restype = c_int
+        lib.oracle_e4m3_encode.argtypes = [f32p, ctypes.c_long, u8p]
+        lib.oracle_e4m3_encode.restype = None
+        lib.oracle_e4m3_decode.argtypes = [u8p, ctypes.c_long, f64p]
+        lib.oracle_e4m3_decode.restype = None
         lib.oracle_attn_partial.argtypes = [u16p, u16p, u16p, i32p, i32p] + [c_int] * 8 + \
             [ctypes.c_double, c_int, c_int, f64p, f64p, f64p]
         lib.oracle_attn_partial.restype = c_int
@@ -108,6 +123,46 @@ class Oracle:
         if st != 0:
             raise ValueError(f"oracle_paged_attn rejected its inputs (status {st})")
         return out
+
+    def paged_attn_fp8(self, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                       *, n_q, n_kv, head_dim, block_size, scale, num_blocks=None, q_len=None,
+                       window=0):
+        """paged_attn over e4m3 caches (uint8 codes) with fp32 per-KV-head scales [n_kv]."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        k_cache = np.ascontiguousarray(k_cache, dtype=np.uint8)
+        v_cache = np.ascontiguousarray(v_cache, dtype=np.uint8)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        assert ks.shape == (n_kv,) and vs.shape == (n_kv,)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        num_seqs = cl.shape[0]
+        q_len = q.shape[1] if q_len is None else q_len
+        if num_blocks is None:
+            num_blocks = k_cache.shape[0]
+        out = np.zeros((num_seqs, q_len, n_q, head_dim), dtype=np.float64)
+        st = self._lib.oracle_paged_attn_fp8(
+            _ptr(q, ctypes.c_uint16), _ptr(k_cache, ctypes.c_uint8), _ptr(v_cache, ctypes.c_uint8),
+            _ptr(ks, ctypes.c_float), _ptr(vs, ctypes.c_float), _ptr(bt, ctypes.c_int32),
+            _ptr(cl, ctypes.c_int32), num_seqs, q_len, n_q, n_kv, head_dim, block_size,
+            bt.shape[1], num_blocks, float(scale), int(window), _ptr(out, ctypes.c_double))
+        if st != 0:
+            raise ValueError(f"oracle_paged_attn_fp8 rejected its inputs (status {st})")
+        return out
+
+    def e4m3_encode(self, x):
+        """fp32 values -> e4m3 codes (nearest, ties to even, saturating at 448)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        codes = np.zeros(x.shape, dtype=np.uint8)
+        self._lib.oracle_e4m3_encode(_ptr(x, ctypes.c_float), x.size, _ptr(codes, ctypes.c_uint8))
+        return codes
+
+    def e4m3_decode(self, codes):
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        x = np.zeros(codes.shape, dtype=np.float64)
+        self._lib.oracle_e4m3_decode(_ptr(codes, ctypes.c_uint8), codes.size,
+                                     _ptr(x, ctypes.c_double))
+        return x
 
     def attn_partial(self, q, k_cache, v_cache, block_tables, context_lens, *, n_q, n_kv,
                      head_dim, block_size, scale, t_begin, t_end, num_blocks=None):
@@ -161,6 +216,25 @@ class Oracle:
             _ptr(k_cache, ctypes.c_uint16), _ptr(v_cache, ctypes.c_uint16))
         if st != 0:
             raise ValueError(f"oracle_kv_append rejected its inputs (status {st})")
+
+    def kv_append_fp8(self, k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, *,
+                      block_size):
+        """In-place quantising scatter into e4m3 caches (numpy uint8 arrays)."""
+        k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+        v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int32)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+        num_blocks, n_kv, bs, d = k_cache.shape
+        assert bs == block_size and ks.shape == (n_kv,) and vs.shape == (n_kv,)
+        st = self._lib.oracle_kv_append_fp8(
+            _ptr(k_new, ctypes.c_uint16), _ptr(v_new, ctypes.c_uint16), _ptr(sm, ctypes.c_int32),
+            sm.shape[0], n_kv, d, block_size, num_blocks, _ptr(ks, ctypes.c_float),
+            _ptr(vs, ctypes.c_float), _ptr(k_cache, ctypes.c_uint8), _ptr(v_cache, ctypes.c_uint8))
+        if st != 0:
+            raise ValueError(f"oracle_kv_append_fp8 rejected its inputs (status {st})")
 
     def copy_blocks(self, pairs, k_cache, v_cache):
         """In-place whole-block copies: block pairs[p, 1] <- block pairs[p, 0]."""

@@ -37,7 +37,15 @@
  *     pos - W + 1 .. pos (its own and the W - 1 before it; CS336 lecture-10
  *     notes, Local attention & sparse variants); W = 0 means no window;
  *   - the softmax is evaluated as max, then sum of exp(s - max): subtracting
- *     the row maximum leaves softmax unchanged and keeps exp finite.
+ *     the row maximum leaves softmax unchanged and keeps exp finite;
+ *   - an 8-bit KV cache ("Efficient inference", Quantization: fewer bytes per
+ *     weight -- the KV cache may be stored in low precision, dequantised
+ *     through a scale; CS336 lecture-10 notes, Quantization & pruning:
+ *     bf16 -> fp8) holds e4m3 codes with one scale per KV head for K and one
+ *     for V: the cached value is code_value * scale.  A new value x is stored
+ *     as the e4m3 code nearest to x / scale, the division taken in fp32 and
+ *     ties going to the even code; quotients beyond the largest finite e4m3
+ *     (448) store +-448.
  *
  * Parallelism: one OpenMP loop over independent (sequence, KV head) units.
  * Each unit is computed by one thread, start to finish, in sequential order,
@@ -70,14 +78,77 @@ int oracle_num_threads(void)
 }
 
 /*
+ * e4m3 (the 8-bit float of the OCP FP8 format, E4M3 variant): sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits.  Exponent field 0 holds the
+ * subnormals m/8 * 2^-6; S.1111.111 is NaN; there is no infinity, so the
+ * largest finite magnitude is 1.75 * 2^8 = 448.
+ */
+static double e4m3_value(uint8_t code)
+{
+    const int e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return (code & 0x80) ? -mag : mag;
+}
+
+/*
+ * The e4m3 code nearest to x, ties to the even code, magnitudes that would
+ * round past 448 (infinities included) saturating to 448, NaN to 0x7F.  Codes grow with magnitude
+ * one ulp at a time (code 8 = 2^-6 follows subnormal 7/8 * 2^-6), so with
+ * 2^e <= |x| < 2^(e+1) the code is 8(e + 7) + rint(|x| / 2^(e-3)) - 8, and
+ * below 2^-6 it is rint(|x| * 2^9); rint rounds half to even.
+ */
+static uint8_t e4m3_code(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    long code;
+    if (a >= 448.0) {
+        code = 0x7E; /* the largest finite code, for infinities too */
+    } else if (a < ldexp(1.0, -6)) {
+        code = (long)rint(ldexp(a, 9));
+    } else {
+        int e2;
+        (void)frexp(a, &e2); /* a = f * 2^e2, f in [0.5, 1): 2^(e2-1) <= a < 2^e2 */
+        const int e = e2 - 1;
+        code = 8L * (e + 7) + (long)rint(ldexp(a, 3 - e)) - 8;
+    }
+    return (uint8_t)(sign | code); /* below 448 the code is at most 0x7E */
+}
+
+void oracle_e4m3_encode(const float *x, long n, uint8_t *codes)
+{
+    for (long i = 0; i < n; ++i)
+        codes[i] = e4m3_code(x[i]);
+}
+
+void oracle_e4m3_decode(const uint8_t *codes, long n, double *x)
+{
+    for (long i = 0; i < n; ++i)
+        x[i] = e4m3_value(codes[i]);
+}
+
+/*
+ * A KV cache as the attention reads it: bf16 bit patterns, or e4m3 codes with
+ * one dequantisation scale per KV head (k_scale[g], v_scale[g]).
+ */
+typedef struct {
+    const uint16_t *k16, *v16; /* bf16 cache, or NULL */
+    const uint8_t *k8, *v8;    /* e4m3 cache, or NULL */
+    const float *k_scale, *v_scale;
+} cache_view;
+
+/*
  * Copy sequence b's logical keys and values for KV head g into dense
  * K[ctx][d], V[ctx][d] by walking its block table: logical token t lives in
  * physical block block_tables[b][t / block_size] at offset t % block_size.
  * Returns 0, or -1 if a block index the walk needs is outside [0, num_blocks).
  */
-static int gather_sequence(const uint16_t *k_cache, const uint16_t *v_cache,
-                           const int32_t *table_row, int ctx, int g, int n_kv,
-                           int head_dim, int block_size, int num_blocks,
+static int gather_sequence(const cache_view *c, const int32_t *table_row, int ctx, int g,
+                           int n_kv, int head_dim, int block_size, int num_blocks,
                            double *K, double *V)
 {
     for (int t = 0; t < ctx; ++t) {
@@ -87,8 +158,13 @@ static int gather_sequence(const uint16_t *k_cache, const uint16_t *v_cache,
             return -1;
         size_t base = (((size_t)blk * n_kv + g) * block_size + off) * head_dim;
         for (int e = 0; e < head_dim; ++e) {
-            K[(size_t)t * head_dim + e] = bf16_value(k_cache[base + e]);
-            V[(size_t)t * head_dim + e] = bf16_value(v_cache[base + e]);
+            if (c->k8) {
+                K[(size_t)t * head_dim + e] = e4m3_value(c->k8[base + e]) * (double)c->k_scale[g];
+                V[(size_t)t * head_dim + e] = e4m3_value(c->v8[base + e]) * (double)c->v_scale[g];
+            } else {
+                K[(size_t)t * head_dim + e] = bf16_value(c->k16[base + e]);
+                V[(size_t)t * head_dim + e] = bf16_value(c->v16[base + e]);
+            }
         }
     }
     return 0;
@@ -101,7 +177,7 @@ static int gather_sequence(const uint16_t *k_cache, const uint16_t *v_cache,
  * success, 1 on bad shape arguments, 2 if a block table or context length is
  * invalid.
  */
-int oracle_paged_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+static int paged_attn(const uint16_t *q, const cache_view *cache,
                       const int32_t *block_tables, const int32_t *context_lens,
                       int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
                       int block_size, int max_blocks_per_seq, int num_blocks,
@@ -128,8 +204,8 @@ int oracle_paged_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t
         double *V = (double *)malloc(sizeof(double) * ((size_t)ctx * head_dim + 1));
         double *s = (double *)malloc(sizeof(double) * ((size_t)ctx + 1));
         double *acc = (double *)malloc(sizeof(double) * (size_t)head_dim);
-        if (gather_sequence(k_cache, v_cache, block_tables + (size_t)b * max_blocks_per_seq,
-                            ctx, g, n_kv, head_dim, block_size, num_blocks, K, V) != 0) {
+        if (gather_sequence(cache, block_tables + (size_t)b * max_blocks_per_seq, ctx, g,
+                            n_kv, head_dim, block_size, num_blocks, K, V) != 0) {
 #pragma omp atomic write
             status = 2;
         } else {
@@ -179,6 +255,30 @@ int oracle_paged_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t
         free(acc);
     }
     return status;
+}
+
+int oracle_paged_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens,
+                      int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
+                      int block_size, int max_blocks_per_seq, int num_blocks,
+                      double scale, int window, double *out)
+{
+    const cache_view c = {k_cache, v_cache, NULL, NULL, NULL, NULL};
+    return paged_attn(q, &c, block_tables, context_lens, num_seqs, q_len, n_q, n_kv, head_dim,
+                      block_size, max_blocks_per_seq, num_blocks, scale, window, out);
+}
+
+/* The same attention over an e4m3 cache: K_t = code * k_scale[g], V_t = code * v_scale[g]. */
+int oracle_paged_attn_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                          const float *k_scale, const float *v_scale,
+                          const int32_t *block_tables, const int32_t *context_lens,
+                          int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
+                          int block_size, int max_blocks_per_seq, int num_blocks,
+                          double scale, int window, double *out)
+{
+    const cache_view c = {NULL, NULL, k_cache, v_cache, k_scale, v_scale};
+    return paged_attn(q, &c, block_tables, context_lens, num_seqs, q_len, n_q, n_kv, head_dim,
+                      block_size, max_blocks_per_seq, num_blocks, scale, window, out);
 }
 
 /*
@@ -315,6 +415,39 @@ int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, const int32_t
             size_t src = ((size_t)i * n_kv + g) * head_dim;
             memcpy(k_cache + dst, k_new + src, sizeof(uint16_t) * head_dim);
             memcpy(v_cache + dst, v_new + src, sizeof(uint16_t) * head_dim);
+        }
+    }
+    return 0;
+}
+
+/*
+ * The same append into an e4m3 cache: the code stored for value x of KV head
+ * g is e4m3_code(x / k_scale[g]) (v_scale[g] for V), the quotient rounded to
+ * fp32 first -- quantise via a scale ("Efficient inference", Quantization:
+ * fewer bytes per weight; CS336 lecture-10 notes, Quantization & pruning).
+ */
+int oracle_kv_append_fp8(const uint16_t *k_new, const uint16_t *v_new,
+                         const int32_t *slot_mapping, int num_tokens, int n_kv, int head_dim,
+                         int block_size, int num_blocks, const float *k_scale,
+                         const float *v_scale, uint8_t *k_cache, uint8_t *v_cache)
+{
+    if (num_tokens < 0 || n_kv < 1 || head_dim < 1 || block_size < 1 || num_blocks < 0)
+        return 1;
+    for (int i = 0; i < num_tokens; ++i) {
+        long slot = slot_mapping[i];
+        if (slot < 0 || slot >= (long)num_blocks * block_size)
+            continue;
+        long blk = slot / block_size;
+        long off = slot % block_size;
+        for (int g = 0; g < n_kv; ++g) {
+            size_t dst = (((size_t)blk * n_kv + g) * block_size + off) * head_dim;
+            size_t src = ((size_t)i * n_kv + g) * head_dim;
+            for (int e = 0; e < head_dim; ++e) {
+                const float kq = (float)bf16_value(k_new[src + e]) / k_scale[g];
+                const float vq = (float)bf16_value(v_new[src + e]) / v_scale[g];
+                k_cache[dst + e] = e4m3_code(kq);
+                v_cache[dst + e] = e4m3_code(vq);
+            }
         }
     }
     return 0;

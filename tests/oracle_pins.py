@@ -31,6 +31,15 @@ What pins what:
   are rescaled and combined exactly).
 * ``pin_kv_append``         -- slots written, everything else byte-identical.
 * ``pin_kv_bytes_golden`` / ``pin_gqa_ratio`` -- the sizes printed on the pages.
+* ``pin_e4m3_decode_library`` / ``pin_e4m3_encode_library`` -- the 8-bit float
+  codec against torch's own ``float8_e4m3fn`` conversions (every code; exact
+  ties, near-ties, subnormals, random values at every magnitude).
+* ``pin_e4m3_saturation``   -- the saturating reading beyond 448, NaN, and
+  decode-then-encode returning every finite code.
+* ``pin_fp8_attention_sdpa`` -- attention over an e4m3 cache equals torch SDPA
+  on the K/V that torch dequantises (code value times the head's scale).
+* ``pin_kv_append_fp8``     -- the quantising append against numpy's fp32
+  division and torch's encoder.
 """
 from __future__ import annotations
 
@@ -52,11 +61,12 @@ def _rand_bf16(rng, shape, scale=1.0):
     return f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * np.float32(scale))
 
 
-def _paged_from_logical(rng, K, V, block_size, extra_blocks=3):
+def _paged_from_logical(rng, K, V, block_size, extra_blocks=3, poison=BF16_POISON):
     """Scatter logical K/V [num_seqs][n_kv][ctx_b][d] (lists) into a shuffled paged cache.
 
     Built by the test itself, independently of the oracle's gather.
-    Returns (k_cache, v_cache, block_tables) with poison in every unused slot.
+    Returns (k_cache, v_cache, block_tables) with poison in every unused slot
+    (the caches take the dtype of K).
     """
     num_seqs = len(K)
     n_kv, d = K[0].shape[0], K[0].shape[2]
@@ -66,8 +76,8 @@ def _paged_from_logical(rng, K, V, block_size, extra_blocks=3):
     perm = rng.permutation(pool)
     max_blocks = max(1, max(nblk))
     bt = np.full((num_seqs, max_blocks), perm[-1], dtype=np.int32)
-    kc = np.full((pool, n_kv, block_size, d), BF16_POISON, dtype=np.uint16)
-    vc = np.full_like(kc, BF16_POISON)
+    kc = np.full((pool, n_kv, block_size, d), poison, dtype=K[0].dtype)
+    vc = np.full_like(kc, poison)
     o = 0
     for b in range(num_seqs):
         for j in range(nblk[b]):
@@ -415,10 +425,143 @@ def pin_gqa_ratio(orc):
         assert mha * n_kv == gqa * n_h
 
 
+# ---------------------------------------------------------------------------
+# 8-bit (e4m3) KV cache
+# ---------------------------------------------------------------------------
+E4M3_NAN = 0x7F
+
+
+def _torch_e4m3(x):
+    """torch's fp32 -> float8_e4m3fn codes (round to nearest even)."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _torch_e4m3_value(codes):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_e4m3_decode_library(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    got, ref = orc.e4m3_decode(codes), _torch_e4m3_value(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.isnan(got[E4M3_NAN]) and np.isnan(got[0xFF]) and np.isnan(got).sum() == 2
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def pin_e4m3_encode_library(orc):
+    rng = np.random.default_rng(41)
+    vals = _torch_e4m3_value(np.arange(256, dtype=np.uint8))
+    pos = np.unique(vals[(vals >= 0) & np.isfinite(vals)])      # 0 .. 448, increasing
+    mids = (pos[:-1] + pos[1:]) / 2                               # exact ties (fp32-exact)
+    tests = [pos, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+             np.nextafter(mids.astype(np.float32), np.float32(np.inf)),
+             np.asarray([2.0 ** -10, 2.0 ** -10 * 1.0000001, 2.0 ** -11, 1e-30, 0.0, 464.0])]
+    for e in range(-12, 9):
+        tests.append(np.abs(rng.standard_normal(2000)) * 2.0 ** e)
+    x = np.concatenate([t.astype(np.float32).ravel() for t in tests])
+    x = x[x <= 464.0]
+    x = np.concatenate([x, -x])
+    got = orc.e4m3_encode(x)
+    ref = _torch_e4m3(x)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(x[i]), int(got[i]), int(ref[i])) for i in bad[:5]]
+
+
+def pin_e4m3_saturation(orc):
+    big = np.asarray([448.0, 455.0, 464.0, 464.01, 479.9, 480.0, 1e6, 3.0e38, np.inf],
+                     dtype=np.float32)
+    assert np.all(orc.e4m3_encode(big) == 0x7E)
+    assert np.all(orc.e4m3_encode(-big) == 0xFE)
+    assert orc.e4m3_encode(np.asarray([np.nan], np.float32))[0] == E4M3_NAN
+    codes = np.asarray([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    assert np.array_equal(orc.e4m3_encode(orc.e4m3_decode(codes).astype(np.float32)), codes)
+
+
+def _fp8_case(rng, ctxs, n_q, n_kv, d, bs, q_len):
+    finite = np.asarray([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    K = [rng.choice(finite, size=(n_kv, c, d)).astype(np.uint8) for c in ctxs]
+    V = [rng.choice(finite, size=(n_kv, c, d)).astype(np.uint8) for c in ctxs]
+    kc, vc, bt = _paged_from_logical(rng, K, V, bs, poison=E4M3_NAN)
+    q = _rand_bf16(rng, (len(ctxs), q_len, n_q, d))
+    ks = rng.uniform(0.002, 0.05, n_kv).astype(np.float32)
+    vs = rng.uniform(0.002, 0.05, n_kv).astype(np.float32)
+    return dict(q=q, K=K, V=V, k_cache=kc, v_cache=vc, block_tables=bt, ks=ks, vs=vs,
+                context_lens=np.asarray(ctxs, dtype=np.int32))
+
+
+def pin_fp8_attention_sdpa(orc):
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(43)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        c = _fp8_case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        G = n_q // n_kv
+        for window in (0, 5):
+            got = orc.paged_attn_fp8(c["q"], c["k_cache"], c["v_cache"], c["ks"], c["vs"],
+                                     c["block_tables"], c["context_lens"], n_q=n_q, n_kv=n_kv,
+                                     head_dim=d, block_size=bs, scale=0.2, window=window)
+            for b, ctx in enumerate(ctxs):
+                q = torch.from_numpy(bf16_bits_to_f32(c["q"][b]).astype(np.float64))
+                k = torch.from_numpy(_torch_e4m3_value(c["K"][b]) *
+                                     c["ks"].astype(np.float64)[:, None, None])
+                v = torch.from_numpy(_torch_e4m3_value(c["V"][b]) *
+                                     c["vs"].astype(np.float64)[:, None, None])
+                k, v = k.repeat_interleave(G, dim=0), v.repeat_interleave(G, dim=0)
+                pos = ctx - q_len + torch.arange(q_len)
+                t = torch.arange(ctx)[None, :]
+                mask = t <= pos[:, None]
+                if window:
+                    mask &= t > pos[:, None] - window
+                ref = F.scaled_dot_product_attention(q.permute(1, 0, 2)[None], k[None], v[None],
+                                                     attn_mask=mask[None, None], scale=0.2)[0]
+                ref = ref.permute(1, 0, 2).numpy()
+                rows_seen = mask.any(dim=1).numpy()
+                np.testing.assert_allclose(got[b][rows_seen], ref[rows_seen], rtol=1e-12,
+                                           atol=1e-12)
+
+
+def pin_kv_append_fp8(orc):
+    rng = np.random.default_rng(44)
+    for n_kv, d, bs, pool in [(2, 8, 4, 6), (4, 64, 16, 5)]:
+        kc = rng.integers(0, 256, size=(pool, n_kv, bs, d), dtype=np.uint8)
+        vc = rng.integers(0, 256, size=(pool, n_kv, bs, d), dtype=np.uint8)
+        nslots = pool * bs
+        slots = np.concatenate([rng.permutation(nslots)[:7].astype(np.int32),
+                                np.asarray([-1, nslots], np.int32)])
+        T = slots.shape[0]
+        kn = _rand_bf16(rng, (T, n_kv, d), 3.0)
+        vn = _rand_bf16(rng, (T, n_kv, d), 3.0)
+        kn[0, 0, :4] = f32_to_bf16_bits(np.asarray([1e4, -1e4, 0.0, -0.0], np.float32))
+        ks = rng.uniform(0.005, 0.05, n_kv).astype(np.float32)
+        vs = rng.uniform(0.005, 0.05, n_kv).astype(np.float32)
+
+        def expect(x_bits, scale):
+            xq = bf16_bits_to_f32(x_bits).astype(np.float32) / scale[:, None]  # fp32 division
+            codes = _torch_e4m3(np.clip(xq, np.float32(-464.0), np.float32(464.0)))
+            codes = np.where(np.abs(xq) > 464.0, np.where(xq < 0, 0xFE, 0x7E), codes)
+            return codes.astype(np.uint8)
+
+        k_ref, v_ref = kc.copy(), vc.copy()
+        for i, sl in enumerate(slots):
+            if 0 <= sl < nslots:
+                k_ref[sl // bs, :, sl % bs, :] = expect(kn[i], ks)
+                v_ref[sl // bs, :, sl % bs, :] = expect(vn[i], vs)
+        k_got, v_got = kc.copy(), vc.copy()
+        orc.kv_append_fp8(kn, vn, slots, k_got, v_got, ks, vs, block_size=bs)
+        assert np.array_equal(k_got, k_ref) and np.array_equal(v_got, v_ref)
+
+
 ALL_PINS = [
     pin_library_sdpa, pin_numpy_dense, pin_equal_scores_mean, pin_single_token, pin_hardmax,
     pin_block_permutation, pin_gqa_equals_repeated_mha, pin_causal_rows, pin_window_sdpa,
     pin_window_extremes, pin_empty_context,
     pin_merge_exact, pin_kv_append, pin_copy_blocks, pin_append_then_attend, pin_kv_bytes_golden,
-    pin_gqa_ratio,
+    pin_gqa_ratio, pin_e4m3_decode_library, pin_e4m3_encode_library, pin_e4m3_saturation,
+    pin_fp8_attention_sdpa, pin_kv_append_fp8,
 ]

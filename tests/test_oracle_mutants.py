@@ -40,6 +40,17 @@ MUTANTS = {
     "merge_no_rescale": ("double w = exp(m[(size_t)s * rows + r] - M);", "double w = 1.0;"),
     "merge_denominator_unweighted": ("denom += w * ls;", "denom += ls;"),
     "partial_max_not_reported": ("m[row] = mx;", "m[row] = 0.0;"),
+    "e4m3_bias_off_by_one": ("ldexp(8.0 + m, e - 10)", "ldexp(8.0 + m, e - 11)"),
+    "e4m3_subnormal_scale": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    "e4m3_ties_away": ("(long)rint(ldexp(a, 3 - e))", "(long)floor(ldexp(a, 3 - e) + 0.5)"),
+    "e4m3_saturates_late": ("    if (a >= 448.0) {", "    if (a >= 480.0) {"),
+    "e4m3_overflow_to_nan": ("code = 0x7E; /* the largest finite code", "code = 0x7F; /* the largest finite code"),
+    "fp8_k_scale_dropped": ("e4m3_value(c->k8[base + e]) * (double)c->k_scale[g]",
+                            "e4m3_value(c->k8[base + e])"),
+    "fp8_v_uses_k_scale": ("e4m3_value(c->v8[base + e]) * (double)c->v_scale[g]",
+                           "e4m3_value(c->v8[base + e]) * (double)c->k_scale[g]"),
+    "fp8_append_head0_scale": ("/ k_scale[g];", "/ k_scale[0];"),
+    "fp8_append_multiplies": ("/ v_scale[g];", "* v_scale[g];"),
     "window_one_too_wide": ("const long first_l = window > 0 ? pos - window + 1 : 0;",
                             "const long first_l = window > 0 ? pos - window : 0;"),
     "copy_direction_swapped": ("memcpy(k_cache + (size_t)dst * per_block, k_cache + (size_t)src * per_block,",
