@@ -2,7 +2,7 @@
 """Benchmark of the paged decode-attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--kv bf16|fp8] [--window W]
 
 A step is one pass of the whole hot path over one batch: kv_append of the
 step's new K/V, then paged decode attention (plus its LSE merge launch) over
@@ -18,6 +18,12 @@ figure through the public API with host buffers, the oracle as a CPU
 baseline, and the SM clocks sampled while the steps ran.  The headline step
 time is the CUDA-graph replay of the step (the three launches captured
 once); the eagerly launched step is reported under "eager".
+
+--kv fp8 times the same step over an 8-bit (e4m3) cache with per-KV-head
+scales (the quantising append, then attention); --window W times
+sliding-window attention.  Their bytes count what the step must move: the
+e4m3 cache is one byte per element, and a window reads at most W + q_len - 1
+tokens per sequence.  The default line (bf16, no window) is the headline.
 
 Under torchrun (N > 1) every rank runs an independent replica of the
 workload on its own GPU (no collective on the data path); the timing is the
@@ -52,6 +58,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_gqa")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16")
+    ap.add_argument("--window", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
@@ -80,13 +88,14 @@ def hbm_peak():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("decode_attn.cu", "ptx.cuh", "tcgen05.cuh", "pkv_internal.h"):
+    for name in ("decode_attn.cuh", "decode_attn.cu", "decode_attn_fp8.cu", "ptx.cuh",
+                 "tcgen05.cuh", "pkv_internal.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_256_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
+def profiled_traffic(key):
     """DRAM bytes per attention launch from the committed ncu summary, if still current."""
     try:
         with open(PROFILE_TRAFFIC) as f:
@@ -95,7 +104,7 @@ def profiled_traffic(workload):
         return None
     if rec.get("kernel_source_sha") != kernel_source_hash():
         return None
-    return rec.get("bytes_per_launch", {}).get(workload)
+    return rec.get("bytes_per_launch", {}).get(key)
 
 
 class ClockSampler:
@@ -178,10 +187,18 @@ def whole_job_gbps(bytes_per_rank, ms_per_step, world):
 
 
 # ---------------------------------------------------------------------------
-def step_bytes(wl):
-    """Algorithmic bytes of one decode step: resident KV + q + out (bf16)."""
+def step_bytes(wl, elem_bytes=2, window=0):
+    """Algorithmic bytes of one decode step: the KV the step must read + q + out (bf16).
+
+    Without a window that is every resident token; with one, a sequence needs
+    only its last W + q_len - 1 tokens (the union of its rows' windows).
+    """
+    import numpy as np
     from paged_kv_cache_256_gb300 import pkv_kv_bytes
-    kv = pkv_kv_bytes(1, wl.n_kv, wl.head_dim, 2, wl.resident_tokens())
+    ctx = wl.context_lens.astype(np.int64)
+    if window > 0:
+        ctx = np.minimum(ctx, window + wl.q_len - 1)
+    kv = pkv_kv_bytes(1, wl.n_kv, wl.head_dim, elem_bytes, int(ctx.sum()))
     q = wl.q.nbytes
     return kv + q + q, kv
 
@@ -274,12 +291,17 @@ def run_ours(args):
     torch.cuda.set_device(device)
 
     import paged_kv_cache_256_gb300 as pkv
-    from paged_kv_cache_256_gb300.device import to_device
-    from paged_kv_cache_256_gb300.workloads import make_workload
+    from paged_kv_cache_256_gb300.device import fp8_to_device, to_device
+    from paged_kv_cache_256_gb300.workloads import fp8_cache_for, make_workload
 
     wl = make_workload(args.workload)
-    total_bytes, kv_bytes = step_bytes(wl)
+    kv8 = args.kv == "fp8"
+    total_bytes, kv_bytes = step_bytes(wl, 1 if kv8 else 2, args.window)
     dw = to_device(wl, device)
+    d8 = fp8_to_device(fp8_cache_for(wl), device) if kv8 else None
+    if kv8:  # the bf16 caches are not used by this step
+        dw.k_cache = dw.v_cache = None
+        torch.cuda.empty_cache()
     ws = pkv.alloc_workspace(wl.num_seqs, wl.q_len, wl.n_q, wl.n_kv, wl.head_dim,
                              wl.block_size, device=device)
     out = torch.empty(tuple(dw.q.shape), dtype=torch.bfloat16, device=device)
@@ -287,11 +309,31 @@ def run_ours(args):
     grid = torch.cuda.get_device_properties(device).multi_processor_count
     launches_per_step = 3 if grid > 1 else 2
 
+    def append(s):
+        if kv8:
+            pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.k_cache, d8.v_cache,
+                                  d8.k_scale, d8.v_scale, stream=s)
+        else:
+            pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache,
+                              stream=s)
+
+    def attend(s):
+        if kv8:
+            pkv.pkv_paged_decode_attn_ex(dw.q, d8.k_cache, d8.v_cache, dw.block_tables,
+                                         dw.context_lens, wl.scale, out, ws, stream=s,
+                                         window=args.window, k_scale=d8.k_scale,
+                                         v_scale=d8.v_scale)
+        elif args.window:
+            pkv.pkv_paged_decode_attn_ex(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
+                                         dw.context_lens, wl.scale, out, ws, stream=s,
+                                         window=args.window)
+        else:
+            pkv.pkv_paged_decode_attn(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
+                                      dw.context_lens, wl.scale, out, ws, stream=s)
+
     def step():
-        pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache,
-                          stream=stream)
-        pkv.pkv_paged_decode_attn(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
-                                  dw.context_lens, wl.scale, out, ws, stream=stream)
+        append(stream)
+        attend(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -316,11 +358,9 @@ def run_ours(args):
     torch.cuda.synchronize(device)
     ev_step[0].record(stream)
     for k in range(K):
-        pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache,
-                          stream=stream)
+        append(stream)
         ev_attn[k].record(stream)
-        pkv.pkv_paged_decode_attn(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
-                                  dw.context_lens, wl.scale, out, ws, stream=stream)
+        attend(stream)
         ev_step[k + 1].record(stream)
     torch.cuda.synchronize(device)
     if world > 1:
@@ -383,10 +423,8 @@ def run_ours(args):
         gs.wait_stream(stream)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=gs):
-            pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache,
-                              stream=gs)
-            pkv.pkv_paged_decode_attn(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
-                                      dw.context_lens, wl.scale, out, ws, stream=gs)
+            append(gs)
+            attend(gs)
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize(device)
@@ -423,15 +461,17 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "us_per_step": round(ms_per_step * 1e3, 2),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 KV (f16 products, fp32 softmax)" if kv8 else "bf16",
         "data": "synthetic",
         "config": {
             "workload": wl.name, "num_seqs": wl.num_seqs, "n_q": wl.n_q, "n_kv": wl.n_kv,
             "head_dim": wl.head_dim, "block_size": wl.block_size, "q_len": wl.q_len,
             "resident_tokens": wl.resident_tokens(), "bytes_per_step": total_bytes,
-            "kv_bytes": kv_bytes,
+            "kv_bytes": kv_bytes, "kv_dtype": args.kv, "window": args.window,
             "l2": f"no flush: resident KV {kv_bytes / L2_BYTES:.1f}x the 129 MB L2",
-            "step": "kv_append + paged_decode_attn (+ lse_merge)",
+            "step": ("kv_append_fp8" if kv8 else "kv_append") +
+                    " + paged_decode_attn (+ lse_merge)",
             "timed_as": step_source,
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
             "step_us_p10_p50_p90": [round(1e3 * x, 2) for x in
@@ -440,7 +480,9 @@ def run_ours(args):
         "roofline": {
             "kernel": "paged_decode_attn (attention + merge launches of one call)",
             "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(wl.name),
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(wl.name + ("/fp8" if kv8 else "") +
+                                        (f"/w{args.window}" if args.window else "")),
             "peak_source": peak_src, "attn_us": round(attn_mean * 1e3, 2),
             "algorithmic_bytes_per_launch": total_bytes,
         },
@@ -449,7 +491,7 @@ def run_ours(args):
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not kv8 and not args.window:
         line["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -46,6 +46,10 @@ typedef enum pkv_status {
     PKV_ERR_OUT_OF_BLOCKS = 7    /* the block pool has too few free blocks (nothing was changed) */
 } pkv_status;
 
+/* kv_dtype values (pkv_attn_params). */
+#define PKV_KV_BF16 0     /* caches hold bf16 */
+#define PKV_KV_FP8_E4M3 1 /* caches hold e4m3 codes with per-KV-head scales */
+
 /* out_dtype values. */
 #define PKV_OUT_BF16 0 /* round-to-nearest-even bf16 */
 #define PKV_OUT_F32 1  /* fp32 (debug / tight-parity path; probabilities kept to ~16 bits) */
@@ -57,6 +61,8 @@ typedef enum pkv_status {
  * winds down and pkv_check_error reports PKV_ERR_TIMEOUT.  The output of
  * such a call is not valid; the context stays usable. */
 #define PKV_FLAG_TEST_STALL 0x2u
+/* pkv_copy_blocks: the caches hold 1-byte (e4m3) elements instead of bf16. */
+#define PKV_FLAG_KV_FP8 0x4u
 /* Bits 16..31 force the number of attention CTAs (0 = one per SM).  Tests
  * use it to move where long contexts are split; results stay within the
  * stated tolerance for every value. */
@@ -131,6 +137,18 @@ int pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cach
  *   cache itself is unchanged: the caller may keep or release blocks that
  *   have left every window.  W >= max_blocks_per_seq * block_size is the same
  *   as 0.  W < 0 returns PKV_ERR_INVALID_ARG.
+ * kv_dtype: PKV_KV_BF16, or PKV_KV_FP8_E4M3 for an 8-bit cache -- fewer
+ *   bytes per cached element, dequantised through a scale ("Efficient
+ *   inference", Quantization: fewer bytes per weight; CS336 lecture-10 notes,
+ *   Quantization & pruning).  k_cache / v_cache then hold e4m3 codes (OCP
+ *   FP8 E4M3: bias 7, largest finite 448, no infinity) in the same layout
+ *   with 1-byte elements, and k_scale / v_scale are DEVICE fp32 arrays
+ *   [n_kv]: the value of code c in KV head g is c * k_scale[g] (V alike).
+ *   The result is the attention over those values.  Inside the kernel Q and
+ *   the probabilities are rounded to f16 (|q| must stay below 65504), the
+ *   products accumulate in fp32.  pkv_kv_append_fp8 writes such a cache.
+ *   Cache pointers must be 16-byte aligned.  k_scale / v_scale are ignored
+ *   for PKV_KV_BF16.  Any other kv_dtype returns PKV_ERR_INVALID_ARG.
  * Every other field, the layouts and the return codes are those of
  * pkv_paged_decode_attn.  `p` is read during the call only.
  */
@@ -155,6 +173,9 @@ typedef struct pkv_attn_params {
     size_t workspace_bytes;
     unsigned flags;
     int window;
+    int kv_dtype;
+    const float *k_scale;
+    const float *v_scale;
 } pkv_attn_params;
 
 int pkv_paged_decode_attn_ex(const pkv_attn_params *p, void *stream);
@@ -223,6 +244,25 @@ int pkv_kv_append(const void *k_new, const void *v_new, const int32_t *slot_mapp
                   void *k_cache, void *v_cache, unsigned flags, void *stream);
 
 /*
+ * pkv_kv_append_fp8 -- pkv_kv_append into an 8-bit (e4m3) cache.
+ *
+ * For every valid slot (as in pkv_kv_append) and KV head g, element e of the
+ * new key row is stored as the e4m3 code nearest to k_new[i][g][e] /
+ * k_scale[g]: the quotient is rounded to fp32 (IEEE division), then to e4m3
+ * with ties to the even code; quotients beyond +-448 (and infinities) store
+ * +-448, NaN stores 0x7F.  V likewise with v_scale.  Quantise through a
+ * scale: "Efficient inference", Quantization: fewer bytes per weight.
+ * k_scale, v_scale: DEVICE fp32 [n_kv]; caches [num_blocks][n_kv][block_size]
+ *   [head_dim] bytes, 16-byte aligned; k_new, v_new as for pkv_kv_append.
+ * flags: reserved, pass 0.
+ * Returns PKV_OK, PKV_ERR_INVALID_ARG or PKV_ERR_CUDA; num_tokens == 0 launches nothing.
+ */
+int pkv_kv_append_fp8(const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                      int num_tokens, int n_kv, int head_dim, int block_size, int num_blocks,
+                      const float *k_scale, const float *v_scale, void *k_cache, void *v_cache,
+                      unsigned flags, void *stream);
+
+/*
  * pkv_copy_blocks -- copy whole physical blocks (every KV head, K and V).
  *
  * For each pair p < num_pairs: block pairs[2p+1] of k_cache and of v_cache
@@ -234,7 +274,9 @@ int pkv_kv_append(const void *k_new, const void *v_new, const int32_t *slot_mapp
  * pairs: device int32 [num_pairs][2]; pairs with an id outside
  *   [0, num_blocks) or with src == dst are skipped.  A destination must not
  *   also be a source in the same call.
- * Caches as for pkv_paged_decode_attn (head_dim a multiple of 8).
+ * Caches as for pkv_paged_decode_attn (head_dim a multiple of 8); with
+ * PKV_FLAG_KV_FP8 in flags they hold 1-byte elements (n_kv * block_size *
+ * head_dim a multiple of 16).
  * Returns PKV_OK, PKV_ERR_INVALID_ARG or PKV_ERR_CUDA; num_pairs == 0 launches nothing.
  */
 int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,

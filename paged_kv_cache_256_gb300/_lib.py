@@ -26,6 +26,9 @@ PKV_OUT_BF16 = 0
 PKV_OUT_F32 = 1
 PKV_FLAG_CHECKED = 0x1
 PKV_FLAG_TEST_STALL = 0x2
+PKV_FLAG_KV_FP8 = 0x4
+PKV_KV_BF16 = 0
+PKV_KV_FP8_E4M3 = 1
 PKV_FLAG_GRID_SHIFT = 16
 
 
@@ -43,7 +46,8 @@ class pkv_attn_params(ctypes.Structure):
         ("max_blocks_per_seq", ctypes.c_int), ("num_blocks", ctypes.c_int),
         ("scale", ctypes.c_float), ("out", ctypes.c_void_p), ("out_dtype", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-        ("flags", ctypes.c_uint), ("window", ctypes.c_int),
+        ("flags", ctypes.c_uint), ("window", ctypes.c_int), ("kv_dtype", ctypes.c_int),
+        ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
     ]
 
 
@@ -58,6 +62,8 @@ SIGNATURES = {
     "pkv_paged_decode_attn_noalloc": ([_vp, _vp, _vp, _i32p, _i32p] + [_c_int] * 8 +
                                       [_c_float, _vp, _c_int, ctypes.c_uint, _vp], _c_int),
     "pkv_kv_append": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp, _vp, ctypes.c_uint, _vp], _c_int),
+    "pkv_kv_append_fp8": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp] * 4 + [ctypes.c_uint, _vp],
+                          _c_int),
     "pkv_check_error": ([_vp, _vp], _c_int),
     "pkv_copy_blocks": ([_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.c_uint,
                          _vp], _c_int),
@@ -126,6 +132,21 @@ def _bf16_like(t, name):
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
 
 
+def _fp8_like(t, name):
+    import torch
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"{name} must hold e4m3 codes (torch.uint8 or float8_e4m3fn), got {t.dtype}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def _f32_vec(t, n, name):
+    import torch
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or \
+            tuple(t.shape) != (n,):
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape ({n},)")
+
+
 def _i32(t, name):
     import torch
     if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
@@ -161,12 +182,12 @@ def alloc_workspace(num_seqs, q_len, n_q, n_kv, head_dim, block_size, flags=0, d
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def _attn_shapes(q, k_cache, v_cache, block_tables, context_lens, out, workspace):
+def _attn_shapes(q, k_cache, v_cache, block_tables, context_lens, out, workspace, kv8=False):
     """Checks shared by the attention entry points; returns (dims, out_dtype)."""
     import torch
     _bf16_like(q, "q")
-    _bf16_like(k_cache, "k_cache")
-    _bf16_like(v_cache, "v_cache")
+    (_fp8_like if kv8 else _bf16_like)(k_cache, "k_cache")
+    (_fp8_like if kv8 else _bf16_like)(v_cache, "v_cache")
     _i32(block_tables, "block_tables")
     _i32(context_lens, "context_lens")
     if q.dim() != 4 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
@@ -206,10 +227,19 @@ def pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale
 
 
 def pkv_paged_decode_attn_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out,
-                             workspace, flags=0, stream=None, window=0):
-    """pkv_paged_decode_attn through the parameter struct; window > 0 = sliding window."""
+                             workspace, flags=0, stream=None, window=0, k_scale=None,
+                             v_scale=None):
+    """pkv_paged_decode_attn through the parameter struct.
+
+    window > 0: sliding window of that many positions.  With k_scale / v_scale
+    (float32 CUDA [n_kv]) the caches are e4m3 codes (uint8 or float8_e4m3fn).
+    """
+    kv8 = k_scale is not None or v_scale is not None
     (num_seqs, q_len, n_q, n_kv, d, bs, max_blocks, num_blocks), out_dtype = _attn_shapes(
-        q, k_cache, v_cache, block_tables, context_lens, out, workspace)
+        q, k_cache, v_cache, block_tables, context_lens, out, workspace, kv8)
+    if kv8:
+        _f32_vec(k_scale, n_kv, "k_scale")
+        _f32_vec(v_scale, n_kv, "v_scale")
     p = pkv_attn_params(
         q=q.data_ptr(), k_cache=k_cache.data_ptr(), v_cache=v_cache.data_ptr(),
         block_tables=block_tables.data_ptr(), context_lens=context_lens.data_ptr(),
@@ -217,7 +247,8 @@ def pkv_paged_decode_attn_ex(q, k_cache, v_cache, block_tables, context_lens, sc
         max_blocks_per_seq=max_blocks, num_blocks=num_blocks, scale=float(scale),
         out=out.data_ptr(), out_dtype=out_dtype, workspace=workspace.data_ptr(),
         workspace_bytes=workspace.numel() * workspace.element_size(), flags=int(flags),
-        window=int(window))
+        window=int(window), kv_dtype=PKV_KV_FP8_E4M3 if kv8 else PKV_KV_BF16,
+        k_scale=k_scale.data_ptr() if kv8 else None, v_scale=v_scale.data_ptr() if kv8 else None)
     st = load_library().pkv_paged_decode_attn_ex(ctypes.byref(p), _stream_ptr(stream))
     _check(st, "pkv_paged_decode_attn_ex")
 
@@ -265,11 +296,39 @@ def pkv_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, flags=0, stream=
     _check(st, "pkv_kv_append")
 
 
+def pkv_kv_append_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, flags=0,
+                      stream=None):
+    """Quantise k_new/v_new [T, n_kv, d] (bf16) into e4m3 cache slots via per-head scales."""
+    _bf16_like(k_new, "k_new")
+    _bf16_like(v_new, "v_new")
+    _fp8_like(k_cache, "k_cache")
+    _fp8_like(v_cache, "v_cache")
+    _i32(slot_mapping, "slot_mapping")
+    T, n_kv, d = k_new.shape
+    num_blocks, n_kv2, bs, d2 = k_cache.shape
+    if v_new.shape != k_new.shape or n_kv2 != n_kv or d2 != d or slot_mapping.shape != (T,) \
+            or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent shapes")
+    _f32_vec(k_scale, n_kv, "k_scale")
+    _f32_vec(v_scale, n_kv, "v_scale")
+    st = load_library().pkv_kv_append_fp8(
+        k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), T, n_kv, d, bs, num_blocks,
+        k_scale.data_ptr(), v_scale.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        int(flags), _stream_ptr(stream))
+    _check(st, "pkv_kv_append_fp8")
+
+
 def pkv_copy_blocks(k_cache, v_cache, pairs, flags=0, stream=None):
-    """Copy whole blocks (all KV heads, K and V): block pairs[p,1] <- block pairs[p,0]."""
+    """Copy whole blocks (all KV heads, K and V): block pairs[p,1] <- block pairs[p,0].
+
+    bf16 caches, or e4m3 caches (uint8 / float8_e4m3fn; PKV_FLAG_KV_FP8 is set for them).
+    """
     import torch
-    _bf16_like(k_cache, "k_cache")
-    _bf16_like(v_cache, "v_cache")
+    kv8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
+    (_fp8_like if kv8 else _bf16_like)(k_cache, "k_cache")
+    (_fp8_like if kv8 else _bf16_like)(v_cache, "v_cache")
+    if kv8:
+        flags = int(flags) | PKV_FLAG_KV_FP8
     if pairs.dtype != torch.int32 or not pairs.is_cuda or not pairs.is_contiguous() or \
             pairs.dim() != 2 or pairs.shape[1] != 2:
         raise ValueError("pairs must be a contiguous int32 CUDA tensor of shape [n, 2]")

@@ -1,1352 +1,13 @@
-// decode_attn.cu -- paged decode attention for sm_103a.
-//
-// What it computes: for every sequence b, new query token i and query head h,
-//   out = softmax_t(scale * q . K_t) V_t over the logical positions t the
-//   causal mask allows (t <= pos = ctx - q_len + i; with a sliding window of
-//   W positions also t > pos - W: CS336 lecture-10 notes, Local attention &
-//   sparse variants), with K_t, V_t found through
-//   the block table (PagedAttention: "Inference Engines", The Breakthrough;
-//   CS336 lecture-10 notes, PagedAttention (vLLM)), and query head h reading
-//   KV head h / (n_q / n_kv) ("Transformer inference mechanics", MHA versus
-//   MQA versus GQA).
-//
-// How (GB300 design):
-//   * A "unit" is one (sequence, KV head).  Its query rows are the G = n_q/n_kv
-//     heads of the group times the q_len new tokens (rows = G * q_len <= 128),
-//     so every KV tile is fetched from HBM once for all of them.
-//   * The whole step is a flat list of (unit, block) work items.  Persistent
-//     CTA c (one per SM) takes the contiguous slice [c*W/grid, (c+1)*W/grid)
-//     of the W items, so every CTA streams the same number of KV bytes however
-//     ragged the context lengths are.  A unit cut by a slice boundary is a
-//     split (flash-decoding); its pieces leave (O, m, l) partials that the
-//     LSE merge kernel combines.
-//   * Warp 8 is the producer: it reads block ids and four of its lanes issue,
-//     side by side, 2-D TMA tile loads (128-byte swizzle) of the K and V
-//     tiles of each (block, KV head) into a ring of shared-memory stages, each
-//     guarded by a full/empty mbarrier pair.  Its walk never stops at unit
-//     boundaries, so HBM stays busy while consumers finish a unit.
-//   * Warps 0..7 consume, each taking every 8th block (and, for more than 8
-//     rows, one 16-row slice of them).  Products run on the tensor cores
-//     (mma.sync m16n8k16, bf16 in, fp32 accumulate); the online softmax
-//     (running max m and sum l, fp32, base 2) is the FlashAttention recurrence
-//     ("Efficient inference", FlashAttention: exact attention without the
-//     matrix).  At the end of a unit the warps' partials are combined in
-//     shared memory by the same exact rule.
-//       - narrow (rows <= 8): tokens on the MMA's M side, S^T = K Q^T and
-//         O^T += V^T P^T, rows padded only to 8;
-//       - wide (rows > 8): rows on the M side in 16-row slices, S = Q K^T and
-//         O += P V.
-//   * fp32 output keeps each probability as a bf16 pair (hi + lo) so the PV
-//     product keeps ~16 bits of it; bf16 output uses one bf16.
-//
-// Bounded waits: every mbarrier wait gives up after a second, records
-// kErrTimeout in the workspace and the kernel winds down without hanging.
-#include <atomic>
-#include <cfloat>
-#include <climits>
-
-#include "pkv_internal.h"
-#include "ptx.cuh"
-#include "tcgen05.cuh"
+// decode_attn.cu -- the paged decode-attention kernels for bf16 KV caches
+// (templates in decode_attn.cuh).
+#include "decode_attn.cuh"
 
 namespace pkv {
-
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kMergeSlots = 4;                   // warps that park a partial per merge round
-constexpr int kIssueLanes = 4;                   // producer lanes issuing loads side by side
-constexpr int kNarrowRows = 8;                   // rows up to which the narrow consumer is used
-constexpr int kTmemMinRows = 64;                 // rows above which the TMEM consumer is used
-
-// Consumer modes, chosen by the number of query rows sharing a KV head.
-constexpr int kModeWide = 0;    // 8 < rows <= 64: mma.sync, rows on the M side
-constexpr int kModeNarrow = 1;  // rows <= 8: mma.sync, tokens on the M side
-constexpr int kModeTmem = 2;    // rows > 64: tcgen05, 128-row tiles, accumulators in TMEM
-
-template <int D, int BS, int MODE>
-struct AttnCfg {
-    static constexpr int kTileBytes = BS * D * 2;  // one K (or V) tile of one (block, head)
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kBoxBytes = BS * 128;  // one 64-column swizzled box
-    // Per-lane floats a warp parks for a merge round: its accumulator, m[2], l[2].
-    static constexpr int kLaneFloats = (MODE == kModeNarrow ? D / 4 : D / 2) + 4;
-    static constexpr int kMergeBytes = MODE == kModeTmem ? 0 : kMergeSlots * 32 * kLaneFloats * 4;
-    // Narrow emit: rows x head_dim fp32 tile (+4 floats of row padding) and (m, l) per row.
-    static constexpr int kTileStride = D + 4;
-    static constexpr int kEmitBytes =
-        MODE == kModeNarrow ? (kNarrowRows * kTileStride + 2 * kNarrowRows) * 4 : 0;
-    // TMEM mode: the unit's 128 query rows as a swizzled K-major tile.
-    static constexpr int kQTileBytes = MODE == kModeTmem ? 128 * D * 2 : 0;
-    static constexpr int kScratchBytes = kMergeBytes + kEmitBytes + kQTileBytes;
-    static constexpr int kBarrierBytes = 2 * 32 * 8;
-    static constexpr int kBudget = 227 * 1024 - 1024 - kScratchBytes - kBarrierBytes - 1024;
-    // In the mma.sync modes the ring depth is a multiple of the consumer-warp
-    // count: block g and block g - kStages then belong to the same warp, so
-    // when a warp waits for round r of a stage it has itself already seen
-    // round r - 1 complete.  (mbarrier parity waits cannot tell round r from
-    // round r - 2; with another warp owning round r - 1 a still-in-flight load
-    // would read as complete.)  The TMEM mode has a single consumer thread.
-    static constexpr int kStagesRaw = kBudget / kStageBytes;
-    static constexpr int kStages =
-        kStagesRaw >= 32 ? 32 : (MODE == kModeTmem ? kStagesRaw : (kStagesRaw / 8) * 8);
-    static constexpr int kSmemBytes =
-        1024 + kStages * kStageBytes + kScratchBytes + 2 * kStages * 8;
-    static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(BS == 16 || BS == 32, "block_size");
-    static_assert(MODE == kModeTmem ? kStages >= 2
-                                    : (kStages % kConsumerWarps == 0 && kStages >= kConsumerWarps),
-                  "ring depth");
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-};
-
-// Byte offset of the 16-byte chunk holding (row, col..col+7) inside a tile
-// stored as D/64 boxes of [BS rows][128 bytes] with the TMA 128-byte swizzle
-// (16-byte chunk index XOR row % 8 within each 1024-byte atom).
-template <int BS>
-__device__ __forceinline__ uint32_t swz(int row, int col) {
-    return static_cast<uint32_t>((col >> 6) * (BS * 128) + row * 128 +
-                                 ((((col & 63) >> 3) ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ int unit_ctx(const AttnArgs& a, int s, int bs) {
-    int ctx = __ldg(a.context_lens + s);
-    const int cap = a.max_blocks_per_seq * bs;
-    return ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-}
-
-__device__ __forceinline__ int unit_blocks(const AttnArgs& a, int s, int bs) {
-    return (unit_ctx(a, s, bs) + bs - 1) / bs;
-}
-
-// First block any row of a unit can see: with a sliding window, the earliest
-// row (position ctx - q_len) sees nothing before ctx - q_len - W + 1, so the
-// blocks before that one are never read.  Always < the unit's block count.
-__device__ __forceinline__ int unit_first_block(const AttnArgs& a, int ctx, int bs) {
-    if (a.window <= 0) return 0;
-    const long long lo = (long long)ctx - a.q_len - a.window + 1;
-    return lo > 0 ? static_cast<int>(lo / bs) : 0;
-}
-
-// Work items (blocks to read) of the units of sequence s: one per KV head each.
-__device__ __forceinline__ int unit_items(const AttnArgs& a, int s, int bs) {
-    const int ctx = unit_ctx(a, s, bs);
-    return (ctx + bs - 1) / bs - unit_first_block(a, ctx, bs);
-}
-
-// Position in the flat work list: sequence s, KV head h, block j of that unit
-// (the unit reads blocks jlo .. nb-1), `left` items still to process in this
-// CTA's slice.
-struct Walk {
-    int s, h, j, jlo, nb, ctx;
-    long long left;
-};
-
-template <int BS>
-__device__ __forceinline__ void walk_next_unit(const AttnArgs& a, Walk& w) {
-    if (++w.h == a.n_kv) {
-        w.h = 0;
-        do {
-            ++w.s;
-            w.nb = w.s < a.num_seqs ? unit_blocks(a, w.s, BS) : 1;
-        } while (w.nb == 0);
-        w.ctx = w.s < a.num_seqs ? unit_ctx(a, w.s, BS) : 0;
-        w.jlo = unit_first_block(a, w.ctx, BS);
-    }
-    w.j = w.jlo;
-}
-
-__device__ __forceinline__ int piece_end(const Walk& w) {
-    return (long long)w.nb < (long long)w.j + w.left ? w.nb : static_cast<int>(w.j + w.left);
-}
-
-// Block-wide inclusive scan of one 64-bit value per thread (all kThreads).
-__device__ __forceinline__ long long block_inclusive_scan(long long v, long long* s_red,
-                                                          long long& total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        long long n = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += n;
-    }
-    if (lane == 31) s_red[warp] = v;
-    __syncthreads();
-    long long before = 0;
-    total = 0;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
-        const long long t = s_red[w];
-        if (w < warp) before += t;
-        total += t;
-    }
-    __syncthreads();
-    return v + before;
-}
-
-// All threads: this CTA's slice [start, end) of the flat (unit, block) list,
-// as the walk position of its first item.
-template <int BS>
-__device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
-                                           long long* s_start) {
-    const int tid = threadIdx.x, cta = blockIdx.x, grid = gridDim.x;
-    long long mine = 0;
-    for (int s = tid; s < a.num_seqs; s += kThreads) mine += unit_items(a, s, BS);
-    long long total_blocks;
-    (void)block_inclusive_scan(mine, s_red, total_blocks);
-    const long long W = total_blocks * a.n_kv;
-    const long long start = (W * cta) / grid;
-    const long long end = (W * (cta + 1)) / grid;
-    if (start < end) {
-        long long base = 0;
-        for (int s0 = 0; s0 < a.num_seqs; s0 += kThreads) {
-            const int s = s0 + tid;
-            const long long v = s < a.num_seqs ? (long long)unit_items(a, s, BS) * a.n_kv : 0;
-            long long chunk;
-            const long long incl = block_inclusive_scan(v, s_red, chunk);
-            const long long excl = incl - v;
-            if (v > 0 && base + excl <= start && start < base + incl) {
-                s_start[0] = s;
-                s_start[1] = start - (base + excl);
-            }
-            base += chunk;
-            __syncthreads();
-            if (s_start[0] >= 0) break;
-        }
-    }
-    __syncthreads();
-    Walk w;
-    w.left = end - start;
-    if (w.left > 0) {
-        w.s = static_cast<int>(s_start[0]);
-        w.nb = unit_blocks(a, w.s, BS);
-        w.ctx = unit_ctx(a, w.s, BS);
-        w.jlo = unit_first_block(a, w.ctx, BS);
-        const int items = w.nb - w.jlo;
-        w.h = static_cast<int>(s_start[1] / items);
-        w.j = w.jlo + static_cast<int>(s_start[1] % items);
-    } else {
-        w.s = w.h = w.j = w.jlo = w.nb = w.ctx = 0;
-    }
-    return w;
-}
-
-// ===================== producer warp =====================
-template <int D, int BS, int kStages, int kStageBytes, int kTileBytes, int kBoxBytes>
-__device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tmap_k,
-                                        const CUtensorMap* tmap_v, Walk w, uint8_t* stages,
-                                        uint64_t* full_bar, uint64_t* empty_bar,
-                                        volatile int* s_abort) {
-    const int lane = threadIdx.x & 31;
-    if (a.test_stall) return;  // failure-path tests: nothing is loaded, every wait expires
-    const uint64_t policy = l2_policy_evict_first();
-    uint32_t gidx = 0, issued = 0;  // issued: fills actually started (a prefix of gidx)
-    bool ok = true;
-    while (w.left > 0 && ok) {
-        const int j1 = piece_end(w);
-        const int32_t* bt = a.block_tables + (size_t)w.s * a.max_blocks_per_seq;
-        int my = w.j + lane < j1 ? __ldg(bt + w.j + lane) : 0;
-        for (int jb = w.j; jb < j1 && ok; jb += 32) {
-            const int n = min(32, j1 - jb);
-            // The next 32 block ids load while this batch is issued.
-            const int nxt = jb + 32 + lane < j1 ? __ldg(bt + jb + 32 + lane) : 0;
-            if (lane < n && (my < 0 || my >= a.num_blocks)) {
-                if (a.checked) atomicOr(a.err, kErrBadBlock);
-                my = -1;  // read as an out-of-bounds (zero-filled) tile
-            }
-            if (*s_abort) ok = false;  // a consumer gave up
-            // Lanes 0..kIssueLanes-1 issue the next blocks side by side: one
-            // serial wait/issue chain per block would cap the stream.
-            for (int k0 = 0; k0 < n && ok; k0 += kIssueLanes) {
-                const int kk = k0 + lane;
-                const int blk = __shfl_sync(0xffffffffu, my, kk & 31);
-                const bool act = lane < kIssueLanes && kk < n;
-                const uint32_t gl = gidx + lane;
-                const uint32_t stage = gl % kStages;
-                bool good = true;
-                if (act) good = mbar_wait_bounded(&empty_bar[stage], ((gl / kStages) & 1u) ^ 1u);
-                const unsigned act_mask = __ballot_sync(0xffffffffu, act);
-                const unsigned good_mask = __ballot_sync(0xffffffffu, act && good);
-                const unsigned fail = act_mask & ~good_mask;
-                // Only the lanes below the first failed wait issue, so the
-                // issued fills stay a prefix of the block sequence.
-                const unsigned issue_mask =
-                    fail ? (good_mask & ((1u << (__ffs(fail) - 1)) - 1u)) : good_mask;
-                if ((issue_mask >> lane) & 1u) {
-                    mbar_arrive_expect_tx(&full_bar[stage], 2 * kTileBytes);
-                    const long long y64 = ((long long)blk * a.n_kv + w.h) * BS;
-                    const int y = (blk < 0 || y64 >= a.tile_rows_total)
-                                      ? a.tile_rows_total
-                                      : static_cast<int>(y64);
-                    uint8_t* kdst = stages + stage * kStageBytes;
-                    uint8_t* vdst = kdst + kTileBytes;
-#pragma unroll
-                    for (int half = 0; half < D / 64; ++half) {
-                        tma_load_2d(kdst + half * kBoxBytes, tmap_k, half * 64, y,
-                                    &full_bar[stage], policy);
-                        tma_load_2d(vdst + half * kBoxBytes, tmap_v, half * 64, y,
-                                    &full_bar[stage], policy);
-                    }
-                }
-                issued = gidx + __popc(issue_mask);
-                if (fail) {
-                    ok = false;
-                    if (lane == 0) {
-                        atomicOr(a.err, kErrTimeout);
-                        *s_abort = 1;
-                    }
-                }
-                gidx += min(kIssueLanes, n - k0);
-            }
-            my = nxt;
-        }
-        w.left -= j1 - w.j;
-        if (w.left > 0) walk_next_unit<BS>(a, w);
-    }
-    // Do not leave the CTA while copies into its shared memory are in flight.
-    if (lane == 0) {
-        const uint32_t first = issued > (uint32_t)kStages ? issued - kStages : 0u;
-        for (uint32_t qi = first; qi < issued; ++qi)
-            if (!mbar_wait_bounded(&full_bar[qi % kStages], (qi / kStages) & 1u)) break;
-    }
-}
-
-// Wait for a stage as a consumer (all 32 lanes).  The verdict is a warp vote,
-// so the warp-collective work that follows runs on all lanes or on none; once
-// anything failed the warp stops waiting and the CTA is told.
-__device__ __forceinline__ bool consumer_wait(const AttnArgs& a, uint64_t* bar, uint32_t parity,
-                                              bool ok, volatile int* s_abort) {
-    bool good = ok && !*s_abort;
-    if (good && !mbar_wait_bounded(bar, parity)) {
-        good = false;
-        atomicOr(a.err, kErrTimeout);
-        *s_abort = 1;
-    }
-    return __all_sync(0xffffffffu, good);
-}
-
-// Combine two online-softmax states of one row: weights a1, a2 for the two
-// accumulators, and the combined (m, l).
-__device__ __forceinline__ void merge_weights(float& m, float& l, float m2, float l2, float& a1,
-                                              float& a2) {
-    const float mn = fmaxf(m, m2);
-    const float mb = mn == -INFINITY ? 0.f : mn;
-    a1 = fast_exp2(m - mb);
-    a2 = fast_exp2(m2 - mb);
-    l = a1 * l + a2 * l2;
-    m = mn;
-}
-
-// ===================== narrow consumer (rows <= 8) =====================
-// Warp w takes blocks g == w (mod 8).  Per 16-token tile of a block:
-//   S^T[tok][row] = K[tok][:] . Q^T[:][row]       (A = K tile via ldmatrix, B = Q^T)
-//   P^T B-fragment = movmatrix.trans of bf16(S^T) (rows move from the column
-//                    index of the accumulator to the lane index of the operand)
-//   O^T[d][row]  += V^T[d][tok] . P^T[tok][row]    (A = V tile via ldmatrix.trans)
-// Lane (g, t) holds rows 2t, 2t+1 of the softmax state; a row's max and sum
-// reduce over the 8 lanes sharing t.
-template <int D, int BS, bool OUT_F32>
-__device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_t* stages,
-                                               float* scratch, uint64_t* full_bar,
-                                               uint64_t* empty_bar, volatile int* s_abort,
-                                               int4& info0, int4& info1) {
-    using C = AttnCfg<D, BS, kModeNarrow>;
-    constexpr int kStages = C::kStages;
-    constexpr int MT = D / 16;   // 16-wide head_dim tiles (M of the PV product)
-    constexpr int KT = D / 16;   // 16-deep k steps of the score product
-    constexpr int PT = BS / 16;  // 16-token tiles per block
-    constexpr int WN = kConsumerWarps;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3, mi = lane >> 3, rr = lane & 7;
-    const int G = a.group, R = a.rows, cta = blockIdx.x;
-    float* emit_tile = scratch + C::kMergeBytes / 4;
-    float* emit_ml = emit_tile + kNarrowRows * C::kTileStride;
-
-    uint32_t gbase = 0;  // sequence number (in this CTA) of the piece's first block
-    bool ok = true;
-    int piece = 0;
-    while (w.left > 0) {
-        const int j0 = w.j, j1 = piece_end(w);
-        const int ctx = w.ctx, s = w.s, h = w.h;
-
-        // Q^T as B fragments: (k = head_dim 2t.., n = row g); rows >= R are zero.
-        uint32_t qb[KT][2];
-        {
-            const bool valid = g < R;
-            const int i = valid ? g / G : 0;
-            const int hq = h * G + (valid ? g % G : 0);
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-                a.q + (((size_t)s * a.q_len + i) * a.n_q + hq) * D);
-#pragma unroll
-            for (int kk = 0; kk < KT; ++kk) {
-                qb[kk][0] = valid ? __ldg(qrow + kk * 8 + t) : 0u;
-                qb[kk][1] = valid ? __ldg(qrow + kk * 8 + 4 + t) : 0u;
-            }
-        }
-        // Row r sees tokens lo..lim: lim = its position, lo = lim - W + 1
-        // with a window (INT_MIN without); padding rows see nothing.
-        int lim[2], lo[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int r = 2 * t + e;
-            lim[e] = r < R ? ctx - a.q_len + r / G : -1;
-            lo[e] = a.window > 0 ? lim[e] - a.window + 1 : INT_MIN;
-        }
-        const int lim_min = ctx - a.q_len;
-        const int lo_max = a.window > 0 ? ctx - a.window : INT_MIN;  // largest lo of a real row
-
-        float o[MT][4];
-#pragma unroll
-        for (int n = 0; n < MT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
-        const int first = static_cast<int>((uint32_t)(warp + WN - (int)(gbase % WN)) % WN);
-        for (int jj = first; jj < j1 - j0; jj += WN) {
-            const int j = j0 + jj;
-            const uint32_t gidx = gbase + jj;
-            const uint32_t stage = gidx % kStages;
-            ok = consumer_wait(a, &full_bar[stage], (gidx / kStages) & 1u, ok, s_abort);
-            if (ok) {
-                const uint32_t kb = smem_addr(stages + stage * C::kStageBytes);
-                const uint32_t vb = kb + C::kTileBytes;
-
-                // ---- S^T = K Q^T, two interleaved accumulators per 16-token tile
-                float st[PT][4], st2[PT][4];
-#pragma unroll
-                for (int p = 0; p < PT; ++p)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) st[p][e] = st2[p][e] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < KT; ++kk) {
-#pragma unroll
-                    for (int tp = 0; tp < PT; ++tp) {
-                        uint32_t ka[4];
-                        ldmatrix_x4(ka, kb + swz<BS>(tp * 16 + (mi & 1) * 8 + rr,
-                                                      kk * 16 + (mi >> 1) * 8));
-                        if (kk & 1)
-                            mma_bf16_16816(st2[tp], ka, qb[kk][0], qb[kk][1]);
-                        else
-                            mma_bf16_16816(st[tp], ka, qb[kk][0], qb[kk][1]);
-                    }
-                }
-
-                // ---- scale, causal / window / tail mask, online softmax (base 2)
-                const int tok0 = j * BS;
-                const bool need_mask = tok0 + BS - 1 > lim_min || tok0 < lo_max;
-                float mloc[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                for (int tp = 0; tp < PT; ++tp) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float x = (st[tp][e] + st2[tp][e]) * a.scale_log2;
-                        const int tk = tok0 + tp * 16 + g + (e >> 1) * 8;
-                        if (need_mask && (tk > lim[e & 1] || tk < lo[e & 1])) x = -INFINITY;
-                        st[tp][e] = x;
-                        mloc[e & 1] = fmaxf(mloc[e & 1], x);
-                    }
-                }
-                float alpha[2], mbase[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    mloc[e] = fmaxf(mloc[e], __shfl_xor_sync(0xffffffffu, mloc[e], 4));
-                    mloc[e] = fmaxf(mloc[e], __shfl_xor_sync(0xffffffffu, mloc[e], 8));
-                    mloc[e] = fmaxf(mloc[e], __shfl_xor_sync(0xffffffffu, mloc[e], 16));
-                    const float mnew = fmaxf(m[e], mloc[e]);
-                    mbase[e] = mnew == -INFINITY ? 0.f : mnew;
-                    alpha[e] = fast_exp2(m[e] - mbase[e]);
-                    m[e] = mnew;
-                }
-                float rsum[2] = {0.f, 0.f};
-#pragma unroll
-                for (int tp = 0; tp < PT; ++tp) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p = fast_exp2(st[tp][e] - mbase[e & 1]);
-                        st[tp][e] = p;
-                        rsum[e & 1] += p;
-                    }
-                }
-                l[0] = l[0] * alpha[0] + rsum[0];
-                l[1] = l[1] * alpha[1] + rsum[1];
-                if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
-#pragma unroll
-                    for (int n = 0; n < MT; ++n) {
-                        o[n][0] *= alpha[0];
-                        o[n][1] *= alpha[1];
-                        o[n][2] *= alpha[0];
-                        o[n][3] *= alpha[1];
-                    }
-                }
-
-                // ---- P^T as B fragments: pack (tok g, rows 2t..) then transpose
-                uint32_t pb[PT][2], pl[PT][2];
-#pragma unroll
-                for (int tp = 0; tp < PT; ++tp) {
-                    const uint32_t h0 = pack_bf16x2(st[tp][0], st[tp][1]);
-                    const uint32_t h1 = pack_bf16x2(st[tp][2], st[tp][3]);
-                    pb[tp][0] = movmatrix_trans(h0);
-                    pb[tp][1] = movmatrix_trans(h1);
-                    if (OUT_F32) {
-                        pl[tp][0] = movmatrix_trans(pack_bf16x2(st[tp][0] - bf16_lo_to_f32(h0),
-                                                                st[tp][1] - bf16_hi_to_f32(h0)));
-                        pl[tp][1] = movmatrix_trans(pack_bf16x2(st[tp][2] - bf16_lo_to_f32(h1),
-                                                                st[tp][3] - bf16_hi_to_f32(h1)));
-                    }
-                }
-
-                // ---- O^T += V^T P^T (V rows past the context are zeroed: they may hold NaN)
-                const bool need_vmask = tok0 + BS > ctx;
-#pragma unroll
-                for (int tp = 0; tp < PT; ++tp) {
-                    uint32_t vm0 = 0xFFFFFFFFu, vm8 = 0xFFFFFFFFu;
-                    if (need_vmask) {
-                        const int ta = tok0 + tp * 16 + 2 * t;
-                        vm0 = (ta < ctx ? 0x0000FFFFu : 0u) | (ta + 1 < ctx ? 0xFFFF0000u : 0u);
-                        vm8 = (ta + 8 < ctx ? 0x0000FFFFu : 0u) | (ta + 9 < ctx ? 0xFFFF0000u : 0u);
-                    }
-#pragma unroll
-                    for (int dm = 0; dm < MT; ++dm) {
-                        uint32_t va[4];
-                        ldmatrix_x4_trans(va, vb + swz<BS>(tp * 16 + (mi >> 1) * 8 + rr,
-                                                            dm * 16 + (mi & 1) * 8));
-                        va[0] &= vm0;
-                        va[1] &= vm0;
-                        va[2] &= vm8;
-                        va[3] &= vm8;
-                        mma_bf16_16816(o[dm], va, pb[tp][0], pb[tp][1]);
-                        if (OUT_F32) mma_bf16_16816(o[dm], va, pl[tp][0], pl[tp][1]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[stage]);
-        }
-        gbase += j1 - j0;
-
-        // ---- row sums across the 8 lanes of a row, then combine the warps' partials
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            l[e] += __shfl_xor_sync(0xffffffffu, l[e], 4);
-            l[e] += __shfl_xor_sync(0xffffffffu, l[e], 8);
-            l[e] += __shfl_xor_sync(0xffffffffu, l[e], 16);
-        }
-        for (int step = WN >> 1; step >= 1; step >>= 1) {
-            if (warp >= step && warp < 2 * step) {
-                float* sl = scratch + (size_t)(warp - step) * 32 * C::kLaneFloats;
-#pragma unroll
-                for (int n = 0; n < MT; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sl[(n * 4 + e) * 32 + lane] = o[n][e];
-                sl[(MT * 4 + 0) * 32 + lane] = m[0];
-                sl[(MT * 4 + 1) * 32 + lane] = m[1];
-                sl[(MT * 4 + 2) * 32 + lane] = l[0];
-                sl[(MT * 4 + 3) * 32 + lane] = l[1];
-            }
-            named_barrier_sync(1, kConsumerThreads);
-            if (warp < step) {
-                const float* sl = scratch + (size_t)warp * 32 * C::kLaneFloats;
-                float a1[2], a2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    merge_weights(m[e], l[e], sl[(MT * 4 + e) * 32 + lane],
-                                  sl[(MT * 4 + 2 + e) * 32 + lane], a1[e], a2[e]);
-#pragma unroll
-                for (int n = 0; n < MT; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o[n][e] = a1[e & 1] * o[n][e] + a2[e & 1] * sl[(n * 4 + e) * 32 + lane];
-            }
-            named_barrier_sync(1, kConsumerThreads);
-        }
-
-        // ---- emit (warp 0): through a row-major tile, then 16-byte stores
-        const bool first_piece = j0 == w.jlo, last_piece = j1 == w.nb;
-        const bool whole = first_piece && last_piece;
-        if (warp == 0) {
-            float scl[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) scl[e] = whole ? (l[e] > 0.f ? 1.f / l[e] : 0.f) : 1.f;
-#pragma unroll
-            for (int n = 0; n < MT; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    emit_tile[(2 * t + (e & 1)) * C::kTileStride + n * 16 + g + (e >> 1) * 8] =
-                        o[n][e] * scl[e & 1];
-            if (g == 0) {
-                emit_ml[(2 * t) * 2 + 0] = m[0];
-                emit_ml[(2 * t) * 2 + 1] = l[0];
-                emit_ml[(2 * t + 1) * 2 + 0] = m[1];
-                emit_ml[(2 * t + 1) * 2 + 1] = l[1];
-            }
-            __syncwarp();
-            if (whole) {
-                constexpr int V = OUT_F32 ? 4 : 8;  // elements per 16-byte store
-                for (int idx = lane; idx < R * (D / V); idx += 32) {
-                    const int r = idx / (D / V), c = (idx % (D / V)) * V;
-                    const int i = r / G, hq = h * G + r % G;
-                    const size_t ob = (((size_t)s * a.q_len + i) * a.n_q + hq) * D + c;
-                    const float* src = emit_tile + r * C::kTileStride + c;
-                    if (OUT_F32) {
-                        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + ob) =
-                            make_float4(src[0], src[1], src[2], src[3]);
-                    } else {
-                        uint4 v;
-                        v.x = pack_bf16x2(src[0], src[1]);
-                        v.y = pack_bf16x2(src[2], src[3]);
-                        v.z = pack_bf16x2(src[4], src[5]);
-                        v.w = pack_bf16x2(src[6], src[7]);
-                        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ob) = v;
-                    }
-                }
-            } else {
-                const int slot = piece == 0 ? 0 : 1;
-                const size_t rec = (size_t)cta * 2 + slot;
-                for (int idx = lane; idx < R * (D / 4); idx += 32) {
-                    const int r = idx / (D / 4), c = (idx % (D / 4)) * 4;
-                    const float* src = emit_tile + r * C::kTileStride + c;
-                    *reinterpret_cast<float4*>(a.rec_o + (rec * R + r) * D + c) =
-                        make_float4(src[0], src[1], src[2], src[3]);
-                }
-                if (lane < R)
-                    *reinterpret_cast<float2*>(a.rec_ml + (rec * R + lane) * 2) =
-                        make_float2(emit_ml[lane * 2], emit_ml[lane * 2 + 1]);
-                const int4 rinfo = make_int4(
-                    s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0), 0);
-                if (slot == 0)
-                    info0 = rinfo;
-                else
-                    info1 = rinfo;
-            }
-            __syncwarp();
-        }
-        ++piece;
-        w.left -= j1 - w.j;
-        if (w.left > 0) walk_next_unit<BS>(a, w);
-    }
-}
-
-// ===================== wide consumer (rows > 8) =====================
-// Warp w owns 16-row slice (w % WM) of the unit's rows and blocks g == w / WM
-// (mod WN), WM * WN = 8.  S = Q K^T (A = Q rows, B = K via ldmatrix), P stays
-// in registers as the A operand of O += P V (B = V via ldmatrix.trans).
-template <int D, int BS, bool OUT_F32>
-__device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t* stages,
-                                             float* scratch, uint64_t* full_bar,
-                                             uint64_t* empty_bar, volatile int* s_abort,
-                                             int4& info0, int4& info1) {
-    using C = AttnCfg<D, BS, kModeWide>;
-    constexpr int kStages = C::kStages;
-    constexpr int NT = D / 8;    // 8-wide output column tiles
-    constexpr int KT = D / 16;   // 16-deep k steps over head_dim
-    constexpr int PT = BS / 16;  // 16-token chunks per block
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int WM = a.warp_rows;
-    const int WN = kConsumerWarps / WM;
-    const int mt = warp % WM;   // which 16-row slice of the unit's rows
-    const int col = warp / WM;  // which residue class of blocks
-    const int g = lane >> 2, t = lane & 3;
-    const int mi = lane >> 3, rr = lane & 7;
-    const int G = a.group, cta = blockIdx.x;
-
-    uint32_t gbase = 0;
-    bool ok = true;
-    int piece = 0;
-    while (w.left > 0) {
-        const int j0 = w.j, j1 = piece_end(w);
-        const int ctx = w.ctx, s = w.s, h = w.h;
-
-        // Query fragments of this unit's two rows per thread (rows >= a.rows are zero).
-        uint32_t qf[KT][4];
-        int lim[2], lo[2];  // row sees tokens lo..lim (lo = INT_MIN without a window)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int r = mt * 16 + g + hh * 8;
-            const bool valid = r < a.rows;
-            const int i = valid ? r / G : 0;
-            const int hq = h * G + (valid ? r % G : 0);
-            lim[hh] = valid ? ctx - a.q_len + i : -1;
-            lo[hh] = a.window > 0 ? lim[hh] - a.window + 1 : INT_MIN;
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-                a.q + (((size_t)s * a.q_len + i) * a.n_q + hq) * D);
-#pragma unroll
-            for (int kk = 0; kk < KT; ++kk) {
-                qf[kk][hh] = valid ? __ldg(qrow + kk * 8 + t) : 0u;
-                qf[kk][2 + hh] = valid ? __ldg(qrow + kk * 8 + 4 + t) : 0u;
-            }
-        }
-        const int lim_min = ctx - a.q_len;  // smallest causal limit of a real row
-        const int lo_max = a.window > 0 ? ctx - a.window : INT_MIN;  // largest lower limit
-
-        float o[NT][4];
-#pragma unroll
-        for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
-        const int first = static_cast<int>((uint32_t)(col + WN - (int)(gbase % WN)) % WN);
-        for (int jj = first; jj < j1 - j0; jj += WN) {
-            const int j = j0 + jj;
-            const uint32_t gidx = gbase + jj;
-            const uint32_t stage = gidx % kStages;
-            ok = consumer_wait(a, &full_bar[stage], (gidx / kStages) & 1u, ok, s_abort);
-            if (ok) {
-                const uint32_t kbase = smem_addr(stages + stage * C::kStageBytes);
-                const uint32_t vbase = kbase + C::kTileBytes;
-
-                // The block is taken 16 tokens at a time (one online-softmax
-                // update per chunk), which keeps the live registers low.
-#pragma unroll 1
-                for (int tp = 0; tp < PT; ++tp) {
-                    // ---- S = Q K^T over 16 tokens
-                    float sc[2][4];
-#pragma unroll
-                    for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-                    for (int kk = 0; kk < KT; ++kk) {
-                        uint32_t b[4];
-                        ldmatrix_x4(b, kbase + swz<BS>(tp * 16 + (mi >> 1) * 8 + rr,
-                                                        kk * 16 + (mi & 1) * 8));
-                        mma_bf16_16816(sc[0], qf[kk], b[0], b[1]);
-                        mma_bf16_16816(sc[1], qf[kk], b[2], b[3]);
-                    }
-
-                    // ---- scale, causal / window / tail mask, online softmax (base 2)
-                    const int tok0 = j * BS + tp * 16;
-                    const bool need_mask = tok0 + 15 > lim_min || tok0 < lo_max;
-                    float mloc[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                    for (int n = 0; n < 2; ++n) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float x = sc[n][e] * a.scale_log2;
-                            const int tk = tok0 + n * 8 + 2 * t + (e & 1);
-                            if (need_mask && (tk > lim[e >> 1] || tk < lo[e >> 1])) x = -INFINITY;
-                            sc[n][e] = x;
-                            mloc[e >> 1] = fmaxf(mloc[e >> 1], x);
-                        }
-                    }
-                    float alpha[2], mbase[2];
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        mloc[hh] = fmaxf(mloc[hh], __shfl_xor_sync(0xffffffffu, mloc[hh], 1));
-                        mloc[hh] = fmaxf(mloc[hh], __shfl_xor_sync(0xffffffffu, mloc[hh], 2));
-                        const float mnew = fmaxf(m[hh], mloc[hh]);
-                        mbase[hh] = mnew == -INFINITY ? 0.f : mnew;
-                        alpha[hh] = fast_exp2(m[hh] - mbase[hh]);
-                        m[hh] = mnew;
-                    }
-                    float rsum[2] = {0.f, 0.f};
-#pragma unroll
-                    for (int n = 0; n < 2; ++n) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float p = fast_exp2(sc[n][e] - mbase[e >> 1]);
-                            sc[n][e] = p;
-                            rsum[e >> 1] += p;
-                        }
-                    }
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) l[hh] = l[hh] * alpha[hh] + rsum[hh];
-                    if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
-#pragma unroll
-                        for (int n = 0; n < NT; ++n) {
-                            o[n][0] *= alpha[0];
-                            o[n][1] *= alpha[0];
-                            o[n][2] *= alpha[1];
-                            o[n][3] *= alpha[1];
-                        }
-                    }
-
-                    // ---- P as bf16 A fragments (fp32 output: hi + lo pair)
-                    uint32_t pa[4], pl[4];
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        const int n = q2 >> 1;
-                        const int e = (q2 & 1) * 2;
-                        const float p0 = sc[n][e], p1 = sc[n][e + 1];
-                        pa[q2] = pack_bf16x2(p0, p1);
-                        if (OUT_F32)
-                            pl[q2] = pack_bf16x2(p0 - bf16_lo_to_f32(pa[q2]),
-                                                 p1 - bf16_hi_to_f32(pa[q2]));
-                    }
-
-                    // ---- O += P V (V rows past the context are zeroed: they may hold NaN)
-                    uint32_t vm0 = 0xFFFFFFFFu, vm8 = 0xFFFFFFFFu;
-                    if (tok0 + 16 > ctx) {
-                        const int ta = tok0 + 2 * t;
-                        vm0 = (ta < ctx ? 0x0000FFFFu : 0u) | (ta + 1 < ctx ? 0xFFFF0000u : 0u);
-                        vm8 = (ta + 8 < ctx ? 0x0000FFFFu : 0u) | (ta + 9 < ctx ? 0xFFFF0000u : 0u);
-                    }
-#pragma unroll
-                    for (int dp = 0; dp < D / 16; ++dp) {
-                        uint32_t b[4];
-                        ldmatrix_x4_trans(b, vbase + swz<BS>(tp * 16 + (mi & 1) * 8 + rr,
-                                                              dp * 16 + (mi >> 1) * 8));
-                        b[0] &= vm0;
-                        b[1] &= vm8;
-                        b[2] &= vm0;
-                        b[3] &= vm8;
-                        mma_bf16_16816(o[2 * dp], pa, b[0], b[1]);
-                        mma_bf16_16816(o[2 * dp + 1], pa, b[2], b[3]);
-                        if (OUT_F32) {
-                            mma_bf16_16816(o[2 * dp], pl, b[0], b[1]);
-                            mma_bf16_16816(o[2 * dp + 1], pl, b[2], b[3]);
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[stage]);
-        }
-        gbase += j1 - j0;
-
-        // ---- row sums across the quad, then combine the WN column partials
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 1);
-            l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 2);
-        }
-        for (int step = WN >> 1; step >= 1; step >>= 1) {
-            if (col >= step && col < 2 * step) {
-                float* sl = scratch + (size_t)((col - step) * WM + mt) * 32 * C::kLaneFloats;
-#pragma unroll
-                for (int n = 0; n < NT; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sl[(n * 4 + e) * 32 + lane] = o[n][e];
-                sl[(NT * 4 + 0) * 32 + lane] = m[0];
-                sl[(NT * 4 + 1) * 32 + lane] = m[1];
-                sl[(NT * 4 + 2) * 32 + lane] = l[0];
-                sl[(NT * 4 + 3) * 32 + lane] = l[1];
-            }
-            named_barrier_sync(1, kConsumerThreads);
-            if (col < step) {
-                const float* sl = scratch + (size_t)(col * WM + mt) * 32 * C::kLaneFloats;
-                float a1[2], a2[2];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-                    merge_weights(m[hh], l[hh], sl[(NT * 4 + hh) * 32 + lane],
-                                  sl[(NT * 4 + 2 + hh) * 32 + lane], a1[hh], a2[hh]);
-#pragma unroll
-                for (int n = 0; n < NT; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o[n][e] = a1[e >> 1] * o[n][e] + a2[e >> 1] * sl[(n * 4 + e) * 32 + lane];
-            }
-            named_barrier_sync(1, kConsumerThreads);
-        }
-
-        // ---- emit: a whole unit goes straight to `out`; a piece becomes a record
-        const bool first_piece = j0 == w.jlo, last_piece = j1 == w.nb;
-        if (col == 0) {
-            if (first_piece && last_piece) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = mt * 16 + g + hh * 8;
-                    if (r >= a.rows) continue;
-                    const int i = r / G, hq = h * G + r % G;
-                    const float inv = l[hh] > 0.f ? 1.f / l[hh] : 0.f;
-                    const size_t ob = (((size_t)s * a.q_len + i) * a.n_q + hq) * D;
-#pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        const float v0 = o[n][2 * hh] * inv, v1 = o[n][2 * hh + 1] * inv;
-                        if (OUT_F32)
-                            *reinterpret_cast<float2*>(static_cast<float*>(a.out) + ob + n * 8 +
-                                                       2 * t) = make_float2(v0, v1);
-                        else
-                            *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + ob +
-                                                         n * 8 + 2 * t) = pack_bf16x2(v0, v1);
-                    }
-                }
-            } else {
-                const int slot = piece == 0 ? 0 : 1;
-                const size_t rec = (size_t)cta * 2 + slot;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = mt * 16 + g + hh * 8;
-                    if (r >= a.rows) continue;
-                    float* ro = a.rec_o + (rec * a.rows + r) * D;
-#pragma unroll
-                    for (int n = 0; n < NT; ++n)
-                        *reinterpret_cast<float2*>(ro + n * 8 + 2 * t) =
-                            make_float2(o[n][2 * hh], o[n][2 * hh + 1]);
-                    if (t == 0)
-                        *reinterpret_cast<float2*>(a.rec_ml + (rec * a.rows + r) * 2) =
-                            make_float2(m[hh], l[hh]);
-                }
-                const int4 rinfo = make_int4(
-                    s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0), 0);
-                if (slot == 0)
-                    info0 = rinfo;
-                else
-                    info1 = rinfo;
-            }
-        }
-        ++piece;
-        w.left -= j1 - w.j;
-        if (w.left > 0) walk_next_unit<BS>(a, w);
-    }
-}
-
-// ===================== TMEM consumer (rows > 64) =====================
-// One 128-row tile per unit (rows >= R are zero), accumulators in TMEM.
-//   warp 4, lane 0 -- QK issuer: S[g&1] = Q K_g^T (tcgen05.mma; A = Q tile,
-//                     B = K stage, both K-major), as soon as the stage has
-//                     landed and the softmax has loaded S[g&1] of block g-2;
-//   warps 0..3     -- softmax, one thread per row (TMEM lane = row, so a row's
-//                     max and sum never leave the thread): P[g&1] = bf16 of
-//                     2^(S*scale - m) into TMEM, running sum l; O is rescaled
-//                     in TMEM only when a row's max grew by more than 2^8 (the
-//                     stale max is used consistently in P and l: exact);
-//   warp 5, lane 0 -- PV issuer: O += P[g&1] V_g (A from TMEM, B = V stage,
-//                     MN-major), then releases the stage.
-// Scores therefore run up to two blocks ahead of the softmax, and the PV
-// update of a block overlaps the softmax of the next.
-template <int D, int BS, bool OUT_F32>
-__device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t* stages,
-                                             uint8_t* qtile, uint64_t* full_bar,
-                                             uint64_t* empty_bar, uint64_t* tcb,
-                                             uint32_t* s_tmem, volatile int* s_abort,
-                                             int4& info0, int4& info1) {
-    using C = AttnCfg<D, BS, kModeTmem>;
-    constexpr int kStages = C::kStages;
-    constexpr uint32_t kTmemCols = 256;
-    constexpr uint32_t kColO = 0, kColS = 128, kColP = 192, kColPL = 224;
-    constexpr int KT = D / 16;   // k steps of S = Q K^T
-    constexpr int PK = BS / 16;  // k steps of O += P V
-    constexpr int kQHalf = 128 * 128;  // bytes of one 64-column half of the Q tile
-    constexpr int kParty = 192;        // warps 0..5 take part in this mode
-    // tcb: [0..1] S ready, [2..3] S read, [4..5] P ready, [6..7] PV done, [8] QK teardown,
-    //      [9] PV teardown
-    uint64_t* s_full = tcb;
-    uint64_t* s_free = tcb + 2;
-    uint64_t* p_full = tcb + 4;
-    uint64_t* pv_done = tcb + 6;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp > 5) return;  // warps 6, 7 have no part in this mode
-    const bool softmax = warp < 4;
-    const int row = threadIdx.x;  // softmax threads: row = TMEM lane
-    const int R = a.rows, G = a.group, cta = blockIdx.x;
-
-    if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
-    tc_fence_before();
-    named_barrier_sync(2, kParty);
-    tc_fence_after();
-    const uint32_t tbase = *s_tmem;
-    const uint32_t tlane = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t idesc_qk = umma_idesc_bf16(128, BS, false);
-    const uint32_t idesc_pv = umma_idesc_bf16(128, D, true);
-    const uint32_t q_saddr = smem_addr(qtile);
-
-    auto issuer_fail = [&](bool& ok) {
-        ok = false;
-        atomicOr(a.err, kErrTimeout);
-        *s_abort = 1;
-    };
-
-    uint32_t gbase = 0;
-    bool ok = true;
-    int piece = 0;
-    while (w.left > 0) {
-        const int j0 = w.j, j1 = piece_end(w), n = j1 - j0;
-        const int ctx = w.ctx, s = w.s, h = w.h;
-        int lim = -1, lo = INT_MIN, i_row = 0, hq_row = 0;
-        if (softmax) {
-            // This unit's query rows into the swizzled Q tile (the previous
-            // unit's score products finished: each of them was waited for).
-            const bool valid = row < R;
-            i_row = valid ? row / G : 0;
-            hq_row = h * G + (valid ? row % G : 0);
-            lim = valid ? ctx - a.q_len + i_row : -1;
-            if (a.window > 0) lo = lim - a.window + 1;
-            const uint4* qrow = reinterpret_cast<const uint4*>(
-                a.q + (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D);
-            uint4 qv[D / 8];
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) qv[c] = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c)
-                *reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + row * 128 +
-                                          (((c & 7) ^ (row & 7)) << 4)) = qv[c];
-            fence_proxy_async_smem();
-        }
-        tc_fence_before();
-        named_barrier_sync(2, kParty);  // Q tile ready; the previous unit's O has been read
-        tc_fence_after();
-
-        if (warp == 4) {
-            // ===================== QK issuer =====================
-            if (lane == 0 && ok) {
-                for (int b = 0; b < n; ++b) {
-                    const uint32_t g = gbase + b, st = g % kStages;
-                    if (*s_abort || !mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u)) {
-                        issuer_fail(ok);
-                        break;
-                    }
-                    if (g >= 2 && !mbar_wait_bounded(&s_free[g & 1u], ((g - 2) >> 1) & 1u)) {
-                        issuer_fail(ok);
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t kb = smem_addr(stages + st * C::kStageBytes);
-                    const uint32_t scol = tbase + kColS + (g & 1u) * BS;
-#pragma unroll
-                    for (int kk = 0; kk < KT; ++kk) {
-                        const uint64_t ad =
-                            umma_smem_desc(q_saddr + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd =
-                            umma_smem_desc(kb + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
-                        umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit(&s_full[g & 1u]);
-                }
-            }
-            __syncwarp();
-        } else if (warp == 5) {
-            // ===================== PV issuer =====================
-            if (lane == 0 && ok) {
-                for (int b = 0; b < n; ++b) {
-                    const uint32_t g = gbase + b, st = g % kStages;
-                    if (*s_abort || !mbar_wait_bounded(&p_full[g & 1u], (g >> 1) & 1u)) {
-                        issuer_fail(ok);
-                        break;
-                    }
-                    tc_fence_after();
-                    // The softmax saw S of this block, so its score product
-                    // (the only other reader of the stage) has completed.
-                    const uint32_t vb = smem_addr(stages + st * C::kStageBytes) + C::kTileBytes;
-                    const uint32_t pcol = tbase + kColP + (g & 1u) * (BS / 2);
-#pragma unroll
-                    for (int kk = 0; kk < PK; ++kk) {
-                        const uint64_t bd = umma_smem_desc(vb + kk * 16 * 128, C::kBoxBytes, 1024);
-                        umma_ts(tbase + kColO, pcol + kk * 8, bd, idesc_pv,
-                                (b > 0 || kk > 0) ? 1u : 0u);
-                        if (OUT_F32)
-                            umma_ts(tbase + kColO, tbase + kColPL + (g & 1u) * (BS / 2) + kk * 8, bd,
-                                    idesc_pv, 1u);
-                    }
-                    umma_commit(&empty_bar[st]);    // K and V of this stage are consumed
-                    umma_commit(&pv_done[g & 1u]);  // its P buffer is free; O is current
-                }
-            }
-            __syncwarp();
-        } else {
-            // ===================== softmax (thread = row) =====================
-            float m_used = -INFINITY, l = 0.f;
-            const int lim_min = ctx - a.q_len;
-            const int lo_max = a.window > 0 ? ctx - a.window : INT_MIN;
-            for (int b = 0; b < n; ++b) {
-                const uint32_t g = gbase + b;
-                ok = consumer_wait(a, &s_full[g & 1u], (g >> 1) & 1u, ok, s_abort);
-                if (!ok) continue;
-                tc_fence_after();
-                float x[BS];
-                {
-                    uint32_t sr[BS];
-                    if constexpr (BS == 32)
-                        tmem_ld32(tlane + kColS + (g & 1u) * BS, sr);
-                    else
-                        tmem_ld16(tlane + kColS + (g & 1u) * BS, sr);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(&s_free[g & 1u]);  // S buffer may take the block after next
-#pragma unroll
-                    for (int c = 0; c < BS; ++c) x[c] = __uint_as_float(sr[c]) * a.scale_log2;
-                }
-                const int tok0 = (j0 + b) * BS;
-                float mloc = -INFINITY;
-                if (tok0 + BS - 1 > lim_min || tok0 < lo_max) {
-#pragma unroll
-                    for (int c = 0; c < BS; ++c)
-                        if (tok0 + c > lim || tok0 + c < lo) x[c] = -INFINITY;
-                }
-#pragma unroll
-                for (int c = 0; c < BS; ++c) mloc = fmaxf(mloc, x[c]);
-                // This block's P buffer was last read by PV two blocks back.
-                if (b > 1) {
-                    ok = consumer_wait(a, &pv_done[g & 1u], ((g - 2) >> 1) & 1u, ok, s_abort);
-                    if (!ok) continue;
-                    tc_fence_after();
-                }
-                const bool grow = mloc > m_used + 8.f;
-                if (__any_sync(0xffffffffu, grow)) {
-                    // O may only be rescaled once the previous block's PV is done.
-                    if (b > 0) {
-                        ok = consumer_wait(a, &pv_done[(g - 1) & 1u], ((g - 1) >> 1) & 1u, ok,
-                                           s_abort);
-                        if (!ok) continue;
-                        tc_fence_after();
-                    }
-                    const float m_new = grow ? mloc : m_used;
-                    const float alpha = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
-                    l *= alpha;
-                    if (b > 0) {
-#pragma unroll 1
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t ov[32];
-                            tmem_ld32(tlane + kColO + c0, ov);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int c = 0; c < 32; ++c)
-                                ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-                            tmem_st32(tlane + kColO + c0, ov);
-                        }
-                        tmem_wait_st();
-                    }
-                    m_used = m_new;
-                }
-                uint32_t ph[BS / 2], pl[BS / 2];
-                float rs = 0.f;
-#pragma unroll
-                for (int c = 0; c < BS; c += 2) {
-                    const float p0 = m_used == -INFINITY ? 0.f : fast_exp2(x[c] - m_used);
-                    const float p1 = m_used == -INFINITY ? 0.f : fast_exp2(x[c + 1] - m_used);
-                    rs += p0 + p1;
-                    ph[c / 2] = pack_bf16x2(p0, p1);
-                    if (OUT_F32)
-                        pl[c / 2] = pack_bf16x2(p0 - bf16_lo_to_f32(ph[c / 2]),
-                                                p1 - bf16_hi_to_f32(ph[c / 2]));
-                }
-                l += rs;
-                if constexpr (BS == 32) {
-                    tmem_st16(tlane + kColP + (g & 1u) * (BS / 2), ph);
-                    if (OUT_F32) tmem_st16(tlane + kColPL + (g & 1u) * (BS / 2), pl);
-                } else {
-                    tmem_st8(tlane + kColP + (g & 1u) * (BS / 2), ph);
-                    if (OUT_F32) tmem_st8(tlane + kColPL + (g & 1u) * (BS / 2), pl);
-                }
-                tmem_wait_st();
-                // V rows past the context may hold NaN; 0 * NaN would poison O.
-                if (tok0 + BS > ctx) {
-                    uint8_t* vt = stages + (g % kStages) * C::kStageBytes + C::kTileBytes;
-                    const int valid = ctx - tok0;  // >= 1: the block holds a resident token
-                    const int chunks = (BS - valid) * 8;  // 16-byte chunks per 64-column half
-                    for (int q = row; q < chunks * (D / 64); q += 128) {
-                        const int half = q / chunks, rq = q % chunks;
-                        *reinterpret_cast<uint4*>(vt + half * C::kBoxBytes + valid * 128 + rq * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
-                }
-                tc_fence_before();
-                mbar_arrive(&p_full[g & 1u]);
-            }
-
-            // ---- epilogue: the last PV, then O out of TMEM row by row
-            if (n > 0) {
-                const uint32_t gl = gbase + n - 1;
-                ok = consumer_wait(a, &pv_done[gl & 1u], (gl >> 1) & 1u, ok, s_abort);
-            }
-            tc_fence_after();
-            const bool first_piece = j0 == w.jlo, last_piece = j1 == w.nb;
-            const bool whole = first_piece && last_piece;
-            if (ok) {
-                const float scl = whole ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
-                const size_t rec = (size_t)cta * 2 + (piece == 0 ? 0 : 1);
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t ov[32];
-                    tmem_ld32(tlane + kColO + c0, ov);
-                    tmem_wait_ld();
-                    if (row < R) {
-                        if (whole) {
-                            const size_t ob =
-                                (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D + c0;
-                            if (OUT_F32) {
-                                float4* op = reinterpret_cast<float4*>(static_cast<float*>(a.out) + ob);
-#pragma unroll
-                                for (int c = 0; c < 32; c += 4)
-                                    op[c / 4] = make_float4(__uint_as_float(ov[c]) * scl,
-                                                            __uint_as_float(ov[c + 1]) * scl,
-                                                            __uint_as_float(ov[c + 2]) * scl,
-                                                            __uint_as_float(ov[c + 3]) * scl);
-                            } else {
-                                uint4* op = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ob);
-#pragma unroll
-                                for (int c = 0; c < 32; c += 8)
-                                    op[c / 8] = make_uint4(
-                                        pack_bf16x2(__uint_as_float(ov[c]) * scl, __uint_as_float(ov[c + 1]) * scl),
-                                        pack_bf16x2(__uint_as_float(ov[c + 2]) * scl, __uint_as_float(ov[c + 3]) * scl),
-                                        pack_bf16x2(__uint_as_float(ov[c + 4]) * scl, __uint_as_float(ov[c + 5]) * scl),
-                                        pack_bf16x2(__uint_as_float(ov[c + 6]) * scl, __uint_as_float(ov[c + 7]) * scl));
-                            }
-                        } else {
-                            float4* op = reinterpret_cast<float4*>(a.rec_o + (rec * R + row) * D + c0);
-#pragma unroll
-                            for (int c = 0; c < 32; c += 4)
-                                op[c / 4] = make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]),
-                                                        __uint_as_float(ov[c + 2]), __uint_as_float(ov[c + 3]));
-                        }
-                    }
-                }
-                if (!whole) {
-                    if (row < R)
-                        *reinterpret_cast<float2*>(a.rec_ml + (rec * R + row) * 2) = make_float2(m_used, l);
-                    if (row == 0) {
-                        const int4 rinfo = make_int4(
-                            s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0), 0);
-                        if (piece == 0)
-                            info0 = rinfo;
-                        else
-                            info1 = rinfo;
-                    }
-                }
-            }
-            tc_fence_before();
-        }
-        gbase += n;
-        ++piece;
-        w.left -= j1 - w.j;
-        if (w.left > 0) walk_next_unit<BS>(a, w);
-    }
-    // Teardown: no tensor-core operation may still be running when TMEM is freed.
-    if ((warp == 4 || warp == 5) && lane == 0) {
-        uint64_t* bar = &tcb[warp == 4 ? 8 : 9];
-        umma_commit(bar);
-        (void)mbar_wait_bounded(bar, 0u);
-    }
-    tc_fence_before();
-    named_barrier_sync(2, kParty);
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
-}
-
-// ===================== kernel =====================
-template <int D, int BS, bool OUT_F32, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-    paged_decode_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                             const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
-    using C = AttnCfg<D, BS, MODE>;
-    constexpr int kStages = C::kStages;
-
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_addr(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    uint8_t* stages = smem;
-    float* scratch = reinterpret_cast<float*>(smem + kStages * C::kStageBytes);
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes +
-                                                     C::kScratchBytes);
-    uint64_t* empty_bar = full_bar + kStages;
-
-    __shared__ long long s_red[kThreads / 32];
-    __shared__ long long s_start[2];
-    __shared__ int s_abort;
-    __shared__ uint64_t s_tcb[10];  // TMEM mode: S ready/read, P ready, PV done (x2 each), 2 teardowns
-    __shared__ uint32_t s_tmem;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // Arrivals that release a stage: one per 16-row slice (wide), one warp
-    // (narrow), one tensor-core commit (TMEM mode).
-    const int releases = MODE == kModeWide ? a.warp_rows : 1;
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], releases);
-        }
-        if (MODE == kModeTmem) {
-            // S ready (a commit), S read (128 rows), P ready (128 rows),
-            // PV done (a commit), two issuer teardowns (a commit each)
-            const uint32_t counts[10] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1};
-            for (int i = 0; i < 10; ++i) mbar_init(&s_tcb[i], counts[i]);
-        }
-        fence_barrier_init();
-        s_abort = 0;
-        s_start[0] = -1;
-        s_start[1] = 0;
-    }
-    if (warp == kConsumerWarps && lane == 0) {
-        prefetch_tensormap(&tmap_k);
-        prefetch_tensormap(&tmap_v);
-    }
-    const Walk w0 = find_slice<BS>(a, s_red, s_start);  // also publishes the barrier init
-    // Let the merge kernel (launched as a programmatic dependent) be scheduled
-    // early; it waits for this whole grid before reading anything.
-    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-    if (warp == kConsumerWarps) {
-        produce<D, BS, kStages, C::kStageBytes, C::kTileBytes, C::kBoxBytes>(
-            a, &tmap_k, &tmap_v, w0, stages, full_bar, empty_bar, &s_abort);
-        return;
-    }
-
-    // Sequences with nothing resident produce zero rows (and are checked).
-    for (int s = blockIdx.x; s < a.num_seqs; s += gridDim.x) {
-        const int raw = __ldg(a.context_lens + s);
-        if (a.checked && tid == 0 &&
-            (raw < 0 || raw > a.max_blocks_per_seq * BS || (raw > 0 && raw < a.q_len)))
-            atomicOr(a.err, kErrBadContext);
-        if (unit_blocks(a, s, BS) == 0) {
-            const size_t n = (size_t)a.q_len * a.n_q * D;
-            const size_t o0 = (size_t)s * n;
-            for (size_t e = tid; e < n; e += kConsumerThreads) {
-                if (OUT_F32)
-                    static_cast<float*>(a.out)[o0 + e] = 0.f;
-                else
-                    static_cast<uint16_t*>(a.out)[o0 + e] = 0;
-            }
-        }
-    }
-
-    int4 info0 = make_int4(0, 0, 0, 0), info1 = make_int4(0, 0, 0, 0);
-    if (w0.left <= 0) info0.z = info1.z = kRecEmpty;
-    if (MODE == kModeNarrow)
-        consume_narrow<D, BS, OUT_F32>(a, w0, stages, scratch, full_bar, empty_bar, &s_abort,
-                                       info0, info1);
-    else if (MODE == kModeWide)
-        consume_wide<D, BS, OUT_F32>(a, w0, stages, scratch, full_bar, empty_bar, &s_abort,
-                                     info0, info1);
-    else
-        consume_tmem<D, BS, OUT_F32>(a, w0, stages, reinterpret_cast<uint8_t*>(scratch), full_bar,
-                                     empty_bar, s_tcb, &s_tmem, &s_abort, info0, info1);
-    if (tid == 0) {
-        a.rec_info[(size_t)blockIdx.x * 2 + 0] = info0;
-        a.rec_info[(size_t)blockIdx.x * 2 + 1] = info1;
-    }
-}
-
-// ---------------------------------------------------------------------------
-template <int D, int BS, bool F32, int MODE>
-static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                              int grid, cudaStream_t stream) {
-    auto kern = paged_decode_attn_kernel<D, BS, F32, MODE>;
-    const int smem = AttnCfg<D, BS, MODE>::kSmemBytes;
-    // The shared-memory opt-in is set once per device for each instantiation.
-    static std::atomic<unsigned long long> opted_in{0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(opted_in.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        opted_in.fetch_or(bit, std::memory_order_release);
-    }
-    kern<<<grid, kThreads, smem, stream>>>(tk, tv, a);
-    return cudaGetLastError();
-}
-
-template <int D, int BS>
-static cudaError_t launch_shape(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                                bool out_f32, int grid, cudaStream_t stream) {
-    if (a.rows <= kNarrowRows)
-        return out_f32 ? launch_one<D, BS, true, kModeNarrow>(a, tk, tv, grid, stream)
-                       : launch_one<D, BS, false, kModeNarrow>(a, tk, tv, grid, stream);
-    if (a.rows > kTmemMinRows)
-        return out_f32 ? launch_one<D, BS, true, kModeTmem>(a, tk, tv, grid, stream)
-                       : launch_one<D, BS, false, kModeTmem>(a, tk, tv, grid, stream);
-    return out_f32 ? launch_one<D, BS, true, kModeWide>(a, tk, tv, grid, stream)
-                   : launch_one<D, BS, false, kModeWide>(a, tk, tv, grid, stream);
-}
 
 cudaError_t launch_decode_attn(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                int head_dim, int block_size, bool out_f32, int grid,
                                cudaStream_t stream) {
-    if (head_dim == 128 && block_size == 16)
-        return launch_shape<128, 16>(a, tk, tv, out_f32, grid, stream);
-    if (head_dim == 128 && block_size == 32)
-        return launch_shape<128, 32>(a, tk, tv, out_f32, grid, stream);
-    if (head_dim == 64 && block_size == 16)
-        return launch_shape<64, 16>(a, tk, tv, out_f32, grid, stream);
-    if (head_dim == 64 && block_size == 32)
-        return launch_shape<64, 32>(a, tk, tv, out_f32, grid, stream);
-    return cudaErrorInvalidValue;
+    return launch_decode_attn_kv<false>(a, tk, tv, head_dim, block_size, out_f32, grid, stream);
 }
 
 }  // namespace pkv

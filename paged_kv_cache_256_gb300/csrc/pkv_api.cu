@@ -46,19 +46,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D view of a cache: rows = num_blocks * n_kv * block_size, columns = head_dim
-// bf16; one box = 64 columns x block_size rows with the 128-byte swizzle.
+// 2-D view of a cache: rows = num_blocks * n_kv * block_size, columns =
+// head_dim elements.  bf16: one box = 64 columns x block_size rows with the
+// 128-byte swizzle.  e4m3 (kv8): one box = a whole row of head_dim bytes x
+// block_size rows, 128-byte swizzle at head_dim 128, 64-byte at 64.
 bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, long long rows,
-                    int block_size) {
+                    int block_size, bool kv8) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)block_size};
+    cuuint64_t strides[1] = {(cuuint64_t)head_dim * (kv8 ? 1 : 2)};
+    cuuint32_t box[2] = {kv8 ? (cuuint32_t)head_dim : 64u, (cuuint32_t)block_size};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUtensorMapSwizzle swz = (!kv8 || head_dim == 128) ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                             : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUresult r = fn(map, kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -69,6 +74,7 @@ struct MapKey {
     const void* base;
     long long rows;
     int head_dim, block_size;
+    bool kv8;
 };
 struct MapEntry {
     MapKey key;
@@ -81,18 +87,18 @@ MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 
 bool cached_cache_map(CUtensorMap* map, const void* base, int head_dim, long long rows,
-                      int block_size) {
+                      int block_size, bool kv8) {
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (const MapEntry& e : g_maps)
         if (e.used && e.key.base == base && e.key.rows == rows && e.key.head_dim == head_dim &&
-            e.key.block_size == block_size) {
+            e.key.block_size == block_size && e.key.kv8 == kv8) {
             *map = e.map;
             return true;
         }
-    if (!make_cache_map(map, base, head_dim, rows, block_size)) return false;
+    if (!make_cache_map(map, base, head_dim, rows, block_size, kv8)) return false;
     MapEntry& e = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % kMapCache;
-    e.key = MapKey{base, rows, head_dim, block_size};
+    e.key = MapKey{base, rows, head_dim, block_size, kv8};
     e.map = *map;
     e.used = true;
     return true;
@@ -142,7 +148,7 @@ using namespace pkv;
 
 extern "C" {
 
-int pkv_version(void) { return 10000; }
+int pkv_version(void) { return 10200; }
 
 const char* pkv_status_string(int status) {
     switch (status) {
@@ -203,6 +209,7 @@ int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cach
     p.workspace_bytes = workspace_bytes;
     p.flags = flags;
     p.window = 0;
+    p.kv_dtype = PKV_KV_BF16;
     return pkv_paged_decode_attn_ex(&p, stream);
 }
 
@@ -225,7 +232,11 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     if (max_blocks_per_seq < 1 || num_blocks < 1) return PKV_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     if (p->window < 0) return PKV_ERR_INVALID_ARG;
+    if (p->kv_dtype != PKV_KV_BF16 && p->kv_dtype != PKV_KV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+    const bool kv8 = p->kv_dtype == PKV_KV_FP8_E4M3;
     if (num_seqs == 0) return PKV_OK;
+    if (kv8 && (!p->k_scale || !p->v_scale || !aligned(p->k_scale, 4) || !aligned(p->v_scale, 4)))
+        return PKV_ERR_INVALID_ARG;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
         return PKV_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
@@ -250,8 +261,8 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
         return PKV_ERR_WORKSPACE;
 
     CUtensorMap tk, tv;
-    if (!cached_cache_map(&tk, k_cache, head_dim, rows_total, block_size) ||
-        !cached_cache_map(&tv, v_cache, head_dim, rows_total, block_size))
+    if (!cached_cache_map(&tk, k_cache, head_dim, rows_total, block_size, kv8) ||
+        !cached_cache_map(&tv, v_cache, head_dim, rows_total, block_size, kv8))
         return PKV_ERR_CUDA;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -274,6 +285,8 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     a.num_blocks = num_blocks;
     a.tile_rows_total = (int)rows_total;
     a.warp_rows = warp_rows_for(rows);
+    a.k_scale = kv8 ? p->k_scale : nullptr;
+    a.v_scale = kv8 ? p->v_scale : nullptr;
     // A window at least as wide as any context is no window.
     a.window = (long long)p->window >= (long long)max_blocks_per_seq * block_size ? 0 : p->window;
     a.checked = (flags & PKV_FLAG_CHECKED) ? 1 : 0;
@@ -282,8 +295,9 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool f32 = out_dtype == PKV_OUT_F32;
-    if (launch_decode_attn(a, tk, tv, head_dim, block_size, f32, grid, s) != cudaSuccess)
-        return PKV_ERR_CUDA;
+    const cudaError_t le = kv8 ? launch_decode_attn_fp8(a, tk, tv, head_dim, block_size, f32, grid, s)
+                               : launch_decode_attn(a, tk, tv, head_dim, block_size, f32, grid, s);
+    if (le != cudaSuccess) return PKV_ERR_CUDA;
     if (grid > 1 && launch_lse_merge(a, head_dim, f32, grid, s) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
@@ -312,12 +326,38 @@ int pkv_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapp
     return PKV_OK;
 }
 
+int pkv_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                      int num_tokens, int n_kv, int head_dim, int block_size, int num_blocks,
+                      const float* k_scale, const float* v_scale, void* k_cache, void* v_cache,
+                      unsigned flags, void* stream) {
+    (void)flags;
+    if (num_tokens < 0 || n_kv < 1 || head_dim < 8 || head_dim % 8 != 0 || block_size < 1 ||
+        num_blocks < 1)
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 4) || !aligned(k_scale, 4) ||
+        !aligned(v_scale, 4))
+        return PKV_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return PKV_ERR_CUDA;
+    if (launch_kv_append_fp8(k_new, v_new, slot_mapping, num_tokens, n_kv, head_dim, block_size,
+                             num_blocks, k_scale, v_scale, k_cache, v_cache, sms,
+                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
 int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                     int num_blocks, int n_kv, int head_dim, int block_size, unsigned flags,
                     void* stream) {
-    (void)flags;
+    const int elem_bytes = (flags & PKV_FLAG_KV_FP8) ? 1 : 2;
     if (num_pairs < 0 || num_blocks < 1 || n_kv < 1 || head_dim < 8 || head_dim % 8 != 0 ||
-        block_size < 1)
+        block_size < 1 || ((long long)n_kv * block_size * head_dim * elem_bytes) % 16 != 0)
         return PKV_ERR_INVALID_ARG;
     if (num_pairs == 0) return PKV_OK;
     if (!k_cache || !v_cache || !pairs) return PKV_ERR_INVALID_ARG;
@@ -328,7 +368,7 @@ int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_
     const int sms = sm_count(dev);
     if (sms <= 0) return PKV_ERR_CUDA;
     if (launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_blocks, n_kv, head_dim,
-                           block_size, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                           block_size, elem_bytes, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
 }

@@ -35,6 +35,8 @@ struct AttnArgs {
     int num_blocks;
     int tile_rows_total;  // num_blocks * n_kv * block_size (rows of the 2-D cache view)
     int warp_rows;        // 16-row tiles per KV unit (1, 2, 4 or 8)
+    const float* k_scale;  // 8-bit caches: [n_kv] dequantisation scales (else unused)
+    const float* v_scale;
     int window;        // 0: full causal attention; W > 0: a row sees its last W positions
     int checked;
     int test_stall;    // failure-path tests: the producer issues nothing
@@ -52,6 +54,10 @@ cudaError_t launch_decode_attn(const AttnArgs& a, const CUtensorMap& tmap_k,
                                const CUtensorMap& tmap_v, int head_dim, int block_size,
                                bool out_f32, int grid, cudaStream_t stream);
 
+cudaError_t launch_decode_attn_fp8(const AttnArgs& a, const CUtensorMap& tmap_k,
+                                   const CUtensorMap& tmap_v, int head_dim, int block_size,
+                                   bool out_f32, int grid, cudaStream_t stream);
+
 cudaError_t launch_lse_merge(const AttnArgs& a, int head_dim, bool out_f32, int grid,
                              cudaStream_t stream);
 
@@ -60,8 +66,14 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
                              int num_blocks, void* k_cache, void* v_cache, int num_sms,
                              cudaStream_t stream);
 
+cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new,
+                                 const int32_t* slot_mapping, int num_tokens, int n_kv,
+                                 int head_dim, int block_size, int num_blocks,
+                                 const float* k_scale, const float* v_scale, void* k_cache,
+                                 void* v_cache, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, int n_kv, int head_dim, int block_size,
-                               int num_sms, cudaStream_t stream);
+                               int elem_bytes, int num_sms, cudaStream_t stream);
 
 }  // namespace pkv

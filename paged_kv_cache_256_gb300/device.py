@@ -50,3 +50,20 @@ def to_device(wl, device="cuda") -> DeviceWorkload:
         v_new=_to_cuda_bf16(wl.v_new, device),
         slot_mapping=_to_cuda_i32(wl.slot_mapping, device),
     )
+
+
+@dataclasses.dataclass
+class DeviceFp8Cache:
+    k_cache: object  # uint8 e4m3 codes
+    v_cache: object
+    k_scale: object  # float32 [n_kv]
+    v_scale: object
+
+
+def fp8_to_device(c, device="cuda") -> DeviceFp8Cache:
+    import torch
+    return DeviceFp8Cache(
+        k_cache=torch.from_numpy(np.ascontiguousarray(c.k_cache)).to(device),
+        v_cache=torch.from_numpy(np.ascontiguousarray(c.v_cache)).to(device),
+        k_scale=torch.from_numpy(np.ascontiguousarray(c.k_scale, dtype=np.float32)).to(device),
+        v_scale=torch.from_numpy(np.ascontiguousarray(c.v_scale, dtype=np.float32)).to(device))

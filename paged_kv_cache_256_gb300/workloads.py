@@ -29,6 +29,12 @@ per layer):
 * Block-table entries past a sequence's last block point at a poison block
   (always a valid index, never out of range).
 * Values: fp32 samples of N(0, 1) rounded to bf16 with round-to-nearest-even.
+
+An 8-bit variant of any workload (:func:`fp8_cache_for`) draws e4m3 codes
+directly -- random sign, exponent field 7 + round(N(0, 1.5)) clipped to
+[1, 14], uniform mantissa -- into the same resident slots, with the e4m3 NaN
+(0x7F) wherever the bf16 cache holds poison, and per-KV-head fp32 scales
+drawn from U(0.05, 0.5).  No quantiser is involved: the codes are the data.
 """
 from __future__ import annotations
 
@@ -41,6 +47,9 @@ import numpy as np
 
 __all__ = [
     "BF16_POISON",
+    "E4M3_POISON",
+    "Fp8Cache",
+    "fp8_cache_for",
     "CONFIGS",
     "Workload",
     "f32_to_bf16_bits",
@@ -51,6 +60,8 @@ __all__ = [
 
 # A quiet NaN with a payload, so poison is recognisable in a dump.
 BF16_POISON = np.uint16(0x7FC1)
+# The e4m3 NaN (S.1111.111).
+E4M3_POISON = np.uint8(0x7F)
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -173,6 +184,52 @@ def _normal_bf16(seed_seq: np.random.SeedSequence, shape, scale_per=None, chunk=
         with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
             list(ex.map(work, range(nchunks)))
     return out.reshape(shape)
+
+
+def _e4m3_codes(seed_seq: np.random.SeedSequence, n: int, chunk=1 << 23) -> np.ndarray:
+    """n seeded e4m3 codes: sign, exponent field 7 + rint(N(0, 1.5)) in [1, 14], mantissa."""
+    out = np.empty(n, dtype=np.uint8)
+    nchunks = (n + chunk - 1) // chunk
+    kids = seed_seq.spawn(max(nchunks, 1))
+
+    def work(c):
+        lo, hi = c * chunk, min(n, (c + 1) * chunk)
+        g = np.random.Generator(np.random.PCG64(kids[c]))
+        e = np.clip(np.rint(7.0 + 1.5 * g.standard_normal(hi - lo, dtype=np.float32)), 1, 14)
+        bits = g.integers(0, 16, size=hi - lo, dtype=np.uint8)  # sign (bit 3) and mantissa
+        out[lo:hi] = ((bits & 8) << 4) | (e.astype(np.uint8) << 3) | (bits & 7)
+
+    if nchunks <= 1:
+        for c in range(nchunks):
+            work(c)
+    else:
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(work, range(nchunks)))
+    return out
+
+
+@dataclasses.dataclass
+class Fp8Cache:
+    k_cache: np.ndarray  # [num_blocks, n_kv, block_size, head_dim] e4m3 codes (uint8)
+    v_cache: np.ndarray
+    k_scale: np.ndarray  # [n_kv] float32: value of code c in head g = c * k_scale[g]
+    v_scale: np.ndarray
+
+
+def fp8_cache_for(wl: Workload, seed: int | None = None) -> Fp8Cache:
+    """Seeded e4m3 caches laid out like ``wl``'s (same resident and poison slots)."""
+    if seed is None:
+        seed = 5000 + sum(wl.name.encode())
+    s_k, s_v, s_s = np.random.SeedSequence([seed, 11]).spawn(3)
+    n = wl.k_cache.size
+    k8 = _e4m3_codes(s_k, n).reshape(wl.k_cache.shape)
+    v8 = _e4m3_codes(s_v, n).reshape(wl.v_cache.shape)
+    k8[wl.k_cache == BF16_POISON] = E4M3_POISON
+    v8[wl.v_cache == BF16_POISON] = E4M3_POISON
+    r = np.random.Generator(np.random.PCG64(s_s))
+    ks = r.uniform(0.05, 0.5, size=wl.n_kv).astype(np.float32)
+    vs = r.uniform(0.05, 0.5, size=wl.n_kv).astype(np.float32)
+    return Fp8Cache(k_cache=k8, v_cache=v8, k_scale=ks, v_scale=vs)
 
 
 def _draw_context_lens(rng, spec, num_seqs):
