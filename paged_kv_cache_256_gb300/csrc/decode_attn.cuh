@@ -463,6 +463,18 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                 for (int p = 0; p < PT; ++p)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) st[p][e] = st2[p][e] = 0.f;
+                // 8-bit V: every fragment of the block is read here, ahead of
+                // the score products and the softmax, so the shared-memory
+                // latency and the widening overlap with them.
+                uint32_t vr[KV8 ? PT : 1][KV8 ? D / 32 : 1][4];
+                if constexpr (KV8) {
+#pragma unroll
+                    for (int tp = 0; tp < PT; ++tp)
+#pragma unroll
+                        for (int j = 0; j < D / 32; ++j)
+                            ldmatrix_x4_trans(vr[tp][j], vb + swz8<D>(tp * 16 + (mi & 1) * 8 + rr,
+                                                                      32 * j + (mi >> 1) * 16));
+                }
                 if constexpr (KV8) {
                     // One x4 load: tokens (0-7, 8-15) x bytes (32j.., 32j+16..) = two k steps.
 #pragma unroll
@@ -595,9 +607,7 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                         // d 32j + 2g (+1) and 32j + 16 + 2g (+1)).
 #pragma unroll
                         for (int j = 0; j < D / 32; ++j) {
-                            uint32_t r[4];
-                            ldmatrix_x4_trans(r, vb + swz8<D>(tp * 16 + (mi & 1) * 8 + rr,
-                                                              32 * j + (mi >> 1) * 16));
+                            const uint32_t* r = vr[tp][j];
                             uint32_t ev[4], od[4];
 #pragma unroll
                             for (int m = 0; m < 4; ++m) {
