@@ -97,8 +97,15 @@ typedef enum pkv_status {
  *   are read; slots past the context in the last block are never used, and
  *   may hold any bits (NaN included).
  *
- * Supported: head_dim in {64, 128}; block_size in {16, 32};
- *   rows = (n_q / n_kv) * q_len <= 128; num_blocks * n_kv * block_size < 2^31.
+ * q_len new tokens per sequence: 1 for plain decoding, a few for a
+ *   speculative-verify step, or a whole prompt chunk (paged / chunked
+ *   prefill: the prompt pass before decoding, "Efficient inference", Two
+ *   phases, two bottlenecks; chunked prefill is named among the scheduling
+ *   techniques in "Transformer inference mechanics", A better connection map).  The rows = (n_q / n_kv) * q_len query rows that share a KV head
+ *   are processed in tiles of 128; each tile reads only the blocks its rows
+ *   can see.
+ * Supported: head_dim in {64, 128}; block_size in {16, 32}; q_len <= 65536;
+ *   rows <= 2^24; num_blocks * n_kv * block_size < 2^31.
  * Rows that see no key (context_lens[b] == 0, or < q_len) are written as zeros.
  *
  * workspace: device memory of at least pkv_paged_decode_attn_workspace_size(...)

@@ -154,41 +154,90 @@ __device__ __forceinline__ int unit_blocks(const AttnArgs& a, int s, int bs) {
     return (unit_ctx(a, s, bs) + bs - 1) / bs;
 }
 
-// First block any row of a unit can see: with a sliding window, the earliest
-// row (position ctx - q_len) sees nothing before ctx - q_len - W + 1, so the
-// blocks before that one are never read.  Always < the unit's block count.
-__device__ __forceinline__ int unit_first_block(const AttnArgs& a, int ctx, int bs) {
+// Query rows come in tiles of a.rows: row R = t * a.rows + r of a unit's
+// G * q_len rows belongs to query token R / G and query head h * G + R % G.
+// A decode step has one tile; a prefill chunk (many new tokens) has several,
+// each its own unit.  Tokens of tile t: first and last.
+__device__ __forceinline__ int tile_first_token(const AttnArgs& a, int t) {
+    return (t * a.rows) / a.group;
+}
+__device__ __forceinline__ int tile_last_token(const AttnArgs& a, int t) {
+    const int last_row = min(a.rows_total, (t + 1) * a.rows) - 1;
+    return last_row / a.group;
+}
+
+// Row r of tile t: its query token i and query head hq; false for padding
+// rows past the last real row.
+__device__ __forceinline__ bool unit_row(const AttnArgs& a, int t, int h, int r, int& i,
+                                         int& hq) {
+    const int R = t * a.rows + r;
+    const bool valid = r < a.rows && R < a.rows_total;
+    i = valid ? R / a.group : 0;
+    hq = h * a.group + (valid ? R % a.group : 0);
+    return valid;
+}
+
+// One past the last block tile t can see: its last row sits at position
+// ctx - q_len + i_last and sees nothing later (causal).  At least one block
+// when ctx > 0, so a tile whose rows all precede the context still writes
+// its zero rows; none when ctx == 0.
+__device__ __forceinline__ int unit_end_block(const AttnArgs& a, int ctx, int t, int bs) {
+    long long vis = (long long)ctx - a.q_len + tile_last_token(a, t) + 1;
+    if (vis < 1) vis = 1;
+    if (vis > ctx) vis = ctx;
+    return static_cast<int>((vis + bs - 1) / bs);
+}
+
+// First block any row of tile t can see: with a sliding window, its earliest
+// row (position ctx - q_len + i_first) sees nothing before that position
+// minus W - 1, so earlier blocks are never read.  Always < unit_end_block.
+__device__ __forceinline__ int unit_first_block(const AttnArgs& a, int ctx, int t, int bs) {
     if (a.window <= 0) return 0;
-    const long long lo = (long long)ctx - a.q_len - a.window + 1;
+    const long long lo = (long long)ctx - a.q_len + tile_first_token(a, t) - a.window + 1;
     return lo > 0 ? static_cast<int>(lo / bs) : 0;
 }
 
-// Work items (blocks to read) of the units of sequence s: one per KV head each.
-__device__ __forceinline__ int unit_items(const AttnArgs& a, int s, int bs) {
-    const int ctx = unit_ctx(a, s, bs);
-    return (ctx + bs - 1) / bs - unit_first_block(a, ctx, bs);
+// Work items (blocks to read) of one KV head of sequence s, over all its tiles.
+__device__ __forceinline__ long long head_items(const AttnArgs& a, int ctx, int bs) {
+    if (ctx == 0) return 0;
+    long long n = 0;
+    for (int t = 0; t < a.q_tiles; ++t)
+        n += unit_end_block(a, ctx, t, bs) - unit_first_block(a, ctx, t, bs);
+    return n;
 }
 
-// Position in the flat work list: sequence s, KV head h, block j of that unit
-// (the unit reads blocks jlo .. nb-1), `left` items still to process in this
-// CTA's slice.
+// Position in the flat work list: sequence s, KV head h, row tile t, block j
+// of that unit (the unit reads blocks jlo .. nb-1), `left` items still to
+// process in this CTA's slice.  Units run tile-fastest, so the tiles of one
+// KV head (which read overlapping blocks) follow each other.
 struct Walk {
-    int s, h, j, jlo, nb, ctx;
+    int s, h, t, j, jlo, nb, ctx;
     long long left;
 };
 
 template <int BS>
-__device__ __forceinline__ void walk_next_unit(const AttnArgs& a, Walk& w) {
-    if (++w.h == a.n_kv) {
-        w.h = 0;
-        do {
-            ++w.s;
-            w.nb = w.s < a.num_seqs ? unit_blocks(a, w.s, BS) : 1;
-        } while (w.nb == 0);
-        w.ctx = w.s < a.num_seqs ? unit_ctx(a, w.s, BS) : 0;
-        w.jlo = unit_first_block(a, w.ctx, BS);
-    }
+__device__ __forceinline__ void walk_set_unit(const AttnArgs& a, Walk& w) {
+    w.nb = unit_end_block(a, w.ctx, w.t, BS);
+    w.jlo = unit_first_block(a, w.ctx, w.t, BS);
     w.j = w.jlo;
+}
+
+template <int BS>
+__device__ __forceinline__ void walk_next_unit(const AttnArgs& a, Walk& w) {
+    if (++w.t == a.q_tiles) {
+        w.t = 0;
+        if (++w.h == a.n_kv) {
+            w.h = 0;
+            do {
+                ++w.s;
+            } while (w.s < a.num_seqs && unit_ctx(a, w.s, BS) == 0);
+            w.ctx = w.s < a.num_seqs ? unit_ctx(a, w.s, BS) : 0;
+        }
+    }
+    walk_set_unit<BS>(a, w);
+    // The slices cover exactly the items of the units; a walk that ran past
+    // the last sequence stops instead of spinning on empty pieces.
+    if (w.s >= a.num_seqs) w.left = 0;
 }
 
 __device__ __forceinline__ int piece_end(const Walk& w) {
@@ -225,7 +274,7 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
                                            long long* s_start) {
     const int tid = threadIdx.x, cta = blockIdx.x, grid = gridDim.x;
     long long mine = 0;
-    for (int s = tid; s < a.num_seqs; s += kThreads) mine += unit_items(a, s, BS);
+    for (int s = tid; s < a.num_seqs; s += kThreads) mine += head_items(a, unit_ctx(a, s, BS), BS);
     long long total_blocks;
     (void)block_inclusive_scan(mine, s_red, total_blocks);
     const long long W = total_blocks * a.n_kv;
@@ -235,7 +284,8 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
         long long base = 0;
         for (int s0 = 0; s0 < a.num_seqs; s0 += kThreads) {
             const int s = s0 + tid;
-            const long long v = s < a.num_seqs ? (long long)unit_items(a, s, BS) * a.n_kv : 0;
+            const long long v =
+                s < a.num_seqs ? head_items(a, unit_ctx(a, s, BS), BS) * a.n_kv : 0;
             long long chunk;
             const long long incl = block_inclusive_scan(v, s_red, chunk);
             const long long excl = incl - v;
@@ -253,14 +303,20 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
     w.left = end - start;
     if (w.left > 0) {
         w.s = static_cast<int>(s_start[0]);
-        w.nb = unit_blocks(a, w.s, BS);
         w.ctx = unit_ctx(a, w.s, BS);
-        w.jlo = unit_first_block(a, w.ctx, BS);
-        const int items = w.nb - w.jlo;
-        w.h = static_cast<int>(s_start[1] / items);
-        w.j = w.jlo + static_cast<int>(s_start[1] % items);
+        const long long per_head = head_items(a, w.ctx, BS);
+        w.h = static_cast<int>(s_start[1] / per_head);
+        long long rem = s_start[1] % per_head;
+        w.t = 0;
+        walk_set_unit<BS>(a, w);
+        while (rem >= w.nb - w.jlo) {  // the tile holding the slice's first item
+            rem -= w.nb - w.jlo;
+            ++w.t;
+            walk_set_unit<BS>(a, w);
+        }
+        w.j = w.jlo + static_cast<int>(rem);
     } else {
-        w.s = w.h = w.j = w.jlo = w.nb = w.ctx = 0;
+        w.s = w.h = w.t = w.j = w.jlo = w.nb = w.ctx = 0;
     }
     return w;
 }
@@ -393,7 +449,7 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
     constexpr int WN = kConsumerWarps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3, mi = lane >> 3, rr = lane & 7;
-    const int G = a.group, R = a.rows, cta = blockIdx.x;
+    const int R = a.rows, cta = blockIdx.x;
     float* emit_tile = scratch + C::kMergeBytes / 4;
     float* emit_ml = emit_tile + kNarrowRows * C::kTileStride;
 
@@ -408,9 +464,8 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
         // 8-bit caches: f16, in the permuted k order of the K fragments.
         uint32_t qb[KT][2];
         {
-            const bool valid = g < R;
-            const int i = valid ? g / G : 0;
-            const int hq = h * G + (valid ? g % G : 0);
+            int i, hq;
+            const bool valid = unit_row(a, w.t, h, g, i, hq);
             const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
                 a.q + (((size_t)s * a.q_len + i) * a.n_q + hq) * D);
 #pragma unroll
@@ -435,12 +490,14 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
         int lim[2], lo[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int r = 2 * t + e;
-            lim[e] = r < R ? ctx - a.q_len + r / G : -1;
+            int ie, he;
+            lim[e] = unit_row(a, w.t, h, 2 * t + e, ie, he) ? ctx - a.q_len + ie : -1;
             lo[e] = a.window > 0 ? lim[e] - a.window + 1 : INT_MIN;
         }
-        const int lim_min = ctx - a.q_len;
-        const int lo_max = a.window > 0 ? ctx - a.window : INT_MIN;  // largest lo of a real row
+        // smallest causal limit and largest window start of the tile's real rows
+        const int lim_min = ctx - a.q_len + tile_first_token(a, w.t);
+        const int lo_max =
+            a.window > 0 ? ctx - a.q_len + tile_last_token(a, w.t) - a.window + 1 : INT_MIN;
 
         float o[MT][4];
 #pragma unroll
@@ -711,7 +768,8 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                 constexpr int V = OUT_F32 ? 4 : 8;  // elements per 16-byte store
                 for (int idx = lane; idx < R * (D / V); idx += 32) {
                     const int r = idx / (D / V), c = (idx % (D / V)) * V;
-                    const int i = r / G, hq = h * G + r % G;
+                    int i, hq;
+                    if (!unit_row(a, w.t, h, r, i, hq)) continue;
                     const size_t ob = (((size_t)s * a.q_len + i) * a.n_q + hq) * D + c;
                     const float* src = emit_tile + r * C::kTileStride + c;
                     if (OUT_F32) {
@@ -739,7 +797,8 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                     *reinterpret_cast<float2*>(a.rec_ml + (rec * R + lane) * 2) =
                         make_float2(emit_ml[lane * 2], emit_ml[lane * 2 + 1]);
                 const int4 rinfo = make_int4(
-                    s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0), 0);
+                    s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0),
+                    w.t);
                 if (slot == 0)
                     info0 = rinfo;
                 else
@@ -774,7 +833,7 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
     const int col = warp / WM;  // which residue class of blocks
     const int g = lane >> 2, t = lane & 3;
     const int mi = lane >> 3, rr = lane & 7;
-    const int G = a.group, cta = blockIdx.x;
+    const int cta = blockIdx.x;
 
     uint32_t gbase = 0;
     bool ok = true;
@@ -789,9 +848,8 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int r = mt * 16 + g + hh * 8;
-            const bool valid = r < a.rows;
-            const int i = valid ? r / G : 0;
-            const int hq = h * G + (valid ? r % G : 0);
+            int i, hq;
+            const bool valid = unit_row(a, w.t, h, r, i, hq);
             lim[hh] = valid ? ctx - a.q_len + i : -1;
             lo[hh] = a.window > 0 ? lim[hh] - a.window + 1 : INT_MIN;
             const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
@@ -812,8 +870,10 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
         }
         const float sl2 = KV8 ? a.scale_log2 * __ldg(a.k_scale + h) : a.scale_log2;
         const float vsc = KV8 ? __ldg(a.v_scale + h) : 1.f;
-        const int lim_min = ctx - a.q_len;  // smallest causal limit of a real row
-        const int lo_max = a.window > 0 ? ctx - a.window : INT_MIN;  // largest lower limit
+        // smallest causal limit and largest window start of the tile's real rows
+        const int lim_min = ctx - a.q_len + tile_first_token(a, w.t);
+        const int lo_max =
+            a.window > 0 ? ctx - a.q_len + tile_last_token(a, w.t) - a.window + 1 : INT_MIN;
 
         float o[NT][4];
 #pragma unroll
@@ -1035,8 +1095,8 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int r = mt * 16 + g + hh * 8;
-                    if (r >= a.rows) continue;
-                    const int i = r / G, hq = h * G + r % G;
+                    int i, hq;
+                    if (!unit_row(a, w.t, h, r, i, hq)) continue;
                     const float inv = (l[hh] > 0.f ? 1.f / l[hh] : 0.f) * vsc;
                     const size_t ob = (((size_t)s * a.q_len + i) * a.n_q + hq) * D;
                     if constexpr (KV8) {
@@ -1092,7 +1152,8 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                             make_float2(m[hh], l[hh]);
                 }
                 const int4 rinfo = make_int4(
-                    s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0), 0);
+                    s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0),
+                    w.t);
                 if (slot == 0)
                     info0 = rinfo;
                 else
@@ -1143,7 +1204,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     if (warp > 5) return;  // warps 6, 7 have no part in this mode
     const bool softmax = warp < 4;
     const int row = threadIdx.x;  // softmax threads: row = TMEM lane
-    const int R = a.rows, G = a.group, cta = blockIdx.x;
+    const int R = a.rows, cta = blockIdx.x;
 
     if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
     tc_fence_before();
@@ -1168,12 +1229,12 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         const int j0 = w.j, j1 = piece_end(w), n = j1 - j0;
         const int ctx = w.ctx, s = w.s, h = w.h;
         int lim = -1, lo = INT_MIN, i_row = 0, hq_row = 0;
+        bool row_ok = false;
         if (softmax) {
             // This unit's query rows into the swizzled Q tile (the previous
             // unit's score products finished: each of them was waited for).
-            const bool valid = row < R;
-            i_row = valid ? row / G : 0;
-            hq_row = h * G + (valid ? row % G : 0);
+            row_ok = unit_row(a, w.t, h, row, i_row, hq_row);
+            const bool valid = row_ok;
             lim = valid ? ctx - a.q_len + i_row : -1;
             if (a.window > 0) lo = lim - a.window + 1;
             const uint4* qrow = reinterpret_cast<const uint4*>(
@@ -1250,8 +1311,9 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         } else {
             // ===================== softmax (thread = row) =====================
             float m_used = -INFINITY, l = 0.f;
-            const int lim_min = ctx - a.q_len;
-            const int lo_max = a.window > 0 ? ctx - a.window : INT_MIN;
+            const int lim_min = ctx - a.q_len + tile_first_token(a, w.t);
+            const int lo_max =
+                a.window > 0 ? ctx - a.q_len + tile_last_token(a, w.t) - a.window + 1 : INT_MIN;
             for (int b = 0; b < n; ++b) {
                 const uint32_t g = gbase + b;
                 ok = consumer_wait(a, &s_full[g & 1u], (g >> 1) & 1u, ok, s_abort);
@@ -1365,7 +1427,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     uint32_t ov[32];
                     tmem_ld32(tlane + kColO + c0, ov);
                     tmem_wait_ld();
-                    if (row < R) {
+                    // whole units write their real rows; records keep every tile row
+                    if (whole ? row_ok : row < R) {
                         if (whole) {
                             const size_t ob =
                                 (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D + c0;
@@ -1401,7 +1464,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         *reinterpret_cast<float2*>(a.rec_ml + (rec * R + row) * 2) = make_float2(m_used, l);
                     if (row == 0) {
                         const int4 rinfo = make_int4(
-                            s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0), 0);
+                            s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0),
+                            w.t);
                         if (piece == 0)
                             info0 = rinfo;
                         else

@@ -1,7 +1,7 @@
 // lse_merge.cu -- combine the split pieces of a (sequence, KV head) unit.
 //
-// Each piece of a unit that the attention kernel split across CTAs left, per
-// query row, its running max m (base-2 domain), running sum l and
+// Each piece of a unit -- a (sequence, KV head, row tile) -- that the
+// attention kernel split across CTAs left, per query row, its running max m (base-2 domain), running sum l and
 // unnormalised output o.  The exact combination is
 //     M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p,
 // the rescale-and-combine rule of the online softmax ("Efficient inference",
@@ -52,7 +52,11 @@ __global__ void __launch_bounds__(kMergeThreads)
     } else {
         return;
     }
-    const int s = head.x, h = head.y;
+    const int s = head.x, h = head.y, tile = head.w;
+    // Row r of the unit's row tile: query token i, query head hq (padding rows of
+    // a partial last tile have no output).
+    const int R = tile * a.rows + r;
+    if (R >= a.rows_total) return;
 
     // Pieces: first_rec, then the first record of every non-empty CTA in
     // (c, c_end].  Find c_end 32 CTAs at a time.
@@ -61,7 +65,8 @@ __global__ void __launch_bounds__(kMergeThreads)
         const int c2 = base + lane;
         int4 in = make_int4(0, 0, 0, 0);
         if (c2 < grid) in = a.rec_info[(size_t)c2 * 2];
-        const bool same = c2 < grid && (in.z & kRecValid) && in.x == s && in.y == h;
+        const bool same =
+            c2 < grid && (in.z & kRecValid) && in.x == s && in.y == h && in.w == tile;
         const bool cont = same || (c2 < grid && (in.z & kRecEmpty));
         const unsigned ends = __ballot_sync(0xffffffffu, (same && (in.z & kRecLast)) || !cont);
         if (ends) {
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 
     const float inv = den > 0.f ? 1.f / den : 0.f;
     const int G = a.group;
-    const int i = r / G, hq = h * G + r % G;
+    const int i = R / G, hq = h * G + R % G;
     const size_t ob = (((size_t)s * a.q_len + i) * a.n_q + hq) * D + lane * V;
     if (OUT_F32) {
         float* op = static_cast<float*>(a.out) + ob;

@@ -108,6 +108,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int kTileRows = 128;
+constexpr int kMaxQLen = 1 << 16;
+constexpr long long kMaxRowsTotal = 1LL << 24;
+
 int warp_rows_for(int rows) {
     const int tiles = (rows + 15) / 16;
     return tiles <= 1 ? 1 : tiles <= 2 ? 2 : tiles <= 4 ? 4 : 8;
@@ -126,8 +130,15 @@ int check_shape(int num_seqs, int q_len, int n_q, int n_kv, int head_dim, int bl
     if (n_q % n_kv != 0) return PKV_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
-    if ((long long)(n_q / n_kv) * q_len > 128) return PKV_ERR_UNSUPPORTED;
+    if (q_len > kMaxQLen || (long long)(n_q / n_kv) * q_len > kMaxRowsTotal)
+        return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
+}
+
+// Query rows sharing one KV head are processed in tiles of at most 128.
+int tile_rows(int n_q, int n_kv, int q_len) {
+    const int rows_total = (n_q / n_kv) * q_len;
+    return rows_total < kTileRows ? rows_total : kTileRows;
 }
 
 }  // namespace
@@ -178,7 +189,7 @@ size_t pkv_paged_decode_attn_workspace_size(int num_seqs, int q_len, int n_q, in
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     const int grid = attn_grid(flags, dev);
     if (grid <= 0) return 0;
-    return workspace_layout(grid, (n_q / n_kv) * q_len, head_dim).total;
+    return workspace_layout(grid, tile_rows(n_q, n_kv, q_len), head_dim).total;
 }
 
 int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
@@ -250,12 +261,14 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     int grid = attn_grid(flags, dev);
     if (grid <= 0) return PKV_ERR_CUDA;
+    const int rows = tile_rows(n_q, n_kv, q_len);
+    const int q_rows_total = (n_q / n_kv) * q_len;
+    const int q_tiles = (q_rows_total + rows - 1) / rows;
     // No more CTAs than (unit, block) items the call can have.
     if (((flags >> PKV_FLAG_GRID_SHIFT) & 0xFFFFu) == 0) {
-        const long long items = (long long)num_seqs * n_kv * max_blocks_per_seq;
+        const long long items = (long long)num_seqs * n_kv * q_tiles * max_blocks_per_seq;
         if (items < grid) grid = (int)items;
     }
-    const int rows = (n_q / n_kv) * q_len;
     const WorkspaceLayout L = workspace_layout(grid, rows, head_dim);
     if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
@@ -281,6 +294,8 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     a.n_kv = n_kv;
     a.group = n_q / n_kv;
     a.rows = rows;
+    a.rows_total = q_rows_total;
+    a.q_tiles = q_tiles;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = num_blocks;
     a.tile_rows_total = (int)rows_total;

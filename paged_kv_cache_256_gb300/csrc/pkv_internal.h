@@ -11,6 +11,7 @@ namespace pkv {
 // Record flags of a split piece (see decode_attn.cu).
 constexpr int kRecValid = 1;  // the slot holds a piece of a split unit
 constexpr int kRecFirst = 2;  // the piece starts at the unit's first block
+// (record info = {sequence, KV head, flags, row tile})
 constexpr int kRecLast = 4;   // the piece ends at the unit's last block
 constexpr int kRecEmpty = 8;  // the CTA owned no blocks at all
 
@@ -29,8 +30,10 @@ struct AttnArgs {
     int q_len;
     int n_q;
     int n_kv;
-    int group;  // n_q / n_kv
-    int rows;   // group * q_len: query rows sharing one KV head
+    int group;       // n_q / n_kv
+    int rows;        // query rows per row tile: min(128, rows_total)
+    int rows_total;  // group * q_len: query rows sharing one KV head
+    int q_tiles;     // ceil(rows_total / rows): row tiles per (sequence, KV head)
     int max_blocks_per_seq;
     int num_blocks;
     int tile_rows_total;  // num_blocks * n_kv * block_size (rows of the 2-D cache view)

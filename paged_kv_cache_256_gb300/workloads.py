@@ -154,6 +154,13 @@ CONFIGS = {
         k_head_scale=(0.5, 4.0),
         description="long-context split-K: batch 4, ctx 131072, 64/8 heads, d 128, bs 16, "
                     "shuffled blocks, K scaled per KV head by U(0.5, 4)"),
+    "llama3_8b_chunked_prefill": dict(
+        index=5, num_seqs=4, q_len=256, n_q=32, n_kv=8, head_dim=128, block_size=16,
+        ctx=("uniform", (1024, 4096)), pool=None, extra_poison=16, k_head_scale=None,
+        description="Llama-3-8B-shaped chunked prefill: batch 4, a 256-token chunk of each "
+                    "prompt appended to a cached prefix (ctx uniform int in [1024, 4096] "
+                    "including the chunk), 32/8 heads, d 128, bs 16: 1024 query rows per KV "
+                    "head in 8 row tiles"),
 }
 
 

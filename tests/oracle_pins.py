@@ -26,6 +26,8 @@ What pins what:
   MQA versus GQA).
 * ``pin_causal_rows``       -- draft token i of gamma equals a one-token query
   over the prefix ending at its own position.
+* ``pin_prefill_sdpa``      -- a block of new tokens (pure or chunked prefill)
+  against torch SDPA, including its own ``is_causal`` flag.
 * ``pin_merge_exact``       -- partials of any split of the key range merge to
   the unsplit result ("Efficient inference", FlashAttention: partial results
   are rescaled and combined exactly).
@@ -300,6 +302,41 @@ def pin_window_extremes(orc):
                     assert np.array_equal(one[b, i, h], want), (b, i, h)
 
 
+def pin_prefill_sdpa(orc):
+    """Many new tokens at once (a prefill chunk): torch SDPA with the causal mask of the
+    chunk's positions, pure prefill (q_len = ctx) and chunked (q_len < ctx), with and
+    without a window."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(29)
+    for ctxs, n_q, n_kv, d, bs, q_len in [([40, 40], 8, 2, 16, 4, 40),
+                                          ([33, 70, 21], 4, 4, 8, 8, 21),
+                                          ([50, 25], 6, 1, 16, 16, 25)]:
+        c = _case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        G = n_q // n_kv
+        for W in (0, 7):
+            got = _run(orc, c, 0.25, window=W)
+            for b, ctx in enumerate(ctxs):
+                q = torch.from_numpy(bf16_bits_to_f32(c["q"][b]).astype(np.float64))
+                k = torch.from_numpy(bf16_bits_to_f32(c["K"][b]).astype(np.float64))
+                v = torch.from_numpy(bf16_bits_to_f32(c["V"][b]).astype(np.float64))
+                k, v = k.repeat_interleave(G, dim=0), v.repeat_interleave(G, dim=0)
+                pos = ctx - q_len + torch.arange(q_len)
+                t = torch.arange(ctx)[None, :]
+                mask = t <= pos[:, None]
+                if W:
+                    mask &= t > pos[:, None] - W
+                if q_len == ctx and not W:  # pure prefill: the library's own causal flag
+                    ref = F.scaled_dot_product_attention(q.permute(1, 0, 2)[None], k[None],
+                                                         v[None], is_causal=True, scale=0.25)[0]
+                else:
+                    ref = F.scaled_dot_product_attention(q.permute(1, 0, 2)[None], k[None],
+                                                         v[None], attn_mask=mask[None, None],
+                                                         scale=0.25)[0]
+                np.testing.assert_allclose(got[b], ref.permute(1, 0, 2).numpy(), rtol=1e-12,
+                                           atol=1e-12)
+
+
 def pin_empty_context(orc):
     rng = np.random.default_rng(19)
     c = _case(rng, [0, 5, 0], 4, 2, 8, 4, 1)
@@ -560,7 +597,7 @@ def pin_kv_append_fp8(orc):
 ALL_PINS = [
     pin_library_sdpa, pin_numpy_dense, pin_equal_scores_mean, pin_single_token, pin_hardmax,
     pin_block_permutation, pin_gqa_equals_repeated_mha, pin_causal_rows, pin_window_sdpa,
-    pin_window_extremes, pin_empty_context,
+    pin_window_extremes, pin_prefill_sdpa, pin_empty_context,
     pin_merge_exact, pin_kv_append, pin_copy_blocks, pin_append_then_attend, pin_kv_bytes_golden,
     pin_gqa_ratio, pin_e4m3_decode_library, pin_e4m3_encode_library, pin_e4m3_saturation,
     pin_fp8_attention_sdpa, pin_kv_append_fp8,

@@ -87,7 +87,8 @@ def attn(lib, **over):
     (dict(head_dim=256), _lib.PKV_ERR_UNSUPPORTED),
     (dict(block_size=8), _lib.PKV_ERR_UNSUPPORTED),
     (dict(block_size=64), _lib.PKV_ERR_UNSUPPORTED),
-    (dict(n_q=64, n_kv=1, q_len=4), _lib.PKV_ERR_UNSUPPORTED),  # 256 rows per KV head
+    (dict(q_len=(1 << 16) + 1), _lib.PKV_ERR_UNSUPPORTED),      # beyond the largest chunk
+    (dict(n_q=1024, n_kv=1, q_len=1 << 15), _lib.PKV_ERR_UNSUPPORTED),  # > 2^24 rows per KV head
     (dict(out_dtype=2), _lib.PKV_ERR_INVALID_ARG),
     (dict(max_blocks=0), _lib.PKV_ERR_INVALID_ARG),
     (dict(num_blocks=0), _lib.PKV_ERR_INVALID_ARG),

@@ -6,7 +6,7 @@ ties, saturating and non-finite inputs.  Attention over an e4m3 cache with
 per-KV-head scales is compared element by element with the oracle's fp64
 attention over the dequantised values, within the same tolerances as the
 bf16 cache: every consumer mode, split units (forced CTA counts), windows,
-and the five named workloads at full size.
+and the named workloads at full size.
 """
 import numpy as np
 import pytest

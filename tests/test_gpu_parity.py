@@ -2,7 +2,7 @@
 
 kv_append and all block-table indexing are compared bit for bit; attention
 outputs element by element within |gpu - ref| <= 1e-2 + 1e-2|ref| (bf16
-output) or 1e-4 + 1e-4|ref| (fp32 output).  The five named workloads run at
+output) or 1e-4 + 1e-4|ref| (fp32 output).  The named workloads run at
 their full sizes in the launch configuration the benchmark times (one CTA
 per SM), and again with the split points moved by forcing other CTA counts.
 """
