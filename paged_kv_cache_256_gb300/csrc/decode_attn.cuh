@@ -84,12 +84,19 @@ constexpr int kModeTmem = 2;    // rows > 64: tcgen05, 128-row tiles, accumulato
 template <int D, int BS, int MODE, bool KV8 = false>
 struct AttnCfg {
     static constexpr int kTileBytes = BS * D * (KV8 ? 1 : 2);  // one K (or V) tile of one (block, head)
-    static constexpr int kStageBytes = 2 * kTileBytes;
     // TMA boxes per tile: bf16 in 64-column (128-byte) boxes; e4m3 rows of D
     // bytes in one box (128-byte swizzle at D = 128, 64-byte at D = 64).
     static constexpr int kBoxes = KV8 ? 1 : D / 64;
     static constexpr int kBoxCols = KV8 ? D : 64;
     static constexpr int kBoxBytes = KV8 ? BS * D : BS * 128;
+    // Blocks per ring stage: one for the mma.sync consumers; 64 keys for the
+    // TMEM consumer, so one score MMA spans them (N = 64).  A stage is laid
+    // out as [K box 0][K box 1 (d 128)][V box 0][V box 1], each region
+    // holding the stage's blocks one after another (kRegion bytes), so the
+    // rows of all its blocks are contiguous within each 64-column region.
+    static constexpr int kBlocksPerStage = MODE == kModeTmem ? 64 / BS : 1;
+    static constexpr int kRegion = kBlocksPerStage * kBoxBytes;
+    static constexpr int kStageBytes = 2 * kBoxes * kRegion;
     // Per-lane floats a warp parks for a merge round: its accumulator, m[2], l[2].
     static constexpr int kLaneFloats = (MODE == kModeNarrow ? D / 4 : D / 2) + 4;
     static constexpr int kMergeBytes = MODE == kModeTmem ? 0 : kMergeSlots * 32 * kLaneFloats * 4;
@@ -322,16 +329,21 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
 }
 
 // ===================== producer warp =====================
+// Fills ring stages of SBS blocks each: a piece of n blocks takes ceil(n / SBS)
+// stages (the last may be partial), counted from the piece's first block.
+// Lanes 0..kIssueLanes-1 fill consecutive stages side by side: one serial
+// wait/issue chain per stage would cap the stream.
 template <int D, int BS, int kStages, int kStageBytes, int kTileBytes, int kBoxBytes, int kBoxes,
-          int kBoxCols>
+          int kBoxCols, int kRegion, int SBS>
 __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tmap_k,
                                         const CUtensorMap* tmap_v, Walk w, uint8_t* stages,
                                         uint64_t* full_bar, uint64_t* empty_bar,
                                         volatile int* s_abort) {
+    static_assert(32 % SBS == 0, "stages must not straddle a batch of 32 block ids");
     const int lane = threadIdx.x & 31;
     if (a.test_stall) return;  // failure-path tests: nothing is loaded, every wait expires
     const uint64_t policy = l2_policy_evict_first();
-    uint32_t gidx = 0, issued = 0;  // issued: fills actually started (a prefix of gidx)
+    uint32_t gidx = 0, issued = 0;  // stages; issued: fills actually started (a prefix of gidx)
     bool ok = true;
     while (w.left > 0 && ok) {
         const int j1 = piece_end(w);
@@ -339,6 +351,7 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
         int my = w.j + lane < j1 ? __ldg(bt + w.j + lane) : 0;
         for (int jb = w.j; jb < j1 && ok; jb += 32) {
             const int n = min(32, j1 - jb);
+            const int ns = (n + SBS - 1) / SBS;  // stages of this batch
             // The next 32 block ids load while this batch is issued.
             const int nxt = jb + 32 + lane < j1 ? __ldg(bt + jb + 32 + lane) : 0;
             if (lane < n && (my < 0 || my >= a.num_blocks)) {
@@ -346,12 +359,15 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                 my = -1;  // read as an out-of-bounds (zero-filled) tile
             }
             if (*s_abort) ok = false;  // a consumer gave up
-            // Lanes 0..kIssueLanes-1 issue the next blocks side by side: one
-            // serial wait/issue chain per block would cap the stream.
-            for (int k0 = 0; k0 < n && ok; k0 += kIssueLanes) {
-                const int kk = k0 + lane;
-                const int blk = __shfl_sync(0xffffffffu, my, kk & 31);
-                const bool act = lane < kIssueLanes && kk < n;
+            for (int k0 = 0; k0 < ns && ok; k0 += kIssueLanes) {
+                const int sk = k0 + lane;  // this lane's stage within the batch
+                const bool act = lane < kIssueLanes && sk < ns;
+                const int nb = SBS == 1 ? 1 : (act ? min(SBS, n - sk * SBS) : 0);
+                // Block ids of this lane's stage, fetched before the wait.
+                int blks[SBS];
+#pragma unroll
+                for (int b = 0; b < SBS; ++b)
+                    blks[b] = __shfl_sync(0xffffffffu, my, (sk * SBS + b) & 31);
                 const uint32_t gl = gidx + lane;
                 const uint32_t stage = gl % kStages;
                 bool good = true;
@@ -360,23 +376,27 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                 const unsigned good_mask = __ballot_sync(0xffffffffu, act && good);
                 const unsigned fail = act_mask & ~good_mask;
                 // Only the lanes below the first failed wait issue, so the
-                // issued fills stay a prefix of the block sequence.
+                // issued fills stay a prefix of the stage sequence.
                 const unsigned issue_mask =
                     fail ? (good_mask & ((1u << (__ffs(fail) - 1)) - 1u)) : good_mask;
-                if ((issue_mask >> lane) & 1u) {
-                    mbar_arrive_expect_tx(&full_bar[stage], 2 * kTileBytes);
-                    const long long y64 = ((long long)blk * a.n_kv + w.h) * BS;
-                    const int y = (blk < 0 || y64 >= a.tile_rows_total)
-                                      ? a.tile_rows_total
-                                      : static_cast<int>(y64);
-                    uint8_t* kdst = stages + stage * kStageBytes;
-                    uint8_t* vdst = kdst + kTileBytes;
+                const bool do_issue = (issue_mask >> lane) & 1u;
+                if (do_issue) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes);
 #pragma unroll
-                    for (int half = 0; half < kBoxes; ++half) {
-                        tma_load_2d(kdst + half * kBoxBytes, tmap_k, half * kBoxCols, y,
-                                    &full_bar[stage], policy);
-                        tma_load_2d(vdst + half * kBoxBytes, tmap_v, half * kBoxCols, y,
-                                    &full_bar[stage], policy);
+                for (int b = 0; b < SBS; ++b) {
+                    const int blk = blks[b];
+                    if (do_issue && b < nb) {
+                        const long long y64 = ((long long)blk * a.n_kv + w.h) * BS;
+                        const int y = (blk < 0 || y64 >= a.tile_rows_total)
+                                          ? a.tile_rows_total
+                                          : static_cast<int>(y64);
+                        uint8_t* kdst = stages + stage * kStageBytes + b * kBoxBytes;
+#pragma unroll
+                        for (int half = 0; half < kBoxes; ++half) {
+                            tma_load_2d(kdst + half * kRegion, tmap_k, half * kBoxCols, y,
+                                        &full_bar[stage], policy);
+                            tma_load_2d(kdst + (kBoxes + half) * kRegion, tmap_v,
+                                        half * kBoxCols, y, &full_bar[stage], policy);
+                        }
                     }
                 }
                 issued = gidx + __popc(issue_mask);
@@ -387,7 +407,7 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                         *s_abort = 1;
                     }
                 }
-                gidx += min(kIssueLanes, n - k0);
+                gidx += min(kIssueLanes, ns - k0);
             }
             my = nxt;
         }
@@ -1168,18 +1188,25 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 
 // ===================== TMEM consumer (rows > 64) =====================
 // One 128-row tile per unit (rows >= R are zero), accumulators in TMEM.
-//   warp 4, lane 0 -- QK issuer: S[g&1] = Q K_g^T (tcgen05.mma; A = Q tile,
-//                     B = K stage, both K-major), as soon as the stage has
-//                     landed and the softmax has loaded S[g&1] of block g-2;
+// Keys are taken kKeys = 64 at a time: one ring stage holds a super-block
+// of 64 / BS blocks with their K rows (and V rows) contiguous, so the three
+// roles synchronise once per 64 keys and one score MMA spans them all:
+//   warp 4, lane 0 -- QK issuer: S[g&1] = Q K^T for the super-block
+//                     (tcgen05.mma, M = 128, N = 64; A = Q tile, B = K
+//                     stage, both K-major) once its stage has landed and the
+//                     softmax has loaded S[g&1] of super-block g-2;
 //   warps 0..3     -- softmax, one thread per row (TMEM lane = row, so a row's
-//                     max and sum never leave the thread): P[g&1] = bf16 of
+//                     max and sum never leave the thread): P[q&1] = bf16 of
 //                     2^(S*scale - m) into TMEM, running sum l; O is rescaled
 //                     in TMEM only when a row's max grew by more than 2^8 (the
 //                     stale max is used consistently in P and l: exact);
-//   warp 5, lane 0 -- PV issuer: O += P[g&1] V_g (A from TMEM, B = V stage,
-//                     MN-major), then releases the stage.
-// Scores therefore run up to two blocks ahead of the softmax, and the PV
-// update of a block overlaps the softmax of the next.
+//   warp 5, lane 0 -- PV issuer: O += P[g&1] V over the super-block's keys
+//                     (A from TMEM, B = V stage, MN-major), then releases
+//                     the stage.
+// Scores therefore run up to two super-blocks ahead of the softmax, and the
+// PV update of one overlaps the softmax of the next.  TMEM columns: O
+// [0, 128), S 2 x 64 from 128, P 2 x 32 from 256, the low halves of P for
+// fp32 output 2 x 32 from 320.
 template <int D, int BS, bool OUT_F32>
 __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t* stages,
                                              uint8_t* qtile, uint64_t* full_bar,
@@ -1188,10 +1215,12 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                                              int4& info0, int4& info1) {
     using C = AttnCfg<D, BS, kModeTmem>;
     constexpr int kStages = C::kStages;
-    constexpr uint32_t kTmemCols = 256;
-    constexpr uint32_t kColO = 0, kColS = 128, kColP = 192, kColPL = 224;
+    constexpr int kKeys = 64;                  // keys per softmax round
+    constexpr int SB = C::kBlocksPerStage;     // blocks per super-block (= per stage)
+    static_assert(SB * BS == kKeys, "a stage holds one super-block");
+    constexpr uint32_t kTmemCols = 512;
+    constexpr uint32_t kColO = 0, kColS = 128, kColP = 256, kColPL = 320;
     constexpr int KT = D / 16;   // k steps of S = Q K^T
-    constexpr int PK = BS / 16;  // k steps of O += P V
     constexpr int kQHalf = 128 * 128;  // bytes of one 64-column half of the Q tile
     constexpr int kParty = 192;        // warps 0..5 take part in this mode
     // tcb: [0..1] S ready, [2..3] S read, [4..5] P ready, [6..7] PV done, [8] QK teardown,
@@ -1212,7 +1241,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     tc_fence_after();
     const uint32_t tbase = *s_tmem;
     const uint32_t tlane = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t idesc_qk = umma_idesc_bf16(128, BS, false);
+    const uint32_t idesc_qk = umma_idesc_bf16(128, kKeys, false);
     const uint32_t idesc_pv = umma_idesc_bf16(128, D, true);
     const uint32_t q_saddr = smem_addr(qtile);
 
@@ -1222,11 +1251,12 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         *s_abort = 1;
     };
 
-    uint32_t gbase = 0;
+    uint32_t gbase = 0;  // sequence number (in this CTA) of the piece's first stage
     bool ok = true;
     int piece = 0;
     while (w.left > 0) {
         const int j0 = w.j, j1 = piece_end(w), n = j1 - j0;
+        const int nsb = (n + SB - 1) / SB;
         const int ctx = w.ctx, s = w.s, h = w.h;
         int lim = -1, lo = INT_MIN, i_row = 0, hq_row = 0;
         bool row_ok = false;
@@ -1255,25 +1285,28 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         if (warp == 4) {
             // ===================== QK issuer =====================
             if (lane == 0 && ok) {
-                for (int b = 0; b < n; ++b) {
-                    const uint32_t g = gbase + b, st = g % kStages;
+                for (int q = 0; q < nsb; ++q) {
+                    const uint32_t g = gbase + q, st = g % kStages;
+                    if (g >= 2 &&
+                        (*s_abort || !mbar_wait_bounded(&s_free[g & 1u], ((g - 2) >> 1) & 1u))) {
+                        issuer_fail(ok);
+                        break;
+                    }
                     if (*s_abort || !mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u)) {
                         issuer_fail(ok);
                         break;
                     }
-                    if (g >= 2 && !mbar_wait_bounded(&s_free[g & 1u], ((g - 2) >> 1) & 1u)) {
-                        issuer_fail(ok);
-                        break;
-                    }
                     tc_fence_after();
+                    // Rows past the stage's blocks (a partial last super-block)
+                    // hold stale keys; the softmax masks their columns.
                     const uint32_t kb = smem_addr(stages + st * C::kStageBytes);
-                    const uint32_t scol = tbase + kColS + (g & 1u) * BS;
+                    const uint32_t scol = tbase + kColS + (g & 1u) * kKeys;
 #pragma unroll
                     for (int kk = 0; kk < KT; ++kk) {
-                        const uint64_t ad =
-                            umma_smem_desc(q_saddr + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd =
-                            umma_smem_desc(kb + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
+                        const uint64_t ad = umma_smem_desc(
+                            q_saddr + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = umma_smem_desc(
+                            kb + (kk >> 2) * C::kRegion + (kk & 3) * 32, 16, 1024);
                         umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&s_full[g & 1u]);
@@ -1283,25 +1316,27 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         } else if (warp == 5) {
             // ===================== PV issuer =====================
             if (lane == 0 && ok) {
-                for (int b = 0; b < n; ++b) {
-                    const uint32_t g = gbase + b, st = g % kStages;
+                for (int q = 0; q < nsb; ++q) {
+                    const uint32_t g = gbase + q, st = g % kStages;
                     if (*s_abort || !mbar_wait_bounded(&p_full[g & 1u], (g >> 1) & 1u)) {
                         issuer_fail(ok);
                         break;
                     }
                     tc_fence_after();
-                    // The softmax saw S of this block, so its score product
+                    // The softmax saw S of this stage, so its score product
                     // (the only other reader of the stage) has completed.
-                    const uint32_t vb = smem_addr(stages + st * C::kStageBytes) + C::kTileBytes;
-                    const uint32_t pcol = tbase + kColP + (g & 1u) * (BS / 2);
-#pragma unroll
-                    for (int kk = 0; kk < PK; ++kk) {
-                        const uint64_t bd = umma_smem_desc(vb + kk * 16 * 128, C::kBoxBytes, 1024);
-                        umma_ts(tbase + kColO, pcol + kk * 8, bd, idesc_pv,
-                                (b > 0 || kk > 0) ? 1u : 0u);
+                    // Only the keys of the stage's blocks enter the product.
+                    const int nk16 = min(SB, n - q * SB) * (BS / 16);
+                    const uint32_t vb =
+                        smem_addr(stages + st * C::kStageBytes) + C::kBoxes * C::kRegion;
+                    const uint32_t pcol = (g & 1u) * (kKeys / 2);
+                    for (int kk = 0; kk < nk16; ++kk) {
+                        const uint64_t bd = umma_smem_desc(vb + kk * 16 * 128, C::kRegion, 1024);
+                        umma_ts(tbase + kColO, tbase + kColP + pcol + kk * 8, bd, idesc_pv,
+                                (q > 0 || kk > 0) ? 1u : 0u);
                         if (OUT_F32)
-                            umma_ts(tbase + kColO, tbase + kColPL + (g & 1u) * (BS / 2) + kk * 8, bd,
-                                    idesc_pv, 1u);
+                            umma_ts(tbase + kColO, tbase + kColPL + pcol + kk * 8, bd, idesc_pv,
+                                    1u);
                     }
                     umma_commit(&empty_bar[st]);    // K and V of this stage are consumed
                     umma_commit(&pv_done[g & 1u]);  // its P buffer is free; O is current
@@ -1314,44 +1349,47 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             const int lim_min = ctx - a.q_len + tile_first_token(a, w.t);
             const int lo_max =
                 a.window > 0 ? ctx - a.q_len + tile_last_token(a, w.t) - a.window + 1 : INT_MIN;
-            for (int b = 0; b < n; ++b) {
-                const uint32_t g = gbase + b;
-                ok = consumer_wait(a, &s_full[g & 1u], (g >> 1) & 1u, ok, s_abort);
+            for (int q = 0; q < nsb; ++q) {
+                const uint32_t sq = gbase + q;  // this super-block's stage
+                const int nb = min(SB, n - q * SB);
+                ok = consumer_wait(a, &s_full[sq & 1u], (sq >> 1) & 1u, ok, s_abort);
                 if (!ok) continue;
                 tc_fence_after();
-                float x[BS];
+                float x[kKeys];
                 {
-                    uint32_t sr[BS];
-                    if constexpr (BS == 32)
-                        tmem_ld32(tlane + kColS + (g & 1u) * BS, sr);
-                    else
-                        tmem_ld16(tlane + kColS + (g & 1u) * BS, sr);
-                    tmem_wait_ld();
+                    uint32_t sr[32];
+#pragma unroll
+                    for (int h2 = 0; h2 < kKeys / 32; ++h2) {
+                        tmem_ld32(tlane + kColS + (sq & 1u) * kKeys + h2 * 32, sr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            x[h2 * 32 + c] = __uint_as_float(sr[c]) * a.scale_log2;
+                    }
                     tc_fence_before();
-                    mbar_arrive(&s_free[g & 1u]);  // S buffer may take the block after next
-#pragma unroll
-                    for (int c = 0; c < BS; ++c) x[c] = __uint_as_float(sr[c]) * a.scale_log2;
+                    mbar_arrive(&s_free[sq & 1u]);  // S buffer may take the super-block after next
                 }
-                const int tok0 = (j0 + b) * BS;
+                const int tok0 = (j0 + q * SB) * BS;  // first key of the super-block
+                const int nkeys = nb * BS;            // columns past it hold stale scores
                 float mloc = -INFINITY;
-                if (tok0 + BS - 1 > lim_min || tok0 < lo_max) {
+                if (nkeys < kKeys || tok0 + kKeys - 1 > lim_min || tok0 < lo_max) {
 #pragma unroll
-                    for (int c = 0; c < BS; ++c)
-                        if (tok0 + c > lim || tok0 + c < lo) x[c] = -INFINITY;
+                    for (int c = 0; c < kKeys; ++c)
+                        if (c >= nkeys || tok0 + c > lim || tok0 + c < lo) x[c] = -INFINITY;
                 }
 #pragma unroll
-                for (int c = 0; c < BS; ++c) mloc = fmaxf(mloc, x[c]);
-                // This block's P buffer was last read by PV two blocks back.
-                if (b > 1) {
-                    ok = consumer_wait(a, &pv_done[g & 1u], ((g - 2) >> 1) & 1u, ok, s_abort);
+                for (int c = 0; c < kKeys; ++c) mloc = fmaxf(mloc, x[c]);
+                // This P buffer was last read by the PV of super-block q - 2.
+                if (q > 1) {
+                    ok = consumer_wait(a, &pv_done[sq & 1u], ((sq - 2) >> 1) & 1u, ok, s_abort);
                     if (!ok) continue;
                     tc_fence_after();
                 }
                 const bool grow = mloc > m_used + 8.f;
                 if (__any_sync(0xffffffffu, grow)) {
-                    // O may only be rescaled once the previous block's PV is done.
-                    if (b > 0) {
-                        ok = consumer_wait(a, &pv_done[(g - 1) & 1u], ((g - 1) >> 1) & 1u, ok,
+                    // O may only be rescaled once the previous super-block's PV is done.
+                    if (q > 0) {
+                        ok = consumer_wait(a, &pv_done[(sq - 1) & 1u], ((sq - 1) >> 1) & 1u, ok,
                                            s_abort);
                         if (!ok) continue;
                         tc_fence_after();
@@ -1359,7 +1397,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     const float m_new = grow ? mloc : m_used;
                     const float alpha = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
                     l *= alpha;
-                    if (b > 0) {
+                    if (q > 0) {
 #pragma unroll 1
                         for (int c0 = 0; c0 < D; c0 += 32) {
                             uint32_t ov[32];
@@ -1374,10 +1412,10 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     }
                     m_used = m_new;
                 }
-                uint32_t ph[BS / 2], pl[BS / 2];
+                uint32_t ph[kKeys / 2], pl[kKeys / 2];
                 float rs = 0.f;
 #pragma unroll
-                for (int c = 0; c < BS; c += 2) {
+                for (int c = 0; c < kKeys; c += 2) {
                     const float p0 = m_used == -INFINITY ? 0.f : fast_exp2(x[c] - m_used);
                     const float p1 = m_used == -INFINITY ? 0.f : fast_exp2(x[c + 1] - m_used);
                     rs += p0 + p1;
@@ -1387,34 +1425,33 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                                                 p1 - bf16_hi_to_f32(ph[c / 2]));
                 }
                 l += rs;
-                if constexpr (BS == 32) {
-                    tmem_st16(tlane + kColP + (g & 1u) * (BS / 2), ph);
-                    if (OUT_F32) tmem_st16(tlane + kColPL + (g & 1u) * (BS / 2), pl);
-                } else {
-                    tmem_st8(tlane + kColP + (g & 1u) * (BS / 2), ph);
-                    if (OUT_F32) tmem_st8(tlane + kColPL + (g & 1u) * (BS / 2), pl);
-                }
+                tmem_st32(tlane + kColP + (sq & 1u) * (kKeys / 2), ph);
+                if (OUT_F32) tmem_st32(tlane + kColPL + (sq & 1u) * (kKeys / 2), pl);
                 tmem_wait_st();
                 // V rows past the context may hold NaN; 0 * NaN would poison O.
-                if (tok0 + BS > ctx) {
-                    uint8_t* vt = stages + (g % kStages) * C::kStageBytes + C::kTileBytes;
-                    const int valid = ctx - tok0;  // >= 1: the block holds a resident token
+                // Only a unit's last block reaches past the context, and it is
+                // the last block of its super-block.
+                const int tokl = tok0 + (nb - 1) * BS;
+                if (tokl + BS > ctx) {
+                    uint8_t* vt = stages + (sq % kStages) * C::kStageBytes +
+                                  C::kBoxes * C::kRegion + (nb - 1) * C::kBoxBytes;
+                    const int valid = ctx - tokl;  // >= 1: the block holds a resident token
                     const int chunks = (BS - valid) * 8;  // 16-byte chunks per 64-column half
-                    for (int q = row; q < chunks * (D / 64); q += 128) {
-                        const int half = q / chunks, rq = q % chunks;
-                        *reinterpret_cast<uint4*>(vt + half * C::kBoxBytes + valid * 128 + rq * 16) =
+                    for (int qq = row; qq < chunks * (D / 64); qq += 128) {
+                        const int half = qq / chunks, rq = qq % chunks;
+                        *reinterpret_cast<uint4*>(vt + half * C::kRegion + valid * 128 + rq * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
                 }
                 tc_fence_before();
-                mbar_arrive(&p_full[g & 1u]);
+                mbar_arrive(&p_full[sq & 1u]);
             }
 
             // ---- epilogue: the last PV, then O out of TMEM row by row
-            if (n > 0) {
-                const uint32_t gl = gbase + n - 1;
-                ok = consumer_wait(a, &pv_done[gl & 1u], (gl >> 1) & 1u, ok, s_abort);
+            if (nsb > 0) {
+                const uint32_t sl = gbase + nsb - 1;
+                ok = consumer_wait(a, &pv_done[sl & 1u], (sl >> 1) & 1u, ok, s_abort);
             }
             tc_fence_after();
             const bool first_piece = j0 == w.jlo, last_piece = j1 == w.nb;
@@ -1475,7 +1512,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             }
             tc_fence_before();
         }
-        gbase += n;
+        gbase += nsb;
         ++piece;
         w.left -= j1 - w.j;
         if (w.left > 0) walk_next_unit<BS>(a, w);
@@ -1546,7 +1583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kConsumerWarps) {
         produce<D, BS, kStages, C::kStageBytes, C::kTileBytes, C::kBoxBytes, C::kBoxes,
-                C::kBoxCols>(
+                C::kBoxCols, C::kRegion, C::kBlocksPerStage>(
             a, &tmap_k, &tmap_v, w0, stages, full_bar, empty_bar, &s_abort);
         return;
     }
