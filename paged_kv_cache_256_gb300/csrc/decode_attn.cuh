@@ -561,14 +561,11 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                             uint32_t r[4];
                             ldmatrix_x4(r, kb + swz8<D>(tp * 16 + (mi & 1) * 8 + rr,
                                                         32 * j + (mi >> 1) * 16));
-                            const uint32_t k0[4] = {e4m3x2_to_f16x2(r[0] & 0xFFFFu),
-                                                    e4m3x2_to_f16x2(r[1] & 0xFFFFu),
-                                                    e4m3x2_to_f16x2(r[0] >> 16),
-                                                    e4m3x2_to_f16x2(r[1] >> 16)};
-                            const uint32_t k1[4] = {e4m3x2_to_f16x2(r[2] & 0xFFFFu),
-                                                    e4m3x2_to_f16x2(r[3] & 0xFFFFu),
-                                                    e4m3x2_to_f16x2(r[2] >> 16),
-                                                    e4m3x2_to_f16x2(r[3] >> 16)};
+                            uint32_t k0[4], k1[4];  // A fragments of k steps 2j, 2j + 1
+                            e4m3x4_to_f16x2x2(r[0], k0[0], k0[2]);
+                            e4m3x4_to_f16x2x2(r[1], k0[1], k0[3]);
+                            e4m3x4_to_f16x2x2(r[2], k1[0], k1[2]);
+                            e4m3x4_to_f16x2x2(r[3], k1[1], k1[3]);
                             mma_f16_16816(st[tp], k0, qb[2 * j][0], qb[2 * j][1]);
                             mma_f16_16816(st2[tp], k1, qb[2 * j + 1][0], qb[2 * j + 1][1]);
                         }
@@ -687,11 +684,8 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                             const uint32_t* r = vr[tp][j];
                             uint32_t ev[4], od[4];
 #pragma unroll
-                            for (int m = 0; m < 4; ++m) {
-                                const uint32_t pr = prmt(r[m], 0u, 0x3120u);
-                                ev[m] = e4m3x2_to_f16x2(pr & 0xFFFFu);
-                                od[m] = e4m3x2_to_f16x2(pr >> 16);
-                            }
+                            for (int m = 0; m < 4; ++m)
+                                e4m3x4_to_f16x2x2(prmt(r[m], 0u, 0x3120u), ev[m], od[m]);
                             const uint32_t ae[4] = {ev[0] & vm0, ev[2] & vm0, ev[1] & vm8,
                                                     ev[3] & vm8};
                             const uint32_t ao[4] = {od[0] & vm0, od[2] & vm0, od[1] & vm8,
@@ -926,14 +920,12 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                             uint32_t r[4];
                             ldmatrix_x4(r, kbase + swz8<D>(tp * 16 + (mi & 1) * 8 + rr,
                                                            32 * j + (mi >> 1) * 16));
-                            mma_f16_16816(sc[0], qf[2 * j], e4m3x2_to_f16x2(r[0] & 0xFFFFu),
-                                          e4m3x2_to_f16x2(r[0] >> 16));
-                            mma_f16_16816(sc[1], qf[2 * j], e4m3x2_to_f16x2(r[1] & 0xFFFFu),
-                                          e4m3x2_to_f16x2(r[1] >> 16));
-                            mma_f16_16816(sc[0], qf[2 * j + 1], e4m3x2_to_f16x2(r[2] & 0xFFFFu),
-                                          e4m3x2_to_f16x2(r[2] >> 16));
-                            mma_f16_16816(sc[1], qf[2 * j + 1], e4m3x2_to_f16x2(r[3] & 0xFFFFu),
-                                          e4m3x2_to_f16x2(r[3] >> 16));
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                uint32_t b0, b1;
+                                e4m3x4_to_f16x2x2(r[m], b0, b1);
+                                mma_f16_16816(sc[m & 1], qf[2 * j + (m >> 1)], b0, b1);
+                            }
                         }
                     } else {
 #pragma unroll
@@ -1030,22 +1022,21 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                             uint32_t r[4];
                             ldmatrix_x4_trans(r, vbase + swz8<D>(tp * 16 + (mi & 1) * 8 + rr,
                                                                  32 * j + (mi >> 1) * 16));
-                            uint32_t ev[4], od[4];
 #pragma unroll
-                            for (int m = 0; m < 4; ++m) {
-                                const uint32_t pr = prmt(r[m], 0u, 0x3120u);
-                                ev[m] = e4m3x2_to_f16x2(pr & 0xFFFFu) & ((m & 1) ? vm8 : vm0);
-                                od[m] = e4m3x2_to_f16x2(pr >> 16) & ((m & 1) ? vm8 : vm0);
-                            }
-                            mma_f16_16816(o[4 * j + 0], pa, ev[0], ev[1]);
-                            mma_f16_16816(o[4 * j + 1], pa, od[0], od[1]);
-                            mma_f16_16816(o[4 * j + 2], pa, ev[2], ev[3]);
-                            mma_f16_16816(o[4 * j + 3], pa, od[2], od[3]);
-                            if (OUT_F32) {
-                                mma_f16_16816(o[4 * j + 0], pl, ev[0], ev[1]);
-                                mma_f16_16816(o[4 * j + 1], pl, od[0], od[1]);
-                                mma_f16_16816(o[4 * j + 2], pl, ev[2], ev[3]);
-                                mma_f16_16816(o[4 * j + 3], pl, od[2], od[3]);
+                            for (int hh = 0; hh < 2; ++hh) {  // d 32j + 16 hh ..
+                                uint32_t e0, o0, e1, o1;    // tokens 0-7 / 8-15, even / odd d
+                                e4m3x4_to_f16x2x2(prmt(r[2 * hh], 0u, 0x3120u), e0, o0);
+                                e4m3x4_to_f16x2x2(prmt(r[2 * hh + 1], 0u, 0x3120u), e1, o1);
+                                e0 &= vm0;
+                                o0 &= vm0;
+                                e1 &= vm8;
+                                o1 &= vm8;
+                                mma_f16_16816(o[4 * j + 2 * hh], pa, e0, e1);
+                                mma_f16_16816(o[4 * j + 2 * hh + 1], pa, o0, o1);
+                                if (OUT_F32) {
+                                    mma_f16_16816(o[4 * j + 2 * hh], pl, e0, e1);
+                                    mma_f16_16816(o[4 * j + 2 * hh + 1], pl, o0, o1);
+                                }
                             }
                         }
                     } else {

@@ -172,14 +172,12 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
-// Two e4m3 codes (low byte -> low half) as an f16 pair; every e4m3 value is
-// exact in f16.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
-    uint32_t d;
-    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-        : "=r"(d)
-        : "r"(pair16));
-    return d;
+// Four e4m3 codes (bytes 0..3) as two f16 pairs: lo = bytes (0, 1), hi = bytes (2, 3).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(v));
 }
 
 // Two fp32 -> two e4m3 codes (nearest, ties to even, saturating at +-448;
