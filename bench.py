@@ -334,15 +334,15 @@ def run_ours(args):
 
     def append(s):
         if kv8:
-            pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.k_cache, d8.v_cache,
-                                  d8.k_scale, d8.v_scale, stream=s)
+            pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.kv_cache, d8.k_scale,
+                                  d8.v_scale, stream=s)
         else:
             pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache,
                               stream=s)
 
     def attend(s):
         if kv8:
-            pkv.pkv_paged_decode_attn_ex(dw.q, d8.k_cache, d8.v_cache, dw.block_tables,
+            pkv.pkv_paged_decode_attn_ex(dw.q, d8.kv_cache, None, dw.block_tables,
                                          dw.context_lens, wl.scale, out, ws, stream=s,
                                          window=args.window, k_scale=d8.k_scale,
                                          v_scale=d8.v_scale)

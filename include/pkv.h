@@ -61,7 +61,7 @@ typedef enum pkv_status {
  * winds down and pkv_check_error reports PKV_ERR_TIMEOUT.  The output of
  * such a call is not valid; the context stays usable. */
 #define PKV_FLAG_TEST_STALL 0x2u
-/* pkv_copy_blocks: the caches hold 1-byte (e4m3) elements instead of bf16. */
+/* pkv_copy_blocks: the cache is the interleaved 8-bit (e4m3) cache. */
 #define PKV_FLAG_KV_FP8 0x4u
 /* Bits 16..31 force the number of attention CTAs (0 = one per SM).  Tests
  * use it to move where long contexts are split; results stay within the
@@ -147,15 +147,21 @@ int pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cach
  * kv_dtype: PKV_KV_BF16, or PKV_KV_FP8_E4M3 for an 8-bit cache -- fewer
  *   bytes per cached element, dequantised through a scale ("Efficient
  *   inference", Quantization: fewer bytes per weight; CS336 lecture-10 notes,
- *   Quantization & pruning).  k_cache / v_cache then hold e4m3 codes (OCP
- *   FP8 E4M3: bias 7, largest finite 448, no infinity) in the same layout
- *   with 1-byte elements, and k_scale / v_scale are DEVICE fp32 arrays
- *   [n_kv]: the value of code c in KV head g is c * k_scale[g] (V alike).
+ *   Quantization & pruning).  The cache is then ONE tensor of e4m3 codes
+ *   (OCP FP8 E4M3: bias 7, largest finite 448, no infinity) passed as
+ *   k_cache, with v_cache NULL:
+ *       kv_cache [num_blocks][n_kv][2][block_size][head_dim]   (1 byte each)
+ *   -- for every (block, KV head) its K rows, then its V rows, so the two
+ *   tiles a KV head reads from a block are one contiguous 2 * block_size *
+ *   head_dim run (random 4 KB runs stream much faster than 2 KB ones).
+ *   k_scale / v_scale are DEVICE fp32 arrays [n_kv]: the value of code c in
+ *   KV head g is c * k_scale[g] for K and c * v_scale[g] for V.
  *   The result is the attention over those values.  Inside the kernel Q and
  *   the probabilities are rounded to f16 (|q| must stay below 65504), the
  *   products accumulate in fp32.  pkv_kv_append_fp8 writes such a cache.
- *   Cache pointers must be 16-byte aligned.  k_scale / v_scale are ignored
- *   for PKV_KV_BF16.  Any other kv_dtype returns PKV_ERR_INVALID_ARG.
+ *   The cache pointer must be 16-byte aligned.  k_scale / v_scale are
+ *   ignored for PKV_KV_BF16.  Any other kv_dtype, a non-NULL v_cache with an
+ *   8-bit cache or a NULL one with bf16, returns PKV_ERR_INVALID_ARG.
  * Every other field, the layouts and the return codes are those of
  * pkv_paged_decode_attn.  `p` is read during the call only.
  */
@@ -259,14 +265,15 @@ int pkv_kv_append(const void *k_new, const void *v_new, const int32_t *slot_mapp
  * with ties to the even code; quotients beyond +-448 (and infinities) store
  * +-448, NaN stores 0x7F.  V likewise with v_scale.  Quantise through a
  * scale: "Efficient inference", Quantization: fewer bytes per weight.
- * k_scale, v_scale: DEVICE fp32 [n_kv]; caches [num_blocks][n_kv][block_size]
- *   [head_dim] bytes, 16-byte aligned; k_new, v_new as for pkv_kv_append.
+ * k_scale, v_scale: DEVICE fp32 [n_kv]; kv_cache: the interleaved 8-bit cache
+ *   [num_blocks][n_kv][2][block_size][head_dim] bytes (K rows at [..][0], V
+ *   rows at [..][1]), 16-byte aligned; k_new, v_new as for pkv_kv_append.
  * flags: reserved, pass 0.
  * Returns PKV_OK, PKV_ERR_INVALID_ARG or PKV_ERR_CUDA; num_tokens == 0 launches nothing.
  */
 int pkv_kv_append_fp8(const void *k_new, const void *v_new, const int32_t *slot_mapping,
                       int num_tokens, int n_kv, int head_dim, int block_size, int num_blocks,
-                      const float *k_scale, const float *v_scale, void *k_cache, void *v_cache,
+                      const float *k_scale, const float *v_scale, void *kv_cache,
                       unsigned flags, void *stream);
 
 /*
@@ -282,8 +289,8 @@ int pkv_kv_append_fp8(const void *k_new, const void *v_new, const int32_t *slot_
  *   [0, num_blocks) or with src == dst are skipped.  A destination must not
  *   also be a source in the same call.
  * Caches as for pkv_paged_decode_attn (head_dim a multiple of 8); with
- * PKV_FLAG_KV_FP8 in flags they hold 1-byte elements (n_kv * block_size *
- * head_dim a multiple of 16).
+ * PKV_FLAG_KV_FP8 in flags, k_cache is the interleaved 8-bit cache (each
+ * block holds K and V) and v_cache must be NULL.
  * Returns PKV_OK, PKV_ERR_INVALID_ARG or PKV_ERR_CUDA; num_pairs == 0 launches nothing.
  */
 int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,

@@ -71,11 +71,11 @@ class Oracle:
         lib.oracle_paged_attn.restype = c_int
         u8p = ctypes.POINTER(ctypes.c_uint8)
         f32p = ctypes.POINTER(ctypes.c_float)
-        lib.oracle_paged_attn_fp8.argtypes = [u16p, u8p, u8p, f32p, f32p, i32p, i32p] + \
+        lib.oracle_paged_attn_fp8.argtypes = [u16p, u8p, f32p, f32p, i32p, i32p] + \
             [c_int] * 8 + [ctypes.c_double, c_int, f64p]
         lib.oracle_paged_attn_fp8.restype = c_int
         lib.oracle_kv_append_fp8.argtypes = [u16p, u16p, i32p] + [c_int] * 5 + \
-            [f32p, f32p, u8p, u8p]
+            [f32p, f32p, u8p]
         lib.oracle_kv_append_fp8.restype = c_int
         lib.oracle_e4m3_encode.argtypes = [f32p, ctypes.c_long, u8p]
         lib.oracle_e4m3_encode.restype = None
@@ -124,13 +124,14 @@ class Oracle:
             raise ValueError(f"oracle_paged_attn rejected its inputs (status {st})")
         return out
 
-    def paged_attn_fp8(self, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+    def paged_attn_fp8(self, q, kv_cache, k_scale, v_scale, block_tables, context_lens,
                        *, n_q, n_kv, head_dim, block_size, scale, num_blocks=None, q_len=None,
                        window=0):
-        """paged_attn over e4m3 caches (uint8 codes) with fp32 per-KV-head scales [n_kv]."""
+        """paged_attn over an e4m3 cache [num_blocks, n_kv, 2, block_size, head_dim] (uint8
+        codes; K rows then V rows) with fp32 per-KV-head scales [n_kv]."""
         q = np.ascontiguousarray(q, dtype=np.uint16)
-        k_cache = np.ascontiguousarray(k_cache, dtype=np.uint8)
-        v_cache = np.ascontiguousarray(v_cache, dtype=np.uint8)
+        kv_cache = np.ascontiguousarray(kv_cache, dtype=np.uint8)
+        assert kv_cache.ndim == 5 and kv_cache.shape[2] == 2
         ks = np.ascontiguousarray(k_scale, dtype=np.float32)
         vs = np.ascontiguousarray(v_scale, dtype=np.float32)
         assert ks.shape == (n_kv,) and vs.shape == (n_kv,)
@@ -139,10 +140,10 @@ class Oracle:
         num_seqs = cl.shape[0]
         q_len = q.shape[1] if q_len is None else q_len
         if num_blocks is None:
-            num_blocks = k_cache.shape[0]
+            num_blocks = kv_cache.shape[0]
         out = np.zeros((num_seqs, q_len, n_q, head_dim), dtype=np.float64)
         st = self._lib.oracle_paged_attn_fp8(
-            _ptr(q, ctypes.c_uint16), _ptr(k_cache, ctypes.c_uint8), _ptr(v_cache, ctypes.c_uint8),
+            _ptr(q, ctypes.c_uint16), _ptr(kv_cache, ctypes.c_uint8),
             _ptr(ks, ctypes.c_float), _ptr(vs, ctypes.c_float), _ptr(bt, ctypes.c_int32),
             _ptr(cl, ctypes.c_int32), num_seqs, q_len, n_q, n_kv, head_dim, block_size,
             bt.shape[1], num_blocks, float(scale), int(window), _ptr(out, ctypes.c_double))
@@ -217,22 +218,21 @@ class Oracle:
         if st != 0:
             raise ValueError(f"oracle_kv_append rejected its inputs (status {st})")
 
-    def kv_append_fp8(self, k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, *,
+    def kv_append_fp8(self, k_new, v_new, slot_mapping, kv_cache, k_scale, v_scale, *,
                       block_size):
-        """In-place quantising scatter into e4m3 caches (numpy uint8 arrays)."""
+        """In-place quantising scatter into an e4m3 cache [num_blocks, n_kv, 2, bs, d] (uint8)."""
         k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
         v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
         sm = np.ascontiguousarray(slot_mapping, dtype=np.int32)
         ks = np.ascontiguousarray(k_scale, dtype=np.float32)
         vs = np.ascontiguousarray(v_scale, dtype=np.float32)
-        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
-        assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
-        num_blocks, n_kv, bs, d = k_cache.shape
-        assert bs == block_size and ks.shape == (n_kv,) and vs.shape == (n_kv,)
+        assert kv_cache.flags.c_contiguous and kv_cache.dtype == np.uint8
+        num_blocks, n_kv, two, bs, d = kv_cache.shape
+        assert two == 2 and bs == block_size and ks.shape == (n_kv,) and vs.shape == (n_kv,)
         st = self._lib.oracle_kv_append_fp8(
             _ptr(k_new, ctypes.c_uint16), _ptr(v_new, ctypes.c_uint16), _ptr(sm, ctypes.c_int32),
             sm.shape[0], n_kv, d, block_size, num_blocks, _ptr(ks, ctypes.c_float),
-            _ptr(vs, ctypes.c_float), _ptr(k_cache, ctypes.c_uint8), _ptr(v_cache, ctypes.c_uint8))
+            _ptr(vs, ctypes.c_float), _ptr(kv_cache, ctypes.c_uint8))
         if st != 0:
             raise ValueError(f"oracle_kv_append_fp8 rejected its inputs (status {st})")
 

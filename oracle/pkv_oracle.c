@@ -42,7 +42,9 @@
  *     weight -- the KV cache may be stored in low precision, dequantised
  *     through a scale; CS336 lecture-10 notes, Quantization & pruning:
  *     bf16 -> fp8) holds e4m3 codes with one scale per KV head for K and one
- *     for V: the cached value is code_value * scale.  A new value x is stored
+ *     for V: the cached value is code_value * scale.  Its layout is
+ *     [num_blocks][n_kv][2][block_size][head_dim]: for every (block, KV
+ *     head) the K rows, then the V rows;  A new value x is stored
  *     as the e4m3 code nearest to x / scale, the division taken in fp32 and
  *     ties going to the even code; quotients beyond the largest finite e4m3
  *     (448) store +-448.
@@ -132,12 +134,14 @@ void oracle_e4m3_decode(const uint8_t *codes, long n, double *x)
 }
 
 /*
- * A KV cache as the attention reads it: bf16 bit patterns, or e4m3 codes with
- * one dequantisation scale per KV head (k_scale[g], v_scale[g]).
+ * A KV cache as the attention reads it: bf16 bit patterns in separate K and V
+ * caches [num_blocks][n_kv][block_size][head_dim], or e4m3 codes in one cache
+ * [num_blocks][n_kv][2][block_size][head_dim] (K rows, then V rows) with one
+ * dequantisation scale per KV head (k_scale[g], v_scale[g]).
  */
 typedef struct {
-    const uint16_t *k16, *v16; /* bf16 cache, or NULL */
-    const uint8_t *k8, *v8;    /* e4m3 cache, or NULL */
+    const uint16_t *k16, *v16; /* bf16 caches, or NULL */
+    const uint8_t *kv8;        /* e4m3 cache, or NULL */
     const float *k_scale, *v_scale;
 } cache_view;
 
@@ -157,10 +161,13 @@ static int gather_sequence(const cache_view *c, const int32_t *table_row, int ct
         if (blk < 0 || blk >= num_blocks)
             return -1;
         size_t base = (((size_t)blk * n_kv + g) * block_size + off) * head_dim;
+        /* e4m3: K row of (blk, g, off) and the V row block_size rows after it */
+        size_t kbase8 = ((((size_t)blk * n_kv + g) * 2) * block_size + off) * head_dim;
+        size_t vbase8 = kbase8 + (size_t)block_size * head_dim;
         for (int e = 0; e < head_dim; ++e) {
-            if (c->k8) {
-                K[(size_t)t * head_dim + e] = e4m3_value(c->k8[base + e]) * (double)c->k_scale[g];
-                V[(size_t)t * head_dim + e] = e4m3_value(c->v8[base + e]) * (double)c->v_scale[g];
+            if (c->kv8) {
+                K[(size_t)t * head_dim + e] = e4m3_value(c->kv8[kbase8 + e]) * (double)c->k_scale[g];
+                V[(size_t)t * head_dim + e] = e4m3_value(c->kv8[vbase8 + e]) * (double)c->v_scale[g];
             } else {
                 K[(size_t)t * head_dim + e] = bf16_value(c->k16[base + e]);
                 V[(size_t)t * head_dim + e] = bf16_value(c->v16[base + e]);
@@ -263,20 +270,20 @@ int oracle_paged_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t
                       int block_size, int max_blocks_per_seq, int num_blocks,
                       double scale, int window, double *out)
 {
-    const cache_view c = {k_cache, v_cache, NULL, NULL, NULL, NULL};
+    const cache_view c = {k_cache, v_cache, NULL, NULL, NULL};
     return paged_attn(q, &c, block_tables, context_lens, num_seqs, q_len, n_q, n_kv, head_dim,
                       block_size, max_blocks_per_seq, num_blocks, scale, window, out);
 }
 
 /* The same attention over an e4m3 cache: K_t = code * k_scale[g], V_t = code * v_scale[g]. */
-int oracle_paged_attn_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+int oracle_paged_attn_fp8(const uint16_t *q, const uint8_t *kv_cache,
                           const float *k_scale, const float *v_scale,
                           const int32_t *block_tables, const int32_t *context_lens,
                           int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
                           int block_size, int max_blocks_per_seq, int num_blocks,
                           double scale, int window, double *out)
 {
-    const cache_view c = {NULL, NULL, k_cache, v_cache, k_scale, v_scale};
+    const cache_view c = {NULL, NULL, kv_cache, k_scale, v_scale};
     return paged_attn(q, &c, block_tables, context_lens, num_seqs, q_len, n_q, n_kv, head_dim,
                       block_size, max_blocks_per_seq, num_blocks, scale, window, out);
 }
@@ -421,15 +428,16 @@ int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, const int32_t
 }
 
 /*
- * The same append into an e4m3 cache: the code stored for value x of KV head
- * g is e4m3_code(x / k_scale[g]) (v_scale[g] for V), the quotient rounded to
- * fp32 first -- quantise via a scale ("Efficient inference", Quantization:
+ * The same append into an e4m3 cache (layout as above: K rows, then V rows
+ * of each (block, KV head)): the code stored for value x of KV head g is
+ * e4m3_code(x / k_scale[g]) (v_scale[g] for V), the quotient rounded to fp32
+ * first -- quantise via a scale ("Efficient inference", Quantization:
  * fewer bytes per weight; CS336 lecture-10 notes, Quantization & pruning).
  */
 int oracle_kv_append_fp8(const uint16_t *k_new, const uint16_t *v_new,
                          const int32_t *slot_mapping, int num_tokens, int n_kv, int head_dim,
                          int block_size, int num_blocks, const float *k_scale,
-                         const float *v_scale, uint8_t *k_cache, uint8_t *v_cache)
+                         const float *v_scale, uint8_t *kv_cache)
 {
     if (num_tokens < 0 || n_kv < 1 || head_dim < 1 || block_size < 1 || num_blocks < 0)
         return 1;
@@ -440,13 +448,14 @@ int oracle_kv_append_fp8(const uint16_t *k_new, const uint16_t *v_new,
         long blk = slot / block_size;
         long off = slot % block_size;
         for (int g = 0; g < n_kv; ++g) {
-            size_t dst = (((size_t)blk * n_kv + g) * block_size + off) * head_dim;
+            size_t kdst = ((((size_t)blk * n_kv + g) * 2) * block_size + off) * head_dim;
+            size_t vdst = kdst + (size_t)block_size * head_dim;
             size_t src = ((size_t)i * n_kv + g) * head_dim;
             for (int e = 0; e < head_dim; ++e) {
                 const float kq = (float)bf16_value(k_new[src + e]) / k_scale[g];
                 const float vq = (float)bf16_value(v_new[src + e]) / v_scale[g];
-                k_cache[dst + e] = e4m3_code(kq);
-                v_cache[dst + e] = e4m3_code(vq);
+                kv_cache[kdst + e] = e4m3_code(kq);
+                kv_cache[vdst + e] = e4m3_code(vq);
             }
         }
     }

@@ -62,7 +62,7 @@ SIGNATURES = {
     "pkv_paged_decode_attn_noalloc": ([_vp, _vp, _vp, _i32p, _i32p] + [_c_int] * 8 +
                                       [_c_float, _vp, _c_int, ctypes.c_uint, _vp], _c_int),
     "pkv_kv_append": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp, _vp, ctypes.c_uint, _vp], _c_int),
-    "pkv_kv_append_fp8": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp] * 4 + [ctypes.c_uint, _vp],
+    "pkv_kv_append_fp8": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp] * 3 + [ctypes.c_uint, _vp],
                           _c_int),
     "pkv_check_error": ([_vp, _vp], _c_int),
     "pkv_copy_blocks": ([_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.c_uint,
@@ -183,17 +183,29 @@ def alloc_workspace(num_seqs, q_len, n_q, n_kv, head_dim, block_size, flags=0, d
 
 
 def _attn_shapes(q, k_cache, v_cache, block_tables, context_lens, out, workspace, kv8=False):
-    """Checks shared by the attention entry points; returns (dims, out_dtype)."""
+    """Checks shared by the attention entry points; returns (dims, out_dtype).
+
+    bf16: k_cache / v_cache [num_blocks, n_kv, bs, d]; 8-bit: k_cache is the
+    interleaved cache [num_blocks, n_kv, 2, bs, d] and v_cache is None.
+    """
     import torch
     _bf16_like(q, "q")
-    (_fp8_like if kv8 else _bf16_like)(k_cache, "k_cache")
-    (_fp8_like if kv8 else _bf16_like)(v_cache, "v_cache")
     _i32(block_tables, "block_tables")
     _i32(context_lens, "context_lens")
-    if q.dim() != 4 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
-        raise ValueError("q must be 4-D and k_cache / v_cache 4-D of equal shape")
+    if kv8:
+        _fp8_like(k_cache, "kv_cache")
+        if v_cache is not None or k_cache.dim() != 5 or k_cache.shape[2] != 2:
+            raise ValueError("an 8-bit cache is one [num_blocks, n_kv, 2, bs, d] tensor")
+        num_blocks, n_kv, _, bs, d2 = k_cache.shape
+    else:
+        _bf16_like(k_cache, "k_cache")
+        _bf16_like(v_cache, "v_cache")
+        if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+            raise ValueError("k_cache / v_cache must be 4-D of equal shape")
+        num_blocks, n_kv, bs, d2 = k_cache.shape
+    if q.dim() != 4:
+        raise ValueError("q must be 4-D")
     num_seqs, q_len, n_q, d = q.shape
-    num_blocks, n_kv, bs, d2 = k_cache.shape
     if d2 != d or block_tables.dim() != 2 or block_tables.shape[0] != num_seqs or \
             context_lens.shape != (num_seqs,) or tuple(out.shape) != tuple(q.shape):
         raise ValueError("inconsistent shapes")
@@ -232,7 +244,9 @@ def pkv_paged_decode_attn_ex(q, k_cache, v_cache, block_tables, context_lens, sc
     """pkv_paged_decode_attn through the parameter struct.
 
     window > 0: sliding window of that many positions.  With k_scale / v_scale
-    (float32 CUDA [n_kv]) the caches are e4m3 codes (uint8 or float8_e4m3fn).
+    (float32 CUDA [n_kv]) the cache is 8-bit: k_cache is the interleaved
+    e4m3 cache [num_blocks, n_kv, 2, bs, d] (uint8 or float8_e4m3fn) and
+    v_cache is None.
     """
     kv8 = k_scale is not None or v_scale is not None
     (num_seqs, q_len, n_q, n_kv, d, bs, max_blocks, num_blocks), out_dtype = _attn_shapes(
@@ -241,7 +255,8 @@ def pkv_paged_decode_attn_ex(q, k_cache, v_cache, block_tables, context_lens, sc
         _f32_vec(k_scale, n_kv, "k_scale")
         _f32_vec(v_scale, n_kv, "v_scale")
     p = pkv_attn_params(
-        q=q.data_ptr(), k_cache=k_cache.data_ptr(), v_cache=v_cache.data_ptr(),
+        q=q.data_ptr(), k_cache=k_cache.data_ptr(),
+        v_cache=None if v_cache is None else v_cache.data_ptr(),
         block_tables=block_tables.data_ptr(), context_lens=context_lens.data_ptr(),
         num_seqs=num_seqs, q_len=q_len, n_q=n_q, n_kv=n_kv, head_dim=d, block_size=bs,
         max_blocks_per_seq=max_blocks, num_blocks=num_blocks, scale=float(scale),
@@ -296,48 +311,58 @@ def pkv_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, flags=0, stream=
     _check(st, "pkv_kv_append")
 
 
-def pkv_kv_append_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, flags=0,
+def pkv_kv_append_fp8(k_new, v_new, slot_mapping, kv_cache, k_scale, v_scale, flags=0,
                       stream=None):
-    """Quantise k_new/v_new [T, n_kv, d] (bf16) into e4m3 cache slots via per-head scales."""
+    """Quantise k_new/v_new [T, n_kv, d] (bf16) via per-head scales into the interleaved
+    e4m3 cache [num_blocks, n_kv, 2, bs, d]."""
     _bf16_like(k_new, "k_new")
     _bf16_like(v_new, "v_new")
-    _fp8_like(k_cache, "k_cache")
-    _fp8_like(v_cache, "v_cache")
+    _fp8_like(kv_cache, "kv_cache")
     _i32(slot_mapping, "slot_mapping")
     T, n_kv, d = k_new.shape
-    num_blocks, n_kv2, bs, d2 = k_cache.shape
-    if v_new.shape != k_new.shape or n_kv2 != n_kv or d2 != d or slot_mapping.shape != (T,) \
-            or v_cache.shape != k_cache.shape:
+    if kv_cache.dim() != 5 or kv_cache.shape[2] != 2:
+        raise ValueError("kv_cache must be [num_blocks, n_kv, 2, bs, d]")
+    num_blocks, n_kv2, _, bs, d2 = kv_cache.shape
+    if v_new.shape != k_new.shape or n_kv2 != n_kv or d2 != d or slot_mapping.shape != (T,):
         raise ValueError("inconsistent shapes")
     _f32_vec(k_scale, n_kv, "k_scale")
     _f32_vec(v_scale, n_kv, "v_scale")
     st = load_library().pkv_kv_append_fp8(
         k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), T, n_kv, d, bs, num_blocks,
-        k_scale.data_ptr(), v_scale.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-        int(flags), _stream_ptr(stream))
+        k_scale.data_ptr(), v_scale.data_ptr(), kv_cache.data_ptr(), int(flags),
+        _stream_ptr(stream))
     _check(st, "pkv_kv_append_fp8")
 
 
 def pkv_copy_blocks(k_cache, v_cache, pairs, flags=0, stream=None):
     """Copy whole blocks (all KV heads, K and V): block pairs[p,1] <- block pairs[p,0].
 
-    bf16 caches, or e4m3 caches (uint8 / float8_e4m3fn; PKV_FLAG_KV_FP8 is set for them).
+    bf16 caches, or the interleaved e4m3 cache [num_blocks, n_kv, 2, bs, d] as k_cache with
+    v_cache None (PKV_FLAG_KV_FP8 is then set).
     """
     import torch
     kv8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
-    (_fp8_like if kv8 else _bf16_like)(k_cache, "k_cache")
-    (_fp8_like if kv8 else _bf16_like)(v_cache, "v_cache")
     if kv8:
+        _fp8_like(k_cache, "kv_cache")
+        if v_cache is not None or k_cache.dim() != 5 or k_cache.shape[2] != 2:
+            raise ValueError("an 8-bit cache is one [num_blocks, n_kv, 2, bs, d] tensor")
         flags = int(flags) | PKV_FLAG_KV_FP8
+    else:
+        _bf16_like(k_cache, "k_cache")
+        _bf16_like(v_cache, "v_cache")
     if pairs.dtype != torch.int32 or not pairs.is_cuda or not pairs.is_contiguous() or \
             pairs.dim() != 2 or pairs.shape[1] != 2:
         raise ValueError("pairs must be a contiguous int32 CUDA tensor of shape [n, 2]")
-    num_blocks, n_kv, bs, d = k_cache.shape
-    if v_cache.shape != k_cache.shape:
-        raise ValueError("inconsistent shapes")
-    st = load_library().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(),
-                                        pairs.shape[0], num_blocks, n_kv, d, bs, int(flags),
-                                        _stream_ptr(stream))
+    if kv8:
+        num_blocks, n_kv, _, bs, d = k_cache.shape
+    else:
+        num_blocks, n_kv, bs, d = k_cache.shape
+        if v_cache.shape != k_cache.shape:
+            raise ValueError("inconsistent shapes")
+    st = load_library().pkv_copy_blocks(k_cache.data_ptr(),
+                                        None if v_cache is None else v_cache.data_ptr(),
+                                        pairs.data_ptr(), pairs.shape[0], num_blocks, n_kv, d, bs,
+                                        int(flags), _stream_ptr(stream))
     _check(st, "pkv_copy_blocks")
 
 

@@ -385,17 +385,20 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                 for (int b = 0; b < SBS; ++b) {
                     const int blk = blks[b];
                     if (do_issue && b < nb) {
-                        const long long y64 = ((long long)blk * a.n_kv + w.h) * BS;
-                        const int y = (blk < 0 || y64 >= a.tile_rows_total)
-                                          ? a.tile_rows_total
-                                          : static_cast<int>(y64);
+                        // K rows of (block, head) in the 2-D cache view; the V rows
+                        // follow them in an 8-bit cache, else they sit at the same
+                        // rows of the V cache.  Bad ids read past the end (zeros).
+                        const long long y64 = ((long long)blk * a.n_kv + w.h) * a.kv_mul * BS;
+                        const bool oob = blk < 0 || y64 >= a.tile_rows_total;
+                        const int yk = oob ? a.tile_rows_total : static_cast<int>(y64);
+                        const int yv = oob ? a.tile_rows_total : yk + a.v_row_off;
                         uint8_t* kdst = stages + stage * kStageBytes + b * kBoxBytes;
 #pragma unroll
                         for (int half = 0; half < kBoxes; ++half) {
-                            tma_load_2d(kdst + half * kRegion, tmap_k, half * kBoxCols, y,
+                            tma_load_2d(kdst + half * kRegion, tmap_k, half * kBoxCols, yk,
                                         &full_bar[stage], policy);
                             tma_load_2d(kdst + (kBoxes + half) * kRegion, tmap_v,
-                                        half * kBoxCols, y, &full_bar[stage], policy);
+                                        half * kBoxCols, yv, &full_bar[stage], policy);
                         }
                     }
                 }

@@ -59,8 +59,10 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
     return cudaGetLastError();
 }
 
-// The quantising append into an 8-bit (e4m3) cache: the code stored for value
-// x of KV head g is the e4m3 nearest to x / scale[g] -- the quotient rounded
+// The quantising append into an 8-bit (e4m3) cache, laid out as
+// [num_blocks][n_kv][2][block_size][head_dim] (each (block, head)'s K rows,
+// then its V rows): the code stored for value x of KV head g is the e4m3
+// nearest to x / scale[g] -- the quotient rounded
 // to fp32 (IEEE division), then to e4m3 with ties to even, saturating at
 // +-448 -- so a cached value decodes to code * scale[g] ("Efficient
 // inference", Quantization: quantise and dequantise through a scale).  One
@@ -76,7 +78,7 @@ __global__ void __launch_bounds__(256)
                          const int32_t* __restrict__ slot_mapping, long long num_tokens, int n_kv,
                          int chunks, int block_size, long long num_slots,
                          const float* __restrict__ k_scale, const float* __restrict__ v_scale,
-                         uint2* __restrict__ k_cache, uint2* __restrict__ v_cache) {
+                         uint2* __restrict__ kv_cache) {
     const long long total = num_tokens * n_kv * 2 * chunks;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
@@ -89,20 +91,20 @@ __global__ void __launch_bounds__(256)
         const long long slot = __ldg(slot_mapping + tok);
         if (slot < 0 || slot >= num_slots) continue;
         const long long blk = slot / block_size, off = slot % block_size;
-        const size_t dst = (((size_t)blk * n_kv + g) * block_size + off) * chunks + chunk;
+        const size_t dst =
+            ((((size_t)blk * n_kv + g) * 2 + which) * block_size + off) * chunks + chunk;
         const size_t src = ((size_t)tok * n_kv + g) * chunks + chunk;
         const uint4 x = __ldg((which == 0 ? k_new : v_new) + src);
         const float sc = __ldg((which == 0 ? k_scale : v_scale) + g);
-        (which == 0 ? k_cache : v_cache)[dst] =
-            make_uint2(quantise4(x.x, x.y, sc), quantise4(x.z, x.w, sc));
+        kv_cache[dst] = make_uint2(quantise4(x.x, x.y, sc), quantise4(x.z, x.w, sc));
     }
 }
 
 cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new,
                                  const int32_t* slot_mapping, int num_tokens, int n_kv,
                                  int head_dim, int block_size, int num_blocks,
-                                 const float* k_scale, const float* v_scale, void* k_cache,
-                                 void* v_cache, int num_sms, cudaStream_t stream) {
+                                 const float* k_scale, const float* v_scale, void* kv_cache,
+                                 int num_sms, cudaStream_t stream) {
     const int chunks = head_dim / 8;
     const long long total = (long long)num_tokens * n_kv * 2 * chunks;
     long long blocks = (total + 255) / 256;
@@ -112,7 +114,7 @@ cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new,
     kv_append_fp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
         num_tokens, n_kv, chunks, block_size, (long long)num_blocks * block_size, k_scale,
-        v_scale, static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache));
+        v_scale, static_cast<uint2*>(kv_cache));
     return cudaGetLastError();
 }
 
@@ -133,10 +135,13 @@ __global__ void __launch_bounds__(256)
         const int src = __ldg(pairs + 2 * p), dst = __ldg(pairs + 2 * p + 1);
         if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks || src == dst) continue;
         uint4* cache = which == 0 ? k_cache : v_cache;
+        if (cache == nullptr) continue;  // one interleaved cache: its blocks hold K and V
         cache[(size_t)dst * chunks_per_block + chunk] = cache[(size_t)src * chunks_per_block + chunk];
     }
 }
 
+// elem_bytes * n_kv * block_size * head_dim bytes per block of each cache; a
+// null v_cache (an interleaved 8-bit cache) copies k_cache only.
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, int n_kv, int head_dim, int block_size,
                                int elem_bytes, int num_sms, cudaStream_t stream) {

@@ -48,7 +48,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D view of a cache: rows = num_blocks * n_kv * block_size, columns =
 // head_dim elements.  bf16: one box = 64 columns x block_size rows with the
-// 128-byte swizzle.  e4m3 (kv8): one box = a whole row of head_dim bytes x
+// 128-byte swizzle.  e4m3 (kv8; one cache whose (block, head) tiles hold the
+// K rows, then the V rows): one box = a whole row of head_dim bytes x
 // block_size rows, 128-byte swizzle at head_dim 128, 64-byte at 64.
 bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, long long rows,
                     int block_size, bool kv8) {
@@ -248,12 +249,14 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     if (num_seqs == 0) return PKV_OK;
     if (kv8 && (!p->k_scale || !p->v_scale || !aligned(p->k_scale, 4) || !aligned(p->v_scale, 4)))
         return PKV_ERR_INVALID_ARG;
-    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-        return PKV_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+    // An 8-bit cache is one interleaved tensor, passed as k_cache; v_cache is NULL.
+    if (kv8 ? v_cache != nullptr : v_cache == nullptr) return PKV_ERR_INVALID_ARG;
+    if (!q || !k_cache || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || (!kv8 && !aligned(v_cache, 16)) ||
+        !aligned(out, 16) ||
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PKV_ERR_INVALID_ARG;
-    const long long rows_total = (long long)num_blocks * n_kv * block_size;
+    const long long rows_total = (long long)num_blocks * n_kv * (kv8 ? 2 : 1) * block_size;
     if (rows_total >= (1LL << 31) - 64) return PKV_ERR_UNSUPPORTED;
     if ((long long)max_blocks_per_seq * block_size >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;
 
@@ -275,7 +278,7 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
 
     CUtensorMap tk, tv;
     if (!cached_cache_map(&tk, k_cache, head_dim, rows_total, block_size, kv8) ||
-        !cached_cache_map(&tv, v_cache, head_dim, rows_total, block_size, kv8))
+        !cached_cache_map(&tv, kv8 ? k_cache : v_cache, head_dim, rows_total, block_size, kv8))
         return PKV_ERR_CUDA;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -299,6 +302,8 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = num_blocks;
     a.tile_rows_total = (int)rows_total;
+    a.kv_mul = kv8 ? 2 : 1;
+    a.v_row_off = kv8 ? block_size : 0;
     a.warp_rows = warp_rows_for(rows);
     a.k_scale = kv8 ? p->k_scale : nullptr;
     a.v_scale = kv8 ? p->v_scale : nullptr;
@@ -343,25 +348,24 @@ int pkv_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapp
 
 int pkv_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping,
                       int num_tokens, int n_kv, int head_dim, int block_size, int num_blocks,
-                      const float* k_scale, const float* v_scale, void* k_cache, void* v_cache,
+                      const float* k_scale, const float* v_scale, void* kv_cache,
                       unsigned flags, void* stream) {
     (void)flags;
     if (num_tokens < 0 || n_kv < 1 || head_dim < 8 || head_dim % 8 != 0 || block_size < 1 ||
         num_blocks < 1)
         return PKV_ERR_INVALID_ARG;
     if (num_tokens == 0) return PKV_OK;
-    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    if (!k_new || !v_new || !slot_mapping || !kv_cache || !k_scale || !v_scale)
         return PKV_ERR_INVALID_ARG;
-    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
-        !aligned(v_cache, 16) || !aligned(slot_mapping, 4) || !aligned(k_scale, 4) ||
-        !aligned(v_scale, 4))
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(kv_cache, 16) ||
+        !aligned(slot_mapping, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
         return PKV_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     const int sms = sm_count(dev);
     if (sms <= 0) return PKV_ERR_CUDA;
     if (launch_kv_append_fp8(k_new, v_new, slot_mapping, num_tokens, n_kv, head_dim, block_size,
-                             num_blocks, k_scale, v_scale, k_cache, v_cache, sms,
+                             num_blocks, k_scale, v_scale, kv_cache, sms,
                              static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
@@ -370,20 +374,23 @@ int pkv_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_
 int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                     int num_blocks, int n_kv, int head_dim, int block_size, unsigned flags,
                     void* stream) {
-    const int elem_bytes = (flags & PKV_FLAG_KV_FP8) ? 1 : 2;
+    // An 8-bit cache is one tensor whose blocks hold K and V (1 byte each): a
+    // block is as many bytes as a bf16 K block, and there is no V pointer.
+    const bool kv8 = (flags & PKV_FLAG_KV_FP8) != 0;
     if (num_pairs < 0 || num_blocks < 1 || n_kv < 1 || head_dim < 8 || head_dim % 8 != 0 ||
-        block_size < 1 || ((long long)n_kv * block_size * head_dim * elem_bytes) % 16 != 0)
+        block_size < 1 || ((long long)n_kv * block_size * head_dim * 2) % 16 != 0)
         return PKV_ERR_INVALID_ARG;
     if (num_pairs == 0) return PKV_OK;
-    if (!k_cache || !v_cache || !pairs) return PKV_ERR_INVALID_ARG;
-    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(pairs, 4))
+    if (!k_cache || !pairs || (kv8 ? v_cache != nullptr : v_cache == nullptr))
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || (!kv8 && !aligned(v_cache, 16)) || !aligned(pairs, 4))
         return PKV_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     const int sms = sm_count(dev);
     if (sms <= 0) return PKV_ERR_CUDA;
     if (launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_blocks, n_kv, head_dim,
-                           block_size, elem_bytes, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                           block_size, 2, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
 }

@@ -36,7 +36,9 @@ struct AttnArgs {
     int q_tiles;     // ceil(rows_total / rows): row tiles per (sequence, KV head)
     int max_blocks_per_seq;
     int num_blocks;
-    int tile_rows_total;  // num_blocks * n_kv * block_size (rows of the 2-D cache view)
+    int tile_rows_total;  // rows of the 2-D cache view: num_blocks * n_kv * kv_mul * block_size
+    int kv_mul;           // 1: separate K and V caches; 2: one cache, K rows then V rows
+    int v_row_off;        // rows from a tile's K rows to its V rows (0 or block_size)
     int warp_rows;        // 16-row tiles per KV unit (1, 2, 4 or 8)
     const float* k_scale;  // 8-bit caches: [n_kv] dequantisation scales (else unused)
     const float* v_scale;
@@ -72,8 +74,8 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
 cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new,
                                  const int32_t* slot_mapping, int num_tokens, int n_kv,
                                  int head_dim, int block_size, int num_blocks,
-                                 const float* k_scale, const float* v_scale, void* k_cache,
-                                 void* v_cache, int num_sms, cudaStream_t stream);
+                                 const float* k_scale, const float* v_scale, void* kv_cache,
+                                 int num_sms, cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, int n_kv, int head_dim, int block_size,

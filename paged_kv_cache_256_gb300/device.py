@@ -54,16 +54,14 @@ def to_device(wl, device="cuda") -> DeviceWorkload:
 
 @dataclasses.dataclass
 class DeviceFp8Cache:
-    k_cache: object  # uint8 e4m3 codes
-    v_cache: object
-    k_scale: object  # float32 [n_kv]
+    kv_cache: object  # uint8 e4m3 codes [num_blocks, n_kv, 2, block_size, head_dim]
+    k_scale: object   # float32 [n_kv]
     v_scale: object
 
 
 def fp8_to_device(c, device="cuda") -> DeviceFp8Cache:
     import torch
     return DeviceFp8Cache(
-        k_cache=torch.from_numpy(np.ascontiguousarray(c.k_cache)).to(device),
-        v_cache=torch.from_numpy(np.ascontiguousarray(c.v_cache)).to(device),
+        kv_cache=torch.from_numpy(np.ascontiguousarray(c.kv_cache)).to(device),
         k_scale=torch.from_numpy(np.ascontiguousarray(c.k_scale, dtype=np.float32)).to(device),
         v_scale=torch.from_numpy(np.ascontiguousarray(c.v_scale, dtype=np.float32)).to(device))

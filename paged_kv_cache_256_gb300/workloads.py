@@ -35,6 +35,8 @@ directly -- random sign, exponent field 7 + round(N(0, 1.5)) clipped to
 [1, 14], uniform mantissa -- into the same resident slots, with the e4m3 NaN
 (0x7F) wherever the bf16 cache holds poison, and per-KV-head fp32 scales
 drawn from U(0.05, 0.5).  No quantiser is involved: the codes are the data.
+The 8-bit cache is one array ``[num_blocks, n_kv, 2, block_size, head_dim]``
+holding each (block, KV head)'s K rows, then its V rows.
 """
 from __future__ import annotations
 
@@ -217,9 +219,8 @@ def _e4m3_codes(seed_seq: np.random.SeedSequence, n: int, chunk=1 << 23) -> np.n
 
 @dataclasses.dataclass
 class Fp8Cache:
-    k_cache: np.ndarray  # [num_blocks, n_kv, block_size, head_dim] e4m3 codes (uint8)
-    v_cache: np.ndarray
-    k_scale: np.ndarray  # [n_kv] float32: value of code c in head g = c * k_scale[g]
+    kv_cache: np.ndarray  # [num_blocks, n_kv, 2, block_size, head_dim] e4m3 codes (uint8)
+    k_scale: np.ndarray   # [n_kv] float32: value of code c in head g = c * k_scale[g]
     v_scale: np.ndarray
 
 
@@ -236,7 +237,8 @@ def fp8_cache_for(wl: Workload, seed: int | None = None) -> Fp8Cache:
     r = np.random.Generator(np.random.PCG64(s_s))
     ks = r.uniform(0.05, 0.5, size=wl.n_kv).astype(np.float32)
     vs = r.uniform(0.05, 0.5, size=wl.n_kv).astype(np.float32)
-    return Fp8Cache(k_cache=k8, v_cache=v8, k_scale=ks, v_scale=vs)
+    kv = np.ascontiguousarray(np.stack([k8, v8], axis=2))
+    return Fp8Cache(kv_cache=kv, k_scale=ks, v_scale=vs)
 
 
 def _draw_context_lens(rng, spec, num_seqs):

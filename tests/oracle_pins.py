@@ -525,10 +525,12 @@ def _fp8_case(rng, ctxs, n_q, n_kv, d, bs, q_len):
     K = [rng.choice(finite, size=(n_kv, c, d)).astype(np.uint8) for c in ctxs]
     V = [rng.choice(finite, size=(n_kv, c, d)).astype(np.uint8) for c in ctxs]
     kc, vc, bt = _paged_from_logical(rng, K, V, bs, poison=E4M3_NAN)
+    # the 8-bit cache keeps each (block, head)'s K rows, then its V rows
+    kv = np.ascontiguousarray(np.stack([kc, vc], axis=2))
     q = _rand_bf16(rng, (len(ctxs), q_len, n_q, d))
     ks = rng.uniform(0.002, 0.05, n_kv).astype(np.float32)
     vs = rng.uniform(0.002, 0.05, n_kv).astype(np.float32)
-    return dict(q=q, K=K, V=V, k_cache=kc, v_cache=vc, block_tables=bt, ks=ks, vs=vs,
+    return dict(q=q, K=K, V=V, kv_cache=kv, block_tables=bt, ks=ks, vs=vs,
                 context_lens=np.asarray(ctxs, dtype=np.int32))
 
 
@@ -540,7 +542,7 @@ def pin_fp8_attention_sdpa(orc):
         c = _fp8_case(rng, ctxs, n_q, n_kv, d, bs, q_len)
         G = n_q // n_kv
         for window in (0, 5):
-            got = orc.paged_attn_fp8(c["q"], c["k_cache"], c["v_cache"], c["ks"], c["vs"],
+            got = orc.paged_attn_fp8(c["q"], c["kv_cache"], c["ks"], c["vs"],
                                      c["block_tables"], c["context_lens"], n_q=n_q, n_kv=n_kv,
                                      head_dim=d, block_size=bs, scale=0.2, window=window)
             for b, ctx in enumerate(ctxs):
@@ -566,8 +568,7 @@ def pin_fp8_attention_sdpa(orc):
 def pin_kv_append_fp8(orc):
     rng = np.random.default_rng(44)
     for n_kv, d, bs, pool in [(2, 8, 4, 6), (4, 64, 16, 5)]:
-        kc = rng.integers(0, 256, size=(pool, n_kv, bs, d), dtype=np.uint8)
-        vc = rng.integers(0, 256, size=(pool, n_kv, bs, d), dtype=np.uint8)
+        kv = rng.integers(0, 256, size=(pool, n_kv, 2, bs, d), dtype=np.uint8)
         nslots = pool * bs
         slots = np.concatenate([rng.permutation(nslots)[:7].astype(np.int32),
                                 np.asarray([-1, nslots], np.int32)])
@@ -584,14 +585,14 @@ def pin_kv_append_fp8(orc):
             codes = np.where(np.abs(xq) > 464.0, np.where(xq < 0, 0xFE, 0x7E), codes)
             return codes.astype(np.uint8)
 
-        k_ref, v_ref = kc.copy(), vc.copy()
+        ref = kv.copy()
         for i, sl in enumerate(slots):
             if 0 <= sl < nslots:
-                k_ref[sl // bs, :, sl % bs, :] = expect(kn[i], ks)
-                v_ref[sl // bs, :, sl % bs, :] = expect(vn[i], vs)
-        k_got, v_got = kc.copy(), vc.copy()
-        orc.kv_append_fp8(kn, vn, slots, k_got, v_got, ks, vs, block_size=bs)
-        assert np.array_equal(k_got, k_ref) and np.array_equal(v_got, v_ref)
+                ref[sl // bs, :, 0, sl % bs, :] = expect(kn[i], ks)
+                ref[sl // bs, :, 1, sl % bs, :] = expect(vn[i], vs)
+        got = kv.copy()
+        orc.kv_append_fp8(kn, vn, slots, got, ks, vs, block_size=bs)
+        assert np.array_equal(got, ref)
 
 
 ALL_PINS = [

@@ -198,22 +198,27 @@ def test_params_entry_host_checks(lib):
                                         None) == _lib.PKV_ERR_UNSUPPORTED
     assert lib.pkv_paged_decode_attn_ex(ctypes.byref(_params(kv_dtype=2)),
                                         None) == _lib.PKV_ERR_INVALID_ARG
-    # an 8-bit cache needs its scales (checked before any device call)
+    # an 8-bit cache needs its scales and no V pointer (checked before any device call)
     assert lib.pkv_paged_decode_attn_ex(
         ctypes.byref(_params(num_seqs=2, kv_dtype=_lib.PKV_KV_FP8_E4M3)),
         None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_paged_decode_attn_ex(
+        ctypes.byref(_params(num_seqs=2, kv_dtype=_lib.PKV_KV_FP8_E4M3, k_scale=FAKE,
+                             v_scale=FAKE)), None) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_paged_decode_attn_ex(
         ctypes.byref(_params(kv_dtype=_lib.PKV_KV_FP8_E4M3)), None) == _lib.PKV_OK
 
 
 def test_fp8_append_and_copy_host_checks(lib):
-    args = [FAKE, FAKE, FAKE, 4, 2, 64, 16, 8, None, FAKE, FAKE, FAKE, 0, None]
+    args = [FAKE, FAKE, FAKE, 4, 2, 64, 16, 8, None, FAKE, FAKE, 0, None]
     assert lib.pkv_kv_append_fp8(*args) == _lib.PKV_ERR_INVALID_ARG  # null k_scale
     args[8] = FAKE
     args[5] = 60  # head_dim not a multiple of 8
     assert lib.pkv_kv_append_fp8(*args) == _lib.PKV_ERR_INVALID_ARG
     args[5], args[3] = 64, 0
     assert lib.pkv_kv_append_fp8(*args) == _lib.PKV_OK  # nothing to append
-    # 1-byte copies need whole 16-byte chunks per block
-    assert lib.pkv_copy_blocks(FAKE, FAKE, FAKE, 1, 8, 1, 8, 1, _lib.PKV_FLAG_KV_FP8,
+    # an interleaved 8-bit cache has no separate V pointer; bf16 caches need one
+    assert lib.pkv_copy_blocks(FAKE, FAKE, FAKE, 1, 8, 2, 64, 16, _lib.PKV_FLAG_KV_FP8,
+                               None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy_blocks(FAKE, None, FAKE, 1, 8, 2, 64, 16, 0,
                                None) == _lib.PKV_ERR_INVALID_ARG

@@ -23,12 +23,12 @@ pytestmark = pytest.mark.gpu
 
 def _append_both(oracle, wl, c8, dw, d8):
     """Quantising append of the workload's new tokens on the GPU and in the oracle."""
-    pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.k_cache, d8.v_cache,
-                          d8.k_scale, d8.v_scale)
-    kc, vc = c8.k_cache.copy(), c8.v_cache.copy()
-    oracle.kv_append_fp8(wl.k_new, wl.v_new, wl.slot_mapping, kc, vc, c8.k_scale, c8.v_scale,
+    pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.kv_cache, d8.k_scale,
+                          d8.v_scale)
+    kv = c8.kv_cache.copy()
+    oracle.kv_append_fp8(wl.k_new, wl.v_new, wl.slot_mapping, kv, c8.k_scale, c8.v_scale,
                          block_size=wl.block_size)
-    return kc, vc
+    return kv
 
 
 def _run(dw, d8, wl, kind, flags=0, window=0):
@@ -37,7 +37,7 @@ def _run(dw, d8, wl, kind, flags=0, window=0):
     out = torch.full(tuple(dw.q.shape), float("nan"), dtype=dt, device="cuda")
     ws = pkv.alloc_workspace(wl.num_seqs, wl.q_len, wl.n_q, wl.n_kv, wl.head_dim,
                              wl.block_size, flags=flags)
-    pkv.pkv_paged_decode_attn_ex(dw.q, d8.k_cache, d8.v_cache, dw.block_tables, dw.context_lens,
+    pkv.pkv_paged_decode_attn_ex(dw.q, d8.kv_cache, None, dw.block_tables, dw.context_lens,
                                  wl.scale, out, ws, flags=flags, window=window,
                                  k_scale=d8.k_scale, v_scale=d8.v_scale)
     st = pkv.pkv_check_error(ws)
@@ -45,8 +45,8 @@ def _run(dw, d8, wl, kind, flags=0, window=0):
     return out
 
 
-def _ref(oracle, wl, c8, kc, vc, window=0):
-    return oracle.paged_attn_fp8(wl.q, kc, vc, c8.k_scale, c8.v_scale, wl.block_tables,
+def _ref(oracle, wl, c8, kv, window=0):
+    return oracle.paged_attn_fp8(wl.q, kv, c8.k_scale, c8.v_scale, wl.block_tables,
                                  wl.context_lens, n_q=wl.n_q, n_kv=wl.n_kv,
                                  head_dim=wl.head_dim, block_size=wl.block_size,
                                  scale=wl.scale, window=window)
@@ -68,20 +68,18 @@ def test_append_special_values_bit_exact(oracle):
     kn.reshape(-1)[16] = 0x7FC0  # a plain bf16 NaN (the helper maps NaN to its poison pattern)
     vn = f32_to_bf16_bits(-x[::-1].copy())
     slots = np.asarray([3, 17, 40, -1, 63, 5], dtype=np.int32)
-    k8 = rng.integers(0, 256, (pool, n_kv, bs, d), dtype=np.uint8)
-    v8 = rng.integers(0, 256, (pool, n_kv, bs, d), dtype=np.uint8)
+    kv8 = rng.integers(0, 256, (pool, n_kv, 2, bs, d), dtype=np.uint8)
     for ks, vs in ([1.0, 1.0], [0.25, 3.0]), ([0.0078125, 1.5], [1.0, 0.1]):
         ks, vs = np.asarray(ks, np.float32), np.asarray(vs, np.float32)
-        kc, vc = k8.copy(), v8.copy()
-        oracle.kv_append_fp8(kn, vn, slots, kc, vc, ks, vs, block_size=bs)
-        gk, gv = torch.from_numpy(k8).cuda(), torch.from_numpy(v8).cuda()
+        ref = kv8.copy()
+        oracle.kv_append_fp8(kn, vn, slots, ref, ks, vs, block_size=bs)
+        g = torch.from_numpy(kv8).cuda()
         to16 = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
-        pkv.pkv_kv_append_fp8(to16(kn), to16(vn), torch.from_numpy(slots).cuda(), gk, gv,
+        pkv.pkv_kv_append_fp8(to16(kn), to16(vn), torch.from_numpy(slots).cuda(), g,
                               torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda())
-        gk, gv = gk.cpu().numpy(), gv.cpu().numpy()
-        bad = np.nonzero(gk != kc)
-        assert bad[0].size == 0, (bad, gk[bad][:8], kc[bad][:8])
-        assert np.array_equal(gv, vc)
+        got = g.cpu().numpy()
+        bad = np.nonzero(got != ref)
+        assert bad[0].size == 0, (bad, got[bad][:8], ref[bad][:8])
 
 
 CASES = [
@@ -104,12 +102,11 @@ def test_fp8_parity(oracle, case, grid):
                      block_size=bs, context_lens=ctxs, seed=401 + n_q + q_len + d)
     c8 = fp8_cache_for(wl)
     dw, d8 = to_device(wl), fp8_to_device(c8)
-    kc, vc = _append_both(oracle, wl, c8, dw, d8)
-    assert np.array_equal(d8.k_cache.cpu().numpy(), kc)
-    assert np.array_equal(d8.v_cache.cpu().numpy(), vc)
+    kv = _append_both(oracle, wl, c8, dw, d8)
+    assert np.array_equal(d8.kv_cache.cpu().numpy(), kv)
     flags = pkv.PKV_FLAG_GRID(grid) if grid else 0
     for window in (0, 17):
-        ref = _ref(oracle, wl, c8, kc, vc, window)
+        ref = _ref(oracle, wl, c8, kv, window)
         for kind in ("bf16", "f32"):
             out = _run(dw, d8, wl, kind, flags, window)
             assert_close(out_to_host(out), ref, kind, f"{case} grid {grid} W {window} {kind}")
@@ -121,28 +118,27 @@ def named8(request, oracle):
     wl = make_workload(request.param)
     c8 = fp8_cache_for(wl)
     dw, d8 = to_device(wl), fp8_to_device(c8)
-    kc, vc = _append_both(oracle, wl, c8, dw, d8)
+    kv = _append_both(oracle, wl, c8, dw, d8)
     torch.cuda.synchronize()
-    ref = _ref(oracle, wl, c8, kc, vc)
-    yield wl, dw, d8, kc, vc, ref
+    ref = _ref(oracle, wl, c8, kv)
+    yield wl, dw, d8, kv, ref
     del dw, d8
     torch.cuda.empty_cache()
 
 
 def test_named_fp8_append_bit_exact(named8):
-    wl, dw, d8, kc, vc, _ = named8
-    assert np.array_equal(d8.k_cache.cpu().numpy(), kc)
-    assert np.array_equal(d8.v_cache.cpu().numpy(), vc)
+    wl, dw, d8, kv, _ = named8
+    assert np.array_equal(d8.kv_cache.cpu().numpy(), kv)
 
 
 @pytest.mark.parametrize("kind", ["bf16", "f32"])
 def test_named_fp8_attention(named8, kind):
-    wl, dw, d8, _, _, ref = named8
+    wl, dw, d8, _, ref = named8
     assert_close(out_to_host(_run(dw, d8, wl, kind)), ref, kind, f"{wl.name}/fp8/{kind}")
 
 
 def test_named_fp8_split_points(named8):
-    wl, dw, d8, _, _, ref = named8
+    wl, dw, d8, _, ref = named8
     for grid in (7, 300):
         out = _run(dw, d8, wl, "f32", flags=pkv.PKV_FLAG_GRID(grid))
         assert_close(out_to_host(out), ref, "f32", f"{wl.name}/fp8/grid{grid}")
@@ -151,11 +147,10 @@ def test_named_fp8_split_points(named8):
 def test_fp8_copy_blocks_bit_exact():
     import torch
     rng = np.random.default_rng(9)
-    k8 = rng.integers(0, 256, (10, 2, 16, 64), dtype=np.uint8)
-    v8 = rng.integers(0, 256, (10, 2, 16, 64), dtype=np.uint8)
+    kv8 = rng.integers(0, 256, (10, 2, 2, 16, 64), dtype=np.uint8)
     pairs = np.asarray([[1, 4], [7, 2], [3, 3], [0, 11]], dtype=np.int32)
-    gk, gv = torch.from_numpy(k8).cuda(), torch.from_numpy(v8).cuda()
-    pkv.pkv_copy_blocks(gk, gv, torch.from_numpy(pairs).cuda())
-    ek, ev = k8.copy(), v8.copy()
-    ek[4], ev[4], ek[2], ev[2] = k8[1], v8[1], k8[7], v8[7]
-    assert np.array_equal(gk.cpu().numpy(), ek) and np.array_equal(gv.cpu().numpy(), ev)
+    g = torch.from_numpy(kv8).cuda()
+    pkv.pkv_copy_blocks(g, None, torch.from_numpy(pairs).cuda())
+    want = kv8.copy()
+    want[4], want[2] = kv8[1], kv8[7]
+    assert np.array_equal(g.cpu().numpy(), want)

@@ -48,7 +48,7 @@ def _run_ex(dw, wl, kind, flags=0, window=0, kv8=None):
     out = torch.full(tuple(dw.q.shape), float("nan"), dtype=dt, device="cuda")
     ws = pkv.alloc_workspace(wl.num_seqs, wl.q_len, wl.n_q, wl.n_kv, wl.head_dim,
                              wl.block_size, flags=flags)
-    kc, vc = (dw.k_cache, dw.v_cache) if kv8 is None else (kv8.k_cache, kv8.v_cache)
+    kc, vc = (dw.k_cache, dw.v_cache) if kv8 is None else (kv8.kv_cache, None)
     pkv.pkv_paged_decode_attn_ex(dw.q, kc, vc, dw.block_tables, dw.context_lens, wl.scale, out,
                                  ws, flags=flags, window=window,
                                  k_scale=None if kv8 is None else kv8.k_scale,
@@ -79,14 +79,14 @@ def test_prefill_fp8_parity(oracle, case):
                      block_size=bs, context_lens=ctxs, seed=601 + n_q)
     c8 = fp8_cache_for(wl)
     dw, d8 = to_device(wl), fp8_to_device(c8)
-    pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.k_cache, d8.v_cache,
-                          d8.k_scale, d8.v_scale)
-    kc, vc = c8.k_cache.copy(), c8.v_cache.copy()
-    oracle.kv_append_fp8(wl.k_new, wl.v_new, wl.slot_mapping, kc, vc, c8.k_scale, c8.v_scale,
+    pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.kv_cache, d8.k_scale,
+                          d8.v_scale)
+    kv = c8.kv_cache.copy()
+    oracle.kv_append_fp8(wl.k_new, wl.v_new, wl.slot_mapping, kv, c8.k_scale, c8.v_scale,
                          block_size=bs)
-    assert np.array_equal(d8.k_cache.cpu().numpy(), kc)
+    assert np.array_equal(d8.kv_cache.cpu().numpy(), kv)
     for grid, window in ((0, 0), (7, 0), (0, 30)):
-        ref = oracle.paged_attn_fp8(wl.q, kc, vc, c8.k_scale, c8.v_scale, wl.block_tables,
+        ref = oracle.paged_attn_fp8(wl.q, kv, c8.k_scale, c8.v_scale, wl.block_tables,
                                     wl.context_lens, n_q=n_q, n_kv=n_kv, head_dim=d,
                                     block_size=bs, scale=wl.scale, window=window)
         flags = pkv.PKV_FLAG_GRID(grid) if grid else 0

@@ -45,10 +45,12 @@ MUTANTS = {
     "e4m3_ties_away": ("(long)rint(ldexp(a, 3 - e))", "(long)floor(ldexp(a, 3 - e) + 0.5)"),
     "e4m3_saturates_late": ("    if (a >= 448.0) {", "    if (a >= 480.0) {"),
     "e4m3_overflow_to_nan": ("code = 0x7E; /* the largest finite code", "code = 0x7F; /* the largest finite code"),
-    "fp8_k_scale_dropped": ("e4m3_value(c->k8[base + e]) * (double)c->k_scale[g]",
-                            "e4m3_value(c->k8[base + e])"),
-    "fp8_v_uses_k_scale": ("e4m3_value(c->v8[base + e]) * (double)c->v_scale[g]",
-                           "e4m3_value(c->v8[base + e]) * (double)c->k_scale[g]"),
+    "fp8_k_scale_dropped": ("e4m3_value(c->kv8[kbase8 + e]) * (double)c->k_scale[g]",
+                            "e4m3_value(c->kv8[kbase8 + e])"),
+    "fp8_v_uses_k_scale": ("e4m3_value(c->kv8[vbase8 + e]) * (double)c->v_scale[g]",
+                           "e4m3_value(c->kv8[vbase8 + e]) * (double)c->k_scale[g]"),
+    "fp8_v_rows_not_offset": ("size_t vbase8 = kbase8 + (size_t)block_size * head_dim;",
+                              "size_t vbase8 = kbase8;"),
     "fp8_append_head0_scale": ("/ k_scale[g];", "/ k_scale[0];"),
     "fp8_append_multiplies": ("/ v_scale[g];", "* v_scale[g];"),
     "window_one_too_wide": ("const long first_l = window > 0 ? pos - window + 1 : 0;",
