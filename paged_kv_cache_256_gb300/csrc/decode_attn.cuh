@@ -89,12 +89,16 @@ struct AttnCfg {
     static constexpr int kBoxes = KV8 ? 1 : D / 64;
     static constexpr int kBoxCols = KV8 ? D : 64;
     static constexpr int kBoxBytes = KV8 ? BS * D : BS * 128;
-    // Blocks per ring stage: one for the mma.sync consumers; 64 keys for the
-    // TMEM consumer, so one score MMA spans them (N = 64).  A stage is laid
-    // out as [K box 0][K box 1 (d 128)][V box 0][V box 1], each region
-    // holding the stage's blocks one after another (kRegion bytes), so the
-    // rows of all its blocks are contiguous within each 64-column region.
-    static constexpr int kBlocksPerStage = MODE == kModeTmem ? 64 / BS : 1;
+    // Blocks per ring stage.  TMEM consumer: 64 keys, so one score MMA spans
+    // them (N = 64).  mma.sync consumers: enough blocks for 8 KB of K + V --
+    // the stream slows down markedly with smaller stages (measured: 4 KB
+    // stages ran at ~4.3 TB/s, 8 KB ones at ~6 TB/s, whatever the dtype),
+    // since every stage costs a barrier round trip and a producer issue.  A
+    // stage is laid out as [K box 0][K box 1 (d 128)][V box 0][V box 1], each
+    // region holding the stage's blocks one after another (kRegion bytes), so
+    // the rows of all its blocks are contiguous within each 64-column region.
+    static constexpr int kBlocksPerStage =
+        MODE == kModeTmem ? 64 / BS : (2 * kTileBytes >= 8192 ? 1 : 8192 / (2 * kTileBytes));
     static constexpr int kRegion = kBlocksPerStage * kBoxBytes;
     static constexpr int kStageBytes = 2 * kBoxes * kRegion;
     // Per-lane floats a warp parks for a merge round: its accumulator, m[2], l[2].
@@ -129,6 +133,8 @@ struct AttnCfg {
                   "ring depth");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     static_assert(!(KV8 && MODE == kModeTmem), "8-bit caches use the mma.sync consumers");
+    // The mma.sync consumers address a block's boxes BS * 128 bytes apart.
+    static_assert(MODE == kModeTmem || kBlocksPerStage == 1 || kBoxes == 1, "stage layout");
 };
 
 // Byte offset of the 16-byte chunk holding (row, col..col+7) inside a tile
@@ -470,13 +476,15 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
     constexpr int KT = D / 16;   // 16-deep k steps of the score product
     constexpr int PT = BS / 16;  // 16-token tiles per block
     constexpr int WN = kConsumerWarps;
+    constexpr int SBS = C::kBlocksPerStage;
+    constexpr int UT = SBS * PT;  // 16-token tiles per stage
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3, mi = lane >> 3, rr = lane & 7;
     const int R = a.rows, cta = blockIdx.x;
     float* emit_tile = scratch + C::kMergeBytes / 4;
     float* emit_ml = emit_tile + kNarrowRows * C::kTileStride;
 
-    uint32_t gbase = 0;  // sequence number (in this CTA) of the piece's first block
+    uint32_t gbase = 0;  // sequence number (in this CTA) of the piece's first stage
     bool ok = true;
     int piece = 0;
     while (w.left > 0) {
@@ -527,40 +535,33 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
         for (int n = 0; n < MT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
 
+        // Warp w takes stages q == w (mod WN); stage q holds blocks
+        // q*SBS .. q*SBS + nb - 1 of the piece.  Tile u of its SBS * PT
+        // 16-token tiles belongs to block u / PT.
+        const int ns = (j1 - j0 + SBS - 1) / SBS;
         const int first = static_cast<int>((uint32_t)(warp + WN - (int)(gbase % WN)) % WN);
-        for (int jj = first; jj < j1 - j0; jj += WN) {
-            const int j = j0 + jj;
-            const uint32_t gidx = gbase + jj;
+        for (int q = first; q < ns; q += WN) {
+            const uint32_t gidx = gbase + q;
             const uint32_t stage = gidx % kStages;
             ok = consumer_wait(a, &full_bar[stage], (gidx / kStages) & 1u, ok, s_abort);
+            const int nb = min(SBS, j1 - j0 - q * SBS);  // blocks in this stage
             if (ok) {
-                const uint32_t kb = smem_addr(stages + stage * C::kStageBytes);
-                const uint32_t vb = kb + C::kTileBytes;
-
+                const uint32_t sb = smem_addr(stages + stage * C::kStageBytes);
                 // ---- S^T = K Q^T, two interleaved accumulators per 16-token tile
-                float st[PT][4], st2[PT][4];
+                float st[UT][4], st2[UT][4];
 #pragma unroll
-                for (int p = 0; p < PT; ++p)
+                for (int u = 0; u < UT; ++u)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) st[p][e] = st2[p][e] = 0.f;
-                // 8-bit V: every fragment of the block is read here, ahead of
-                // the score products and the softmax, so the shared-memory
-                // latency and the widening overlap with them.
-                uint32_t vr[KV8 ? PT : 1][KV8 ? D / 32 : 1][4];
-                if constexpr (KV8) {
+                    for (int e = 0; e < 4; ++e) st[u][e] = st2[u][e] = 0.f;
 #pragma unroll
-                    for (int tp = 0; tp < PT; ++tp)
+                for (int u = 0; u < UT; ++u) {
+                    const int bi = u / PT, tp = u % PT;
+                    if (bi >= nb) continue;
+                    const uint32_t kb = sb + bi * C::kBoxBytes;
+                    if constexpr (KV8) {
+                        // One x4 load: tokens (0-7, 8-15) x bytes (32j.., 32j+16..) = two k steps.
 #pragma unroll
-                        for (int j = 0; j < D / 32; ++j)
-                            ldmatrix_x4_trans(vr[tp][j], vb + swz8<D>(tp * 16 + (mi & 1) * 8 + rr,
-                                                                      32 * j + (mi >> 1) * 16));
-                }
-                if constexpr (KV8) {
-                    // One x4 load: tokens (0-7, 8-15) x bytes (32j.., 32j+16..) = two k steps.
-#pragma unroll
-                    for (int j = 0; j < D / 32; ++j) {
-#pragma unroll
-                        for (int tp = 0; tp < PT; ++tp) {
+                        for (int j = 0; j < D / 32; ++j) {
                             uint32_t r[4];
                             ldmatrix_x4(r, kb + swz8<D>(tp * 16 + (mi & 1) * 8 + rr,
                                                         32 * j + (mi >> 1) * 16));
@@ -569,38 +570,37 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                             e4m3x4_to_f16x2x2(r[1], k0[1], k0[3]);
                             e4m3x4_to_f16x2x2(r[2], k1[0], k1[2]);
                             e4m3x4_to_f16x2x2(r[3], k1[1], k1[3]);
-                            mma_f16_16816(st[tp], k0, qb[2 * j][0], qb[2 * j][1]);
-                            mma_f16_16816(st2[tp], k1, qb[2 * j + 1][0], qb[2 * j + 1][1]);
+                            mma_f16_16816(st[u], k0, qb[2 * j][0], qb[2 * j][1]);
+                            mma_f16_16816(st2[u], k1, qb[2 * j + 1][0], qb[2 * j + 1][1]);
                         }
-                    }
-                } else {
+                    } else {
 #pragma unroll
-                    for (int kk = 0; kk < KT; ++kk) {
-#pragma unroll
-                        for (int tp = 0; tp < PT; ++tp) {
+                        for (int kk = 0; kk < KT; ++kk) {
                             uint32_t ka[4];
                             ldmatrix_x4(ka, kb + swz<BS>(tp * 16 + (mi & 1) * 8 + rr,
                                                           kk * 16 + (mi >> 1) * 8));
                             if (kk & 1)
-                                mma_bf16_16816(st2[tp], ka, qb[kk][0], qb[kk][1]);
+                                mma_bf16_16816(st2[u], ka, qb[kk][0], qb[kk][1]);
                             else
-                                mma_bf16_16816(st[tp], ka, qb[kk][0], qb[kk][1]);
+                                mma_bf16_16816(st[u], ka, qb[kk][0], qb[kk][1]);
                         }
                     }
                 }
 
                 // ---- scale, causal / window / tail mask, online softmax (base 2)
-                const int tok0 = j * BS;
-                const bool need_mask = tok0 + BS - 1 > lim_min || tok0 < lo_max;
                 float mloc[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                for (int tp = 0; tp < PT; ++tp) {
+                for (int u = 0; u < UT; ++u) {
+                    const int bi = u / PT, tp = u % PT;
+                    const int tok0 = (j0 + q * SBS + bi) * BS;
+                    const bool need_mask = tok0 + BS - 1 > lim_min || tok0 < lo_max;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float x = (st[tp][e] + st2[tp][e]) * sl2;
+                        float x = (st[u][e] + st2[u][e]) * sl2;
                         const int tk = tok0 + tp * 16 + g + (e >> 1) * 8;
-                        if (need_mask && (tk > lim[e & 1] || tk < lo[e & 1])) x = -INFINITY;
-                        st[tp][e] = x;
+                        if (bi >= nb || (need_mask && (tk > lim[e & 1] || tk < lo[e & 1])))
+                            x = -INFINITY;
+                        st[u][e] = x;
                         mloc[e & 1] = fmaxf(mloc[e & 1], x);
                     }
                 }
@@ -617,11 +617,11 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                 }
                 float rsum[2] = {0.f, 0.f};
 #pragma unroll
-                for (int tp = 0; tp < PT; ++tp) {
+                for (int u = 0; u < UT; ++u) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float p = fast_exp2(st[tp][e] - mbase[e & 1]);
-                        st[tp][e] = p;
+                        const float p = fast_exp2(st[u][e] - mbase[e & 1]);
+                        st[u][e] = p;
                         rsum[e & 1] += p;
                     }
                 }
@@ -639,40 +639,43 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
 
                 // ---- P^T as B fragments: pack (tok g, rows 2t..) then transpose
                 // (bf16 against a bf16 cache, f16 against an 8-bit one)
-                uint32_t pb[PT][2], pl[PT][2];
+                uint32_t pb[UT][2], pl[UT][2];
 #pragma unroll
-                for (int tp = 0; tp < PT; ++tp) {
+                for (int u = 0; u < UT; ++u) {
                     if constexpr (KV8) {
-                        const uint32_t h0 = pack_f16x2(st[tp][0], st[tp][1]);
-                        const uint32_t h1 = pack_f16x2(st[tp][2], st[tp][3]);
-                        pb[tp][0] = movmatrix_trans(h0);
-                        pb[tp][1] = movmatrix_trans(h1);
+                        const uint32_t h0 = pack_f16x2(st[u][0], st[u][1]);
+                        const uint32_t h1 = pack_f16x2(st[u][2], st[u][3]);
+                        pb[u][0] = movmatrix_trans(h0);
+                        pb[u][1] = movmatrix_trans(h1);
                         if (OUT_F32) {
-                            pl[tp][0] = movmatrix_trans(pack_f16x2(st[tp][0] - f16_lo_to_f32(h0),
-                                                                   st[tp][1] - f16_hi_to_f32(h0)));
-                            pl[tp][1] = movmatrix_trans(pack_f16x2(st[tp][2] - f16_lo_to_f32(h1),
-                                                                   st[tp][3] - f16_hi_to_f32(h1)));
+                            pl[u][0] = movmatrix_trans(pack_f16x2(st[u][0] - f16_lo_to_f32(h0),
+                                                                  st[u][1] - f16_hi_to_f32(h0)));
+                            pl[u][1] = movmatrix_trans(pack_f16x2(st[u][2] - f16_lo_to_f32(h1),
+                                                                  st[u][3] - f16_hi_to_f32(h1)));
                         }
                     } else {
-                        const uint32_t h0 = pack_bf16x2(st[tp][0], st[tp][1]);
-                        const uint32_t h1 = pack_bf16x2(st[tp][2], st[tp][3]);
-                        pb[tp][0] = movmatrix_trans(h0);
-                        pb[tp][1] = movmatrix_trans(h1);
+                        const uint32_t h0 = pack_bf16x2(st[u][0], st[u][1]);
+                        const uint32_t h1 = pack_bf16x2(st[u][2], st[u][3]);
+                        pb[u][0] = movmatrix_trans(h0);
+                        pb[u][1] = movmatrix_trans(h1);
                         if (OUT_F32) {
-                            pl[tp][0] = movmatrix_trans(pack_bf16x2(st[tp][0] - bf16_lo_to_f32(h0),
-                                                                    st[tp][1] - bf16_hi_to_f32(h0)));
-                            pl[tp][1] = movmatrix_trans(pack_bf16x2(st[tp][2] - bf16_lo_to_f32(h1),
-                                                                    st[tp][3] - bf16_hi_to_f32(h1)));
+                            pl[u][0] = movmatrix_trans(pack_bf16x2(st[u][0] - bf16_lo_to_f32(h0),
+                                                                   st[u][1] - bf16_hi_to_f32(h0)));
+                            pl[u][1] = movmatrix_trans(pack_bf16x2(st[u][2] - bf16_lo_to_f32(h1),
+                                                                   st[u][3] - bf16_hi_to_f32(h1)));
                         }
                     }
                 }
 
                 // ---- O^T += V^T P^T (V rows past the context are zeroed: they may hold NaN)
-                const bool need_vmask = tok0 + BS > ctx;
 #pragma unroll
-                for (int tp = 0; tp < PT; ++tp) {
+                for (int u = 0; u < UT; ++u) {
+                    const int bi = u / PT, tp = u % PT;
+                    if (bi >= nb) continue;
+                    const uint32_t vb = sb + C::kBoxes * C::kRegion + bi * C::kBoxBytes;
+                    const int tok0 = (j0 + q * SBS + bi) * BS;
                     uint32_t vm0 = 0xFFFFFFFFu, vm8 = 0xFFFFFFFFu;
-                    if (need_vmask) {
+                    if (tok0 + BS > ctx) {
                         const int ta = tok0 + tp * 16 + 2 * t;
                         vm0 = (ta < ctx ? 0x0000FFFFu : 0u) | (ta + 1 < ctx ? 0xFFFF0000u : 0u);
                         vm8 = (ta + 8 < ctx ? 0x0000FFFFu : 0u) | (ta + 9 < ctx ? 0xFFFF0000u : 0u);
@@ -684,20 +687,22 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                         // d 32j + 2g (+1) and 32j + 16 + 2g (+1)).
 #pragma unroll
                         for (int j = 0; j < D / 32; ++j) {
-                            const uint32_t* r = vr[tp][j];
+                            uint32_t r[4];
+                            ldmatrix_x4_trans(r, vb + swz8<D>(tp * 16 + (mi & 1) * 8 + rr,
+                                                              32 * j + (mi >> 1) * 16));
                             uint32_t ev[4], od[4];
 #pragma unroll
-                            for (int m = 0; m < 4; ++m)
-                                e4m3x4_to_f16x2x2(prmt(r[m], 0u, 0x3120u), ev[m], od[m]);
+                            for (int mm = 0; mm < 4; ++mm)
+                                e4m3x4_to_f16x2x2(prmt(r[mm], 0u, 0x3120u), ev[mm], od[mm]);
                             const uint32_t ae[4] = {ev[0] & vm0, ev[2] & vm0, ev[1] & vm8,
                                                     ev[3] & vm8};
                             const uint32_t ao[4] = {od[0] & vm0, od[2] & vm0, od[1] & vm8,
                                                     od[3] & vm8};
-                            mma_f16_16816(o[2 * j], ae, pb[tp][0], pb[tp][1]);
-                            mma_f16_16816(o[2 * j + 1], ao, pb[tp][0], pb[tp][1]);
+                            mma_f16_16816(o[2 * j], ae, pb[u][0], pb[u][1]);
+                            mma_f16_16816(o[2 * j + 1], ao, pb[u][0], pb[u][1]);
                             if (OUT_F32) {
-                                mma_f16_16816(o[2 * j], ae, pl[tp][0], pl[tp][1]);
-                                mma_f16_16816(o[2 * j + 1], ao, pl[tp][0], pl[tp][1]);
+                                mma_f16_16816(o[2 * j], ae, pl[u][0], pl[u][1]);
+                                mma_f16_16816(o[2 * j + 1], ao, pl[u][0], pl[u][1]);
                             }
                         }
                     } else {
@@ -710,8 +715,8 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                             va[1] &= vm0;
                             va[2] &= vm8;
                             va[3] &= vm8;
-                            mma_bf16_16816(o[dm], va, pb[tp][0], pb[tp][1]);
-                            if (OUT_F32) mma_bf16_16816(o[dm], va, pl[tp][0], pl[tp][1]);
+                            mma_bf16_16816(o[dm], va, pb[u][0], pb[u][1]);
+                            if (OUT_F32) mma_bf16_16816(o[dm], va, pl[u][0], pl[u][1]);
                         }
                     }
                 }
@@ -719,7 +724,7 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
         }
-        gbase += j1 - j0;
+        gbase += ns;
 
         // ---- row sums across the 8 lanes of a row, then combine the warps' partials
 #pragma unroll
@@ -840,6 +845,7 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                                              int4& info0, int4& info1) {
     using C = AttnCfg<D, BS, kModeWide, KV8>;
     constexpr int kStages = C::kStages;
+    constexpr int SBS = C::kBlocksPerStage;
     constexpr int NT = D / 8;    // 8-wide output column tiles
     constexpr int KT = D / 16;   // 16-deep k steps over head_dim
     constexpr int PT = BS / 16;  // 16-token chunks per block
@@ -897,20 +903,27 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
         for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
 
+        // Column col takes stages q == col (mod WN); stage q holds blocks
+        // q*SBS .. q*SBS + nb - 1 of the piece.
+        const int ns = (j1 - j0 + SBS - 1) / SBS;
         const int first = static_cast<int>((uint32_t)(col + WN - (int)(gbase % WN)) % WN);
-        for (int jj = first; jj < j1 - j0; jj += WN) {
-            const int j = j0 + jj;
-            const uint32_t gidx = gbase + jj;
+        for (int q = first; q < ns; q += WN) {
+            const uint32_t gidx = gbase + q;
             const uint32_t stage = gidx % kStages;
             ok = consumer_wait(a, &full_bar[stage], (gidx / kStages) & 1u, ok, s_abort);
+            const int nb = min(SBS, j1 - j0 - q * SBS);  // blocks in this stage
             if (ok) {
-                const uint32_t kbase = smem_addr(stages + stage * C::kStageBytes);
-                const uint32_t vbase = kbase + C::kTileBytes;
+                const uint32_t sb = smem_addr(stages + stage * C::kStageBytes);
 
-                // The block is taken 16 tokens at a time (one online-softmax
-                // update per chunk), which keeps the live registers low.
+                // The stage's blocks are taken 16 tokens at a time (one
+                // online-softmax update per chunk): chunk u is token tile
+                // u % PT of block u / PT.  This keeps the live registers low.
 #pragma unroll 1
-                for (int tp = 0; tp < PT; ++tp) {
+                for (int u = 0; u < nb * PT; ++u) {
+                    const int bi = u / PT, tp = u % PT;
+                    const int j = j0 + q * SBS + bi;
+                    const uint32_t kbase = sb + bi * C::kBoxBytes;
+                    const uint32_t vbase = sb + C::kBoxes * C::kRegion + bi * C::kBoxBytes;
                     // ---- S = Q K^T over 16 tokens
                     float sc[2][4];
 #pragma unroll
@@ -1065,7 +1078,7 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
         }
-        gbase += j1 - j0;
+        gbase += ns;
 
         // ---- row sums across the quad, then combine the WN column partials
 #pragma unroll
