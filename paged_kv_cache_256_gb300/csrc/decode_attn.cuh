@@ -101,6 +101,17 @@ struct AttnCfg {
         MODE == kModeTmem ? 64 / BS : (2 * kTileBytes >= 8192 ? 1 : 8192 / (2 * kTileBytes));
     static constexpr int kRegion = kBlocksPerStage * kBoxBytes;
     static constexpr int kStageBytes = 2 * kBoxes * kRegion;
+    // An 8-bit cache keeps a (block, head)'s V rows right after its K rows,
+    // so one TMA box of 2 * BS rows fetches both: in its stages block b
+    // occupies [K rows][V rows] at b * 2 * kBoxBytes.  (bf16: K region(s),
+    // then V region(s), block b at b * kBoxBytes within each.)
+    __device__ static uint32_t k_tile(uint32_t stage, int b) {
+        return KV8 ? stage + b * 2 * kBoxBytes : stage + b * kBoxBytes;
+    }
+    __device__ static uint32_t v_tile(uint32_t stage, int b) {
+        return KV8 ? stage + b * 2 * kBoxBytes + kBoxBytes
+                   : stage + kBoxes * kRegion + b * kBoxBytes;
+    }
     // Per-lane floats a warp parks for a merge round: its accumulator, m[2], l[2].
     static constexpr int kLaneFloats = (MODE == kModeNarrow ? D / 4 : D / 2) + 4;
     static constexpr int kMergeBytes = MODE == kModeTmem ? 0 : kMergeSlots * 32 * kLaneFloats * 4;
@@ -340,7 +351,7 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
 // Lanes 0..kIssueLanes-1 fill consecutive stages side by side: one serial
 // wait/issue chain per stage would cap the stream.
 template <int D, int BS, int kStages, int kStageBytes, int kTileBytes, int kBoxBytes, int kBoxes,
-          int kBoxCols, int kRegion, int SBS>
+          int kBoxCols, int kRegion, int SBS, bool KV8>
 __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tmap_k,
                                         const CUtensorMap* tmap_v, Walk w, uint8_t* stages,
                                         uint64_t* full_bar, uint64_t* empty_bar,
@@ -398,13 +409,19 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                         const bool oob = blk < 0 || y64 >= a.tile_rows_total;
                         const int yk = oob ? a.tile_rows_total : static_cast<int>(y64);
                         const int yv = oob ? a.tile_rows_total : yk + a.v_row_off;
-                        uint8_t* kdst = stages + stage * kStageBytes + b * kBoxBytes;
+                        if constexpr (KV8) {
+                            // one box of 2 * BS rows: the K rows, then the V rows
+                            tma_load_2d(stages + stage * kStageBytes + b * 2 * kBoxBytes, tmap_k,
+                                        0, yk, &full_bar[stage], policy);
+                        } else {
+                            uint8_t* kdst = stages + stage * kStageBytes + b * kBoxBytes;
 #pragma unroll
-                        for (int half = 0; half < kBoxes; ++half) {
-                            tma_load_2d(kdst + half * kRegion, tmap_k, half * kBoxCols, yk,
-                                        &full_bar[stage], policy);
-                            tma_load_2d(kdst + (kBoxes + half) * kRegion, tmap_v,
-                                        half * kBoxCols, yv, &full_bar[stage], policy);
+                            for (int half = 0; half < kBoxes; ++half) {
+                                tma_load_2d(kdst + half * kRegion, tmap_k, half * kBoxCols, yk,
+                                            &full_bar[stage], policy);
+                                tma_load_2d(kdst + (kBoxes + half) * kRegion, tmap_v,
+                                            half * kBoxCols, yv, &full_bar[stage], policy);
+                            }
                         }
                     }
                 }
@@ -557,7 +574,7 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                 for (int u = 0; u < UT; ++u) {
                     const int bi = u / PT, tp = u % PT;
                     if (bi >= nb) continue;
-                    const uint32_t kb = sb + bi * C::kBoxBytes;
+                    const uint32_t kb = C::k_tile(sb, bi);
                     if constexpr (KV8) {
                         // One x4 load: tokens (0-7, 8-15) x bytes (32j.., 32j+16..) = two k steps.
 #pragma unroll
@@ -672,7 +689,7 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                 for (int u = 0; u < UT; ++u) {
                     const int bi = u / PT, tp = u % PT;
                     if (bi >= nb) continue;
-                    const uint32_t vb = sb + C::kBoxes * C::kRegion + bi * C::kBoxBytes;
+                    const uint32_t vb = C::v_tile(sb, bi);
                     const int tok0 = (j0 + q * SBS + bi) * BS;
                     uint32_t vm0 = 0xFFFFFFFFu, vm8 = 0xFFFFFFFFu;
                     if (tok0 + BS > ctx) {
@@ -922,8 +939,8 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                 for (int u = 0; u < nb * PT; ++u) {
                     const int bi = u / PT, tp = u % PT;
                     const int j = j0 + q * SBS + bi;
-                    const uint32_t kbase = sb + bi * C::kBoxBytes;
-                    const uint32_t vbase = sb + C::kBoxes * C::kRegion + bi * C::kBoxBytes;
+                    const uint32_t kbase = C::k_tile(sb, bi);
+                    const uint32_t vbase = C::v_tile(sb, bi);
                     // ---- S = Q K^T over 16 tokens
                     float sc[2][4];
 #pragma unroll
@@ -1590,7 +1607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kConsumerWarps) {
         produce<D, BS, kStages, C::kStageBytes, C::kTileBytes, C::kBoxBytes, C::kBoxes,
-                C::kBoxCols, C::kRegion, C::kBlocksPerStage>(
+                C::kBoxCols, C::kRegion, C::kBlocksPerStage, KV8>(
             a, &tmap_k, &tmap_v, w0, stages, full_bar, empty_bar, &s_abort);
         return;
     }

@@ -57,7 +57,9 @@ bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, long long 
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)head_dim * (kv8 ? 1 : 2)};
-    cuuint32_t box[2] = {kv8 ? (cuuint32_t)head_dim : 64u, (cuuint32_t)block_size};
+    // e4m3: one box covers a (block, head)'s K rows and the V rows after them
+    cuuint32_t box[2] = {kv8 ? (cuuint32_t)head_dim : 64u,
+                         (cuuint32_t)(kv8 ? 2 * block_size : block_size)};
     cuuint32_t estr[2] = {1u, 1u};
     const CUtensorMapSwizzle swz = (!kv8 || head_dim == 128) ? CU_TENSOR_MAP_SWIZZLE_128B
                                                              : CU_TENSOR_MAP_SWIZZLE_64B;
