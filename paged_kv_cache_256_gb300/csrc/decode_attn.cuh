@@ -291,46 +291,98 @@ __device__ __forceinline__ long long block_inclusive_scan(long long v, long long
     return v + before;
 }
 
-// All threads: this CTA's slice [start, end) of the flat (unit, block) list,
-// as the walk position of its first item.
+// The partition weighs a unit as its blocks plus a.unit_cost: the fixed work
+// of a unit (query load, cross-warp combine, output) in block equivalents.
+// Without it a CTA whose slice covers many short sequences does many units'
+// fixed work for the same bytes and finishes last.
+__device__ __forceinline__ long long seq_cost(const AttnArgs& a, int ctx, int bs) {
+    if (ctx == 0) return 0;
+    return (head_items(a, ctx, bs) + (long long)a.q_tiles * a.unit_cost) * a.n_kv;
+}
+
+// Block item (within the sequence) at cost offset o of a sequence: a position
+// inside a unit's fixed-cost prefix maps to the unit's first block.  The map
+// is non-decreasing, so consecutive CTAs' slices meet exactly.
+template <int BS>
+__device__ __forceinline__ long long cost_to_item(const AttnArgs& a, int ctx, long long o) {
+    const long long hi = head_items(a, ctx, BS);
+    const long long hc = hi + (long long)a.q_tiles * a.unit_cost;
+    const long long h = o / hc;
+    long long o2 = o % hc, before = 0;
+    for (int t = 0; t < a.q_tiles; ++t) {
+        const long long n = unit_end_block(a, ctx, t, BS) - unit_first_block(a, ctx, t, BS);
+        if (o2 < n + a.unit_cost)
+            return h * hi + before + (o2 > a.unit_cost ? o2 - a.unit_cost : 0);
+        o2 -= n + a.unit_cost;
+        before += n;
+    }
+    return h * hi + before;
+}
+
+// All threads: this CTA's slice of the flat (unit, block) list -- cost range
+// [c*C/grid, (c+1)*C/grid) mapped to block items -- as the walk position of
+// its first item.  s_pos: {seq, cost offset, item base} of the start and of
+// the end boundary.
 template <int BS>
 __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
-                                           long long* s_start) {
+                                           long long* s_pos) {
     const int tid = threadIdx.x, cta = blockIdx.x, grid = gridDim.x;
-    long long mine = 0;
-    for (int s = tid; s < a.num_seqs; s += kThreads) mine += head_items(a, unit_ctx(a, s, BS), BS);
-    long long total_blocks;
-    (void)block_inclusive_scan(mine, s_red, total_blocks);
-    const long long W = total_blocks * a.n_kv;
-    const long long start = (W * cta) / grid;
-    const long long end = (W * (cta + 1)) / grid;
+    long long mine_c = 0, mine_r = 0;
+    for (int s = tid; s < a.num_seqs; s += kThreads) {
+        const int ctx = unit_ctx(a, s, BS);
+        mine_c += seq_cost(a, ctx, BS);
+        mine_r += head_items(a, ctx, BS) * a.n_kv;
+    }
+    long long total_c, total_r;
+    (void)block_inclusive_scan(mine_c, s_red, total_c);
+    (void)block_inclusive_scan(mine_r, s_red, total_r);
+    const long long start = (total_c * cta) / grid;
+    const long long end = (total_c * (cta + 1)) / grid;
+    const bool end_inside = end < total_c;
     if (start < end) {
-        long long base = 0;
+        long long base_c = 0, base_r = 0;
         for (int s0 = 0; s0 < a.num_seqs; s0 += kThreads) {
             const int s = s0 + tid;
-            const long long v =
-                s < a.num_seqs ? head_items(a, unit_ctx(a, s, BS), BS) * a.n_kv : 0;
-            long long chunk;
-            const long long incl = block_inclusive_scan(v, s_red, chunk);
-            const long long excl = incl - v;
-            if (v > 0 && base + excl <= start && start < base + incl) {
-                s_start[0] = s;
-                s_start[1] = start - (base + excl);
+            const int ctx = s < a.num_seqs ? unit_ctx(a, s, BS) : 0;
+            const long long vc = s < a.num_seqs ? seq_cost(a, ctx, BS) : 0;
+            const long long vr = s < a.num_seqs ? head_items(a, ctx, BS) * a.n_kv : 0;
+            long long chunk_c, chunk_r;
+            const long long incl_c = block_inclusive_scan(vc, s_red, chunk_c);
+            const long long incl_r = block_inclusive_scan(vr, s_red, chunk_r);
+            const long long excl_c = base_c + incl_c - vc, excl_r = base_r + incl_r - vr;
+            if (vc > 0 && excl_c <= start && start < excl_c + vc) {
+                s_pos[0] = s;
+                s_pos[1] = start - excl_c;
+                s_pos[2] = excl_r;
             }
-            base += chunk;
+            if (end_inside && vc > 0 && excl_c <= end && end < excl_c + vc) {
+                s_pos[3] = s;
+                s_pos[4] = end - excl_c;
+                s_pos[5] = excl_r;
+            }
+            base_c += chunk_c;
+            base_r += chunk_r;
             __syncthreads();
-            if (s_start[0] >= 0) break;
+            if (s_pos[0] >= 0 && (!end_inside || s_pos[3] >= 0)) break;
         }
     }
     __syncthreads();
     Walk w;
-    w.left = end - start;
+    long long item0 = 0, item1 = 0;
+    if (start < end && s_pos[0] >= 0 && (!end_inside || s_pos[3] >= 0)) {
+        item0 = s_pos[2] + cost_to_item<BS>(a, unit_ctx(a, static_cast<int>(s_pos[0]), BS), s_pos[1]);
+        item1 = end_inside ? s_pos[5] + cost_to_item<BS>(
+                                            a, unit_ctx(a, static_cast<int>(s_pos[3]), BS), s_pos[4])
+                           : total_r;
+    }
+    w.left = item1 - item0;
     if (w.left > 0) {
-        w.s = static_cast<int>(s_start[0]);
+        w.s = static_cast<int>(s_pos[0]);
         w.ctx = unit_ctx(a, w.s, BS);
+        const long long off = item0 - s_pos[2];  // items into the sequence
         const long long per_head = head_items(a, w.ctx, BS);
-        w.h = static_cast<int>(s_start[1] / per_head);
-        long long rem = s_start[1] % per_head;
+        w.h = static_cast<int>(off / per_head);
+        long long rem = off % per_head;
         w.t = 0;
         walk_set_unit<BS>(a, w);
         while (rem >= w.nb - w.jlo) {  // the tile holding the slice's first item
@@ -340,6 +392,7 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
         }
         w.j = w.jlo + static_cast<int>(rem);
     } else {
+        w.left = 0;
         w.s = w.h = w.t = w.j = w.jlo = w.nb = w.ctx = 0;
     }
     return w;
@@ -1571,7 +1624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* empty_bar = full_bar + kStages;
 
     __shared__ long long s_red[kThreads / 32];
-    __shared__ long long s_start[2];
+    __shared__ long long s_pos[6];
     __shared__ int s_abort;
     __shared__ uint64_t s_tcb[10];  // TMEM mode: S ready/read, P ready, PV done (x2 each), 2 teardowns
     __shared__ uint32_t s_tmem;
@@ -1593,14 +1646,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_barrier_init();
         s_abort = 0;
-        s_start[0] = -1;
-        s_start[1] = 0;
+        for (int i = 0; i < 6; ++i) s_pos[i] = -1;
     }
     if (warp == kConsumerWarps && lane == 0) {
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
-    const Walk w0 = find_slice<BS>(a, s_red, s_start);  // also publishes the barrier init
+    const Walk w0 = find_slice<BS>(a, s_red, s_pos);  // also publishes the barrier init
     // Let the merge kernel (launched as a programmatic dependent) be scheduled
     // early; it waits for this whole grid before reading anything.
     if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

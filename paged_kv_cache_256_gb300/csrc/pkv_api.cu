@@ -138,6 +138,20 @@ int check_shape(int num_seqs, int q_len, int n_q, int n_kv, int head_dim, int bl
     return PKV_OK;
 }
 
+// A unit's fixed work (query load, cross-warp combine, output) in blocks of
+// streaming time: the weight the work partition gives each unit on top of
+// its blocks.  Measured per consumer on GB300 (ragged GQA, MQA verify and
+// chunked-prefill batches; uniform contexts do not care): rows <= 8 -- 6 for
+// bf16, 32 for 8-bit blocks, which stream in half the time while the unit's
+// fixed work grows (Q widened to f16); 8 < rows with an 8-bit cache -- 4
+// (every row-slice warp widens each tile, so blocks cost more); tensor-memory
+// consumer -- 12 (a 32 KB Q tile and the O read-out per unit).
+int unit_cost_for(int rows, bool kv8) {
+    if (rows <= 8) return kv8 ? 32 : 6;
+    if (kv8) return 4;
+    return rows > 64 ? 12 : 6;
+}
+
 // Query rows sharing one KV head are processed in tiles of at most 128.
 int tile_rows(int n_q, int n_kv, int q_len) {
     const int rows_total = (n_q / n_kv) * q_len;
@@ -307,6 +321,7 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     a.kv_mul = kv8 ? 2 : 1;
     a.v_row_off = kv8 ? block_size : 0;
     a.warp_rows = warp_rows_for(rows);
+    a.unit_cost = unit_cost_for(rows, kv8);
     a.k_scale = kv8 ? p->k_scale : nullptr;
     a.v_scale = kv8 ? p->v_scale : nullptr;
     // A window at least as wide as any context is no window.

@@ -43,6 +43,7 @@ struct AttnArgs {
     const float* k_scale;  // 8-bit caches: [n_kv] dequantisation scales (else unused)
     const float* v_scale;
     int window;        // 0: full causal attention; W > 0: a row sees its last W positions
+    int unit_cost;     // a unit's fixed work in block equivalents (work partition weight)
     int checked;
     int test_stall;    // failure-path tests: the producer issues nothing
     float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
