@@ -51,8 +51,8 @@
 //     one byte permute that separates the even and odd d of the pair, so the
 //     output columns are d = 32j + 16h + 2c + parity.  The per-head K scale
 //     is folded into the score scale and the V scale into the final
-//     normalisation.  Rows > 64 use the wide consumer (tcgen05 kind::f16
-//     would need Q in 8 bits).
+//     normalisation.  Rows > 64 use the tensor-memory consumer on f16 copies
+//     of the stages (see there).
 //
 // Bounded waits: every mbarrier wait gives up after a second, records
 // kErrTimeout in the workspace and the kernel winds down without hanging.
@@ -121,7 +121,11 @@ struct AttnCfg {
         MODE == kModeNarrow ? (kNarrowRows * kTileStride + 2 * kNarrowRows) * 4 : 0;
     // TMEM mode: the unit's 128 query rows as a swizzled K-major tile.
     static constexpr int kQTileBytes = MODE == kModeTmem ? 128 * D * 2 : 0;
-    static constexpr int kScratchBytes = kMergeBytes + kEmitBytes + kQTileBytes;
+    // TMEM mode over an 8-bit cache: two f16 copies of a 64-key stage (K and
+    // V, each 64 rows in D/64 swizzled 64-column regions).
+    static constexpr int kCvtRegion = 64 * 128;
+    static constexpr int kCvtBytes = (MODE == kModeTmem && KV8) ? 2 * 2 * (D / 64) * kCvtRegion : 0;
+    static constexpr int kScratchBytes = kMergeBytes + kEmitBytes + kQTileBytes + kCvtBytes;
     static constexpr int kMaxStages = KV8 ? 48 : 32;
     static constexpr int kBarrierBytes = 2 * kMaxStages * 8;
     static constexpr int kBudget = 227 * 1024 - 1024 - kScratchBytes - kBarrierBytes - 1024;
@@ -143,7 +147,6 @@ struct AttnCfg {
                                     : (kStages % kConsumerWarps == 0 && kStages >= kConsumerWarps),
                   "ring depth");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-    static_assert(!(KV8 && MODE == kModeTmem), "8-bit caches use the mma.sync consumers");
     // The mma.sync consumers address a block's boxes BS * 128 bytes apart.
     static_assert(MODE == kModeTmem || kBlocksPerStage == 1 || kBoxes == 1, "stage layout");
 };
@@ -1284,13 +1287,19 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 // PV update of one overlaps the softmax of the next.  TMEM columns: O
 // [0, 128), S 2 x 64 from 128, P 2 x 32 from 256, the low halves of P for
 // fp32 output 2 x 32 from 320.
-template <int D, int BS, bool OUT_F32>
+// Over an 8-bit cache (KV8) warps 6 and 7 widen each landed stage into one of
+// two f16 copies (K and V in the layout the bf16 stages have, V rows past the
+// context zeroed) and free the stage; the MMAs read the copies as kind::f16
+// with Q and P in f16 (every e4m3 value is exact in f16), and the PV product
+// frees the copy.  The per-head K scale joins the score scale, the V scale
+// the normalisation.
+template <int D, int BS, bool OUT_F32, bool KV8>
 __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t* stages,
                                              uint8_t* qtile, uint64_t* full_bar,
                                              uint64_t* empty_bar, uint64_t* tcb,
                                              uint32_t* s_tmem, volatile int* s_abort,
                                              int4& info0, int4& info1) {
-    using C = AttnCfg<D, BS, kModeTmem>;
+    using C = AttnCfg<D, BS, kModeTmem, KV8>;
     constexpr int kStages = C::kStages;
     constexpr int kKeys = 64;                  // keys per softmax round
     constexpr int SB = C::kBlocksPerStage;     // blocks per super-block (= per stage)
@@ -1299,15 +1308,21 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     constexpr uint32_t kColO = 0, kColS = 128, kColP = 256, kColPL = 320;
     constexpr int KT = D / 16;   // k steps of S = Q K^T
     constexpr int kQHalf = 128 * 128;  // bytes of one 64-column half of the Q tile
-    constexpr int kParty = 192;        // warps 0..5 take part in this mode
+    constexpr int kParty = KV8 ? 256 : 192;  // warps 0..5 take part (0..7 with converters)
+    constexpr int kHalves = D / 64;          // 64-column regions of an f16 K or V copy
     // tcb: [0..1] S ready, [2..3] S read, [4..5] P ready, [6..7] PV done, [8] QK teardown,
     //      [9] PV teardown
     uint64_t* s_full = tcb;
     uint64_t* s_free = tcb + 2;
     uint64_t* p_full = tcb + 4;
     uint64_t* pv_done = tcb + 6;
+    uint64_t* cvt_full = tcb + 10;  // 8-bit cache: f16 copy [g&1] ready
+    uint64_t* cvt_free = tcb + 12;  // 8-bit cache: f16 copy [g&1] read by its PV product
+    // f16 copies (8-bit cache): copy c at cvt + c * kCopy, K regions then V regions
+    uint8_t* cvt = qtile + C::kQTileBytes;
+    constexpr int kCopy = 2 * kHalves * C::kCvtRegion;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp > 5) return;  // warps 6, 7 have no part in this mode
+    if (warp > 5 && !KV8) return;  // warps 6, 7 have no part in this mode over bf16
     const bool softmax = warp < 4;
     const int row = threadIdx.x;  // softmax threads: row = TMEM lane
     const int R = a.rows, cta = blockIdx.x;
@@ -1318,8 +1333,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     tc_fence_after();
     const uint32_t tbase = *s_tmem;
     const uint32_t tlane = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t idesc_qk = umma_idesc_bf16(128, kKeys, false);
-    const uint32_t idesc_pv = umma_idesc_bf16(128, D, true);
+    const uint32_t idesc_qk = KV8 ? umma_idesc_f16(128, kKeys, false) : umma_idesc_bf16(128, kKeys, false);
+    const uint32_t idesc_pv = KV8 ? umma_idesc_f16(128, D, true) : umma_idesc_bf16(128, D, true);
     const uint32_t q_saddr = smem_addr(qtile);
 
     auto issuer_fail = [&](bool& ok) {
@@ -1348,7 +1363,12 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 a.q + (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D);
             uint4 qv[D / 8];
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) qv[c] = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < D / 8; ++c) {
+                qv[c] = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (KV8)  // f16 operands: Q as f16 too
+                    qv[c] = make_uint4(bf16x2_to_f16x2(qv[c].x), bf16x2_to_f16x2(qv[c].y),
+                                       bf16x2_to_f16x2(qv[c].z), bf16x2_to_f16x2(qv[c].w));
+            }
 #pragma unroll
             for (int c = 0; c < D / 8; ++c)
                 *reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + row * 128 +
@@ -1369,21 +1389,25 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         issuer_fail(ok);
                         break;
                     }
-                    if (*s_abort || !mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u)) {
+                    if (*s_abort ||
+                        !(KV8 ? mbar_wait_bounded(&cvt_full[g & 1u], (g >> 1) & 1u)
+                              : mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u))) {
                         issuer_fail(ok);
                         break;
                     }
                     tc_fence_after();
                     // Rows past the stage's blocks (a partial last super-block)
                     // hold stale keys; the softmax masks their columns.
-                    const uint32_t kb = smem_addr(stages + st * C::kStageBytes);
+                    const uint32_t kb = KV8 ? smem_addr(cvt + (g & 1u) * kCopy)
+                                            : smem_addr(stages + st * C::kStageBytes);
+                    constexpr uint32_t kKRegion = KV8 ? C::kCvtRegion : C::kRegion;
                     const uint32_t scol = tbase + kColS + (g & 1u) * kKeys;
 #pragma unroll
                     for (int kk = 0; kk < KT; ++kk) {
                         const uint64_t ad = umma_smem_desc(
                             q_saddr + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
                         const uint64_t bd = umma_smem_desc(
-                            kb + (kk >> 2) * C::kRegion + (kk & 3) * 32, 16, 1024);
+                            kb + (kk >> 2) * kKRegion + (kk & 3) * 32, 16, 1024);
                         umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&s_full[g & 1u]);
@@ -1405,24 +1429,82 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     // Only the keys of the stage's blocks enter the product.
                     const int nk16 = min(SB, n - q * SB) * (BS / 16);
                     const uint32_t vb =
-                        smem_addr(stages + st * C::kStageBytes) + C::kBoxes * C::kRegion;
+                        KV8 ? smem_addr(cvt + (g & 1u) * kCopy) + kHalves * C::kCvtRegion
+                            : smem_addr(stages + st * C::kStageBytes) + C::kBoxes * C::kRegion;
+                    constexpr uint32_t kVRegion = KV8 ? C::kCvtRegion : C::kRegion;
                     const uint32_t pcol = (g & 1u) * (kKeys / 2);
                     for (int kk = 0; kk < nk16; ++kk) {
-                        const uint64_t bd = umma_smem_desc(vb + kk * 16 * 128, C::kRegion, 1024);
+                        const uint64_t bd = umma_smem_desc(vb + kk * 16 * 128, kVRegion, 1024);
                         umma_ts(tbase + kColO, tbase + kColP + pcol + kk * 8, bd, idesc_pv,
                                 (q > 0 || kk > 0) ? 1u : 0u);
                         if (OUT_F32)
                             umma_ts(tbase + kColO, tbase + kColPL + pcol + kk * 8, bd, idesc_pv,
                                     1u);
                     }
-                    umma_commit(&empty_bar[st]);    // K and V of this stage are consumed
-                    umma_commit(&pv_done[g & 1u]);  // its P buffer is free; O is current
+                    if (KV8)
+                        umma_commit(&cvt_free[g & 1u]);  // the f16 copy is consumed
+                    else
+                        umma_commit(&empty_bar[st]);  // K and V of this stage are consumed
+                    umma_commit(&pv_done[g & 1u]);    // its P buffer is free; O is current
                 }
             }
             __syncwarp();
+        } else if (warp >= 6) {
+            // ===================== f16 copies (8-bit cache; warps 6, 7) ============
+            if constexpr (KV8) {
+                // Warp 6 widens the K rows, warp 7 the V rows; each arrives on
+                // its own (the copy-ready and stage-free barriers count 2), so
+                // neither ever waits for the other.
+                const int isv = warp - 6;
+                constexpr int kChunks = D / 16;  // 16-byte e4m3 chunks per row
+                for (int q = 0; q < nsb; ++q) {
+                    const uint32_t g = gbase + q, st = g % kStages;
+                    bool good = !*s_abort && mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u);
+                    if (good && g >= 2)
+                        good = mbar_wait_bounded(&cvt_free[g & 1u], ((g - 2) >> 1) & 1u);
+                    if (!__all_sync(0xffffffffu, good)) {
+                        if (lane == 0) {
+                            atomicOr(a.err, kErrTimeout);
+                            *s_abort = 1;
+                        }
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nb = min(SB, n - q * SB);
+                    const int tok0 = (j0 + q * SB) * BS;
+                    const uint8_t* src = stages + st * C::kStageBytes + isv * C::kBoxBytes;
+                    uint8_t* dst = cvt + (g & 1u) * kCopy + isv * kHalves * C::kCvtRegion;
+                    // item = (key row n, 16-byte chunk cb of e4m3 codes)
+                    for (int it = lane; it < 64 * kChunks; it += 32) {
+                        const int nrow = it / kChunks, cb = it % kChunks;
+                        const int b = nrow / BS, r = nrow % BS;
+                        uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+                        if (b < nb && tok0 + nrow < ctx) {  // a resident key: widen
+                            const uint8_t* box = src + b * 2 * C::kBoxBytes;
+                            const uint4 v = *reinterpret_cast<const uint4*>(box + swz8<D>(r, cb * 16));
+                            e4m3x4_to_f16x2x2(v.x, o0.x, o0.y);
+                            e4m3x4_to_f16x2x2(v.y, o0.z, o0.w);
+                            e4m3x4_to_f16x2x2(v.z, o1.x, o1.y);
+                            e4m3x4_to_f16x2x2(v.w, o1.z, o1.w);
+                        }
+                        // f16 chunks 2cb, 2cb + 1 (d 16cb ..): region (2cb) / 8, chunk (2cb) % 8
+                        uint8_t* row = dst + ((2 * cb) / 8) * C::kCvtRegion + nrow * 128;
+                        const int c0 = (2 * cb) % 8;
+                        *reinterpret_cast<uint4*>(row + ((c0 ^ (nrow & 7)) << 4)) = o0;
+                        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (nrow & 7)) << 4)) = o1;
+                    }
+                    fence_proxy_async_smem();  // the copy, for the tensor cores
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&cvt_full[g & 1u]);
+                        mbar_arrive(&empty_bar[st]);  // (both warps: the e4m3 stage is free)
+                    }
+                }
+            }
         } else {
             // ===================== softmax (thread = row) =====================
             float m_used = -INFINITY, l = 0.f;
+            const float sl2 = KV8 ? a.scale_log2 * __ldg(a.k_scale + h) : a.scale_log2;
             const int lim_min = ctx - a.q_len + tile_first_token(a, w.t);
             const int lo_max =
                 a.window > 0 ? ctx - a.q_len + tile_last_token(a, w.t) - a.window + 1 : INT_MIN;
@@ -1441,7 +1523,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         tmem_wait_ld();
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            x[h2 * 32 + c] = __uint_as_float(sr[c]) * a.scale_log2;
+                            x[h2 * 32 + c] = __uint_as_float(sr[c]) * sl2;
                     }
                     tc_fence_before();
                     mbar_arrive(&s_free[sq & 1u]);  // S buffer may take the super-block after next
@@ -1496,10 +1578,17 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     const float p0 = m_used == -INFINITY ? 0.f : fast_exp2(x[c] - m_used);
                     const float p1 = m_used == -INFINITY ? 0.f : fast_exp2(x[c + 1] - m_used);
                     rs += p0 + p1;
-                    ph[c / 2] = pack_bf16x2(p0, p1);
-                    if (OUT_F32)
-                        pl[c / 2] = pack_bf16x2(p0 - bf16_lo_to_f32(ph[c / 2]),
-                                                p1 - bf16_hi_to_f32(ph[c / 2]));
+                    if constexpr (KV8) {
+                        ph[c / 2] = pack_f16x2(p0, p1);
+                        if (OUT_F32)
+                            pl[c / 2] = pack_f16x2(p0 - f16_lo_to_f32(ph[c / 2]),
+                                                   p1 - f16_hi_to_f32(ph[c / 2]));
+                    } else {
+                        ph[c / 2] = pack_bf16x2(p0, p1);
+                        if (OUT_F32)
+                            pl[c / 2] = pack_bf16x2(p0 - bf16_lo_to_f32(ph[c / 2]),
+                                                    p1 - bf16_hi_to_f32(ph[c / 2]));
+                    }
                 }
                 l += rs;
                 tmem_st32(tlane + kColP + (sq & 1u) * (kKeys / 2), ph);
@@ -1509,7 +1598,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 // Only a unit's last block reaches past the context, and it is
                 // the last block of its super-block.
                 const int tokl = tok0 + (nb - 1) * BS;
-                if (tokl + BS > ctx) {
+                if (!KV8 && tokl + BS > ctx) {  // (the f16 copies come zeroed there)
                     uint8_t* vt = stages + (sq % kStages) * C::kStageBytes +
                                   C::kBoxes * C::kRegion + (nb - 1) * C::kBoxBytes;
                     const int valid = ctx - tokl;  // >= 1: the block holds a resident token
@@ -1534,7 +1623,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             const bool first_piece = j0 == w.jlo, last_piece = j1 == w.nb;
             const bool whole = first_piece && last_piece;
             if (ok) {
-                const float scl = whole ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
+                const float vsc = KV8 ? __ldg(a.v_scale + h) : 1.f;
+                const float scl = (whole ? (l > 0.f ? 1.f / l : 0.f) : 1.f) * vsc;
                 const size_t rec = (size_t)cta * 2 + (piece == 0 ? 0 : 1);
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
@@ -1565,11 +1655,12 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                                         pack_bf16x2(__uint_as_float(ov[c + 6]) * scl, __uint_as_float(ov[c + 7]) * scl));
                             }
                         } else {
+                            // a record keeps o unnormalised (scl is the V scale, 1 for bf16)
                             float4* op = reinterpret_cast<float4*>(a.rec_o + (rec * R + row) * D + c0);
 #pragma unroll
                             for (int c = 0; c < 32; c += 4)
-                                op[c / 4] = make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]),
-                                                        __uint_as_float(ov[c + 2]), __uint_as_float(ov[c + 3]));
+                                op[c / 4] = make_float4(__uint_as_float(ov[c]) * scl, __uint_as_float(ov[c + 1]) * scl,
+                                                        __uint_as_float(ov[c + 2]) * scl, __uint_as_float(ov[c + 3]) * scl);
                         }
                     }
                 }
@@ -1626,13 +1717,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ long long s_red[kThreads / 32];
     __shared__ long long s_pos[6];
     __shared__ int s_abort;
-    __shared__ uint64_t s_tcb[10];  // TMEM mode: S ready/read, P ready, PV done (x2 each), 2 teardowns
+    // TMEM mode: S ready/read, P ready, PV done (x2 each), 2 teardowns, and over an
+    // 8-bit cache f16 copy ready / free (x2 each)
+    __shared__ uint64_t s_tcb[14];
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Arrivals that release a stage: one per 16-row slice (wide), one warp
-    // (narrow), one tensor-core commit (TMEM mode).
-    const int releases = MODE == kModeWide ? a.warp_rows : 1;
+    // (narrow), one tensor-core commit (TMEM mode), the two converter warps
+    // (TMEM mode over an 8-bit cache).
+    const int releases = MODE == kModeWide ? a.warp_rows : (MODE == kModeTmem && KV8 ? 2 : 1);
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full_bar[i], 1);
@@ -1641,8 +1735,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (MODE == kModeTmem) {
             // S ready (a commit), S read (128 rows), P ready (128 rows),
             // PV done (a commit), two issuer teardowns (a commit each)
-            const uint32_t counts[10] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1};
-            for (int i = 0; i < 10; ++i) mbar_init(&s_tcb[i], counts[i]);
+            const uint32_t counts[14] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1, KV8 ? 2u : 1u,
+                                         KV8 ? 2u : 1u, 1, 1};
+            for (int i = 0; i < 14; ++i) mbar_init(&s_tcb[i], counts[i]);
         }
         fence_barrier_init();
         s_abort = 0;
@@ -1691,8 +1786,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         consume_wide<D, BS, OUT_F32, KV8>(a, w0, stages, scratch, full_bar, empty_bar, &s_abort,
                                           info0, info1);
     else
-        consume_tmem<D, BS, OUT_F32>(a, w0, stages, reinterpret_cast<uint8_t*>(scratch), full_bar,
-                                     empty_bar, s_tcb, &s_tmem, &s_abort, info0, info1);
+        consume_tmem<D, BS, OUT_F32, KV8>(a, w0, stages, reinterpret_cast<uint8_t*>(scratch),
+                                          full_bar, empty_bar, s_tcb, &s_tmem, &s_abort, info0,
+                                          info1);
     if (tid == 0) {
         a.rec_info[(size_t)blockIdx.x * 2 + 0] = info0;
         a.rec_info[(size_t)blockIdx.x * 2 + 1] = info1;
@@ -1720,18 +1816,16 @@ static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CU
     return cudaGetLastError();
 }
 
-// Consumer by rows per KV head: narrow (<= 8), wide, TMEM (> 64; bf16 caches only).
+// Consumer by rows per KV head: narrow (<= 8), wide, TMEM (> 64).
 template <int D, int BS, bool KV8>
 static cudaError_t launch_shape(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                 bool out_f32, int grid, cudaStream_t stream) {
     if (a.rows <= kNarrowRows)
         return out_f32 ? launch_one<D, BS, true, kModeNarrow, KV8>(a, tk, tv, grid, stream)
                        : launch_one<D, BS, false, kModeNarrow, KV8>(a, tk, tv, grid, stream);
-    if constexpr (!KV8) {
-        if (a.rows > kTmemMinRows)
-            return out_f32 ? launch_one<D, BS, true, kModeTmem, false>(a, tk, tv, grid, stream)
-                           : launch_one<D, BS, false, kModeTmem, false>(a, tk, tv, grid, stream);
-    }
+    if (a.rows > kTmemMinRows)
+        return out_f32 ? launch_one<D, BS, true, kModeTmem, KV8>(a, tk, tv, grid, stream)
+                       : launch_one<D, BS, false, kModeTmem, KV8>(a, tk, tv, grid, stream);
     return out_f32 ? launch_one<D, BS, true, kModeWide, KV8>(a, tk, tv, grid, stream)
                    : launch_one<D, BS, false, kModeWide, KV8>(a, tk, tv, grid, stream);
 }

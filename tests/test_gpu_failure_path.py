@@ -39,3 +39,37 @@ def test_expired_waits_are_reported_and_the_context_survives(oracle, case):
     # the context is still usable and the next call is right
     _, _, ref = oracle_after_append(oracle, wl)
     assert_close(out_to_host(run_attn(dw, wl, "bf16")), ref, "bf16", "after a timed-out call")
+
+
+def test_expired_waits_over_an_8bit_cache(oracle):
+    """The same with an e4m3 cache and 128 rows per KV head (tensor-memory consumer
+    with its f16-copy warps): every wait expires, the report arrives, the next call
+    is right."""
+    import torch
+    from paged_kv_cache_256_gb300.device import fp8_to_device
+    from paged_kv_cache_256_gb300.workloads import fp8_cache_for
+    n_q, n_kv, q_len, d, bs, ctxs = 32, 1, 4, 128, 32, [90, 700, 33]
+    wl = make_custom(num_seqs=len(ctxs), q_len=q_len, n_q=n_q, n_kv=n_kv, head_dim=d,
+                     block_size=bs, context_lens=ctxs, seed=78)
+    c8 = fp8_cache_for(wl)
+    dw, d8 = to_device(wl), fp8_to_device(c8)
+    pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.kv_cache, d8.k_scale, d8.v_scale)
+    kv = c8.kv_cache.copy()
+    oracle.kv_append_fp8(wl.k_new, wl.v_new, wl.slot_mapping, kv, c8.k_scale, c8.v_scale,
+                         block_size=bs)
+    out = torch.empty(tuple(dw.q.shape), dtype=torch.float32, device="cuda")
+
+    def call(flags):
+        ws = pkv.alloc_workspace(wl.num_seqs, q_len, n_q, n_kv, d, bs, flags=flags)
+        pkv.pkv_paged_decode_attn_ex(dw.q, d8.kv_cache, None, dw.block_tables, dw.context_lens,
+                                     wl.scale, out, ws, flags=flags, k_scale=d8.k_scale,
+                                     v_scale=d8.v_scale)
+        return pkv.pkv_check_error(ws)
+
+    assert call(pkv.PKV_FLAG_TEST_STALL | pkv.PKV_FLAG_GRID(4)) == pkv.PKV_ERR_TIMEOUT
+    assert call(0) == pkv.PKV_OK
+    ref = oracle.paged_attn_fp8(wl.q, kv, c8.k_scale, c8.v_scale, wl.block_tables,
+                                wl.context_lens, n_q=n_q, n_kv=n_kv, head_dim=d, block_size=bs,
+                                scale=wl.scale)
+    assert_close(out_to_host(out), ref, "f32", "8-bit cache after a timed-out call")
+
