@@ -204,32 +204,72 @@ __device__ __forceinline__ bool unit_row(const AttnArgs& a, int t, int h, int r,
     return valid;
 }
 
-// One past the last block tile t can see: its last row sits at position
-// ctx - q_len + i_last and sees nothing later (causal).  At least one block
-// when ctx > 0, so a tile whose rows all precede the context still writes
-// its zero rows; none when ctx == 0.
-__device__ __forceinline__ int unit_end_block(const AttnArgs& a, int ctx, int t, int bs) {
-    long long vis = (long long)ctx - a.q_len + tile_last_token(a, t) + 1;
-    if (vis < 1) vis = 1;
-    if (vis > ctx) vis = ctx;
-    return static_cast<int>((vis + bs - 1) / bs);
+// One past the last block a tile whose last query token is last_tok can see:
+// that row sits at position ctx - q_len + last_tok and sees nothing later
+// (causal).  At least one block when ctx > 0, so a tile whose rows all
+// precede the context still writes its zero rows; none when ctx == 0.
+// (ctx - q_len + last_tok + 1 <= ctx: no overflow.)
+__device__ __forceinline__ int tok_end_block(const AttnArgs& a, int ctx, int last_tok, int bs) {
+    const int vis = max(1, min(ctx - a.q_len + last_tok + 1, ctx));
+    return static_cast<int>((static_cast<unsigned>(vis) + bs - 1) / static_cast<unsigned>(bs));
 }
 
-// First block any row of tile t can see: with a sliding window, its earliest
-// row (position ctx - q_len + i_first) sees nothing before that position
-// minus W - 1, so earlier blocks are never read.  Always < unit_end_block.
-__device__ __forceinline__ int unit_first_block(const AttnArgs& a, int ctx, int t, int bs) {
+// First block a tile whose first query token is first_tok can see: with a
+// sliding window, its earliest row (position ctx - q_len + first_tok) sees
+// nothing before that position minus W - 1, so earlier blocks are never
+// read.  Always < tok_end_block of the same tile.
+__device__ __forceinline__ int tok_first_block(const AttnArgs& a, int ctx, int first_tok, int bs) {
     if (a.window <= 0) return 0;
-    const long long lo = (long long)ctx - a.q_len + tile_first_token(a, t) - a.window + 1;
-    return lo > 0 ? static_cast<int>(lo / bs) : 0;
+    const long long lo = (long long)ctx - a.q_len + first_tok - a.window + 1;
+    return lo > 0 ? static_cast<int>(static_cast<unsigned>(lo) / static_cast<unsigned>(bs)) : 0;
 }
+
+__device__ __forceinline__ int unit_end_block(const AttnArgs& a, int ctx, int t, int bs) {
+    return tok_end_block(a, ctx, tile_last_token(a, t), bs);
+}
+__device__ __forceinline__ int unit_first_block(const AttnArgs& a, int ctx, int t, int bs) {
+    return tok_first_block(a, ctx, tile_first_token(a, t), bs);
+}
+
+// The first and last query tokens of tiles 0, 1, 2, ... in turn, without a
+// division per tile: the first row t * rows of the tile is carried as a
+// token and a row within the token's group.
+struct TileSteps {
+    int fq, fr, dq, dr, g, qmax;
+    __device__ __forceinline__ explicit TileSteps(const AttnArgs& a)
+        : fq(0), fr(0), dq(a.rows / a.group), dr(a.rows % a.group), g(a.group), qmax(a.q_len - 1) {}
+    __device__ __forceinline__ int first() const { return fq; }
+    __device__ __forceinline__ int last() const {  // the row before the next tile's first
+        int nq = fq + dq, nr = fr + dr;
+        if (nr >= g) {
+            nr -= g;
+            ++nq;
+        }
+        return min(nr > 0 ? nq : nq - 1, qmax);
+    }
+    __device__ __forceinline__ void next() {
+        fq += dq;
+        fr += dr;
+        if (fr >= g) {
+            fr -= g;
+            ++fq;
+        }
+    }
+};
 
 // Work items (blocks to read) of one KV head of sequence s, over all its tiles.
 __device__ __forceinline__ long long head_items(const AttnArgs& a, int ctx, int bs) {
     if (ctx == 0) return 0;
+    // One row tile and no window (every decode step): the unit reads every block.
+    if (a.q_tiles == 1 && a.window <= 0)
+        return static_cast<long long>((static_cast<unsigned>(ctx) + bs - 1) / static_cast<unsigned>(bs));
+    TileSteps ts(a);
     long long n = 0;
-    for (int t = 0; t < a.q_tiles; ++t)
-        n += unit_end_block(a, ctx, t, bs) - unit_first_block(a, ctx, t, bs);
+#pragma unroll 1
+    for (int t = 0; t < a.q_tiles; ++t) {
+        n += tok_end_block(a, ctx, ts.last(), bs) - tok_first_block(a, ctx, ts.first(), bs);
+        ts.next();
+    }
     return n;
 }
 
@@ -271,130 +311,181 @@ __device__ __forceinline__ int piece_end(const Walk& w) {
     return (long long)w.nb < (long long)w.j + w.left ? w.nb : static_cast<int>(w.j + w.left);
 }
 
-// Block-wide inclusive scan of one 64-bit value per thread (all kThreads).
-__device__ __forceinline__ long long block_inclusive_scan(long long v, long long* s_red,
-                                                          long long& total) {
+// Block-wide inclusive scan of two 64-bit values per thread (all kThreads);
+// s_red holds 2 * kThreads / 32 values.
+__device__ __forceinline__ void block_inclusive_scan2(long long& c, long long& r, long long* s_red,
+                                                      long long& total_c, long long& total_r) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        long long n = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += n;
+        const long long nc = __shfl_up_sync(0xffffffffu, c, off);
+        const long long nr = __shfl_up_sync(0xffffffffu, r, off);
+        if (lane >= off) {
+            c += nc;
+            r += nr;
+        }
     }
-    if (lane == 31) s_red[warp] = v;
+    if (lane == 31) {
+        s_red[2 * warp] = c;
+        s_red[2 * warp + 1] = r;
+    }
     __syncthreads();
-    long long before = 0;
-    total = 0;
+    long long bc = 0, br = 0;
+    total_c = total_r = 0;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) {
-        const long long t = s_red[w];
-        if (w < warp) before += t;
-        total += t;
+        const long long tc = s_red[2 * w], tr = s_red[2 * w + 1];
+        if (w < warp) {
+            bc += tc;
+            br += tr;
+        }
+        total_c += tc;
+        total_r += tr;
     }
     __syncthreads();
-    return v + before;
+    c += bc;
+    r += br;
+}
+
+// a / b for a >= 0, b > 0: one 32-bit division when both fit, as they do but
+// for batches of billions of blocks.
+__device__ __forceinline__ long long div_nn(long long a, long long b) {
+    if ((((unsigned long long)a | (unsigned long long)b) >> 32) == 0)
+        return static_cast<long long>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+    return a / b;
+}
+
+// Block item (within the sequence) at cost offset o of a sequence: a position
+// inside a unit's fixed-cost prefix maps to the unit's first block.  The map
+// is non-decreasing, so consecutive CTAs' slices meet exactly.  Also the
+// item's unit (KV head h, row tile t) and block j.
+struct ItemPos {
+    long long item;
+    int h, t, j;
+};
+
+template <int BS>
+__device__ __forceinline__ ItemPos cost_to_item(const AttnArgs& a, int ctx, long long o) {
+    const long long hi = head_items(a, ctx, BS);
+    const long long hc = hi + (long long)a.q_tiles * a.unit_cost;
+    const long long h = div_nn(o, hc);
+    long long o2 = o - h * hc, before = 0;  // o2 < hc: some tile holds it
+    ItemPos p;
+    p.h = static_cast<int>(h);
+    TileSteps ts(a);
+#pragma unroll 1
+    for (int t = 0;; ++t) {
+        const int jlo = tok_first_block(a, ctx, ts.first(), BS);
+        const long long n = tok_end_block(a, ctx, ts.last(), BS) - jlo;
+        if (o2 < n + a.unit_cost || t + 1 >= a.q_tiles) {
+            const long long k = o2 > a.unit_cost ? o2 - a.unit_cost : 0;
+            p.item = h * hi + before + k;
+            p.t = t;
+            p.j = jlo + static_cast<int>(k);
+            return p;
+        }
+        o2 -= n + a.unit_cost;
+        before += n;
+        ts.next();
+    }
 }
 
 // The partition weighs a unit as its blocks plus a.unit_cost: the fixed work
 // of a unit (query load, cross-warp combine, output) in block equivalents.
 // Without it a CTA whose slice covers many short sequences does many units'
-// fixed work for the same bytes and finishes last.
-__device__ __forceinline__ long long seq_cost(const AttnArgs& a, int ctx, int bs) {
-    if (ctx == 0) return 0;
-    return (head_items(a, ctx, bs) + (long long)a.q_tiles * a.unit_cost) * a.n_kv;
-}
-
-// Block item (within the sequence) at cost offset o of a sequence: a position
-// inside a unit's fixed-cost prefix maps to the unit's first block.  The map
-// is non-decreasing, so consecutive CTAs' slices meet exactly.
-template <int BS>
-__device__ __forceinline__ long long cost_to_item(const AttnArgs& a, int ctx, long long o) {
-    const long long hi = head_items(a, ctx, BS);
-    const long long hc = hi + (long long)a.q_tiles * a.unit_cost;
-    const long long h = o / hc;
-    long long o2 = o % hc, before = 0;
-    for (int t = 0; t < a.q_tiles; ++t) {
-        const long long n = unit_end_block(a, ctx, t, BS) - unit_first_block(a, ctx, t, BS);
-        if (o2 < n + a.unit_cost)
-            return h * hi + before + (o2 > a.unit_cost ? o2 - a.unit_cost : 0);
-        o2 -= n + a.unit_cost;
-        before += n;
-    }
-    return h * hi + before;
-}
-
+// fixed work for the same bytes and finishes last.  A sequence with context
+// ctx costs (head_items + q_tiles * unit_cost) * n_kv, nothing when empty.
+//
 // All threads: this CTA's slice of the flat (unit, block) list -- cost range
 // [c*C/grid, (c+1)*C/grid) mapped to block items -- as the walk position of
-// its first item.  s_pos: {seq, cost offset, item base} of the start and of
-// the end boundary.
+// its first item.  Each thread takes kSliceSeqs consecutive sequences per
+// round, so one round (one load of the context lengths, one scan) covers
+// batches of up to kThreads * kSliceSeqs sequences; the thread whose
+// sequences hold the slice's first (last) cost position computes its walk
+// and publishes it.  s_pos: {start found, item0, end found, item1}.
+// This code runs once per launch, so its cost is mostly instruction fetch
+// of cold code: it is kept small (no unrolling; one sequence per thread per
+// round), which measured several times faster than unrolled variants.
+constexpr int kSliceSeqs = 1;
+
 template <int BS>
 __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
-                                           long long* s_pos) {
+                                           long long* s_pos, Walk* s_walk) {
     const int tid = threadIdx.x, cta = blockIdx.x, grid = gridDim.x;
-    long long mine_c = 0, mine_r = 0;
-    for (int s = tid; s < a.num_seqs; s += kThreads) {
-        const int ctx = unit_ctx(a, s, BS);
-        mine_c += seq_cost(a, ctx, BS);
-        mine_r += head_items(a, ctx, BS) * a.n_kv;
-    }
-    long long total_c, total_r;
-    (void)block_inclusive_scan(mine_c, s_red, total_c);
-    (void)block_inclusive_scan(mine_r, s_red, total_r);
-    const long long start = (total_c * cta) / grid;
-    const long long end = (total_c * (cta + 1)) / grid;
-    const bool end_inside = end < total_c;
-    if (start < end) {
-        long long base_c = 0, base_r = 0;
-        for (int s0 = 0; s0 < a.num_seqs; s0 += kThreads) {
-            const int s = s0 + tid;
-            const int ctx = s < a.num_seqs ? unit_ctx(a, s, BS) : 0;
-            const long long vc = s < a.num_seqs ? seq_cost(a, ctx, BS) : 0;
-            const long long vr = s < a.num_seqs ? head_items(a, ctx, BS) * a.n_kv : 0;
-            long long chunk_c, chunk_r;
-            const long long incl_c = block_inclusive_scan(vc, s_red, chunk_c);
-            const long long incl_r = block_inclusive_scan(vr, s_red, chunk_r);
-            const long long excl_c = base_c + incl_c - vc, excl_r = base_r + incl_r - vr;
-            if (vc > 0 && excl_c <= start && start < excl_c + vc) {
-                s_pos[0] = s;
-                s_pos[1] = start - excl_c;
-                s_pos[2] = excl_r;
-            }
-            if (end_inside && vc > 0 && excl_c <= end && end < excl_c + vc) {
-                s_pos[3] = s;
-                s_pos[4] = end - excl_c;
-                s_pos[5] = excl_r;
-            }
-            base_c += chunk_c;
-            base_r += chunk_r;
-            __syncthreads();
-            if (s_pos[0] >= 0 && (!end_inside || s_pos[3] >= 0)) break;
+    constexpr int kRound = kThreads * kSliceSeqs;
+    long long total_c = 0, total_r = 0;
+    if (a.num_seqs > kRound) {  // several rounds: totals first
+        long long mc = 0, mr = 0;
+        for (int s = tid; s < a.num_seqs; s += kThreads) {
+            const int ctx = unit_ctx(a, s, BS);
+            const long long hi = head_items(a, ctx, BS);
+            mc += ctx > 0 ? (hi + (long long)a.q_tiles * a.unit_cost) * a.n_kv : 0;
+            mr += hi * a.n_kv;
         }
+        block_inclusive_scan2(mc, mr, s_red, total_c, total_r);
     }
-    __syncthreads();
+    long long start = 0, end = 0, base_c = 0, base_r = 0;
+    for (int s0 = 0; s0 < a.num_seqs; s0 += kRound) {
+        const int sb = s0 + tid * kSliceSeqs;
+        int ctx[kSliceSeqs];
+        long long vc[kSliceSeqs], vr[kSliceSeqs], ic = 0, ir = 0;
+#pragma unroll
+        for (int k = 0; k < kSliceSeqs; ++k) ctx[k] = sb + k < a.num_seqs ? unit_ctx(a, sb + k, BS) : 0;
+#pragma unroll
+        for (int k = 0; k < kSliceSeqs; ++k) {
+            const long long hi = head_items(a, ctx[k], BS);
+            vc[k] = ctx[k] > 0 ? (hi + (long long)a.q_tiles * a.unit_cost) * a.n_kv : 0;
+            vr[k] = hi * a.n_kv;
+            ic += vc[k];
+            ir += vr[k];
+        }
+        const long long lc = ic, lr = ir;
+        long long rc, rr;
+        block_inclusive_scan2(ic, ir, s_red, rc, rr);
+        if (a.num_seqs <= kRound) {
+            total_c = rc;
+            total_r = rr;
+        }
+        start = div_nn(total_c * cta, grid);
+        end = div_nn(total_c * (cta + 1), grid);
+        if (start >= end) break;  // (uniform) an empty slice
+        long long ec = base_c + ic - lc, er = base_r + ir - lr;
+#pragma unroll
+        for (int k = 0; k < kSliceSeqs; ++k) {
+            if (vc[k] > 0 && ec <= start && start < ec + vc[k]) {
+                const ItemPos p = cost_to_item<BS>(a, ctx[k], start - ec);
+                Walk w;
+                w.s = sb + k;
+                w.ctx = ctx[k];
+                w.h = p.h;
+                w.t = p.t;
+                walk_set_unit<BS>(a, w);
+                w.j = p.j;
+                w.left = 0;
+                *s_walk = w;
+                s_pos[1] = er + p.item;
+                s_pos[0] = 1;
+            }
+            if (end < total_c && vc[k] > 0 && ec <= end && end < ec + vc[k]) {
+                s_pos[3] = er + cost_to_item<BS>(a, ctx[k], end - ec).item;
+                s_pos[2] = 1;
+            }
+            ec += vc[k];
+            er += vr[k];
+        }
+        base_c += rc;
+        base_r += rr;
+        __syncthreads();
+        if (s_pos[0] >= 0 && (end >= total_c || s_pos[2] >= 0)) break;
+    }
+    __syncthreads();  // (also publishes the barrier init when no round ran)
     Walk w;
-    long long item0 = 0, item1 = 0;
-    if (start < end && s_pos[0] >= 0 && (!end_inside || s_pos[3] >= 0)) {
-        item0 = s_pos[2] + cost_to_item<BS>(a, unit_ctx(a, static_cast<int>(s_pos[0]), BS), s_pos[1]);
-        item1 = end_inside ? s_pos[5] + cost_to_item<BS>(
-                                            a, unit_ctx(a, static_cast<int>(s_pos[3]), BS), s_pos[4])
-                           : total_r;
+    w.left = 0;
+    if (start < end && s_pos[0] >= 0 && (end >= total_c || s_pos[2] >= 0)) {
+        w = *s_walk;
+        w.left = (end < total_c ? s_pos[3] : total_r) - s_pos[1];
     }
-    w.left = item1 - item0;
-    if (w.left > 0) {
-        w.s = static_cast<int>(s_pos[0]);
-        w.ctx = unit_ctx(a, w.s, BS);
-        const long long off = item0 - s_pos[2];  // items into the sequence
-        const long long per_head = head_items(a, w.ctx, BS);
-        w.h = static_cast<int>(off / per_head);
-        long long rem = off % per_head;
-        w.t = 0;
-        walk_set_unit<BS>(a, w);
-        while (rem >= w.nb - w.jlo) {  // the tile holding the slice's first item
-            rem -= w.nb - w.jlo;
-            ++w.t;
-            walk_set_unit<BS>(a, w);
-        }
-        w.j = w.jlo + static_cast<int>(rem);
-    } else {
+    if (w.left <= 0) {
         w.left = 0;
         w.s = w.h = w.t = w.j = w.jlo = w.nb = w.ctx = 0;
     }
@@ -1503,8 +1594,18 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             }
         } else {
             // ===================== softmax (thread = row) =====================
-            float m_used = -INFINITY, l = 0.f;
-            const float sl2 = KV8 ? a.scale_log2 * __ldg(a.k_scale + h) : a.scale_log2;
+            // Scores stay raw: the row's extreme is taken over raw scores and
+            // the exponent of a key is (S - S_ext) * sl2, so the extreme key
+            // itself weighs exactly 1.  Over a negative scale the largest
+            // scaled score is the smallest raw one; a zero scale makes every
+            // visible score 0 (S is replaced by 0 and scaled by 1).  m_used is
+            // the scaled running max, mr_used the raw score it came from.
+            float m_used = -INFINITY, mr_used = 0.f, l = 0.f;
+            const float sl2_in = KV8 ? a.scale_log2 * __ldg(a.k_scale + h) : a.scale_log2;
+            const bool zero_scale = sl2_in == 0.f;
+            const float sl2 = zero_scale ? 1.f : sl2_in;
+            const bool neg = sl2 < 0.f;
+            const float hidden = neg ? INFINITY : -INFINITY;  // a masked raw score
             const int lim_min = ctx - a.q_len + tile_first_token(a, w.t);
             const int lo_max =
                 a.window > 0 ? ctx - a.q_len + tile_last_token(a, w.t) - a.window + 1 : INT_MIN;
@@ -1516,28 +1617,49 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 tc_fence_after();
                 float x[kKeys];
                 {
-                    uint32_t sr[32];
+                    uint32_t s0[32], s1[32];
+                    tmem_ld32(tlane + kColS + (sq & 1u) * kKeys, s0);
+                    tmem_ld32(tlane + kColS + (sq & 1u) * kKeys + 32, s1);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int h2 = 0; h2 < kKeys / 32; ++h2) {
-                        tmem_ld32(tlane + kColS + (sq & 1u) * kKeys + h2 * 32, sr);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            x[h2 * 32 + c] = __uint_as_float(sr[c]) * sl2;
+                    for (int c = 0; c < 32; ++c) {
+                        x[c] = __uint_as_float(s0[c]);
+                        x[32 + c] = __uint_as_float(s1[c]);
                     }
                     tc_fence_before();
                     mbar_arrive(&s_free[sq & 1u]);  // S buffer may take the super-block after next
                 }
+                if (zero_scale) {
+#pragma unroll
+                    for (int c = 0; c < kKeys; ++c) x[c] = 0.f;
+                }
                 const int tok0 = (j0 + q * SB) * BS;  // first key of the super-block
                 const int nkeys = nb * BS;            // columns past it hold stale scores
-                float mloc = -INFINITY;
                 if (nkeys < kKeys || tok0 + kKeys - 1 > lim_min || tok0 < lo_max) {
 #pragma unroll
                     for (int c = 0; c < kKeys; ++c)
-                        if (c >= nkeys || tok0 + c > lim || tok0 + c < lo) x[c] = -INFINITY;
+                        if (c >= nkeys || tok0 + c > lim || tok0 + c < lo) x[c] = hidden;
                 }
+                // The row's extreme raw score: a tree of three-input max (min).
+                float t[22];
+                if (!neg) {
 #pragma unroll
-                for (int c = 0; c < kKeys; ++c) mloc = fmaxf(mloc, x[c]);
+                    for (int i = 0; i < 21; ++i) t[i] = max3f(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+                    t[21] = x[63];
+#pragma unroll
+                    for (int i = 0; i < 7; ++i) t[i] = max3f(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+                    t[0] = max3f(max3f(t[0], t[1], t[2]), max3f(t[3], t[4], t[5]),
+                                 max3f(t[6], t[21], t[21]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 21; ++i) t[i] = min3f(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+                    t[21] = x[63];
+#pragma unroll
+                    for (int i = 0; i < 7; ++i) t[i] = min3f(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+                    t[0] = min3f(min3f(t[0], t[1], t[2]), min3f(t[3], t[4], t[5]),
+                                 min3f(t[6], t[21], t[21]));
+                }
+                const float mloc = t[0] == hidden ? -INFINITY : t[0] * sl2;
                 // This P buffer was last read by the PV of super-block q - 2.
                 if (q > 1) {
                     ok = consumer_wait(a, &pv_done[sq & 1u], ((sq - 2) >> 1) & 1u, ok, s_abort);
@@ -1553,8 +1675,15 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         if (!ok) continue;
                         tc_fence_after();
                     }
-                    const float m_new = grow ? mloc : m_used;
-                    const float alpha = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
+                    // alpha rescales weights taken against the old raw extreme
+                    // to the new one, in the same arithmetic as the weights.
+                    const float alpha = m_used == -INFINITY ? 0.f
+                                        : grow             ? fast_exp2((mr_used - t[0]) * sl2)
+                                                           : 1.f;
+                    if (grow) {
+                        m_used = mloc;
+                        mr_used = t[0];
+                    }
                     l *= alpha;
                     if (q > 0) {
 #pragma unroll 1
@@ -1569,27 +1698,42 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         }
                         tmem_wait_st();
                     }
-                    m_used = m_new;
                 }
+                // With m_used = -inf every score of the row is masked (hidden
+                // scales to -inf): the offset mr_used = 0 gives p = 0 for all.
                 uint32_t ph[kKeys / 2], pl[kKeys / 2];
-                float rs = 0.f;
+                float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
-                for (int c = 0; c < kKeys; c += 2) {
-                    const float p0 = m_used == -INFINITY ? 0.f : fast_exp2(x[c] - m_used);
-                    const float p1 = m_used == -INFINITY ? 0.f : fast_exp2(x[c + 1] - m_used);
-                    rs += p0 + p1;
+                for (int c = 0; c < kKeys; c += 4) {
+                    const float p0 = fast_exp2((x[c] - mr_used) * sl2);
+                    const float p1 = fast_exp2((x[c + 1] - mr_used) * sl2);
+                    const float p2 = fast_exp2((x[c + 2] - mr_used) * sl2);
+                    const float p3 = fast_exp2((x[c + 3] - mr_used) * sl2);
+                    rs0 += p0;
+                    rs1 += p1;
+                    rs2 += p2;
+                    rs3 += p3;
                     if constexpr (KV8) {
                         ph[c / 2] = pack_f16x2(p0, p1);
-                        if (OUT_F32)
+                        ph[c / 2 + 1] = pack_f16x2(p2, p3);
+                        if (OUT_F32) {
                             pl[c / 2] = pack_f16x2(p0 - f16_lo_to_f32(ph[c / 2]),
                                                    p1 - f16_hi_to_f32(ph[c / 2]));
+                            pl[c / 2 + 1] = pack_f16x2(p2 - f16_lo_to_f32(ph[c / 2 + 1]),
+                                                       p3 - f16_hi_to_f32(ph[c / 2 + 1]));
+                        }
                     } else {
                         ph[c / 2] = pack_bf16x2(p0, p1);
-                        if (OUT_F32)
+                        ph[c / 2 + 1] = pack_bf16x2(p2, p3);
+                        if (OUT_F32) {
                             pl[c / 2] = pack_bf16x2(p0 - bf16_lo_to_f32(ph[c / 2]),
                                                     p1 - bf16_hi_to_f32(ph[c / 2]));
+                            pl[c / 2 + 1] = pack_bf16x2(p2 - bf16_lo_to_f32(ph[c / 2 + 1]),
+                                                        p3 - bf16_hi_to_f32(ph[c / 2 + 1]));
+                        }
                     }
                 }
+                const float rs = (rs0 + rs1) + (rs2 + rs3);
                 l += rs;
                 tmem_st32(tlane + kColP + (sq & 1u) * (kKeys / 2), ph);
                 if (OUT_F32) tmem_st32(tlane + kColPL + (sq & 1u) * (kKeys / 2), pl);
@@ -1714,8 +1858,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      C::kScratchBytes);
     uint64_t* empty_bar = full_bar + kStages;
 
-    __shared__ long long s_red[kThreads / 32];
-    __shared__ long long s_pos[6];
+    __shared__ long long s_red[2 * kThreads / 32];
+    __shared__ long long s_pos[4];
+    __shared__ Walk s_walk;
     __shared__ int s_abort;
     // TMEM mode: S ready/read, P ready, PV done (x2 each), 2 teardowns, and over an
     // 8-bit cache f16 copy ready / free (x2 each)
@@ -1741,13 +1886,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_barrier_init();
         s_abort = 0;
-        for (int i = 0; i < 6; ++i) s_pos[i] = -1;
+        for (int i = 0; i < 4; ++i) s_pos[i] = -1;
     }
     if (warp == kConsumerWarps && lane == 0) {
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
-    const Walk w0 = find_slice<BS>(a, s_red, s_pos);  // also publishes the barrier init
+    const Walk w0 = find_slice<BS>(a, s_red, s_pos, &s_walk);  // also publishes the barrier init
     // Let the merge kernel (launched as a programmatic dependent) be scheduled
     // early; it waits for this whole grid before reading anything.
     if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

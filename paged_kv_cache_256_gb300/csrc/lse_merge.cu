@@ -9,14 +9,18 @@
 // in CS336 lecture-10 notes, PagedAttention (vLLM)).  Pieces with l == 0 (no
 // visible key) weigh nothing, and a row whose pieces are all empty is zero.
 //
-// Grid (attention CTAs) x (row groups of 8); one warp per output row.  Block
-// (c, y) looks at the records of attention CTA c: if one of them starts a
-// split unit (the unit's first block, not its last), its warps find the
-// CTAs c+1, c+2, ... holding the unit's other pieces with a lane-parallel
-// ballot over their records and combine rows 8y..8y+7.  Every split unit has
-// exactly one starting piece, so each unit is merged exactly once.  All loads
-// of one row are independent of each other, so a row costs a few memory
-// latencies whatever the number of pieces.
+// Grid (attention CTAs) x (row groups); each warp merges kMergeRowsPerWarp
+// output rows.  Block (c, y) looks at the records of attention CTA c: if one
+// of them starts a split unit (the unit's first block, not its last), its
+// warps find the CTAs c+1, c+2, ... holding the unit's other pieces with a
+// lane-parallel ballot over their records and combine their rows.  Every
+// split unit has exactly one starting piece, so each unit is merged exactly
+// once.  The loads are arranged in as few dependent rounds as possible: the
+// records of CTA c and of the next 32 CTAs together; then every piece's
+// (m, l) (lane k <-> piece k) together with the outputs of the first
+// kMergeChunk pieces; M, the weights and the denominator follow from
+// registers.  Pieces come in groups of 32 and the running combination is
+// rescaled when a later group raises M (the same exact rule).
 //
 // The kernel is launched as a programmatic dependent of the attention kernel:
 // it may start while the attention grid drains and waits (griddepcontrol)
@@ -26,21 +30,59 @@
 
 namespace pkv {
 
-constexpr int kMergeRowsPerBlock = 8;
-constexpr int kMergeThreads = kMergeRowsPerBlock * 32;
+constexpr int kMergeWarps = 8;
+constexpr int kMergeRowsPerWarp = 2;
+constexpr int kMergeRowsPerBlock = kMergeWarps * kMergeRowsPerWarp;
+constexpr int kMergeChunk = 4;  // pieces whose outputs are loaded together
+
+template <int V>
+struct VecF;
+template <>
+struct VecF<4> {
+    __device__ static void load(const float* p, float (&x)[4]) {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        x[0] = v.x;
+        x[1] = v.y;
+        x[2] = v.z;
+        x[3] = v.w;
+    }
+};
+template <>
+struct VecF<2> {
+    __device__ static void load(const float* p, float (&x)[2]) {
+        const float2 v = *reinterpret_cast<const float2*>(p);
+        x[0] = v.x;
+        x[1] = v.y;
+    }
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
 
 template <int D, bool OUT_F32>
-__global__ void __launch_bounds__(kMergeThreads)
+__global__ void __launch_bounds__(kMergeWarps * 32, 4)
     lse_merge_kernel(const AttnArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int V = D / 32;  // consecutive columns per lane
+    constexpr int RW = kMergeRowsPerWarp;
     const int c = blockIdx.x, grid = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.y * kMergeRowsPerBlock + warp;
-    if (r >= a.rows) return;
+    const int r0 = (blockIdx.y * kMergeWarps + warp) * RW;  // this warp's first row
+    if (r0 >= a.rows) return;
 
+    // Round 1: CTA c's records and the first records of CTAs c+1 .. c+32.
     const int4 i1 = a.rec_info[(size_t)c * 2 + 1];
     const int4 i0 = a.rec_info[(size_t)c * 2 + 0];
+    const int cn = c + 1 + lane;
+    const int4 nx = cn < grid ? a.rec_info[(size_t)cn * 2] : make_int4(0, 0, 0, 0);
     int first_rec;
     int4 head;
     if (i1.z & kRecValid) {
@@ -53,18 +95,13 @@ __global__ void __launch_bounds__(kMergeThreads)
         return;
     }
     const int s = head.x, h = head.y, tile = head.w;
-    // Row r of the unit's row tile: query token i, query head hq (padding rows of
-    // a partial last tile have no output).
-    const int R = tile * a.rows + r;
-    if (R >= a.rows_total) return;
 
-    // Pieces: first_rec, then the first record of every non-empty CTA in
-    // (c, c_end].  Find c_end 32 CTAs at a time.
-    int c_end = -1;
-    for (int base = c + 1; base < grid && c_end < 0; base += 32) {
+    // The unit's last piece: the first CTA after c whose first record closes
+    // the unit, with only this unit's pieces or empty CTAs between.
+    int npc = -1;  // the pieces are c (first_rec) and the CTAs c+1 .. c+npc
+    for (int base = c + 1; base < grid && npc < 0; base += 32) {
         const int c2 = base + lane;
-        int4 in = make_int4(0, 0, 0, 0);
-        if (c2 < grid) in = a.rec_info[(size_t)c2 * 2];
+        const int4 in = base == c + 1 ? nx : (c2 < grid ? a.rec_info[(size_t)c2 * 2] : make_int4(0, 0, 0, 0));
         const bool same =
             c2 < grid && (in.z & kRecValid) && in.x == s && in.y == h && in.w == tile;
         const bool cont = same || (c2 < grid && (in.z & kRecEmpty));
@@ -76,88 +113,112 @@ __global__ void __launch_bounds__(kMergeThreads)
                 if (lane == 0) atomicOr(a.err, kErrInternal);
                 return;
             }
-            c_end = base + k;
+            npc = base + k - c;
         }
     }
-    if (c_end < 0) {
+    if (npc < 0) {
         if (lane == 0) atomicOr(a.err, kErrInternal);
         return;
     }
 
-    // Pass 1 (lane k <-> piece k of each group of 32): largest running max and
-    // the weighted denominator.
-    const int npieces = c_end - c + 1;  // candidate slots; empty CTAs weigh 0
-    float M = -INFINITY;
-    for (int k0 = 0; k0 < npieces; k0 += 32) {
-        const int k = k0 + lane;
-        if (k < npieces) {
-            const int rec = k == 0 ? first_rec : (c + k) * 2;
-            const bool live = k == 0 || !(a.rec_info[(size_t)(c + k) * 2].z & kRecEmpty);
-            if (live) {
-                const float2 ml = *reinterpret_cast<const float2*>(a.rec_ml + ((size_t)rec * a.rows + r) * 2);
-                if (ml.y > 0.f) M = fmaxf(M, ml.x);
-            }
-        }
+    float M[RW], den[RW], acc[RW][V];
+#pragma unroll
+    for (int rr = 0; rr < RW; ++rr) {
+        M[rr] = -INFINITY;
+        den[rr] = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[rr][v] = 0.f;
     }
+    // Flags of CTA c + lane (lanes >= 1), from round 1.
+    const int z_near = __shfl_sync(0xffffffffu, nx.z, (lane + 31) & 31);
+    for (int kg = 0; kg <= npc; kg += 32) {
+        // Lane k <-> piece kg + k: its record, or -1 (past the unit, or an
+        // empty CTA whose slots hold nothing of it).
+        const int k = kg + lane;
+        int rec = -1;
+        if (k == 0) {
+            rec = first_rec;
+        } else if (k <= npc) {
+            const int z = kg == 0 ? z_near : a.rec_info[(size_t)(c + k) * 2].z;
+            if (!(z & kRecEmpty)) rec = (c + k) * 2;
+        }
+        const int cnt = min(32, npc + 1 - kg);  // pieces of this group
+        float2 ml[RW];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float mb = M == -INFINITY ? 0.f : M;
-
-    float acc[V];
+        for (int rr = 0; rr < RW; ++rr)
+            ml[rr] = (rec >= 0 && r0 + rr < a.rows)
+                         ? *reinterpret_cast<const float2*>(a.rec_ml + ((size_t)rec * a.rows + r0 + rr) * 2)
+                         : make_float2(-INFINITY, 0.f);
+        for (int q0 = 0; q0 < cnt; q0 += kMergeChunk) {
+            float x[kMergeChunk][RW][V];
+            int live = 0;
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = 0.f;
-    float den = 0.f;
-    for (int k0 = 0; k0 < npieces; k0 += 32) {
-        const int k = k0 + lane;
-        float wk = 0.f, lk = 0.f;
-        if (k < npieces) {
-            const int rec = k == 0 ? first_rec : (c + k) * 2;
-            const bool live = k == 0 || !(a.rec_info[(size_t)(c + k) * 2].z & kRecEmpty);
-            if (live) {
-                const float2 ml = *reinterpret_cast<const float2*>(a.rec_ml + ((size_t)rec * a.rows + r) * 2);
-                if (ml.y > 0.f) {
-                    wk = fast_exp2(ml.x - mb);
-                    lk = ml.y;
+            for (int u = 0; u < kMergeChunk; ++u) {
+                const int q = q0 + u;
+                const int rq = __shfl_sync(0xffffffffu, rec, q & 31);
+                const bool ok = q < cnt && rq >= 0;
+                live |= ok ? 1 << u : 0;
+#pragma unroll
+                for (int rr = 0; rr < RW; ++rr) {
+                    if (ok && r0 + rr < a.rows)
+                        VecF<V>::load(a.rec_o + ((size_t)rq * a.rows + r0 + rr) * D + lane * V, x[u][rr]);
+                    else
+#pragma unroll
+                        for (int v = 0; v < V; ++v) x[u][rr][v] = 0.f;
+                }
+            }
+            float wk[RW];
+#pragma unroll
+            for (int rr = 0; rr < RW; ++rr) {
+                if (q0 == 0) {
+                    // The group's largest running max; pieces with l == 0 weigh nothing.
+                    const float mg = warp_max(ml[rr].y > 0.f ? ml[rr].x : -INFINITY);
+                    if (mg > M[rr]) {
+                        const float f = M[rr] == -INFINITY ? 0.f : fast_exp2(M[rr] - mg);
+                        den[rr] *= f;
+#pragma unroll
+                        for (int v = 0; v < V; ++v) acc[rr][v] *= f;
+                        M[rr] = mg;
+                    }
+                }
+                wk[rr] = ml[rr].y > 0.f ? fast_exp2(ml[rr].x - M[rr]) : 0.f;
+                if (q0 == 0) den[rr] += warp_sum(wk[rr] * ml[rr].y);
+            }
+#pragma unroll
+            for (int u = 0; u < kMergeChunk; ++u) {
+#pragma unroll
+                for (int rr = 0; rr < RW; ++rr) {
+                    const float w = __shfl_sync(0xffffffffu, wk[rr], (q0 + u) & 31);
+                    if ((live >> u & 1) && w != 0.f) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) acc[rr][v] += w * x[u][rr][v];
+                    }
                 }
             }
         }
-        float dpart = wk * lk;
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) dpart += __shfl_xor_sync(0xffffffffu, dpart, off);
-        den += dpart;
-        // Pass 2: every lane accumulates its V columns over the group's pieces.
-        const int cnt = min(32, npieces - k0);
-        for (int q = 0; q < cnt; ++q) {
-            const float wq = __shfl_sync(0xffffffffu, wk, q);
-            if (wq == 0.f) continue;  // uniform across the warp
-            const int kq = k0 + q;
-            const int rec = kq == 0 ? first_rec : (c + kq) * 2;
-            const float* ro = a.rec_o + ((size_t)rec * a.rows + r) * D + lane * V;
-            if (V == 4) {
-                const float4 x = *reinterpret_cast<const float4*>(ro);
-                acc[0] += wq * x.x;
-                acc[1] += wq * x.y;
-                acc[2] += wq * x.z;
-                acc[3] += wq * x.w;
-            } else {
-#pragma unroll
-                for (int v = 0; v < V; ++v) acc[v] += wq * ro[v];
-            }
-        }
     }
 
-    const float inv = den > 0.f ? 1.f / den : 0.f;
     const int G = a.group;
-    const int i = R / G, hq = h * G + R % G;
-    const size_t ob = (((size_t)s * a.q_len + i) * a.n_q + hq) * D + lane * V;
-    if (OUT_F32) {
-        float* op = static_cast<float*>(a.out) + ob;
 #pragma unroll
-        for (int v = 0; v < V; ++v) op[v] = acc[v] * inv;
-    } else {
-        uint32_t* op = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + ob);
+    for (int rr = 0; rr < RW; ++rr) {
+        const int r = r0 + rr;
+        // Row r of the unit's row tile: query token i, query head hq (padding
+        // rows of a partial last tile have no output).
+        const int R = tile * a.rows + r;
+        if (r >= a.rows || R >= a.rows_total) continue;
+        const float inv = den[rr] > 0.f ? 1.f / den[rr] : 0.f;
+        const int i = R / G, hq = h * G + R % G;
+        const size_t ob = (((size_t)s * a.q_len + i) * a.n_q + hq) * D + lane * V;
+        if (OUT_F32) {
+            float* op = static_cast<float*>(a.out) + ob;
 #pragma unroll
-        for (int v = 0; v < V; v += 2) op[v / 2] = pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
+            for (int v = 0; v < V; ++v) op[v] = acc[rr][v] * inv;
+        } else {
+            uint32_t* op = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + ob);
+#pragma unroll
+            for (int v = 0; v < V; v += 2)
+                op[v / 2] = pack_bf16x2(acc[rr][v] * inv, acc[rr][v + 1] * inv);
+        }
     }
 }
 
@@ -165,7 +226,7 @@ template <int D, bool F32>
 static cudaError_t launch_merge_one(const AttnArgs& a, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, (a.rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock, 1);
-    cfg.blockDim = dim3(kMergeThreads, 1, 1);
+    cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

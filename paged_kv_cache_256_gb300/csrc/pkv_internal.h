@@ -23,7 +23,7 @@ struct AttnArgs {
     const int32_t* context_lens;  // [num_seqs]
     void* out;                    // [num_seqs][q_len][n_q][head_dim] bf16 or f32
     unsigned* err;                // workspace error word
-    int4* rec_info;               // [grid][2] {seq, kv head, flags, 0}
+    int4* rec_info;               // [grid][2] {seq, kv head, flags, row tile}
     float* rec_ml;                // [grid][2][rows][2] {m (log2 domain), l}
     float* rec_o;                 // [grid][2][rows][head_dim] unnormalised output
     int num_seqs;

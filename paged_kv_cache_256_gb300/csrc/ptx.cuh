@@ -148,6 +148,19 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Largest / smallest of three (the three-source forms of PTX max.f32 and
+// min.f32, sm_100 and later; a NaN source is ignored as in fmaxf).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` goes to the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

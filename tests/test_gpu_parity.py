@@ -115,6 +115,26 @@ def test_shape_sweep(oracle, case, grid):
         assert_close(out_to_host(out), ref, kind, f"sweep {case} grid {grid} {kind}")
 
 
+@pytest.mark.parametrize("num_seqs", [288, 289, 700, 3000])
+@pytest.mark.parametrize("grid", [0, 7, 300])
+def test_large_batches(oracle, num_seqs, grid):
+    """Batches of many short sequences, some empty: the work partition scans
+    the context lengths one sequence per thread (288 per round), so these
+    sizes cover an exact round and several rounds."""
+    rng = np.random.default_rng(num_seqs)
+    ctxs = rng.integers(1, 80, num_seqs)
+    ctxs[rng.random(num_seqs) < 0.1] = 0
+    wl = make_custom(num_seqs=num_seqs, q_len=1, n_q=8, n_kv=2, head_dim=64, block_size=16,
+                     context_lens=[int(c) for c in ctxs], seed=11 + num_seqs)
+    dw = to_device(wl)
+    pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache)
+    _, _, ref = oracle_after_append(oracle, wl)
+    flags = pkv.PKV_FLAG_GRID(grid) if grid else 0
+    for kind in ("bf16", "f32"):
+        out = run_attn(dw, wl, kind, flags=flags)
+        assert_close(out_to_host(out), ref, kind, f"{num_seqs} seqs grid {grid} {kind}")
+
+
 def test_block_relabelling_is_bit_identical():
     """Moving physical blocks (and rewriting the table) leaves the output bit-identical."""
     import torch
