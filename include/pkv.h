@@ -101,9 +101,10 @@ typedef enum pkv_status {
  *   speculative-verify step, or a whole prompt chunk (paged / chunked
  *   prefill: the prompt pass before decoding, "Efficient inference", Two
  *   phases, two bottlenecks; chunked prefill is named among the scheduling
- *   techniques in "Transformer inference mechanics", A better connection map).  The rows = (n_q / n_kv) * q_len query rows that share a KV head
- *   are processed in tiles of 128; each tile reads only the blocks its rows
- *   can see.
+ *   techniques in "Transformer inference mechanics", A better connection
+ *   map).  The rows = (n_q / n_kv) * q_len query rows that share a KV head
+ *   are processed in tiles of at most 128 (whole query tokens when one
+ *   token's heads fit); each tile reads only the blocks its rows can see.
  * Supported: head_dim in {64, 128}; block_size in {16, 32}; q_len <= 65536;
  *   rows <= 2^24; num_blocks * n_kv * block_size < 2^31.
  * Rows that see no key (context_lens[b] == 0, or < q_len) are written as zeros.

@@ -497,8 +497,13 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
 // stages (the last may be partial), counted from the piece's first block.
 // Lanes 0..kIssueLanes-1 fill consecutive stages side by side: one serial
 // wait/issue chain per stage would cap the stream.
+// ORDERED (the tensor-memory consumer, which frees stages strictly in order):
+// stages are refilled one at a time in order, each stage's TMA boxes spread
+// over the lanes, so a freed stage is refilled at once instead of waiting for
+// the stages issued beside it, and the first stages of a launch land first
+// instead of together.
 template <int D, int BS, int kStages, int kStageBytes, int kTileBytes, int kBoxBytes, int kBoxes,
-          int kBoxCols, int kRegion, int SBS, bool KV8>
+          int kBoxCols, int kRegion, int SBS, bool KV8, bool ORDERED>
 __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tmap_k,
                                         const CUtensorMap* tmap_v, Walk w, uint8_t* stages,
                                         uint64_t* full_bar, uint64_t* empty_bar,
@@ -523,7 +528,53 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                 my = -1;  // read as an out-of-bounds (zero-filled) tile
             }
             if (*s_abort) ok = false;  // a consumer gave up
-            for (int k0 = 0; k0 < ns && ok; k0 += kIssueLanes) {
+            if constexpr (ORDERED) {
+                // boxes per block: K and V halves (bf16), or one K+V box (8-bit)
+                constexpr int kBpb = KV8 ? 1 : 2 * kBoxes;
+                static_assert(SBS * kBpb <= 32, "one box per lane");
+                for (int k = 0; k < ns && ok; ++k) {
+                    const int nb = min(SBS, n - k * SBS);
+                    const int blk = __shfl_sync(0xffffffffu, my, (k * SBS + lane / kBpb) & 31);
+                    const uint32_t stage = gidx % kStages;
+                    bool good = true;
+                    if (lane == 0) {
+                        good = mbar_wait_bounded(&empty_bar[stage], ((gidx / kStages) & 1u) ^ 1u);
+                        if (good) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes);
+                    }
+                    good = __shfl_sync(0xffffffffu, good, 0);
+                    __syncwarp();
+                    if (!good) {
+                        ok = false;
+                        if (lane == 0) {
+                            atomicOr(a.err, kErrTimeout);
+                            *s_abort = 1;
+                        }
+                        break;
+                    }
+                    if (lane < nb * kBpb) {
+                        const int b = lane / kBpb, box = lane % kBpb;
+                        const long long y64 = ((long long)blk * a.n_kv + w.h) * a.kv_mul * BS;
+                        const bool oob = blk < 0 || y64 >= a.tile_rows_total;
+                        const int yk = oob ? a.tile_rows_total : static_cast<int>(y64);
+                        if constexpr (KV8) {
+                            tma_load_2d(stages + stage * kStageBytes + b * 2 * kBoxBytes, tmap_k,
+                                        0, yk, &full_bar[stage], policy);
+                        } else {
+                            // box: K half (box < kBoxes), then V half
+                            const int half = box % kBoxes;
+                            const bool isv = box >= kBoxes;
+                            const int yv = oob ? a.tile_rows_total : yk + a.v_row_off;
+                            tma_load_2d(stages + stage * kStageBytes + b * kBoxBytes +
+                                            (isv ? kBoxes + half : half) * kRegion,
+                                        isv ? tmap_v : tmap_k, half * kBoxCols, isv ? yv : yk,
+                                        &full_bar[stage], policy);
+                        }
+                    }
+                    ++gidx;
+                    issued = gidx;
+                }
+            }
+            for (int k0 = 0; !ORDERED && k0 < ns && ok; k0 += kIssueLanes) {
                 const int sk = k0 + lane;  // this lane's stage within the batch
                 const bool act = lane < kIssueLanes && sk < ns;
                 const int nb = SBS == 1 ? 1 : (act ? min(SBS, n - sk * SBS) : 0);
@@ -1384,12 +1435,27 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 // with Q and P in f16 (every e4m3 value is exact in f16), and the PV product
 // frees the copy.  The per-head K scale joins the score scale, the V scale
 // the normalisation.
+// The query tile of unit (sequence s, KV head h, row tile t) by TMA (query
+// map present): D/64 boxes of 64 columns x a.rows rows, landing as the
+// swizzled K-major tile the score MMA reads; completes on `bar`.  Rows of a
+// partial tile past a.rows keep stale bits; their scores are all masked.
+template <int D>
+__device__ __forceinline__ void issue_q_tile(const AttnArgs& a, const CUtensorMap* tmap_q,
+                                             uint8_t* qtile, uint64_t* bar, int s, int h, int t) {
+    const int r0 = t * a.rows;
+    const int y = h * a.group + r0 % a.group, z = s * a.q_len + r0 / a.group;
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(D / 64) * 128u * static_cast<uint32_t>(a.rows));
+#pragma unroll
+    for (int half = 0; half < D / 64; ++half)
+        tma_load_3d(qtile + half * 128 * 128, tmap_q, half * 64, y, z, bar);
+}
+
 template <int D, int BS, bool OUT_F32, bool KV8>
 __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t* stages,
-                                             uint8_t* qtile, uint64_t* full_bar,
-                                             uint64_t* empty_bar, uint64_t* tcb,
-                                             uint32_t* s_tmem, volatile int* s_abort,
-                                             int4& info0, int4& info1) {
+                                             uint8_t* qtile, const CUtensorMap* tmap_q,
+                                             uint64_t* full_bar, uint64_t* empty_bar,
+                                             uint64_t* tcb, uint32_t* s_tmem,
+                                             volatile int* s_abort, int4& info0, int4& info1) {
     using C = AttnCfg<D, BS, kModeTmem, KV8>;
     constexpr int kStages = C::kStages;
     constexpr int kKeys = 64;                  // keys per softmax round
@@ -1402,13 +1468,16 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     constexpr int kParty = KV8 ? 256 : 192;  // warps 0..5 take part (0..7 with converters)
     constexpr int kHalves = D / 64;          // 64-column regions of an f16 K or V copy
     // tcb: [0..1] S ready, [2..3] S read, [4..5] P ready, [6..7] PV done, [8] QK teardown,
-    //      [9] PV teardown
+    //      [9] PV teardown, [10..13] f16 copies, [14] Q landed, [15] Q read, [16] Q widened
     uint64_t* s_full = tcb;
     uint64_t* s_free = tcb + 2;
     uint64_t* p_full = tcb + 4;
     uint64_t* pv_done = tcb + 6;
     uint64_t* cvt_full = tcb + 10;  // 8-bit cache: f16 copy [g&1] ready
     uint64_t* cvt_free = tcb + 12;  // 8-bit cache: f16 copy [g&1] read by its PV product
+    uint64_t* q_full = tcb + 14;    // query tile landed (TMA)
+    uint64_t* q_empty = tcb + 15;   // the piece's score products have read the query tile
+    uint64_t* q_conv = tcb + 16;    // 8-bit cache: the query tile widened to f16
     // f16 copies (8-bit cache): copy c at cvt + c * kCopy, K regions then V regions
     uint8_t* cvt = qtile + C::kQTileBytes;
     constexpr int kCopy = 2 * kHalves * C::kCvtRegion;
@@ -1437,6 +1506,10 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     uint32_t gbase = 0;  // sequence number (in this CTA) of the piece's first stage
     bool ok = true;
     int piece = 0;
+    // QK issuer: a query-tile TMA not yet seen to land (the first was issued
+    // before the consumers started).
+    bool q_pending = a.q_tma && w.left > 0;
+    uint32_t q_pending_par = 0;
     while (w.left > 0) {
         const int j0 = w.j, j1 = piece_end(w), n = j1 - j0;
         const int nsb = (n + SB - 1) / SB;
@@ -1444,12 +1517,34 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         int lim = -1, lo = INT_MIN, i_row = 0, hq_row = 0;
         bool row_ok = false;
         if (softmax) {
+            row_ok = unit_row(a, w.t, h, row, i_row, hq_row);
+            lim = row_ok ? ctx - a.q_len + i_row : -1;
+            if (a.window > 0) lo = lim - a.window + 1;
+        }
+        if (softmax && a.q_tma) {
+            if constexpr (KV8) {
+                // The TMA tile is bf16; the f16 MMAs want f16: each thread widens
+                // its own row in place.  Every thread arrives, so the issuer's
+                // wait ends (and reports) even after a timeout here.
+                const bool good = consumer_wait(a, q_full, piece & 1, ok, s_abort);
+                if (good) {
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) {
+                        uint4* pq = reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + row * 128 +
+                                                             (((c & 7) ^ (row & 7)) << 4));
+                        const uint4 v = *pq;
+                        *pq = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
+                                         bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+                    }
+                    fence_proxy_async_smem();
+                }
+                ok = good;
+                mbar_arrive(q_conv);
+            }
+        } else if (softmax) {
             // This unit's query rows into the swizzled Q tile (the previous
             // unit's score products finished: each of them was waited for).
-            row_ok = unit_row(a, w.t, h, row, i_row, hq_row);
             const bool valid = row_ok;
-            lim = valid ? ctx - a.q_len + i_row : -1;
-            if (a.window > 0) lo = lim - a.window + 1;
             const uint4* qrow = reinterpret_cast<const uint4*>(
                 a.q + (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D);
             uint4 qv[D / 8];
@@ -1466,12 +1561,30 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                                           (((c & 7) ^ (row & 7)) << 4)) = qv[c];
             fence_proxy_async_smem();
         }
-        tc_fence_before();
-        named_barrier_sync(2, kParty);  // Q tile ready; the previous unit's O has been read
-        tc_fence_after();
+        if (!a.q_tma) {
+            tc_fence_before();
+            named_barrier_sync(2, kParty);  // Q tile ready; the previous unit's O has been read
+            tc_fence_after();
+        }
+        // (With TMA query tiles the roles need no barrier per piece: the issuer
+        // waits for the tile, and the first PV product of a piece, which
+        // overwrites O, waits for P of its first super-block, which the
+        // softmax threads write only after reading the previous O.)
 
         if (warp == 4) {
             // ===================== QK issuer =====================
+            if (lane == 0 && ok && a.q_tma) {
+                // This piece's query tile: landed, and over an 8-bit cache
+                // widened (the copy is waited for itself, so that a tile still
+                // in flight after a failed widening is waited for at teardown).
+                if (*s_abort || !mbar_wait_bounded(q_full, piece & 1)) {
+                    issuer_fail(ok);
+                } else {
+                    q_pending = false;
+                    if (KV8 && !mbar_wait_bounded(q_conv, piece & 1)) issuer_fail(ok);
+                }
+                tc_fence_after();
+            }
             if (lane == 0 && ok) {
                 for (int q = 0; q < nsb; ++q) {
                     const uint32_t g = gbase + q, st = g % kStages;
@@ -1502,6 +1615,23 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&s_full[g & 1u]);
+                }
+            }
+            if (lane == 0 && ok && a.q_tma) {
+                // The next piece's query tile, once this piece's score
+                // products have read this one.
+                Walk wn = w;
+                wn.left -= j1 - w.j;
+                if (wn.left > 0) walk_next_unit<BS>(a, wn);
+                if (wn.left > 0) {
+                    umma_commit(q_empty);
+                    if (!mbar_wait_bounded(q_empty, piece & 1)) {
+                        issuer_fail(ok);
+                    } else {
+                        issue_q_tile<D>(a, tmap_q, qtile, q_full, wn.s, wn.h, wn.t);
+                        q_pending = true;
+                        q_pending_par = (piece + 1) & 1;
+                    }
                 }
             }
             __syncwarp();
@@ -1829,11 +1959,13 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         w.left -= j1 - w.j;
         if (w.left > 0) walk_next_unit<BS>(a, w);
     }
-    // Teardown: no tensor-core operation may still be running when TMEM is freed.
+    // Teardown: no tensor-core operation may still be running when TMEM is
+    // freed, and no query-tile copy may still be landing.
     if ((warp == 4 || warp == 5) && lane == 0) {
         uint64_t* bar = &tcb[warp == 4 ? 8 : 9];
         umma_commit(bar);
         (void)mbar_wait_bounded(bar, 0u);
+        if (warp == 4 && q_pending) (void)mbar_wait_bounded(q_full, q_pending_par);
     }
     tc_fence_before();
     named_barrier_sync(2, kParty);
@@ -1845,7 +1977,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
 template <int D, int BS, bool OUT_F32, int MODE, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_decode_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                             const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
+                             const __grid_constant__ CUtensorMap tmap_v,
+                             const __grid_constant__ CUtensorMap tmap_q, const AttnArgs a) {
     using C = AttnCfg<D, BS, MODE, KV8>;
     constexpr int kStages = C::kStages;
 
@@ -1862,9 +1995,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ long long s_pos[4];
     __shared__ Walk s_walk;
     __shared__ int s_abort;
-    // TMEM mode: S ready/read, P ready, PV done (x2 each), 2 teardowns, and over an
-    // 8-bit cache f16 copy ready / free (x2 each)
-    __shared__ uint64_t s_tcb[14];
+    // TMEM mode: S ready/read, P ready, PV done (x2 each), 2 teardowns, over an
+    // 8-bit cache f16 copy ready / free (x2 each), query tile landed / read /
+    // widened
+    __shared__ uint64_t s_tcb[17];
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1879,10 +2013,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (MODE == kModeTmem) {
             // S ready (a commit), S read (128 rows), P ready (128 rows),
-            // PV done (a commit), two issuer teardowns (a commit each)
-            const uint32_t counts[14] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1, KV8 ? 2u : 1u,
-                                         KV8 ? 2u : 1u, 1, 1};
-            for (int i = 0; i < 14; ++i) mbar_init(&s_tcb[i], counts[i]);
+            // PV done (a commit), two issuer teardowns (a commit each), f16
+            // copy ready (two converter warps) / free (a commit), query tile
+            // landed (the TMA) / read (a commit) / widened (128 rows)
+            const uint32_t counts[17] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1, KV8 ? 2u : 1u,
+                                         KV8 ? 2u : 1u, 1, 1, 1, 1, 128};
+            for (int i = 0; i < 17; ++i) mbar_init(&s_tcb[i], counts[i]);
         }
         fence_barrier_init();
         s_abort = 0;
@@ -1897,9 +2033,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // early; it waits for this whole grid before reading anything.
     if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    // Tensor-memory consumer with TMA query tiles: the first tile is issued
+    // before the producer's first stage, so it is not queued behind the ring fill.
+    if constexpr (MODE == kModeTmem) {
+        if (a.q_tma) {
+            if (warp == 4) {
+                if (lane == 0 && w0.left > 0)
+                    issue_q_tile<D>(a, &tmap_q, reinterpret_cast<uint8_t*>(scratch), &s_tcb[14],
+                                    w0.s, w0.h, w0.t);
+                __syncwarp();
+                named_barrier_arrive(3, 64);
+            } else if (warp == kConsumerWarps) {
+                named_barrier_sync(3, 64);
+            }
+        }
+    }
     if (warp == kConsumerWarps) {
         produce<D, BS, kStages, C::kStageBytes, C::kTileBytes, C::kBoxBytes, C::kBoxes,
-                C::kBoxCols, C::kRegion, C::kBlocksPerStage, KV8>(
+                C::kBoxCols, C::kRegion, C::kBlocksPerStage, KV8, MODE == kModeTmem>(
             a, &tmap_k, &tmap_v, w0, stages, full_bar, empty_bar, &s_abort);
         return;
     }
@@ -1932,8 +2083,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           info0, info1);
     else
         consume_tmem<D, BS, OUT_F32, KV8>(a, w0, stages, reinterpret_cast<uint8_t*>(scratch),
-                                          full_bar, empty_bar, s_tcb, &s_tmem, &s_abort, info0,
-                                          info1);
+                                          &tmap_q, full_bar, empty_bar, s_tcb, &s_tmem, &s_abort,
+                                          info0, info1);
     if (tid == 0) {
         a.rec_info[(size_t)blockIdx.x * 2 + 0] = info0;
         a.rec_info[(size_t)blockIdx.x * 2 + 1] = info1;
@@ -1943,7 +2094,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 template <int D, int BS, bool F32, int MODE, bool KV8>
 static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                              int grid, cudaStream_t stream) {
+                              const CUtensorMap& tq, int grid, cudaStream_t stream) {
     auto kern = paged_decode_attn_kernel<D, BS, F32, MODE, KV8>;
     const int smem = AttnCfg<D, BS, MODE, KV8>::kSmemBytes;
     // The shared-memory opt-in is set once per device for each instantiation.
@@ -1957,36 +2108,38 @@ static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CU
         if (e != cudaSuccess) return e;
         opted_in.fetch_or(bit, std::memory_order_release);
     }
-    kern<<<grid, kThreads, smem, stream>>>(tk, tv, a);
+    kern<<<grid, kThreads, smem, stream>>>(tk, tv, tq, a);
     return cudaGetLastError();
 }
 
 // Consumer by rows per KV head: narrow (<= 8), wide, TMEM (> 64).
 template <int D, int BS, bool KV8>
 static cudaError_t launch_shape(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                                bool out_f32, int grid, cudaStream_t stream) {
+                                const CUtensorMap& tq, bool out_f32, int grid,
+                                cudaStream_t stream) {
     if (a.rows <= kNarrowRows)
-        return out_f32 ? launch_one<D, BS, true, kModeNarrow, KV8>(a, tk, tv, grid, stream)
-                       : launch_one<D, BS, false, kModeNarrow, KV8>(a, tk, tv, grid, stream);
+        return out_f32 ? launch_one<D, BS, true, kModeNarrow, KV8>(a, tk, tv, tq, grid, stream)
+                       : launch_one<D, BS, false, kModeNarrow, KV8>(a, tk, tv, tq, grid, stream);
     if (a.rows > kTmemMinRows)
-        return out_f32 ? launch_one<D, BS, true, kModeTmem, KV8>(a, tk, tv, grid, stream)
-                       : launch_one<D, BS, false, kModeTmem, KV8>(a, tk, tv, grid, stream);
-    return out_f32 ? launch_one<D, BS, true, kModeWide, KV8>(a, tk, tv, grid, stream)
-                   : launch_one<D, BS, false, kModeWide, KV8>(a, tk, tv, grid, stream);
+        return out_f32 ? launch_one<D, BS, true, kModeTmem, KV8>(a, tk, tv, tq, grid, stream)
+                       : launch_one<D, BS, false, kModeTmem, KV8>(a, tk, tv, tq, grid, stream);
+    return out_f32 ? launch_one<D, BS, true, kModeWide, KV8>(a, tk, tv, tq, grid, stream)
+                   : launch_one<D, BS, false, kModeWide, KV8>(a, tk, tv, tq, grid, stream);
 }
 
 template <bool KV8>
 static cudaError_t launch_decode_attn_kv(const AttnArgs& a, const CUtensorMap& tk,
-                                         const CUtensorMap& tv, int head_dim, int block_size,
-                                         bool out_f32, int grid, cudaStream_t stream) {
+                                         const CUtensorMap& tv, const CUtensorMap& tq,
+                                         int head_dim, int block_size, bool out_f32, int grid,
+                                         cudaStream_t stream) {
     if (head_dim == 128 && block_size == 16)
-        return launch_shape<128, 16, KV8>(a, tk, tv, out_f32, grid, stream);
+        return launch_shape<128, 16, KV8>(a, tk, tv, tq, out_f32, grid, stream);
     if (head_dim == 128 && block_size == 32)
-        return launch_shape<128, 32, KV8>(a, tk, tv, out_f32, grid, stream);
+        return launch_shape<128, 32, KV8>(a, tk, tv, tq, out_f32, grid, stream);
     if (head_dim == 64 && block_size == 16)
-        return launch_shape<64, 16, KV8>(a, tk, tv, out_f32, grid, stream);
+        return launch_shape<64, 16, KV8>(a, tk, tv, tq, out_f32, grid, stream);
     if (head_dim == 64 && block_size == 32)
-        return launch_shape<64, 32, KV8>(a, tk, tv, out_f32, grid, stream);
+        return launch_shape<64, 32, KV8>(a, tk, tv, tq, out_f32, grid, stream);
     return cudaErrorInvalidValue;
 }
 

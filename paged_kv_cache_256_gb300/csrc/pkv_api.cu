@@ -107,6 +107,55 @@ bool cached_cache_map(CUtensorMap* map, const void* base, int head_dim, long lon
     return true;
 }
 
+// 3-D view of the queries for the tensor-memory consumer: [tokens =
+// num_seqs * q_len][n_q heads][head_dim] bf16, one box = 64 columns x by
+// heads x bz tokens with the 128-byte swizzle, so a row tile lands as the
+// K-major operand the score MMA reads (row r = token-major, head-minor).
+bool make_q_map(CUtensorMap* map, const void* q, int head_dim, int n_q, long long tokens, int by,
+                int bz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_q, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_q * head_dim * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)by, (cuuint32_t)bz};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct QMapKey {
+    const void* q;
+    long long tokens;
+    int head_dim, n_q, by, bz;
+};
+struct QMapEntry {
+    QMapKey key;
+    CUtensorMap map;
+    bool used;
+};
+QMapEntry g_qmaps[kMapCache];
+int g_qmap_next = 0;
+
+bool cached_q_map(CUtensorMap* map, const void* q, int head_dim, int n_q, long long tokens, int by,
+                  int bz) {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (const QMapEntry& e : g_qmaps)
+        if (e.used && e.key.q == q && e.key.tokens == tokens && e.key.head_dim == head_dim &&
+            e.key.n_q == n_q && e.key.by == by && e.key.bz == bz) {
+            *map = e.map;
+            return true;
+        }
+    if (!make_q_map(map, q, head_dim, n_q, tokens, by, bz)) return false;
+    QMapEntry& e = g_qmaps[g_qmap_next];
+    g_qmap_next = (g_qmap_next + 1) % kMapCache;
+    e.key = QMapKey{q, tokens, head_dim, n_q, by, bz};
+    e.map = *map;
+    e.used = true;
+    return true;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -152,10 +201,29 @@ int unit_cost_for(int rows, bool kv8) {
     return rows > 64 ? 12 : 6;
 }
 
-// Query rows sharing one KV head are processed in tiles of at most 128.
+// Query rows sharing one KV head are processed in tiles of at most 128,
+// holding whole query tokens when a token's group of heads fits in a tile.
 int tile_rows(int n_q, int n_kv, int q_len) {
-    const int rows_total = (n_q / n_kv) * q_len;
-    return rows_total < kTileRows ? rows_total : kTileRows;
+    const int group = n_q / n_kv;
+    const int rows_total = group * q_len;
+    if (rows_total <= kTileRows) return rows_total;
+    return group <= kTileRows ? (kTileRows / group) * group : kTileRows;
+}
+
+// A tile as one TMA box of the query map (by heads x bz tokens): whole
+// tokens of `group` heads, or part of one token's heads when a token's
+// group spans several tiles.  0 when a tile cannot be one box.
+bool q_box(int group, int rows, int* by, int* bz) {
+    if (rows % group == 0) {
+        *by = group;
+        *bz = rows / group;
+    } else if (group % rows == 0) {
+        *by = rows;
+        *bz = 1;
+    } else {
+        return false;
+    }
+    return *by <= 256 && *bz <= 256;
 }
 
 }  // namespace
@@ -292,10 +360,20 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
 
-    CUtensorMap tk, tv;
+    CUtensorMap tk, tv, tq;
     if (!cached_cache_map(&tk, k_cache, head_dim, rows_total, block_size, kv8) ||
         !cached_cache_map(&tv, kv8 ? k_cache : v_cache, head_dim, rows_total, block_size, kv8))
         return PKV_ERR_CUDA;
+    // The tensor-memory consumer (more than 64 rows) takes its query tiles by
+    // TMA when a tile is one box; otherwise its threads load them.
+    std::memset(&tq, 0, sizeof tq);
+    int q_tma = 0, by = 0, bz = 0;
+    if (rows > 64 && (long long)num_seqs * q_len < (1LL << 31) &&
+        q_box(n_q / n_kv, rows, &by, &bz)) {
+        if (!cached_q_map(&tq, q, head_dim, n_q, (long long)num_seqs * q_len, by, bz))
+            return PKV_ERR_CUDA;
+        q_tma = 1;
+    }
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     AttnArgs a;
@@ -329,11 +407,13 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     a.checked = (flags & PKV_FLAG_CHECKED) ? 1 : 0;
     a.test_stall = (flags & PKV_FLAG_TEST_STALL) ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.q_tma = q_tma;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool f32 = out_dtype == PKV_OUT_F32;
-    const cudaError_t le = kv8 ? launch_decode_attn_fp8(a, tk, tv, head_dim, block_size, f32, grid, s)
-                               : launch_decode_attn(a, tk, tv, head_dim, block_size, f32, grid, s);
+    const cudaError_t le =
+        kv8 ? launch_decode_attn_fp8(a, tk, tv, tq, head_dim, block_size, f32, grid, s)
+            : launch_decode_attn(a, tk, tv, tq, head_dim, block_size, f32, grid, s);
     if (le != cudaSuccess) return PKV_ERR_CUDA;
     if (grid > 1 && launch_lse_merge(a, head_dim, f32, grid, s) != cudaSuccess)
         return PKV_ERR_CUDA;

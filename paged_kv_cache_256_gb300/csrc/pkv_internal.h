@@ -31,7 +31,7 @@ struct AttnArgs {
     int n_q;
     int n_kv;
     int group;       // n_q / n_kv
-    int rows;        // query rows per row tile: min(128, rows_total)
+    int rows;        // query rows per row tile: rows_total if <= 128, else <= 128 (whole tokens when they fit)
     int rows_total;  // group * q_len: query rows sharing one KV head
     int q_tiles;     // ceil(rows_total / rows): row tiles per (sequence, KV head)
     int max_blocks_per_seq;
@@ -47,6 +47,7 @@ struct AttnArgs {
     int checked;
     int test_stall;    // failure-path tests: the producer issues nothing
     float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
+    int q_tma;         // tensor-memory consumer: query tiles arrive by TMA (the q map is valid)
 };
 
 struct WorkspaceLayout {
@@ -57,11 +58,13 @@ WorkspaceLayout workspace_layout(int grid, int rows, int head_dim);
 
 
 cudaError_t launch_decode_attn(const AttnArgs& a, const CUtensorMap& tmap_k,
-                               const CUtensorMap& tmap_v, int head_dim, int block_size,
+                               const CUtensorMap& tmap_v, const CUtensorMap& tmap_q,
+                               int head_dim, int block_size,
                                bool out_f32, int grid, cudaStream_t stream);
 
 cudaError_t launch_decode_attn_fp8(const AttnArgs& a, const CUtensorMap& tmap_k,
-                                   const CUtensorMap& tmap_v, int head_dim, int block_size,
+                                   const CUtensorMap& tmap_v, const CUtensorMap& tmap_q,
+                                   int head_dim, int block_size,
                                    bool out_f32, int grid, cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const AttnArgs& a, int head_dim, bool out_f32, int grid,

@@ -28,7 +28,15 @@ CASES = [
     (64, 32, 32, 1, 9, [9, 40, 700]),                               # MQA: 288 rows, 3 tiles
     (128, 32, 64, 8, 50, [50, 77, 2000]),                           # G 8: 400 rows, 4 tiles
     (128, 16, 16, 2, 20, [20, 5, 300]),                             # ctx 5 < q_len: zero rows
+    # groups that are not powers of two: tiles of whole tokens (126 rows), a
+    # token's heads spread over tiles (256 = 2 x 128), one token per tile
+    # (96), and tiles that split a token's heads (200: no single TMA box)
+    (128, 16, 48, 8, 30, [30, 31, 400]),                            # G 6: 180 rows, 126 + 54
+    (64, 16, 256, 1, 2, [2, 90, 600]),                              # G 256: 4 tiles of 128
+    (128, 32, 96, 1, 3, [3, 64, 333]),                              # G 96: 3 tiles of one token
+    (64, 32, 200, 1, 2, [2, 45, 500]),                              # G 200: 4 tiles, split tokens
 ]
+FP8_CASES = CASES[:4] + CASES[5:]
 
 
 def _setup(oracle, case, seed):
@@ -72,7 +80,7 @@ def test_prefill_parity(oracle, case, grid):
             assert_close(out_to_host(out), ref, kind, f"{case} grid {grid} W {window} {kind}")
 
 
-@pytest.mark.parametrize("case", CASES[:4], ids=lambda c: "d{}_bs{}_q{}_kv{}_ql{}".format(*c[:5]))
+@pytest.mark.parametrize("case", FP8_CASES, ids=lambda c: "d{}_bs{}_q{}_kv{}_ql{}".format(*c[:5]))
 def test_prefill_fp8_parity(oracle, case):
     d, bs, n_q, n_kv, q_len, ctxs = case
     wl = make_custom(num_seqs=len(ctxs), q_len=q_len, n_q=n_q, n_kv=n_kv, head_dim=d,
