@@ -18,6 +18,15 @@
  *     stream) and must belong to the current CUDA device.  Calls are
  *     asynchronous on that stream: a PKV_OK return means "validated and
  *     launched"; faults inside a kernel surface at the next synchronisation.
+ *   - Programmatic overlap: the attention kernel is launched as a
+ *     programmatic dependent of the kernel before it on the stream, and the
+ *     append kernels let their dependents start at once.  So an attention
+ *     call right after an append begins its work partition (it reads
+ *     context_lens, and nothing else) while the append runs, and reads the
+ *     caches, q and block_tables, and writes anything, only after it has
+ *     completed.  A preceding kernel that does not signal early completion
+ *     (any kernel outside this library) is waited for as usual; one that
+ *     does must not write context_lens.
  *   - Argument checks run on the host before anything is launched; a failed
  *     check returns a status and launches nothing.
  *   - Device pointers to bf16 / fp32 tensors must be 16-byte aligned, int32

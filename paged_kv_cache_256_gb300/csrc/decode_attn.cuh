@@ -2029,6 +2029,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmap_v);
     }
     const Walk w0 = find_slice<BS>(a, s_red, s_pos, &s_walk);  // also publishes the barrier init
+    // This kernel is launched as a programmatic dependent of the previous
+    // kernel on the stream: the work partition above (which reads only the
+    // context lengths) may overlap it, e.g. the cache append that precedes
+    // every decode step; nothing else is read or written before it completes.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // Let the merge kernel (launched as a programmatic dependent) be scheduled
     // early; it waits for this whole grid before reading anything.
     if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -2108,7 +2113,18 @@ static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CU
         if (e != cudaSuccess) return e;
         opted_in.fetch_or(bit, std::memory_order_release);
     }
-    kern<<<grid, kThreads, smem, stream>>>(tk, tv, tq, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tk, tv, tq, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -21,6 +21,9 @@ __global__ void __launch_bounds__(256)
                      const int32_t* __restrict__ slot_mapping, long long num_tokens, int n_kv,
                      int chunks, int block_size, long long num_slots, uint4* __restrict__ k_cache,
                      uint4* __restrict__ v_cache) {
+    // The attention call that follows may start its work partition now (it
+    // reads no cache before this grid completes).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long total = num_tokens * n_kv * 2 * chunks;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
@@ -79,6 +82,9 @@ __global__ void __launch_bounds__(256)
                          int chunks, int block_size, long long num_slots,
                          const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                          uint2* __restrict__ kv_cache) {
+    // The attention call that follows may start its work partition now (it
+    // reads no cache before this grid completes).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long total = num_tokens * n_kv * 2 * chunks;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
