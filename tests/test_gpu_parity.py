@@ -135,6 +135,35 @@ def test_large_batches(oracle, num_seqs, grid):
         assert_close(out_to_host(out), ref, kind, f"{num_seqs} seqs grid {grid} {kind}")
 
 
+@pytest.mark.parametrize("n_q,q_len", [(8, 1), (32, 4)], ids=["narrow", "tmem"])
+def test_inputs_written_just_before_the_call_are_seen(oracle, n_q, q_len):
+    """Stream order with programmatic launches: q and the context lengths are
+    rewritten by ordinary kernels, the append runs, and the attention call
+    follows at once, with no synchronisation between them: the output must be
+    that of the rewritten inputs (the attention's work partition may overlap
+    the append, never the kernels before it)."""
+    import torch
+    ctxs = [33, 700, 5, 260]
+    wl = make_custom(num_seqs=len(ctxs), q_len=q_len, n_q=n_q, n_kv=1 if n_q == 32 else 2,
+                     head_dim=128, block_size=16, context_lens=ctxs, seed=91 + n_q)
+    dw = to_device(wl)
+    q_right, cl_right = dw.q.clone(), dw.context_lens.clone()
+    _, _, ref = oracle_after_append(oracle, wl)
+    ws = pkv.alloc_workspace(wl.num_seqs, wl.q_len, wl.n_q, wl.n_kv, wl.head_dim, wl.block_size)
+    out = torch.empty(tuple(dw.q.shape), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(3):
+        dw.q.zero_()
+        dw.context_lens.fill_(1)
+        dw.q.copy_(q_right)
+        dw.context_lens.copy_(cl_right)
+        pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache)
+        pkv.pkv_paged_decode_attn(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
+                                  dw.context_lens, wl.scale, out, ws)
+        assert pkv.pkv_check_error(ws) == pkv.PKV_OK
+        assert_close(out_to_host(out), ref, "f32", "inputs rewritten before the call")
+
+
 def test_block_relabelling_is_bit_identical():
     """Moving physical blocks (and rewriting the table) leaves the output bit-identical."""
     import torch
