@@ -98,11 +98,16 @@ def hbm_peak():
 
 
 def kernel_source_hash():
+    """Hash of the attention kernel's sources, line comments and blank lines
+    left out (a comment edit does not change the kernel the counters came from)."""
     h = hashlib.sha256()
     for name in ("decode_attn.cuh", "decode_attn.cu", "decode_attn_fp8.cu", "ptx.cuh",
                  "tcgen05.cuh", "pkv_internal.h"):
-        with open(os.path.join(ROOT, "paged_kv_cache_256_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_256_gb300", "csrc", name)) as f:
+            for line in f:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

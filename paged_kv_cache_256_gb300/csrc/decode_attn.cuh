@@ -79,7 +79,7 @@ constexpr int kTmemMinRows = 64;                 // rows above which the TMEM co
 // Consumer modes, chosen by the number of query rows sharing a KV head.
 constexpr int kModeWide = 0;    // 8 < rows <= 64: mma.sync, rows on the M side
 constexpr int kModeNarrow = 1;  // rows <= 8: mma.sync, tokens on the M side
-constexpr int kModeTmem = 2;    // rows > 64: tcgen05, 128-row tiles, accumulators in TMEM
+constexpr int kModeTmem = 2;    // rows > 64: tcgen05, M = 128 row tiles, accumulators in TMEM
 
 template <int D, int BS, int MODE, bool KV8 = false>
 struct AttnCfg {
@@ -1409,7 +1409,8 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 }
 
 // ===================== TMEM consumer (rows > 64) =====================
-// One 128-row tile per unit (rows >= R are zero), accumulators in TMEM.
+// One row tile (R <= 128 rows, on the MMA's M = 128; rows >= R are padding
+// whose scores are all masked) per unit, accumulators in TMEM.
 // Keys are taken kKeys = 64 at a time: one ring stage holds a super-block
 // of 64 / BS blocks with their K rows (and V rows) contiguous, so the three
 // roles synchronise once per 64 keys and one score MMA spans them all:
