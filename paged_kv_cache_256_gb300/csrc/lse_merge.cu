@@ -30,9 +30,11 @@
 
 namespace pkv {
 
-constexpr int kMergeWarps = 8;
+// Warps per block: 8 for units of up to 64 rows; 4 for 128-row units (MQA
+// verify, prefill tiles), whose eight times as many blocks then start two to
+// an SM beside the attention CTAs (measured: MQA verify 40.1 -> 39.4 us,
+// prefill 97.0 -> 96.4 us; GQA slower with 4).
 constexpr int kMergeRowsPerWarp = 2;
-constexpr int kMergeRowsPerBlock = kMergeWarps * kMergeRowsPerWarp;
 constexpr int kMergeChunk = 4;  // pieces whose outputs are loaded together
 
 template <int V>
@@ -67,8 +69,8 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-template <int D, bool OUT_F32>
-__global__ void __launch_bounds__(kMergeWarps * 32, 4)
+template <int D, bool OUT_F32, int kMergeWarps>
+__global__ void __launch_bounds__(kMergeWarps * 32, 32 / kMergeWarps)
     lse_merge_kernel(const AttnArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int V = D / 32;  // consecutive columns per lane
@@ -222,10 +224,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
     }
 }
 
-template <int D, bool F32>
+template <int D, bool F32, int kMergeWarps>
 static cudaError_t launch_merge_one(const AttnArgs& a, int grid, cudaStream_t stream) {
+    constexpr int kRowsPerBlock = kMergeWarps * kMergeRowsPerWarp;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, (a.rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock, 1);
+    cfg.gridDim = dim3(grid, (a.rows + kRowsPerBlock - 1) / kRowsPerBlock, 1);
     cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -234,19 +237,25 @@ static cudaError_t launch_merge_one(const AttnArgs& a, int grid, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, lse_merge_kernel<D, F32>, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, lse_merge_kernel<D, F32, kMergeWarps>, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int D, bool F32>
+static cudaError_t launch_merge_rows(const AttnArgs& a, int grid, cudaStream_t stream) {
+    return a.rows > 64 ? launch_merge_one<D, F32, 4>(a, grid, stream)
+                       : launch_merge_one<D, F32, 8>(a, grid, stream);
 }
 
 cudaError_t launch_lse_merge(const AttnArgs& a, int head_dim, bool out_f32, int grid,
                              cudaStream_t stream) {
     if (head_dim == 128)
-        return out_f32 ? launch_merge_one<128, true>(a, grid, stream)
-                       : launch_merge_one<128, false>(a, grid, stream);
+        return out_f32 ? launch_merge_rows<128, true>(a, grid, stream)
+                       : launch_merge_rows<128, false>(a, grid, stream);
     if (head_dim == 64)
-        return out_f32 ? launch_merge_one<64, true>(a, grid, stream)
-                       : launch_merge_one<64, false>(a, grid, stream);
+        return out_f32 ? launch_merge_rows<64, true>(a, grid, stream)
+                       : launch_merge_rows<64, false>(a, grid, stream);
     return cudaErrorInvalidValue;
 }
 
