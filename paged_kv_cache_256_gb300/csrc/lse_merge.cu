@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 32 / kMergeWarps)
     const int r0 = (blockIdx.y * kMergeWarps + warp) * RW;  // this warp's first row
     if (r0 >= a.rows) return;
 
-    // Round 1: CTA c's records and the first records of CTAs c+1 .. c+32.
+    // First load round: CTA c's records and the first records of CTAs c+1 .. c+32.
     const int4 i1 = a.rec_info[(size_t)c * 2 + 1];
     const int4 i0 = a.rec_info[(size_t)c * 2 + 0];
     const int cn = c + 1 + lane;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 32 / kMergeWarps)
 #pragma unroll
         for (int v = 0; v < V; ++v) acc[rr][v] = 0.f;
     }
-    // Flags of CTA c + lane (lanes >= 1), from round 1.
+    // Flags of CTA c + lane (lanes >= 1), from the first load round.
     const int z_near = __shfl_sync(0xffffffffu, nx.z, (lane + 31) & 31);
     for (int kg = 0; kg <= npc; kg += 32) {
         // Lane k <-> piece kg + k: its record, or -1 (past the unit, or an
