@@ -55,6 +55,10 @@ MUTANTS = {
     "fp8_append_multiplies": ("/ v_scale[g];", "* v_scale[g];"),
     "window_one_too_wide": ("const long first_l = window > 0 ? pos - window + 1 : 0;",
                             "const long first_l = window > 0 ? pos - window : 0;"),
+    "window_one_too_narrow": ("const long first_l = window > 0 ? pos - window + 1 : 0;",
+                              "const long first_l = window > 0 ? pos - window + 2 : 0;"),
+    "window_ignored": ("const long first_l = window > 0 ? pos - window + 1 : 0;",
+                       "const long first_l = 0;"),
     "copy_direction_swapped": ("memcpy(k_cache + (size_t)dst * per_block, k_cache + (size_t)src * per_block,",
                                "memcpy(k_cache + (size_t)src * per_block, k_cache + (size_t)dst * per_block,"),
 }
