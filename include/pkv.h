@@ -26,7 +26,8 @@
  *     caches, q and block_tables, and writes anything, only after it has
  *     completed.  A preceding kernel that does not signal early completion
  *     (any kernel outside this library) is waited for as usual; one that
- *     does must not write context_lens.
+ *     does must not write context_lens, unless the call passes
+ *     PKV_FLAG_NO_EARLY_START.
  *   - Argument checks run on the host before anything is launched; a failed
  *     check returns a status and launches nothing.
  *   - Device pointers to bf16 / fp32 tensors must be 16-byte aligned, int32
@@ -72,6 +73,11 @@ typedef enum pkv_status {
 #define PKV_FLAG_TEST_STALL 0x2u
 /* pkv_copy_blocks: the cache is the interleaved 8-bit (e4m3) cache. */
 #define PKV_FLAG_KV_FP8 0x4u
+/* Attention calls: launch the attention kernel as an ordinary (not a
+ * programmatic) dependent of the kernel before it, so it reads nothing,
+ * context_lens included, before that kernel has completed.  For callers whose
+ * preceding kernel signals early completion and writes context_lens. */
+#define PKV_FLAG_NO_EARLY_START 0x8u
 /* Bits 16..31 force the number of attention CTAs (0 = one per SM).  Tests
  * use it to move where long contexts are split; results stay within the
  * stated tolerance for every value. */
@@ -229,9 +235,10 @@ size_t pkv_paged_decode_attn_workspace_size(int num_seqs, int q_len, int n_q, in
  *   - Sizes whose workspace would exceed 24 MiB return PKV_ERR_WORKSPACE
  *     (every supported shape fits at up to 180 SMs; a forced CTA count in
  *     `flags` can exceed it).
- *   - PKV_FLAG_CHECKED returns PKV_ERR_UNSUPPORTED: the device-side report
- *     would land in the scratch array, which the caller cannot read.  For the
- *     same reason an expired in-kernel wait is not reported by this call.
+ *   - PKV_FLAG_CHECKED and PKV_FLAG_TEST_STALL return PKV_ERR_UNSUPPORTED:
+ *     device-side reports would land in the scratch array, which the caller
+ *     cannot read.  For the same reason an expired in-kernel wait is not
+ *     reported by this call.
  *   - The first call on a device looks up the scratch array's device address
  *     (with that device current); make that first call before any stream
  *     capture on the device.

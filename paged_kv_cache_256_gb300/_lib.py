@@ -27,6 +27,7 @@ PKV_OUT_F32 = 1
 PKV_FLAG_CHECKED = 0x1
 PKV_FLAG_TEST_STALL = 0x2
 PKV_FLAG_KV_FP8 = 0x4
+PKV_FLAG_NO_EARLY_START = 0x8
 PKV_KV_BF16 = 0
 PKV_KV_FP8_E4M3 = 1
 PKV_FLAG_GRID_SHIFT = 16
@@ -215,8 +216,10 @@ def _attn_shapes(q, k_cache, v_cache, block_tables, context_lens, out, workspace
         out_dtype = PKV_OUT_BF16
     else:
         raise TypeError("out must be bfloat16 or float32")
-    if not out.is_cuda or not out.is_contiguous() or not workspace.is_cuda:
-        raise ValueError("out and workspace must be contiguous CUDA tensors")
+    if not out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CUDA tensor")
+    if workspace is not None and not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
     return (num_seqs, q_len, n_q, n_kv, d, bs, block_tables.shape[1], num_blocks), out_dtype
 
 
@@ -275,17 +278,8 @@ def pkv_paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_len
     For callers that cannot allocate device memory; see include/pkv.h for the
     24 MiB limit, the shared-scratch caveats and the first-call set-up.
     """
-    import torch
-    _bf16_like(q, "q")
-    _bf16_like(k_cache, "k_cache")
-    _bf16_like(v_cache, "v_cache")
-    _i32(block_tables, "block_tables")
-    _i32(context_lens, "context_lens")
-    num_seqs, q_len, n_q, d = q.shape
-    num_blocks, n_kv, bs, d2 = k_cache.shape
-    if d2 != d or tuple(out.shape) != tuple(q.shape) or v_cache.shape != k_cache.shape:
-        raise ValueError("inconsistent shapes")
-    out_dtype = PKV_OUT_F32 if out.dtype == torch.float32 else PKV_OUT_BF16
+    (num_seqs, q_len, n_q, n_kv, d, bs, _, num_blocks), out_dtype = _attn_shapes(
+        q, k_cache, v_cache, block_tables, context_lens, out, None)
     st = load_library().pkv_paged_decode_attn_noalloc(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
         context_lens.data_ptr(), num_seqs, q_len, n_q, n_kv, d, bs, block_tables.shape[1],

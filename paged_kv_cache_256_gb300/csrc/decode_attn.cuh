@@ -23,10 +23,10 @@
 //     ragged the context lengths are.  A unit cut by a slice boundary is a
 //     split (flash-decoding); its pieces leave (O, m, l) partials that the
 //     LSE merge kernel combines.
-//   * Warp 8 is the producer: it reads block ids and four of its lanes issue,
-//     side by side, 2-D TMA tile loads (128-byte swizzle) of the K and V
-//     tiles of each (block, KV head) into a ring of shared-memory stages, each
-//     guarded by a full/empty mbarrier pair.  Its walk never stops at unit
+//   * Warp 8 is the producer: it reads block ids and kIssueLanes (8) of its
+//     lanes issue, side by side, 2-D TMA tile loads (128-byte swizzle) of the
+//     K and V tiles of each (block, KV head) into a ring of shared-memory
+//     stages, each guarded by a full/empty mbarrier pair.  Its walk never stops at unit
 //     boundaries, so HBM stays busy while consumers finish a unit.
 //   * Warps 0..7 consume, each taking every 8th block (and, for more than 8
 //     rows, one 16-row slice of them).  Products run on the tensor cores
@@ -2125,7 +2125,7 @@ static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CU
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = a.early_start ? 1 : 0;  // without it, griddepcontrol.wait returns at once
     e = cudaLaunchKernelEx(&cfg, kern, tk, tv, tq, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -409,6 +409,7 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     a.test_stall = (flags & PKV_FLAG_TEST_STALL) ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.q_tma = q_tma;
+    a.early_start = (flags & PKV_FLAG_NO_EARLY_START) ? 0 : 1;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool f32 = out_dtype == PKV_OUT_F32;

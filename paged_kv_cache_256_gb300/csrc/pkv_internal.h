@@ -48,6 +48,7 @@ struct AttnArgs {
     int test_stall;    // failure-path tests: the producer issues nothing
     float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
     int q_tma;         // tensor-memory consumer: query tiles arrive by TMA (the q map is valid)
+    int early_start;   // launched as a programmatic dependent of the previous kernel
 };
 
 struct WorkspaceLayout {

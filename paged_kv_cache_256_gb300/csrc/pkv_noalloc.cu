@@ -52,9 +52,11 @@ extern "C" int pkv_paged_decode_attn_noalloc(
     const int32_t* context_lens, int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
     int block_size, int max_blocks_per_seq, int num_blocks, float scale, void* out,
     int out_dtype, unsigned flags, void* stream) {
-    // The device-side report of CHECKED mode lands in the scratch array, which
-    // this caller cannot read back; refuse the flag rather than drop reports.
-    if (flags & PKV_FLAG_CHECKED) return PKV_ERR_UNSUPPORTED;
+    // Device-side reports (CHECKED mode, an expired wait) land in the scratch
+    // array, which this caller cannot read back.  Refuse CHECKED rather than
+    // drop its reports, and refuse the test-only stall flag, whose only effect
+    // here would be an invalid output with PKV_OK.
+    if (flags & (PKV_FLAG_CHECKED | PKV_FLAG_TEST_STALL)) return PKV_ERR_UNSUPPORTED;
     const size_t need = pkv_paged_decode_attn_workspace_size(num_seqs, q_len, n_q, n_kv,
                                                              head_dim, block_size, 0, flags);
     if (need == 0 || num_seqs == 0) {

@@ -79,17 +79,29 @@ int pkv_pool_share(pkv_block_pool* pool, const int32_t* blocks, int n) {
 
 int pkv_pool_release(pkv_block_pool* pool, const int32_t* blocks, int n) {
     if (!pool || n < 0 || (n > 0 && !blocks)) return PKV_ERR_INVALID_ARG;
-    // The same id may appear several times; check the combined drop first.
-    std::vector<int32_t> drop(pool->refcount.size(), 0);
+    // O(n) work and no allocation: drop the counts one by one (the same id
+    // may appear several times); if one would go below zero, put back the
+    // drops already made and fail.
+    const int num_blocks = static_cast<int>(pool->refcount.size());
     for (int i = 0; i < n; ++i) {
         const int32_t b = blocks[i];
-        if (b < 0 || b >= static_cast<int>(pool->refcount.size())) return PKV_ERR_INVALID_ARG;
-        if (++drop[b] > pool->refcount[b]) return PKV_ERR_INVALID_ARG;
+        if (b < 0 || b >= num_blocks || pool->refcount[b] == 0) {
+            for (int k = 0; k < i; ++k) ++pool->refcount[blocks[k]];
+            return PKV_ERR_INVALID_ARG;
+        }
+        --pool->refcount[b];
     }
+    // Blocks whose count reached zero join the free list once each (-1 marks
+    // "already pushed" during this pass and is reset to 0 afterwards).
     for (int i = 0; i < n; ++i) {
         const int32_t b = blocks[i];
-        if (--pool->refcount[b] == 0) pool->free_list.push_back(b);
+        if (pool->refcount[b] == 0) {
+            pool->free_list.push_back(b);
+            pool->refcount[b] = -1;
+        }
     }
+    for (int i = 0; i < n; ++i)
+        if (pool->refcount[blocks[i]] < 0) pool->refcount[blocks[i]] = 0;
     return PKV_OK;
 }
 

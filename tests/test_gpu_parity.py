@@ -135,13 +135,15 @@ def test_large_batches(oracle, num_seqs, grid):
         assert_close(out_to_host(out), ref, kind, f"{num_seqs} seqs grid {grid} {kind}")
 
 
+@pytest.mark.parametrize("flags", [0, pkv.PKV_FLAG_NO_EARLY_START], ids=["early", "no_early"])
 @pytest.mark.parametrize("n_q,q_len", [(8, 1), (32, 4)], ids=["narrow", "tmem"])
-def test_inputs_written_just_before_the_call_are_seen(oracle, n_q, q_len):
+def test_inputs_written_just_before_the_call_are_seen(oracle, n_q, q_len, flags):
     """Stream order with programmatic launches: q and the context lengths are
     rewritten by ordinary kernels, the append runs, and the attention call
     follows at once, with no synchronisation between them: the output must be
     that of the rewritten inputs (the attention's work partition may overlap
-    the append, never the kernels before it)."""
+    the append, never the kernels before it; with PKV_FLAG_NO_EARLY_START it
+    overlaps nothing)."""
     import torch
     ctxs = [33, 700, 5, 260]
     wl = make_custom(num_seqs=len(ctxs), q_len=q_len, n_q=n_q, n_kv=1 if n_q == 32 else 2,
@@ -159,7 +161,7 @@ def test_inputs_written_just_before_the_call_are_seen(oracle, n_q, q_len):
         dw.context_lens.copy_(cl_right)
         pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache)
         pkv.pkv_paged_decode_attn(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
-                                  dw.context_lens, wl.scale, out, ws)
+                                  dw.context_lens, wl.scale, out, ws, flags=flags)
         assert pkv.pkv_check_error(ws) == pkv.PKV_OK
         assert_close(out_to_host(out), ref, "f32", "inputs rewritten before the call")
 
