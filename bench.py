@@ -2,28 +2,37 @@
 """Benchmark of the paged decode-attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--kv bf16|fp8] [--window W]
+                    [--workload NAME] [--kv bf16|fp8] [--window W] [--only]
 
 A step is one pass of the whole hot path over one batch: kv_append of the
 step's new K/V, then paged decode attention (plus its LSE merge launch) over
-every sequence.  The default workload is the Llama-3-8B-shaped GQA continuous
-batch (64 sequences, contexts uniform in [128, 8192], 32 query / 8 KV heads,
-head_dim 128, block 16), whose KV cache (~1.03 GB) is 8x the 129 MB L2, so
-no flush is needed between steps.
+every sequence.  Each step is captured once as a CUDA graph and replayed; the
+attention call alone is captured as a second graph.  Before every timed
+replay the L2 is flushed (a write of 2x the 129 MB L2, then a read of 2x the
+L2), outside the replay's own pair of CUDA events, so every step starts cold
+and its bytes come from HBM whatever the size of its working set.
 
-Printed (rank 0, one JSON line): effective HBM GB/s of the step, where bytes =
-resident KV + q + out, with microseconds per step, the fraction of the
-measured HBM peak, the roofline of the attention launch, the end-to-end
-figure through the public API with host buffers, the oracle as a CPU
-baseline, and the SM clocks sampled while the steps ran.  The headline step
-time is the CUDA-graph replay of the step (the three launches captured
-once); the eagerly launched step is reported under "eager".
+Printed (rank 0, one JSON line):
+  * the headline workload (default: the Llama-3-8B-shaped GQA continuous
+    batch, 64 sequences, contexts uniform in [128, 8192], 32 query / 8 KV
+    heads, head_dim 128, block 16): effective GB/s of exactly K timed steps,
+    where bytes = resident KV + q + out, microseconds per step, and the
+    fraction of the measured copy peak, of a measured read-stream peak and of
+    the nominal HBM rate;
+  * its roofline from the attention call's own replays (attention + merge
+    launches) in the same mode, with percentiles over at least 200 steps;
+  * the end-to-end figure through the public API with host buffers, the
+    oracle as a CPU baseline, and the SM clocks sampled while the steps ran;
+  * `per_workload`: the same step and attention figures for every other
+    named workload -- tiny, the MHA layer, MQA speculative verify, 128k
+    contexts, the 8-bit (e4m3) cache on GQA / MQA verify / prefill, and the
+    chunked-prefill chunk (a tensor-core roofline) -- 200 flushed steps each.
 
---kv fp8 times the same step over an 8-bit (e4m3) cache with per-KV-head
-scales (the quantising append, then attention); --window W times
-sliding-window attention.  Their bytes count what the step must move: the
-e4m3 cache is one byte per element, and a window reads at most W + q_len - 1
-tokens per sequence.  The default line (bf16, no window) is the headline.
+--kv fp8 makes the headline the same step over an 8-bit (e4m3) cache (the
+quantising append, then attention); --window W times sliding-window
+attention.  Their bytes count what the step must move: the e4m3 cache is one
+byte per element, and a window reads at most W + q_len - 1 tokens per
+sequence.  --only skips the per-workload lines (profiling runs).
 
 Under torchrun (N > 1) every rank runs an independent replica of the
 workload on its own GPU (no collective on the data path); the timing is the
@@ -48,6 +57,7 @@ METRIC = "paged decode attn effective HBM GB/s (% of GB300 peak) and μs per dec
 UNIT = "GB/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attn_traffic.json")
 
 
@@ -62,9 +72,10 @@ def parse_args():
     ap.add_argument("--window", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-soak", action="store_true",
                     help="skip the 1 s untimed load before the timed steps (profiling runs)")
+    ap.add_argument("--only", action="store_true",
+                    help="time the chosen workload only (no per-workload lines)")
     return ap.parse_args()
 
 
@@ -191,7 +202,10 @@ def max_over_ranks(values, device=None):
     import torch.distributed as dist
     if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
         return [float(v) for v in values]
-    dev = device if dist.get_backend() == "nccl" else "cpu"
+    if dist.get_backend() == "nccl":
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    else:
+        dev = "cpu"
     t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return [float(x) for x in t.cpu()]
@@ -306,8 +320,272 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
-def run_ours(args):
+# Workloads timed beside the headline, each as (key, workload, kv dtype, window).
+PER_WORKLOAD = [
+    ("tiny", "tiny", "bf16", 0),
+    ("llama2_7b_mha", "llama2_7b_mha", "bf16", 0),
+    ("mqa_spec_verify", "mqa_spec_verify", "bf16", 0),
+    ("long_splitk", "long_splitk", "bf16", 0),
+    ("llama3_8b_gqa/e4m3", "llama3_8b_gqa", "fp8", 0),
+    ("mqa_spec_verify/e4m3", "mqa_spec_verify", "fp8", 0),
+    ("llama3_8b_chunked_prefill", "llama3_8b_chunked_prefill", "bf16", 0),
+    ("llama3_8b_chunked_prefill/e4m3", "llama3_8b_chunked_prefill", "fp8", 0),
+]
+DIST_STEPS = 200  # steps behind each percentile line
+
+
+class L2Flush:
+    """Evicts the L2 before a timed step: a write of 2x the L2, then a read of 2x the L2
+    (the read evicts the dirty lines the write left, so their write-back lands here and
+    not in the timed step that follows)."""
+
+    def __init__(self, device):
+        import torch
+        import paged_kv_cache_256_gb300 as pkv
+        self.pkv = pkv
+        n = 2 * L2_BYTES
+        self.wbuf = torch.empty(n, dtype=torch.uint8, device=device)
+        self.rbuf = torch.zeros(n, dtype=torch.uint8, device=device)
+        self.sink = torch.zeros(1, dtype=torch.int32, device=device)
+        self.k = 0
+
+    def __call__(self):
+        self.k = (self.k + 1) & 0x7F
+        self.wbuf.fill_(self.k)
+        self.pkv.pkv_read_stream(self.rbuf, self.sink)
+
+    describe = ("flushed before every timed step: a write of 2x the 129 MB L2, then a read "
+                "of 2x the L2 (pkv_read_stream), outside the timed events")
+
+
+def read_peak(device, nbytes=2 << 30, reps=8):
+    """Best read rate of pkv_read_stream over a 2 GiB buffer (16x the L2), GB/s."""
+    import torch
+    import paged_kv_cache_256_gb300 as pkv
+    buf = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+    sink = torch.zeros(1, dtype=torch.int32, device=device)
+    best, best_c = 0.0, 0
+    for c in (1, 2, 3, 4):
+        pkv.pkv_read_stream(buf, sink, c)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in ev:
+            a.record()
+            pkv.pkv_read_stream(buf, sink, c)
+            b.record()
+        torch.cuda.synchronize(device)
+        gbs = nbytes / (min(a.elapsed_time(b) for a, b in ev) * 1e-3) / 1e9
+        if gbs > best:
+            best, best_c = gbs, c
+    del buf
+    return {"gbs": round(best, 1), "ctas_per_sm": best_c, "bytes": nbytes,
+            "kernel": "pkv_read_stream (16-byte loads, 8 in flight per thread, 512-thread CTAs)"}
+
+
+def pctl(xs):
+    """p10, p50, p90 of a list (ms) in microseconds."""
+    q = statistics.quantiles(xs, n=10) if len(xs) >= 10 else [min(xs)] * 4 + [max(xs)] * 5
+    return [round(1e3 * q[0], 2), round(1e3 * statistics.median(xs), 2), round(1e3 * q[8], 2)]
+
+
+class Case:
+    """One workload on the device: its step (append + attention) and its attention call,
+    eager and as CUDA graphs."""
+
+    def __init__(self, name, kv, window, device):
+        import torch
+        import paged_kv_cache_256_gb300 as pkv
+        from paged_kv_cache_256_gb300.device import fp8_to_device, to_device
+        from paged_kv_cache_256_gb300.workloads import fp8_cache_for, make_workload
+        self.pkv, self.device = pkv, device
+        self.wl = wl = make_workload(name)
+        self.kv8 = kv == "fp8"
+        self.window = window
+        self.total_bytes, self.kv_bytes = step_bytes(wl, 1 if self.kv8 else 2, window)
+        self.flops = step_flops(wl, window)
+        self.dw = to_device(wl, device)
+        self.d8 = fp8_to_device(fp8_cache_for(wl), device) if self.kv8 else None
+        if self.kv8:  # the bf16 caches are not used by this step
+            self.dw.k_cache = self.dw.v_cache = None
+            torch.cuda.empty_cache()
+        self.ws = pkv.alloc_workspace(wl.num_seqs, wl.q_len, wl.n_q, wl.n_kv, wl.head_dim,
+                                      wl.block_size, device=device)
+        self.out = torch.empty(tuple(self.dw.q.shape), dtype=torch.bfloat16, device=device)
+        grid = torch.cuda.get_device_properties(device).multi_processor_count
+        self.launches_per_step = 3 if grid > 1 else 2
+        self.prefill = wl.group * wl.q_len > 128  # many query rows per KV head: compute-bound
+
+    def append(self, s):
+        pkv, dw, d8 = self.pkv, self.dw, self.d8
+        if self.kv8:
+            pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.kv_cache, d8.k_scale,
+                                  d8.v_scale, stream=s)
+        else:
+            pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache,
+                              stream=s)
+
+    def attend(self, s):
+        pkv, dw, d8, wl = self.pkv, self.dw, self.d8, self.wl
+        if self.kv8:
+            pkv.pkv_paged_decode_attn_ex(dw.q, d8.kv_cache, None, dw.block_tables,
+                                         dw.context_lens, wl.scale, self.out, self.ws, stream=s,
+                                         window=self.window, k_scale=d8.k_scale,
+                                         v_scale=d8.v_scale)
+        elif self.window:
+            pkv.pkv_paged_decode_attn_ex(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
+                                         dw.context_lens, wl.scale, self.out, self.ws, stream=s,
+                                         window=self.window)
+        else:
+            pkv.pkv_paged_decode_attn(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
+                                      dw.context_lens, wl.scale, self.out, self.ws, stream=s)
+
+    def step(self, s):
+        self.append(s)
+        self.attend(s)
+
+    def check(self, what):
+        st = self.pkv.pkv_check_error(self.ws)
+        if st != self.pkv.PKV_OK:
+            raise RuntimeError(f"{self.wl.name}: {what} reported {self.pkv.pkv_status_string(st)}")
+
+    def capture(self, warmup):
+        """Eager warm-up steps, then the step and the attention call captured as graphs."""
+        import torch
+        stream = torch.cuda.current_stream(self.device)
+        for _ in range(max(3, warmup)):
+            self.step(stream)
+        torch.cuda.synchronize(self.device)
+        self.check("warm-up")
+        self.graphs = {}
+        for kind, fn in (("step", self.step), ("attn", self.attend)):
+            gs = torch.cuda.Stream(self.device)
+            gs.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=gs):
+                fn(gs)
+            stream.wait_stream(gs)
+            for _ in range(3):
+                g.replay()
+            self.graphs[kind] = g
+        torch.cuda.synchronize(self.device)
+        self.check("graph warm-up")
+
+    def time_replays(self, kind, n, flush):
+        """n replays of one graph, the L2 flushed before each, each timed by its own events."""
+        import torch
+        g = self.graphs[kind]
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            flush()
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize(self.device)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def release(self):
+        import torch
+        self.graphs = None
+        self.dw = self.d8 = self.ws = self.out = None
+        torch.cuda.synchronize(self.device)
+        torch.cuda.empty_cache()
+
+
+def roofline_of(case, attn_ms, hbm, rpeak):
+    """Roofline of the attention call (attention + merge launches) from its mean time."""
+    achieved = case.total_bytes / (attn_ms * 1e-3) / 1e9
+    key = case.wl.name + ("/fp8" if case.kv8 else "") + (f"/w{case.window}" if case.window else "")
+    r = {"kernel": "paged_decode_attn (attention + merge launches of one call)", "bound": "hbm",
+         "achieved": round(achieved, 2), "peak": hbm[0], "unit": "GB/s",
+         "frac": round(achieved / hbm[0], 4),
+         "frac_of_read_peak": round(achieved / rpeak, 4) if rpeak else None,
+         "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+         "traffic": profiled_traffic(key), "peak_source": hbm[1],
+         "attn_us": round(attn_ms * 1e3, 2), "algorithmic_bytes_per_launch": case.total_bytes,
+         "flops_per_launch": case.flops}
+    if case.prefill:
+        # A prefill chunk is a dense contraction: its roofline is the tensor peak.
+        tpeak, tsrc = tensor_peak()
+        tflops = case.flops / (attn_ms * 1e-3) / 1e12
+        r.update({"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak,
+                  "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4), "peak_source": tsrc,
+                  "frac_of_read_peak": None, "frac_of_nominal": None,
+                  "hbm_gbs_of_algorithmic_bytes": round(achieved, 2)})
+    return r
+
+
+def workload_line(case, step_ms, attn_ms, hbm, rpeak, world):
+    """One per-workload entry: distributions of flushed graph replays of the step and of
+    the attention call."""
+    mean_step, mean_attn = max_over_ranks([statistics.fmean(step_ms), statistics.fmean(attn_ms)])
+    wl = case.wl
+    return {
+        "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "n_q": wl.n_q, "n_kv": wl.n_kv,
+                   "head_dim": wl.head_dim, "block_size": wl.block_size, "q_len": wl.q_len,
+                   "kv_dtype": "e4m3" if case.kv8 else "bf16", "window": case.window,
+                   "resident_tokens": wl.resident_tokens(), "bytes_per_step": case.total_bytes},
+        "us_per_step": round(mean_step * 1e3, 2),
+        "step_us_p10_p50_p90": pctl(step_ms),
+        "value": round(whole_job_gbps(case.total_bytes, mean_step, world), 2), "unit": UNIT,
+        "pct_of_peak": round(100.0 * case.total_bytes / (mean_step * 1e-3) / 1e9 / hbm[0], 2),
+        "attn_us": round(mean_attn * 1e3, 2),
+        "attn_us_p10_p50_p90": pctl(attn_ms),
+        "steps_timed": len(step_ms),
+        "roofline": roofline_of(case, mean_attn, hbm, rpeak),
+    }
+
+
+def e2e_of(case, K, world):
+    """The step through the public API with host buffers: this step's inputs copied from
+    pinned host memory, the step, and `out` copied back, all inside the timed region."""
     import numpy as np
+    import torch
+    wl, dw, device = case.wl, case.dw, case.device
+    stream = torch.cuda.current_stream(device)
+    host = {
+        "q": torch.from_numpy(wl.q.view(np.int16)).pin_memory(),
+        "k_new": torch.from_numpy(wl.k_new.view(np.int16)).pin_memory(),
+        "v_new": torch.from_numpy(wl.v_new.view(np.int16)).pin_memory(),
+        "slot_mapping": torch.from_numpy(wl.slot_mapping).pin_memory(),
+        "block_tables": torch.from_numpy(wl.block_tables).pin_memory(),
+        "context_lens": torch.from_numpy(wl.context_lens).pin_memory(),
+    }
+    out_host = torch.empty(tuple(case.out.shape), dtype=torch.int16).pin_memory()
+    dev = {
+        "q": dw.q.view(torch.int16), "k_new": dw.k_new.view(torch.int16),
+        "v_new": dw.v_new.view(torch.int16), "slot_mapping": dw.slot_mapping,
+        "block_tables": dw.block_tables, "context_lens": dw.context_lens,
+    }
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k2, t in host.items():
+            dev[k2].copy_(t, non_blocking=True)
+        case.step(stream)
+        out_host.copy_(case.out.view(torch.int16), non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / K])[0]
+    case.check("end-to-end steps")
+    return {"value": round(whole_job_gbps(case.total_bytes, e2e_ms, world), 2), "unit": UNIT,
+            "us_per_step": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "timed_as": "eager launches, back to back, host copies in the timed region"}
+
+
+def run_ours(args):
     import torch
 
     world, rank, local = dist_env()
@@ -318,219 +596,97 @@ def run_ours(args):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
 
-    import paged_kv_cache_256_gb300 as pkv
-    from paged_kv_cache_256_gb300.device import fp8_to_device, to_device
-    from paged_kv_cache_256_gb300.workloads import fp8_cache_for, make_workload
+    hbm = hbm_peak()
+    flush = L2Flush(device)
+    rpk = read_peak(device)
+    rpeak = max_over_ranks([-rpk["gbs"]])[0] * -1.0  # the slowest rank's read peak
 
-    wl = make_workload(args.workload)
-    kv8 = args.kv == "fp8"
-    total_bytes, kv_bytes = step_bytes(wl, 1 if kv8 else 2, args.window)
-    dw = to_device(wl, device)
-    d8 = fp8_to_device(fp8_cache_for(wl), device) if kv8 else None
-    if kv8:  # the bf16 caches are not used by this step
-        dw.k_cache = dw.v_cache = None
-        torch.cuda.empty_cache()
-    ws = pkv.alloc_workspace(wl.num_seqs, wl.q_len, wl.n_q, wl.n_kv, wl.head_dim,
-                             wl.block_size, device=device)
-    out = torch.empty(tuple(dw.q.shape), dtype=torch.bfloat16, device=device)
-    stream = torch.cuda.current_stream(device)
-    grid = torch.cuda.get_device_properties(device).multi_processor_count
-    launches_per_step = 3 if grid > 1 else 2
-
-    def append(s):
-        if kv8:
-            pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.kv_cache, d8.k_scale,
-                                  d8.v_scale, stream=s)
-        else:
-            pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache,
-                              stream=s)
-
-    def attend(s):
-        if kv8:
-            pkv.pkv_paged_decode_attn_ex(dw.q, d8.kv_cache, None, dw.block_tables,
-                                         dw.context_lens, wl.scale, out, ws, stream=s,
-                                         window=args.window, k_scale=d8.k_scale,
-                                         v_scale=d8.v_scale)
-        elif args.window:
-            pkv.pkv_paged_decode_attn_ex(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
-                                         dw.context_lens, wl.scale, out, ws, stream=s,
-                                         window=args.window)
-        else:
-            pkv.pkv_paged_decode_attn(dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
-                                      dw.context_lens, wl.scale, out, ws, stream=s)
-
-    def step():
-        append(stream)
-        attend(stream)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize(device)
-    st = pkv.pkv_check_error(ws)
-    if st != pkv.PKV_OK:
-        raise RuntimeError(f"warm-up reported {pkv.pkv_status_string(st)}")
-
-    K = args.steps
-    ev_step = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
-    ev_attn = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
-    # Let the sampler see the GPU under load before and through the timed steps.
+    # ---- the headline workload: exactly K timed steps, then its distributions
+    case = Case(args.workload, args.kv, args.window, device)
+    case.capture(args.warmup)
+    # Let the sampler see the GPU under load before the timed steps.
     t_soak = time.perf_counter()
     while not args.no_soak and time.perf_counter() - t_soak < 1.0:
-        for _ in range(50):
-            step()
-        torch.cuda.synchronize(device)
+        case.time_replays("step", 20, flush)
+    K = args.steps
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
-    ev_step[0].record(stream)
-    for k in range(K):
-        append(stream)
-        ev_attn[k].record(stream)
-        attend(stream)
-        ev_step[k + 1].record(stream)
+    step_ms_k = case.time_replays("step", K, flush)
     torch.cuda.synchronize(device)
     if world > 1:
         torch.distributed.barrier()
-    st = pkv.pkv_check_error(ws)
-    if st != pkv.PKV_OK:
-        raise RuntimeError(f"timed steps reported {pkv.pkv_status_string(st)}")
+    case.check("timed steps")
+    ms_per_step = max_over_ranks([statistics.fmean(step_ms_k)])[0]
+    n_dist = max(K, DIST_STEPS)
+    step_ms = step_ms_k + case.time_replays("step", n_dist - K, flush) if n_dist > K else step_ms_k
+    attn_ms = case.time_replays("attn", n_dist, flush)
+    case.check("distribution steps")
+    head = workload_line(case, step_ms, attn_ms, hbm, rpeak, world)
+    e2e = None if args.no_e2e else e2e_of(case, K, world)
+    wl = case.wl
+    launches = case.launches_per_step * K
+    headline_case = (wl.name, case.kv8, case.window)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not case.kv8 and \
+            not args.window:
+        cpu = cpu_baseline(wl)
+    case.release()
 
-    total_ms = ev_step[0].elapsed_time(ev_step[K])
-    attn_ms = [ev_attn[k].elapsed_time(ev_step[k + 1]) for k in range(K)]
-    step_ms = [ev_step[k].elapsed_time(ev_step[k + 1]) for k in range(K)]
-    ms_per_step, attn_mean = max_over_ranks([total_ms / K, sum(attn_ms) / K], device)
-
-    # ---- end to end through the public API, host buffers, copies inside the timed region
-    e2e = None
-    if not args.no_e2e:
-        host = {
-            "q": torch.from_numpy(wl.q.view(np.int16)).pin_memory(),
-            "k_new": torch.from_numpy(wl.k_new.view(np.int16)).pin_memory(),
-            "v_new": torch.from_numpy(wl.v_new.view(np.int16)).pin_memory(),
-            "slot_mapping": torch.from_numpy(wl.slot_mapping).pin_memory(),
-            "block_tables": torch.from_numpy(wl.block_tables).pin_memory(),
-            "context_lens": torch.from_numpy(wl.context_lens).pin_memory(),
-        }
-        out_host = torch.empty(tuple(out.shape), dtype=torch.int16).pin_memory()
-        dev = {
-            "q": dw.q.view(torch.int16), "k_new": dw.k_new.view(torch.int16),
-            "v_new": dw.v_new.view(torch.int16), "slot_mapping": dw.slot_mapping,
-            "block_tables": dw.block_tables, "context_lens": dw.context_lens,
-        }
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_host.numel() * out_host.element_size()
-
-        def e2e_step():
-            for k2, t in host.items():
-                dev[k2].copy_(t, non_blocking=True)
-            step()
-            out_host.copy_(out.view(torch.int16), non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize(device)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if world > 1:
-            torch.distributed.barrier()
-        e0.record(stream)
-        for _ in range(K):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(device)
-        e2e_ms = max_over_ranks([e0.elapsed_time(e1) / K], device)[0]
-        e2e = {"value": round(whole_job_gbps(total_bytes, e2e_ms, world), 2), "unit": UNIT,
-               "us_per_step": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
-
-    # ---- the same step replayed from a CUDA graph (no host launch cost)
-    graph = None
-    if not args.no_graph:
-        gs = torch.cuda.Stream(device)
-        gs.wait_stream(stream)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=gs):
-            append(gs)
-            attend(gs)
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize(device)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if world > 1:
-            torch.distributed.barrier()
-        g0.record(stream)
-        for _ in range(K):
-            g.replay()
-        g1.record(stream)
-        torch.cuda.synchronize(device)
-        g_ms = max_over_ranks([g0.elapsed_time(g1) / K], device)[0]
-        st = pkv.pkv_check_error(ws)
-        if st != pkv.PKV_OK:
-            raise RuntimeError(f"graph replay reported {pkv.pkv_status_string(st)}")
-        graph = {"value": round(whole_job_gbps(total_bytes, g_ms, world), 2), "unit": UNIT,
-                 "us_per_step": round(g_ms * 1e3, 2)}
-
+    # ---- the other workloads: the same flushed graph replays, DIST_STEPS of each
+    per = {}
+    if not args.only:
+        for key, name, kv, window in PER_WORKLOAD:
+            if (name, kv == "fp8", window) == headline_case:
+                continue
+            c = Case(name, kv, window, device)
+            c.capture(args.warmup)
+            s_ms = c.time_replays("step", DIST_STEPS, flush)
+            a_ms = c.time_replays("attn", DIST_STEPS, flush)
+            c.check("timed steps")
+            per[key] = workload_line(c, s_ms, a_ms, hbm, rpeak, world)
+            c.release()
     clk = clocks.stop()
 
-    # The headline step is the CUDA-graph replay (how a decode loop is served);
-    # the eagerly launched step is reported beside it.
-    eager = {"value": round(whole_job_gbps(total_bytes, ms_per_step, world), 2), "unit": UNIT,
-             "us_per_step": round(ms_per_step * 1e3, 2)}
-    step_source = "eager launches"
-    if graph is not None:
-        ms_per_step = graph["us_per_step"] / 1e3
-        step_source = "CUDA-graph replay of the step"
-    peak, peak_src = hbm_peak()
+    total_bytes = case.total_bytes
     value = whole_job_gbps(total_bytes, ms_per_step, world)
-    achieved = total_bytes / (attn_mean * 1e-3) / 1e9
-    flops = step_flops(wl, args.window)
-    prefill = wl.group * wl.q_len > 128  # many query rows per KV head: compute-bound
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "us_per_step": round(ms_per_step * 1e3, 2),
-        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "pct_of_peak": round(100.0 * value / world / hbm[0], 2),
+        "pct_of_read_peak": round(100.0 * value / world / rpeak, 2),
+        "pct_of_nominal": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 KV (f16 products, fp32 softmax)" if kv8 else "bf16",
+        "dtype": "e4m3 KV (f16 products, fp32 softmax)" if case.kv8 else "bf16",
         "data": "synthetic",
         "config": {
             "workload": wl.name, "num_seqs": wl.num_seqs, "n_q": wl.n_q, "n_kv": wl.n_kv,
             "head_dim": wl.head_dim, "block_size": wl.block_size, "q_len": wl.q_len,
             "resident_tokens": wl.resident_tokens(), "bytes_per_step": total_bytes,
-            "kv_bytes": kv_bytes, "kv_dtype": args.kv, "window": args.window,
-            "l2": f"no flush: resident KV {kv_bytes / L2_BYTES:.1f}x the 129 MB L2",
-            "step": ("kv_append_fp8" if kv8 else "kv_append") +
+            "kv_bytes": case.kv_bytes, "kv_dtype": "e4m3" if case.kv8 else "bf16",
+            "window": case.window, "l2": L2Flush.describe,
+            "step": ("kv_append_fp8" if case.kv8 else "kv_append") +
                     " + paged_decode_attn (+ lse_merge)",
-            "timed_as": step_source,
+            "timed_as": "CUDA-graph replay of the step, one pair of events per step",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-            "step_us_p10_p50_p90": [round(1e3 * x, 2) for x in
-                                     statistics.quantiles(step_ms, n=10)[::4]] if K >= 10 else None,
+            "step_us_p10_p50_p90": head["step_us_p10_p50_p90"],
+            "attn_us_p10_p50_p90": head["attn_us_p10_p50_p90"],
+            "percentiles_over_steps": n_dist,
         },
-        "roofline": {
-            "kernel": "paged_decode_attn (attention + merge launches of one call)",
-            "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "flops_per_launch": flops,
-            "traffic": profiled_traffic(wl.name + ("/fp8" if kv8 else "") +
-                                        (f"/w{args.window}" if args.window else "")),
-            "peak_source": peak_src, "attn_us": round(attn_mean * 1e3, 2),
-            "algorithmic_bytes_per_launch": total_bytes,
-        },
+        "roofline": head["roofline"],
+        "read_peak_gbs": rpeak,
+        "read_peak": rpk,
+        "nominal_hbm_gbs": NOMINAL_HBM_GBS,
         "e2e": e2e,
-        "eager": eager,
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches,
+        "per_workload": per,
         "clocks": clk,
     }
-    if prefill:
-        # A prefill chunk is a dense contraction: its roofline is the tensor peak.
-        tpeak, tsrc = tensor_peak()
-        tflops = flops / (attn_mean * 1e-3) / 1e12
-        line["roofline"].update({"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak,
-                                 "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
-                                 "peak_source": tsrc,
-                                 "hbm_gbs_of_algorithmic_bytes": round(achieved, 2)})
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not kv8 and not args.window:
-        line["cpu_baseline"] = cpu_baseline(wl)
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -379,6 +379,20 @@ const char *pkv_status_string(int status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int pkv_version(void);
 
+/*
+ * Diagnostics (not part of the attention path).
+ *
+ * pkv_read_stream -- read `bytes` of device memory at `buf` once, with 16-byte
+ * vector loads from ctas_per_sm (1..4) CTAs of 512 threads per SM, and XOR
+ * the data into the device word *sink.  Its rate is a practical read peak of
+ * the device (a copy's rate counts reads and writes together), and reading
+ * more than the L2 holds evicts everything the L2 held before.
+ * buf 16-byte aligned, bytes a multiple of 16, sink 4-byte aligned.
+ * Returns PKV_OK, PKV_ERR_INVALID_ARG or PKV_ERR_CUDA; bytes == 0 launches nothing.
+ */
+int pkv_read_stream(const void *buf, size_t bytes, unsigned *sink, int ctas_per_sm,
+                    void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,4 +24,4 @@ from ._lib import (  # noqa: F401
     pkv_kv_bytes, pkv_paged_decode_attn, pkv_paged_decode_attn_ex, pkv_paged_decode_attn_noalloc,
     pkv_attn_params,
     pkv_paged_decode_attn_workspace_size,
-    pkv_status_string, pkv_version)
+    pkv_read_stream, pkv_status_string, pkv_version)

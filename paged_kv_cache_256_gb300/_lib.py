@@ -79,6 +79,7 @@ SIGNATURES = {
     "pkv_kv_bytes": ([_c_int] * 4 + [ctypes.c_int64], ctypes.c_int64),
     "pkv_status_string": ([_c_int], ctypes.c_char_p),
     "pkv_version": ([], _c_int),
+    "pkv_read_stream": ([_vp, _c_size, _vp, _c_int, _vp], _c_int),
 }
 
 
@@ -451,6 +452,19 @@ class BlockPool:
 
     def append_slots(self, table, nblocks, ctx, n_new):
         return pkv_pool_append_slots(self.handle, table, nblocks, ctx, n_new, self.block_size)
+
+
+def pkv_read_stream(buf, sink, ctas_per_sm=2, stream=None) -> None:
+    """Read all of `buf` (a contiguous CUDA tensor) once, XOR-folding it into `sink`
+    (an int32 CUDA tensor of one element): a read-bandwidth probe and L2 evictor."""
+    import torch
+    if not buf.is_cuda or not buf.is_contiguous() or sink.dtype != torch.int32 or \
+            not sink.is_cuda or sink.numel() < 1:
+        raise ValueError("buf must be a contiguous CUDA tensor and sink an int32 CUDA tensor")
+    nbytes = buf.numel() * buf.element_size()
+    _check(load_library().pkv_read_stream(buf.data_ptr(), nbytes - nbytes % 16, sink.data_ptr(),
+                                          int(ctas_per_sm), _stream_ptr(stream)),
+           "pkv_read_stream")
 
 
 def pkv_check_error(workspace, stream=None) -> int:
