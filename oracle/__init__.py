@@ -13,8 +13,10 @@ Functions (each follows the passage cited in ``pkv_oracle.c``):
 * :func:`attn_partial` -- (o, m, l) of one key range: the online-softmax state.
 * :func:`lse_merge`    -- exact combination of partials.
 * :func:`paged_attn_fp8` -- the same attention over an e4m3 cache with per-KV-head scales.
+* :func:`paged_attn_fp8_block` -- the same with one scale per (block, KV head).
 * :func:`kv_append`    -- bit copy of new K/V rows into their slots.
 * :func:`kv_append_fp8` -- quantising append into an e4m3 cache.
+* :func:`kv_append_fp8_block` -- quantising append that sets per-(block, KV head) scales.
 * :func:`e4m3_encode`, :func:`e4m3_decode` -- the 8-bit float codec.
 * :func:`copy_blocks`  -- whole-block copies (copy-on-write).
 * :func:`kv_bytes`     -- M_kv = 2 L n_kv d_h (s b) p.
@@ -77,6 +79,11 @@ class Oracle:
         lib.oracle_kv_append_fp8.argtypes = [u16p, u16p, i32p] + [c_int] * 5 + \
             [f32p, f32p, u8p]
         lib.oracle_kv_append_fp8.restype = c_int
+        lib.oracle_paged_attn_fp8_block.argtypes = [u16p, u8p, f32p, i32p, i32p] + \
+            [c_int] * 8 + [ctypes.c_double, c_int, f64p]
+        lib.oracle_paged_attn_fp8_block.restype = c_int
+        lib.oracle_kv_append_fp8_block.argtypes = [u16p, u16p, i32p] + [c_int] * 5 + [u8p, f32p]
+        lib.oracle_kv_append_fp8_block.restype = c_int
         lib.oracle_e4m3_encode.argtypes = [f32p, ctypes.c_long, u8p]
         lib.oracle_e4m3_encode.restype = None
         lib.oracle_e4m3_decode.argtypes = [u8p, ctypes.c_long, f64p]
@@ -149,6 +156,33 @@ class Oracle:
             bt.shape[1], num_blocks, float(scale), int(window), _ptr(out, ctypes.c_double))
         if st != 0:
             raise ValueError(f"oracle_paged_attn_fp8 rejected its inputs (status {st})")
+        return out
+
+    def paged_attn_fp8_block(self, q, kv_cache, kv_scales, block_tables, context_lens, *, n_q,
+                             n_kv, head_dim, block_size, scale, num_blocks=None, q_len=None,
+                             window=0):
+        """paged_attn over an e4m3 cache [num_blocks, n_kv, 2, block_size, head_dim] whose
+        scales are per (block, KV head): kv_scales fp32 [num_blocks, n_kv, 4] = (K scale,
+        V scale, reserved, reserved)."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        kv_cache = np.ascontiguousarray(kv_cache, dtype=np.uint8)
+        assert kv_cache.ndim == 5 and kv_cache.shape[2] == 2
+        sc = np.ascontiguousarray(kv_scales, dtype=np.float32)
+        assert sc.shape == (kv_cache.shape[0], n_kv, 4)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        num_seqs = cl.shape[0]
+        q_len = q.shape[1] if q_len is None else q_len
+        if num_blocks is None:
+            num_blocks = kv_cache.shape[0]
+        out = np.zeros((num_seqs, q_len, n_q, head_dim), dtype=np.float64)
+        st = self._lib.oracle_paged_attn_fp8_block(
+            _ptr(q, ctypes.c_uint16), _ptr(kv_cache, ctypes.c_uint8), _ptr(sc, ctypes.c_float),
+            _ptr(bt, ctypes.c_int32), _ptr(cl, ctypes.c_int32), num_seqs, q_len, n_q, n_kv,
+            head_dim, block_size, bt.shape[1], num_blocks, float(scale), int(window),
+            _ptr(out, ctypes.c_double))
+        if st != 0:
+            raise ValueError(f"oracle_paged_attn_fp8_block rejected its inputs (status {st})")
         return out
 
     def e4m3_encode(self, x):
@@ -235,6 +269,24 @@ class Oracle:
             _ptr(vs, ctypes.c_float), _ptr(kv_cache, ctypes.c_uint8))
         if st != 0:
             raise ValueError(f"oracle_kv_append_fp8 rejected its inputs (status {st})")
+
+    def kv_append_fp8_block(self, k_new, v_new, slot_mapping, kv_cache, kv_scales, *,
+                            block_size):
+        """In-place quantising scatter into an e4m3 cache [num_blocks, n_kv, 2, bs, d] (uint8)
+        with per-(block, KV head) scales kv_scales [num_blocks, n_kv, 4] (float32, updated)."""
+        k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+        v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int32)
+        assert kv_cache.flags.c_contiguous and kv_cache.dtype == np.uint8
+        assert kv_scales.flags.c_contiguous and kv_scales.dtype == np.float32
+        num_blocks, n_kv, two, bs, d = kv_cache.shape
+        assert two == 2 and bs == block_size and kv_scales.shape == (num_blocks, n_kv, 4)
+        st = self._lib.oracle_kv_append_fp8_block(
+            _ptr(k_new, ctypes.c_uint16), _ptr(v_new, ctypes.c_uint16), _ptr(sm, ctypes.c_int32),
+            sm.shape[0], n_kv, d, block_size, num_blocks, _ptr(kv_cache, ctypes.c_uint8),
+            _ptr(kv_scales, ctypes.c_float))
+        if st != 0:
+            raise ValueError(f"oracle_kv_append_fp8_block rejected its inputs (status {st})")
 
     def copy_blocks(self, pairs, k_cache, v_cache):
         """In-place whole-block copies: block pairs[p, 1] <- block pairs[p, 0]."""

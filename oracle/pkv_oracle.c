@@ -47,7 +47,12 @@
  *     head) the K rows, then the V rows;  A new value x is stored
  *     as the e4m3 code nearest to x / scale, the division taken in fp32 and
  *     ties going to the even code; quotients beyond the largest finite e4m3
- *     (448) store +-448.
+ *     (448) store +-448;
+ *   - the same 8-bit cache may instead carry one scale per (block, KV head)
+ *     for K and one for V, kept in [num_blocks][n_kv][4] fp32 (K scale, V
+ *     scale, two reserved words), so that a scale follows the values of its
+ *     own block.  The appending side sets them as written out at
+ *     oracle_kv_append_fp8_block.
  *
  * Parallelism: one OpenMP loop over independent (sequence, KV head) units.
  * Each unit is computed by one thread, start to finish, in sequential order,
@@ -143,6 +148,7 @@ typedef struct {
     const uint16_t *k16, *v16; /* bf16 caches, or NULL */
     const uint8_t *kv8;        /* e4m3 cache, or NULL */
     const float *k_scale, *v_scale;
+    const float *blk_scales;   /* e4m3 cache with per-(block, head) scales, or NULL */
 } cache_view;
 
 /*
@@ -164,10 +170,15 @@ static int gather_sequence(const cache_view *c, const int32_t *table_row, int ct
         /* e4m3: K row of (blk, g, off) and the V row block_size rows after it */
         size_t kbase8 = ((((size_t)blk * n_kv + g) * 2) * block_size + off) * head_dim;
         size_t vbase8 = kbase8 + (size_t)block_size * head_dim;
+        /* the scales of this token's values: its physical block's, or its head's */
+        const double ks = c->blk_scales ? (double)c->blk_scales[((size_t)blk * n_kv + g) * 4 + 0]
+                          : c->kv8      ? (double)c->k_scale[g] : 0.0;
+        const double vs = c->blk_scales ? (double)c->blk_scales[((size_t)blk * n_kv + g) * 4 + 1]
+                          : c->kv8      ? (double)c->v_scale[g] : 0.0;
         for (int e = 0; e < head_dim; ++e) {
             if (c->kv8) {
-                K[(size_t)t * head_dim + e] = e4m3_value(c->kv8[kbase8 + e]) * (double)c->k_scale[g];
-                V[(size_t)t * head_dim + e] = e4m3_value(c->kv8[vbase8 + e]) * (double)c->v_scale[g];
+                K[(size_t)t * head_dim + e] = e4m3_value(c->kv8[kbase8 + e]) * ks;
+                V[(size_t)t * head_dim + e] = e4m3_value(c->kv8[vbase8 + e]) * vs;
             } else {
                 K[(size_t)t * head_dim + e] = bf16_value(c->k16[base + e]);
                 V[(size_t)t * head_dim + e] = bf16_value(c->v16[base + e]);
@@ -270,7 +281,7 @@ int oracle_paged_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t
                       int block_size, int max_blocks_per_seq, int num_blocks,
                       double scale, int window, double *out)
 {
-    const cache_view c = {k_cache, v_cache, NULL, NULL, NULL};
+    const cache_view c = {k_cache, v_cache, NULL, NULL, NULL, NULL};
     return paged_attn(q, &c, block_tables, context_lens, num_seqs, q_len, n_q, n_kv, head_dim,
                       block_size, max_blocks_per_seq, num_blocks, scale, window, out);
 }
@@ -283,7 +294,23 @@ int oracle_paged_attn_fp8(const uint16_t *q, const uint8_t *kv_cache,
                           int block_size, int max_blocks_per_seq, int num_blocks,
                           double scale, int window, double *out)
 {
-    const cache_view c = {NULL, NULL, kv_cache, k_scale, v_scale};
+    const cache_view c = {NULL, NULL, kv_cache, k_scale, v_scale, NULL};
+    return paged_attn(q, &c, block_tables, context_lens, num_seqs, q_len, n_q, n_kv, head_dim,
+                      block_size, max_blocks_per_seq, num_blocks, scale, window, out);
+}
+
+/*
+ * The same attention over an e4m3 cache with one scale per (physical block,
+ * KV head): token t of sequence b in KV head g decodes as code * s, s the K
+ * (or V) scale of kv_scales[block_tables[b][t / block_size]][g].
+ */
+int oracle_paged_attn_fp8_block(const uint16_t *q, const uint8_t *kv_cache,
+                                const float *kv_scales, const int32_t *block_tables,
+                                const int32_t *context_lens, int num_seqs, int q_len, int n_q,
+                                int n_kv, int head_dim, int block_size, int max_blocks_per_seq,
+                                int num_blocks, double scale, int window, double *out)
+{
+    const cache_view c = {NULL, NULL, kv_cache, NULL, NULL, kv_scales};
     return paged_attn(q, &c, block_tables, context_lens, num_seqs, q_len, n_q, n_kv, head_dim,
                       block_size, max_blocks_per_seq, num_blocks, scale, window, out);
 }
@@ -457,6 +484,112 @@ int oracle_kv_append_fp8(const uint16_t *k_new, const uint16_t *v_new,
                 kv_cache[kdst + e] = e4m3_code(kq);
                 kv_cache[vdst + e] = e4m3_code(vq);
             }
+        }
+    }
+    return 0;
+}
+
+/*
+ * The quantising append into an e4m3 cache with per-(block, KV head) scales
+ * (layouts as for oracle_paged_attn_fp8_block).  Quantise and dequantise
+ * through a scale ("Efficient inference", Quantization: fewer bytes per
+ * weight; CS336 lecture-10 notes, Quantization & pruning), here one scale per
+ * block so that it follows the values of the block.  For every block B that
+ * receives tokens in this call and every KV head, separately for K and V:
+ *   - R = the call's tokens whose slots fall in B, o_min their lowest offset;
+ *     the rows below o_min are the block's resident rows;
+ *   - s_old = the stored scale if o_min > 0, else 0 (a block written from
+ *     offset 0 starts over); scale 0 means "no value but zeros so far";
+ *   - a = the largest finite |x| over R's rows (non-finite values are stored
+ *     as they encode: NaN as the NaN code, infinities saturated);
+ *   - s_new = s_old if a == 0, else the larger of s_old and 2^e, the smallest
+ *     power of two with e >= -126 and a <= 448 * 2^e;
+ *   - if s_new > s_old > 0, each resident row code c becomes
+ *     E(fp32(fp32(value(c) * s_old) / s_new)) -- with powers of two exact
+ *     except where the smaller value falls below the normal e4m3 range;
+ *   - each token of R, in call order, writes E(fp32(x / s_new)) at its
+ *     offset (E(x) itself when s_new == 0); a later token wins on a shared
+ *     offset;
+ *   - the scale entry becomes s_new (its two reserved words 0).
+ * E is e4m3_code.  Slots outside [0, num_blocks * block_size) are skipped.
+ */
+int oracle_kv_append_fp8_block(const uint16_t *k_new, const uint16_t *v_new,
+                               const int32_t *slot_mapping, int num_tokens, int n_kv,
+                               int head_dim, int block_size, int num_blocks,
+                               uint8_t *kv_cache, float *kv_scales)
+{
+    if (num_tokens < 0 || n_kv < 1 || head_dim < 1 || block_size < 1 || num_blocks < 0)
+        return 1;
+    const long nslots = (long)num_blocks * block_size;
+    for (int i = 0; i < num_tokens; ++i) {
+        const long slot = slot_mapping[i];
+        if (slot < 0 || slot >= nslots)
+            continue;
+        const long blk = slot / block_size;
+        /* each block once, at the first of its tokens in call order */
+        int seen = 0;
+        for (int j = 0; j < i; ++j) {
+            const long sj = slot_mapping[j];
+            if (sj >= 0 && sj < nslots && sj / block_size == blk)
+                seen = 1;
+        }
+        if (seen)
+            continue;
+        long o_min = block_size;
+        for (int j = i; j < num_tokens; ++j) {
+            const long sj = slot_mapping[j];
+            if (sj >= 0 && sj < nslots && sj / block_size == blk && sj % block_size < o_min)
+                o_min = sj % block_size;
+        }
+        for (int g = 0; g < n_kv; ++g) {
+            for (int which = 0; which < 2; ++which) { /* 0: K, 1: V */
+                const uint16_t *src = which == 0 ? k_new : v_new;
+                float *sc = kv_scales + ((size_t)blk * n_kv + g) * 4;
+                uint8_t *rows = kv_cache +
+                                (((size_t)blk * n_kv + g) * 2 + which) * (size_t)block_size * head_dim;
+                const float s_old = o_min > 0 ? sc[which] : 0.0f;
+                double a = 0.0;
+                for (int j = i; j < num_tokens; ++j) {
+                    const long sj = slot_mapping[j];
+                    if (sj < 0 || sj >= nslots || sj / block_size != blk)
+                        continue;
+                    for (int e = 0; e < head_dim; ++e) {
+                        const double x = bf16_value(src[((size_t)j * n_kv + g) * head_dim + e]);
+                        if (isfinite(x) && fabs(x) > a)
+                            a = fabs(x);
+                    }
+                }
+                float s_new = s_old;
+                if (a > 0.0) {
+                    int e = -126;
+                    while (ldexp(448.0, e) < a)
+                        ++e;
+                    const float s_req = (float)ldexp(1.0, e);
+                    if (s_req > s_new)
+                        s_new = s_req;
+                }
+                if (s_new > s_old && s_old > 0.0f) {
+                    for (long r = 0; r < o_min; ++r)
+                        for (int e = 0; e < head_dim; ++e) {
+                            uint8_t *cp = rows + (size_t)r * head_dim + e;
+                            const float v = (float)e4m3_value(*cp) * s_old;
+                            *cp = e4m3_code(v / s_new);
+                        }
+                }
+                for (int j = i; j < num_tokens; ++j) {
+                    const long sj = slot_mapping[j];
+                    if (sj < 0 || sj >= nslots || sj / block_size != blk)
+                        continue;
+                    for (int e = 0; e < head_dim; ++e) {
+                        const float x = (float)bf16_value(src[((size_t)j * n_kv + g) * head_dim + e]);
+                        rows[(size_t)(sj % block_size) * head_dim + e] =
+                            e4m3_code(s_new > 0.0f ? x / s_new : x);
+                    }
+                }
+                sc[which] = s_new;
+            }
+            kv_scales[((size_t)blk * n_kv + g) * 4 + 2] = 0.0f;
+            kv_scales[((size_t)blk * n_kv + g) * 4 + 3] = 0.0f;
         }
     }
     return 0;

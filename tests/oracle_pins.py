@@ -42,6 +42,23 @@ What pins what:
   on the K/V that torch dequantises (code value times the head's scale).
 * ``pin_kv_append_fp8``     -- the quantising append against numpy's fp32
   division and torch's encoder.
+* ``pin_fp8_block_attention_sdpa`` -- attention over an e4m3 cache with one
+  scale per (block, KV head) equals torch SDPA on K/V the test dequantises
+  itself, logical block by logical block; unused blocks carry NaN scales.
+* ``pin_fp8_block_equals_per_head`` -- block scales that are the same for every
+  block of a head give the per-head result bit for bit.
+* ``pin_fp8_block_append_fresh`` -- a block written from offset 0: its scale is
+  the smallest power of two that keeps every finite value within 448 (checked
+  as an inequality, not recomputed), the codes are torch's encoding of the fp32
+  quotients, non-finite values are stored as they encode, all-zero blocks
+  keep scale 0.
+* ``pin_fp8_block_append_growth`` -- a later token with larger values raises
+  the scale by a power of two: resident rows keep their exact value where it
+  stays in the normal e4m3 range and move by at most half a subnormal step
+  below it; rows past the new tokens are not touched; smaller values leave the
+  scale and the resident rows alone.
+* ``pin_fp8_block_append_then_attend`` -- bf16 rows appended through the block
+  scales and attended over stay within the e4m3 rounding of the bf16 result.
 """
 from __future__ import annotations
 
@@ -595,11 +612,219 @@ def pin_kv_append_fp8(orc):
         assert np.array_equal(got, ref)
 
 
+# ---------------------------------------------------------------------------
+# 8-bit cache with one scale per (block, KV head)
+# ---------------------------------------------------------------------------
+def _fp8_block_case(rng, ctxs, n_q, n_kv, d, bs, q_len):
+    """Codes as in _fp8_case, plus a K and a V scale per logical block of every sequence,
+    placed into the physical scale tensor by the test; unused blocks get NaN scales."""
+    c = _fp8_case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+    pool = c["kv_cache"].shape[0]
+    scales = np.full((pool, n_kv, 4), np.nan, dtype=np.float32)
+    logical = []  # per sequence: [n_kv][nblocks][2] scales
+    for b, ctx in enumerate(ctxs):
+        nb = math.ceil(ctx / bs)
+        ls = rng.uniform(0.001, 0.08, size=(n_kv, nb, 2)).astype(np.float32)
+        logical.append(ls)
+        for j in range(nb):
+            scales[c["block_tables"][b, j], :, 0:2] = ls[:, j, :]
+            scales[c["block_tables"][b, j], :, 2:4] = 0.0
+    c["scales"], c["logical_scales"] = scales, logical
+    return c
+
+
+def pin_fp8_block_attention_sdpa(orc):
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(47)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES:
+        c = _fp8_block_case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        G = n_q // n_kv
+        for window in (0, 5):
+            got = orc.paged_attn_fp8_block(c["q"], c["kv_cache"], c["scales"],
+                                           c["block_tables"], c["context_lens"], n_q=n_q,
+                                           n_kv=n_kv, head_dim=d, block_size=bs, scale=0.2,
+                                           window=window)
+            for b, ctx in enumerate(ctxs):
+                ls = c["logical_scales"][b].astype(np.float64)      # [n_kv][nb][2]
+                tok = np.arange(ctx) // bs                           # logical block of token t
+                q = torch.from_numpy(bf16_bits_to_f32(c["q"][b]).astype(np.float64))
+                k = torch.from_numpy(_torch_e4m3_value(c["K"][b]) * ls[:, tok, 0][:, :, None])
+                v = torch.from_numpy(_torch_e4m3_value(c["V"][b]) * ls[:, tok, 1][:, :, None])
+                k, v = k.repeat_interleave(G, dim=0), v.repeat_interleave(G, dim=0)
+                pos = ctx - q_len + torch.arange(q_len)
+                t = torch.arange(ctx)[None, :]
+                mask = t <= pos[:, None]
+                if window:
+                    mask &= t > pos[:, None] - window
+                ref = F.scaled_dot_product_attention(q.permute(1, 0, 2)[None], k[None], v[None],
+                                                     attn_mask=mask[None, None], scale=0.2)[0]
+                ref = ref.permute(1, 0, 2).numpy()
+                rows_seen = mask.any(dim=1).numpy()
+                np.testing.assert_allclose(got[b][rows_seen], ref[rows_seen], rtol=1e-12,
+                                           atol=1e-12)
+
+
+def pin_fp8_block_equals_per_head(orc):
+    rng = np.random.default_rng(48)
+    for ctxs, n_q, n_kv, d, bs, q_len in SHAPES[:4]:
+        c = _fp8_case(rng, ctxs, n_q, n_kv, d, bs, q_len)
+        pool = c["kv_cache"].shape[0]
+        scales = np.zeros((pool, n_kv, 4), dtype=np.float32)
+        scales[:, :, 0], scales[:, :, 1] = c["ks"][None, :], c["vs"][None, :]
+        kw = dict(n_q=n_q, n_kv=n_kv, head_dim=d, block_size=bs, scale=0.3)
+        a = orc.paged_attn_fp8_block(c["q"], c["kv_cache"], scales, c["block_tables"],
+                                     c["context_lens"], **kw)
+        b = orc.paged_attn_fp8(c["q"], c["kv_cache"], c["ks"], c["vs"], c["block_tables"],
+                               c["context_lens"], **kw)
+        assert np.array_equal(a, b)
+
+
+def _pow2_exponent(x):
+    """e with x == 2^e exactly, or None."""
+    m, e = math.frexp(float(x))
+    return e - 1 if m == 0.5 else None
+
+
+def _check_block_scale(s, rows_f32):
+    """The stored scale of a block whose new values are rows_f32 (no resident rows)."""
+    fin = rows_f32[np.isfinite(rows_f32)]
+    a = float(np.abs(fin).max()) if fin.size else 0.0
+    if a == 0.0:
+        assert s == 0.0, s
+        return
+    e = _pow2_exponent(s)
+    assert e is not None and e >= -126, s
+    assert a <= 448.0 * s, (a, s)                        # nothing saturates ...
+    assert e == -126 or a > 224.0 * s, (a, s)            # ... and half the scale would
+
+
+def pin_fp8_block_append_fresh(orc):
+    rng = np.random.default_rng(49)
+    n_kv, d, bs, pool = 2, 16, 4, 6
+    kv = rng.integers(0, 256, size=(pool, n_kv, 2, bs, d), dtype=np.uint8)
+    scales = rng.uniform(1.0, 5.0, size=(pool, n_kv, 4)).astype(np.float32)  # stale entries
+    # block 1 gets offsets 0..2 (a run), block 4 offset 0 with all-zero rows, block 3
+    # offset 0 with non-finite values and tiny ones; -1 and out-of-range slots skipped
+    slots = np.asarray([4, 5, 6, -1, 16, 12, pool * bs], dtype=np.int32)
+    T = slots.shape[0]
+    kx = rng.standard_normal((T, n_kv, d)).astype(np.float32) * np.float32(3.0)
+    vx = rng.standard_normal((T, n_kv, d)).astype(np.float32) * np.float32(0.01)
+    kx[4], vx[4] = 0.0, -0.0
+    kx[5, 0, :4] = [np.nan, np.inf, -np.inf, 1e-3]
+    kx[5, 1] = np.float32(2.0 ** -135)
+    kn, vn = f32_to_bf16_bits(kx), f32_to_bf16_bits(vx)
+    kn[5, 0, 0] = 0x7FC0
+    got_kv, got_sc = kv.copy(), scales.copy()
+    orc.kv_append_fp8_block(kn, vn, slots, got_kv, got_sc, block_size=bs)
+    touched = {1: [0, 1, 2], 4: [4], 3: [5]}
+    for blk, toks in touched.items():
+        for g in range(n_kv):
+            for which, bits in ((0, kn), (1, vn)):
+                x = bf16_bits_to_f32(bits[toks, g, :])
+                s = float(got_sc[blk, g, which])
+                _check_block_scale(s, x)
+                q = x / np.float32(s) if s > 0 else x               # fp32 division
+                want = _torch_e4m3(np.clip(q, np.float32(-464.0), np.float32(464.0)))
+                want = np.where(np.isinf(q), np.where(q < 0, 0xFE, 0x7E), want)
+                want = np.where(np.isnan(q), 0x7F, want)
+                offs = [int(slots[t]) % bs for t in toks]
+                assert np.array_equal(got_kv[blk, g, which, offs], want.astype(np.uint8)), \
+                    (blk, g, which)
+            assert got_sc[blk, g, 2] == 0.0 and got_sc[blk, g, 3] == 0.0
+    assert got_sc[4, 0, 0] == 0.0 and got_sc[4, 1, 1] == 0.0   # all zeros: scale 0
+    # untouched blocks and the untouched rows of touched blocks keep their bytes
+    for blk in range(pool):
+        if blk not in touched:
+            assert np.array_equal(got_kv[blk], kv[blk]) and np.array_equal(got_sc[blk], scales[blk])
+    assert np.array_equal(got_kv[1, :, :, 3], kv[1, :, :, 3])
+    assert np.array_equal(got_kv[4, :, :, 1:], kv[4, :, :, 1:])
+
+
+def pin_fp8_block_append_growth(orc):
+    rng = np.random.default_rng(50)
+    n_kv, d, bs, pool = 2, 32, 8, 3
+    finite = np.asarray([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    for k in (1, 3, 9):
+        kv = rng.choice(finite, size=(pool, n_kv, 2, bs, d)).astype(np.uint8)
+        s_old = np.float32(2.0 ** -6)
+        scales = np.zeros((pool, n_kv, 4), dtype=np.float32)
+        scales[:, :, 0:2] = s_old
+        # block 2 holds 3 resident rows; the new token at offset 3 needs 2^k times the range
+        x = rng.standard_normal((1, n_kv, d)).astype(np.float32)
+        x *= np.float32(448.0 * float(s_old) * 2.0 ** k * 0.9) / np.abs(x).max(axis=2, keepdims=True)
+        slots = np.asarray([2 * bs + 3], dtype=np.int32)
+        kn = vn = f32_to_bf16_bits(x)
+        got_kv, got_sc = kv.copy(), scales.copy()
+        orc.kv_append_fp8_block(kn, vn, slots, got_kv, got_sc, block_size=bs)
+        for g in range(n_kv):
+            for which in (0, 1):
+                s_new = float(got_sc[2, g, which])
+                assert s_new == float(s_old) * 2.0 ** k, (k, s_new)
+                old_v = _torch_e4m3_value(kv[2, g, which, :3]) * float(s_old)
+                new_v = _torch_e4m3_value(got_kv[2, g, which, :3]) * s_new
+                normal = np.abs(old_v) >= 2.0 ** -6 * s_new
+                assert np.array_equal(new_v[normal], old_v[normal]), (k, g, which)
+                assert np.all(np.abs(new_v - old_v) <= 2.0 ** -10 * s_new), (k, g, which)
+                # rows past the new token are not resident: untouched
+                assert np.array_equal(got_kv[2, g, which, 4:], kv[2, g, which, 4:])
+        assert np.array_equal(got_kv[:2], kv[:2]) and np.array_equal(got_sc[:2], scales[:2])
+    # smaller values: the scale and the resident rows stay
+    kv = rng.choice(finite, size=(pool, n_kv, 2, bs, d)).astype(np.uint8)
+    scales = np.full((pool, n_kv, 4), 2.0 ** -3, dtype=np.float32)
+    small = f32_to_bf16_bits(rng.standard_normal((1, n_kv, d)).astype(np.float32) * 1e-3)
+    got_kv, got_sc = kv.copy(), scales.copy()
+    orc.kv_append_fp8_block(small, small, np.asarray([bs + 5], np.int32), got_kv, got_sc,
+                            block_size=bs)
+    assert np.all(got_sc[1, :, 0:2] == np.float32(2.0 ** -3))
+    assert np.array_equal(got_kv[1, :, :, :5], kv[1, :, :, :5])
+    assert np.array_equal(got_kv[1, :, :, 6:], kv[1, :, :, 6:])
+
+
+def pin_fp8_block_append_then_attend(orc):
+    """Rows appended one decode step at a time through the block scales, then attended over:
+    within the e4m3 rounding (relative 2^-4 per value) of attention over the bf16 rows."""
+    rng = np.random.default_rng(51)
+    n_q, n_kv, d, bs = 4, 2, 16, 4
+    ctxs = [3, 9, 14]
+    pool = 12
+    perm = rng.permutation(pool).astype(np.int32)
+    bt = np.zeros((len(ctxs), 4), dtype=np.int32)
+    o = 0
+    for b, c in enumerate(ctxs):
+        nb = math.ceil(c / bs)
+        bt[b, :nb] = perm[o:o + nb]
+        bt[b, nb:] = perm[-1]
+        o += nb
+    kv = np.full((pool, n_kv, 2, bs, d), E4M3_NAN, dtype=np.uint8)
+    sc = np.full((pool, n_kv, 4), np.nan, dtype=np.float32)
+    k16 = np.full((pool, n_kv, bs, d), BF16_POISON, dtype=np.uint16)
+    v16 = np.full_like(k16, BF16_POISON)
+    for t in range(max(ctxs)):                     # one token per live sequence per step
+        live = [b for b, c in enumerate(ctxs) if t < c]
+        slots = np.asarray([bt[b, t // bs] * bs + t % bs for b in live], dtype=np.int32)
+        growth = np.float32(2.0 ** (t % 5))        # values that grow and shrink over time
+        kn = _rand_bf16(rng, (len(live), n_kv, d), growth)
+        vn = _rand_bf16(rng, (len(live), n_kv, d), 4.0 / growth)
+        orc.kv_append_fp8_block(kn, vn, slots, kv, sc, block_size=bs)
+        orc.kv_append(kn, vn, slots, k16, v16, block_size=bs)
+    q = _rand_bf16(rng, (len(ctxs), 1, n_q, d), 0.3)
+    kw = dict(n_q=n_q, n_kv=n_kv, head_dim=d, block_size=bs, scale=0.25)
+    got = orc.paged_attn_fp8_block(q, kv, sc, bt, np.asarray(ctxs, np.int32), **kw)
+    ref = orc.paged_attn(q, k16, v16, bt, np.asarray(ctxs, np.int32), **kw)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref)
+    assert np.all(err <= 0.25 * np.abs(ref) + 0.25), float(err.max())
+    assert np.mean(err) < 0.1, float(np.mean(err))
+
+
 ALL_PINS = [
     pin_library_sdpa, pin_numpy_dense, pin_equal_scores_mean, pin_single_token, pin_hardmax,
     pin_block_permutation, pin_gqa_equals_repeated_mha, pin_causal_rows, pin_window_sdpa,
     pin_window_extremes, pin_prefill_sdpa, pin_empty_context,
     pin_merge_exact, pin_kv_append, pin_copy_blocks, pin_append_then_attend, pin_kv_bytes_golden,
     pin_gqa_ratio, pin_e4m3_decode_library, pin_e4m3_encode_library, pin_e4m3_saturation,
-    pin_fp8_attention_sdpa, pin_kv_append_fp8,
+    pin_fp8_attention_sdpa, pin_kv_append_fp8, pin_fp8_block_attention_sdpa,
+    pin_fp8_block_equals_per_head, pin_fp8_block_append_fresh, pin_fp8_block_append_growth,
+    pin_fp8_block_append_then_attend,
 ]

@@ -45,10 +45,10 @@ MUTANTS = {
     "e4m3_ties_away": ("(long)rint(ldexp(a, 3 - e))", "(long)floor(ldexp(a, 3 - e) + 0.5)"),
     "e4m3_saturates_late": ("    if (a >= 448.0) {", "    if (a >= 480.0) {"),
     "e4m3_overflow_to_nan": ("code = 0x7E; /* the largest finite code", "code = 0x7F; /* the largest finite code"),
-    "fp8_k_scale_dropped": ("e4m3_value(c->kv8[kbase8 + e]) * (double)c->k_scale[g]",
-                            "e4m3_value(c->kv8[kbase8 + e])"),
-    "fp8_v_uses_k_scale": ("e4m3_value(c->kv8[vbase8 + e]) * (double)c->v_scale[g]",
-                           "e4m3_value(c->kv8[vbase8 + e]) * (double)c->k_scale[g]"),
+    "fp8_k_scale_dropped": (": c->kv8      ? (double)c->k_scale[g] : 0.0;",
+                            ": c->kv8      ? 1.0 : 0.0;"),
+    "fp8_v_uses_k_scale": (": c->kv8      ? (double)c->v_scale[g] : 0.0;",
+                           ": c->kv8      ? (double)c->k_scale[g] : 0.0;"),
     "fp8_v_rows_not_offset": ("size_t vbase8 = kbase8 + (size_t)block_size * head_dim;",
                               "size_t vbase8 = kbase8;"),
     "fp8_append_head0_scale": ("/ k_scale[g];", "/ k_scale[0];"),
@@ -59,6 +59,32 @@ MUTANTS = {
                               "const long first_l = window > 0 ? pos - window + 2 : 0;"),
     "window_ignored": ("const long first_l = window > 0 ? pos - window + 1 : 0;",
                        "const long first_l = 0;"),
+    "fp8_block_no_requantise": ("if (s_new > s_old && s_old > 0.0f) {", "if (0) {"),
+    "fp8_block_ignores_restart": ("const float s_old = o_min > 0 ? sc[which] : 0.0f;",
+                                  "const float s_old = sc[which];"),
+    "fp8_block_scale_too_small": ("while (ldexp(448.0, e) < a)", "while (ldexp(224.0, e) < a)"),
+    "fp8_block_scale_too_large": ("const float s_req = (float)ldexp(1.0, e);",
+                                  "const float s_req = (float)ldexp(1.0, e + 1);"),
+    "fp8_block_attn_logical_scale": (
+        "(double)c->blk_scales[((size_t)blk * n_kv + g) * 4 + 0]",
+        "(double)c->blk_scales[((size_t)(t / block_size) * n_kv + g) * 4 + 0]"),
+    "fp8_block_v_uses_k_scale": ("(double)c->blk_scales[((size_t)blk * n_kv + g) * 4 + 1]",
+                                 "(double)c->blk_scales[((size_t)blk * n_kv + g) * 4 + 0]"),
+    "fp8_block_requantise_all_rows": ("for (long r = 0; r < o_min; ++r)",
+                                      "for (long r = 0; r < block_size; ++r)"),
+    "fp8_block_amax_first_token_only": (
+        "                for (int j = i; j < num_tokens; ++j) {\n"
+        "                    const long sj = slot_mapping[j];\n"
+        "                    if (sj < 0 || sj >= nslots || sj / block_size != blk)\n"
+        "                        continue;\n"
+        "                    for (int e = 0; e < head_dim; ++e) {\n"
+        "                        const double x",
+        "                for (int j = i; j < i + 1; ++j) {\n"
+        "                    const long sj = slot_mapping[j];\n"
+        "                    if (sj < 0 || sj >= nslots || sj / block_size != blk)\n"
+        "                        continue;\n"
+        "                    for (int e = 0; e < head_dim; ++e) {\n"
+        "                        const double x"),
     "copy_direction_swapped": ("memcpy(k_cache + (size_t)dst * per_block, k_cache + (size_t)src * per_block,",
                                "memcpy(k_cache + (size_t)src * per_block, k_cache + (size_t)dst * per_block,"),
 }
