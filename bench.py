@@ -68,7 +68,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_gqa")
-    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16")
+    ap.add_argument("--kv", choices=["bf16", "fp8", "fp8blk"], default="bf16")
     ap.add_argument("--window", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -327,7 +327,9 @@ PER_WORKLOAD = [
     ("mqa_spec_verify", "mqa_spec_verify", "bf16", 0),
     ("long_splitk", "long_splitk", "bf16", 0),
     ("llama3_8b_gqa/e4m3", "llama3_8b_gqa", "fp8", 0),
+    ("llama3_8b_gqa/e4m3_block_scales", "llama3_8b_gqa", "fp8blk", 0),
     ("mqa_spec_verify/e4m3", "mqa_spec_verify", "fp8", 0),
+    ("mqa_spec_verify/e4m3_block_scales", "mqa_spec_verify", "fp8blk", 0),
     ("llama3_8b_chunked_prefill", "llama3_8b_chunked_prefill", "bf16", 0),
     ("llama3_8b_chunked_prefill/e4m3", "llama3_8b_chunked_prefill", "fp8", 0),
 ]
@@ -396,15 +398,24 @@ class Case:
         import torch
         import paged_kv_cache_256_gb300 as pkv
         from paged_kv_cache_256_gb300.device import fp8_to_device, to_device
-        from paged_kv_cache_256_gb300.workloads import fp8_cache_for, make_workload
+        from paged_kv_cache_256_gb300.workloads import (fp8_block_scales_for, fp8_cache_for,
+                                                        make_workload)
         self.pkv, self.device = pkv, device
         self.wl = wl = make_workload(name)
-        self.kv8 = kv == "fp8"
+        self.kv8 = kv in ("fp8", "fp8blk")
+        self.blk = kv == "fp8blk"
+        self.kv_name = {"bf16": "bf16", "fp8": "e4m3", "fp8blk": "e4m3, per-block scales"}[kv]
         self.window = window
         self.total_bytes, self.kv_bytes = step_bytes(wl, 1 if self.kv8 else 2, window)
+        if self.blk:  # each (block, KV head) read also brings its 16-byte scale entry
+            import numpy as np
+            nblk = (wl.context_lens.astype(np.int64) + wl.block_size - 1) // wl.block_size
+            self.total_bytes += 16 * wl.n_kv * int(nblk.sum())
         self.flops = step_flops(wl, window)
         self.dw = to_device(wl, device)
         self.d8 = fp8_to_device(fp8_cache_for(wl), device) if self.kv8 else None
+        self.dsc = (torch.from_numpy(fp8_block_scales_for(wl)).to(device) if self.blk
+                    else None)
         if self.kv8:  # the bf16 caches are not used by this step
             self.dw.k_cache = self.dw.v_cache = None
             torch.cuda.empty_cache()
@@ -417,7 +428,10 @@ class Case:
 
     def append(self, s):
         pkv, dw, d8 = self.pkv, self.dw, self.d8
-        if self.kv8:
+        if self.blk:
+            pkv.pkv_kv_append_fp8_block(dw.k_new, dw.v_new, dw.slot_mapping, d8.kv_cache,
+                                        self.dsc, stream=s)
+        elif self.kv8:
             pkv.pkv_kv_append_fp8(dw.k_new, dw.v_new, dw.slot_mapping, d8.kv_cache, d8.k_scale,
                                   d8.v_scale, stream=s)
         else:
@@ -426,7 +440,11 @@ class Case:
 
     def attend(self, s):
         pkv, dw, d8, wl = self.pkv, self.dw, self.d8, self.wl
-        if self.kv8:
+        if self.blk:
+            pkv.pkv_paged_decode_attn_ex(dw.q, d8.kv_cache, None, dw.block_tables,
+                                         dw.context_lens, wl.scale, self.out, self.ws, stream=s,
+                                         window=self.window, kv_scales=self.dsc)
+        elif self.kv8:
             pkv.pkv_paged_decode_attn_ex(dw.q, d8.kv_cache, None, dw.block_tables,
                                          dw.context_lens, wl.scale, self.out, self.ws, stream=s,
                                          window=self.window, k_scale=d8.k_scale,
@@ -487,7 +505,7 @@ class Case:
     def release(self):
         import torch
         self.graphs = None
-        self.dw = self.d8 = self.ws = self.out = None
+        self.dw = self.d8 = self.dsc = self.ws = self.out = None
         torch.cuda.synchronize(self.device)
         torch.cuda.empty_cache()
 
@@ -495,7 +513,8 @@ class Case:
 def roofline_of(case, attn_ms, hbm, rpeak):
     """Roofline of the attention call (attention + merge launches) from its mean time."""
     achieved = case.total_bytes / (attn_ms * 1e-3) / 1e9
-    key = case.wl.name + ("/fp8" if case.kv8 else "") + (f"/w{case.window}" if case.window else "")
+    key = case.wl.name + ("/fp8blk" if case.blk else "/fp8" if case.kv8 else "") + \
+        (f"/w{case.window}" if case.window else "")
     r = {"kernel": "paged_decode_attn (attention + merge launches of one call)", "bound": "hbm",
          "achieved": round(achieved, 2), "peak": hbm[0], "unit": "GB/s",
          "frac": round(achieved / hbm[0], 4),
@@ -523,7 +542,7 @@ def workload_line(case, step_ms, attn_ms, hbm, rpeak, world):
     return {
         "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "n_q": wl.n_q, "n_kv": wl.n_kv,
                    "head_dim": wl.head_dim, "block_size": wl.block_size, "q_len": wl.q_len,
-                   "kv_dtype": "e4m3" if case.kv8 else "bf16", "window": case.window,
+                   "kv_dtype": case.kv_name, "window": case.window,
                    "resident_tokens": wl.resident_tokens(), "bytes_per_step": case.total_bytes},
         "us_per_step": round(mean_step * 1e3, 2),
         "step_us_p10_p50_p90": pctl(step_ms),
@@ -628,7 +647,7 @@ def run_ours(args):
     e2e = None if args.no_e2e else e2e_of(case, K, world)
     wl = case.wl
     launches = case.launches_per_step * K
-    headline_case = (wl.name, case.kv8, case.window)
+    headline_case = (wl.name, args.kv, case.window)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not case.kv8 and \
             not args.window:
@@ -639,7 +658,7 @@ def run_ours(args):
     per = {}
     if not args.only:
         for key, name, kv, window in PER_WORKLOAD:
-            if (name, kv == "fp8", window) == headline_case:
+            if (name, kv, window) == headline_case:
                 continue
             c = Case(name, kv, window, device)
             c.capture(args.warmup)
@@ -666,9 +685,10 @@ def run_ours(args):
             "workload": wl.name, "num_seqs": wl.num_seqs, "n_q": wl.n_q, "n_kv": wl.n_kv,
             "head_dim": wl.head_dim, "block_size": wl.block_size, "q_len": wl.q_len,
             "resident_tokens": wl.resident_tokens(), "bytes_per_step": total_bytes,
-            "kv_bytes": case.kv_bytes, "kv_dtype": "e4m3" if case.kv8 else "bf16",
+            "kv_bytes": case.kv_bytes, "kv_dtype": case.kv_name,
             "window": case.window, "l2": L2Flush.describe,
-            "step": ("kv_append_fp8" if case.kv8 else "kv_append") +
+            "step": ("kv_append_fp8_block" if case.blk else "kv_append_fp8" if case.kv8
+                     else "kv_append") +
                     " + paged_decode_attn (+ lse_merge)",
             "timed_as": "CUDA-graph replay of the step, one pair of events per step",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",

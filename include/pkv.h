@@ -59,6 +59,7 @@ typedef enum pkv_status {
 /* kv_dtype values (pkv_attn_params). */
 #define PKV_KV_BF16 0     /* caches hold bf16 */
 #define PKV_KV_FP8_E4M3 1 /* caches hold e4m3 codes with per-KV-head scales */
+#define PKV_KV_FP8_E4M3_BLOCK 2 /* e4m3 codes with one scale per (block, KV head) */
 
 /* out_dtype values. */
 #define PKV_OUT_BF16 0 /* round-to-nearest-even bf16 */
@@ -78,6 +79,9 @@ typedef enum pkv_status {
  * context_lens included, before that kernel has completed.  For callers whose
  * preceding kernel signals early completion and writes context_lens. */
 #define PKV_FLAG_NO_EARLY_START 0x8u
+/* pkv_copy_blocks: the 8-bit cache has per-(block, KV head) scales; v_cache
+ * is then its scale tensor, copied with the blocks (needs PKV_FLAG_KV_FP8). */
+#define PKV_FLAG_KV_BLOCK_SCALES 0x10u
 /* Bits 16..31 force the number of attention CTAs (0 = one per SM).  Tests
  * use it to move where long contexts are split; results stay within the
  * stated tolerance for every value. */
@@ -178,6 +182,15 @@ int pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cach
  *   The cache pointer must be 16-byte aligned.  k_scale / v_scale are
  *   ignored for PKV_KV_BF16.  Any other kv_dtype, a non-NULL v_cache with an
  *   8-bit cache or a NULL one with bf16, returns PKV_ERR_INVALID_ARG.
+ *   PKV_KV_FP8_E4M3_BLOCK: the same 8-bit cache, but each (block, KV head)
+ *   has its own scales, so a scale follows the values of its block
+ *   (pkv_kv_append_fp8_block sets them):
+ *       kv_scales [num_blocks][n_kv][4]   fp32, 16-byte aligned
+ *   holding the K scale, the V scale and two reserved words per (block,
+ *   head).  Token t of sequence b decodes as code * the scale of block
+ *   block_tables[b][t / block_size].  k_scale / v_scale are ignored; a NULL
+ *   or misaligned kv_scales returns PKV_ERR_INVALID_ARG.  A block id outside
+ *   [0, num_blocks) reads zero codes and zero scales (as for bf16).
  * Every other field, the layouts and the return codes are those of
  * pkv_paged_decode_attn.  `p` is read during the call only.
  */
@@ -205,6 +218,7 @@ typedef struct pkv_attn_params {
     int kv_dtype;
     const float *k_scale;
     const float *v_scale;
+    const float *kv_scales; /* PKV_KV_FP8_E4M3_BLOCK only */
 } pkv_attn_params;
 
 int pkv_paged_decode_attn_ex(const pkv_attn_params *p, void *stream);
@@ -294,6 +308,50 @@ int pkv_kv_append_fp8(const void *k_new, const void *v_new, const int32_t *slot_
                       unsigned flags, void *stream);
 
 /*
+ * pkv_kv_append_fp8_block -- quantising append into an 8-bit (e4m3) cache
+ * whose scales are per (block, KV head) (PKV_KV_FP8_E4M3_BLOCK).
+ *
+ * Quantise through a scale ("Efficient inference", Quantization: fewer bytes
+ * per weight; CS336 lecture-10 notes, Quantization & pruning: bf16 -> fp8),
+ * with the scale kept per block so that it follows the data.  For every
+ * block B that receives tokens in this call and every KV head, for K and V
+ * separately:
+ *   - the run = the call's tokens whose slots fall in B, o_min their lowest
+ *     offset; rows below o_min are the block's resident rows;
+ *   - s_old = the stored scale if o_min > 0, else 0 (a block written from
+ *     offset 0 starts over); scale 0 means "nothing but zeros so far";
+ *   - a = the largest finite |x| of the run's new rows;
+ *   - s_new = s_old if a == 0, else the larger of s_old and 2^e, the smallest
+ *     power of two (e >= -126) with a <= 448 * 2^e, so no new value saturates;
+ *   - if s_new > s_old > 0 the resident rows are re-quantised: code c becomes
+ *     the e4m3 nearest to fp32(fp32(value(c) * s_old) / s_new) -- exact, the
+ *     ratio being a power of two, except where a value falls below the
+ *     normal e4m3 range (2^-6 * s_new);
+ *   - each new row stores the e4m3 nearest to fp32(x / s_new) (ties to even;
+ *     NaN stores 0x7F, infinities +-448; with s_new == 0 every value is 0 or
+ *     non-finite and stores its own code); the scale entry becomes s_new and
+ *     its two reserved words 0.
+ * Precondition: the tokens that land in one block are consecutive entries of
+ *   slot_mapping, ignoring skipped slots (as they are when each sequence's
+ *   new tokens are listed together, in order).  Otherwise two parts of the
+ *   call update the same block at once and its codes and scale are
+ *   unspecified; nothing outside that block changes.  Two tokens naming the
+ *   same slot leave the later one's row.
+ * k_new, v_new [num_tokens][n_kv][head_dim] bf16 (head_dim a multiple of 8,
+ *   at most 1024); slot_mapping [num_tokens] int32; kv_cache the interleaved
+ *   cache [num_blocks][n_kv][2][block_size][head_dim] (16-byte aligned);
+ *   kv_scales [num_blocks][n_kv][4] fp32 (16-byte aligned), read and written.
+ * A freshly allocated block needs no initialisation (its first token lands at
+ *   offset 0).  flags: reserved, pass 0.
+ * Returns PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED (more than 2^31
+ * rows or slots) or PKV_ERR_CUDA; num_tokens == 0 launches nothing.
+ */
+int pkv_kv_append_fp8_block(const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                            int num_tokens, int n_kv, int head_dim, int block_size,
+                            int num_blocks, void *kv_cache, float *kv_scales, unsigned flags,
+                            void *stream);
+
+/*
  * pkv_copy_blocks -- copy whole physical blocks (every KV head, K and V).
  *
  * For each pair p < num_pairs: block pairs[2p+1] of k_cache and of v_cache
@@ -307,7 +365,9 @@ int pkv_kv_append_fp8(const void *k_new, const void *v_new, const int32_t *slot_
  *   also be a source in the same call.
  * Caches as for pkv_paged_decode_attn (head_dim a multiple of 8); with
  * PKV_FLAG_KV_FP8 in flags, k_cache is the interleaved 8-bit cache (each
- * block holds K and V) and v_cache must be NULL.
+ * block holds K and V) and v_cache must be NULL -- or, with
+ * PKV_FLAG_KV_BLOCK_SCALES as well, the cache's [num_blocks][n_kv][4] fp32
+ * scale tensor (16-byte aligned), whose entries are copied with the blocks.
  * Returns PKV_OK, PKV_ERR_INVALID_ARG or PKV_ERR_CUDA; num_pairs == 0 launches nothing.
  */
 int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,

@@ -521,26 +521,40 @@ int oracle_kv_append_fp8_block(const uint16_t *k_new, const uint16_t *v_new,
     if (num_tokens < 0 || n_kv < 1 || head_dim < 1 || block_size < 1 || num_blocks < 0)
         return 1;
     const long nslots = (long)num_blocks * block_size;
+    /* The tokens of each block, in call order: head[B] is the first, next[i] the
+     * one after token i (-1 ends a list). */
+    int *head = (int *)malloc(sizeof(int) * ((size_t)num_blocks + 1));
+    int *tail = (int *)malloc(sizeof(int) * ((size_t)num_blocks + 1));
+    int *next = (int *)malloc(sizeof(int) * ((size_t)num_tokens + 1));
+    if (!head || !tail || !next) {
+        free(head);
+        free(tail);
+        free(next);
+        return 3;
+    }
+    for (long b = 0; b < num_blocks; ++b)
+        head[b] = tail[b] = -1;
     for (int i = 0; i < num_tokens; ++i) {
+        next[i] = -1;
         const long slot = slot_mapping[i];
         if (slot < 0 || slot >= nslots)
             continue;
         const long blk = slot / block_size;
-        /* each block once, at the first of its tokens in call order */
-        int seen = 0;
-        for (int j = 0; j < i; ++j) {
-            const long sj = slot_mapping[j];
-            if (sj >= 0 && sj < nslots && sj / block_size == blk)
-                seen = 1;
-        }
-        if (seen)
-            continue;
+        if (head[blk] < 0)
+            head[blk] = i;
+        else
+            next[tail[blk]] = i;
+        tail[blk] = i;
+    }
+    for (int i = 0; i < num_tokens; ++i) {
+        const long slot = slot_mapping[i];
+        if (slot < 0 || slot >= nslots || head[slot / block_size] != i)
+            continue; /* each block once, at the first of its tokens */
+        const long blk = slot / block_size;
         long o_min = block_size;
-        for (int j = i; j < num_tokens; ++j) {
-            const long sj = slot_mapping[j];
-            if (sj >= 0 && sj < nslots && sj / block_size == blk && sj % block_size < o_min)
-                o_min = sj % block_size;
-        }
+        for (int j = i; j >= 0; j = next[j])
+            if (slot_mapping[j] % block_size < o_min)
+                o_min = slot_mapping[j] % block_size;
         for (int g = 0; g < n_kv; ++g) {
             for (int which = 0; which < 2; ++which) { /* 0: K, 1: V */
                 const uint16_t *src = which == 0 ? k_new : v_new;
@@ -549,16 +563,12 @@ int oracle_kv_append_fp8_block(const uint16_t *k_new, const uint16_t *v_new,
                                 (((size_t)blk * n_kv + g) * 2 + which) * (size_t)block_size * head_dim;
                 const float s_old = o_min > 0 ? sc[which] : 0.0f;
                 double a = 0.0;
-                for (int j = i; j < num_tokens; ++j) {
-                    const long sj = slot_mapping[j];
-                    if (sj < 0 || sj >= nslots || sj / block_size != blk)
-                        continue;
+                for (int j = i; j >= 0; j = next[j])
                     for (int e = 0; e < head_dim; ++e) {
                         const double x = bf16_value(src[((size_t)j * n_kv + g) * head_dim + e]);
                         if (isfinite(x) && fabs(x) > a)
                             a = fabs(x);
                     }
-                }
                 float s_new = s_old;
                 if (a > 0.0) {
                     int e = -126;
@@ -576,22 +586,21 @@ int oracle_kv_append_fp8_block(const uint16_t *k_new, const uint16_t *v_new,
                             *cp = e4m3_code(v / s_new);
                         }
                 }
-                for (int j = i; j < num_tokens; ++j) {
-                    const long sj = slot_mapping[j];
-                    if (sj < 0 || sj >= nslots || sj / block_size != blk)
-                        continue;
+                for (int j = i; j >= 0; j = next[j])
                     for (int e = 0; e < head_dim; ++e) {
                         const float x = (float)bf16_value(src[((size_t)j * n_kv + g) * head_dim + e]);
-                        rows[(size_t)(sj % block_size) * head_dim + e] =
+                        rows[(size_t)(slot_mapping[j] % block_size) * head_dim + e] =
                             e4m3_code(s_new > 0.0f ? x / s_new : x);
                     }
-                }
                 sc[which] = s_new;
             }
             kv_scales[((size_t)blk * n_kv + g) * 4 + 2] = 0.0f;
             kv_scales[((size_t)blk * n_kv + g) * 4 + 3] = 0.0f;
         }
     }
+    free(head);
+    free(tail);
+    free(next);
     return 0;
 }
 

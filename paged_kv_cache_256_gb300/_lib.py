@@ -28,8 +28,10 @@ PKV_FLAG_CHECKED = 0x1
 PKV_FLAG_TEST_STALL = 0x2
 PKV_FLAG_KV_FP8 = 0x4
 PKV_FLAG_NO_EARLY_START = 0x8
+PKV_FLAG_KV_BLOCK_SCALES = 0x10
 PKV_KV_BF16 = 0
 PKV_KV_FP8_E4M3 = 1
+PKV_KV_FP8_E4M3_BLOCK = 2
 PKV_FLAG_GRID_SHIFT = 16
 
 
@@ -49,6 +51,7 @@ class pkv_attn_params(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("flags", ctypes.c_uint), ("window", ctypes.c_int), ("kv_dtype", ctypes.c_int),
         ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("kv_scales", ctypes.c_void_p),
     ]
 
 
@@ -65,6 +68,8 @@ SIGNATURES = {
     "pkv_kv_append": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp, _vp, ctypes.c_uint, _vp], _c_int),
     "pkv_kv_append_fp8": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp] * 3 + [ctypes.c_uint, _vp],
                           _c_int),
+    "pkv_kv_append_fp8_block": ([_vp, _vp, _i32p] + [_c_int] * 5 + [_vp] * 2 +
+                                [ctypes.c_uint, _vp], _c_int),
     "pkv_check_error": ([_vp, _vp], _c_int),
     "pkv_copy_blocks": ([_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.c_uint,
                          _vp], _c_int),
@@ -140,6 +145,14 @@ def _fp8_like(t, name):
         raise TypeError(f"{name} must hold e4m3 codes (torch.uint8 or float8_e4m3fn), got {t.dtype}")
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def _scales_tensor(t, num_blocks, n_kv, name="kv_scales"):
+    import torch
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or \
+            tuple(t.shape) != (num_blocks, n_kv, 4):
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape "
+                         f"({num_blocks}, {n_kv}, 4)")
 
 
 def _f32_vec(t, n, name):
@@ -244,18 +257,24 @@ def pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale
 
 def pkv_paged_decode_attn_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out,
                              workspace, flags=0, stream=None, window=0, k_scale=None,
-                             v_scale=None):
+                             v_scale=None, kv_scales=None):
     """pkv_paged_decode_attn through the parameter struct.
 
     window > 0: sliding window of that many positions.  With k_scale / v_scale
     (float32 CUDA [n_kv]) the cache is 8-bit: k_cache is the interleaved
     e4m3 cache [num_blocks, n_kv, 2, bs, d] (uint8 or float8_e4m3fn) and
-    v_cache is None.
+    v_cache is None.  With kv_scales (float32 CUDA [num_blocks, n_kv, 4]) the
+    8-bit cache has one K and one V scale per (block, KV head) instead.
     """
-    kv8 = k_scale is not None or v_scale is not None
+    blk = kv_scales is not None
+    kv8 = blk or k_scale is not None or v_scale is not None
     (num_seqs, q_len, n_q, n_kv, d, bs, max_blocks, num_blocks), out_dtype = _attn_shapes(
         q, k_cache, v_cache, block_tables, context_lens, out, workspace, kv8)
-    if kv8:
+    if blk:
+        if k_scale is not None or v_scale is not None:
+            raise ValueError("pass either per-head scales or per-block scales, not both")
+        _scales_tensor(kv_scales, num_blocks, n_kv)
+    elif kv8:
         _f32_vec(k_scale, n_kv, "k_scale")
         _f32_vec(v_scale, n_kv, "v_scale")
     p = pkv_attn_params(
@@ -266,8 +285,11 @@ def pkv_paged_decode_attn_ex(q, k_cache, v_cache, block_tables, context_lens, sc
         max_blocks_per_seq=max_blocks, num_blocks=num_blocks, scale=float(scale),
         out=out.data_ptr(), out_dtype=out_dtype, workspace=workspace.data_ptr(),
         workspace_bytes=workspace.numel() * workspace.element_size(), flags=int(flags),
-        window=int(window), kv_dtype=PKV_KV_FP8_E4M3 if kv8 else PKV_KV_BF16,
-        k_scale=k_scale.data_ptr() if kv8 else None, v_scale=v_scale.data_ptr() if kv8 else None)
+        window=int(window),
+        kv_dtype=PKV_KV_FP8_E4M3_BLOCK if blk else PKV_KV_FP8_E4M3 if kv8 else PKV_KV_BF16,
+        k_scale=k_scale.data_ptr() if kv8 and not blk else None,
+        v_scale=v_scale.data_ptr() if kv8 and not blk else None,
+        kv_scales=kv_scales.data_ptr() if blk else None)
     st = load_library().pkv_paged_decode_attn_ex(ctypes.byref(p), _stream_ptr(stream))
     _check(st, "pkv_paged_decode_attn_ex")
 
@@ -333,15 +355,19 @@ def pkv_copy_blocks(k_cache, v_cache, pairs, flags=0, stream=None):
     """Copy whole blocks (all KV heads, K and V): block pairs[p,1] <- block pairs[p,0].
 
     bf16 caches, or the interleaved e4m3 cache [num_blocks, n_kv, 2, bs, d] as k_cache with
-    v_cache None (PKV_FLAG_KV_FP8 is then set).
+    v_cache None (PKV_FLAG_KV_FP8 is then set) or, for a cache with per-block scales, its
+    float32 scale tensor [num_blocks, n_kv, 4] (copied with the blocks).
     """
     import torch
     kv8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
     if kv8:
         _fp8_like(k_cache, "kv_cache")
-        if v_cache is not None or k_cache.dim() != 5 or k_cache.shape[2] != 2:
+        if k_cache.dim() != 5 or k_cache.shape[2] != 2:
             raise ValueError("an 8-bit cache is one [num_blocks, n_kv, 2, bs, d] tensor")
         flags = int(flags) | PKV_FLAG_KV_FP8
+        if v_cache is not None:
+            _scales_tensor(v_cache, k_cache.shape[0], k_cache.shape[1])
+            flags |= PKV_FLAG_KV_BLOCK_SCALES
     else:
         _bf16_like(k_cache, "k_cache")
         _bf16_like(v_cache, "v_cache")
@@ -359,6 +385,28 @@ def pkv_copy_blocks(k_cache, v_cache, pairs, flags=0, stream=None):
                                         pairs.data_ptr(), pairs.shape[0], num_blocks, n_kv, d, bs,
                                         int(flags), _stream_ptr(stream))
     _check(st, "pkv_copy_blocks")
+
+
+def pkv_kv_append_fp8_block(k_new, v_new, slot_mapping, kv_cache, kv_scales, flags=0,
+                            stream=None):
+    """Quantise k_new/v_new [T, n_kv, d] (bf16) into the interleaved e4m3 cache
+    [num_blocks, n_kv, 2, bs, d], setting the per-(block, KV head) scales kv_scales
+    (float32 [num_blocks, n_kv, 4]) from the data; see include/pkv.h for the rule."""
+    _bf16_like(k_new, "k_new")
+    _bf16_like(v_new, "v_new")
+    _fp8_like(kv_cache, "kv_cache")
+    _i32(slot_mapping, "slot_mapping")
+    T, n_kv, d = k_new.shape
+    if kv_cache.dim() != 5 or kv_cache.shape[2] != 2:
+        raise ValueError("kv_cache must be [num_blocks, n_kv, 2, bs, d]")
+    num_blocks, n_kv2, _, bs, d2 = kv_cache.shape
+    if v_new.shape != k_new.shape or n_kv2 != n_kv or d2 != d or slot_mapping.shape != (T,):
+        raise ValueError("inconsistent shapes")
+    _scales_tensor(kv_scales, num_blocks, n_kv)
+    st = load_library().pkv_kv_append_fp8_block(
+        k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), T, n_kv, d, bs, num_blocks,
+        kv_cache.data_ptr(), kv_scales.data_ptr(), int(flags), _stream_ptr(stream))
+    _check(st, "pkv_kv_append_fp8_block")
 
 
 # ---- block pool (host memory only; numpy int32 arrays are passed by pointer)

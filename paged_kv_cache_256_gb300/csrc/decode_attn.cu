@@ -4,10 +4,10 @@
 
 namespace pkv {
 
-cudaError_t launch_decode_attn(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                               int head_dim, int block_size, bool out_f32, int grid,
-                               cudaStream_t stream) {
-    return launch_decode_attn_kv<false>(a, tk, tv, tq, head_dim, block_size, out_f32, grid, stream);
+cudaError_t launch_decode_attn(const AttnArgs& a, const AttnMaps& maps, int head_dim,
+                               int block_size, bool out_f32, int grid, cudaStream_t stream) {
+    return launch_decode_attn_kv<false, false>(a, maps, head_dim, block_size, out_f32, grid,
+                                               stream);
 }
 
 }  // namespace pkv

@@ -76,12 +76,21 @@ constexpr int kIssueLanes = 8;                   // producer lanes issuing loads
 constexpr int kNarrowRows = 8;                   // rows up to which the narrow consumer is used
 constexpr int kTmemMinRows = 64;                 // rows above which the TMEM consumer is used
 
+// Per-(block, KV head) scales weigh a block's probabilities by its V scale over
+// the largest one seen so far; the weights go to f16 for the MMA, so they carry
+// a power-of-two headroom, taken back out of the accumulator at the end, that
+// keeps small ratios out of f16's subnormal range: 2^14 where probabilities
+// are at most 1 (mma.sync consumers), 2^7 where the lazily rescaled ones reach
+// 2^8 (tensor-memory consumer) -- at most 2^15 either way, below f16's 65504.
+constexpr float kPShiftSync = 16384.f, kPShiftSyncInv = 1.f / 16384.f;
+constexpr float kPShiftTmem = 128.f, kPShiftTmemInv = 1.f / 128.f;
+
 // Consumer modes, chosen by the number of query rows sharing a KV head.
 constexpr int kModeWide = 0;    // 8 < rows <= 64: mma.sync, rows on the M side
 constexpr int kModeNarrow = 1;  // rows <= 8: mma.sync, tokens on the M side
 constexpr int kModeTmem = 2;    // rows > 64: tcgen05, M = 128 row tiles, accumulators in TMEM
 
-template <int D, int BS, int MODE, bool KV8 = false>
+template <int D, int BS, int MODE, bool KV8 = false, bool BLK = false>
 struct AttnCfg {
     static constexpr int kTileBytes = BS * D * (KV8 ? 1 : 2);  // one K (or V) tile of one (block, head)
     // TMA boxes per tile: bf16 in 64-column (128-byte) boxes; e4m3 rows of D
@@ -125,8 +134,15 @@ struct AttnCfg {
     // V, each 64 rows in D/64 swizzled 64-column regions).
     static constexpr int kCvtRegion = 64 * 128;
     static constexpr int kCvtBytes = (MODE == kModeTmem && KV8) ? 2 * 2 * (D / 64) * kCvtRegion : 0;
-    static constexpr int kScratchBytes = kMergeBytes + kEmitBytes + kQTileBytes + kCvtBytes;
-    static constexpr int kMaxStages = KV8 ? 48 : 32;
+    // Per-(block, KV head) scales (BLK): each block of a stage brings 16 bytes
+    // {K scale, V scale, 0, 0} by TMA with its tiles, into a slot beside the
+    // ring; the tensor-memory consumer's converter warps copy a super-block's
+    // scales next to its f16 copy (2 copies x blocks x {K, V}).
+    static constexpr int kSlotBytes = BLK ? kBlocksPerStage * 16 : 0;
+    static constexpr int kCvtSlotBytes = (BLK && MODE == kModeTmem) ? 2 * kBlocksPerStage * 8 : 0;
+    static constexpr int kScratchBytes =
+        kMergeBytes + kEmitBytes + kQTileBytes + kCvtBytes + kCvtSlotBytes;
+    static constexpr int kMaxStages = MODE == kModeTmem ? (KV8 ? 24 : 16) : (KV8 ? 48 : 32);
     static constexpr int kBarrierBytes = 2 * kMaxStages * 8;
     static constexpr int kBudget = 227 * 1024 - 1024 - kScratchBytes - kBarrierBytes - 1024;
     // In the mma.sync modes the ring depth is a multiple of the consumer-warp
@@ -135,12 +151,12 @@ struct AttnCfg {
     // round r - 1 complete.  (mbarrier parity waits cannot tell round r from
     // round r - 2; with another warp owning round r - 1 a still-in-flight load
     // would read as complete.)  The TMEM mode has a single consumer thread.
-    static constexpr int kStagesRaw = kBudget / kStageBytes;
+    static constexpr int kStagesRaw = kBudget / (kStageBytes + kSlotBytes);
     static constexpr int kStages =
         kStagesRaw >= kMaxStages ? kMaxStages
                                  : (MODE == kModeTmem ? kStagesRaw : (kStagesRaw / 8) * 8);
     static constexpr int kSmemBytes =
-        1024 + kStages * kStageBytes + kScratchBytes + 2 * kStages * 8;
+        1024 + kStages * kStageBytes + kScratchBytes + 2 * kStages * 8 + kStages * kSlotBytes;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BS == 16 || BS == 32, "block_size");
     static_assert(MODE == kModeTmem ? kStages >= 2
@@ -504,12 +520,18 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
 // over the lanes, so a freed stage is refilled at once instead of waiting for
 // the stages issued beside it, and the first stages of a launch land first
 // instead of together.
+// BLK: each block's 16-byte scale entry comes with its tiles, as a plain
+// 16-byte bulk copy into the stage's slot; an out-of-range block id (whose
+// tiles read zeros) gets a zero slot written by the issuing lane before the
+// stage's arrival, and no copy.
 template <int D, int BS, int kStages, int kStageBytes, int kTileBytes, int kBoxBytes, int kBoxes,
-          int kBoxCols, int kRegion, int SBS, bool KV8, bool ORDERED>
+          int kBoxCols, int kRegion, int SBS, bool KV8, bool ORDERED, bool BLK>
 __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tmap_k,
                                         const CUtensorMap* tmap_v, Walk w, uint8_t* stages,
-                                        uint64_t* full_bar, uint64_t* empty_bar,
+                                        uint8_t* slots, uint64_t* full_bar, uint64_t* empty_bar,
                                         volatile int* s_abort) {
+    // a block's scale entry: (block, head) row of [num_blocks][n_kv][4] fp32
+    auto scale_src = [&](int blk) { return a.kv_scales + ((size_t)blk * a.n_kv + w.h) * 4; };
     static_assert(32 % SBS == 0, "stages must not straddle a batch of 32 block ids");
     const int lane = threadIdx.x & 31;
     if (a.test_stall) return;  // failure-path tests: nothing is loaded, every wait expires
@@ -539,10 +561,8 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                     const int blk = __shfl_sync(0xffffffffu, my, (k * SBS + lane / kBpb) & 31);
                     const uint32_t stage = gidx % kStages;
                     bool good = true;
-                    if (lane == 0) {
+                    if (lane == 0)
                         good = mbar_wait_bounded(&empty_bar[stage], ((gidx / kStages) & 1u) ^ 1u);
-                        if (good) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes);
-                    }
                     good = __shfl_sync(0xffffffffu, good, 0);
                     __syncwarp();
                     if (!good) {
@@ -553,11 +573,30 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                         }
                         break;
                     }
+                    // BLK: lane b < nb owns block b's scale slot (one box per block)
+                    uint32_t slot_tx = 0;
+                    if constexpr (BLK) {
+                        static_assert(kBpb == 1, "scale slots assume one box per block");
+                        const bool mine = lane < nb;
+                        if (mine && blk < 0) {
+                            *reinterpret_cast<uint4*>(slots + (stage * SBS + lane) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                            fence_proxy_async_smem_cta();
+                        }
+                        slot_tx = 16u * __popc(__ballot_sync(0xffffffffu, mine && blk >= 0));
+                        __syncwarp();  // the zero slots before the stage's arrival
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes + slot_tx);
                     if (lane < nb * kBpb) {
                         const int b = lane / kBpb, box = lane % kBpb;
                         const long long y64 = ((long long)blk * a.n_kv + w.h) * a.kv_mul * BS;
                         const bool oob = blk < 0 || y64 >= a.tile_rows_total;
                         const int yk = oob ? a.tile_rows_total : static_cast<int>(y64);
+                        if constexpr (BLK) {
+                            if (blk >= 0)
+                                bulk_load_16(slots + (stage * SBS + b) * 16, scale_src(blk),
+                                             &full_bar[stage], policy);
+                        }
                         if constexpr (KV8) {
                             tma_load_2d(stages + stage * kStageBytes + b * 2 * kBoxBytes, tmap_k,
                                         0, yk, &full_bar[stage], policy);
@@ -597,7 +636,24 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                 const unsigned issue_mask =
                     fail ? (good_mask & ((1u << (__ffs(fail) - 1)) - 1u)) : good_mask;
                 const bool do_issue = (issue_mask >> lane) & 1u;
-                if (do_issue) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes);
+                uint32_t slot_tx = 0;
+                if constexpr (BLK) {
+                    // this lane's stage: zero slots for out-of-range ids, a copy for the rest
+                    bool zeroed = false;
+#pragma unroll
+                    for (int b = 0; b < SBS; ++b) {
+                        if (!do_issue || b >= nb) continue;
+                        if (blks[b] >= 0) {
+                            slot_tx += 16u;
+                        } else {
+                            *reinterpret_cast<uint4*>(slots + (stage * SBS + b) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                            zeroed = true;
+                        }
+                    }
+                    if (zeroed) fence_proxy_async_smem_cta();
+                }
+                if (do_issue) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes + slot_tx);
 #pragma unroll
                 for (int b = 0; b < SBS; ++b) {
                     const int blk = blks[b];
@@ -609,6 +665,11 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                         const bool oob = blk < 0 || y64 >= a.tile_rows_total;
                         const int yk = oob ? a.tile_rows_total : static_cast<int>(y64);
                         const int yv = oob ? a.tile_rows_total : yk + a.v_row_off;
+                        if constexpr (BLK) {
+                            if (blk >= 0)
+                                bulk_load_16(slots + (stage * SBS + b) * 16, scale_src(blk),
+                                             &full_bar[stage], policy);
+                        }
                         if constexpr (KV8) {
                             // one box of 2 * BS rows: the K rows, then the V rows
                             tma_load_2d(stages + stage * kStageBytes + b * 2 * kBoxBytes, tmap_k,
@@ -682,12 +743,18 @@ __device__ __forceinline__ void merge_weights(float& m, float& l, float m2, floa
 //   O^T[d][row]  += V^T[d][tok] . P^T[tok][row]    (A = V tile via ldmatrix.trans)
 // Lane (g, t) holds rows 2t, 2t+1 of the softmax state; a row's max and sum
 // reduce over the 8 lanes sharing t.
-template <int D, int BS, bool OUT_F32, bool KV8>
+//
+// Per-(block, KV head) scales (BLK): the K scale of a tile's block joins that
+// tile's score scale; the V scale multiplies the tile's probabilities
+// relative to vrun, the largest V scale the warp has met in this unit (the
+// accumulator is rescaled when vrun grows, the running sum l is not), and the
+// accumulator is multiplied by vrun at the unit's end.
+template <int D, int BS, bool OUT_F32, bool KV8, bool BLK>
 __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_t* stages,
-                                               float* scratch, uint64_t* full_bar,
-                                               uint64_t* empty_bar, volatile int* s_abort,
-                                               int4& info0, int4& info1) {
-    using C = AttnCfg<D, BS, kModeNarrow, KV8>;
+                                               const uint8_t* slots, float* scratch,
+                                               uint64_t* full_bar, uint64_t* empty_bar,
+                                               volatile int* s_abort, int4& info0, int4& info1) {
+    using C = AttnCfg<D, BS, kModeNarrow, KV8, BLK>;
     constexpr int kStages = C::kStages;
     constexpr int MT = D / 16;   // 16-wide head_dim tiles (M of the PV product)
     constexpr int KT = D / 16;   // 16-deep k steps of the score product
@@ -730,9 +797,10 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
             }
         }
         // Per-unit scales: the K dequantisation scale joins the score scale,
-        // the V one the final normalisation.
-        const float sl2 = KV8 ? a.scale_log2 * __ldg(a.k_scale + h) : a.scale_log2;
-        const float vsc = KV8 ? __ldg(a.v_scale + h) : 1.f;
+        // the V one the final normalisation (per-block scales come per stage).
+        const float sl2 = (KV8 && !BLK) ? a.scale_log2 * __ldg(a.k_scale + h) : a.scale_log2;
+        const float vsc = (KV8 && !BLK) ? __ldg(a.v_scale + h) : 1.f;
+        float vrun = 0.f;  // BLK: largest V scale of this unit so far
         // Row r sees tokens lo..lim: lim = its position, lo = lim - W + 1
         // with a window (INT_MIN without); padding rows see nothing.
         int lim[2], lo[2];
@@ -764,6 +832,30 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
             const int nb = min(SBS, j1 - j0 - q * SBS);  // blocks in this stage
             if (ok) {
                 const uint32_t sb = smem_addr(stages + stage * C::kStageBytes);
+                // BLK: this stage's block scales; kf = score scale x K scale,
+                // rat = V scale / vrun, vfac rescales the accumulator when vrun grows.
+                float kf[SBS], rat[SBS], vfac = 1.f;
+#pragma unroll
+                for (int b = 0; b < SBS; ++b) kf[b] = sl2;
+                if constexpr (BLK) {
+                    float vs[SBS], smax = 0.f;
+#pragma unroll
+                    for (int b = 0; b < SBS; ++b) {
+                        const float2 sc = b < nb ? *reinterpret_cast<const float2*>(
+                                                       slots + (stage * SBS + b) * 16)
+                                                 : make_float2(0.f, 0.f);
+                        kf[b] = sl2 * sc.x;
+                        vs[b] = sc.y;
+                        smax = fmaxf(smax, sc.y);
+                    }
+                    if (smax > vrun) {
+                        vfac = vrun / smax;
+                        vrun = smax;
+                    }
+                    const float rinv = vrun > 0.f ? kPShiftSync / vrun : 0.f;
+#pragma unroll
+                    for (int b = 0; b < SBS; ++b) rat[b] = vs[b] * rinv;
+                }
                 // ---- S^T = K Q^T, two interleaved accumulators per 16-token tile
                 float st[UT][4], st2[UT][4];
 #pragma unroll
@@ -813,7 +905,7 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                     const bool need_mask = tok0 + BS - 1 > lim_min || tok0 < lo_max;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float x = (st[u][e] + st2[u][e]) * sl2;
+                        float x = (st[u][e] + st2[u][e]) * kf[bi];
                         const int tk = tok0 + tp * 16 + g + (e >> 1) * 8;
                         if (bi >= nb || (need_mask && (tk > lim[e & 1] || tk < lo[e & 1])))
                             x = -INFINITY;
@@ -844,6 +936,16 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                 }
                 l[0] = l[0] * alpha[0] + rsum[0];
                 l[1] = l[1] * alpha[1] + rsum[1];
+                if constexpr (BLK) {
+                    // the accumulator also follows vrun; the probabilities of each
+                    // block are weighed by its V scale relative to vrun
+                    alpha[0] *= vfac;
+                    alpha[1] *= vfac;
+#pragma unroll
+                    for (int u = 0; u < UT; ++u)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) st[u][e] *= rat[u / PT];
+                }
                 if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
                     for (int n = 0; n < MT; ++n) {
@@ -944,6 +1046,13 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
         gbase += ns;
 
         // ---- row sums across the 8 lanes of a row, then combine the warps' partials
+        if constexpr (BLK) {  // the accumulator in value units (vrun is warp-uniform)
+            const float back = vrun * kPShiftSyncInv;
+#pragma unroll
+            for (int n = 0; n < MT; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[n][e] *= back;
+        }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             l[e] += __shfl_xor_sync(0xffffffffu, l[e], 4);
@@ -1055,12 +1164,15 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
 // Warp w owns 16-row slice (w % WM) of the unit's rows and blocks g == w / WM
 // (mod WN), WM * WN = 8.  S = Q K^T (A = Q rows, B = K via ldmatrix), P stays
 // in registers as the A operand of O += P V (B = V via ldmatrix.trans).
-template <int D, int BS, bool OUT_F32, bool KV8>
+// Per-(block, KV head) scales (BLK): as in the narrow consumer -- the K scale
+// of a chunk's block joins its score scale, its V scale weighs the chunk's
+// probabilities relative to vrun, and the accumulator follows vrun.
+template <int D, int BS, bool OUT_F32, bool KV8, bool BLK>
 __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t* stages,
-                                             float* scratch, uint64_t* full_bar,
-                                             uint64_t* empty_bar, volatile int* s_abort,
-                                             int4& info0, int4& info1) {
-    using C = AttnCfg<D, BS, kModeWide, KV8>;
+                                             const uint8_t* slots, float* scratch,
+                                             uint64_t* full_bar, uint64_t* empty_bar,
+                                             volatile int* s_abort, int4& info0, int4& info1) {
+    using C = AttnCfg<D, BS, kModeWide, KV8, BLK>;
     constexpr int kStages = C::kStages;
     constexpr int SBS = C::kBlocksPerStage;
     constexpr int NT = D / 8;    // 8-wide output column tiles
@@ -1108,8 +1220,9 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                 }
             }
         }
-        const float sl2 = KV8 ? a.scale_log2 * __ldg(a.k_scale + h) : a.scale_log2;
-        const float vsc = KV8 ? __ldg(a.v_scale + h) : 1.f;
+        const float sl2 = (KV8 && !BLK) ? a.scale_log2 * __ldg(a.k_scale + h) : a.scale_log2;
+        const float vsc = (KV8 && !BLK) ? __ldg(a.v_scale + h) : 1.f;
+        float vrun = 0.f, vinv = 0.f;  // BLK: largest V scale of this unit so far; headroom / it
         // smallest causal limit and largest window start of the tile's real rows
         const int lim_min = ctx - a.q_len + tile_first_token(a, w.t);
         const int lo_max =
@@ -1131,6 +1244,21 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
             const int nb = min(SBS, j1 - j0 - q * SBS);  // blocks in this stage
             if (ok) {
                 const uint32_t sb = smem_addr(stages + stage * C::kStageBytes);
+                const uint8_t* sslot = slots + stage * SBS * 16;  // BLK: the blocks' scales
+                if constexpr (BLK) {
+                    float smax = 0.f;
+                    for (int b = 0; b < nb; ++b)
+                        smax = fmaxf(smax, reinterpret_cast<const float*>(sslot + b * 16)[1]);
+                    if (smax > vrun) {
+                        const float vfac = vrun / smax;
+#pragma unroll
+                        for (int n = 0; n < NT; ++n)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) o[n][e] *= vfac;
+                        vrun = smax;
+                        vinv = kPShiftSync / smax;
+                    }
+                }
 
                 // The stage's blocks are taken 16 tokens at a time (one
                 // online-softmax update per chunk): chunk u is token tile
@@ -1174,12 +1302,18 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                     // ---- scale, causal / window / tail mask, online softmax (base 2)
                     const int tok0 = j * BS + tp * 16;
                     const bool need_mask = tok0 + 15 > lim_min || tok0 < lo_max;
+                    float kfb = sl2, ratb = 1.f;  // BLK: this block's score factor, V weight
+                    if constexpr (BLK) {
+                        const float2 bsc = *reinterpret_cast<const float2*>(sslot + bi * 16);
+                        kfb = sl2 * bsc.x;
+                        ratb = bsc.y * vinv;
+                    }
                     float mloc[2] = {-INFINITY, -INFINITY};
 #pragma unroll
                     for (int n = 0; n < 2; ++n) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            float x = sc[n][e] * sl2;
+                            float x = sc[n][e] * kfb;
                             const int tk = tok0 + n * 8 + 2 * t + (e & 1);
                             if (need_mask && (tk > lim[e >> 1] || tk < lo[e >> 1])) x = -INFINITY;
                             sc[n][e] = x;
@@ -1208,6 +1342,12 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
                     }
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) l[hh] = l[hh] * alpha[hh] + rsum[hh];
+                    if constexpr (BLK) {
+#pragma unroll
+                        for (int n = 0; n < 2; ++n)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sc[n][e] *= ratb;
+                    }
                     if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {
@@ -1298,6 +1438,13 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
         gbase += ns;
 
         // ---- row sums across the quad, then combine the WN column partials
+        if constexpr (BLK) {  // the accumulator in value units (vrun is warp-uniform)
+            const float back = vrun * kPShiftSyncInv;
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[n][e] *= back;
+        }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 1);
@@ -1453,13 +1600,20 @@ __device__ __forceinline__ void issue_q_tile(const AttnArgs& a, const CUtensorMa
         tma_load_3d(qtile + half * 128 * 128, tmap_q, half * 64, y, z, bar);
 }
 
-template <int D, int BS, bool OUT_F32, bool KV8>
+// Per-(block, KV head) scales (BLK, 8-bit cache only): the converter warps
+// copy each super-block's K and V scales beside its f16 copy; the softmax
+// multiplies each key's raw score by the score scale times its block's K
+// scale before taking the row maximum, and weighs each block's probabilities
+// by its V scale relative to vrun, the largest V scale of the unit so far (O
+// is rescaled in TMEM when vrun grows, together with a grown maximum).
+template <int D, int BS, bool OUT_F32, bool KV8, bool BLK>
 __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t* stages,
-                                             uint8_t* qtile, const CUtensorMap* tmap_q,
-                                             uint64_t* full_bar, uint64_t* empty_bar,
-                                             uint64_t* tcb, uint32_t* s_tmem,
+                                             const uint8_t* slots, uint8_t* qtile,
+                                             const CUtensorMap* tmap_q, uint64_t* full_bar,
+                                             uint64_t* empty_bar, uint64_t* tcb, uint32_t* s_tmem,
                                              volatile int* s_abort, int4& info0, int4& info1) {
-    using C = AttnCfg<D, BS, kModeTmem, KV8>;
+    static_assert(!BLK || KV8, "block scales come with the 8-bit cache");
+    using C = AttnCfg<D, BS, kModeTmem, KV8, BLK>;
     constexpr int kStages = C::kStages;
     constexpr int kKeys = 64;                  // keys per softmax round
     constexpr int SB = C::kBlocksPerStage;     // blocks per super-block (= per stage)
@@ -1484,6 +1638,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     // f16 copies (8-bit cache): copy c at cvt + c * kCopy, K regions then V regions
     uint8_t* cvt = qtile + C::kQTileBytes;
     constexpr int kCopy = 2 * kHalves * C::kCvtRegion;
+    // BLK: scales of the super-block in f16 copy c: [c][block][K, V]
+    float* cvt_sc = reinterpret_cast<float*>(cvt + C::kCvtBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp > 5 && !KV8) return;  // warps 6, 7 have no part in this mode over bf16
     const bool softmax = warp < 4;
@@ -1696,6 +1852,13 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     tc_fence_after();
                     const int nb = min(SB, n - q * SB);
                     const int tok0 = (j0 + q * SB) * BS;
+                    if constexpr (BLK) {
+                        // this warp's half of the blocks' scales (K: warp 6, V: warp 7),
+                        // before the stage is given back
+                        if (lane < nb)
+                            cvt_sc[((g & 1u) * SB + lane) * 2 + isv] =
+                                reinterpret_cast<const float*>(slots + (st * SB + lane) * 16)[isv];
+                    }
                     const uint8_t* src = stages + st * C::kStageBytes + isv * C::kBoxBytes;
                     uint8_t* dst = cvt + (g & 1u) * kCopy + isv * kHalves * C::kCvtRegion;
                     // item = (key row n, 16-byte chunk cb of e4m3 codes)
@@ -1734,10 +1897,14 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             // visible score 0 (S is replaced by 0 and scaled by 1).  m_used is
             // the scaled running max, mr_used the raw score it came from.
             float m_used = -INFINITY, mr_used = 0.f, l = 0.f;
-            const float sl2_in = KV8 ? a.scale_log2 * __ldg(a.k_scale + h) : a.scale_log2;
+            // BLK: scores arrive already multiplied by their block's factor (score
+            // scale x K scale), so the row extreme is a plain maximum.
+            const float sl2_in = BLK ? 1.f
+                                 : KV8 ? a.scale_log2 * __ldg(a.k_scale + h) : a.scale_log2;
             const bool zero_scale = sl2_in == 0.f;
             const float sl2 = zero_scale ? 1.f : sl2_in;
             const bool neg = sl2 < 0.f;
+            float vrun = 0.f, vinv = 0.f;  // BLK: largest V scale of the unit so far; headroom / it
             const float hidden = neg ? INFINITY : -INFINITY;  // a masked raw score
             const int lim_min = ctx - a.q_len + tile_first_token(a, w.t);
             const int lo_max =
@@ -1761,6 +1928,34 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     }
                     tc_fence_before();
                     mbar_arrive(&s_free[sq & 1u]);  // S buffer may take the super-block after next
+                }
+                // BLK: the blocks' scales (written by the converter warps, acquired through
+                // their copy-ready barrier, whose phase for this super-block has completed)
+                float rat[SB], vfac = 1.f;
+                bool vgrow = false;
+                if constexpr (BLK) {
+                    ok = consumer_wait(a, &cvt_full[sq & 1u], (sq >> 1) & 1u, ok, s_abort);
+                    if (!ok) continue;
+                    float kf[SB], vs[SB], smax = 0.f;
+#pragma unroll
+                    for (int b = 0; b < SB; ++b) {
+                        const float2 sc = b < nb ? *reinterpret_cast<const float2*>(
+                                                       cvt_sc + ((sq & 1u) * SB + b) * 2)
+                                                 : make_float2(0.f, 0.f);
+                        kf[b] = a.scale_log2 * sc.x;
+                        vs[b] = sc.y;
+                        smax = fmaxf(smax, sc.y);
+                    }
+#pragma unroll
+                    for (int c = 0; c < kKeys; ++c) x[c] *= kf[c / BS];
+                    if (smax > vrun) {
+                        vgrow = true;
+                        vfac = vrun / smax;
+                        vrun = smax;
+                        vinv = kPShiftTmem / smax;
+                    }
+#pragma unroll
+                    for (int b = 0; b < SB; ++b) rat[b] = vs[b] * vinv;
                 }
                 if (zero_scale) {
 #pragma unroll
@@ -1800,7 +1995,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     tc_fence_after();
                 }
                 const bool grow = mloc > m_used + 8.f;
-                if (__any_sync(0xffffffffu, grow)) {
+                if (__any_sync(0xffffffffu, grow) || vgrow) {  // (vgrow is CTA-uniform)
                     // O may only be rescaled once the previous super-block's PV is done.
                     if (q > 0) {
                         ok = consumer_wait(a, &pv_done[(sq - 1) & 1u], ((sq - 1) >> 1) & 1u, ok,
@@ -1824,9 +2019,10 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                             uint32_t ov[32];
                             tmem_ld32(tlane + kColO + c0, ov);
                             tmem_wait_ld();
+                            const float oscale = alpha * vfac;
 #pragma unroll
                             for (int c = 0; c < 32; ++c)
-                                ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+                                ov[c] = __float_as_uint(__uint_as_float(ov[c]) * oscale);
                             tmem_st32(tlane + kColO + c0, ov);
                         }
                         tmem_wait_st();
@@ -1838,14 +2034,21 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
                 for (int c = 0; c < kKeys; c += 4) {
-                    const float p0 = fast_exp2((x[c] - mr_used) * sl2);
-                    const float p1 = fast_exp2((x[c + 1] - mr_used) * sl2);
-                    const float p2 = fast_exp2((x[c + 2] - mr_used) * sl2);
-                    const float p3 = fast_exp2((x[c + 3] - mr_used) * sl2);
+                    float p0 = fast_exp2((x[c] - mr_used) * sl2);
+                    float p1 = fast_exp2((x[c + 1] - mr_used) * sl2);
+                    float p2 = fast_exp2((x[c + 2] - mr_used) * sl2);
+                    float p3 = fast_exp2((x[c + 3] - mr_used) * sl2);
                     rs0 += p0;
                     rs1 += p1;
                     rs2 += p2;
                     rs3 += p3;
+                    if constexpr (BLK) {  // four keys of one block (BS is a multiple of 4)
+                        const float r = rat[c / BS];
+                        p0 *= r;
+                        p1 *= r;
+                        p2 *= r;
+                        p3 *= r;
+                    }
                     if constexpr (KV8) {
                         ph[c / 2] = pack_f16x2(p0, p1);
                         ph[c / 2 + 1] = pack_f16x2(p2, p3);
@@ -1900,7 +2103,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             const bool first_piece = j0 == w.jlo, last_piece = j1 == w.nb;
             const bool whole = first_piece && last_piece;
             if (ok) {
-                const float vsc = KV8 ? __ldg(a.v_scale + h) : 1.f;
+                const float vsc = BLK ? vrun * kPShiftTmemInv : KV8 ? __ldg(a.v_scale + h) : 1.f;
                 const float scl = (whole ? (l > 0.f ? 1.f / l : 0.f) : 1.f) * vsc;
                 const size_t rec = (size_t)cta * 2 + (piece == 0 ? 0 : 1);
 #pragma unroll 1
@@ -1977,12 +2180,12 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
 }
 
 // ===================== kernel =====================
-template <int D, int BS, bool OUT_F32, int MODE, bool KV8>
+template <int D, int BS, bool OUT_F32, int MODE, bool KV8, bool BLK>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_decode_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v,
                              const __grid_constant__ CUtensorMap tmap_q, const AttnArgs a) {
-    using C = AttnCfg<D, BS, MODE, KV8>;
+    using C = AttnCfg<D, BS, MODE, KV8, BLK>;
     constexpr int kStages = C::kStages;
 
     extern __shared__ uint8_t smem_raw[];
@@ -1993,6 +2196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes +
                                                      C::kScratchBytes);
     uint64_t* empty_bar = full_bar + kStages;
+    // BLK: the scale slots of the ring, kBlocksPerStage x 16 bytes per stage
+    uint8_t* slots = reinterpret_cast<uint8_t*>(empty_bar + kStages);
 
     __shared__ long long s_red[2 * kThreads / 32];
     __shared__ long long s_pos[4];
@@ -2058,8 +2263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == kConsumerWarps) {
         produce<D, BS, kStages, C::kStageBytes, C::kTileBytes, C::kBoxBytes, C::kBoxes,
-                C::kBoxCols, C::kRegion, C::kBlocksPerStage, KV8, MODE == kModeTmem>(
-            a, &tmap_k, &tmap_v, w0, stages, full_bar, empty_bar, &s_abort);
+                C::kBoxCols, C::kRegion, C::kBlocksPerStage, KV8, MODE == kModeTmem, BLK>(
+            a, &tmap_k, &tmap_v, w0, stages, slots, full_bar, empty_bar, &s_abort);
         return;
     }
 
@@ -2084,15 +2289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     int4 info0 = make_int4(0, 0, 0, 0), info1 = make_int4(0, 0, 0, 0);
     if (w0.left <= 0) info0.z = info1.z = kRecEmpty;
     if constexpr (MODE == kModeNarrow)
-        consume_narrow<D, BS, OUT_F32, KV8>(a, w0, stages, scratch, full_bar, empty_bar, &s_abort,
-                                            info0, info1);
+        consume_narrow<D, BS, OUT_F32, KV8, BLK>(a, w0, stages, slots, scratch, full_bar,
+                                                 empty_bar, &s_abort, info0, info1);
     else if constexpr (MODE == kModeWide)
-        consume_wide<D, BS, OUT_F32, KV8>(a, w0, stages, scratch, full_bar, empty_bar, &s_abort,
-                                          info0, info1);
+        consume_wide<D, BS, OUT_F32, KV8, BLK>(a, w0, stages, slots, scratch, full_bar, empty_bar,
+                                               &s_abort, info0, info1);
     else
-        consume_tmem<D, BS, OUT_F32, KV8>(a, w0, stages, reinterpret_cast<uint8_t*>(scratch),
-                                          &tmap_q, full_bar, empty_bar, s_tcb, &s_tmem, &s_abort,
-                                          info0, info1);
+        consume_tmem<D, BS, OUT_F32, KV8, BLK>(a, w0, stages, slots,
+                                               reinterpret_cast<uint8_t*>(scratch), &tmap_q,
+                                               full_bar, empty_bar, s_tcb, &s_tmem, &s_abort,
+                                               info0, info1);
     if (tid == 0) {
         a.rec_info[(size_t)blockIdx.x * 2 + 0] = info0;
         a.rec_info[(size_t)blockIdx.x * 2 + 1] = info1;
@@ -2100,11 +2306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int D, int BS, bool F32, int MODE, bool KV8>
-static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& tq, int grid, cudaStream_t stream) {
-    auto kern = paged_decode_attn_kernel<D, BS, F32, MODE, KV8>;
-    const int smem = AttnCfg<D, BS, MODE, KV8>::kSmemBytes;
+template <int D, int BS, bool F32, int MODE, bool KV8, bool BLK>
+static cudaError_t launch_one(const AttnArgs& a, const AttnMaps& m, int grid,
+                              cudaStream_t stream) {
+    auto kern = paged_decode_attn_kernel<D, BS, F32, MODE, KV8, BLK>;
+    const int smem = AttnCfg<D, BS, MODE, KV8, BLK>::kSmemBytes;
     // The shared-memory opt-in is set once per device for each instantiation.
     static std::atomic<unsigned long long> opted_in{0};
     int dev = 0;
@@ -2126,39 +2332,37 @@ static cudaError_t launch_one(const AttnArgs& a, const CUtensorMap& tk, const CU
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.early_start ? 1 : 0;  // without it, griddepcontrol.wait returns at once
-    e = cudaLaunchKernelEx(&cfg, kern, tk, tv, tq, a);
+    e = cudaLaunchKernelEx(&cfg, kern, m.k, m.v, m.q, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 // Consumer by rows per KV head: narrow (<= 8), wide, TMEM (> 64).
-template <int D, int BS, bool KV8>
-static cudaError_t launch_shape(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& tq, bool out_f32, int grid,
+template <int D, int BS, bool KV8, bool BLK>
+static cudaError_t launch_shape(const AttnArgs& a, const AttnMaps& m, bool out_f32, int grid,
                                 cudaStream_t stream) {
     if (a.rows <= kNarrowRows)
-        return out_f32 ? launch_one<D, BS, true, kModeNarrow, KV8>(a, tk, tv, tq, grid, stream)
-                       : launch_one<D, BS, false, kModeNarrow, KV8>(a, tk, tv, tq, grid, stream);
+        return out_f32 ? launch_one<D, BS, true, kModeNarrow, KV8, BLK>(a, m, grid, stream)
+                       : launch_one<D, BS, false, kModeNarrow, KV8, BLK>(a, m, grid, stream);
     if (a.rows > kTmemMinRows)
-        return out_f32 ? launch_one<D, BS, true, kModeTmem, KV8>(a, tk, tv, tq, grid, stream)
-                       : launch_one<D, BS, false, kModeTmem, KV8>(a, tk, tv, tq, grid, stream);
-    return out_f32 ? launch_one<D, BS, true, kModeWide, KV8>(a, tk, tv, tq, grid, stream)
-                   : launch_one<D, BS, false, kModeWide, KV8>(a, tk, tv, tq, grid, stream);
+        return out_f32 ? launch_one<D, BS, true, kModeTmem, KV8, BLK>(a, m, grid, stream)
+                       : launch_one<D, BS, false, kModeTmem, KV8, BLK>(a, m, grid, stream);
+    return out_f32 ? launch_one<D, BS, true, kModeWide, KV8, BLK>(a, m, grid, stream)
+                   : launch_one<D, BS, false, kModeWide, KV8, BLK>(a, m, grid, stream);
 }
 
-template <bool KV8>
-static cudaError_t launch_decode_attn_kv(const AttnArgs& a, const CUtensorMap& tk,
-                                         const CUtensorMap& tv, const CUtensorMap& tq,
-                                         int head_dim, int block_size, bool out_f32, int grid,
+template <bool KV8, bool BLK>
+static cudaError_t launch_decode_attn_kv(const AttnArgs& a, const AttnMaps& m, int head_dim,
+                                         int block_size, bool out_f32, int grid,
                                          cudaStream_t stream) {
     if (head_dim == 128 && block_size == 16)
-        return launch_shape<128, 16, KV8>(a, tk, tv, tq, out_f32, grid, stream);
+        return launch_shape<128, 16, KV8, BLK>(a, m, out_f32, grid, stream);
     if (head_dim == 128 && block_size == 32)
-        return launch_shape<128, 32, KV8>(a, tk, tv, tq, out_f32, grid, stream);
+        return launch_shape<128, 32, KV8, BLK>(a, m, out_f32, grid, stream);
     if (head_dim == 64 && block_size == 16)
-        return launch_shape<64, 16, KV8>(a, tk, tv, tq, out_f32, grid, stream);
+        return launch_shape<64, 16, KV8, BLK>(a, m, out_f32, grid, stream);
     if (head_dim == 64 && block_size == 32)
-        return launch_shape<64, 32, KV8>(a, tk, tv, tq, out_f32, grid, stream);
+        return launch_shape<64, 32, KV8, BLK>(a, m, out_f32, grid, stream);
     return cudaErrorInvalidValue;
 }
 

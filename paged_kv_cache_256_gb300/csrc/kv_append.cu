@@ -124,13 +124,187 @@ cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new,
     return cudaGetLastError();
 }
 
+// The quantising append into an 8-bit cache with one scale per (block, KV
+// head) (layout as above, scales [num_blocks][n_kv][4] fp32 = K scale, V
+// scale, reserved, reserved).  A scale follows the values of its block: it is
+// the smallest power of two 2^e (e >= -126) that keeps the block's largest
+// finite value within 448, it only grows while the block fills, and when it
+// grows the block's resident rows (those below the call's first offset in
+// the block) are re-quantised by the power-of-two ratio -- exact except for
+// values that fall below the normal e4m3 range.  A block written from offset
+// 0 starts over (its stored scale is ignored); scale 0 stands for "nothing
+// but zeros so far".  ("Efficient inference", Quantization: quantise and
+// dequantise through a scale.)
+//
+// One warp per (token, KV head).  The warp of the first token of a run --
+// consecutive tokens (skipped slots aside) landing in one block -- handles
+// the whole run for its head, K then V: the largest |x| over the run's rows,
+// the new scale, the re-quantised resident rows, the run's codes, the scale
+// entry.  Every other warp returns.  Lanes take 4 consecutive elements of a
+// row at a time.
+constexpr int kAppendWarps = 8;
+
+// The smallest power of two s = 2^e, e >= -126, with a <= 448 * s (a > 0,
+// finite).  r = fp32(a / 448) rounds across no power of two that matters:
+// a has 8 significant bits, so when a / 448 exceeds 2^e it does so by at
+// least 1/224 of it, far more than fp32 rounding; hence ceil(log2(r)) is
+// exactly the wanted e.
+__device__ __forceinline__ float pow2_scale_for(float a) {
+    const float r = __fdiv_rn(a, 448.f);
+    const uint32_t u = __float_as_uint(r);
+    int e = static_cast<int>((u >> 23) & 0xFF) - 127;  // floor(log2 r) for normal r
+    if ((u & 0x7FFFFFu) != 0) ++e;                      // not a power of two: round up
+    if (((u >> 23) & 0xFF) == 0) e = -126;              // r subnormal or 0: below 2^-126
+    if (e < -126) e = -126;
+    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+// Four bf16 (two 32-bit words) -> four e4m3 codes of x / s (x itself for s == 0).
+__device__ __forceinline__ uint32_t quantise4_by(uint32_t lo2, uint32_t hi2, float s) {
+    float x0 = bf16_lo_to_f32(lo2), x1 = bf16_hi_to_f32(lo2);
+    float x2 = bf16_lo_to_f32(hi2), x3 = bf16_hi_to_f32(hi2);
+    if (s > 0.f) {
+        x0 = __fdiv_rn(x0, s);
+        x1 = __fdiv_rn(x1, s);
+        x2 = __fdiv_rn(x2, s);
+        x3 = __fdiv_rn(x3, s);
+    }
+    return f32x2_to_e4m3x2(x0, x1) | (f32x2_to_e4m3x2(x2, x3) << 16);
+}
+
+// Four codes re-quantised from scale s_old to s_new: e4m3 of fp32(fp32(v * s_old) / s_new).
+__device__ __forceinline__ uint32_t requantise4(uint32_t codes, float s_old, float s_new) {
+    uint32_t lo, hi;  // f16 pairs of bytes (0, 1) and (2, 3); every e4m3 value is exact in f16
+    e4m3x4_to_f16x2x2(codes, lo, hi);
+    const float v0 = __fdiv_rn(f16_lo_to_f32(lo) * s_old, s_new);
+    const float v1 = __fdiv_rn(f16_hi_to_f32(lo) * s_old, s_new);
+    const float v2 = __fdiv_rn(f16_lo_to_f32(hi) * s_old, s_new);
+    const float v3 = __fdiv_rn(f16_hi_to_f32(hi) * s_old, s_new);
+    return f32x2_to_e4m3x2(v0, v1) | (f32x2_to_e4m3x2(v2, v3) << 16);
+}
+
+__global__ void __launch_bounds__(kAppendWarps * 32)
+    kv_append_fp8_block_kernel(const uint16_t* __restrict__ k_new,
+                               const uint16_t* __restrict__ v_new,
+                               const int32_t* __restrict__ slot_mapping, int num_tokens, int n_kv,
+                               int head_dim, int block_size, long long num_slots,
+                               uint8_t* __restrict__ kv_cache, float* __restrict__ kv_scales) {
+    // The attention call that follows may start its work partition now (it
+    // reads no cache before this grid completes).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const long long item = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+    if (item >= (long long)num_tokens * n_kv) return;
+    const int t = static_cast<int>(item / n_kv), g = static_cast<int>(item % n_kv);
+    const long long slot = __ldg(slot_mapping + t);
+    if (slot < 0 || slot >= num_slots) return;
+    const long long blk = slot / block_size;
+    auto valid = [&](long long s) { return s >= 0 && s < num_slots; };
+
+    // Does the nearest earlier valid token land in the same block?  (Lanes look
+    // 32 tokens back at a time; the answer is warp-uniform.)
+    for (int base = t - 1; base >= 0; base -= 32) {
+        const int p = base - lane;
+        const long long sp = p >= 0 ? __ldg(slot_mapping + p) : -1;
+        const unsigned vm = __ballot_sync(0xffffffffu, p >= 0 && valid(sp));
+        if (vm) {
+            const long long sprev = __shfl_sync(0xffffffffu, sp, __ffs(vm) - 1);
+            if (sprev / block_size == blk) return;  // not the run's first token
+            break;
+        }
+    }
+    // The run: tokens t .. end-1 (skipped slots included), and its lowest offset.
+    int end = t + 1;
+    long long o_min = slot % block_size;
+    for (int base = t + 1; base < num_tokens; base += 32) {
+        const int p = base + lane;
+        const long long sp = p < num_tokens ? __ldg(slot_mapping + p) : -1;
+        const bool other = p < num_tokens && valid(sp) && sp / block_size != blk;
+        const unsigned stop = __ballot_sync(0xffffffffu, other || p >= num_tokens);
+        const int lim = stop ? __ffs(stop) - 1 : 32;  // lanes below lim are in the run
+        long long off = (lane < lim && valid(sp)) ? sp % block_size : (long long)block_size;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) off = min(off, __shfl_xor_sync(0xffffffffu, off, o));
+        o_min = min(o_min, off);
+        end = base + lim;
+        if (stop) break;
+    }
+
+    for (int which = 0; which < 2; ++which) {  // K, then V
+        const uint16_t* src = which == 0 ? k_new : v_new;
+        float* entry = kv_scales + ((size_t)blk * n_kv + g) * 4;
+        uint8_t* rows = kv_cache + (((size_t)blk * n_kv + g) * 2 + which) * (size_t)block_size * head_dim;
+        // largest finite |x| over the run's rows
+        float amax = 0.f;
+        for (int j = t; j < end; ++j) {
+            const long long sj = __ldg(slot_mapping + j);
+            if (!valid(sj)) continue;
+            const uint16_t* row = src + ((size_t)j * n_kv + g) * head_dim;
+            for (int e = lane * 4; e < head_dim; e += 128) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + e));
+                const float x[4] = {bf16_lo_to_f32(v.x), bf16_hi_to_f32(v.x), bf16_lo_to_f32(v.y),
+                                    bf16_hi_to_f32(v.y)};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (isfinite(x[k])) amax = fmaxf(amax, fabsf(x[k]));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float s_old = o_min > 0 ? entry[which] : 0.f;
+        float s_new = s_old;
+        if (amax > 0.f) s_new = fmaxf(s_old, pow2_scale_for(amax));
+        if (s_new > s_old && s_old > 0.f) {  // re-quantise the resident rows
+            for (long long r = 0; r < o_min; ++r)
+                for (int e = lane * 4; e < head_dim; e += 128) {
+                    uint32_t* cp = reinterpret_cast<uint32_t*>(rows + r * head_dim + e);
+                    *cp = requantise4(*cp, s_old, s_new);
+                }
+        }
+        for (int j = t; j < end; ++j) {  // the run's rows, in call order
+            const long long sj = __ldg(slot_mapping + j);
+            if (!valid(sj)) continue;
+            const uint16_t* row = src + ((size_t)j * n_kv + g) * head_dim;
+            uint8_t* dst = rows + (sj % block_size) * head_dim;
+            for (int e = lane * 4; e < head_dim; e += 128) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + e));
+                *reinterpret_cast<uint32_t*>(dst + e) = quantise4_by(v.x, v.y, s_new);
+            }
+            __syncwarp();  // a later token on the same offset writes after this one
+        }
+        if (lane == 0) entry[which] = s_new;
+        __syncwarp();
+    }
+    if (lane == 0) {
+        float* entry = kv_scales + ((size_t)blk * n_kv + g) * 4;
+        entry[2] = 0.f;
+        entry[3] = 0.f;
+    }
+}
+
+cudaError_t launch_kv_append_fp8_block(const void* k_new, const void* v_new,
+                                       const int32_t* slot_mapping, int num_tokens, int n_kv,
+                                       int head_dim, int block_size, int num_blocks,
+                                       void* kv_cache, float* kv_scales, cudaStream_t stream) {
+    const long long items = (long long)num_tokens * n_kv;
+    const long long blocks = (items + kAppendWarps - 1) / kAppendWarps;
+    kv_append_fp8_block_kernel<<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, stream>>>(
+        static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), slot_mapping,
+        num_tokens, n_kv, head_dim, block_size, (long long)num_blocks * block_size,
+        static_cast<uint8_t*>(kv_cache), kv_scales);
+    return cudaGetLastError();
+}
+
 // One thread moves one 16-byte chunk of a (K or V) block; consecutive threads
 // cover consecutive chunks of the same block, so reads and writes are full
 // 16-byte vector accesses over whole contiguous blocks.
+// scales (8-bit cache with per-block scales): the [num_blocks][n_kv][4] fp32
+// scale tensor, n_kv 16-byte chunks per block, copied by the threads that
+// would copy V (an interleaved cache has no separate V).
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                        const int32_t* __restrict__ pairs, int num_pairs, int num_blocks,
-                       long long chunks_per_block) {
+                       long long chunks_per_block, uint4* __restrict__ scales, int n_kv) {
     const long long total = (long long)num_pairs * 2 * chunks_per_block;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
@@ -140,6 +314,11 @@ __global__ void __launch_bounds__(256)
         const int p = static_cast<int>(rest >> 1);
         const int src = __ldg(pairs + 2 * p), dst = __ldg(pairs + 2 * p + 1);
         if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks || src == dst) continue;
+        if (which == 1 && scales != nullptr) {
+            if (chunk < n_kv)
+                scales[(size_t)dst * n_kv + chunk] = scales[(size_t)src * n_kv + chunk];
+            continue;
+        }
         uint4* cache = which == 0 ? k_cache : v_cache;
         if (cache == nullptr) continue;  // one interleaved cache: its blocks hold K and V
         cache[(size_t)dst * chunks_per_block + chunk] = cache[(size_t)src * chunks_per_block + chunk];
@@ -150,7 +329,7 @@ __global__ void __launch_bounds__(256)
 // null v_cache (an interleaved 8-bit cache) copies k_cache only.
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, int n_kv, int head_dim, int block_size,
-                               int elem_bytes, int num_sms, cudaStream_t stream) {
+                               int elem_bytes, void* scales, int num_sms, cudaStream_t stream) {
     const long long chunks = (long long)n_kv * block_size * head_dim * elem_bytes / 16;
     const long long total = (long long)num_pairs * 2 * chunks;
     long long blocks = (total + 255) / 256;
@@ -159,7 +338,7 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pair
     if (blocks < 1) blocks = 1;
     copy_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), pairs, num_pairs, num_blocks,
-        chunks);
+        chunks, static_cast<uint4*>(scales), n_kv);
     return cudaGetLastError();
 }
 

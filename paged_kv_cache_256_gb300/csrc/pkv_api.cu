@@ -329,11 +329,16 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     if (max_blocks_per_seq < 1 || num_blocks < 1) return PKV_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     if (p->window < 0) return PKV_ERR_INVALID_ARG;
-    if (p->kv_dtype != PKV_KV_BF16 && p->kv_dtype != PKV_KV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
-    const bool kv8 = p->kv_dtype == PKV_KV_FP8_E4M3;
-    if (num_seqs == 0) return PKV_OK;
-    if (kv8 && (!p->k_scale || !p->v_scale || !aligned(p->k_scale, 4) || !aligned(p->v_scale, 4)))
+    if (p->kv_dtype != PKV_KV_BF16 && p->kv_dtype != PKV_KV_FP8_E4M3 &&
+        p->kv_dtype != PKV_KV_FP8_E4M3_BLOCK)
         return PKV_ERR_INVALID_ARG;
+    const bool blk = p->kv_dtype == PKV_KV_FP8_E4M3_BLOCK;
+    const bool kv8 = p->kv_dtype == PKV_KV_FP8_E4M3 || blk;
+    if (num_seqs == 0) return PKV_OK;
+    if (kv8 && !blk &&
+        (!p->k_scale || !p->v_scale || !aligned(p->k_scale, 4) || !aligned(p->v_scale, 4)))
+        return PKV_ERR_INVALID_ARG;
+    if (blk && (!p->kv_scales || !aligned(p->kv_scales, 16))) return PKV_ERR_INVALID_ARG;
     // An 8-bit cache is one interleaved tensor, passed as k_cache; v_cache is NULL.
     if (kv8 ? v_cache != nullptr : v_cache == nullptr) return PKV_ERR_INVALID_ARG;
     if (!q || !k_cache || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
@@ -361,17 +366,17 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
 
-    CUtensorMap tk, tv, tq;
-    if (!cached_cache_map(&tk, k_cache, head_dim, rows_total, block_size, kv8) ||
-        !cached_cache_map(&tv, kv8 ? k_cache : v_cache, head_dim, rows_total, block_size, kv8))
+    AttnMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    if (!cached_cache_map(&maps.k, k_cache, head_dim, rows_total, block_size, kv8) ||
+        !cached_cache_map(&maps.v, kv8 ? k_cache : v_cache, head_dim, rows_total, block_size, kv8))
         return PKV_ERR_CUDA;
     // The tensor-memory consumer (more than 64 rows) takes its query tiles by
     // TMA when a tile is one box; otherwise its threads load them.
-    std::memset(&tq, 0, sizeof tq);
     int q_tma = 0, by = 0, bz = 0;
     if (rows > 64 && (long long)num_seqs * q_len < (1LL << 31) &&
         q_box(n_q / n_kv, rows, &by, &bz)) {
-        if (!cached_q_map(&tq, q, head_dim, n_q, (long long)num_seqs * q_len, by, bz))
+        if (!cached_q_map(&maps.q, q, head_dim, n_q, (long long)num_seqs * q_len, by, bz))
             return PKV_ERR_CUDA;
         q_tma = 1;
     }
@@ -401,8 +406,9 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     a.v_row_off = kv8 ? block_size : 0;
     a.warp_rows = warp_rows_for(rows);
     a.unit_cost = unit_cost_for(rows, kv8);
-    a.k_scale = kv8 ? p->k_scale : nullptr;
-    a.v_scale = kv8 ? p->v_scale : nullptr;
+    a.k_scale = (kv8 && !blk) ? p->k_scale : nullptr;
+    a.v_scale = (kv8 && !blk) ? p->v_scale : nullptr;
+    a.kv_scales = blk ? p->kv_scales : nullptr;
     // A window at least as wide as any context is no window.
     a.window = (long long)p->window >= (long long)max_blocks_per_seq * block_size ? 0 : p->window;
     a.checked = (flags & PKV_FLAG_CHECKED) ? 1 : 0;
@@ -414,8 +420,9 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool f32 = out_dtype == PKV_OUT_F32;
     const cudaError_t le =
-        kv8 ? launch_decode_attn_fp8(a, tk, tv, tq, head_dim, block_size, f32, grid, s)
-            : launch_decode_attn(a, tk, tv, tq, head_dim, block_size, f32, grid, s);
+        blk   ? launch_decode_attn_fp8_block(a, maps, head_dim, block_size, f32, grid, s)
+        : kv8 ? launch_decode_attn_fp8(a, maps, head_dim, block_size, f32, grid, s)
+              : launch_decode_attn(a, maps, head_dim, block_size, f32, grid, s);
     if (le != cudaSuccess) return PKV_ERR_CUDA;
     if (grid > 1 && launch_lse_merge(a, head_dim, f32, grid, s) != cudaSuccess)
         return PKV_ERR_CUDA;
@@ -470,26 +477,53 @@ int pkv_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_
     return PKV_OK;
 }
 
+int pkv_kv_append_fp8_block(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                            int num_tokens, int n_kv, int head_dim, int block_size,
+                            int num_blocks, void* kv_cache, float* kv_scales, unsigned flags,
+                            void* stream) {
+    (void)flags;
+    if (num_tokens < 0 || n_kv < 1 || head_dim < 8 || head_dim % 8 != 0 || head_dim > 1024 ||
+        block_size < 1 || num_blocks < 1)
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !kv_cache || !kv_scales) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(kv_cache, 16) ||
+        !aligned(slot_mapping, 4) || !aligned(kv_scales, 16))
+        return PKV_ERR_INVALID_ARG;
+    if ((long long)num_tokens * n_kv >= (1LL << 31) ||
+        (long long)num_blocks * block_size >= (1LL << 31))
+        return PKV_ERR_UNSUPPORTED;
+    if (launch_kv_append_fp8_block(k_new, v_new, slot_mapping, num_tokens, n_kv, head_dim,
+                                   block_size, num_blocks, kv_cache, kv_scales,
+                                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
 int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                     int num_blocks, int n_kv, int head_dim, int block_size, unsigned flags,
                     void* stream) {
     // An 8-bit cache is one tensor whose blocks hold K and V (1 byte each): a
-    // block is as many bytes as a bf16 K block, and there is no V pointer.
+    // block is as many bytes as a bf16 K block, and there is no V pointer;
+    // with per-block scales, v_cache is the scale tensor, copied with the blocks.
     const bool kv8 = (flags & PKV_FLAG_KV_FP8) != 0;
+    const bool blk = (flags & PKV_FLAG_KV_BLOCK_SCALES) != 0;
+    if (blk && !kv8) return PKV_ERR_INVALID_ARG;
     if (num_pairs < 0 || num_blocks < 1 || n_kv < 1 || head_dim < 8 || head_dim % 8 != 0 ||
         block_size < 1 || ((long long)n_kv * block_size * head_dim * 2) % 16 != 0)
         return PKV_ERR_INVALID_ARG;
     if (num_pairs == 0) return PKV_OK;
-    if (!k_cache || !pairs || (kv8 ? v_cache != nullptr : v_cache == nullptr))
+    if (!k_cache || !pairs || ((kv8 && !blk) ? v_cache != nullptr : v_cache == nullptr))
         return PKV_ERR_INVALID_ARG;
-    if (!aligned(k_cache, 16) || (!kv8 && !aligned(v_cache, 16)) || !aligned(pairs, 4))
+    if (!aligned(k_cache, 16) || (v_cache && !aligned(v_cache, 16)) || !aligned(pairs, 4))
         return PKV_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     const int sms = sm_count(dev);
     if (sms <= 0) return PKV_ERR_CUDA;
-    if (launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_blocks, n_kv, head_dim,
-                           block_size, 2, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (launch_copy_blocks(k_cache, kv8 ? nullptr : v_cache, pairs, num_pairs, num_blocks, n_kv,
+                           head_dim, block_size, 2, blk ? v_cache : nullptr, sms,
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
 }

@@ -49,6 +49,13 @@ struct AttnArgs {
     float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
     int q_tma;         // tensor-memory consumer: query tiles arrive by TMA (the q map is valid)
     int early_start;   // launched as a programmatic dependent of the previous kernel
+    const float* kv_scales;  // per-(block, KV head) scales [num_blocks][n_kv][4], or null
+};
+
+// The tensor maps of one attention launch: the K and V cache views and the
+// query tiles (tensor-memory consumer).
+struct AttnMaps {
+    CUtensorMap k, v, q;
 };
 
 struct WorkspaceLayout {
@@ -58,15 +65,15 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(int grid, int rows, int head_dim);
 
 
-cudaError_t launch_decode_attn(const AttnArgs& a, const CUtensorMap& tmap_k,
-                               const CUtensorMap& tmap_v, const CUtensorMap& tmap_q,
-                               int head_dim, int block_size,
-                               bool out_f32, int grid, cudaStream_t stream);
+cudaError_t launch_decode_attn(const AttnArgs& a, const AttnMaps& maps, int head_dim,
+                               int block_size, bool out_f32, int grid, cudaStream_t stream);
 
-cudaError_t launch_decode_attn_fp8(const AttnArgs& a, const CUtensorMap& tmap_k,
-                                   const CUtensorMap& tmap_v, const CUtensorMap& tmap_q,
-                                   int head_dim, int block_size,
-                                   bool out_f32, int grid, cudaStream_t stream);
+cudaError_t launch_decode_attn_fp8(const AttnArgs& a, const AttnMaps& maps, int head_dim,
+                                   int block_size, bool out_f32, int grid, cudaStream_t stream);
+
+cudaError_t launch_decode_attn_fp8_block(const AttnArgs& a, const AttnMaps& maps, int head_dim,
+                                         int block_size, bool out_f32, int grid,
+                                         cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const AttnArgs& a, int head_dim, bool out_f32, int grid,
                              cudaStream_t stream);
@@ -82,8 +89,13 @@ cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new,
                                  const float* k_scale, const float* v_scale, void* kv_cache,
                                  int num_sms, cudaStream_t stream);
 
+cudaError_t launch_kv_append_fp8_block(const void* k_new, const void* v_new,
+                                       const int32_t* slot_mapping, int num_tokens, int n_kv,
+                                       int head_dim, int block_size, int num_blocks,
+                                       void* kv_cache, float* kv_scales, cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, int n_kv, int head_dim, int block_size,
-                               int elem_bytes, int num_sms, cudaStream_t stream);
+                               int elem_bytes, void* scales, int num_sms, cudaStream_t stream);
 
 }  // namespace pkv

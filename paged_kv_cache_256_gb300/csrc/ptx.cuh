@@ -96,6 +96,23 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// 16 bytes global -> shared as one (non-tensor) bulk copy, completing on `bar`
+// (tx bytes).  Both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_load_16(void* dst, const void* src, uint64_t* bar,
+                                             uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(16u), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory writes before later
+// async-proxy (bulk copy, tensor core) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem_cta() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 3-D tiled bulk tensor load global -> shared, completing on `bar` (tx bytes).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
                                             uint64_t* bar) {

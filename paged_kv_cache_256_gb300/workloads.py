@@ -52,6 +52,7 @@ __all__ = [
     "E4M3_POISON",
     "Fp8Cache",
     "fp8_cache_for",
+    "fp8_block_scales_for",
     "CONFIGS",
     "Workload",
     "f32_to_bf16_bits",
@@ -239,6 +240,18 @@ def fp8_cache_for(wl: Workload, seed: int | None = None) -> Fp8Cache:
     vs = r.uniform(0.05, 0.5, size=wl.n_kv).astype(np.float32)
     kv = np.ascontiguousarray(np.stack([k8, v8], axis=2))
     return Fp8Cache(kv_cache=kv, k_scale=ks, v_scale=vs)
+
+
+def fp8_block_scales_for(wl: Workload, seed: int | None = None) -> np.ndarray:
+    """Seeded per-(block, KV head) scales [num_blocks, n_kv, 4] float32 for an 8-bit cache:
+    a K and a V scale per block, powers of two 2^k with k uniform in [-8, -3], then two
+    zero words."""
+    if seed is None:
+        seed = 7000 + sum(wl.name.encode())
+    r = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 13])))
+    sc = np.zeros((wl.num_blocks, wl.n_kv, 4), dtype=np.float32)
+    sc[:, :, 0:2] = np.ldexp(np.float32(1.0), r.integers(-8, -2, size=(wl.num_blocks, wl.n_kv, 2)))
+    return sc
 
 
 def _draw_context_lens(rng, spec, num_seqs):

@@ -196,8 +196,17 @@ def test_params_entry_host_checks(lib):
                                         None) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_paged_decode_attn_ex(ctypes.byref(_params(head_dim=96)),
                                         None) == _lib.PKV_ERR_UNSUPPORTED
-    assert lib.pkv_paged_decode_attn_ex(ctypes.byref(_params(kv_dtype=2)),
+    assert lib.pkv_paged_decode_attn_ex(ctypes.byref(_params(kv_dtype=3)),
                                         None) == _lib.PKV_ERR_INVALID_ARG
+    # per-block scales: the scale tensor is required and 16-byte aligned
+    blk = _lib.PKV_KV_FP8_E4M3_BLOCK
+    assert lib.pkv_paged_decode_attn_ex(
+        ctypes.byref(_params(num_seqs=2, kv_dtype=blk, v_cache=None)),
+        None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_paged_decode_attn_ex(
+        ctypes.byref(_params(num_seqs=2, kv_dtype=blk, v_cache=None, kv_scales=FAKE + 8)),
+        None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_paged_decode_attn_ex(ctypes.byref(_params(kv_dtype=blk)), None) == _lib.PKV_OK
     # an 8-bit cache needs its scales and no V pointer (checked before any device call)
     assert lib.pkv_paged_decode_attn_ex(
         ctypes.byref(_params(num_seqs=2, kv_dtype=_lib.PKV_KV_FP8_E4M3)),
@@ -207,6 +216,25 @@ def test_params_entry_host_checks(lib):
                              v_scale=FAKE)), None) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_paged_decode_attn_ex(
         ctypes.byref(_params(kv_dtype=_lib.PKV_KV_FP8_E4M3)), None) == _lib.PKV_OK
+
+
+def test_fp8_block_append_and_copy_host_checks(lib):
+    args = [FAKE, FAKE, FAKE, 4, 2, 64, 16, 8, FAKE, None, 0, None]
+    assert lib.pkv_kv_append_fp8_block(*args) == _lib.PKV_ERR_INVALID_ARG  # null kv_scales
+    args[9] = FAKE + 4
+    assert lib.pkv_kv_append_fp8_block(*args) == _lib.PKV_ERR_INVALID_ARG  # misaligned scales
+    args[9] = FAKE
+    args[5] = 60
+    assert lib.pkv_kv_append_fp8_block(*args) == _lib.PKV_ERR_INVALID_ARG  # head_dim % 8
+    args[5], args[3] = 64, 0
+    assert lib.pkv_kv_append_fp8_block(*args) == _lib.PKV_OK  # nothing to append
+    # block scales need the 8-bit flag and a scale tensor in place of v_cache
+    both = _lib.PKV_FLAG_KV_FP8 | _lib.PKV_FLAG_KV_BLOCK_SCALES
+    assert lib.pkv_copy_blocks(FAKE, FAKE, FAKE, 1, 8, 2, 64, 16, _lib.PKV_FLAG_KV_BLOCK_SCALES,
+                               None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy_blocks(FAKE, None, FAKE, 1, 8, 2, 64, 16, both,
+                               None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy_blocks(FAKE, FAKE, FAKE, 0, 8, 2, 64, 16, both, None) == _lib.PKV_OK
 
 
 def test_fp8_append_and_copy_host_checks(lib):

@@ -73,16 +73,10 @@ MUTANTS = {
     "fp8_block_requantise_all_rows": ("for (long r = 0; r < o_min; ++r)",
                                       "for (long r = 0; r < block_size; ++r)"),
     "fp8_block_amax_first_token_only": (
-        "                for (int j = i; j < num_tokens; ++j) {\n"
-        "                    const long sj = slot_mapping[j];\n"
-        "                    if (sj < 0 || sj >= nslots || sj / block_size != blk)\n"
-        "                        continue;\n"
+        "                for (int j = i; j >= 0; j = next[j])\n"
         "                    for (int e = 0; e < head_dim; ++e) {\n"
         "                        const double x",
-        "                for (int j = i; j < i + 1; ++j) {\n"
-        "                    const long sj = slot_mapping[j];\n"
-        "                    if (sj < 0 || sj >= nslots || sj / block_size != blk)\n"
-        "                        continue;\n"
+        "                for (int j = i; j == i; j = next[j])\n"
         "                    for (int e = 0; e < head_dim; ++e) {\n"
         "                        const double x"),
     "copy_direction_swapped": ("memcpy(k_cache + (size_t)dst * per_block, k_cache + (size_t)src * per_block,",
