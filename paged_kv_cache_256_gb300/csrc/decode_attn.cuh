@@ -540,6 +540,19 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
     bool ok = true;
     while (w.left > 0 && ok) {
         const int j1 = piece_end(w);
+        // The consumers load this unit's query rows when they reach it, about a
+        // ring later: fetch them into the L2 now (one bulk prefetch per query
+        // token of the row tile), so that load does not wait on HBM.
+        {
+            const int R0 = w.t * a.rows, R1 = min(a.rows_total, R0 + a.rows);
+            const int i0 = R0 / a.group, i1 = (R1 - 1) / a.group;
+            for (int i = i0 + lane; i <= i1; i += 32) {
+                const int lo = max(R0, i * a.group) - i * a.group;
+                const int hi = min(R1, (i + 1) * a.group) - i * a.group;
+                prefetch_l2_bulk(a.q + (((size_t)w.s * a.q_len + i) * a.n_q + w.h * a.group + lo) * D,
+                                 static_cast<uint32_t>((hi - lo) * D * 2));
+            }
+        }
         const int32_t* bt = a.block_tables + (size_t)w.s * a.max_blocks_per_seq;
         int my = w.j + lane < j1 ? __ldg(bt + w.j + lane) : 0;
         for (int jb = w.j; jb < j1 && ok; jb += 32) {
@@ -1861,24 +1874,43 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     }
                     const uint8_t* src = stages + st * C::kStageBytes + isv * C::kBoxBytes;
                     uint8_t* dst = cvt + (g & 1u) * kCopy + isv * kHalves * C::kCvtRegion;
-                    // item = (key row n, 16-byte chunk cb of e4m3 codes)
-                    for (int it = lane; it < 64 * kChunks; it += 32) {
-                        const int nrow = it / kChunks, cb = it % kChunks;
-                        const int b = nrow / BS, r = nrow % BS;
-                        uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
-                        if (b < nb && tok0 + nrow < ctx) {  // a resident key: widen
-                            const uint8_t* box = src + b * 2 * C::kBoxBytes;
-                            const uint4 v = *reinterpret_cast<const uint4*>(box + swz8<D>(r, cb * 16));
-                            e4m3x4_to_f16x2x2(v.x, o0.x, o0.y);
-                            e4m3x4_to_f16x2x2(v.y, o0.z, o0.w);
-                            e4m3x4_to_f16x2x2(v.z, o1.x, o1.y);
-                            e4m3x4_to_f16x2x2(v.w, o1.z, o1.w);
+                    // item = (key row n, 16-byte chunk cb of e4m3 codes), 32 items per
+                    // round; four rounds' loads are issued before any is widened (one
+                    // round at a time left each load's latency exposed: ~1.4 us per
+                    // 64-key stage).  Rows of blocks past the stage's last are read (they
+                    // lie inside the stage) and replaced by zeros, as are keys past the
+                    // context.
+                    constexpr int kRounds = 64 * kChunks / 32, kBatch = 4;
+                    static_assert(kRounds % kBatch == 0, "converter rounds");
+#pragma unroll
+                    for (int r0 = 0; r0 < kRounds; r0 += kBatch) {
+                        uint4 v[kBatch];
+                        bool res[kBatch];
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) {
+                            const int it = lane + 32 * (r0 + u);
+                            const int nrow = it / kChunks, cb = it % kChunks;
+                            const int b = nrow / BS, r = nrow % BS;
+                            res[u] = b < nb && tok0 + nrow < ctx;  // a resident key
+                            v[u] = *reinterpret_cast<const uint4*>(src + b * 2 * C::kBoxBytes +
+                                                                   swz8<D>(r, cb * 16));
                         }
-                        // f16 chunks 2cb, 2cb + 1 (d 16cb ..): region (2cb) / 8, chunk (2cb) % 8
-                        uint8_t* row = dst + ((2 * cb) / 8) * C::kCvtRegion + nrow * 128;
-                        const int c0 = (2 * cb) % 8;
-                        *reinterpret_cast<uint4*>(row + ((c0 ^ (nrow & 7)) << 4)) = o0;
-                        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (nrow & 7)) << 4)) = o1;
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) {
+                            const int it = lane + 32 * (r0 + u);
+                            const int nrow = it / kChunks, cb = it % kChunks;
+                            uint4 o0, o1;
+                            e4m3x4_to_f16x2x2(v[u].x, o0.x, o0.y);
+                            e4m3x4_to_f16x2x2(v[u].y, o0.z, o0.w);
+                            e4m3x4_to_f16x2x2(v[u].z, o1.x, o1.y);
+                            e4m3x4_to_f16x2x2(v[u].w, o1.z, o1.w);
+                            if (!res[u]) o0 = o1 = make_uint4(0u, 0u, 0u, 0u);
+                            // f16 chunks 2cb, 2cb + 1 (d 16cb ..): region (2cb) / 8, chunk (2cb) % 8
+                            uint8_t* row = dst + ((2 * cb) / 8) * C::kCvtRegion + nrow * 128;
+                            const int c0 = (2 * cb) % 8;
+                            *reinterpret_cast<uint4*>(row + ((c0 ^ (nrow & 7)) << 4)) = o0;
+                            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (nrow & 7)) << 4)) = o1;
+                        }
                     }
                     fence_proxy_async_smem();  // the copy, for the tensor cores
                     __syncwarp();

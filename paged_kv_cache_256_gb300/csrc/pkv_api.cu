@@ -189,15 +189,17 @@ int check_shape(int num_seqs, int q_len, int n_q, int n_kv, int head_dim, int bl
 
 // A unit's fixed work (query load, cross-warp combine, output) in blocks of
 // streaming time: the weight the work partition gives each unit on top of
-// its blocks.  Measured per consumer on GB300 (ragged GQA, MQA verify and
-// chunked-prefill batches; uniform contexts do not care): rows <= 8 -- 6 for
-// bf16, 32 for 8-bit blocks, which stream in half the time while the unit's
-// fixed work grows (Q widened to f16); 8 < rows <= 64 with an 8-bit cache --
-// 4 (every row-slice warp widens each tile, so blocks cost more);
-// tensor-memory consumer -- 12 (the O read-out per unit and the pipeline
-// fill), 10 over an 8-bit cache (blocks cost more: each is widened to f16).
+// its blocks.  Measured per consumer on GB300 with the L2 evicted before each
+// call (ragged GQA, MQA verify and chunked-prefill batches; uniform contexts
+// do not care): rows <= 8 -- 10 for bf16 (GQA 168.4 / 166.4 / 163.9 / 164.4 /
+// 166.3 us at 6 / 8 / 10 / 12 / 16), 32 for 8-bit blocks, which stream in
+// half the time while the unit's fixed work grows (Q widened to f16);
+// 8 < rows <= 64 with an 8-bit cache -- 4 (every row-slice warp widens each
+// tile, so blocks cost more); tensor-memory consumer -- 12 (the O read-out
+// per unit and the pipeline fill), 10 over an 8-bit cache (blocks cost more:
+// each is widened to f16).
 int unit_cost_for(int rows, bool kv8) {
-    if (rows <= 8) return kv8 ? 32 : 6;
+    if (rows <= 8) return kv8 ? 32 : 10;
     if (rows > 64) return kv8 ? 10 : 12;
     return kv8 ? 4 : 6;
 }

@@ -107,6 +107,14 @@ __device__ __forceinline__ void bulk_load_16(void* dst, const void* src, uint64_
         : "memory");
 }
 
+// Fetch `bytes` (a multiple of 16, from a 16-byte aligned address) of global
+// memory into the L2 without waiting for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // Order this thread's earlier generic-proxy shared-memory writes before later
 // async-proxy (bulk copy, tensor core) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem_cta() {
