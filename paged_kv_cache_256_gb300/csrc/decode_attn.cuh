@@ -71,6 +71,15 @@ namespace pkv {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+// The tensor-memory consumer over an 8-bit cache adds three warps (9, 10, 11)
+// that widen stages to f16 beside warps 6 and 7: five converter warps on
+// schedulers 2, 3, 1, 2, 3 (two warps on schedulers 2 and 3 alone took
+// ~1.2 us per 64-key stage, the pace of the whole pipeline).  ptxas caps a
+// thread at 168 registers for 288 and for 384 threads alike.
+constexpr int kTmemConverters = 5;
+__host__ __device__ constexpr int threads_for(int mode, bool kv8) {
+    return mode == 2 && kv8 ? kThreads + 3 * 32 : kThreads;
+}
 constexpr int kMergeSlots = 4;                   // warps that park a partial per merge round
 constexpr int kIssueLanes = 8;                   // producer lanes issuing loads side by side
 constexpr int kNarrowRows = 8;                   // rows up to which the narrow consumer is used
@@ -328,8 +337,9 @@ __device__ __forceinline__ int piece_end(const Walk& w) {
     return (long long)w.nb < (long long)w.j + w.left ? w.nb : static_cast<int>(w.j + w.left);
 }
 
-// Block-wide inclusive scan of two 64-bit values per thread (all kThreads);
-// s_red holds 2 * kThreads / 32 values.
+// Block-wide inclusive scan of two 64-bit values per thread (all NT threads);
+// s_red holds 2 * NT / 32 values.
+template <int NT>
 __device__ __forceinline__ void block_inclusive_scan2(long long& c, long long& r, long long* s_red,
                                                       long long& total_c, long long& total_r) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -350,7 +360,7 @@ __device__ __forceinline__ void block_inclusive_scan2(long long& c, long long& r
     long long bc = 0, br = 0;
     total_c = total_r = 0;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
         const long long tc = s_red[2 * w], tr = s_red[2 * w + 1];
         if (w < warp) {
             bc += tc;
@@ -425,21 +435,21 @@ __device__ __forceinline__ ItemPos cost_to_item(const AttnArgs& a, int ctx, long
 // round), which measured several times faster than unrolled variants.
 constexpr int kSliceSeqs = 1;
 
-template <int BS>
+template <int BS, int NT>
 __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
                                            long long* s_pos, Walk* s_walk) {
     const int tid = threadIdx.x, cta = blockIdx.x, grid = gridDim.x;
-    constexpr int kRound = kThreads * kSliceSeqs;
+    constexpr int kRound = NT * kSliceSeqs;
     long long total_c = 0, total_r = 0;
     if (a.num_seqs > kRound) {  // several rounds: totals first
         long long mc = 0, mr = 0;
-        for (int s = tid; s < a.num_seqs; s += kThreads) {
+        for (int s = tid; s < a.num_seqs; s += NT) {
             const int ctx = unit_ctx(a, s, BS);
             const long long hi = head_items(a, ctx, BS);
             mc += ctx > 0 ? (hi + (long long)a.q_tiles * a.unit_cost) * a.n_kv : 0;
             mr += hi * a.n_kv;
         }
-        block_inclusive_scan2(mc, mr, s_red, total_c, total_r);
+        block_inclusive_scan2<NT>(mc, mr, s_red, total_c, total_r);
     }
     long long start = 0, end = 0, base_c = 0, base_r = 0;
     for (int s0 = 0; s0 < a.num_seqs; s0 += kRound) {
@@ -458,7 +468,7 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
         }
         const long long lc = ic, lr = ir;
         long long rc, rr;
-        block_inclusive_scan2(ic, ir, s_red, rc, rr);
+        block_inclusive_scan2<NT>(ic, ir, s_red, rc, rr);
         if (a.num_seqs <= kRound) {
             total_c = rc;
             total_r = rr;
@@ -1592,8 +1602,8 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 // PV update of one overlaps the softmax of the next.  TMEM columns: O
 // [0, 128), S 2 x 64 from 128, P 2 x 32 from 256, the low halves of P for
 // fp32 output 2 x 32 from 320.
-// Over an 8-bit cache (KV8) warps 6 and 7 widen each landed stage into one of
-// two f16 copies (K and V in the layout the bf16 stages have, V rows past the
+// Over an 8-bit cache (KV8) five converter warps (6, 7, 9, 10, 11) widen each
+// landed stage into one of two f16 copies (K and V in the layout the bf16 stages have, V rows past the
 // context zeroed) and free the stage; the MMAs read the copies as kind::f16
 // with Q and P in f16 (every e4m3 value is exact in f16), and the PV product
 // frees the copy.  The per-head K scale joins the score scale, the V scale
@@ -1635,7 +1645,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     constexpr uint32_t kColO = 0, kColS = 128, kColP = 256, kColPL = 320;
     constexpr int KT = D / 16;   // k steps of S = Q K^T
     constexpr int kQHalf = 128 * 128;  // bytes of one 64-column half of the Q tile
-    constexpr int kParty = KV8 ? 256 : 192;  // warps 0..5 take part (0..7 with converters)
+    // warps 0..5 take part, and the converter warps 6, 7, 9, 10, 11 over an 8-bit cache
+    constexpr int kParty = KV8 ? threads_for(kModeTmem, true) - 32 : 192;
     constexpr int kHalves = D / 64;          // 64-column regions of an f16 K or V copy
     // tcb: [0..1] S ready, [2..3] S read, [4..5] P ready, [6..7] PV done, [8] QK teardown,
     //      [9] PV teardown, [10..13] f16 copies, [14] Q landed, [15] Q read, [16] Q widened
@@ -1843,13 +1854,18 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             }
             __syncwarp();
         } else if (warp >= 6) {
-            // ===================== f16 copies (8-bit cache; warps 6, 7) ============
+            // ===================== f16 copies (8-bit cache; five warps) ============
             if constexpr (KV8) {
-                // Warp 6 widens the K rows, warp 7 the V rows; each arrives on
-                // its own (the copy-ready and stage-free barriers count 2), so
-                // neither ever waits for the other.
-                const int isv = warp - 6;
-                constexpr int kChunks = D / 16;  // 16-byte e4m3 chunks per row
+                // A stage's 2 x 64 rows (K rows, then V rows) are 2 * kRounds rounds
+                // of 32 (row, 16-byte chunk) items; round k goes to converter k % 5
+                // (warps 6, 7, 9, 10, 11).  Each converter arrives on its own when its
+                // rounds are done (the copy-ready and stage-free barriers count 5).
+                const int ci = warp < kConsumerWarps ? warp - 6 : warp - 7;
+                constexpr int kChunks = D / 16;             // 16-byte e4m3 chunks per row
+                constexpr int kRounds = 64 * kChunks / 32;  // rounds of K (or of V)
+                constexpr int kAll = 2 * kRounds;
+                constexpr int kMine = (kAll + kTmemConverters - 1) / kTmemConverters;
+                constexpr int kBatch = 4;  // rounds whose loads are issued together
                 for (int q = 0; q < nsb; ++q) {
                     const uint32_t g = gbase + q, st = g % kStages;
                     bool good = !*s_abort && mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u);
@@ -1866,38 +1882,39 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     const int nb = min(SB, n - q * SB);
                     const int tok0 = (j0 + q * SB) * BS;
                     if constexpr (BLK) {
-                        // this warp's half of the blocks' scales (K: warp 6, V: warp 7),
-                        // before the stage is given back
-                        if (lane < nb)
-                            cvt_sc[((g & 1u) * SB + lane) * 2 + isv] =
-                                reinterpret_cast<const float*>(slots + (st * SB + lane) * 16)[isv];
+                        // the blocks' scales (K: converter 0, V: converter 1), before the
+                        // stage is given back
+                        if (ci < 2 && lane < nb)
+                            cvt_sc[((g & 1u) * SB + lane) * 2 + ci] =
+                                reinterpret_cast<const float*>(slots + (st * SB + lane) * 16)[ci];
                     }
-                    const uint8_t* src = stages + st * C::kStageBytes + isv * C::kBoxBytes;
-                    uint8_t* dst = cvt + (g & 1u) * kCopy + isv * kHalves * C::kCvtRegion;
-                    // item = (key row n, 16-byte chunk cb of e4m3 codes), 32 items per
-                    // round; four rounds' loads are issued before any is widened (one
-                    // round at a time left each load's latency exposed: ~1.4 us per
-                    // 64-key stage).  Rows of blocks past the stage's last are read (they
-                    // lie inside the stage) and replaced by zeros, as are keys past the
-                    // context.
-                    constexpr int kRounds = 64 * kChunks / 32, kBatch = 4;
-                    static_assert(kRounds % kBatch == 0, "converter rounds");
+                    const uint8_t* stage_src = stages + st * C::kStageBytes;
+                    uint8_t* copy = cvt + (g & 1u) * kCopy;
+                    // Rows of blocks past the stage's last are read (they lie inside the
+                    // stage) and replaced by zeros, as are keys past the context.
 #pragma unroll
-                    for (int r0 = 0; r0 < kRounds; r0 += kBatch) {
+                    for (int j0r = 0; j0r < kMine; j0r += kBatch) {
                         uint4 v[kBatch];
                         bool res[kBatch];
 #pragma unroll
                         for (int u = 0; u < kBatch; ++u) {
-                            const int it = lane + 32 * (r0 + u);
-                            const int nrow = it / kChunks, cb = it % kChunks;
-                            const int b = nrow / BS, r = nrow % BS;
-                            res[u] = b < nb && tok0 + nrow < ctx;  // a resident key
-                            v[u] = *reinterpret_cast<const uint4*>(src + b * 2 * C::kBoxBytes +
-                                                                   swz8<D>(r, cb * 16));
+                            const int k = ci + kTmemConverters * (j0r + u);
+                            res[u] = false;
+                            if (j0r + u < kMine && k < kAll) {
+                                const int isv = k / kRounds, it = lane + 32 * (k % kRounds);
+                                const int nrow = it / kChunks, cb = it % kChunks;
+                                const int b = nrow / BS, r = nrow % BS;
+                                res[u] = b < nb && tok0 + nrow < ctx;  // a resident key
+                                v[u] = *reinterpret_cast<const uint4*>(
+                                    stage_src + isv * C::kBoxBytes + b * 2 * C::kBoxBytes +
+                                    swz8<D>(r, cb * 16));
+                            }
                         }
 #pragma unroll
                         for (int u = 0; u < kBatch; ++u) {
-                            const int it = lane + 32 * (r0 + u);
+                            const int k = ci + kTmemConverters * (j0r + u);
+                            if (!(j0r + u < kMine && k < kAll)) continue;
+                            const int isv = k / kRounds, it = lane + 32 * (k % kRounds);
                             const int nrow = it / kChunks, cb = it % kChunks;
                             uint4 o0, o1;
                             e4m3x4_to_f16x2x2(v[u].x, o0.x, o0.y);
@@ -1906,7 +1923,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                             e4m3x4_to_f16x2x2(v[u].w, o1.z, o1.w);
                             if (!res[u]) o0 = o1 = make_uint4(0u, 0u, 0u, 0u);
                             // f16 chunks 2cb, 2cb + 1 (d 16cb ..): region (2cb) / 8, chunk (2cb) % 8
-                            uint8_t* row = dst + ((2 * cb) / 8) * C::kCvtRegion + nrow * 128;
+                            uint8_t* row = copy + isv * kHalves * C::kCvtRegion +
+                                           ((2 * cb) / 8) * C::kCvtRegion + nrow * 128;
                             const int c0 = (2 * cb) % 8;
                             *reinterpret_cast<uint4*>(row + ((c0 ^ (nrow & 7)) << 4)) = o0;
                             *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (nrow & 7)) << 4)) = o1;
@@ -1916,7 +1934,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(&cvt_full[g & 1u]);
-                        mbar_arrive(&empty_bar[st]);  // (both warps: the e4m3 stage is free)
+                        mbar_arrive(&empty_bar[st]);  // (every converter: the e4m3 stage is free)
                     }
                 }
             }
@@ -2213,7 +2231,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
 
 // ===================== kernel =====================
 template <int D, int BS, bool OUT_F32, int MODE, bool KV8, bool BLK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
     paged_decode_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v,
                              const __grid_constant__ CUtensorMap tmap_q, const AttnArgs a) {
@@ -2231,7 +2249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // BLK: the scale slots of the ring, kBlocksPerStage x 16 bytes per stage
     uint8_t* slots = reinterpret_cast<uint8_t*>(empty_bar + kStages);
 
-    __shared__ long long s_red[2 * kThreads / 32];
+    constexpr int NT = threads_for(MODE, KV8);
+    __shared__ long long s_red[2 * NT / 32];
     __shared__ long long s_pos[4];
     __shared__ Walk s_walk;
     __shared__ int s_abort;
@@ -2243,9 +2262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Arrivals that release a stage: one per 16-row slice (wide), one warp
-    // (narrow), one tensor-core commit (TMEM mode), the two converter warps
+    // (narrow), one tensor-core commit (TMEM mode), the five converter warps
     // (TMEM mode over an 8-bit cache).
-    const int releases = MODE == kModeWide ? a.warp_rows : (MODE == kModeTmem && KV8 ? 2 : 1);
+    const int releases =
+        MODE == kModeWide ? a.warp_rows : (MODE == kModeTmem && KV8 ? kTmemConverters : 1);
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full_bar[i], 1);
@@ -2254,10 +2274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (MODE == kModeTmem) {
             // S ready (a commit), S read (128 rows), P ready (128 rows),
             // PV done (a commit), two issuer teardowns (a commit each), f16
-            // copy ready (two converter warps) / free (a commit), query tile
+            // copy ready (the converter warps) / free (a commit), query tile
             // landed (the TMA) / read (a commit) / widened (128 rows)
-            const uint32_t counts[17] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1, KV8 ? 2u : 1u,
-                                         KV8 ? 2u : 1u, 1, 1, 1, 1, 128};
+            const uint32_t cvt = KV8 ? (uint32_t)kTmemConverters : 1u;
+            const uint32_t counts[17] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1, cvt, cvt,
+                                         1, 1, 1, 1, 128};
             for (int i = 0; i < 17; ++i) mbar_init(&s_tcb[i], counts[i]);
         }
         fence_barrier_init();
@@ -2268,7 +2289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
-    const Walk w0 = find_slice<BS>(a, s_red, s_pos, &s_walk);  // also publishes the barrier init
+    const Walk w0 = find_slice<BS, NT>(a, s_red, s_pos, &s_walk);  // also publishes the barrier init
     // This kernel is launched as a programmatic dependent of the previous
     // kernel on the stream: the work partition above (which reads only the
     // context lengths) may overlap it, e.g. the cache append that precedes
@@ -2356,7 +2377,7 @@ static cudaError_t launch_one(const AttnArgs& a, const AttnMaps& m, int grid,
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_for(MODE, KV8), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
