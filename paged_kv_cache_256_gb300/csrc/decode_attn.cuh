@@ -530,10 +530,11 @@ __device__ __forceinline__ Walk find_slice(const AttnArgs& a, long long* s_red,
 // over the lanes, so a freed stage is refilled at once instead of waiting for
 // the stages issued beside it, and the first stages of a launch land first
 // instead of together.
-// BLK: each block's 16-byte scale entry comes with its tiles, as a plain
-// 16-byte bulk copy into the stage's slot; an out-of-range block id (whose
-// tiles read zeros) gets a zero slot written by the issuing lane before the
-// stage's arrival, and no copy.
+// BLK: each block's 16-byte scale entry comes with its tiles into the stage's
+// slot, by an LSU asynchronous copy tracked by the stage's full barrier (as
+// 16-byte TMA bulk copies they cost 8-bit GQA 14 us of 115: twice the TMA
+// operations per stage); an out-of-range block id (whose tiles read zeros)
+// gets a zero slot written by the issuing lane before the stage's arrival.
 template <int D, int BS, int kStages, int kStageBytes, int kTileBytes, int kBoxBytes, int kBoxes,
           int kBoxCols, int kRegion, int SBS, bool KV8, bool ORDERED, bool BLK>
 __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tmap_k,
@@ -597,29 +598,25 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                         break;
                     }
                     // BLK: lane b < nb owns block b's scale slot (one box per block)
-                    uint32_t slot_tx = 0;
                     if constexpr (BLK) {
                         static_assert(kBpb == 1, "scale slots assume one box per block");
-                        const bool mine = lane < nb;
-                        if (mine && blk < 0) {
-                            *reinterpret_cast<uint4*>(slots + (stage * SBS + lane) * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
-                            fence_proxy_async_smem_cta();
+                        if (lane < nb) {
+                            uint8_t* slot = slots + (stage * SBS + lane) * 16;
+                            if (blk >= 0) {
+                                cp_async_16(slot, scale_src(blk));
+                                cp_async_mbar_arrive(&full_bar[stage]);
+                            } else {
+                                *reinterpret_cast<uint4*>(slot) = make_uint4(0u, 0u, 0u, 0u);
+                            }
                         }
-                        slot_tx = 16u * __popc(__ballot_sync(0xffffffffu, mine && blk >= 0));
-                        __syncwarp();  // the zero slots before the stage's arrival
+                        __syncwarp();  // the slots' arrivals and zeros before the stage's arrival
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes + slot_tx);
+                    if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes);
                     if (lane < nb * kBpb) {
                         const int b = lane / kBpb, box = lane % kBpb;
                         const long long y64 = ((long long)blk * a.n_kv + w.h) * a.kv_mul * BS;
                         const bool oob = blk < 0 || y64 >= a.tile_rows_total;
                         const int yk = oob ? a.tile_rows_total : static_cast<int>(y64);
-                        if constexpr (BLK) {
-                            if (blk >= 0)
-                                bulk_load_16(slots + (stage * SBS + b) * 16, scale_src(blk),
-                                             &full_bar[stage], policy);
-                        }
                         if constexpr (KV8) {
                             tma_load_2d(stages + stage * kStageBytes + b * 2 * kBoxBytes, tmap_k,
                                         0, yk, &full_bar[stage], policy);
@@ -659,24 +656,25 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                 const unsigned issue_mask =
                     fail ? (good_mask & ((1u << (__ffs(fail) - 1)) - 1u)) : good_mask;
                 const bool do_issue = (issue_mask >> lane) & 1u;
-                uint32_t slot_tx = 0;
                 if constexpr (BLK) {
-                    // this lane's stage: zero slots for out-of-range ids, a copy for the rest
-                    bool zeroed = false;
+                    // this lane's stage: a copy for each in-range block, zeros for the rest
+                    if (do_issue) {
+                        bool copied = false;
 #pragma unroll
-                    for (int b = 0; b < SBS; ++b) {
-                        if (!do_issue || b >= nb) continue;
-                        if (blks[b] >= 0) {
-                            slot_tx += 16u;
-                        } else {
-                            *reinterpret_cast<uint4*>(slots + (stage * SBS + b) * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
-                            zeroed = true;
+                        for (int b = 0; b < SBS; ++b) {
+                            if (b >= nb) continue;
+                            uint8_t* slot = slots + (stage * SBS + b) * 16;
+                            if (blks[b] >= 0) {
+                                cp_async_16(slot, scale_src(blks[b]));
+                                copied = true;
+                            } else {
+                                *reinterpret_cast<uint4*>(slot) = make_uint4(0u, 0u, 0u, 0u);
+                            }
                         }
+                        if (copied) cp_async_mbar_arrive(&full_bar[stage]);
                     }
-                    if (zeroed) fence_proxy_async_smem_cta();
                 }
-                if (do_issue) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes + slot_tx);
+                if (do_issue) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes);
 #pragma unroll
                 for (int b = 0; b < SBS; ++b) {
                     const int blk = blks[b];
@@ -688,11 +686,6 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                         const bool oob = blk < 0 || y64 >= a.tile_rows_total;
                         const int yk = oob ? a.tile_rows_total : static_cast<int>(y64);
                         const int yv = oob ? a.tile_rows_total : yk + a.v_row_off;
-                        if constexpr (BLK) {
-                            if (blk >= 0)
-                                bulk_load_16(slots + (stage * SBS + b) * 16, scale_src(blk),
-                                             &full_bar[stage], policy);
-                        }
                         if constexpr (KV8) {
                             // one box of 2 * BS rows: the K rows, then the V rows
                             tma_load_2d(stages + stage * kStageBytes + b * 2 * kBoxBytes, tmap_k,
@@ -2288,6 +2281,26 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
     if (warp == kConsumerWarps && lane == 0) {
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
+        // Small tables read piecemeal later, fetched into the L2 now with one
+        // sequential prefetch per CTA (each CTA a 1/grid share): the block
+        // tables, which the producers read right after the work partition, and
+        // (per-block scales) the scale entries, one 16-byte read per block that
+        // from HBM cost a random access each (8-bit GQA 116.0 -> 101.3 us without them).
+        auto share = [&](const void* base, size_t bytes) {
+            const size_t per = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~size_t(15);
+            const size_t lo = per * blockIdx.x;
+            if (lo < bytes) {
+                const size_t n = bytes - lo < per ? bytes - lo : per;
+                prefetch_l2_bulk(static_cast<const uint8_t*>(base) + lo, static_cast<uint32_t>(n));
+            }
+        };
+        // (the tables are only 4-byte aligned: the prefetch covers the 16-byte-aligned
+        // interior of their span and never reaches past it)
+        const uintptr_t tb = reinterpret_cast<uintptr_t>(a.block_tables);
+        const uintptr_t t0 = (tb + 15) & ~uintptr_t(15);
+        const uintptr_t t1 = (tb + (size_t)a.num_seqs * a.max_blocks_per_seq * 4) & ~uintptr_t(15);
+        if (t1 > t0) share(reinterpret_cast<const void*>(t0), t1 - t0);
+        if (BLK) share(a.kv_scales, (size_t)a.num_blocks * a.n_kv * 16);
     }
     const Walk w0 = find_slice<BS, NT>(a, s_red, s_pos, &s_walk);  // also publishes the barrier init
     // This kernel is launched as a programmatic dependent of the previous

@@ -142,7 +142,7 @@ cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new,
 // the new scale, the re-quantised resident rows, the run's codes, the scale
 // entry.  Every other warp returns.  Lanes take 4 consecutive elements of a
 // row at a time.
-constexpr int kAppendWarps = 8;
+constexpr int kAppendWarps = 4;  // small CTAs: a decode step's few runs spread over more SMs
 
 // The smallest power of two s = 2^e, e >= -126, with a <= 448 * s (a > 0,
 // finite).  r = fp32(a / 448) rounds across no power of two that matters:
@@ -159,27 +159,45 @@ __device__ __forceinline__ float pow2_scale_for(float a) {
     return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
+// Division by a block scale s.  The scales this append sets are powers of two
+// 2^e (-126 <= e <= 127), and for those x / s and x * 2^-e are the same real
+// number rounded once, so multiplying by the exact reciprocal gives the IEEE
+// quotient bit for bit (subnormal and overflowing results included); any
+// other stored scale is divided by.
+struct DivBy {
+    float s, inv;
+    bool pow2;
+    __device__ __forceinline__ explicit DivBy(float sc) : s(sc) {
+        const uint32_t u = __float_as_uint(sc), ex = (u >> 23) & 0xFFu;
+        pow2 = (u & 0x807FFFFFu) == 0u && ex >= 1u && ex <= 253u;
+        inv = pow2 ? __uint_as_float((254u - ex) << 23) : 0.f;
+    }
+    __device__ __forceinline__ float operator()(float x) const {
+        return pow2 ? x * inv : __fdiv_rn(x, s);
+    }
+};
+
 // Four bf16 (two 32-bit words) -> four e4m3 codes of x / s (x itself for s == 0).
-__device__ __forceinline__ uint32_t quantise4_by(uint32_t lo2, uint32_t hi2, float s) {
+__device__ __forceinline__ uint32_t quantise4_by(uint32_t lo2, uint32_t hi2, const DivBy& d) {
     float x0 = bf16_lo_to_f32(lo2), x1 = bf16_hi_to_f32(lo2);
     float x2 = bf16_lo_to_f32(hi2), x3 = bf16_hi_to_f32(hi2);
-    if (s > 0.f) {
-        x0 = __fdiv_rn(x0, s);
-        x1 = __fdiv_rn(x1, s);
-        x2 = __fdiv_rn(x2, s);
-        x3 = __fdiv_rn(x3, s);
+    if (d.s > 0.f) {
+        x0 = d(x0);
+        x1 = d(x1);
+        x2 = d(x2);
+        x3 = d(x3);
     }
     return f32x2_to_e4m3x2(x0, x1) | (f32x2_to_e4m3x2(x2, x3) << 16);
 }
 
 // Four codes re-quantised from scale s_old to s_new: e4m3 of fp32(fp32(v * s_old) / s_new).
-__device__ __forceinline__ uint32_t requantise4(uint32_t codes, float s_old, float s_new) {
+__device__ __forceinline__ uint32_t requantise4(uint32_t codes, float s_old, const DivBy& d) {
     uint32_t lo, hi;  // f16 pairs of bytes (0, 1) and (2, 3); every e4m3 value is exact in f16
     e4m3x4_to_f16x2x2(codes, lo, hi);
-    const float v0 = __fdiv_rn(f16_lo_to_f32(lo) * s_old, s_new);
-    const float v1 = __fdiv_rn(f16_hi_to_f32(lo) * s_old, s_new);
-    const float v2 = __fdiv_rn(f16_lo_to_f32(hi) * s_old, s_new);
-    const float v3 = __fdiv_rn(f16_hi_to_f32(hi) * s_old, s_new);
+    const float v0 = d(f16_lo_to_f32(lo) * s_old);
+    const float v1 = d(f16_hi_to_f32(lo) * s_old);
+    const float v2 = d(f16_lo_to_f32(hi) * s_old);
+    const float v3 = d(f16_hi_to_f32(hi) * s_old);
     return f32x2_to_e4m3x2(v0, v1) | (f32x2_to_e4m3x2(v2, v3) << 16);
 }
 
@@ -193,36 +211,48 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
     // reads no cache before this grid completes).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
-    const long long item = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
-    if (item >= (long long)num_tokens * n_kv) return;
-    const int t = static_cast<int>(item / n_kv), g = static_cast<int>(item % n_kv);
-    const long long slot = __ldg(slot_mapping + t);
-    if (slot < 0 || slot >= num_slots) return;
-    const long long blk = slot / block_size;
-    auto valid = [&](long long s) { return s >= 0 && s < num_slots; };
+    // (the host limits num_tokens * n_kv to fewer than 2^31)
+    const unsigned item = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+    if (item >= static_cast<unsigned>(num_tokens * n_kv)) return;
+    const int t = static_cast<int>(item / static_cast<unsigned>(n_kv));
+    const int g = static_cast<int>(item % static_cast<unsigned>(n_kv));
+    // (the host limits the slots to fewer than 2^31: 32-bit arithmetic throughout)
+    const int nslots = static_cast<int>(num_slots);
+    const unsigned ubs = static_cast<unsigned>(block_size);
+    auto valid = [&](int s) { return s >= 0 && s < nslots; };
+    auto block_of = [&](int s) { return static_cast<int>(static_cast<unsigned>(s) / ubs); };
+    auto offset_of = [&](int s) { return static_cast<int>(static_cast<unsigned>(s) % ubs); };
+    // First round of loads, all independent: this token's slot and the 32
+    // slots on either side of it (the usual run fits in them).
+    const int slot = __ldg(slot_mapping + t);
+    const int pb0 = t - 1 - lane, pf0 = t + 1 + lane;
+    const int sb0 = pb0 >= 0 ? __ldg(slot_mapping + pb0) : -1;
+    const int sf0 = pf0 < num_tokens ? __ldg(slot_mapping + pf0) : -1;
+    if (!valid(slot)) return;
+    const int blk = block_of(slot);
 
     // Does the nearest earlier valid token land in the same block?  (Lanes look
     // 32 tokens back at a time; the answer is warp-uniform.)
     for (int base = t - 1; base >= 0; base -= 32) {
         const int p = base - lane;
-        const long long sp = p >= 0 ? __ldg(slot_mapping + p) : -1;
+        const int sp = base == t - 1 ? sb0 : (p >= 0 ? __ldg(slot_mapping + p) : -1);
         const unsigned vm = __ballot_sync(0xffffffffu, p >= 0 && valid(sp));
         if (vm) {
-            const long long sprev = __shfl_sync(0xffffffffu, sp, __ffs(vm) - 1);
-            if (sprev / block_size == blk) return;  // not the run's first token
+            const int sprev = __shfl_sync(0xffffffffu, sp, __ffs(vm) - 1);
+            if (block_of(sprev) == blk) return;  // not the run's first token
             break;
         }
     }
     // The run: tokens t .. end-1 (skipped slots included), and its lowest offset.
     int end = t + 1;
-    long long o_min = slot % block_size;
+    int o_min = offset_of(slot);
     for (int base = t + 1; base < num_tokens; base += 32) {
         const int p = base + lane;
-        const long long sp = p < num_tokens ? __ldg(slot_mapping + p) : -1;
-        const bool other = p < num_tokens && valid(sp) && sp / block_size != blk;
+        const int sp = base == t + 1 ? sf0 : (p < num_tokens ? __ldg(slot_mapping + p) : -1);
+        const bool other = p < num_tokens && valid(sp) && block_of(sp) != blk;
         const unsigned stop = __ballot_sync(0xffffffffu, other || p >= num_tokens);
         const int lim = stop ? __ffs(stop) - 1 : 32;  // lanes below lim are in the run
-        long long off = (lane < lim && valid(sp)) ? sp % block_size : (long long)block_size;
+        int off = (lane < lim && valid(sp)) ? offset_of(sp) : block_size;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) off = min(off, __shfl_xor_sync(0xffffffffu, off, o));
         o_min = min(o_min, off);
@@ -230,56 +260,67 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
         if (stop) break;
     }
 
-    for (int which = 0; which < 2; ++which) {  // K, then V
-        const uint16_t* src = which == 0 ? k_new : v_new;
-        float* entry = kv_scales + ((size_t)blk * n_kv + g) * 4;
-        uint8_t* rows = kv_cache + (((size_t)blk * n_kv + g) * 2 + which) * (size_t)block_size * head_dim;
-        // largest finite |x| over the run's rows
-        float amax = 0.f;
-        for (int j = t; j < end; ++j) {
-            const long long sj = __ldg(slot_mapping + j);
-            if (!valid(sj)) continue;
-            const uint16_t* row = src + ((size_t)j * n_kv + g) * head_dim;
-            for (int e = lane * 4; e < head_dim; e += 128) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + e));
+    // Second round, all independent: the block's scale entry and the run's K
+    // and V rows (largest finite |x| of each).
+    float* entry = kv_scales + ((size_t)blk * n_kv + g) * 4;
+    const float2 s_old2 = o_min > 0 ? *reinterpret_cast<const float2*>(entry) : make_float2(0.f, 0.f);
+    float amax[2] = {0.f, 0.f};
+#pragma unroll 4
+    for (int j = t; j < end; ++j) {
+        const int sj = __ldg(slot_mapping + j);
+        if (!valid(sj)) continue;
+        const size_t rowo = ((size_t)j * n_kv + g) * head_dim;
+        for (int e = lane * 4; e < head_dim; e += 128) {
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>((which == 0 ? k_new : v_new) + rowo + e));
                 const float x[4] = {bf16_lo_to_f32(v.x), bf16_hi_to_f32(v.x), bf16_lo_to_f32(v.y),
                                     bf16_hi_to_f32(v.y)};
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    if (isfinite(x[k])) amax = fmaxf(amax, fabsf(x[k]));
+                    if (isfinite(x[k])) amax[which] = fmaxf(amax[which], fabsf(x[k]));
             }
         }
+    }
+    float s_new2[2];
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float s_old = o_min > 0 ? entry[which] : 0.f;
+    for (int which = 0; which < 2; ++which) {
+        float m = amax[which];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float s_old = which == 0 ? s_old2.x : s_old2.y;
         float s_new = s_old;
-        if (amax > 0.f) s_new = fmaxf(s_old, pow2_scale_for(amax));
+        if (m > 0.f) s_new = fmaxf(s_old, pow2_scale_for(m));
+        s_new2[which] = s_new;
+        uint8_t* rows = kv_cache + (((size_t)blk * n_kv + g) * 2 + which) * (size_t)block_size * head_dim;
         if (s_new > s_old && s_old > 0.f) {  // re-quantise the resident rows
-            for (long long r = 0; r < o_min; ++r)
+            const DivBy d(s_new);
+            for (int r = 0; r < o_min; ++r)
                 for (int e = lane * 4; e < head_dim; e += 128) {
-                    uint32_t* cp = reinterpret_cast<uint32_t*>(rows + r * head_dim + e);
-                    *cp = requantise4(*cp, s_old, s_new);
+                    uint32_t* cp = reinterpret_cast<uint32_t*>(rows + (size_t)r * head_dim + e);
+                    *cp = requantise4(*cp, s_old, d);
                 }
         }
-        for (int j = t; j < end; ++j) {  // the run's rows, in call order
-            const long long sj = __ldg(slot_mapping + j);
-            if (!valid(sj)) continue;
-            const uint16_t* row = src + ((size_t)j * n_kv + g) * head_dim;
-            uint8_t* dst = rows + (sj % block_size) * head_dim;
+    }
+    // The run's codes, in call order (a later token on the same offset writes
+    // after an earlier one), then the scale entry.
+    const DivBy dk(s_new2[0]), dv(s_new2[1]);
+    for (int j = t; j < end; ++j) {
+        const int sj = __ldg(slot_mapping + j);
+        if (!valid(sj)) continue;
+        const size_t rowo = ((size_t)j * n_kv + g) * head_dim;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            uint8_t* dst = kv_cache + (((size_t)blk * n_kv + g) * 2 + which) * (size_t)block_size * head_dim +
+                           (size_t)offset_of(sj) * head_dim;
             for (int e = lane * 4; e < head_dim; e += 128) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + e));
-                *reinterpret_cast<uint32_t*>(dst + e) = quantise4_by(v.x, v.y, s_new);
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>((which == 0 ? k_new : v_new) + rowo + e));
+                *reinterpret_cast<uint32_t*>(dst + e) = quantise4_by(v.x, v.y, which == 0 ? dk : dv);
             }
-            __syncwarp();  // a later token on the same offset writes after this one
         }
-        if (lane == 0) entry[which] = s_new;
         __syncwarp();
     }
-    if (lane == 0) {
-        float* entry = kv_scales + ((size_t)blk * n_kv + g) * 4;
-        entry[2] = 0.f;
-        entry[3] = 0.f;
-    }
+    if (lane == 0) *reinterpret_cast<float4*>(entry) = make_float4(s_new2[0], s_new2[1], 0.f, 0.f);
 }
 
 cudaError_t launch_kv_append_fp8_block(const void* k_new, const void* v_new,

@@ -115,6 +115,21 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) 
                  : "memory");
 }
 
+// 16 bytes global -> shared by an (LSU, not TMA) asynchronous copy, cached in
+// L2 only.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+
+// An arrival on `bar` once this thread's earlier cp.async copies have landed;
+// the barrier's pending count is raised at once, so its phase cannot complete
+// before then, and its expected arrival count is unchanged.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // Order this thread's earlier generic-proxy shared-memory writes before later
 // async-proxy (bulk copy, tensor core) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem_cta() {
