@@ -82,6 +82,11 @@ typedef enum pkv_status {
 /* pkv_copy_blocks: the 8-bit cache has per-(block, KV head) scales; v_cache
  * is then its scale tensor, copied with the blocks (needs PKV_FLAG_KV_FP8). */
 #define PKV_FLAG_KV_BLOCK_SCALES 0x10u
+/* Attention calls on a bf16 cache with head_dim 128 and more than 64 query
+ * rows per KV head: fetch each V tile as two 64-column copies, the form used
+ * when the driver declines the one-copy (three-dimensional) view of the V
+ * cache.  Results are bit-identical either way; tests use it to run both. */
+#define PKV_FLAG_TILE_2D 0x20u
 /* Bits 16..31 force the number of attention CTAs (0 = one per SM).  Tests
  * use it to move where long contexts are split; results stay within the
  * stated tolerance for every value. */

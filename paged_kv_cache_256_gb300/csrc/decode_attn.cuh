@@ -115,6 +115,8 @@ struct AttnCfg {
     // stage is laid out as [K box 0][K box 1 (d 128)][V box 0][V box 1], each
     // region holding the stage's blocks one after another (kRegion bytes), so
     // the rows of all its blocks are contiguous within each 64-column region.
+    // (TMEM consumer, bf16 at d 128, V by 3-D copies: the V half of the stage
+    // is [block][half][rows] instead, one copy per block.)
     static constexpr int kBlocksPerStage =
         MODE == kModeTmem ? 64 / BS : (2 * kTileBytes >= 8192 ? 1 : 8192 / (2 * kTileBytes));
     static constexpr int kRegion = kBlocksPerStage * kBoxBytes;
@@ -139,16 +141,22 @@ struct AttnCfg {
         MODE == kModeNarrow ? (kNarrowRows * kTileStride + 2 * kNarrowRows) * 4 : 0;
     // TMEM mode: the unit's 128 query rows as a swizzled K-major tile.
     static constexpr int kQTileBytes = MODE == kModeTmem ? 128 * D * 2 : 0;
-    // TMEM mode over an 8-bit cache: two f16 copies of a 64-key stage (K and
-    // V, each 64 rows in D/64 swizzled 64-column regions).
+    // TMEM mode over an 8-bit cache: kCvtCopies f16 copies of a 64-key stage
+    // (K and V, each 64 rows in D/64 swizzled 64-column regions).  A copy is
+    // held from its conversion until its PV product completes; with two, the
+    // conversion of stage g + 2 waited for PV(g) and the softmax for that
+    // conversion (MQA verify e4m3: one stage per ~1.5 us against ~0.8 over bf16).
+    static constexpr int kCvtCopies = 3;
     static constexpr int kCvtRegion = 64 * 128;
-    static constexpr int kCvtBytes = (MODE == kModeTmem && KV8) ? 2 * 2 * (D / 64) * kCvtRegion : 0;
+    static constexpr int kCvtBytes =
+        (MODE == kModeTmem && KV8) ? kCvtCopies * 2 * (D / 64) * kCvtRegion : 0;
     // Per-(block, KV head) scales (BLK): each block of a stage brings 16 bytes
-    // {K scale, V scale, 0, 0} by TMA with its tiles, into a slot beside the
-    // ring; the tensor-memory consumer's converter warps copy a super-block's
-    // scales next to its f16 copy (2 copies x blocks x {K, V}).
+    // {K scale, V scale, 0, 0} with its tiles, into a slot beside the ring;
+    // the tensor-memory consumer's converter warps copy a super-block's scales
+    // next to its f16 copy (kCvtCopies copies x blocks x {K, V}).
     static constexpr int kSlotBytes = BLK ? kBlocksPerStage * 16 : 0;
-    static constexpr int kCvtSlotBytes = (BLK && MODE == kModeTmem) ? 2 * kBlocksPerStage * 8 : 0;
+    static constexpr int kCvtSlotBytes =
+        (BLK && MODE == kModeTmem) ? kCvtCopies * kBlocksPerStage * 8 : 0;
     static constexpr int kScratchBytes =
         kMergeBytes + kEmitBytes + kQTileBytes + kCvtBytes + kCvtSlotBytes;
     static constexpr int kMaxStages = MODE == kModeTmem ? (KV8 ? 24 : 16) : (KV8 ? 48 : 32);
@@ -577,12 +585,14 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
             }
             if (*s_abort) ok = false;  // a consumer gave up
             if constexpr (ORDERED) {
-                // boxes per block: K and V halves (bf16), or one K+V box (8-bit)
-                constexpr int kBpb = KV8 ? 1 : 2 * kBoxes;
-                static_assert(SBS * kBpb <= 32, "one box per lane");
+                // boxes per block: K and V halves (bf16; V in one box through
+                // the 3-D view), or one K+V box (8-bit)
+                static_assert(SBS * (KV8 ? 1 : 2 * kBoxes) <= 32, "one box per lane");
+                const bool v3 = !KV8 && kBoxes == 2 && a.tile_3d;
+                const int bpb = KV8 ? 1 : (v3 ? kBoxes + 1 : 2 * kBoxes);
                 for (int k = 0; k < ns && ok; ++k) {
                     const int nb = min(SBS, n - k * SBS);
-                    const int blk = __shfl_sync(0xffffffffu, my, (k * SBS + lane / kBpb) & 31);
+                    const int blk = __shfl_sync(0xffffffffu, my, (k * SBS + lane / bpb) & 31);
                     const uint32_t stage = gidx % kStages;
                     bool good = true;
                     if (lane == 0)
@@ -599,7 +609,7 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                     }
                     // BLK: lane b < nb owns block b's scale slot (one box per block)
                     if constexpr (BLK) {
-                        static_assert(kBpb == 1, "scale slots assume one box per block");
+                        static_assert(KV8, "scale slots assume one box per block");
                         if (lane < nb) {
                             uint8_t* slot = slots + (stage * SBS + lane) * 16;
                             if (blk >= 0) {
@@ -612,14 +622,21 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                         __syncwarp();  // the slots' arrivals and zeros before the stage's arrival
                     }
                     if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], nb * 2 * kTileBytes);
-                    if (lane < nb * kBpb) {
-                        const int b = lane / kBpb, box = lane % kBpb;
+                    if (lane < nb * bpb) {
+                        const int b = lane / bpb, box = lane % bpb;
                         const long long y64 = ((long long)blk * a.n_kv + w.h) * a.kv_mul * BS;
                         const bool oob = blk < 0 || y64 >= a.tile_rows_total;
                         const int yk = oob ? a.tile_rows_total : static_cast<int>(y64);
                         if constexpr (KV8) {
                             tma_load_2d(stages + stage * kStageBytes + b * 2 * kBoxBytes, tmap_k,
                                         0, yk, &full_bar[stage], policy);
+                        } else if (v3 && box == kBoxes) {
+                            // block b's V tile, both halves: [half 0 rows][half 1 rows] at
+                            // b * 2 * kBoxBytes of the stage's V region
+                            tma_load_3d_hint(stages + stage * kStageBytes + kBoxes * kRegion +
+                                                 b * 2 * kBoxBytes,
+                                             tmap_v, 0, oob ? a.tile_rows_total : yk + a.v_row_off,
+                                             0, &full_bar[stage], policy);
                         } else {
                             // box: K half (box < kBoxes), then V half
                             const int half = box % kBoxes;
@@ -1596,8 +1613,8 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 // [0, 128), S 2 x 64 from 128, P 2 x 32 from 256, the low halves of P for
 // fp32 output 2 x 32 from 320.
 // Over an 8-bit cache (KV8) five converter warps (6, 7, 9, 10, 11) widen each
-// landed stage into one of two f16 copies (K and V in the layout the bf16 stages have, V rows past the
-// context zeroed) and free the stage; the MMAs read the copies as kind::f16
+// landed stage into one of three f16 copies (K and V in the layout the bf16
+// stages have, V rows past the context zeroed) and free the stage; the MMAs read the copies as kind::f16
 // with Q and P in f16 (every e4m3 value is exact in f16), and the PV product
 // frees the copy.  The per-head K scale joins the score scale, the V scale
 // the normalisation.
@@ -1642,16 +1659,18 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     constexpr int kParty = KV8 ? threads_for(kModeTmem, true) - 32 : 192;
     constexpr int kHalves = D / 64;          // 64-column regions of an f16 K or V copy
     // tcb: [0..1] S ready, [2..3] S read, [4..5] P ready, [6..7] PV done, [8] QK teardown,
-    //      [9] PV teardown, [10..13] f16 copies, [14] Q landed, [15] Q read, [16] Q widened
+    //      [9] PV teardown, [10..12] f16 copy ready, [13..15] f16 copy read, [16] Q landed,
+    //      [17] Q read, [18] Q widened
     uint64_t* s_full = tcb;
     uint64_t* s_free = tcb + 2;
     uint64_t* p_full = tcb + 4;
     uint64_t* pv_done = tcb + 6;
-    uint64_t* cvt_full = tcb + 10;  // 8-bit cache: f16 copy [g&1] ready
-    uint64_t* cvt_free = tcb + 12;  // 8-bit cache: f16 copy [g&1] read by its PV product
-    uint64_t* q_full = tcb + 14;    // query tile landed (TMA)
-    uint64_t* q_empty = tcb + 15;   // the piece's score products have read the query tile
-    uint64_t* q_conv = tcb + 16;    // 8-bit cache: the query tile widened to f16
+    constexpr uint32_t kCopies = C::kCvtCopies;
+    uint64_t* cvt_full = tcb + 10;  // 8-bit cache: f16 copy [g % kCopies] ready
+    uint64_t* cvt_free = tcb + 13;  // 8-bit cache: f16 copy [g % kCopies] read by its PV product
+    uint64_t* q_full = tcb + 16;    // query tile landed (TMA)
+    uint64_t* q_empty = tcb + 17;   // the piece's score products have read the query tile
+    uint64_t* q_conv = tcb + 18;    // 8-bit cache: the query tile widened to f16
     // f16 copies (8-bit cache): copy c at cvt + c * kCopy, K regions then V regions
     uint8_t* cvt = qtile + C::kQTileBytes;
     constexpr int kCopy = 2 * kHalves * C::kCvtRegion;
@@ -1672,6 +1691,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     const uint32_t idesc_qk = KV8 ? umma_idesc_f16(128, kKeys, false) : umma_idesc_bf16(128, kKeys, false);
     const uint32_t idesc_pv = KV8 ? umma_idesc_f16(128, D, true) : umma_idesc_bf16(128, D, true);
     const uint32_t q_saddr = smem_addr(qtile);
+    // bf16 V tiles by one 3-D copy each: a stage's V region is [block][half][rows]
+    const bool v3 = !KV8 && C::kBoxes == 2 && a.tile_3d;
 
     auto issuer_fail = [&](bool& ok) {
         ok = false;
@@ -1770,7 +1791,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         break;
                     }
                     if (*s_abort ||
-                        !(KV8 ? mbar_wait_bounded(&cvt_full[g & 1u], (g >> 1) & 1u)
+                        !(KV8 ? mbar_wait_bounded(&cvt_full[g % kCopies], (g / kCopies) & 1u)
                               : mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u))) {
                         issuer_fail(ok);
                         break;
@@ -1778,7 +1799,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     tc_fence_after();
                     // Rows past the stage's blocks (a partial last super-block)
                     // hold stale keys; the softmax masks their columns.
-                    const uint32_t kb = KV8 ? smem_addr(cvt + (g & 1u) * kCopy)
+                    const uint32_t kb = KV8 ? smem_addr(cvt + (g % kCopies) * kCopy)
                                             : smem_addr(stages + st * C::kStageBytes);
                     constexpr uint32_t kKRegion = KV8 ? C::kCvtRegion : C::kRegion;
                     const uint32_t scol = tbase + kColS + (g & 1u) * kKeys;
@@ -1826,12 +1847,18 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     // Only the keys of the stage's blocks enter the product.
                     const int nk16 = min(SB, n - q * SB) * (BS / 16);
                     const uint32_t vb =
-                        KV8 ? smem_addr(cvt + (g & 1u) * kCopy) + kHalves * C::kCvtRegion
+                        KV8 ? smem_addr(cvt + (g % kCopies) * kCopy) + kHalves * C::kCvtRegion
                             : smem_addr(stages + st * C::kStageBytes) + C::kBoxes * C::kRegion;
-                    constexpr uint32_t kVRegion = KV8 ? C::kCvtRegion : C::kRegion;
+                    // The V rows of 16 keys and the distance to their second
+                    // 64-column half: halves of all the stage's blocks apart
+                    // (2-D copies), or each block's two halves together (3-D).
+                    const uint32_t vlbo = KV8 ? C::kCvtRegion : (v3 ? C::kBoxBytes : C::kRegion);
                     const uint32_t pcol = (g & 1u) * (kKeys / 2);
                     for (int kk = 0; kk < nk16; ++kk) {
-                        const uint64_t bd = umma_smem_desc(vb + kk * 16 * 128, kVRegion, 1024);
+                        const uint32_t vrow =
+                            v3 ? (kk / (BS / 16)) * 2 * C::kBoxBytes + (kk % (BS / 16)) * 16 * 128
+                               : kk * 16 * 128;
+                        const uint64_t bd = umma_smem_desc(vb + vrow, vlbo, 1024);
                         umma_ts(tbase + kColO, tbase + kColP + pcol + kk * 8, bd, idesc_pv,
                                 (q > 0 || kk > 0) ? 1u : 0u);
                         if (OUT_F32)
@@ -1839,7 +1866,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                                     1u);
                     }
                     if (KV8)
-                        umma_commit(&cvt_free[g & 1u]);  // the f16 copy is consumed
+                        umma_commit(&cvt_free[g % kCopies]);  // the f16 copy is consumed
                     else
                         umma_commit(&empty_bar[st]);  // K and V of this stage are consumed
                     umma_commit(&pv_done[g & 1u]);    // its P buffer is free; O is current
@@ -1862,8 +1889,9 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 for (int q = 0; q < nsb; ++q) {
                     const uint32_t g = gbase + q, st = g % kStages;
                     bool good = !*s_abort && mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u);
-                    if (good && g >= 2)
-                        good = mbar_wait_bounded(&cvt_free[g & 1u], ((g - 2) >> 1) & 1u);
+                    if (good && g >= kCopies)
+                        good = mbar_wait_bounded(&cvt_free[g % kCopies],
+                                                 ((g - kCopies) / kCopies) & 1u);
                     if (!__all_sync(0xffffffffu, good)) {
                         if (lane == 0) {
                             atomicOr(a.err, kErrTimeout);
@@ -1878,11 +1906,11 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         // the blocks' scales (K: converter 0, V: converter 1), before the
                         // stage is given back
                         if (ci < 2 && lane < nb)
-                            cvt_sc[((g & 1u) * SB + lane) * 2 + ci] =
+                            cvt_sc[((g % kCopies) * SB + lane) * 2 + ci] =
                                 reinterpret_cast<const float*>(slots + (st * SB + lane) * 16)[ci];
                     }
                     const uint8_t* stage_src = stages + st * C::kStageBytes;
-                    uint8_t* copy = cvt + (g & 1u) * kCopy;
+                    uint8_t* copy = cvt + (g % kCopies) * kCopy;
                     // Rows of blocks past the stage's last are read (they lie inside the
                     // stage) and replaced by zeros, as are keys past the context.
 #pragma unroll
@@ -1926,7 +1954,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     fence_proxy_async_smem();  // the copy, for the tensor cores
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(&cvt_full[g & 1u]);
+                        mbar_arrive(&cvt_full[g % kCopies]);
                         mbar_arrive(&empty_bar[st]);  // (every converter: the e4m3 stage is free)
                     }
                 }
@@ -1977,13 +2005,14 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 float rat[SB], vfac = 1.f;
                 bool vgrow = false;
                 if constexpr (BLK) {
-                    ok = consumer_wait(a, &cvt_full[sq & 1u], (sq >> 1) & 1u, ok, s_abort);
+                    ok = consumer_wait(a, &cvt_full[sq % kCopies], (sq / kCopies) & 1u, ok,
+                                       s_abort);
                     if (!ok) continue;
                     float kf[SB], vs[SB], smax = 0.f;
 #pragma unroll
                     for (int b = 0; b < SB; ++b) {
                         const float2 sc = b < nb ? *reinterpret_cast<const float2*>(
-                                                       cvt_sc + ((sq & 1u) * SB + b) * 2)
+                                                       cvt_sc + ((sq % kCopies) * SB + b) * 2)
                                                  : make_float2(0.f, 0.f);
                         kf[b] = a.scale_log2 * sc.x;
                         vs[b] = sc.y;
@@ -2123,12 +2152,14 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 const int tokl = tok0 + (nb - 1) * BS;
                 if (!KV8 && tokl + BS > ctx) {  // (the f16 copies come zeroed there)
                     uint8_t* vt = stages + (sq % kStages) * C::kStageBytes +
-                                  C::kBoxes * C::kRegion + (nb - 1) * C::kBoxBytes;
+                                  C::kBoxes * C::kRegion +
+                                  (nb - 1) * (v3 ? 2 * C::kBoxBytes : C::kBoxBytes);
+                    const int hstride = v3 ? C::kBoxBytes : C::kRegion;  // to the second half
                     const int valid = ctx - tokl;  // >= 1: the block holds a resident token
                     const int chunks = (BS - valid) * 8;  // 16-byte chunks per 64-column half
                     for (int qq = row; qq < chunks * (D / 64); qq += 128) {
                         const int half = qq / chunks, rq = qq % chunks;
-                        *reinterpret_cast<uint4*>(vt + half * C::kRegion + valid * 128 + rq * 16) =
+                        *reinterpret_cast<uint4*>(vt + half * hstride + valid * 128 + rq * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
@@ -2248,9 +2279,9 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
     __shared__ Walk s_walk;
     __shared__ int s_abort;
     // TMEM mode: S ready/read, P ready, PV done (x2 each), 2 teardowns, over an
-    // 8-bit cache f16 copy ready / free (x2 each), query tile landed / read /
+    // 8-bit cache f16 copy ready / free (x3 each), query tile landed / read /
     // widened
-    __shared__ uint64_t s_tcb[17];
+    __shared__ uint64_t s_tcb[19];
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -2270,9 +2301,10 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
             // copy ready (the converter warps) / free (a commit), query tile
             // landed (the TMA) / read (a commit) / widened (128 rows)
             const uint32_t cvt = KV8 ? (uint32_t)kTmemConverters : 1u;
-            const uint32_t counts[17] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1, cvt, cvt,
-                                         1, 1, 1, 1, 128};
-            for (int i = 0; i < 17; ++i) mbar_init(&s_tcb[i], counts[i]);
+            const uint32_t counts[19] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1, cvt, cvt, cvt,
+                                         1, 1, 1, 1, 1, 128};
+            static_assert(C::kCvtCopies == 3, "barrier counts: three f16 copies");
+            for (int i = 0; i < 19; ++i) mbar_init(&s_tcb[i], counts[i]);
         }
         fence_barrier_init();
         s_abort = 0;
@@ -2318,7 +2350,7 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
         if (a.q_tma) {
             if (warp == 4) {
                 if (lane == 0 && w0.left > 0)
-                    issue_q_tile<D>(a, &tmap_q, reinterpret_cast<uint8_t*>(scratch), &s_tcb[14],
+                    issue_q_tile<D>(a, &tmap_q, reinterpret_cast<uint8_t*>(scratch), &s_tcb[16],
                                     w0.s, w0.h, w0.t);
                 __syncwarp();
                 named_barrier_arrive(3, 64);

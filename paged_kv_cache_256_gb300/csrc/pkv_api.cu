@@ -70,6 +70,26 @@ bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, long long 
     return r == CUDA_SUCCESS;
 }
 
+// 3-D view of a bf16 cache with head_dim 128: {64 columns, rows, 2 column
+// halves}, the halves 128 bytes apart, so one box of 64 x block_size x 2
+// brings a whole (block, KV head) tile as its two 128-byte-swizzled half
+// tiles one after the other -- one copy where the 2-D view needs two.  The
+// strides are not in increasing order (the half stride lies inside a row); a
+// driver that declines such a view returns an error and the caller keeps the
+// 2-D view.
+bool make_cache_map_3d(CUtensorMap* map, const void* base, long long rows, int block_size) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64u, (cuuint64_t)rows, 2u};
+    cuuint64_t strides[2] = {256u, 128u};
+    cuuint32_t box[3] = {64u, (cuuint32_t)block_size, 2u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Encoding a tensor map is a driver call; decode loops pass the same caches
 // every step, so the last few encodings are kept (keyed by everything that
 // goes into them).
@@ -77,7 +97,7 @@ struct MapKey {
     const void* base;
     long long rows;
     int head_dim, block_size;
-    bool kv8;
+    bool kv8, three_d;
 };
 struct MapEntry {
     MapKey key;
@@ -90,18 +110,20 @@ MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 
 bool cached_cache_map(CUtensorMap* map, const void* base, int head_dim, long long rows,
-                      int block_size, bool kv8) {
+                      int block_size, bool kv8, bool three_d = false) {
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (const MapEntry& e : g_maps)
         if (e.used && e.key.base == base && e.key.rows == rows && e.key.head_dim == head_dim &&
-            e.key.block_size == block_size && e.key.kv8 == kv8) {
+            e.key.block_size == block_size && e.key.kv8 == kv8 && e.key.three_d == three_d) {
             *map = e.map;
             return true;
         }
-    if (!make_cache_map(map, base, head_dim, rows, block_size, kv8)) return false;
+    if (three_d ? !make_cache_map_3d(map, base, rows, block_size)
+                : !make_cache_map(map, base, head_dim, rows, block_size, kv8))
+        return false;
     MapEntry& e = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % kMapCache;
-    e.key = MapKey{base, rows, head_dim, block_size, kv8};
+    e.key = MapKey{base, rows, head_dim, block_size, kv8, three_d};
     e.map = *map;
     e.used = true;
     return true;
@@ -372,7 +394,15 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
 
     AttnMaps maps;
     std::memset(&maps, 0, sizeof maps);
-    if (!cached_cache_map(&maps.k, k_cache, head_dim, rows_total, block_size, kv8) ||
+    if (!cached_cache_map(&maps.k, k_cache, head_dim, rows_total, block_size, kv8))
+        return PKV_ERR_CUDA;
+    // The tensor-memory consumer over a bf16 head_dim-128 cache takes each V
+    // tile in one copy through the 3-D view where the driver accepts it.
+    int tile_3d = 0;
+    if (!kv8 && head_dim == 128 && rows > 64 && !(flags & PKV_FLAG_TILE_2D) &&
+        cached_cache_map(&maps.v, v_cache, head_dim, rows_total, block_size, false, true))
+        tile_3d = 1;
+    if (!tile_3d &&
         !cached_cache_map(&maps.v, kv8 ? k_cache : v_cache, head_dim, rows_total, block_size, kv8))
         return PKV_ERR_CUDA;
     // The tensor-memory consumer (more than 64 rows) takes its query tiles by
@@ -420,6 +450,7 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     a.scale_log2 = scale * 1.4426950408889634f;
     a.q_tma = q_tma;
     a.early_start = (flags & PKV_FLAG_NO_EARLY_START) ? 0 : 1;
+    a.tile_3d = tile_3d;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool f32 = out_dtype == PKV_OUT_F32;

@@ -50,10 +50,12 @@ struct AttnArgs {
     int q_tma;         // tensor-memory consumer: query tiles arrive by TMA (the q map is valid)
     int early_start;   // launched as a programmatic dependent of the previous kernel
     const float* kv_scales;  // per-(block, KV head) scales [num_blocks][n_kv][4], or null
+    int tile_3d;  // the V map is a 3-D view: a V tile's two 64-column halves in one copy
 };
 
 // The tensor maps of one attention launch: the K and V cache views and the
-// query tiles (tensor-memory consumer).
+// query tiles (tensor-memory consumer).  With AttnArgs::tile_3d the V view is
+// three-dimensional: {64 columns, rows, 2 column halves}.
 struct AttnMaps {
     CUtensorMap k, v, q;
 };

@@ -45,6 +45,17 @@ def test_binding_exposes_same_names():
         assert hasattr(pkg, name), name
 
 
+def test_header_constants_match_the_binding():
+    """Every numeric #define PKV_... of the header has the same value in the binding."""
+    import paged_kv_cache_256_gb300 as pkg
+    text = open(HEADER).read()
+    defs = re.findall(r"^#define\s+(PKV_\w+)\s+(0x[0-9A-Fa-f]+|\d+)u?\b", text, flags=re.M)
+    assert len(defs) >= 10
+    for name, value in defs:
+        assert getattr(_lib, name) == int(value, 0), name
+        assert getattr(pkg, name, getattr(_lib, name)) == int(value, 0), name
+
+
 def test_status_strings(lib):
     for code in range(8):
         assert _lib.status_name(code).startswith("PKV_")

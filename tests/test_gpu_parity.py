@@ -55,6 +55,23 @@ def test_split_points_do_not_change_the_result(named, grid):
     assert_close(out_to_host(out), ref, "f32", f"{wl.name}/grid{grid}")
 
 
+@pytest.mark.parametrize("kind", ["bf16", "f32"])
+def test_one_and_two_copy_v_tiles_agree_bit_for_bit(named, kind):
+    """With more than 64 rows per KV head a bf16 head_dim-128 V tile arrives by
+    one 3-D copy, or by two 64-column copies under PKV_FLAG_TILE_2D; the
+    products read the same values, so the outputs match bit for bit."""
+    wl, dw, _, _, _ = named
+    a = run_attn(dw, wl, kind)
+    b = run_attn(dw, wl, kind, flags=pkv.PKV_FLAG_TILE_2D)
+    assert np.array_equal(a.cpu().view(torch_int_of(kind)).numpy(),
+                          b.cpu().view(torch_int_of(kind)).numpy())
+
+
+def torch_int_of(kind):
+    import torch
+    return torch.int16 if kind == "bf16" else torch.int32
+
+
 def test_repeatable_bit_for_bit(named):
     wl, dw, _, _, _ = named
     a = bf16_to_host_bits(run_attn(dw, wl, "bf16"))
@@ -241,11 +258,14 @@ def test_checked_mode_reports_bad_tables():
     assert call(dw.block_tables, dw.context_lens) == pkv.PKV_OK
 
 
-def test_unchecked_bad_block_id_reads_zeros_without_fault():
+@pytest.mark.parametrize("n_q,n_kv,q_len,head_dim", [(4, 2, 1, 64), (8, 2, 1, 128),
+                                                      (32, 1, 4, 128)],
+                         ids=["narrow_d64", "narrow_d128", "tmem_d128"])
+def test_unchecked_bad_block_id_reads_zeros_without_fault(n_q, n_kv, q_len, head_dim):
     """Without CHECKED, an out-of-range id is read as a zero tile (no access outside the cache)."""
     import torch
-    wl = make_custom(num_seqs=2, q_len=1, n_q=4, n_kv=2, head_dim=64, block_size=16,
-                     context_lens=[40, 20], seed=11)
+    wl = make_custom(num_seqs=2, q_len=q_len, n_q=n_q, n_kv=n_kv, head_dim=head_dim,
+                     block_size=16, context_lens=[40, 20], seed=11)
     dw = to_device(wl)
     pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache)
     bt = wl.block_tables.copy()
@@ -253,6 +273,9 @@ def test_unchecked_bad_block_id_reads_zeros_without_fault():
     dw.block_tables = torch.from_numpy(bt).cuda()
     out = run_attn(dw, wl, "f32")
     assert torch.isfinite(out).all()
+    # the zero tile is the same whichever way the tiles are fetched
+    out2 = run_attn(dw, wl, "f32", flags=pkv.PKV_FLAG_TILE_2D)
+    assert torch.equal(out.view(torch.int32), out2.view(torch.int32))
 
 
 def test_kv_append_skips_padding_and_out_of_range_slots():
