@@ -1962,8 +1962,9 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         } else {
             // ===================== softmax (thread = row) =====================
             // Scores stay raw: the row's extreme is taken over raw scores and
-            // the exponent of a key is (S - S_ext) * sl2, so the extreme key
-            // itself weighs exactly 1.  Over a negative scale the largest
+            // the exponent of a key is S * sl2 - S_ext * sl2, so the extreme
+            // key itself weighs 1 (to the rounding of S_ext * sl2, ~1e-7
+            // relative, which cancels against the same weight in l).  Over a negative scale the largest
             // scaled score is the smallest raw one; a zero scale makes every
             // visible score 0 (S is replaced by 0 and scaled by 1).  m_used is
             // the scaled running max, mr_used the raw score it came from.
@@ -2102,14 +2103,17 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 }
                 // With m_used = -inf every score of the row is masked (hidden
                 // scales to -inf): the offset mr_used = 0 gives p = 0 for all.
+                // The exponent S * sl2 - mr_used * sl2 is one FMA per key (the
+                // extreme key's weight is 1 within a few ulp of its exponent).
+                const float msl = mr_used * sl2;
                 uint32_t ph[kKeys / 2], pl[kKeys / 2];
                 float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
                 for (int c = 0; c < kKeys; c += 4) {
-                    float p0 = fast_exp2((x[c] - mr_used) * sl2);
-                    float p1 = fast_exp2((x[c + 1] - mr_used) * sl2);
-                    float p2 = fast_exp2((x[c + 2] - mr_used) * sl2);
-                    float p3 = fast_exp2((x[c + 3] - mr_used) * sl2);
+                    float p0 = fast_exp2(fmaf(x[c], sl2, -msl));
+                    float p1 = fast_exp2(fmaf(x[c + 1], sl2, -msl));
+                    float p2 = fast_exp2(fmaf(x[c + 2], sl2, -msl));
+                    float p3 = fast_exp2(fmaf(x[c + 3], sl2, -msl));
                     rs0 += p0;
                     rs1 += p1;
                     rs2 += p2;
@@ -2180,41 +2184,67 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 const float vsc = BLK ? vrun * kPShiftTmemInv : KV8 ? __ldg(a.v_scale + h) : 1.f;
                 const float scl = (whole ? (l > 0.f ? 1.f / l : 0.f) : 1.f) * vsc;
                 const size_t rec = (size_t)cta * 2 + (piece == 0 ? 0 : 1);
+                if (whole && !OUT_F32) {
+                    // bf16 rows: each thread its own row, 16 bytes per store
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t ov[32];
-                    tmem_ld32(tlane + kColO + c0, ov);
-                    tmem_wait_ld();
-                    // whole units write their real rows; records keep every tile row
-                    if (whole ? row_ok : row < R) {
-                        if (whole) {
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t ov[32];
+                        tmem_ld32(tlane + kColO + c0, ov);
+                        tmem_wait_ld();
+                        if (row_ok) {
                             const size_t ob =
                                 (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D + c0;
-                            if (OUT_F32) {
-                                float4* op = reinterpret_cast<float4*>(static_cast<float*>(a.out) + ob);
+                            uint4* op = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ob);
 #pragma unroll
-                                for (int c = 0; c < 32; c += 4)
-                                    op[c / 4] = make_float4(__uint_as_float(ov[c]) * scl,
-                                                            __uint_as_float(ov[c + 1]) * scl,
-                                                            __uint_as_float(ov[c + 2]) * scl,
-                                                            __uint_as_float(ov[c + 3]) * scl);
-                            } else {
-                                uint4* op = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ob);
+                            for (int c = 0; c < 32; c += 8)
+                                op[c / 8] = make_uint4(
+                                    pack_bf16x2(__uint_as_float(ov[c]) * scl, __uint_as_float(ov[c + 1]) * scl),
+                                    pack_bf16x2(__uint_as_float(ov[c + 2]) * scl, __uint_as_float(ov[c + 3]) * scl),
+                                    pack_bf16x2(__uint_as_float(ov[c + 4]) * scl, __uint_as_float(ov[c + 5]) * scl),
+                                    pack_bf16x2(__uint_as_float(ov[c + 6]) * scl, __uint_as_float(ov[c + 7]) * scl));
+                        }
+                    }
+                } else {
+                    // fp32 rows (a record keeps o unnormalised: scl is then the V
+                    // scale, 1 for bf16; or an fp32 output row).  O is read in the
+                    // 16x256b shape, so four lanes store 32 contiguous bytes of one
+                    // row and a store instruction reaches 8 rows, not 32 (the
+                    // per-row form took ~1.5 us per 64 KB record).
+                    const int g8 = lane >> 2, q4 = lane & 3;
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int rq = (warp & 3) * 32 + hh * 16;  // first row of the half
+                        float* dst[2];
+                        float sc[2];
 #pragma unroll
-                                for (int c = 0; c < 32; c += 8)
-                                    op[c / 8] = make_uint4(
-                                        pack_bf16x2(__uint_as_float(ov[c]) * scl, __uint_as_float(ov[c + 1]) * scl),
-                                        pack_bf16x2(__uint_as_float(ov[c + 2]) * scl, __uint_as_float(ov[c + 3]) * scl),
-                                        pack_bf16x2(__uint_as_float(ov[c + 4]) * scl, __uint_as_float(ov[c + 5]) * scl),
-                                        pack_bf16x2(__uint_as_float(ov[c + 6]) * scl, __uint_as_float(ov[c + 7]) * scl));
+                        for (int u = 0; u < 2; ++u) {
+                            const int r = rq + g8 + 8 * u;  // tile row (lane r % 32 holds its scl)
+                            sc[u] = __shfl_sync(0xffffffffu, scl, (r & 31));
+                            dst[u] = nullptr;
+                            if (whole) {
+                                int ir = 0, hr = 0;
+                                if (unit_row(a, w.t, h, r, ir, hr))
+                                    dst[u] = static_cast<float*>(a.out) +
+                                             (((size_t)s * a.q_len + ir) * a.n_q + hr) * D;
+                            } else if (r < R) {
+                                dst[u] = a.rec_o + (rec * R + r) * D;
                             }
-                        } else {
-                            // a record keeps o unnormalised (scl is the V scale, 1 for bf16)
-                            float4* op = reinterpret_cast<float4*>(a.rec_o + (rec * R + row) * D + c0);
+                        }
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t ov[16];
+                            tmem_ld_16x256b_x4(tbase + ((uint32_t)rq << 16) + kColO + c0, ov);
+                            tmem_wait_ld();
 #pragma unroll
-                            for (int c = 0; c < 32; c += 4)
-                                op[c / 4] = make_float4(__uint_as_float(ov[c]) * scl, __uint_as_float(ov[c + 1]) * scl,
-                                                        __uint_as_float(ov[c + 2]) * scl, __uint_as_float(ov[c + 3]) * scl);
+                            for (int j = 0; j < 4; ++j) {
+                                const int c = c0 + 8 * j + 2 * q4;
+#pragma unroll
+                                for (int u = 0; u < 2; ++u)
+                                    if (dst[u])
+                                        *reinterpret_cast<float2*>(dst[u] + c) =
+                                            make_float2(__uint_as_float(ov[4 * j + 2 * u]) * sc[u],
+                                                        __uint_as_float(ov[4 * j + 2 * u + 1]) * sc[u]);
+                            }
                         }
                     }
                 }

@@ -74,7 +74,13 @@ def test_window_parity(oracle, case, grid):
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "d{}_bs{}_q{}_kv{}_ql{}".format(*c[:5]))
 def test_window_extremes_are_exact(oracle, case):
-    """W = 0 and W >= every context equal the positional entry bit for bit; W = 1 is V."""
+    """W = 0 and W >= every context equal the positional entry bit for bit; W = 1 is V.
+
+    W = 1 leaves one key per row, whose weight is 1: exactly so on the mma.sync
+    consumers (exponent (S - S_max) * scale), and to the rounding of S_max * scale
+    on the tensor-memory consumer (>64 rows), which forms the exponent as one FMA
+    S * scale - S_max * scale; its fp32 output is then V within 2^-20 relative
+    (bf16 output: V exactly either way)."""
     import torch
     wl, dw, kc, vc = _setup(oracle, case, seed=311 + case[2])
     ws = pkv.alloc_workspace(wl.num_seqs, wl.q_len, wl.n_q, wl.n_kv, wl.head_dim, wl.block_size)
@@ -98,8 +104,11 @@ def test_window_extremes_are_exact(oracle, case):
                 v = vc[blk, :, pos % wl.block_size]          # [n_kv, d] bf16 bits
                 want = np.repeat(v[:, None], G, axis=1).reshape(wl.n_q, wl.head_dim)
                 from paged_kv_cache_256_gb300.workloads import bf16_bits_to_f32
-                assert np.array_equal(got[b, i], bf16_bits_to_f32(want).astype(np.float64)), \
-                    (kind, b, i)
+                vw = bf16_bits_to_f32(want).astype(np.float64)
+                if kind == "f32" and G * wl.q_len > 64:
+                    assert np.all(np.abs(got[b, i] - vw) <= 2.0 ** -20 * np.abs(vw)), (kind, b, i)
+                else:
+                    assert np.array_equal(got[b, i], vw), (kind, b, i)
 
 
 @pytest.mark.parametrize("case", [CASES[0], CASES[2], CASES[4]], ids=["narrow", "wide", "tmem"])
