@@ -112,8 +112,8 @@ def kernel_source_hash():
     """Hash of the attention kernel's sources, line comments and blank lines
     left out (a comment edit does not change the kernel the counters came from)."""
     h = hashlib.sha256()
-    for name in ("decode_attn.cuh", "decode_attn.cu", "decode_attn_fp8.cu", "ptx.cuh",
-                 "tcgen05.cuh", "pkv_internal.h"):
+    for name in ("decode_attn.cuh", "decode_attn.cu", "decode_attn_fp8.cu",
+                 "decode_attn_fp8_block.cu", "ptx.cuh", "tcgen05.cuh", "pkv_internal.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_256_gb300", "csrc", name)) as f:
             for line in f:
                 code = line.split("//", 1)[0].strip()
