@@ -61,6 +61,7 @@
 #include <atomic>
 #include <cfloat>
 #include <climits>
+#include <type_traits>
 
 #include "pkv_internal.h"
 #include "ptx.cuh"
@@ -1026,51 +1027,67 @@ __device__ __forceinline__ void consume_narrow(const AttnArgs& a, Walk w, uint8_
                     if (bi >= nb) continue;
                     const uint32_t vb = C::v_tile(sb, bi);
                     const int tok0 = (j0 + q * SBS + bi) * BS;
-                    uint32_t vm0 = 0xFFFFFFFFu, vm8 = 0xFFFFFFFFu;
-                    if (tok0 + BS > ctx) {
-                        const int ta = tok0 + tp * 16 + 2 * t;
-                        vm0 = (ta < ctx ? 0x0000FFFFu : 0u) | (ta + 1 < ctx ? 0xFFFF0000u : 0u);
-                        vm8 = (ta + 8 < ctx ? 0x0000FFFFu : 0u) | (ta + 9 < ctx ? 0xFFFF0000u : 0u);
-                    }
-                    if constexpr (KV8) {
-                        // x4.trans over tokens (0-7, 8-15) x bytes (32j.., 32j+16..): lane
-                        // (g, t) gets d (2g, 2g+1) of tokens (2t, 2t+1); the permute splits
-                        // them into the even-d and odd-d A fragments (M rows g, g+8 are
-                        // d 32j + 2g (+1) and 32j + 16 + 2g (+1)).
+                    // Only a unit's last block reaches past the context: the
+                    // masked form runs there alone (the warp-uniform branch
+                    // spares every other tile the mask instructions).
+                    auto pv_tile = [&](auto masked) {
+                        constexpr bool kMasked = decltype(masked)::value;
+                        uint32_t vm0 = 0xFFFFFFFFu, vm8 = 0xFFFFFFFFu;
+                        if (kMasked) {
+                            const int ta = tok0 + tp * 16 + 2 * t;
+                            vm0 = (ta < ctx ? 0x0000FFFFu : 0u) |
+                                  (ta + 1 < ctx ? 0xFFFF0000u : 0u);
+                            vm8 = (ta + 8 < ctx ? 0x0000FFFFu : 0u) |
+                                  (ta + 9 < ctx ? 0xFFFF0000u : 0u);
+                        }
+                        if constexpr (KV8) {
+                            // x4.trans over tokens (0-7, 8-15) x bytes (32j.., 32j+16..): lane
+                            // (g, t) gets d (2g, 2g+1) of tokens (2t, 2t+1); the permute splits
+                            // them into the even-d and odd-d A fragments (M rows g, g+8 are
+                            // d 32j + 2g (+1) and 32j + 16 + 2g (+1)).
 #pragma unroll
-                        for (int j = 0; j < D / 32; ++j) {
-                            uint32_t r[4];
-                            ldmatrix_x4_trans(r, vb + swz8<D>(tp * 16 + (mi & 1) * 8 + rr,
-                                                              32 * j + (mi >> 1) * 16));
-                            uint32_t ev[4], od[4];
+                            for (int j = 0; j < D / 32; ++j) {
+                                uint32_t r[4];
+                                ldmatrix_x4_trans(r, vb + swz8<D>(tp * 16 + (mi & 1) * 8 + rr,
+                                                                  32 * j + (mi >> 1) * 16));
+                                uint32_t ev[4], od[4];
 #pragma unroll
-                            for (int mm = 0; mm < 4; ++mm)
-                                e4m3x4_to_f16x2x2(prmt(r[mm], 0u, 0x3120u), ev[mm], od[mm]);
-                            const uint32_t ae[4] = {ev[0] & vm0, ev[2] & vm0, ev[1] & vm8,
-                                                    ev[3] & vm8};
-                            const uint32_t ao[4] = {od[0] & vm0, od[2] & vm0, od[1] & vm8,
-                                                    od[3] & vm8};
-                            mma_f16_16816(o[2 * j], ae, pb[u][0], pb[u][1]);
-                            mma_f16_16816(o[2 * j + 1], ao, pb[u][0], pb[u][1]);
-                            if (OUT_F32) {
-                                mma_f16_16816(o[2 * j], ae, pl[u][0], pl[u][1]);
-                                mma_f16_16816(o[2 * j + 1], ao, pl[u][0], pl[u][1]);
+                                for (int mm = 0; mm < 4; ++mm)
+                                    e4m3x4_to_f16x2x2(prmt(r[mm], 0u, 0x3120u), ev[mm], od[mm]);
+                                uint32_t ae[4] = {ev[0], ev[2], ev[1], ev[3]};
+                                uint32_t ao[4] = {od[0], od[2], od[1], od[3]};
+                                if constexpr (kMasked) {
+                                    ae[0] &= vm0; ae[1] &= vm0; ae[2] &= vm8; ae[3] &= vm8;
+                                    ao[0] &= vm0; ao[1] &= vm0; ao[2] &= vm8; ao[3] &= vm8;
+                                }
+                                mma_f16_16816(o[2 * j], ae, pb[u][0], pb[u][1]);
+                                mma_f16_16816(o[2 * j + 1], ao, pb[u][0], pb[u][1]);
+                                if (OUT_F32) {
+                                    mma_f16_16816(o[2 * j], ae, pl[u][0], pl[u][1]);
+                                    mma_f16_16816(o[2 * j + 1], ao, pl[u][0], pl[u][1]);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int dm = 0; dm < MT; ++dm) {
+                                uint32_t va[4];
+                                ldmatrix_x4_trans(va, vb + swz<BS>(tp * 16 + (mi >> 1) * 8 + rr,
+                                                                    dm * 16 + (mi & 1) * 8));
+                                if constexpr (kMasked) {
+                                    va[0] &= vm0;
+                                    va[1] &= vm0;
+                                    va[2] &= vm8;
+                                    va[3] &= vm8;
+                                }
+                                mma_bf16_16816(o[dm], va, pb[u][0], pb[u][1]);
+                                if (OUT_F32) mma_bf16_16816(o[dm], va, pl[u][0], pl[u][1]);
                             }
                         }
-                    } else {
-#pragma unroll
-                        for (int dm = 0; dm < MT; ++dm) {
-                            uint32_t va[4];
-                            ldmatrix_x4_trans(va, vb + swz<BS>(tp * 16 + (mi >> 1) * 8 + rr,
-                                                                dm * 16 + (mi & 1) * 8));
-                            va[0] &= vm0;
-                            va[1] &= vm0;
-                            va[2] &= vm8;
-                            va[3] &= vm8;
-                            mma_bf16_16816(o[dm], va, pb[u][0], pb[u][1]);
-                            if (OUT_F32) mma_bf16_16816(o[dm], va, pl[u][0], pl[u][1]);
-                        }
-                    }
+                    };
+                    if (tok0 + BS > ctx)
+                        pv_tile(std::true_type{});
+                    else
+                        pv_tile(std::false_type{});
                 }
             }
             __syncwarp();
@@ -2202,6 +2219,27 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                                     pack_bf16x2(__uint_as_float(ov[c + 2]) * scl, __uint_as_float(ov[c + 3]) * scl),
                                     pack_bf16x2(__uint_as_float(ov[c + 4]) * scl, __uint_as_float(ov[c + 5]) * scl),
                                     pack_bf16x2(__uint_as_float(ov[c + 6]) * scl, __uint_as_float(ov[c + 7]) * scl));
+                        }
+                    }
+                } else if constexpr (BLK) {
+                    // Per-block scales: fp32 rows one per thread.  (This
+                    // instantiation runs 384 threads at the 168-register cap;
+                    // the 16x256b form below measured 1.6 us slower here.)
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t ov[32];
+                        tmem_ld32(tlane + kColO + c0, ov);
+                        tmem_wait_ld();
+                        if (whole ? row_ok : row < R) {
+                            float* op =
+                                whole ? static_cast<float*>(a.out) +
+                                            (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D + c0
+                                      : a.rec_o + (rec * R + row) * D + c0;
+#pragma unroll
+                            for (int c = 0; c < 32; c += 4)
+                                *reinterpret_cast<float4*>(op + c) = make_float4(
+                                    __uint_as_float(ov[c]) * scl, __uint_as_float(ov[c + 1]) * scl,
+                                    __uint_as_float(ov[c + 2]) * scl, __uint_as_float(ov[c + 3]) * scl);
                         }
                     }
                 } else {
