@@ -87,6 +87,12 @@ typedef enum pkv_status {
  * when the driver declines the one-copy (three-dimensional) view of the V
  * cache.  Results are bit-identical either way; tests use it to run both. */
 #define PKV_FLAG_TILE_2D 0x20u
+/* Attention calls: keep one tile of at most 128 query rows per unit even
+ * where two would be taken together (the paired form: bf16 cache, bf16
+ * output, more than 128 query rows per KV head; it also falls back to one
+ * tile when the workspace is smaller than the size query reports).  Results
+ * agree within the stated tolerance; tests use it to run both forms. */
+#define PKV_FLAG_ONE_TILE 0x40u
 /* Bits 16..31 force the number of attention CTAs (0 = one per SM).  Tests
  * use it to move where long contexts are split; results stay within the
  * stated tolerance for every value. */

@@ -18,7 +18,7 @@ from ._lib import (  # noqa: F401
     PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_FLAG_CHECKED, PKV_FLAG_GRID, PKV_FLAG_TEST_STALL, PKV_OK, PKV_OUT_BF16,
     PKV_ERR_OUT_OF_BLOCKS, PKV_OUT_F32, BlockPool, PkvError, alloc_workspace, load_library,
     PKV_FLAG_KV_FP8, PKV_FLAG_NO_EARLY_START, PKV_KV_BF16, PKV_KV_FP8_E4M3,
-    PKV_FLAG_KV_BLOCK_SCALES, PKV_FLAG_TILE_2D, PKV_KV_FP8_E4M3_BLOCK, pkv_kv_append_fp8_block,
+    PKV_FLAG_KV_BLOCK_SCALES, PKV_FLAG_TILE_2D, PKV_FLAG_ONE_TILE, PKV_KV_FP8_E4M3_BLOCK, pkv_kv_append_fp8_block,
     pkv_check_error, pkv_copy_blocks, pkv_kv_append, pkv_kv_append_fp8, pkv_pool_alloc, pkv_pool_append_slots,
     pkv_pool_create, pkv_pool_destroy, pkv_pool_num_free, pkv_pool_refcount, pkv_pool_release,
     pkv_pool_share,

@@ -30,6 +30,7 @@ PKV_FLAG_KV_FP8 = 0x4
 PKV_FLAG_NO_EARLY_START = 0x8
 PKV_FLAG_KV_BLOCK_SCALES = 0x10
 PKV_FLAG_TILE_2D = 0x20
+PKV_FLAG_ONE_TILE = 0x40
 PKV_KV_BF16 = 0
 PKV_KV_FP8_E4M3 = 1
 PKV_KV_FP8_E4M3_BLOCK = 2

@@ -79,7 +79,9 @@ constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 // thread at 168 registers for 288 and for 384 threads alike.
 constexpr int kTmemConverters = 5;
 __host__ __device__ constexpr int threads_for(int mode, bool kv8) {
-    return mode == 2 && kv8 ? kThreads + 3 * 32 : kThreads;
+    // tensor-memory consumer: + 3 converter warps over an 8-bit cache; the
+    // paired form (mode 3) has eight softmax warps, the producer and two issuers
+    return mode == 3 ? kThreads + 2 * 32 : (mode == 2 && kv8 ? kThreads + 3 * 32 : kThreads);
 }
 constexpr int kMergeSlots = 4;                   // warps that park a partial per merge round
 constexpr int kIssueLanes = 8;                   // producer lanes issuing loads side by side
@@ -99,9 +101,13 @@ constexpr float kPShiftTmem = 128.f, kPShiftTmemInv = 1.f / 128.f;
 constexpr int kModeWide = 0;    // 8 < rows <= 64: mma.sync, rows on the M side
 constexpr int kModeNarrow = 1;  // rows <= 8: mma.sync, tokens on the M side
 constexpr int kModeTmem = 2;    // rows > 64: tcgen05, M = 128 row tiles, accumulators in TMEM
+constexpr int kModeTmem2 = 3;   // 256-row units: two M = 128 row tiles on every stage (bf16 only)
 
 template <int D, int BS, int MODE, bool KV8 = false, bool BLK = false>
 struct AttnCfg {
+    static constexpr bool kTmem = MODE == kModeTmem || MODE == kModeTmem2;
+    static constexpr int kQRows = MODE == kModeTmem2 ? 256 : 128;  // rows of the query tile
+    static_assert(MODE != kModeTmem2 || (!KV8 && !BLK), "the paired form is bf16 only");
     static constexpr int kTileBytes = BS * D * (KV8 ? 1 : 2);  // one K (or V) tile of one (block, head)
     // TMA boxes per tile: bf16 in 64-column (128-byte) boxes; e4m3 rows of D
     // bytes in one box (128-byte swizzle at D = 128, 64-byte at D = 64).
@@ -119,7 +125,7 @@ struct AttnCfg {
     // (TMEM consumer, bf16 at d 128, V by 3-D copies: the V half of the stage
     // is [block][half][rows] instead, one copy per block.)
     static constexpr int kBlocksPerStage =
-        MODE == kModeTmem ? 64 / BS : (2 * kTileBytes >= 8192 ? 1 : 8192 / (2 * kTileBytes));
+        kTmem ? 64 / BS : (2 * kTileBytes >= 8192 ? 1 : 8192 / (2 * kTileBytes));
     static constexpr int kRegion = kBlocksPerStage * kBoxBytes;
     static constexpr int kStageBytes = 2 * kBoxes * kRegion;
     // An 8-bit cache keeps a (block, head)'s V rows right after its K rows,
@@ -135,13 +141,13 @@ struct AttnCfg {
     }
     // Per-lane floats a warp parks for a merge round: its accumulator, m[2], l[2].
     static constexpr int kLaneFloats = (MODE == kModeNarrow ? D / 4 : D / 2) + 4;
-    static constexpr int kMergeBytes = MODE == kModeTmem ? 0 : kMergeSlots * 32 * kLaneFloats * 4;
+    static constexpr int kMergeBytes = kTmem ? 0 : kMergeSlots * 32 * kLaneFloats * 4;
     // Narrow emit: rows x head_dim fp32 tile (+4 floats of row padding) and (m, l) per row.
     static constexpr int kTileStride = D + 4;
     static constexpr int kEmitBytes =
         MODE == kModeNarrow ? (kNarrowRows * kTileStride + 2 * kNarrowRows) * 4 : 0;
     // TMEM mode: the unit's 128 query rows as a swizzled K-major tile.
-    static constexpr int kQTileBytes = MODE == kModeTmem ? 128 * D * 2 : 0;
+    static constexpr int kQTileBytes = kTmem ? kQRows * D * 2 : 0;
     // TMEM mode over an 8-bit cache: kCvtCopies f16 copies of a 64-key stage
     // (K and V, each 64 rows in D/64 swizzled 64-column regions).  A copy is
     // held from its conversion until its PV product completes; with two, the
@@ -150,17 +156,17 @@ struct AttnCfg {
     static constexpr int kCvtCopies = 3;
     static constexpr int kCvtRegion = 64 * 128;
     static constexpr int kCvtBytes =
-        (MODE == kModeTmem && KV8) ? kCvtCopies * 2 * (D / 64) * kCvtRegion : 0;
+        (kTmem && KV8) ? kCvtCopies * 2 * (D / 64) * kCvtRegion : 0;
     // Per-(block, KV head) scales (BLK): each block of a stage brings 16 bytes
     // {K scale, V scale, 0, 0} with its tiles, into a slot beside the ring;
     // the tensor-memory consumer's converter warps copy a super-block's scales
     // next to its f16 copy (kCvtCopies copies x blocks x {K, V}).
     static constexpr int kSlotBytes = BLK ? kBlocksPerStage * 16 : 0;
     static constexpr int kCvtSlotBytes =
-        (BLK && MODE == kModeTmem) ? kCvtCopies * kBlocksPerStage * 8 : 0;
+        (BLK && kTmem) ? kCvtCopies * kBlocksPerStage * 8 : 0;
     static constexpr int kScratchBytes =
         kMergeBytes + kEmitBytes + kQTileBytes + kCvtBytes + kCvtSlotBytes;
-    static constexpr int kMaxStages = MODE == kModeTmem ? (KV8 ? 24 : 16) : (KV8 ? 48 : 32);
+    static constexpr int kMaxStages = kTmem ? (KV8 ? 24 : 16) : (KV8 ? 48 : 32);
     static constexpr int kBarrierBytes = 2 * kMaxStages * 8;
     static constexpr int kBudget = 227 * 1024 - 1024 - kScratchBytes - kBarrierBytes - 1024;
     // In the mma.sync modes the ring depth is a multiple of the consumer-warp
@@ -172,18 +178,18 @@ struct AttnCfg {
     static constexpr int kStagesRaw = kBudget / (kStageBytes + kSlotBytes);
     static constexpr int kStages =
         kStagesRaw >= kMaxStages ? kMaxStages
-                                 : (MODE == kModeTmem ? kStagesRaw : (kStagesRaw / 8) * 8);
+                                 : (kTmem ? kStagesRaw : (kStagesRaw / 8) * 8);
     static constexpr int kSmemBytes =
         1024 + kStages * kStageBytes + kScratchBytes + 2 * kStages * 8 + kStages * kSlotBytes;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BS == 16 || BS == 32, "block_size");
-    static_assert(MODE == kModeTmem ? kStages >= 2
+    static_assert(kTmem ? kStages >= 2
                                     : (kStages % kConsumerWarps == 0 && kStages >= kConsumerWarps),
                   "ring depth");
-    static_assert(MODE == kModeTmem || kStages >= kIssueLanes, "one stage per issue lane");
+    static_assert(kTmem || kStages >= kIssueLanes, "one stage per issue lane");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     // The mma.sync consumers address a block's boxes BS * 128 bytes apart.
-    static_assert(MODE == kModeTmem || kBlocksPerStage == 1 || kBoxes == 1, "stage layout");
+    static_assert(kTmem || kBlocksPerStage == 1 || kBoxes == 1, "stage layout");
 };
 
 // Byte offset of the 16-byte chunk holding (row, col..col+7) inside a tile
@@ -1637,9 +1643,10 @@ __device__ __forceinline__ void consume_wide(const AttnArgs& a, Walk w, uint8_t*
 // the normalisation.
 // The query tile of unit (sequence s, KV head h, row tile t) by TMA (query
 // map present): D/64 boxes of 64 columns x a.rows rows, landing as the
-// swizzled K-major tile the score MMA reads; completes on `bar`.  Rows of a
+// swizzled K-major tile the score MMA reads (64-column region r at
+// r * QROWS * 128 bytes); completes on `bar`.  Rows of a
 // partial tile past a.rows keep stale bits; their scores are all masked.
-template <int D>
+template <int D, int QROWS>
 __device__ __forceinline__ void issue_q_tile(const AttnArgs& a, const CUtensorMap* tmap_q,
                                              uint8_t* qtile, uint64_t* bar, int s, int h, int t) {
     const int r0 = t * a.rows;
@@ -1647,7 +1654,7 @@ __device__ __forceinline__ void issue_q_tile(const AttnArgs& a, const CUtensorMa
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(D / 64) * 128u * static_cast<uint32_t>(a.rows));
 #pragma unroll
     for (int half = 0; half < D / 64; ++half)
-        tma_load_3d(qtile + half * 128 * 128, tmap_q, half * 64, y, z, bar);
+        tma_load_3d(qtile + half * QROWS * 128, tmap_q, half * 64, y, z, bar);
 }
 
 // Per-(block, KV head) scales (BLK, 8-bit cache only): the converter warps
@@ -1656,47 +1663,72 @@ __device__ __forceinline__ void issue_q_tile(const AttnArgs& a, const CUtensorMa
 // scale before taking the row maximum, and weighs each block's probabilities
 // by its V scale relative to vrun, the largest V scale of the unit so far (O
 // is rescaled in TMEM when vrun grows, together with a grown maximum).
-template <int D, int BS, bool OUT_F32, bool KV8, bool BLK>
+//
+// T2 = 2 (the paired form, 256-row units over a bf16 cache, bf16 output):
+// the unit's rows are two 128-row sub-tiles that share every stage.  Softmax
+// warps 0-3 take sub-tile 0 and warps 4-7 sub-tile 1 (TMEM lanes again 0..127,
+// in their own columns: O of sub-tile u at u * 128, its score slot at 256 +
+// u * 64, its two P buffers at 384 + u * 64); warp 9 issues both score
+// products of a stage, warp 10 both PV products, and a stage is freed when
+// both are done.  Each sub-tile has one score slot: the softmax reads S at
+// the start of its round, so the next stage's product can refill the slot
+// while the exponentials run.  Half the stages per score FLOP (the producer
+// spends ~60 ns of TMA issue per box, which bounded the one-tile form on
+// chunked prefill) at the price of a 64 KB query tile (a five-stage ring).
+template <int D, int BS, bool OUT_F32, bool KV8, bool BLK, int T2 = 1>
 __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t* stages,
                                              const uint8_t* slots, uint8_t* qtile,
                                              const CUtensorMap* tmap_q, uint64_t* full_bar,
                                              uint64_t* empty_bar, uint64_t* tcb, uint32_t* s_tmem,
                                              volatile int* s_abort, int4& info0, int4& info1) {
     static_assert(!BLK || KV8, "block scales come with the 8-bit cache");
-    using C = AttnCfg<D, BS, kModeTmem, KV8, BLK>;
+    static_assert(T2 == 1 || (!KV8 && !OUT_F32), "the paired form: bf16 cache, bf16 output");
+    using C = AttnCfg<D, BS, T2 == 2 ? kModeTmem2 : kModeTmem, KV8, BLK>;
     constexpr int kStages = C::kStages;
     constexpr int kKeys = 64;                  // keys per softmax round
     constexpr int SB = C::kBlocksPerStage;     // blocks per super-block (= per stage)
     static_assert(SB * BS == kKeys, "a stage holds one super-block");
     constexpr uint32_t kTmemCols = 512;
-    constexpr uint32_t kColO = 0, kColS = 128, kColP = 256, kColPL = 320;
+    // O of sub-tile u at kColO + 128 u; score slots of 64 columns from kColS;
+    // P buffers of 32 columns from kColP (two per sub-tile); fp32 output's low
+    // halves of P from kColPL (one-tile form only)
+    constexpr uint32_t kColO = 0, kColS = T2 == 2 ? 256 : 128, kColP = T2 == 2 ? 384 : 256,
+                       kColPL = 320;
     constexpr int KT = D / 16;   // k steps of S = Q K^T
-    constexpr int kQHalf = 128 * 128;  // bytes of one 64-column half of the Q tile
-    // warps 0..5 take part, and the converter warps 6, 7, 9, 10, 11 over an 8-bit cache
-    constexpr int kParty = KV8 ? threads_for(kModeTmem, true) - 32 : 192;
+    constexpr int kQHalf = C::kQRows * 128;  // bytes of one 64-column half of the Q tile
+    // warps 0..5 take part (paired: 0..7, 9, 10), and the converter warps 6, 7,
+    // 9, 10, 11 over an 8-bit cache
+    constexpr int kParty = KV8 ? threads_for(kModeTmem, true) - 32 : (T2 == 2 ? 320 : 192);
+    constexpr int kQKWarp = T2 == 2 ? 9 : 4, kPVWarp = T2 == 2 ? 10 : 5;
     constexpr int kHalves = D / 64;          // 64-column regions of an f16 K or V copy
-    // tcb: [0..1] S ready, [2..3] S read, [4..5] P ready, [6..7] PV done, [8] QK teardown,
-    //      [9] PV teardown, [10..12] f16 copy ready, [13..15] f16 copy read, [16] Q landed,
-    //      [17] Q read, [18] Q widened
+    // tcb: [0..1] S ready, [2..3] S read (per score slot), [4..7] P ready, [8..11] PV done
+    //      (per sub-tile u and P buffer b: 2u + b), [12] QK teardown, [13] PV teardown,
+    //      [14..16] f16 copy ready, [17..19] f16 copy read, [20] Q landed, [21] Q read,
+    //      [22] Q widened
     uint64_t* s_full = tcb;
     uint64_t* s_free = tcb + 2;
     uint64_t* p_full = tcb + 4;
-    uint64_t* pv_done = tcb + 6;
+    uint64_t* pv_done = tcb + 8;
     constexpr uint32_t kCopies = C::kCvtCopies;
-    uint64_t* cvt_full = tcb + 10;  // 8-bit cache: f16 copy [g % kCopies] ready
-    uint64_t* cvt_free = tcb + 13;  // 8-bit cache: f16 copy [g % kCopies] read by its PV product
-    uint64_t* q_full = tcb + 16;    // query tile landed (TMA)
-    uint64_t* q_empty = tcb + 17;   // the piece's score products have read the query tile
-    uint64_t* q_conv = tcb + 18;    // 8-bit cache: the query tile widened to f16
+    uint64_t* cvt_full = tcb + 14;  // 8-bit cache: f16 copy [g % kCopies] ready
+    uint64_t* cvt_free = tcb + 17;  // 8-bit cache: f16 copy [g % kCopies] read by its PV product
+    uint64_t* q_full = tcb + 20;    // query tile landed (TMA)
+    uint64_t* q_empty = tcb + 21;   // the piece's score products have read the query tile
+    uint64_t* q_conv = tcb + 22;    // 8-bit cache: the query tile widened to f16
+    // Score slot of stage g for sub-tile u, and the parity of its g-th use.
+    auto sslot = [](uint32_t g, int u) -> uint32_t { return T2 == 2 ? (uint32_t)u : (g & 1u); };
+    auto spar = [](uint32_t g) -> uint32_t { return T2 == 2 ? (g & 1u) : ((g >> 1) & 1u); };
     // f16 copies (8-bit cache): copy c at cvt + c * kCopy, K regions then V regions
     uint8_t* cvt = qtile + C::kQTileBytes;
     constexpr int kCopy = 2 * kHalves * C::kCvtRegion;
     // BLK: scales of the super-block in f16 copy c: [c][block][K, V]
     float* cvt_sc = reinterpret_cast<float*>(cvt + C::kCvtBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp > 5 && !KV8) return;  // warps 6, 7 have no part in this mode over bf16
-    const bool softmax = warp < 4;
-    const int row = threadIdx.x;  // softmax threads: row = TMEM lane
+    if (!KV8 && T2 == 1 && warp > 5) return;  // warps 6, 7 have no part in this mode over bf16
+    const bool softmax = warp < 4 * T2;
+    const int sub = T2 == 2 ? ((warp >> 2) & 1) : 0;  // softmax threads: their sub-tile
+    const int row = threadIdx.x & 127;                // softmax threads: row = TMEM lane
+    const int trow = sub * 128 + row;                 // ... and their row of the unit's tile
     const int R = a.rows, cta = blockIdx.x;
 
     if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
@@ -1731,7 +1763,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         int lim = -1, lo = INT_MIN, i_row = 0, hq_row = 0;
         bool row_ok = false;
         if (softmax) {
-            row_ok = unit_row(a, w.t, h, row, i_row, hq_row);
+            row_ok = unit_row(a, w.t, h, trow, i_row, hq_row);
             lim = row_ok ? ctx - a.q_len + i_row : -1;
             if (a.window > 0) lo = lim - a.window + 1;
         }
@@ -1744,8 +1776,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 if (good) {
 #pragma unroll
                     for (int c = 0; c < D / 8; ++c) {
-                        uint4* pq = reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + row * 128 +
-                                                             (((c & 7) ^ (row & 7)) << 4));
+                        uint4* pq = reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + trow * 128 +
+                                                             (((c & 7) ^ (trow & 7)) << 4));
                         const uint4 v = *pq;
                         *pq = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
                                          bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
@@ -1771,8 +1803,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             }
 #pragma unroll
             for (int c = 0; c < D / 8; ++c)
-                *reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + row * 128 +
-                                          (((c & 7) ^ (row & 7)) << 4)) = qv[c];
+                *reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + trow * 128 +
+                                          (((c & 7) ^ (trow & 7)) << 4)) = qv[c];
             fence_proxy_async_smem();
         }
         if (!a.q_tma) {
@@ -1785,7 +1817,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         // overwrites O, waits for P of its first super-block, which the
         // softmax threads write only after reading the previous O.)
 
-        if (warp == 4) {
+        if (warp == kQKWarp) {
             // ===================== QK issuer =====================
             if (lane == 0 && ok && a.q_tma) {
                 // This piece's query tile: landed, and over an 8-bit cache
@@ -1800,35 +1832,43 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 tc_fence_after();
             }
             if (lane == 0 && ok) {
-                for (int q = 0; q < nsb; ++q) {
+                // A score slot is reused by the stage T2 later (paired: the same
+                // sub-tile's next stage; else the stage after next).
+                constexpr uint32_t kReuse = T2 == 2 ? 1u : 2u;
+                for (int q = 0; q < nsb && ok; ++q) {
                     const uint32_t g = gbase + q, st = g % kStages;
-                    if (g >= 2 &&
-                        (*s_abort || !mbar_wait_bounded(&s_free[g & 1u], ((g - 2) >> 1) & 1u))) {
-                        issuer_fail(ok);
-                        break;
-                    }
                     if (*s_abort ||
                         !(KV8 ? mbar_wait_bounded(&cvt_full[g % kCopies], (g / kCopies) & 1u)
                               : mbar_wait_bounded(&full_bar[st], (g / kStages) & 1u))) {
                         issuer_fail(ok);
                         break;
                     }
-                    tc_fence_after();
                     // Rows past the stage's blocks (a partial last super-block)
                     // hold stale keys; the softmax masks their columns.
                     const uint32_t kb = KV8 ? smem_addr(cvt + (g % kCopies) * kCopy)
                                             : smem_addr(stages + st * C::kStageBytes);
                     constexpr uint32_t kKRegion = KV8 ? C::kCvtRegion : C::kRegion;
-                    const uint32_t scol = tbase + kColS + (g & 1u) * kKeys;
 #pragma unroll
-                    for (int kk = 0; kk < KT; ++kk) {
-                        const uint64_t ad = umma_smem_desc(
-                            q_saddr + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = umma_smem_desc(
-                            kb + (kk >> 2) * kKRegion + (kk & 3) * 32, 16, 1024);
-                        umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                    for (int u = 0; u < T2; ++u) {
+                        const uint32_t slot = sslot(g, u);
+                        if (g >= kReuse && (*s_abort || !mbar_wait_bounded(&s_free[slot],
+                                                                          spar(g - kReuse)))) {
+                            issuer_fail(ok);
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t scol = tbase + kColS + slot * kKeys;
+#pragma unroll
+                        for (int kk = 0; kk < KT; ++kk) {
+                            const uint64_t ad = umma_smem_desc(
+                                q_saddr + (kk >> 2) * kQHalf + u * 128 * 128 + (kk & 3) * 32, 16,
+                                1024);
+                            const uint64_t bd = umma_smem_desc(
+                                kb + (kk >> 2) * kKRegion + (kk & 3) * 32, 16, 1024);
+                            umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&s_full[slot]);
                     }
-                    umma_commit(&s_full[g & 1u]);
                 }
             }
             if (lane == 0 && ok && a.q_tma) {
@@ -1842,25 +1882,18 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     if (!mbar_wait_bounded(q_empty, piece & 1)) {
                         issuer_fail(ok);
                     } else {
-                        issue_q_tile<D>(a, tmap_q, qtile, q_full, wn.s, wn.h, wn.t);
+                        issue_q_tile<D, C::kQRows>(a, tmap_q, qtile, q_full, wn.s, wn.h, wn.t);
                         q_pending = true;
                         q_pending_par = (piece + 1) & 1;
                     }
                 }
             }
             __syncwarp();
-        } else if (warp == 5) {
+        } else if (warp == kPVWarp) {
             // ===================== PV issuer =====================
             if (lane == 0 && ok) {
-                for (int q = 0; q < nsb; ++q) {
+                for (int q = 0; q < nsb && ok; ++q) {
                     const uint32_t g = gbase + q, st = g % kStages;
-                    if (*s_abort || !mbar_wait_bounded(&p_full[g & 1u], (g >> 1) & 1u)) {
-                        issuer_fail(ok);
-                        break;
-                    }
-                    tc_fence_after();
-                    // The softmax saw S of this stage, so its score product
-                    // (the only other reader of the stage) has completed.
                     // Only the keys of the stage's blocks enter the product.
                     const int nk16 = min(SB, n - q * SB) * (BS / 16);
                     const uint32_t vb =
@@ -1871,26 +1904,40 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     // (2-D copies), or each block's two halves together (3-D).
                     const uint32_t vlbo = KV8 ? C::kCvtRegion : (v3 ? C::kBoxBytes : C::kRegion);
                     const uint32_t pcol = (g & 1u) * (kKeys / 2);
-                    for (int kk = 0; kk < nk16; ++kk) {
-                        const uint32_t vrow =
-                            v3 ? (kk / (BS / 16)) * 2 * C::kBoxBytes + (kk % (BS / 16)) * 16 * 128
-                               : kk * 16 * 128;
-                        const uint64_t bd = umma_smem_desc(vb + vrow, vlbo, 1024);
-                        umma_ts(tbase + kColO, tbase + kColP + pcol + kk * 8, bd, idesc_pv,
-                                (q > 0 || kk > 0) ? 1u : 0u);
-                        if (OUT_F32)
-                            umma_ts(tbase + kColO, tbase + kColPL + pcol + kk * 8, bd, idesc_pv,
-                                    1u);
+#pragma unroll
+                    for (int u = 0; u < T2; ++u) {
+                        const uint32_t pb = 2u * u + (g & 1u);  // P buffer of sub-tile u
+                        if (*s_abort || !mbar_wait_bounded(&p_full[pb], (g >> 1) & 1u)) {
+                            issuer_fail(ok);
+                            break;
+                        }
+                        tc_fence_after();
+                        // The softmax saw S of this stage, so its score product
+                        // (with the other sub-tile's, the only readers of the
+                        // stage's K) has completed.
+                        const uint32_t ocol = tbase + kColO + u * 128;
+                        const uint32_t pc = tbase + kColP + u * kKeys + pcol;
+                        for (int kk = 0; kk < nk16; ++kk) {
+                            const uint32_t vrow =
+                                v3 ? (kk / (BS / 16)) * 2 * C::kBoxBytes +
+                                         (kk % (BS / 16)) * 16 * 128
+                                   : kk * 16 * 128;
+                            const uint64_t bd = umma_smem_desc(vb + vrow, vlbo, 1024);
+                            umma_ts(ocol, pc + kk * 8, bd, idesc_pv, (q > 0 || kk > 0) ? 1u : 0u);
+                            if (OUT_F32)
+                                umma_ts(ocol, tbase + kColPL + pcol + kk * 8, bd, idesc_pv, 1u);
+                        }
+                        umma_commit(&pv_done[pb]);  // its P buffer is free; O is current
                     }
+                    if (!ok) break;
                     if (KV8)
                         umma_commit(&cvt_free[g % kCopies]);  // the f16 copy is consumed
                     else
                         umma_commit(&empty_bar[st]);  // K and V of this stage are consumed
-                    umma_commit(&pv_done[g & 1u]);    // its P buffer is free; O is current
                 }
             }
             __syncwarp();
-        } else if (warp >= 6) {
+        } else if (!softmax) {
             // ===================== f16 copies (8-bit cache; five warps) ============
             if constexpr (KV8) {
                 // A stage's 2 x 64 rows (K rows, then V rows) are 2 * kRounds rounds
@@ -2001,14 +2048,14 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             for (int q = 0; q < nsb; ++q) {
                 const uint32_t sq = gbase + q;  // this super-block's stage
                 const int nb = min(SB, n - q * SB);
-                ok = consumer_wait(a, &s_full[sq & 1u], (sq >> 1) & 1u, ok, s_abort);
+                ok = consumer_wait(a, &s_full[sslot(sq, sub)], spar(sq), ok, s_abort);
                 if (!ok) continue;
                 tc_fence_after();
                 float x[kKeys];
                 {
                     uint32_t s0[32], s1[32];
-                    tmem_ld32(tlane + kColS + (sq & 1u) * kKeys, s0);
-                    tmem_ld32(tlane + kColS + (sq & 1u) * kKeys + 32, s1);
+                    tmem_ld32(tlane + kColS + sslot(sq, sub) * kKeys, s0);
+                    tmem_ld32(tlane + kColS + sslot(sq, sub) * kKeys + 32, s1);
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
@@ -2016,7 +2063,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         x[32 + c] = __uint_as_float(s1[c]);
                     }
                     tc_fence_before();
-                    mbar_arrive(&s_free[sq & 1u]);  // S buffer may take the super-block after next
+                    mbar_arrive(&s_free[sslot(sq, sub)]);  // the score slot may be refilled
                 }
                 // BLK: the blocks' scales (written by the converter warps, acquired through
                 // their copy-ready barrier, whose phase for this super-block has completed)
@@ -2080,7 +2127,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 const float mloc = t[0] == hidden ? -INFINITY : t[0] * sl2;
                 // This P buffer was last read by the PV of super-block q - 2.
                 if (q > 1) {
-                    ok = consumer_wait(a, &pv_done[sq & 1u], ((sq - 2) >> 1) & 1u, ok, s_abort);
+                    ok = consumer_wait(a, &pv_done[2 * sub + (sq & 1u)], ((sq - 2) >> 1) & 1u, ok,
+                                       s_abort);
                     if (!ok) continue;
                     tc_fence_after();
                 }
@@ -2088,8 +2136,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 if (__any_sync(0xffffffffu, grow) || vgrow) {  // (vgrow is CTA-uniform)
                     // O may only be rescaled once the previous super-block's PV is done.
                     if (q > 0) {
-                        ok = consumer_wait(a, &pv_done[(sq - 1) & 1u], ((sq - 1) >> 1) & 1u, ok,
-                                           s_abort);
+                        ok = consumer_wait(a, &pv_done[2 * sub + ((sq - 1) & 1u)],
+                                           ((sq - 1) >> 1) & 1u, ok, s_abort);
                         if (!ok) continue;
                         tc_fence_after();
                     }
@@ -2107,13 +2155,13 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
 #pragma unroll 1
                         for (int c0 = 0; c0 < D; c0 += 32) {
                             uint32_t ov[32];
-                            tmem_ld32(tlane + kColO + c0, ov);
+                            tmem_ld32(tlane + kColO + sub * 128 + c0, ov);
                             tmem_wait_ld();
                             const float oscale = alpha * vfac;
 #pragma unroll
                             for (int c = 0; c < 32; ++c)
                                 ov[c] = __float_as_uint(__uint_as_float(ov[c]) * oscale);
-                            tmem_st32(tlane + kColO + c0, ov);
+                            tmem_st32(tlane + kColO + sub * 128 + c0, ov);
                         }
                         tmem_wait_st();
                     }
@@ -2164,14 +2212,16 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 }
                 const float rs = (rs0 + rs1) + (rs2 + rs3);
                 l += rs;
-                tmem_st32(tlane + kColP + (sq & 1u) * (kKeys / 2), ph);
+                tmem_st32(tlane + kColP + sub * kKeys + (sq & 1u) * (kKeys / 2), ph);
                 if (OUT_F32) tmem_st32(tlane + kColPL + (sq & 1u) * (kKeys / 2), pl);
                 tmem_wait_st();
                 // V rows past the context may hold NaN; 0 * NaN would poison O.
                 // Only a unit's last block reaches past the context, and it is
                 // the last block of its super-block.
                 const int tokl = tok0 + (nb - 1) * BS;
-                if (!KV8 && tokl + BS > ctx) {  // (the f16 copies come zeroed there)
+                // (Paired: sub-tile 0 alone; the PV issuer takes sub-tile 1
+                // after sub-tile 0's P, so after these zeros.)
+                if (!KV8 && sub == 0 && tokl + BS > ctx) {  // (the f16 copies come zeroed there)
                     uint8_t* vt = stages + (sq % kStages) * C::kStageBytes +
                                   C::kBoxes * C::kRegion +
                                   (nb - 1) * (v3 ? 2 * C::kBoxBytes : C::kBoxBytes);
@@ -2186,13 +2236,13 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     fence_proxy_async_smem();
                 }
                 tc_fence_before();
-                mbar_arrive(&p_full[sq & 1u]);
+                mbar_arrive(&p_full[2 * sub + (sq & 1u)]);
             }
 
             // ---- epilogue: the last PV, then O out of TMEM row by row
             if (nsb > 0) {
                 const uint32_t sl = gbase + nsb - 1;
-                ok = consumer_wait(a, &pv_done[sl & 1u], (sl >> 1) & 1u, ok, s_abort);
+                ok = consumer_wait(a, &pv_done[2 * sub + (sl & 1u)], (sl >> 1) & 1u, ok, s_abort);
             }
             tc_fence_after();
             const bool first_piece = j0 == w.jlo, last_piece = j1 == w.nb;
@@ -2206,7 +2256,7 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t ov[32];
-                        tmem_ld32(tlane + kColO + c0, ov);
+                        tmem_ld32(tlane + kColO + sub * 128 + c0, ov);
                         tmem_wait_ld();
                         if (row_ok) {
                             const size_t ob =
@@ -2228,13 +2278,13 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t ov[32];
-                        tmem_ld32(tlane + kColO + c0, ov);
+                        tmem_ld32(tlane + kColO + sub * 128 + c0, ov);
                         tmem_wait_ld();
-                        if (whole ? row_ok : row < R) {
+                        if (whole ? row_ok : trow < R) {
                             float* op =
                                 whole ? static_cast<float*>(a.out) +
                                             (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D + c0
-                                      : a.rec_o + (rec * R + row) * D + c0;
+                                      : a.rec_o + (rec * R + trow) * D + c0;
 #pragma unroll
                             for (int c = 0; c < 32; c += 4)
                                 *reinterpret_cast<float4*>(op + c) = make_float4(
@@ -2256,7 +2306,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         float sc[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int r = rq + g8 + 8 * u;  // tile row (lane r % 32 holds its scl)
+                            // tile row; lane r % 32 holds its scl
+                            const int r = sub * 128 + rq + g8 + 8 * u;
                             sc[u] = __shfl_sync(0xffffffffu, scl, (r & 31));
                             dst[u] = nullptr;
                             if (whole) {
@@ -2271,7 +2322,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
 #pragma unroll 1
                         for (int c0 = 0; c0 < D; c0 += 32) {
                             uint32_t ov[16];
-                            tmem_ld_16x256b_x4(tbase + ((uint32_t)rq << 16) + kColO + c0, ov);
+                            tmem_ld_16x256b_x4(tbase + ((uint32_t)rq << 16) + kColO + sub * 128 + c0,
+                                               ov);
                             tmem_wait_ld();
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
@@ -2287,9 +2339,9 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     }
                 }
                 if (!whole) {
-                    if (row < R)
-                        *reinterpret_cast<float2*>(a.rec_ml + (rec * R + row) * 2) = make_float2(m_used, l);
-                    if (row == 0) {
+                    if (trow < R)
+                        *reinterpret_cast<float2*>(a.rec_ml + (rec * R + trow) * 2) = make_float2(m_used, l);
+                    if (trow == 0) {
                         const int4 rinfo = make_int4(
                             s, h, kRecValid | (first_piece ? kRecFirst : 0) | (last_piece ? kRecLast : 0),
                             w.t);
@@ -2309,11 +2361,11 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     }
     // Teardown: no tensor-core operation may still be running when TMEM is
     // freed, and no query-tile copy may still be landing.
-    if ((warp == 4 || warp == 5) && lane == 0) {
-        uint64_t* bar = &tcb[warp == 4 ? 8 : 9];
+    if ((warp == kQKWarp || warp == kPVWarp) && lane == 0) {
+        uint64_t* bar = &tcb[warp == kQKWarp ? 12 : 13];
         umma_commit(bar);
         (void)mbar_wait_bounded(bar, 0u);
-        if (warp == 4 && q_pending) (void)mbar_wait_bounded(q_full, q_pending_par);
+        if (warp == kQKWarp && q_pending) (void)mbar_wait_bounded(q_full, q_pending_par);
     }
     tc_fence_before();
     named_barrier_sync(2, kParty);
@@ -2346,10 +2398,10 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
     __shared__ long long s_pos[4];
     __shared__ Walk s_walk;
     __shared__ int s_abort;
-    // TMEM mode: S ready/read, P ready, PV done (x2 each), 2 teardowns, over an
-    // 8-bit cache f16 copy ready / free (x3 each), query tile landed / read /
-    // widened
-    __shared__ uint64_t s_tcb[19];
+    // TMEM modes: S ready/read (x2 each), P ready, PV done (x4 each), 2
+    // teardowns, over an 8-bit cache f16 copy ready / free (x3 each), query
+    // tile landed / read / widened
+    __shared__ uint64_t s_tcb[23];
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -2363,16 +2415,17 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
             mbar_init(&full_bar[i], 1);
             mbar_init(&empty_bar[i], releases);
         }
-        if (MODE == kModeTmem) {
-            // S ready (a commit), S read (128 rows), P ready (128 rows),
-            // PV done (a commit), two issuer teardowns (a commit each), f16
+        if (C::kTmem) {
+            // S ready (a commit), S read (128 rows), P ready (128 rows) and
+            // PV done (a commit) per sub-tile and buffer, two issuer
+            // teardowns (a commit each), f16
             // copy ready (the converter warps) / free (a commit), query tile
             // landed (the TMA) / read (a commit) / widened (128 rows)
             const uint32_t cvt = KV8 ? (uint32_t)kTmemConverters : 1u;
-            const uint32_t counts[19] = {1, 1, 128, 128, 128, 128, 1, 1, 1, 1, cvt, cvt, cvt,
-                                         1, 1, 1, 1, 1, 128};
+            const uint32_t counts[23] = {1,   1,   128, 128, 128, 128, 128, 128, 1, 1, 1, 1,
+                                         1,   1,   cvt, cvt, cvt, 1,   1,   1,   1, 1, 128};
             static_assert(C::kCvtCopies == 3, "barrier counts: three f16 copies");
-            for (int i = 0; i < 19; ++i) mbar_init(&s_tcb[i], counts[i]);
+            for (int i = 0; i < 23; ++i) mbar_init(&s_tcb[i], counts[i]);
         }
         fence_barrier_init();
         s_abort = 0;
@@ -2414,12 +2467,12 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
 
     // Tensor-memory consumer with TMA query tiles: the first tile is issued
     // before the producer's first stage, so it is not queued behind the ring fill.
-    if constexpr (MODE == kModeTmem) {
+    if constexpr (C::kTmem) {
         if (a.q_tma) {
-            if (warp == 4) {
+            if (warp == (MODE == kModeTmem2 ? 9 : 4)) {  // the QK issuer
                 if (lane == 0 && w0.left > 0)
-                    issue_q_tile<D>(a, &tmap_q, reinterpret_cast<uint8_t*>(scratch), &s_tcb[16],
-                                    w0.s, w0.h, w0.t);
+                    issue_q_tile<D, C::kQRows>(a, &tmap_q, reinterpret_cast<uint8_t*>(scratch),
+                                               &s_tcb[20], w0.s, w0.h, w0.t);
                 __syncwarp();
                 named_barrier_arrive(3, 64);
             } else if (warp == kConsumerWarps) {
@@ -2429,7 +2482,7 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
     }
     if (warp == kConsumerWarps) {
         produce<D, BS, kStages, C::kStageBytes, C::kTileBytes, C::kBoxBytes, C::kBoxes,
-                C::kBoxCols, C::kRegion, C::kBlocksPerStage, KV8, MODE == kModeTmem, BLK>(
+                C::kBoxCols, C::kRegion, C::kBlocksPerStage, KV8, C::kTmem, BLK>(
             a, &tmap_k, &tmap_v, w0, stages, slots, full_bar, empty_bar, &s_abort);
         return;
     }
@@ -2461,10 +2514,9 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
         consume_wide<D, BS, OUT_F32, KV8, BLK>(a, w0, stages, slots, scratch, full_bar, empty_bar,
                                                &s_abort, info0, info1);
     else
-        consume_tmem<D, BS, OUT_F32, KV8, BLK>(a, w0, stages, slots,
-                                               reinterpret_cast<uint8_t*>(scratch), &tmap_q,
-                                               full_bar, empty_bar, s_tcb, &s_tmem, &s_abort,
-                                               info0, info1);
+        consume_tmem<D, BS, OUT_F32, KV8, BLK, MODE == kModeTmem2 ? 2 : 1>(
+            a, w0, stages, slots, reinterpret_cast<uint8_t*>(scratch), &tmap_q, full_bar,
+            empty_bar, s_tcb, &s_tmem, &s_abort, info0, info1);
     if (tid == 0) {
         a.rec_info[(size_t)blockIdx.x * 2 + 0] = info0;
         a.rec_info[(size_t)blockIdx.x * 2 + 1] = info1;
@@ -2510,6 +2562,12 @@ static cudaError_t launch_shape(const AttnArgs& a, const AttnMaps& m, bool out_f
     if (a.rows <= kNarrowRows)
         return out_f32 ? launch_one<D, BS, true, kModeNarrow, KV8, BLK>(a, m, grid, stream)
                        : launch_one<D, BS, false, kModeNarrow, KV8, BLK>(a, m, grid, stream);
+    if (a.rows > 128) {  // the paired form: bf16 cache and output only (chosen by the host)
+        if constexpr (!KV8 && !BLK) {
+            if (!out_f32) return launch_one<D, BS, false, kModeTmem2, false, false>(a, m, grid, stream);
+        }
+        return cudaErrorInvalidValue;
+    }
     if (a.rows > kTmemMinRows)
         return out_f32 ? launch_one<D, BS, true, kModeTmem, KV8, BLK>(a, m, grid, stream)
                        : launch_one<D, BS, false, kModeTmem, KV8, BLK>(a, m, grid, stream);

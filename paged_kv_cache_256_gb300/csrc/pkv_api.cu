@@ -223,6 +223,7 @@ int check_shape(int num_seqs, int q_len, int n_q, int n_kv, int head_dim, int bl
 // Per-block scales (fetched with the tiles by LSU copies) leave these weights
 // as they are (8-bit GQA with block scales 100.4 us at 32, 104.3 at 24).
 int unit_cost_for(int rows, bool kv8) {
+    if (rows > 128) return 16;  // the paired tensor-memory form (bf16 only)
     if (rows <= 8) return kv8 ? 32 : 10;
     if (rows > 64) return kv8 ? 10 : 12;
     return kv8 ? 4 : 6;
@@ -235,6 +236,13 @@ int tile_rows(int n_q, int n_kv, int q_len) {
     const int rows_total = group * q_len;
     if (rows_total <= kTileRows) return rows_total;
     return group <= kTileRows ? (kTileRows / group) * group : kTileRows;
+}
+
+// Rows of the paired tensor-memory form: two tiles per unit when a KV head
+// has more than one tile of more than 64 rows; else the one-tile rows.
+int paired_rows(int n_q, int n_kv, int q_len) {
+    const int rows = tile_rows(n_q, n_kv, q_len);
+    return (rows > 64 && (n_q / n_kv) * q_len > rows) ? 2 * rows : rows;
 }
 
 // A tile as one TMA box of the query map (by heads x bz tokens): whole
@@ -269,6 +277,18 @@ WorkspaceLayout workspace_layout(int grid, int rows, int head_dim) {
 
 using namespace pkv;
 
+namespace pkv {
+size_t attn_workspace_min_bytes(int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
+                                int block_size, unsigned flags) {
+    if (check_shape(num_seqs, q_len, n_q, n_kv, head_dim, block_size) != PKV_OK) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int grid = attn_grid(flags, dev);
+    if (grid <= 0) return 0;
+    return workspace_layout(grid, tile_rows(n_q, n_kv, q_len), head_dim).total;
+}
+}  // namespace pkv
+
 extern "C" {
 
 int pkv_version(void) { return 10200; }
@@ -301,8 +321,10 @@ size_t pkv_paged_decode_attn_workspace_size(int num_seqs, int q_len, int n_q, in
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     const int grid = attn_grid(flags, dev);
     if (grid <= 0) return 0;
-    return workspace_layout(grid, tile_rows(n_q, n_kv, q_len), head_dim).total;
+    // sized for the larger tiling the call may choose (the paired form)
+    return workspace_layout(grid, paired_rows(n_q, n_kv, q_len), head_dim).total;
 }
+
 
 int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_tables, const int32_t* context_lens,
@@ -378,17 +400,30 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-    int grid = attn_grid(flags, dev);
-    if (grid <= 0) return PKV_ERR_CUDA;
-    const int rows = tile_rows(n_q, n_kv, q_len);
+    const int grid0 = attn_grid(flags, dev);
+    if (grid0 <= 0) return PKV_ERR_CUDA;
+    // Query rows per unit: one tile of at most 128 rows, or over a bf16 cache
+    // with bf16 output two such tiles (the paired tensor-memory form, which
+    // reads each stage once for both) when the workspace holds their records.
     const int q_rows_total = (n_q / n_kv) * q_len;
-    const int q_tiles = (q_rows_total + rows - 1) / rows;
-    // No more CTAs than (unit, block) items the call can have.
-    if (((flags >> PKV_FLAG_GRID_SHIFT) & 0xFFFFu) == 0) {
-        const long long items = (long long)num_seqs * n_kv * q_tiles * max_blocks_per_seq;
-        if (items < grid) grid = (int)items;
+    const int rows1 = tile_rows(n_q, n_kv, q_len);
+    const int rows2 = paired_rows(n_q, n_kv, q_len);
+    const bool pair_ok = rows2 > rows1 && !kv8 && out_dtype == PKV_OUT_BF16 &&
+                         !(flags & PKV_FLAG_ONE_TILE);
+    int rows = rows1, q_tiles = 1, grid = grid0;
+    WorkspaceLayout L;
+    for (int attempt = pair_ok ? 0 : 1; attempt < 2; ++attempt) {
+        rows = attempt == 0 ? rows2 : rows1;
+        q_tiles = (q_rows_total + rows - 1) / rows;
+        grid = grid0;
+        // No more CTAs than (unit, block) items the call can have.
+        if (((flags >> PKV_FLAG_GRID_SHIFT) & 0xFFFFu) == 0) {
+            const long long items = (long long)num_seqs * n_kv * q_tiles * max_blocks_per_seq;
+            if (items < grid) grid = (int)items;
+        }
+        L = workspace_layout(grid, rows, head_dim);
+        if (workspace && workspace_bytes >= L.total) break;
     }
-    const WorkspaceLayout L = workspace_layout(grid, rows, head_dim);
     if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
 

@@ -56,6 +56,12 @@ struct AttnArgs {
 // The tensor maps of one attention launch: the K and V cache views and the
 // query tiles (tensor-memory consumer).  With AttnArgs::tile_3d the V view is
 // three-dimensional: {64 columns, rows, 2 column halves}.
+// Workspace bytes of an attention call in its one-tile form (the least any
+// call of these sizes needs; pkv_paged_decode_attn_workspace_size reports
+// the paired form's, which some calls use).  0 for invalid shapes.
+size_t attn_workspace_min_bytes(int num_seqs, int q_len, int n_q, int n_kv, int head_dim,
+                                int block_size, unsigned flags);
+
 struct AttnMaps {
     CUtensorMap k, v, q;
 };

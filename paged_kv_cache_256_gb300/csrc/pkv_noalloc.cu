@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "../../include/pkv.h"
+#include "pkv_internal.h"
 
 namespace {
 
@@ -57,8 +58,10 @@ extern "C" int pkv_paged_decode_attn_noalloc(
     // drop its reports, and refuse the test-only stall flag, whose only effect
     // here would be an invalid output with PKV_OK.
     if (flags & (PKV_FLAG_CHECKED | PKV_FLAG_TEST_STALL)) return PKV_ERR_UNSUPPORTED;
-    const size_t need = pkv_paged_decode_attn_workspace_size(num_seqs, q_len, n_q, n_kv,
-                                                             head_dim, block_size, 0, flags);
+    // The one-tile form's need: a call whose paired form does not fit the
+    // scratch runs in the one-tile form.
+    const size_t need = pkv::attn_workspace_min_bytes(num_seqs, q_len, n_q, n_kv, head_dim,
+                                                      block_size, flags);
     if (need == 0 || num_seqs == 0) {
         // Invalid shapes (or an empty batch): the regular entry point gives the
         // precise status and launches nothing.

@@ -3,7 +3,9 @@
 A call with many new tokens per sequence -- a whole prompt (q_len = ctx) or a
 chunk of one appended to a cached prefix (q_len < ctx) -- has more than 128
 query rows per KV head; they are processed in row tiles of 128, each tile
-reading only the blocks its causal (and window) limits allow.  Covered:
+reading only the blocks its causal (and window) limits allow; over a bf16
+cache with bf16 output two such tiles share each stage (256-row units),
+unless PKV_FLAG_ONE_TILE or a smaller workspace keeps one.  Covered:
 several tiles with a partial last one, every group size (MHA, GQA, MQA),
 rows that see no key (ctx < q_len), windows, split units (forced CTA
 counts), bf16 and fp32 output, bf16 and e4m3 caches, and the named
@@ -75,9 +77,12 @@ def test_prefill_parity(oracle, case, grid):
         ref = oracle.paged_attn(wl.q, kc, vc, wl.block_tables, wl.context_lens, n_q=wl.n_q,
                                 n_kv=wl.n_kv, head_dim=wl.head_dim, block_size=wl.block_size,
                                 scale=wl.scale, window=window)
-        for kind in ("bf16", "f32"):
-            out = _run_ex(dw, wl, kind, flags, window)
-            assert_close(out_to_host(out), ref, kind, f"{case} grid {grid} W {window} {kind}")
+        # bf16 output over a bf16 cache takes two 128-row tiles per unit (the
+        # paired form) where a KV head has more; PKV_FLAG_ONE_TILE keeps one.
+        for kind, extra in (("bf16", 0), ("bf16", pkv.PKV_FLAG_ONE_TILE), ("f32", 0)):
+            out = _run_ex(dw, wl, kind, flags | extra, window)
+            assert_close(out_to_host(out), ref, kind,
+                         f"{case} grid {grid} W {window} {kind} one_tile={bool(extra)}")
 
 
 @pytest.mark.parametrize("case", FP8_CASES, ids=lambda c: "d{}_bs{}_q{}_kv{}_ql{}".format(*c[:5]))

@@ -80,6 +80,31 @@ def test_noalloc_many_ctas_then_few(oracle, n_q, n_kv, q_len):
             assert_close(out_to_host(out), ref, kind, f"noalloc grid {grid} {kind}")
 
 
+def test_noalloc_prefill_keeps_one_tile_when_the_paired_form_does_not_fit(oracle):
+    """The named chunked prefill's paired form (two 128-row tiles per unit over a
+    bf16 cache, bf16 output) needs ~40 MB of split records at one CTA per SM,
+    more than the fixed scratch: the call keeps one tile per unit, bit-identical
+    to the regular call with PKV_FLAG_ONE_TILE and within tolerance of the oracle."""
+    lib = _lib.load_library()
+    wl = make_workload("llama3_8b_chunked_prefill")
+    dw = to_device(wl)
+    pkv.pkv_kv_append(dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache)
+    _, _, ref = oracle_after_append(oracle, wl)
+    one = torch.empty(tuple(dw.q.shape), dtype=torch.bfloat16, device="cuda")
+    flags = pkv.PKV_FLAG_ONE_TILE
+    ws = pkv.alloc_workspace(wl.num_seqs, wl.q_len, wl.n_q, wl.n_kv, wl.head_dim, wl.block_size,
+                             flags=flags)
+    pkv.pkv_paged_decode_attn(dw.q, dw.k_cache, dw.v_cache, dw.block_tables, dw.context_lens,
+                              wl.scale, one, ws, flags=flags)
+    assert pkv.pkv_check_error(ws) == pkv.PKV_OK
+    got = torch.full(tuple(dw.q.shape), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = _call_noalloc(lib, wl, dw, got)
+    assert st == pkv.PKV_OK, _lib.status_name(st)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), one.view(torch.int16))
+    assert_close(out_to_host(got), ref, "bf16", "noalloc chunked prefill")
+
+
 def test_noalloc_rejects_what_it_cannot_serve():
     lib = _lib.load_library()
     wl = make_workload("tiny")
