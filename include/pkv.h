@@ -83,9 +83,10 @@ typedef enum pkv_status {
  * is then its scale tensor, copied with the blocks (needs PKV_FLAG_KV_FP8). */
 #define PKV_FLAG_KV_BLOCK_SCALES 0x10u
 /* Attention calls on a bf16 cache with head_dim 128 and more than 64 query
- * rows per KV head: fetch each V tile as two 64-column copies, the form used
- * when the driver declines the one-copy (three-dimensional) view of the V
- * cache.  Results are bit-identical either way; tests use it to run both. */
+ * rows per KV head: fetch each K and V tile as two 64-column copies, the
+ * form used when the driver declines the one-copy (four-dimensional) views
+ * of the caches.  Results are bit-identical either way; tests use it to run
+ * both. */
 #define PKV_FLAG_TILE_2D 0x20u
 /* Attention calls: keep one tile of at most 128 query rows per unit even
  * where two would be taken together (the paired form: bf16 cache, bf16

@@ -122,8 +122,9 @@ struct AttnCfg {
     // stage is laid out as [K box 0][K box 1 (d 128)][V box 0][V box 1], each
     // region holding the stage's blocks one after another (kRegion bytes), so
     // the rows of all its blocks are contiguous within each 64-column region.
-    // (TMEM consumer, bf16 at d 128, V by 3-D copies: the V half of the stage
-    // is [block][half][rows] instead, one copy per block.)
+    // (TMEM consumer, bf16 at d 128, through the grouped 4-D views: each half
+    // of the stage is [block][8-row group][half][8 rows][128 bytes] instead,
+    // one copy per block for K and one for V.)
     static constexpr int kBlocksPerStage =
         kTmem ? 64 / BS : (2 * kTileBytes >= 8192 ? 1 : 8192 / (2 * kTileBytes));
     static constexpr int kRegion = kBlocksPerStage * kBoxBytes;
@@ -592,11 +593,12 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
             }
             if (*s_abort) ok = false;  // a consumer gave up
             if constexpr (ORDERED) {
-                // boxes per block: K and V halves (bf16; V in one box through
-                // the 3-D view), or one K+V box (8-bit)
+                // boxes per block: K and V halves (bf16), one K and one V box
+                // through the grouped 4-D views (bf16, d 128), or one K+V box
+                // (8-bit)
                 static_assert(SBS * (KV8 ? 1 : 2 * kBoxes) <= 32, "one box per lane");
-                const bool v3 = !KV8 && kBoxes == 2 && a.tile_3d;
-                const int bpb = KV8 ? 1 : (v3 ? kBoxes + 1 : 2 * kBoxes);
+                const bool g4 = !KV8 && kBoxes == 2 && a.tile_4d;
+                const int bpb = KV8 ? 1 : (g4 ? 2 : 2 * kBoxes);
                 for (int k = 0; k < ns && ok; ++k) {
                     const int nb = min(SBS, n - k * SBS);
                     const int blk = __shfl_sync(0xffffffffu, my, (k * SBS + lane / bpb) & 31);
@@ -637,13 +639,16 @@ __device__ __forceinline__ void produce(const AttnArgs& a, const CUtensorMap* tm
                         if constexpr (KV8) {
                             tma_load_2d(stages + stage * kStageBytes + b * 2 * kBoxBytes, tmap_k,
                                         0, yk, &full_bar[stage], policy);
-                        } else if (v3 && box == kBoxes) {
-                            // block b's V tile, both halves: [half 0 rows][half 1 rows] at
-                            // b * 2 * kBoxBytes of the stage's V region
-                            tma_load_3d_hint(stages + stage * kStageBytes + kBoxes * kRegion +
-                                                 b * 2 * kBoxBytes,
-                                             tmap_v, 0, oob ? a.tile_rows_total : yk + a.v_row_off,
-                                             0, &full_bar[stage], policy);
+                        } else if (g4) {
+                            // block b's K (box 0) or V (box 1) tile in one copy, as
+                            // [8-row group][half][8 rows][128 bytes] at b * 2 * kBoxBytes
+                            // of the stage's K or V region
+                            const bool isv = box == 1;
+                            const int y = isv && !oob ? yk + a.v_row_off : yk;
+                            tma_load_4d_hint(stages + stage * kStageBytes +
+                                                 (isv ? kBoxes * kRegion : 0) + b * 2 * kBoxBytes,
+                                             isv ? tmap_v : tmap_k, 0, 0, 0, y >> 3,
+                                             &full_bar[stage], policy);
                         } else {
                             // box: K half (box < kBoxes), then V half
                             const int half = box % kBoxes;
@@ -1740,8 +1745,10 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     const uint32_t idesc_qk = KV8 ? umma_idesc_f16(128, kKeys, false) : umma_idesc_bf16(128, kKeys, false);
     const uint32_t idesc_pv = KV8 ? umma_idesc_f16(128, D, true) : umma_idesc_bf16(128, D, true);
     const uint32_t q_saddr = smem_addr(qtile);
-    // bf16 V tiles by one 3-D copy each: a stage's V region is [block][half][rows]
-    const bool v3 = !KV8 && C::kBoxes == 2 && a.tile_3d;
+    // bf16 tiles at d 128 by one 4-D copy each: a stage's K and V regions are
+    // [block][8-row group][half][8 rows][128 bytes] (uniform 2048-byte stride
+    // between 8-row groups, halves 1024 bytes apart)
+    const bool g4 = !KV8 && C::kBoxes == 2 && a.tile_4d;
 
     auto issuer_fail = [&](bool& ok) {
         ok = false;
@@ -1863,8 +1870,10 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                             const uint64_t ad = umma_smem_desc(
                                 q_saddr + (kk >> 2) * kQHalf + u * 128 * 128 + (kk & 3) * 32, 16,
                                 1024);
-                            const uint64_t bd = umma_smem_desc(
-                                kb + (kk >> 2) * kKRegion + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd =
+                                g4 ? umma_smem_desc(kb + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048)
+                                   : umma_smem_desc(kb + (kk >> 2) * kKRegion + (kk & 3) * 32, 16,
+                                                    1024);
                             umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
                         }
                         umma_commit(&s_full[slot]);
@@ -1899,10 +1908,12 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                     const uint32_t vb =
                         KV8 ? smem_addr(cvt + (g % kCopies) * kCopy) + kHalves * C::kCvtRegion
                             : smem_addr(stages + st * C::kStageBytes) + C::kBoxes * C::kRegion;
-                    // The V rows of 16 keys and the distance to their second
-                    // 64-column half: halves of all the stage's blocks apart
-                    // (2-D copies), or each block's two halves together (3-D).
-                    const uint32_t vlbo = KV8 ? C::kCvtRegion : (v3 ? C::kBoxBytes : C::kRegion);
+                    // The V rows of 16 keys, the distance to their second
+                    // 64-column half and between their 8-row groups: halves of
+                    // all the stage's blocks apart (2-D copies), or the grouped
+                    // 4-D layout's 1024 and 2048 bytes.
+                    const uint32_t vlbo = KV8 ? C::kCvtRegion : (g4 ? 1024u : C::kRegion);
+                    const uint32_t vsbo = g4 ? 2048u : 1024u;
                     const uint32_t pcol = (g & 1u) * (kKeys / 2);
 #pragma unroll
                     for (int u = 0; u < T2; ++u) {
@@ -1918,11 +1929,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         const uint32_t ocol = tbase + kColO + u * 128;
                         const uint32_t pc = tbase + kColP + u * kKeys + pcol;
                         for (int kk = 0; kk < nk16; ++kk) {
-                            const uint32_t vrow =
-                                v3 ? (kk / (BS / 16)) * 2 * C::kBoxBytes +
-                                         (kk % (BS / 16)) * 16 * 128
-                                   : kk * 16 * 128;
-                            const uint64_t bd = umma_smem_desc(vb + vrow, vlbo, 1024);
+                            const uint32_t vrow = g4 ? kk * 4096 : kk * 16 * 128;
+                            const uint64_t bd = umma_smem_desc(vb + vrow, vlbo, vsbo);
                             umma_ts(ocol, pc + kk * 8, bd, idesc_pv, (q > 0 || kk > 0) ? 1u : 0u);
                             if (OUT_F32)
                                 umma_ts(ocol, tbase + kColPL + pcol + kk * 8, bd, idesc_pv, 1u);
@@ -2224,13 +2232,15 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 if (!KV8 && sub == 0 && tokl + BS > ctx) {  // (the f16 copies come zeroed there)
                     uint8_t* vt = stages + (sq % kStages) * C::kStageBytes +
                                   C::kBoxes * C::kRegion +
-                                  (nb - 1) * (v3 ? 2 * C::kBoxBytes : C::kBoxBytes);
-                    const int hstride = v3 ? C::kBoxBytes : C::kRegion;  // to the second half
+                                  (nb - 1) * (g4 ? 2 * C::kBoxBytes : C::kBoxBytes);
                     const int valid = ctx - tokl;  // >= 1: the block holds a resident token
                     const int chunks = (BS - valid) * 8;  // 16-byte chunks per 64-column half
                     for (int qq = row; qq < chunks * (D / 64); qq += 128) {
                         const int half = qq / chunks, rq = qq % chunks;
-                        *reinterpret_cast<uint4*>(vt + half * hstride + valid * 128 + rq * 16) =
+                        const int r = valid + (rq >> 3);  // the row, and its chunk rq & 7
+                        const int off = g4 ? (r >> 3) * 2048 + half * 1024 + (r & 7) * 128
+                                           : half * C::kRegion + r * 128;
+                        *reinterpret_cast<uint4*>(vt + off + (rq & 7) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();

@@ -70,21 +70,25 @@ bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, long long 
     return r == CUDA_SUCCESS;
 }
 
-// 3-D view of a bf16 cache with head_dim 128: {64 columns, rows, 2 column
-// halves}, the halves 128 bytes apart, so one box of 64 x block_size x 2
-// brings a whole (block, KV head) tile as its two 128-byte-swizzled half
-// tiles one after the other -- one copy where the 2-D view needs two.  The
-// strides are not in increasing order (the half stride lies inside a row); a
-// driver that declines such a view returns an error and the caller keeps the
-// 2-D view.
-bool make_cache_map_3d(CUtensorMap* map, const void* base, long long rows, int block_size) {
+// Grouped 4-D view of a bf16 cache with head_dim 128 for the tensor-memory
+// consumer: {64 columns, 8 rows, 2 column halves, row groups of 8}, strides
+// 256 (row), 128 (half) and 2048 (group) bytes.  One box of 64 x 8 x 2 x
+// block_size/8 brings a whole (block, KV head) tile and lands it as
+// [8-row group][half][8 rows][128 bytes], 128-byte swizzled: the 8-row groups
+// of consecutive blocks then lie at one stride (2048 bytes) and the halves
+// 1024 bytes apart, the K-major layout the N = 64 score product and the
+// MN-major layout the PV product read -- one copy per tile where the 2-D view
+// needs two.  The strides are not in increasing order (the half stride lies
+// inside a row); a driver that declines such a view returns an error and the
+// caller keeps the 2-D view.  rows is a multiple of 8 (block_size is).
+bool make_cache_map_4d(CUtensorMap* map, const void* base, long long rows, int block_size) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {64u, (cuuint64_t)rows, 2u};
-    cuuint64_t strides[2] = {256u, 128u};
-    cuuint32_t box[3] = {64u, (cuuint32_t)block_size, 2u};
-    cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+    cuuint64_t dims[4] = {64u, 8u, 2u, (cuuint64_t)(rows / 8)};
+    cuuint64_t strides[3] = {256u, 128u, 2048u};
+    cuuint32_t box[4] = {64u, 8u, 2u, (cuuint32_t)(block_size / 8)};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -97,7 +101,7 @@ struct MapKey {
     const void* base;
     long long rows;
     int head_dim, block_size;
-    bool kv8, three_d;
+    bool kv8, grouped;
 };
 struct MapEntry {
     MapKey key;
@@ -110,20 +114,20 @@ MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 
 bool cached_cache_map(CUtensorMap* map, const void* base, int head_dim, long long rows,
-                      int block_size, bool kv8, bool three_d = false) {
+                      int block_size, bool kv8, bool grouped = false) {
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (const MapEntry& e : g_maps)
         if (e.used && e.key.base == base && e.key.rows == rows && e.key.head_dim == head_dim &&
-            e.key.block_size == block_size && e.key.kv8 == kv8 && e.key.three_d == three_d) {
+            e.key.block_size == block_size && e.key.kv8 == kv8 && e.key.grouped == grouped) {
             *map = e.map;
             return true;
         }
-    if (three_d ? !make_cache_map_3d(map, base, rows, block_size)
+    if (grouped ? !make_cache_map_4d(map, base, rows, block_size)
                 : !make_cache_map(map, base, head_dim, rows, block_size, kv8))
         return false;
     MapEntry& e = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % kMapCache;
-    e.key = MapKey{base, rows, head_dim, block_size, kv8, three_d};
+    e.key = MapKey{base, rows, head_dim, block_size, kv8, grouped};
     e.map = *map;
     e.used = true;
     return true;
@@ -429,16 +433,18 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
 
     AttnMaps maps;
     std::memset(&maps, 0, sizeof maps);
-    if (!cached_cache_map(&maps.k, k_cache, head_dim, rows_total, block_size, kv8))
-        return PKV_ERR_CUDA;
-    // The tensor-memory consumer over a bf16 head_dim-128 cache takes each V
-    // tile in one copy through the 3-D view where the driver accepts it.
-    int tile_3d = 0;
+    // The tensor-memory consumer over a bf16 head_dim-128 cache takes each K
+    // and V tile in one copy through the grouped 4-D views where the driver
+    // accepts them; everything else reads through the 2-D views.
+    int tile_4d = 0;
     if (!kv8 && head_dim == 128 && rows > 64 && !(flags & PKV_FLAG_TILE_2D) &&
+        cached_cache_map(&maps.k, k_cache, head_dim, rows_total, block_size, false, true) &&
         cached_cache_map(&maps.v, v_cache, head_dim, rows_total, block_size, false, true))
-        tile_3d = 1;
-    if (!tile_3d &&
-        !cached_cache_map(&maps.v, kv8 ? k_cache : v_cache, head_dim, rows_total, block_size, kv8))
+        tile_4d = 1;
+    if (!tile_4d &&
+        (!cached_cache_map(&maps.k, k_cache, head_dim, rows_total, block_size, kv8) ||
+         !cached_cache_map(&maps.v, kv8 ? k_cache : v_cache, head_dim, rows_total, block_size,
+                           kv8)))
         return PKV_ERR_CUDA;
     // The tensor-memory consumer (more than 64 rows) takes its query tiles by
     // TMA when a tile is one box; otherwise its threads load them.
@@ -485,7 +491,7 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     a.scale_log2 = scale * 1.4426950408889634f;
     a.q_tma = q_tma;
     a.early_start = (flags & PKV_FLAG_NO_EARLY_START) ? 0 : 1;
-    a.tile_3d = tile_3d;
+    a.tile_4d = tile_4d;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool f32 = out_dtype == PKV_OUT_F32;

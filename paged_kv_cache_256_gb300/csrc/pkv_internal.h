@@ -50,12 +50,12 @@ struct AttnArgs {
     int q_tma;         // tensor-memory consumer: query tiles arrive by TMA (the q map is valid)
     int early_start;   // launched as a programmatic dependent of the previous kernel
     const float* kv_scales;  // per-(block, KV head) scales [num_blocks][n_kv][4], or null
-    int tile_3d;  // the V map is a 3-D view: a V tile's two 64-column halves in one copy
+    int tile_4d;  // the K and V maps are grouped 4-D views: a whole tile in one copy
 };
 
 // The tensor maps of one attention launch: the K and V cache views and the
-// query tiles (tensor-memory consumer).  With AttnArgs::tile_3d the V view is
-// three-dimensional: {64 columns, rows, 2 column halves}.
+// query tiles (tensor-memory consumer).  With AttnArgs::tile_4d the K and V
+// views are four-dimensional: {64 columns, 8 rows, 2 column halves, row groups}.
 // Workspace bytes of an attention call in its one-tile form (the least any
 // call of these sizes needs; pkv_paged_decode_attn_workspace_size reports
 // the paired form's, which some calls use).  0 for invalid shapes.

@@ -56,10 +56,11 @@ def test_split_points_do_not_change_the_result(named, grid):
 
 
 @pytest.mark.parametrize("kind", ["bf16", "f32"])
-def test_one_and_two_copy_v_tiles_agree_bit_for_bit(named, kind):
-    """With more than 64 rows per KV head a bf16 head_dim-128 V tile arrives by
-    one 3-D copy, or by two 64-column copies under PKV_FLAG_TILE_2D; the
-    products read the same values, so the outputs match bit for bit."""
+def test_one_and_two_copy_tiles_agree_bit_for_bit(named, kind):
+    """With more than 64 rows per KV head a bf16 head_dim-128 K or V tile arrives
+    by one copy through a grouped 4-D view, or by two 64-column copies under
+    PKV_FLAG_TILE_2D; the products read the same values, so the outputs match
+    bit for bit."""
     wl, dw, _, _, _ = named
     a = run_attn(dw, wl, kind)
     b = run_attn(dw, wl, kind, flags=pkv.PKV_FLAG_TILE_2D)
