@@ -147,8 +147,14 @@ struct AttnCfg {
     static constexpr int kTileStride = D + 4;
     static constexpr int kEmitBytes =
         MODE == kModeNarrow ? (kNarrowRows * kTileStride + 2 * kNarrowRows) * 4 : 0;
-    // TMEM mode: the unit's 128 query rows as a swizzled K-major tile.
-    static constexpr int kQTileBytes = kTmem ? kQRows * D * 2 : 0;
+    // TMEM mode over bf16: the unit's 128 (paired: 256) query rows as a
+    // swizzled K-major tile, fetched by TMA while the piece before it ends.
+    // Over an 8-bit cache the query rows live in tensor memory instead, which
+    // leaves the 32 KB to the ring: eight 64-key stages instead of six
+    // (measured: MQA verify 51.7 -> 49.7 us, with block scales 62.7 -> 55.8,
+    // chunked prefill 125.4 -> 117.3).  Over bf16 the extra stage did not pay
+    // for the later query rows (MQA verify 40.2 -> 41.5 us).
+    static constexpr int kQTileBytes = (kTmem && !KV8) ? kQRows * D * 2 : 0;
     // TMEM mode over an 8-bit cache: kCvtCopies f16 copies of a 64-key stage
     // (K and V, each 64 rows in D/64 swizzled 64-column regions).  A copy is
     // held from its conversion until its PV product completes; with two, the
@@ -1699,6 +1705,12 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     // halves of P from kColPL (one-tile form only)
     constexpr uint32_t kColO = 0, kColS = T2 == 2 ? 256 : 128, kColP = T2 == 2 ? 384 : 256,
                        kColPL = 320;
+    // Over an 8-bit cache the query rows are the score product's A operand in
+    // tensor memory, columns kColQ .. kColQ + D/2 (two f16 per column, the
+    // lower index in the low half), each softmax thread storing its own row;
+    // over bf16 the products read a query tile in shared memory.
+    constexpr bool kQT = KV8;
+    constexpr uint32_t kColQ = 384;
     constexpr int KT = D / 16;   // k steps of S = Q K^T
     constexpr int kQHalf = C::kQRows * 128;  // bytes of one 64-column half of the Q tile
     // warps 0..5 take part (paired: 0..7, 9, 10), and the converter warps 6, 7,
@@ -1708,8 +1720,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     constexpr int kHalves = D / 64;          // 64-column regions of an f16 K or V copy
     // tcb: [0..1] S ready, [2..3] S read (per score slot), [4..7] P ready, [8..11] PV done
     //      (per sub-tile u and P buffer b: 2u + b), [12] QK teardown, [13] PV teardown,
-    //      [14..16] f16 copy ready, [17..19] f16 copy read, [20] Q landed, [21] Q read,
-    //      [22] Q widened
+    //      [14..16] f16 copy ready, [17..19] f16 copy read, [20] Q landed (TMA) or
+    //      stored (tensor memory), [21] Q read
     uint64_t* s_full = tcb;
     uint64_t* s_free = tcb + 2;
     uint64_t* p_full = tcb + 4;
@@ -1717,9 +1729,8 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
     constexpr uint32_t kCopies = C::kCvtCopies;
     uint64_t* cvt_full = tcb + 14;  // 8-bit cache: f16 copy [g % kCopies] ready
     uint64_t* cvt_free = tcb + 17;  // 8-bit cache: f16 copy [g % kCopies] read by its PV product
-    uint64_t* q_full = tcb + 20;    // query tile landed (TMA)
+    uint64_t* q_full = tcb + 20;    // query tile landed (TMA), or stored into tensor memory
     uint64_t* q_empty = tcb + 21;   // the piece's score products have read the query tile
-    uint64_t* q_conv = tcb + 22;    // 8-bit cache: the query tile widened to f16
     // Score slot of stage g for sub-tile u, and the parity of its g-th use.
     auto sslot = [](uint32_t g, int u) -> uint32_t { return T2 == 2 ? (uint32_t)u : (g & 1u); };
     auto spar = [](uint32_t g) -> uint32_t { return T2 == 2 ? (g & 1u) : ((g >> 1) & 1u); };
@@ -1755,6 +1766,42 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
         atomicOr(a.err, kErrTimeout);
         *s_abort = 1;
     };
+    // 8-bit cache: this thread's query row of the unit at walk position wq,
+    // or null for a row outside the unit.
+    auto q_row_src = [&](const Walk& wq) -> const uint4* {
+        int iq = 0, hq = 0;
+        if (!unit_row(a, wq.t, wq.h, trow, iq, hq)) return nullptr;
+        return reinterpret_cast<const uint4*>(a.q + (((size_t)wq.s * a.q_len + iq) * a.n_q + hq) * D);
+    };
+    // ... as raw bf16 pairs (zeros outside the unit): tensor-memory columns
+    // 0..31 of the row in q0, 32..63 (head_dim 128) in q1.
+    auto q_rows_load = [&](const Walk& wq, uint32_t (&q0)[32], uint32_t (&q1)[32]) {
+        const uint4* src = q_row_src(wq);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            const uint4 v = src ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            if (c < 8) {
+                q0[4 * c] = v.x, q0[4 * c + 1] = v.y, q0[4 * c + 2] = v.z, q0[4 * c + 3] = v.w;
+            } else {
+                q1[4 * c - 32] = v.x, q1[4 * c - 31] = v.y, q1[4 * c - 30] = v.z,
+                q1[4 * c - 29] = v.w;
+            }
+        }
+    };
+    // ... widened to f16 (the f16 products take f16 on both sides), stored
+    // as the thread's lane of the A operand, and announced to the score issuer.
+    auto q_rows_store = [&](uint32_t (&q0)[32], uint32_t (&q1)[32]) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            q0[j] = bf16x2_to_f16x2(q0[j]);
+            if (D == 128) q1[j] = bf16x2_to_f16x2(q1[j]);
+        }
+        tmem_st32(tlane + kColQ, q0);
+        if constexpr (D == 128) tmem_st32(tlane + kColQ + 32, q1);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(q_full);
+    };
 
     uint32_t gbase = 0;  // sequence number (in this CTA) of the piece's first stage
     bool ok = true;
@@ -1774,27 +1821,24 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
             lim = row_ok ? ctx - a.q_len + i_row : -1;
             if (a.window > 0) lo = lim - a.window + 1;
         }
-        if (softmax && a.q_tma) {
-            if constexpr (KV8) {
-                // The TMA tile is bf16; the f16 MMAs want f16: each thread widens
-                // its own row in place.  Every thread arrives, so the issuer's
-                // wait ends (and reports) even after a timeout here.
-                const bool good = consumer_wait(a, q_full, piece & 1, ok, s_abort);
-                if (good) {
-#pragma unroll
-                    for (int c = 0; c < D / 8; ++c) {
-                        uint4* pq = reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + trow * 128 +
-                                                             (((c & 7) ^ (trow & 7)) << 4));
-                        const uint4 v = *pq;
-                        *pq = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
-                                         bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-                    }
-                    fence_proxy_async_smem();
+        if constexpr (kQT) {
+            // The first piece's query rows; each later piece's are stored by
+            // the piece before it, ahead of its output, from the L2, where
+            // they are fetched now.
+            if (softmax) {
+                if (piece == 0) {
+                    uint32_t q0[32], q1[32];
+                    q_rows_load(w, q0, q1);
+                    q_rows_store(q0, q1);
                 }
-                ok = good;
-                mbar_arrive(q_conv);
+                Walk wn = w;
+                wn.left -= j1 - w.j;
+                if (wn.left > 0) {
+                    walk_next_unit<BS>(a, wn);
+                    if (const uint4* src = q_row_src(wn)) prefetch_l2_bulk(src, D * 2);
+                }
             }
-        } else if (softmax) {
+        } else if (softmax && !a.q_tma) {
             // This unit's query rows into the swizzled Q tile (the previous
             // unit's score products finished: each of them was waited for).
             const bool valid = row_ok;
@@ -1802,40 +1846,33 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 a.q + (((size_t)s * a.q_len + i_row) * a.n_q + hq_row) * D);
             uint4 qv[D / 8];
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                qv[c] = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-                if constexpr (KV8)  // f16 operands: Q as f16 too
-                    qv[c] = make_uint4(bf16x2_to_f16x2(qv[c].x), bf16x2_to_f16x2(qv[c].y),
-                                       bf16x2_to_f16x2(qv[c].z), bf16x2_to_f16x2(qv[c].w));
-            }
+            for (int c = 0; c < D / 8; ++c) qv[c] = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int c = 0; c < D / 8; ++c)
                 *reinterpret_cast<uint4*>(qtile + (c >> 3) * kQHalf + trow * 128 +
                                           (((c & 7) ^ (trow & 7)) << 4)) = qv[c];
             fence_proxy_async_smem();
         }
-        if (!a.q_tma) {
+        if (!kQT && !a.q_tma) {
             tc_fence_before();
             named_barrier_sync(2, kParty);  // Q tile ready; the previous unit's O has been read
             tc_fence_after();
         }
-        // (With TMA query tiles the roles need no barrier per piece: the issuer
-        // waits for the tile, and the first PV product of a piece, which
-        // overwrites O, waits for P of its first super-block, which the
-        // softmax threads write only after reading the previous O.)
+        // (With TMA query tiles, or query rows in tensor memory, the roles need
+        // no barrier per piece: the issuer waits for the rows, and the first PV
+        // product of a piece, which overwrites O, waits for P of its first
+        // super-block, which the softmax threads write only after reading the
+        // previous O.)
 
         if (warp == kQKWarp) {
             // ===================== QK issuer =====================
-            if (lane == 0 && ok && a.q_tma) {
-                // This piece's query tile: landed, and over an 8-bit cache
-                // widened (the copy is waited for itself, so that a tile still
-                // in flight after a failed widening is waited for at teardown).
-                if (*s_abort || !mbar_wait_bounded(q_full, piece & 1)) {
+            if (lane == 0 && ok && (kQT || a.q_tma)) {
+                // This piece's query rows: stored into tensor memory by the
+                // softmax threads, or the tile landed in shared memory.
+                if (*s_abort || !mbar_wait_bounded(q_full, piece & 1))
                     issuer_fail(ok);
-                } else {
+                else
                     q_pending = false;
-                    if (KV8 && !mbar_wait_bounded(q_conv, piece & 1)) issuer_fail(ok);
-                }
                 tc_fence_after();
             }
             if (lane == 0 && ok) {
@@ -1867,20 +1904,25 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                         const uint32_t scol = tbase + kColS + slot * kKeys;
 #pragma unroll
                         for (int kk = 0; kk < KT; ++kk) {
-                            const uint64_t ad = umma_smem_desc(
-                                q_saddr + (kk >> 2) * kQHalf + u * 128 * 128 + (kk & 3) * 32, 16,
-                                1024);
                             const uint64_t bd =
                                 g4 ? umma_smem_desc(kb + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048)
                                    : umma_smem_desc(kb + (kk >> 2) * kKRegion + (kk & 3) * 32, 16,
                                                     1024);
-                            umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                            if constexpr (kQT) {
+                                // 16 query columns = 8 tensor-memory columns per k step
+                                umma_ts(scol, tbase + kColQ + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                            } else {
+                                const uint64_t ad = umma_smem_desc(
+                                    q_saddr + (kk >> 2) * kQHalf + u * 128 * 128 + (kk & 3) * 32, 16,
+                                    1024);
+                                umma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                            }
                         }
                         umma_commit(&s_full[slot]);
                     }
                 }
             }
-            if (lane == 0 && ok && a.q_tma) {
+            if (lane == 0 && ok && !kQT && a.q_tma) {
                 // The next piece's query tile, once this piece's score
                 // products have read this one.
                 Walk wn = w;
@@ -2249,6 +2291,21 @@ __device__ __forceinline__ void consume_tmem(const AttnArgs& a, Walk w, uint8_t*
                 mbar_arrive(&p_full[2 * sub + (sq & 1u)]);
             }
 
+            if constexpr (kQT) {
+                // The next piece's query rows, before this piece's output, so
+                // that its score products overlap the output's stores.  They
+                // may be overwritten now: this piece's last S was read above,
+                // so every score product that read them has completed.
+                Walk wn = w;
+                wn.left -= j1 - w.j;
+                if (wn.left > 0) {
+                    walk_next_unit<BS>(a, wn);
+                    uint32_t q0[32], q1[32];
+                    q_rows_load(wn, q0, q1);
+                    q_rows_store(q0, q1);
+                }
+            }
+
             // ---- epilogue: the last PV, then O out of TMEM row by row
             if (nsb > 0) {
                 const uint32_t sl = gbase + nsb - 1;
@@ -2410,8 +2467,8 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
     __shared__ int s_abort;
     // TMEM modes: S ready/read (x2 each), P ready, PV done (x4 each), 2
     // teardowns, over an 8-bit cache f16 copy ready / free (x3 each), query
-    // tile landed / read / widened
-    __shared__ uint64_t s_tcb[23];
+    // rows ready, query tile read
+    __shared__ uint64_t s_tcb[22];
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -2429,13 +2486,15 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
             // S ready (a commit), S read (128 rows), P ready (128 rows) and
             // PV done (a commit) per sub-tile and buffer, two issuer
             // teardowns (a commit each), f16
-            // copy ready (the converter warps) / free (a commit), query tile
-            // landed (the TMA) / read (a commit) / widened (128 rows)
+            // copy ready (the converter warps) / free (a commit), query rows
+            // stored in tensor memory (128 rows; 8-bit cache) or the query
+            // tile landed (the TMA; bf16), query tile read (a commit)
             const uint32_t cvt = KV8 ? (uint32_t)kTmemConverters : 1u;
-            const uint32_t counts[23] = {1,   1,   128, 128, 128, 128, 128, 128, 1, 1, 1, 1,
-                                         1,   1,   cvt, cvt, cvt, 1,   1,   1,   1, 1, 128};
+            const uint32_t qin = KV8 ? 128u : 1u;
+            const uint32_t counts[22] = {1,   1,   128, 128, 128, 128, 128, 128, 1,   1, 1,
+                                         1,   1,   1,   cvt, cvt, cvt, 1,   1,   1,   qin, 1};
             static_assert(C::kCvtCopies == 3, "barrier counts: three f16 copies");
-            for (int i = 0; i < 23; ++i) mbar_init(&s_tcb[i], counts[i]);
+            for (int i = 0; i < 22; ++i) mbar_init(&s_tcb[i], counts[i]);
         }
         fence_barrier_init();
         s_abort = 0;
@@ -2475,9 +2534,10 @@ __global__ void __launch_bounds__(threads_for(MODE, KV8), 1)
     // early; it waits for this whole grid before reading anything.
     if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // Tensor-memory consumer with TMA query tiles: the first tile is issued
-    // before the producer's first stage, so it is not queued behind the ring fill.
-    if constexpr (C::kTmem) {
+    // Tensor-memory consumer with TMA query tiles (bf16 cache): the first
+    // tile is issued before the producer's first stage, so it is not queued
+    // behind the ring fill.
+    if constexpr (C::kTmem && !KV8) {
         if (a.q_tma) {
             if (warp == (MODE == kModeTmem2 ? 9 : 4)) {  // the QK issuer
                 if (lane == 0 && w0.left > 0)

@@ -446,10 +446,12 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
          !cached_cache_map(&maps.v, kv8 ? k_cache : v_cache, head_dim, rows_total, block_size,
                            kv8)))
         return PKV_ERR_CUDA;
-    // The tensor-memory consumer (more than 64 rows) takes its query tiles by
-    // TMA when a tile is one box; otherwise its threads load them.
+    // The tensor-memory consumer (more than 64 rows) over a bf16 cache takes
+    // its query tiles by TMA when a tile is one box; otherwise its threads
+    // load them.  (Over an 8-bit cache its threads store their query rows,
+    // widened to f16, into tensor memory.)
     int q_tma = 0, by = 0, bz = 0;
-    if (rows > 64 && (long long)num_seqs * q_len < (1LL << 31) &&
+    if (rows > 64 && !kv8 && (long long)num_seqs * q_len < (1LL << 31) &&
         q_box(n_q / n_kv, rows, &by, &bz)) {
         if (!cached_q_map(&maps.q, q, head_dim, n_q, (long long)num_seqs * q_len, by, bz))
             return PKV_ERR_CUDA;

@@ -47,7 +47,7 @@ struct AttnArgs {
     int checked;
     int test_stall;    // failure-path tests: the producer issues nothing
     float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
-    int q_tma;         // tensor-memory consumer: query tiles arrive by TMA (the q map is valid)
+    int q_tma;         // tensor-memory consumer, bf16 cache: query tiles arrive by TMA (the q map is valid)
     int early_start;   // launched as a programmatic dependent of the previous kernel
     const float* kv_scales;  // per-(block, KV head) scales [num_blocks][n_kv][4], or null
     int tile_4d;  // the K and V maps are grouped 4-D views: a whole tile in one copy
