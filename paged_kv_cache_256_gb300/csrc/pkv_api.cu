@@ -222,14 +222,17 @@ int check_shape(int num_seqs, int q_len, int n_q, int n_kv, int head_dim, int bl
 // half the time while the unit's fixed work grows (Q widened to f16);
 // 8 < rows <= 64 with an 8-bit cache -- 4 (every row-slice warp widens each
 // tile, so blocks cost more); tensor-memory consumer -- 12 (the O read-out
-// per unit and the pipeline fill), 10 over an 8-bit cache (blocks cost more:
-// each is widened to f16).
+// per unit and the pipeline fill; MQA verify 41.5 / 41.5 / 41.9 us at 10 /
+// 12 / 16), 14 over an 8-bit cache, whose eight-stage ring streams blocks
+// faster than its units' fixed work (MQA verify 49.7 / 47.6 / 49.7 / 51.7 us
+// at 10 / 14 / 18 / 22, with block scales 55.8 / 53.8 / 55.8 / 57.8, chunked
+// prefill 117.2 / 113.3 / 109.0 / 111.1).
 // Per-block scales (fetched with the tiles by LSU copies) leave these weights
 // as they are (8-bit GQA with block scales 100.4 us at 32, 104.3 at 24).
 int unit_cost_for(int rows, bool kv8) {
     if (rows > 128) return 16;  // the paired tensor-memory form (bf16 only)
     if (rows <= 8) return kv8 ? 32 : 10;
-    if (rows > 64) return kv8 ? 10 : 12;
+    if (rows > 64) return kv8 ? 14 : 12;
     return kv8 ? 4 : 6;
 }
 
