@@ -113,10 +113,12 @@ def _ref(oracle, wl, kv, sc, window=0):
                                        block_size=wl.block_size, scale=wl.scale, window=window)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_block_append_special_values_bit_exact(oracle, d):
     """Fresh blocks, growth, restart at offset 0, zeros, non-finite values, skipped slots
-    and a duplicated slot inside a run, over three calls."""
+    and a duplicated slot inside a run, over three calls.  (head_dim 256: rows wider than
+    a warp's 128 elements, which the append takes in several passes; the attention call
+    supports 64 and 128 only.)"""
     import torch
     n_kv, bs, pool = 2, 16, 6
     rng = np.random.default_rng(60 + d)
