@@ -96,14 +96,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-// 16 bytes global -> shared as one (non-tensor) bulk copy, completing on `bar`
-// (tx bytes).  Both addresses 16-byte aligned.
-__device__ __forceinline__ void bulk_load_16(void* dst, const void* src, uint64_t* bar,
-                                             uint64_t policy) {
+// `bytes` global -> shared as one (non-tensor) bulk copy, completing on `bar`
+// (tx bytes).  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(16u), "r"(smem_addr(bar)), "l"(policy)
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
 
