@@ -249,7 +249,7 @@ template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(kUnitThreads, kUnitBlocksPerSm)
     lse_merge_units_kernel(const AttnArgs a, int attn_grid) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    constexpr int CW = D / 16;  // columns per thread
+    constexpr int CW = D / 16;  // columns per thread: CW / 4 groups of 4, 64 columns apart
     extern __shared__ __align__(128) float s_buf[];  // [kUnitPieces][kUnitRows][D]
     __shared__ int4 s_info[kUnitMaxGrid][2];
     __shared__ int s_cta[kUnitMaxGrid], s_first[kUnitMaxGrid], s_npc[kUnitMaxGrid];
@@ -322,7 +322,9 @@ __global__ void __launch_bounds__(kUnitThreads, kUnitBlocksPerSm)
 
     const int groups = (a.rows + kUnitRows - 1) / kUnitRows;
     const int n_items = s_n * groups;
-    const int row = tid >> 4, col = (tid & 15) * CW;
+    // 16 threads per row; a group of 4 columns per thread and 64-column chunk,
+    // so each chunk's loads and stores are contiguous across the 16 threads
+    const int row = tid >> 4, col = (tid & 15) * 4;
     const uint64_t pol = l2_policy_evict_first();
     uint32_t phase = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -386,11 +388,10 @@ __global__ void __launch_bounds__(kUnitThreads, kUnitBlocksPerSm)
                 if (!(ml[j].y > 0.f)) continue;
                 const float w = fast_exp2(ml[j].x - M);
                 den += w * ml[j].y;
-                const float4* x =
-                    reinterpret_cast<const float4*>(s_buf + (j * kUnitRows + row) * D + col);
+                const float* x = s_buf + (j * kUnitRows + row) * D + col;
 #pragma unroll
                 for (int v = 0; v < CW / 4; ++v) {
-                    const float4 q = x[v];
+                    const float4 q = *reinterpret_cast<const float4*>(x + 64 * v);
                     acc[4 * v] += w * q.x;
                     acc[4 * v + 1] += w * q.y;
                     acc[4 * v + 2] += w * q.z;
@@ -406,18 +407,16 @@ __global__ void __launch_bounds__(kUnitThreads, kUnitBlocksPerSm)
         const float inv = den > 0.f ? 1.f / den : 0.f;
         const int G = a.group, i = R / G, hq = head.y * G + R % G;
         const size_t ob = (((size_t)head.x * a.q_len + i) * a.n_q + hq) * D + col;
-        if (OUT_F32) {
-            float4* op = reinterpret_cast<float4*>(static_cast<float*>(a.out) + ob);
 #pragma unroll
-            for (int v = 0; v < CW / 4; ++v)
-                op[v] = make_float4(acc[4 * v] * inv, acc[4 * v + 1] * inv, acc[4 * v + 2] * inv,
-                                    acc[4 * v + 3] * inv);
-        } else {
-            uint2* op = reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + ob);
-#pragma unroll
-            for (int v = 0; v < CW / 4; ++v)
-                op[v] = make_uint2(pack_bf16x2(acc[4 * v] * inv, acc[4 * v + 1] * inv),
-                                   pack_bf16x2(acc[4 * v + 2] * inv, acc[4 * v + 3] * inv));
+        for (int v = 0; v < CW / 4; ++v) {
+            if (OUT_F32)
+                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + ob + 64 * v) =
+                    make_float4(acc[4 * v] * inv, acc[4 * v + 1] * inv, acc[4 * v + 2] * inv,
+                                acc[4 * v + 3] * inv);
+            else
+                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + ob + 64 * v) =
+                    make_uint2(pack_bf16x2(acc[4 * v] * inv, acc[4 * v + 1] * inv),
+                               pack_bf16x2(acc[4 * v + 2] * inv, acc[4 * v + 3] * inv));
         }
     }
 }
