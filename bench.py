@@ -557,31 +557,39 @@ def workload_line(case, step_ms, attn_ms, hbm, rpeak, world):
 
 def e2e_of(case, K, world):
     """The step through the public API with host buffers: this step's inputs copied from
-    pinned host memory, the step, and `out` copied back, all inside the timed region."""
+    pinned host memory, the step, and `out` copied back, all inside the timed region.
+    The inputs (q, new K/V rows, slots, block tables, context lengths) sit back to back in
+    one pinned staging buffer, as a serving loop would pack them, and arrive by one copy
+    into a device buffer of the same layout that the calls read."""
+    import dataclasses
     import numpy as np
     import torch
-    wl, dw, device = case.wl, case.dw, case.device
+    wl, device = case.wl, case.device
     stream = torch.cuda.current_stream(device)
-    host = {
-        "q": torch.from_numpy(wl.q.view(np.int16)).pin_memory(),
-        "k_new": torch.from_numpy(wl.k_new.view(np.int16)).pin_memory(),
-        "v_new": torch.from_numpy(wl.v_new.view(np.int16)).pin_memory(),
-        "slot_mapping": torch.from_numpy(wl.slot_mapping).pin_memory(),
-        "block_tables": torch.from_numpy(wl.block_tables).pin_memory(),
-        "context_lens": torch.from_numpy(wl.context_lens).pin_memory(),
-    }
+    fields = [("q", wl.q.view(np.int16), torch.bfloat16), ("k_new", wl.k_new.view(np.int16), torch.bfloat16),
+              ("v_new", wl.v_new.view(np.int16), torch.bfloat16),
+              ("slot_mapping", wl.slot_mapping, torch.int32),
+              ("block_tables", wl.block_tables, torch.int32),
+              ("context_lens", wl.context_lens, torch.int32)]
+    offs, size = [], 0
+    for _, arr, _ in fields:
+        offs.append(size)
+        size = (size + arr.nbytes + 255) // 256 * 256  # each field 256-byte aligned
+    host_stage = torch.zeros(size, dtype=torch.uint8).pin_memory()
+    dev_stage = torch.empty(size, dtype=torch.uint8, device=device)
+    views = {}
+    for (name, arr, dt), off in zip(fields, offs):
+        flat = np.ascontiguousarray(arr).view(np.uint8).ravel()
+        host_stage[off:off + flat.size].copy_(torch.from_numpy(flat))
+        views[name] = dev_stage[off:off + flat.size].view(dt).view(arr.shape)
     out_host = torch.empty(tuple(case.out.shape), dtype=torch.int16).pin_memory()
-    dev = {
-        "q": dw.q.view(torch.int16), "k_new": dw.k_new.view(torch.int16),
-        "v_new": dw.v_new.view(torch.int16), "slot_mapping": dw.slot_mapping,
-        "block_tables": dw.block_tables, "context_lens": dw.context_lens,
-    }
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = size
     d2h = out_host.numel() * out_host.element_size()
+    saved = case.dw
+    case.dw = dataclasses.replace(saved, **views)
 
     def e2e_step():
-        for k2, t in host.items():
-            dev[k2].copy_(t, non_blocking=True)
+        dev_stage.copy_(host_stage, non_blocking=True)
         case.step(stream)
         out_host.copy_(case.out.view(torch.int16), non_blocking=True)
 
@@ -598,10 +606,12 @@ def e2e_of(case, K, world):
     torch.cuda.synchronize(device)
     e2e_ms = max_over_ranks([e0.elapsed_time(e1) / K])[0]
     case.check("end-to-end steps")
+    case.dw = saved
     return {"value": round(whole_job_gbps(case.total_bytes, e2e_ms, world), 2), "unit": UNIT,
             "us_per_step": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "timed_as": "eager launches, back to back, host copies in the timed region"}
+            "timed_as": "eager launches, back to back; per step one host-to-device copy of the "
+                        "packed inputs and one device-to-host copy of out, in the timed region"}
 
 
 def run_ours(args):
