@@ -84,7 +84,7 @@ typedef enum pkv_status {
 #define PKV_FLAG_KV_BLOCK_SCALES 0x10u
 /* Attention calls on a bf16 cache with head_dim 128 and more than 64 query
  * rows per KV head: fetch each K and V tile as two 64-column copies, the
- * form used when the driver declines the one-copy (four-dimensional) views
+ * form used when the CUDA driver declines the one-copy (four-dimensional) views
  * of the caches.  Results are bit-identical either way; tests use it to run
  * both. */
 #define PKV_FLAG_TILE_2D 0x20u

@@ -437,7 +437,7 @@ int pkv_paged_decode_attn_ex(const pkv_attn_params* p, void* stream) {
     AttnMaps maps;
     std::memset(&maps, 0, sizeof maps);
     // The tensor-memory consumer over a bf16 head_dim-128 cache takes each K
-    // and V tile in one copy through the grouped 4-D views where the driver
+    // and V tile in one copy through the grouped 4-D views where the CUDA driver
     // accepts them; everything else reads through the 2-D views.
     int tile_4d = 0;
     if (!kv8 && head_dim == 128 && rows > 64 && !(flags & PKV_FLAG_TILE_2D) &&
