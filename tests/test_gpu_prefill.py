@@ -136,5 +136,10 @@ def test_named_chunked_prefill(oracle):
         assert_close(out_to_host(run_attn(dw, wl, kind)), ref, kind, f"{wl.name}/{kind}")
     out = run_attn(dw, wl, "f32", flags=pkv.PKV_FLAG_GRID(300))
     assert_close(out_to_host(out), ref, "f32", f"{wl.name}/grid300")
+    # bf16 output runs the paired form; its split units are combined by the
+    # unit-list merge up to 256 CTAs and by the row-group merge beyond
+    for grid in (256, 257, 2000):
+        out = run_attn(dw, wl, "bf16", flags=pkv.PKV_FLAG_GRID(grid))
+        assert_close(out_to_host(out), ref, "bf16", f"{wl.name}/bf16/grid{grid}")
     del dw
     torch.cuda.empty_cache()
