@@ -14,14 +14,17 @@ from tests.gpu_common import assert_close, oracle_after_append, out_to_host, run
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # (n_q, n_kv, q_len, head_dim, block_size, contexts): narrow, wide and TMEM consumers
+    # (n_q, n_kv, q_len, head_dim, block_size, contexts): narrow, wide and TMEM
+    # consumers, and the paired TMEM form (256-row units of a prefill chunk,
+    # whose split units the unit-list merge combines)
     (8, 2, 1, 128, 16, [40, 300, 17]),
     (32, 2, 1, 128, 16, [64, 500]),
     (32, 1, 4, 128, 32, [90, 700, 33]),
+    (32, 8, 64, 128, 16, [64, 100, 700]),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=["narrow", "wide", "tmem"])
+@pytest.mark.parametrize("case", CASES, ids=["narrow", "wide", "tmem", "paired"])
 def test_expired_waits_are_reported_and_the_context_survives(oracle, case):
     import torch
     n_q, n_kv, q_len, d, bs, ctxs = case
